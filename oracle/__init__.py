@@ -1,0 +1,241 @@
+"""float64 CPU oracle for the Megatron tensor-parallel FFN sublayer.
+
+TEST INFRASTRUCTURE ONLY.  Only ``tests/``, ``__graft_entry__.smoke()`` and the
+CPU-baseline / reference legs of ``bench.py`` may import this package.  It
+shares no code with the CUDA library under ``megatron_tensor_transformer_w1_gb300``
+and never imports it.
+
+The arithmetic lives in ``tpffn_oracle.c`` (plain loops, float64); this module
+only compiles it with gcc on first use and marshals numpy arrays.  The forms it
+computes are stated in that file's header:
+
+* the dense FFN and its explicitly column/row-sharded form with the rank-ordered
+  shard-sum ("7.9 Tensor and pipeline parallelism (TP, PP)", §2.1 "The FFN,
+  sharded"; SwiGLU per "S17 Tensor & Pipeline Parallelism", listing "the
+  megatron pattern");
+* the backward by the chain rule, with the dx shard-sum (the f operator of §2.1);
+* the row-parallel attention output projection (§2.2 "Attention, sharded"),
+  as activation NONE.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "tpffn_oracle.c")
+_LIB = os.path.join(_HERE, "liboracle.so")
+_lock = threading.Lock()
+_lib = None
+
+ACT_NONE = 0
+ACT_GELU_TANH = 1
+ACT_SWIGLU = 2
+ACT_IDENTITY = 3  # oracle-only: sigma = identity, for the linear special case
+
+ACT_BY_NAME = {"none": ACT_NONE, "gelu_tanh": ACT_GELU_TANH, "swiglu": ACT_SWIGLU,
+               "identity": ACT_IDENTITY}
+
+
+def build(force: bool = False) -> str:
+    """Compile the oracle with gcc (OpenMP over independent outputs only)."""
+    if force or not os.path.exists(_LIB) or os.path.getmtime(_LIB) < os.path.getmtime(_SRC):
+        tmp = _LIB + ".tmp%d" % os.getpid()
+        subprocess.check_call(["gcc", "-O2", "-fopenmp", "-shared", "-fPIC", "-std=c11",
+                               _SRC, "-o", tmp, "-lm"])
+        os.replace(tmp, _LIB)
+    return _LIB
+
+
+class _Ffn(ctypes.Structure):
+    _fields_ = [("N", ctypes.c_int64), ("d", ctypes.c_int64), ("d_ff", ctypes.c_int64),
+                ("T_p", ctypes.c_int), ("act", ctypes.c_int), ("round_bf16", ctypes.c_int),
+                ("x", ctypes.c_void_p), ("W1", ctypes.c_void_p), ("W3", ctypes.c_void_p),
+                ("b1", ctypes.c_void_p), ("W2", ctypes.c_void_p), ("b2", ctypes.c_void_p)]
+
+
+def load_library(path):
+    """Load an oracle shared object (the default one, or a test's variant)."""
+    lib = ctypes.CDLL(path)
+    for name in ("orc_gelu_tanh", "orc_gelu_tanh_grad", "orc_silu", "orc_silu_grad",
+                         "orc_round_bf16", "orc_sigmoid"):
+        f = getattr(lib, name)
+        f.restype = ctypes.c_double
+        f.argtypes = [ctypes.c_double]
+    lib.orc_num_threads.restype = ctypes.c_int
+    return lib
+
+
+def _load():
+    global _lib
+    with _lock:
+        if _lib is None:
+            _lib = load_library(build())
+    return _lib
+
+
+def _f64(a):
+    if a is None:
+        return None
+    a = np.ascontiguousarray(a, dtype=np.float64)
+    return a
+
+
+def _ptr(a):
+    return None if a is None else a.ctypes.data_as(ctypes.c_void_p)
+
+
+def _i64(a):
+    return None if a is None else np.ascontiguousarray(a, dtype=np.int64)
+
+
+class FFN:
+    """One FFN problem: the float64 values the oracle computes with.
+
+    x  : [N, d] (act "none": [N, d_ff], the concatenated head outputs)
+    W1, W3 : [d_ff, d]   W2 : [d, d_ff]   b1 : [d_ff]   b2 : [d]
+    round_bf16 : round the stored activations to bf16 (see tpffn_oracle.c).
+    """
+
+    def __init__(self, x, W2, T_p, act, W1=None, W3=None, b1=None, b2=None, round_bf16=False,
+                 lib=None):
+        self._lib = lib
+        self.act = ACT_BY_NAME[act] if isinstance(act, str) else int(act)
+        self.x = _f64(x)
+        self.W1, self.W3, self.W2 = _f64(W1), _f64(W3), _f64(W2)
+        self.b1, self.b2 = _f64(b1), _f64(b2)
+        self.N = self.x.shape[0]
+        self.d = self.W2.shape[0]
+        self.d_ff = self.W2.shape[1]
+        self.T_p = int(T_p)
+        if self.d_ff % self.T_p:
+            raise ValueError("d_ff must be divisible by T_p")
+        if self.act == ACT_NONE:
+            assert self.x.shape == (self.N, self.d_ff)
+        else:
+            assert self.x.shape == (self.N, self.d) and self.W1.shape == (self.d_ff, self.d)
+        if self.act == ACT_SWIGLU:
+            assert self.W3 is not None and self.W3.shape == (self.d_ff, self.d)
+        self.round_bf16 = bool(round_bf16)
+        self._s = _Ffn(self.N, self.d, self.d_ff, self.T_p, self.act, int(self.round_bf16),
+                       _ptr(self.x), _ptr(self.W1), _ptr(self.W3), _ptr(self.b1),
+                       _ptr(self.W2), _ptr(self.b2))
+
+    def lib(self):
+        return self._lib if self._lib is not None else _load()
+
+    @property
+    def d_in(self):
+        return self.d_ff if self.act == ACT_NONE else self.d
+
+    def _rows(self, rows):
+        if rows is None:
+            return self.N, None
+        rows = _i64(rows)
+        assert rows.min() >= 0 and rows.max() < self.N
+        return len(rows), rows
+
+    # ------------------------------------------------------------- forward
+    def forward_dense(self, rows=None, want_h=False):
+        lib = self.lib()
+        n, r = self._rows(rows)
+        y = np.zeros((n, self.d))
+        h = np.zeros((n, self.d_ff)) if want_h else None
+        lib.orc_ffn_forward_dense(ctypes.byref(self._s), ctypes.c_int64(n), _ptr(r), _ptr(y), _ptr(h))
+        return (y, h) if want_h else y
+
+    def forward_sharded(self, rows=None):
+        """Returns dict(y, partials [T_p, n, d], h [n, d_ff], z_saved, ag_saved)."""
+        lib = self.lib()
+        n, r = self._rows(rows)
+        y = np.zeros((n, self.d))
+        part = np.zeros((self.T_p, n, self.d))
+        h = np.zeros((n, self.d_ff))
+        z = np.zeros((n, self.d_ff))
+        ag = np.zeros((n, 2, self.d_ff))
+        lib.orc_ffn_forward_sharded(ctypes.byref(self._s), ctypes.c_int64(n), _ptr(r),
+                                    _ptr(part), _ptr(y), _ptr(h), _ptr(z), _ptr(ag))
+        return dict(y=y, partials=part, h=h, z_saved=z, ag_saved=ag)
+
+    def forward_rowsplit_bad(self):
+        lib = self.lib()
+        y = np.zeros((self.N, self.d))
+        lib.orc_ffn_forward_rowsplit_bad(ctypes.byref(self._s), _ptr(y))
+        return y
+
+    # ------------------------------------------------------------ backward
+    def backward_rows(self, dy, rows=None):
+        """Returns dict(dx [n, d_in], dx_partials [T_p, n, d] (not for NONE))."""
+        lib = self.lib()
+        dy = _f64(dy)
+        assert dy.shape == (self.N, self.d)
+        n, r = self._rows(rows)
+        dx = np.zeros((n, self.d_in))
+        part = None if self.act == ACT_NONE else np.zeros((self.T_p, n, self.d))
+        lib.orc_ffn_backward_rows(ctypes.byref(self._s), _ptr(dy), ctypes.c_int64(n), _ptr(r),
+                                  _ptr(part), _ptr(dx))
+        return dict(dx=dx, dx_partials=part)
+
+    def backward_dense_dx(self, dy):
+        lib = self.lib()
+        dy = _f64(dy)
+        dx = np.zeros((self.N, self.d))
+        lib.orc_ffn_backward_dense_dx(ctypes.byref(self._s), _ptr(dy), _ptr(dx))
+        return dx
+
+    def wgrad_entries(self, dy, js, ks=None, cs=None):
+        """Gradient entries: dW1[js][:, ks], dW3[js][:, ks], dW2[cs][:, js],
+        db1[js], db2[cs].  ks is ignored for act NONE."""
+        lib = self.lib()
+        dy = _f64(dy)
+        js = _i64(js)
+        ks = _i64(ks if ks is not None else np.zeros(0))
+        cs = _i64(cs if cs is not None else np.zeros(0))
+        nj, nk, nc = len(js), len(ks), len(cs)
+        out = dict(dW1=np.zeros((nj, nk)), dW3=np.zeros((nj, nk)), dW2=np.zeros((nc, nj)),
+                   db1=np.zeros(nj), db2=np.zeros(nc))
+        lib.orc_ffn_wgrad_entries(ctypes.byref(self._s), _ptr(dy),
+                                  ctypes.c_int64(nj), _ptr(js), ctypes.c_int64(nk), _ptr(ks),
+                                  ctypes.c_int64(nc), _ptr(cs),
+                                  _ptr(out["dW1"]), _ptr(out["dW3"]), _ptr(out["dW2"]),
+                                  _ptr(out["db1"]), _ptr(out["db2"]))
+        return out
+
+    def backward_full(self, dy):
+        """All gradients in full (small problems only)."""
+        js = np.arange(self.d_ff)
+        ks = np.arange(self.d) if self.act != ACT_NONE else None
+        cs = np.arange(self.d)
+        w = self.wgrad_entries(dy, js, ks, cs)
+        b = self.backward_rows(dy)
+        w.update(b)
+        return w
+
+
+# -------------------------------------------------------------- scalar API
+def gelu_tanh(u):
+    return _load().orc_gelu_tanh(float(u))
+
+
+def gelu_tanh_grad(u):
+    return _load().orc_gelu_tanh_grad(float(u))
+
+
+def silu(u):
+    return _load().orc_silu(float(u))
+
+
+def silu_grad(u):
+    return _load().orc_silu_grad(float(u))
+
+
+def round_bf16(u):
+    return _load().orc_round_bf16(float(u))
+
+
+def num_threads():
+    return _load().orc_num_threads()

@@ -1,0 +1,432 @@
+/*
+ * tpffn_oracle.c -- plain, slow, float64 CPU oracle for the Megatron
+ * tensor-parallel feed-forward sublayer.
+ *
+ * TEST INFRASTRUCTURE ONLY.  Nothing on the product path may call, link or
+ * load this file: only the tests, the package's smoke check and the CPU
+ * baseline leg of the benchmark use it.  It shares no code, header, table or
+ * helper with the CUDA library.
+ *
+ * What it computes (all in float64, row-major, weights stored [out][in]):
+ *
+ *   Dense form -- "7.9 Tensor and pipeline parallelism (TP, PP)", §2.1
+ *   "The FFN, sharded", first display:  y = W2 sigma(W1 x), applied to each
+ *   token row x of an [N, d] activation (so y_n = W2 sigma(W1 x_n)).
+ *     GELU : z = W1 x + b1,  h = gelu_tanh(z)
+ *     SwiGLU ("S17 Tensor & Pipeline Parallelism", listing "the megatron
+ *     pattern"):  a = W1 x, g = W3 x, h = silu(a) * g
+ *     NONE : h = x (a row-parallel linear alone, e.g. the attention output
+ *     projection of §2.2 "Attention, sharded")
+ *     IDENTITY (oracle-only, for the linear special-case pin): h = W1 x + b1
+ *   then y = W2 h + b2.
+ *
+ *   Sharded form -- same §2.1: rows [t*s, (t+1)*s) of W1 (and W3, b1) form
+ *   shard t ("column-shard W1 along its output dimension"), columns
+ *   [t*s, (t+1)*s) of W2 form shard t ("row-shard W2 along its input
+ *   dimension"); h^(t) = sigma(W1^(t) x), y^(t) = W2^(t) h^(t), and the
+ *   g-operator sums y = sum_t y^(t), taken here in the order t = 0..T_p-1.
+ *   b2 is added once after the sum (the page says only that biases "shard
+ *   analogously"; adding b2 per shard would add it T_p times).
+ *
+ *   Backward -- not written out on the pages; §2.1 fixes only where the sums
+ *   go (g: all-reduce forward / identity backward, f: identity forward /
+ *   all-reduce backward).  The oracle applies the ordinary chain rule:
+ *     dh = W2^T dy,  dz = dh * sigma'(z)  (SwiGLU: da = dh*g*silu'(a),
+ *     dg = dh*silu(a)),  dW2 = dy h^T, dW1 = dz x^T, dW3 = dg x^T,
+ *     db1 = sum_n dz, db2 = sum_n dy,  dx = sum_t (W1^(t)T dz^(t) [+ W3^(t)T dg^(t)])
+ *   with the dx shard-sum (the f operator) again in the order t = 0..T_p-1.
+ *
+ * Precision modes.  round_bf16 == 0: every intermediate is float64.
+ * round_bf16 == 1: the activations that the configuration stores in bf16
+ * ("bf16 weights/activations, fp32 accumulate") are rounded to bf16
+ * (round-to-nearest-even) at the points where they are stored: z (saved),
+ * h, a and g (saved), dz / da / dg.  Sums stay in float64.
+ *
+ * Activation functions: gelu_tanh is the tanh approximation of Hendrycks &
+ * Gimpel (2016), 0.5 u (1 + tanh(sqrt(2/pi) (u + 0.044715 u^3))); silu(u) =
+ * u / (1 + exp(-u)).  libm tanh/exp in double precision.
+ *
+ * Parallelism: OpenMP over independent outputs only (token rows, hidden
+ * units).  Every sum runs in one thread, in index order, so results do not
+ * depend on the thread count.
+ */
+#define _DEFAULT_SOURCE 1
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+#ifdef _OPENMP
+#include <omp.h>
+#endif
+
+#define ORC_ACT_NONE 0
+#define ORC_ACT_GELU_TANH 1
+#define ORC_ACT_SWIGLU 2
+#define ORC_ACT_IDENTITY 3
+
+/* ---------------------------------------------------------------- scalars */
+
+/* gelu_tanh(u) = 0.5 u (1 + tanh(c (u + 0.044715 u^3))), c = sqrt(2/pi). */
+double orc_gelu_tanh(double u) {
+  const double c = sqrt(2.0 / M_PI);
+  return 0.5 * u * (1.0 + tanh(c * (u + 0.044715 * u * u * u)));
+}
+
+/* d/du of the expression above (product rule, tanh' = 1 - tanh^2). */
+double orc_gelu_tanh_grad(double u) {
+  const double c = sqrt(2.0 / M_PI);
+  double inner = c * (u + 0.044715 * u * u * u);
+  double th = tanh(inner);
+  double dinner = c * (1.0 + 3.0 * 0.044715 * u * u);
+  return 0.5 * (1.0 + th) + 0.5 * u * (1.0 - th * th) * dinner;
+}
+
+double orc_sigmoid(double u) { return 1.0 / (1.0 + exp(-u)); }
+
+double orc_silu(double u) { return u * orc_sigmoid(u); }
+
+/* silu'(u) = sg (1 + u (1 - sg)),  sg = sigmoid(u). */
+double orc_silu_grad(double u) {
+  double sg = orc_sigmoid(u);
+  return sg * (1.0 + u * (1.0 - sg));
+}
+
+/* Round a double to the nearest bfloat16 value (8 significand bits incl. the
+ * implicit one, exponent range of float32), ties to even.  Written from the
+ * format's definition: find the two neighbouring bf16 values and pick. */
+double orc_round_bf16(double v) {
+  if (v == 0.0 || isnan(v) || isinf(v)) return v;
+  double a = fabs(v);
+  int e;
+  frexp(a, &e);              /* a = m * 2^e, m in [0.5, 1) */
+  int unit_exp = e - 8;      /* spacing of 8-bit significands at this binade */
+  if (e - 1 < -126) unit_exp = -126 - 7;   /* subnormal bf16 spacing */
+  double ulp = ldexp(1.0, unit_exp);
+  double q = a / ulp;        /* exact: power-of-two scaling */
+  double lo = floor(q);
+  double rem = q - lo;
+  double r;
+  if (rem > 0.5) r = lo + 1.0;
+  else if (rem < 0.5) r = lo;
+  else r = (fmod(lo, 2.0) == 0.0) ? lo : lo + 1.0;
+  double out = r * ulp;
+  if (out > 3.3895313892515355e38) out = INFINITY;   /* beyond bf16 max */
+  return v < 0 ? -out : out;
+}
+
+static inline double RND(int on, double v) { return on ? orc_round_bf16(v) : v; }
+
+static double act_fwd(int act, double u) {
+  switch (act) {
+    case ORC_ACT_GELU_TANH: return orc_gelu_tanh(u);
+    case ORC_ACT_IDENTITY: return u;
+    default: return u;
+  }
+}
+static double act_grad(int act, double u) {
+  switch (act) {
+    case ORC_ACT_GELU_TANH: return orc_gelu_tanh_grad(u);
+    default: return 1.0;
+  }
+}
+
+/* ------------------------------------------------------------ the problem */
+
+typedef struct {
+  int64_t N, d, d_ff;
+  int T_p, act, round_bf16;
+  const double* x;   /* [N][d]   (act NONE: [N][d_ff], the concatenated heads) */
+  const double* W1;  /* [d_ff][d] (unused for NONE) */
+  const double* W3;  /* [d_ff][d] (SwiGLU only) */
+  const double* b1;  /* [d_ff] or NULL */
+  const double* W2;  /* [d][d_ff] */
+  const double* b2;  /* [d] or NULL */
+} orc_ffn;
+
+/* Hidden pre-activations of token n, hidden unit j.  Dot products in index
+ * order over the input width. */
+static double dot_row(const double* a, const double* b, int64_t len) {
+  double acc = 0.0;
+  for (int64_t k = 0; k < len; ++k) acc += a[k] * b[k];
+  return acc;
+}
+
+/* Forward quantities of one (token n, hidden j) pair.
+ * out: h (the stored hidden activation), zs / as / gs (the saved values). */
+static void hidden_unit(const orc_ffn* P, int64_t n, int64_t j, double* h,
+                        double* z_saved, double* a_saved, double* g_saved) {
+  const int R = P->round_bf16;
+  if (P->act == ORC_ACT_NONE) {
+    *h = P->x[n * P->d_ff + j];
+    return;
+  }
+  const double* xn = P->x + n * P->d;
+  if (P->act == ORC_ACT_SWIGLU) {
+    double a = dot_row(xn, P->W1 + j * P->d, P->d);
+    double g = dot_row(xn, P->W3 + j * P->d, P->d);
+    *h = RND(R, orc_silu(a) * g);
+    if (a_saved) *a_saved = RND(R, a);
+    if (g_saved) *g_saved = RND(R, g);
+    return;
+  }
+  double z = dot_row(xn, P->W1 + j * P->d, P->d);
+  if (P->b1) z += P->b1[j];
+  *h = RND(R, act_fwd(P->act, z));
+  if (z_saved) *z_saved = RND(R, z);
+}
+
+static int64_t shard_width(const orc_ffn* P) { return P->d_ff / P->T_p; }
+
+/* ------------------------------------------------------------- forward */
+
+/* Dense form over a subset of token rows (rows == NULL: all N rows).
+ * y: [n_rows][d].  h (optional): [n_rows][d_ff]. */
+void orc_ffn_forward_dense(const orc_ffn* P, int64_t n_rows, const int64_t* rows,
+                           double* y, double* h) {
+  const int64_t d = P->d, dff = P->d_ff;
+#pragma omp parallel for schedule(dynamic, 1)
+  for (int64_t r = 0; r < n_rows; ++r) {
+    int64_t n = rows ? rows[r] : r;
+    double* hrow = (double*)malloc(sizeof(double) * dff);
+    for (int64_t j = 0; j < dff; ++j) hidden_unit(P, n, j, &hrow[j], NULL, NULL, NULL);
+    for (int64_t c = 0; c < d; ++c) {
+      double acc = 0.0;
+      for (int64_t j = 0; j < dff; ++j) acc += P->W2[c * dff + j] * hrow[j];
+      if (P->b2) acc += P->b2[c];
+      y[r * d + c] = acc;
+    }
+    if (h) memcpy(h + r * dff, hrow, sizeof(double) * dff);
+    free(hrow);
+  }
+}
+
+/* Explicitly sharded form over a subset of token rows.
+ * partials: [T_p][n_rows][d] (optional), y: [n_rows][d],
+ * h: [n_rows][d_ff] (optional), z_saved: [n_rows][d_ff] (optional, GELU),
+ * ag_saved: [n_rows][2][d_ff] (optional, SwiGLU: a then g). */
+void orc_ffn_forward_sharded(const orc_ffn* P, int64_t n_rows, const int64_t* rows,
+                             double* partials, double* y, double* h,
+                             double* z_saved, double* ag_saved) {
+  const int64_t d = P->d, dff = P->d_ff, s = shard_width(P);
+  const int T = P->T_p;
+#pragma omp parallel for schedule(dynamic, 1)
+  for (int64_t r = 0; r < n_rows; ++r) {
+    int64_t n = rows ? rows[r] : r;
+    double* part = (double*)malloc(sizeof(double) * (size_t)T * d);
+    double* ht = (double*)malloc(sizeof(double) * s);
+    for (int t = 0; t < T; ++t) {
+      /* shard t: hidden units [t*s, (t+1)*s) -- no data from other shards */
+      for (int64_t jj = 0; jj < s; ++jj) {
+        int64_t j = t * s + jj;
+        double zs = 0, as = 0, gs = 0;
+        hidden_unit(P, n, j, &ht[jj], &zs, &as, &gs);
+        if (h) h[r * dff + j] = ht[jj];
+        if (z_saved) z_saved[r * dff + j] = zs;
+        if (ag_saved) { ag_saved[(r * 2 + 0) * dff + j] = as; ag_saved[(r * 2 + 1) * dff + j] = gs; }
+      }
+      /* y^(t) = W2^(t) h^(t): columns [t*s, (t+1)*s) of W2 */
+      for (int64_t c = 0; c < d; ++c) {
+        double acc = 0.0;
+        for (int64_t jj = 0; jj < s; ++jj) acc += P->W2[c * dff + t * s + jj] * ht[jj];
+        part[(int64_t)t * d + c] = acc;
+      }
+    }
+    /* g operator: y = sum_t y^(t), t ascending, then b2 once */
+    for (int64_t c = 0; c < d; ++c) {
+      double acc = 0.0;
+      for (int t = 0; t < T; ++t) acc += part[(int64_t)t * d + c];
+      if (P->b2) acc += P->b2[c];
+      y[r * d + c] = acc;
+      if (partials)
+        for (int t = 0; t < T; ++t) partials[((int64_t)t * n_rows + r) * d + c] = part[(int64_t)t * d + c];
+    }
+    free(ht);
+    free(part);
+  }
+}
+
+/* Counter-example the pages warn about ("the bad option" of splitting the
+ * first matrix by rows, i.e. along the input dimension): each shard applies
+ * the activation to its partial product, and the results are summed:
+ * h_bad = sum_t sigma(W1[:, t-th input slice] x[t-th slice] + b1/T_p).
+ * Used only to show that it does NOT reproduce the dense output. */
+void orc_ffn_forward_rowsplit_bad(const orc_ffn* P, double* y) {
+  const int64_t d = P->d, dff = P->d_ff;
+  const int T = P->T_p;
+  const int64_t kw = d / T;
+  for (int64_t n = 0; n < P->N; ++n) {
+    const double* xn = P->x + n * d;
+    for (int64_t c = 0; c < d; ++c) y[n * d + c] = P->b2 ? P->b2[c] : 0.0;
+    for (int64_t j = 0; j < dff; ++j) {
+      double hj = 0.0;
+      for (int t = 0; t < T; ++t) {
+        double zt = 0.0;
+        for (int64_t k = t * kw; k < (t + 1) * kw; ++k) zt += P->W1[j * d + k] * xn[k];
+        if (P->b1) zt += P->b1[j] / T;
+        hj += act_fwd(P->act, zt);
+      }
+      for (int64_t c = 0; c < d; ++c) y[n * d + c] += P->W2[c * dff + j] * hj;
+    }
+  }
+}
+
+/* ------------------------------------------------------------ backward */
+
+/* Backward quantities of one (token n, hidden j): dh (exact), then the
+ * stored gradient(s): dz (GELU / IDENTITY), or da, dg (SwiGLU), or dc = dh
+ * (NONE).  h is also returned (for dW2). */
+static void hidden_unit_bwd(const orc_ffn* P, const double* dy, int64_t n, int64_t j,
+                            double* h, double* dz, double* dg) {
+  const int R = P->round_bf16;
+  const int64_t d = P->d, dff = P->d_ff;
+  double dh = 0.0;
+  for (int64_t c = 0; c < d; ++c) dh += dy[n * d + c] * P->W2[c * dff + j];
+  double zs = 0, as = 0, gs = 0;
+  hidden_unit(P, n, j, h, &zs, &as, &gs);
+  if (P->act == ORC_ACT_NONE) { *dz = dh; if (dg) *dg = 0.0; return; }
+  if (P->act == ORC_ACT_SWIGLU) {
+    /* as, gs are the saved (possibly bf16) a and g */
+    *dz = RND(R, dh * gs * orc_silu_grad(as));
+    if (dg) *dg = RND(R, dh * orc_silu(as));
+    return;
+  }
+  *dz = RND(R, dh * act_grad(P->act, zs));
+  if (dg) *dg = 0.0;
+}
+
+/* dx for a subset of token rows, with the per-shard partials.
+ * dx: [n_rows][d_in]  with d_in = d (d_ff for NONE, where shard t owns the
+ * input columns [t*s, (t+1)*s) and no sum is taken).
+ * dx_partials: [T_p][n_rows][d] (optional; not for NONE). */
+void orc_ffn_backward_rows(const orc_ffn* P, const double* dy, int64_t n_rows,
+                           const int64_t* rows, double* dx_partials, double* dx) {
+  const int64_t d = P->d, dff = P->d_ff, s = shard_width(P);
+  const int T = P->T_p;
+#pragma omp parallel for schedule(dynamic, 1)
+  for (int64_t r = 0; r < n_rows; ++r) {
+    int64_t n = rows ? rows[r] : r;
+    double* dz = (double*)malloc(sizeof(double) * dff);
+    double* dg = (double*)malloc(sizeof(double) * dff);
+    for (int64_t j = 0; j < dff; ++j) {
+      double hj;
+      hidden_unit_bwd(P, dy, n, j, &hj, &dz[j], &dg[j]);
+    }
+    if (P->act == ORC_ACT_NONE) {
+      for (int64_t j = 0; j < dff; ++j) dx[r * dff + j] = dz[j];
+    } else {
+      double* part = (double*)malloc(sizeof(double) * (size_t)T * d);
+      for (int t = 0; t < T; ++t)
+        for (int64_t k = 0; k < d; ++k) {
+          double acc = 0.0;
+          for (int64_t jj = 0; jj < s; ++jj) {
+            int64_t j = t * s + jj;
+            acc += dz[j] * P->W1[j * d + k];
+            if (P->act == ORC_ACT_SWIGLU) acc += dg[j] * P->W3[j * d + k];
+          }
+          part[(int64_t)t * d + k] = acc;
+        }
+      /* f operator in backward: dx = sum_t dx^(t), t ascending */
+      for (int64_t k = 0; k < d; ++k) {
+        double acc = 0.0;
+        for (int t = 0; t < T; ++t) acc += part[(int64_t)t * d + k];
+        dx[r * d + k] = acc;
+        if (dx_partials)
+          for (int t = 0; t < T; ++t) dx_partials[((int64_t)t * n_rows + r) * d + k] = part[(int64_t)t * d + k];
+      }
+      free(part);
+    }
+    free(dg);
+    free(dz);
+  }
+}
+
+/* Dense-form dx (no shards): dx = W1^T dz (+ W3^T dg) summed over all hidden
+ * units in index order.  Used for the shard-sum invariant of the backward. */
+void orc_ffn_backward_dense_dx(const orc_ffn* P, const double* dy, double* dx) {
+  const int64_t d = P->d, dff = P->d_ff;
+#pragma omp parallel for schedule(dynamic, 1)
+  for (int64_t n = 0; n < P->N; ++n) {
+    double* dz = (double*)malloc(sizeof(double) * dff);
+    double* dg = (double*)malloc(sizeof(double) * dff);
+    for (int64_t j = 0; j < dff; ++j) { double hj; hidden_unit_bwd(P, dy, n, j, &hj, &dz[j], &dg[j]); }
+    for (int64_t k = 0; k < d; ++k) {
+      double acc = 0.0;
+      for (int64_t j = 0; j < dff; ++j) {
+        acc += dz[j] * P->W1[j * d + k];
+        if (P->act == ORC_ACT_SWIGLU) acc += dg[j] * P->W3[j * d + k];
+      }
+      dx[n * d + k] = acc;
+    }
+    free(dg);
+    free(dz);
+  }
+}
+
+/* Weight and bias gradients at selected entries.  Each shard owns its own
+ * weights, so there is no cross-shard sum here.
+ *   js [n_j]: hidden units;  ks [n_k]: input features (d; unused for NONE);
+ *   cs [n_c]: output features.
+ *   dW1 [n_j][n_k] = sum_n dz[n][j] x[n][k]      (GELU/IDENTITY/SwiGLU's da)
+ *   dW3 [n_j][n_k] = sum_n dg[n][j] x[n][k]      (SwiGLU)
+ *   dW2 [n_c][n_j] = sum_n dy[n][c] h[n][j]
+ *   db1 [n_j]      = sum_n dz[n][j]
+ *   db2 [n_c]      = sum_n dy[n][c]
+ * Any output pointer may be NULL. */
+void orc_ffn_wgrad_entries(const orc_ffn* P, const double* dy,
+                           int64_t n_j, const int64_t* js, int64_t n_k, const int64_t* ks,
+                           int64_t n_c, const int64_t* cs,
+                           double* dW1, double* dW3, double* dW2, double* db1, double* db2) {
+  const int64_t N = P->N, d = P->d;
+  const int64_t d_in = (P->act == ORC_ACT_NONE) ? P->d_ff : P->d;
+  (void)d_in;
+#pragma omp parallel for schedule(dynamic, 1)
+  for (int64_t a = 0; a < n_j; ++a) {
+    int64_t j = js[a];
+    double* hcol = (double*)malloc(sizeof(double) * N);
+    double* dzcol = (double*)malloc(sizeof(double) * N);
+    double* dgcol = (double*)malloc(sizeof(double) * N);
+    for (int64_t n = 0; n < N; ++n) hidden_unit_bwd(P, dy, n, j, &hcol[n], &dzcol[n], &dgcol[n]);
+    if (P->act != ORC_ACT_NONE) {
+      for (int64_t b = 0; b < n_k; ++b) {
+        int64_t k = ks[b];
+        double acc1 = 0.0, acc3 = 0.0;
+        for (int64_t n = 0; n < N; ++n) {
+          acc1 += dzcol[n] * P->x[n * d + k];
+          acc3 += dgcol[n] * P->x[n * d + k];
+        }
+        if (dW1) dW1[a * n_k + b] = acc1;
+        if (dW3) dW3[a * n_k + b] = acc3;
+      }
+    }
+    for (int64_t b = 0; b < n_c; ++b) {
+      int64_t c = cs[b];
+      double acc = 0.0;
+      for (int64_t n = 0; n < N; ++n) acc += dy[n * d + c] * hcol[n];
+      if (dW2) dW2[b * n_j + a] = acc;
+    }
+    if (db1) {
+      double acc = 0.0;
+      for (int64_t n = 0; n < N; ++n) acc += dzcol[n];
+      db1[a] = acc;
+    }
+    free(dgcol);
+    free(dzcol);
+    free(hcol);
+  }
+  if (db2) {
+    for (int64_t b = 0; b < n_c; ++b) {
+      double acc = 0.0;
+      for (int64_t n = 0; n < N; ++n) acc += dy[n * d + cs[b]];
+      db2[b] = acc;
+    }
+  }
+}
+
+/* Number of OpenMP threads the oracle will use (for reporting). */
+int orc_num_threads(void) {
+#ifdef _OPENMP
+  return omp_get_max_threads();
+#else
+  return 1;
+#endif
+}

@@ -1,0 +1,152 @@
+"""Seeded synthetic inputs shared by the oracle side and the CUDA side.
+
+This module holds no arithmetic of the method: it only draws normal variates
+from numpy's PCG64 generator (one independent stream per tensor, spawned from
+one SeedSequence per workload) and rounds them to the workload's storage type
+with PyTorch's own conversion (round-to-nearest-even).  Both sides then read
+the very same rounded values: the CUDA library as bf16/fp32 device tensors,
+the oracle as their exact float64 widenings.
+
+Workloads (tokens N, model width d, hidden width d_ff, shards T_p):
+
+=============================  =====  ====  =====  ===  =========  =====
+name                           N      d     d_ff   T_p  act        dtype
+=============================  =====  ====  =====  ===  =========  =====
+tiny_gelu_fp32                 8      64    256    2    gelu_tanh  f32
+gpt2_small_gelu_bf16           4096   768   3072   4    gelu_tanh  bf16 (+ biases)
+llama3_8b_swiglu_bf16          8192   4096  14336  8    swiglu     bf16
+megatron_8p3b_gelu_bf16        8192   3072  12288  8    gelu_tanh  bf16
+megatron_8p3b_attn_out_bf16    8192   3072  3072   8    none       bf16 (24 heads x 128)
+llama3_70b_decode_swiglu_bf16  32     8192  28672  8    swiglu     bf16 (forward only)
+=============================  =====  ====  =====  ===  =========  =====
+
+Value distributions: activations x (or the concatenated head outputs c) and
+the upstream gradient dy are N(0, 1); weights are N(0, 1/fan_in) (W1, W3:
+fan_in d; W2: fan_in d_ff), except the GPT-2-small workload, whose weights
+are N(0, 0.02^2) and biases N(0, 0.01^2).
+"""
+from __future__ import annotations
+
+import dataclasses
+
+import numpy as np
+import torch
+
+BASE_SEED = 20260000
+
+
+@dataclasses.dataclass(frozen=True)
+class Workload:
+    name: str
+    N: int
+    d: int
+    d_ff: int
+    T_p: int
+    act: str             # "gelu_tanh" | "swiglu" | "none"
+    dtype: str           # "f32" | "bf16"
+    bias: bool = False
+    fwd_only: bool = False
+    w_std: float | None = None   # fixed weight std (else 1/sqrt(fan_in))
+    b_std: float = 0.0
+    seed_index: int = 0
+    n_heads: int = 0     # act "none": heads feeding the projection
+    n_kv_heads: int = 0
+    head_dim: int = 0
+
+    @property
+    def s(self):
+        return self.d_ff // self.T_p
+
+    @property
+    def d_in(self):
+        return self.d_ff if self.act == "none" else self.d
+
+    def fwd_flops(self):
+        mult = {"gelu_tanh": 4, "swiglu": 6, "none": 2}[self.act]
+        return mult * self.N * self.d * self.d_ff
+
+    def bwd_flops(self):
+        return 2 * self.fwd_flops()
+
+    def weight_bytes(self):
+        esz = 4 if self.dtype == "f32" else 2
+        n_mats = {"gelu_tanh": 2, "swiglu": 3, "none": 1}[self.act]
+        return n_mats * self.d * self.d_ff * esz
+
+    def replace(self, **kw):
+        return dataclasses.replace(self, **kw)
+
+
+WORKLOADS = {
+    w.name: w for w in [
+        Workload("tiny_gelu_fp32", 8, 64, 256, 2, "gelu_tanh", "f32", seed_index=1),
+        Workload("gpt2_small_gelu_bf16", 4096, 768, 3072, 4, "gelu_tanh", "bf16", bias=True,
+                 w_std=0.02, b_std=0.01, seed_index=2),
+        Workload("llama3_8b_swiglu_bf16", 8192, 4096, 14336, 8, "swiglu", "bf16", seed_index=3),
+        Workload("megatron_8p3b_gelu_bf16", 8192, 3072, 12288, 8, "gelu_tanh", "bf16", seed_index=4),
+        Workload("megatron_8p3b_attn_out_bf16", 8192, 3072, 3072, 8, "none", "bf16",
+                 seed_index=5, n_heads=24, n_kv_heads=24, head_dim=128),
+        Workload("llama3_70b_decode_swiglu_bf16", 32, 8192, 28672, 8, "swiglu", "bf16",
+                 fwd_only=True, seed_index=6),
+    ]
+}
+
+
+def _torch_dtype(dtype):
+    return torch.float32 if dtype == "f32" else torch.bfloat16
+
+
+def _draw(rng, shape, std, dtype):
+    """N(0, std^2) values rounded to the storage dtype (torch RNE cast)."""
+    if dtype == "f32":
+        a = rng.standard_normal(shape, dtype=np.float64) * std
+        return torch.from_numpy(a).to(torch.float32)
+    a = rng.standard_normal(shape, dtype=np.float32)
+    if std != 1.0:
+        a *= np.float32(std)
+    return torch.from_numpy(a).to(torch.bfloat16)
+
+
+_ORDER = ("x", "W1", "W3", "W2", "b1", "b2", "dy")
+
+
+def make_inputs(w: Workload, seed: int | None = None):
+    """Host tensors of the workload's storage dtype.
+
+    Keys: x [N, d_in], W1, W3 [d_ff, d] (W3 for SwiGLU only), W2 [d, d_ff],
+    b1 [d_ff], b2 [d] (biased workloads only), dy [N, d] (not forward-only).
+    Missing tensors are None.
+    """
+    seed = BASE_SEED + w.seed_index if seed is None else seed
+    streams = np.random.SeedSequence(seed).spawn(len(_ORDER))
+    rng = {k: np.random.Generator(np.random.PCG64(s)) for k, s in zip(_ORDER, streams)}
+    dt = w.dtype
+    out = dict.fromkeys(_ORDER)
+    out["x"] = _draw(rng["x"], (w.N, w.d_in), 1.0, dt)
+    if w.act != "none":
+        std1 = w.w_std if w.w_std is not None else 1.0 / np.sqrt(w.d)
+        out["W1"] = _draw(rng["W1"], (w.d_ff, w.d), std1, dt)
+        if w.act == "swiglu":
+            out["W3"] = _draw(rng["W3"], (w.d_ff, w.d), std1, dt)
+    std2 = w.w_std if w.w_std is not None else 1.0 / np.sqrt(w.d_ff)
+    out["W2"] = _draw(rng["W2"], (w.d, w.d_ff), std2, dt)
+    if w.bias:
+        out["b1"] = _draw(rng["b1"], (w.d_ff,), w.b_std, dt)
+        out["b2"] = _draw(rng["b2"], (w.d,), w.b_std, dt)
+    if not w.fwd_only:
+        out["dy"] = _draw(rng["dy"], (w.N, w.d), 1.0, dt)
+    return out
+
+
+def small_case(N, d, d_ff, T_p, act, dtype="bf16", bias=False, seed=7, fwd_only=False):
+    """A small workload of the same value distributions (for full-oracle parity)."""
+    return Workload(f"small_{act}_{dtype}_{N}x{d}x{d_ff}_tp{T_p}", N, d, d_ff, T_p, act, dtype,
+                    bias=bias, fwd_only=fwd_only, w_std=(0.05 if bias else None),
+                    b_std=(0.02 if bias else 0.0), seed_index=seed)
+
+
+def to_f64(t):
+    """Exact float64 widening of a host tensor (None passes through)."""
+    if t is None:
+        return None
+    return t.to(torch.float64).numpy()
