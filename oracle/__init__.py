@@ -21,6 +21,7 @@ from __future__ import annotations
 
 import ctypes
 import os
+import platform
 import subprocess
 import threading
 
@@ -28,7 +29,7 @@ import numpy as np
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 _SRC = os.path.join(_HERE, "tpffn_oracle.c")
-_LIB = os.path.join(_HERE, "liboracle.so")
+_LIB = os.path.join(_HERE, f"liboracle-{platform.machine()}.so")
 _lock = threading.Lock()
 _lib = None
 
@@ -203,6 +204,24 @@ class FFN:
                                   ctypes.c_int64(nc), _ptr(cs),
                                   _ptr(out["dW1"]), _ptr(out["dW3"]), _ptr(out["dW2"]),
                                   _ptr(out["db1"]), _ptr(out["db2"]))
+        return out
+
+    def hidden_rows(self, dy=None, rows=None):
+        """Values of the stored hidden quantities before bf16 rounding, for
+        selected token rows: dict(h_pre, z_pre, g_pre, dz_pre, dg_pre), each
+        [n, d_ff] (the dz/dg entries only when dy is given)."""
+        lib = self.lib()
+        n, r = self._rows(rows)
+        out = {k: np.zeros((n, self.d_ff)) for k in ("h_pre", "z_pre", "g_pre", "dz_pre", "dg_pre")}
+        dyp = None
+        if dy is not None:
+            dyp = _f64(dy)
+            assert dyp.shape == (self.N, self.d)
+        lib.orc_ffn_hidden_rows(ctypes.byref(self._s), _ptr(dyp), ctypes.c_int64(n), _ptr(r),
+                                _ptr(out["h_pre"]), _ptr(out["z_pre"]), _ptr(out["g_pre"]),
+                                _ptr(out["dz_pre"]), _ptr(out["dg_pre"]))
+        if dy is None:
+            del out["dz_pre"], out["dg_pre"]
         return out
 
     def backward_full(self, dy):

@@ -152,27 +152,39 @@ static double dot_row(const double* a, const double* b, int64_t len) {
 }
 
 /* Forward quantities of one (token n, hidden j) pair.
- * out: h (the stored hidden activation), zs / as / gs (the saved values). */
-static void hidden_unit(const orc_ffn* P, int64_t n, int64_t j, double* h,
-                        double* z_saved, double* a_saved, double* g_saved) {
+ * out: h (the stored hidden activation), z_saved / a_saved / g_saved (the
+ * saved values), and optionally the values before bf16 rounding:
+ * pre[0] = sigma(z) (or silu(a) g), pre[1] = z (or a), pre[2] = g. */
+static void hidden_unit_ex(const orc_ffn* P, int64_t n, int64_t j, double* h,
+                           double* z_saved, double* a_saved, double* g_saved, double* pre) {
   const int R = P->round_bf16;
   if (P->act == ORC_ACT_NONE) {
     *h = P->x[n * P->d_ff + j];
+    if (pre) { pre[0] = *h; pre[1] = 0.0; pre[2] = 0.0; }
     return;
   }
   const double* xn = P->x + n * P->d;
   if (P->act == ORC_ACT_SWIGLU) {
     double a = dot_row(xn, P->W1 + j * P->d, P->d);
     double g = dot_row(xn, P->W3 + j * P->d, P->d);
-    *h = RND(R, orc_silu(a) * g);
+    double hv = orc_silu(a) * g;
+    *h = RND(R, hv);
     if (a_saved) *a_saved = RND(R, a);
     if (g_saved) *g_saved = RND(R, g);
+    if (pre) { pre[0] = hv; pre[1] = a; pre[2] = g; }
     return;
   }
   double z = dot_row(xn, P->W1 + j * P->d, P->d);
   if (P->b1) z += P->b1[j];
-  *h = RND(R, act_fwd(P->act, z));
+  double hv = act_fwd(P->act, z);
+  *h = RND(R, hv);
   if (z_saved) *z_saved = RND(R, z);
+  if (pre) { pre[0] = hv; pre[1] = z; pre[2] = 0.0; }
+}
+
+static void hidden_unit(const orc_ffn* P, int64_t n, int64_t j, double* h,
+                        double* z_saved, double* a_saved, double* g_saved) {
+  hidden_unit_ex(P, n, j, h, z_saved, a_saved, g_saved, NULL);
 }
 
 static int64_t shard_width(const orc_ffn* P) { return P->d_ff / P->T_p; }
@@ -274,24 +286,59 @@ void orc_ffn_forward_rowsplit_bad(const orc_ffn* P, double* y) {
 
 /* Backward quantities of one (token n, hidden j): dh (exact), then the
  * stored gradient(s): dz (GELU / IDENTITY), or da, dg (SwiGLU), or dc = dh
- * (NONE).  h is also returned (for dW2). */
-static void hidden_unit_bwd(const orc_ffn* P, const double* dy, int64_t n, int64_t j,
-                            double* h, double* dz, double* dg) {
+ * (NONE).  h is also returned (for dW2).  pre (optional): the values of dz
+ * (da) and dg before bf16 rounding. */
+static void hidden_unit_bwd_ex(const orc_ffn* P, const double* dy, int64_t n, int64_t j,
+                               double* h, double* dz, double* dg, double* pre) {
   const int R = P->round_bf16;
   const int64_t d = P->d, dff = P->d_ff;
   double dh = 0.0;
   for (int64_t c = 0; c < d; ++c) dh += dy[n * d + c] * P->W2[c * dff + j];
   double zs = 0, as = 0, gs = 0;
   hidden_unit(P, n, j, h, &zs, &as, &gs);
-  if (P->act == ORC_ACT_NONE) { *dz = dh; if (dg) *dg = 0.0; return; }
+  double v0 = dh, v1 = 0.0;
   if (P->act == ORC_ACT_SWIGLU) {
     /* as, gs are the saved (possibly bf16) a and g */
-    *dz = RND(R, dh * gs * orc_silu_grad(as));
-    if (dg) *dg = RND(R, dh * orc_silu(as));
-    return;
+    v0 = dh * gs * orc_silu_grad(as);
+    v1 = dh * orc_silu(as);
+  } else if (P->act != ORC_ACT_NONE) {
+    v0 = dh * act_grad(P->act, zs);
   }
-  *dz = RND(R, dh * act_grad(P->act, zs));
-  if (dg) *dg = 0.0;
+  if (pre) { pre[0] = v0; pre[1] = v1; }
+  if (P->act == ORC_ACT_NONE) { *dz = dh; if (dg) *dg = 0.0; return; }
+  *dz = RND(R, v0);
+  if (dg) *dg = RND(R, v1);
+}
+
+static void hidden_unit_bwd(const orc_ffn* P, const double* dy, int64_t n, int64_t j,
+                            double* h, double* dz, double* dg) {
+  hidden_unit_bwd_ex(P, dy, n, j, h, dz, dg, NULL);
+}
+
+/* Stored hidden quantities of selected token rows together with their
+ * values before bf16 rounding, each [n_rows][d_ff] (any pointer may be NULL):
+ *   h_pre  : sigma(z) or silu(a) g          z_pre : z (GELU) or a (SwiGLU)
+ *   g_pre  : g (SwiGLU)                     dz_pre: dh sigma'(z_saved) or da
+ *   dg_pre : dg (SwiGLU)
+ * The tests use them to find rounding decisions that lie within float noise
+ * of a bf16 midpoint (dy may be NULL when no backward values are wanted). */
+void orc_ffn_hidden_rows(const orc_ffn* P, const double* dy, int64_t n_rows, const int64_t* rows,
+                         double* h_pre, double* z_pre, double* g_pre, double* dz_pre, double* dg_pre) {
+  const int64_t dff = P->d_ff;
+#pragma omp parallel for schedule(dynamic, 1)
+  for (int64_t r = 0; r < n_rows; ++r) {
+    int64_t n = rows ? rows[r] : r;
+    for (int64_t j = 0; j < dff; ++j) {
+      double h, zs, as, gs, pre[3], bpre[2] = {0.0, 0.0}, dz, dg;
+      hidden_unit_ex(P, n, j, &h, &zs, &as, &gs, pre);
+      if (dy) hidden_unit_bwd_ex(P, dy, n, j, &h, &dz, &dg, bpre);
+      if (h_pre) h_pre[r * dff + j] = pre[0];
+      if (z_pre) z_pre[r * dff + j] = pre[1];
+      if (g_pre) g_pre[r * dff + j] = pre[2];
+      if (dz_pre) dz_pre[r * dff + j] = bpre[0];
+      if (dg_pre) dg_pre[r * dff + j] = bpre[1];
+    }
+  }
 }
 
 /* dx for a subset of token rows, with the per-shard partials.

@@ -26,7 +26,7 @@ MUTATIONS = {
                      "for (int t = 0; t < T; ++t) acc += part[(int64_t)t * d + c] + (P->b2 ? P->b2[c] : 0.0);\n      if (P->b2)"),
     "ties_to_odd": ("(fmod(lo, 2.0) == 0.0) ? lo : lo + 1.0", "(fmod(lo, 2.0) == 0.0) ? lo + 1.0 : lo"),
     "dW1_uses_h": ("acc1 += dzcol[n] * P->x[n * d + k];", "acc1 += hcol[n] * P->x[n * d + k];"),
-    "dg_uses_grad": ("if (dg) *dg = RND(R, dh * orc_silu(as));", "if (dg) *dg = RND(R, dh * orc_silu_grad(as));"),
+    "dg_uses_grad": ("v1 = dh * orc_silu(as);", "v1 = dh * orc_silu_grad(as);"),
     "gelu_grad_drops_term": ("return 0.5 * (1.0 + th) + 0.5 * u * (1.0 - th * th) * dinner;",
                              "return 0.5 * (1.0 + th) + 0.5 * u * (1.0 - th) * dinner;"),
     "dx_skips_last_shard": ("for (int t = 0; t < T; ++t) acc += part[(int64_t)t * d + k];",

@@ -283,3 +283,30 @@ def test_bf16_mode_rounds_only_stored_activations():
     for t in range(2):
         ref = sp["h"][:, t * s:(t + 1) * s] @ f["W2"][:, t * s:(t + 1) * s].T
         np.testing.assert_allclose(sp["partials"][t], ref, rtol=1e-12, atol=1e-13)
+
+
+def test_hidden_dump_rounds_to_stored_values():
+    """The pre-rounding dump rounds (RNE, bf16) to exactly the stored values,
+    and equals them in float64 mode."""
+    for act in ("gelu_tanh", "swiglu"):
+        w = small_case(11, 16, 48, 3, act, dtype="bf16", bias=(act == "gelu_tanh"), seed=43)
+        f = {k: to_f64(v) for k, v in make_inputs(w).items()}
+        kw = dict(W1=f["W1"], W3=f["W3"], b1=f["b1"], b2=f["b2"])
+        for rb in (False, True):
+            P = oracle.FFN(f["x"], f["W2"], 3, act, round_bf16=rb, **kw)
+            dump = P.hidden_rows(f["dy"])
+            sh = P.forward_sharded()
+            # the oracle's own bf16 rounding (pinned above against PyTorch); a
+            # float64 -> float32 -> bf16 cast would round twice
+            R = np.vectorize(oracle.round_bf16) if rb else (lambda a: a)
+            np.testing.assert_array_equal(R(dump["h_pre"]), sh["h"])
+            if act == "swiglu":
+                np.testing.assert_array_equal(R(dump["z_pre"]), sh["ag_saved"][:, 0])
+                np.testing.assert_array_equal(R(dump["g_pre"]), sh["ag_saved"][:, 1])
+            else:
+                np.testing.assert_array_equal(R(dump["z_pre"]), sh["z_saved"])
+            js = np.arange(w.d_ff)
+            e = P.wgrad_entries(f["dy"], js)
+            # db1 = sum over tokens of the stored dz
+            if act == "gelu_tanh":
+                np.testing.assert_allclose(R(dump["dz_pre"]).sum(0), e["db1"], rtol=1e-12, atol=1e-12)
