@@ -1,0 +1,473 @@
+"""Benchmark of the tensor-parallel FFN hot path on GB300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+One step = one pass of the whole path over one batch of the Llama-3-8B-shaped
+SwiGLU workload (8192 tokens, d = 4096, d_ff = 14336, T_p = 8, bf16): packing
+of W1/W3 (shard_columns) and W2 (shard_rows), forward with the g-operator
+shard-sum, backward with the f-operator dx shard-sum and all weight
+gradients.  `value` is the algorithmic fwd+bwd FLOP rate (6+12 N d d_ff per
+step) with inputs resident in HBM; `e2e` repeats the step through the same
+API with x and dy copied in from pinned host memory and y and dx copied back
+inside the timed region.  The decode-shaped workload (Llama-3-70B SwiGLU,
+32 tokens) is reported in `decode` as HBM GB/s of its compulsory bytes.
+
+--impl reference times the float64 CPU oracle on the host cores on a bounded
+sample of the same workload (the oracle is the reference of this build).
+Under torchrun (N > 1) every rank runs its own replica on its own GPU (the
+shards are virtual ranks inside one GPU, so ranks share no data) and the
+line reports the whole-job rate over the slowest rank.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import shutil
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "TP-FFN fwd+bwd TFLOP/s & % BF16 tensor peak; decode-path HBM GB/s"
+MAIN = "llama3_8b_swiglu_bf16"
+DECODE = "llama3_70b_decode_swiglu_bf16"
+
+# DRAM bytes per launch from ncu captures (dram__bytes_read.sum +
+# dram__bytes_write.sum), by kernel name; None until captured for the current
+# kernel code.  Sources are the summaries under profiles/.
+NCU_TRAFFIC = {}
+
+
+def _peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return dict(hbm=d.get("hbm_gbs", 6800.0), bf16=d.get("bf16_tflops", 1900.0),
+                    bf16_sus=d.get("bf16_tflops_sustained", 1700.0), source="measured")
+    return dict(hbm=6800.0, bf16=1900.0, bf16_sus=1700.0, source="fallback")
+
+
+# ------------------------------------------------------------------ clocks
+class ClockSampler:
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+    NAMES = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = None
+
+    def __enter__(self):
+        exe = shutil.which("nvidia-smi")
+        if exe:
+            fd, self.path = tempfile.mkstemp(suffix=".csv")
+            os.close(fd)
+            self.proc = subprocess.Popen([exe, f"--query-gpu={self.QUERY}", "--format=csv,noheader,nounits",
+                                          "-i", str(self.gpu), "-lms", "100"], stdout=open(self.path, "w"),
+                                         stderr=subprocess.DEVNULL)
+            time.sleep(0.3)
+        return self
+
+    def __exit__(self, *a):
+        if self.proc:
+            time.sleep(0.25)
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self):
+        if not self.path or not os.path.exists(self.path):
+            return None
+        sms, maxes, reasons = [], [], set()
+        for line in open(self.path):
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sms.append(float(f[1]))
+                maxes.append(float(f[2]))
+            except ValueError:
+                continue
+            for name, val in zip(self.NAMES, f[5:9]):
+                if val.lower().startswith("active"):
+                    reasons.add(name)
+        os.unlink(self.path)
+        if not sms:
+            return None
+        return {"sm_mhz": statistics.median(sms), "sm_max_mhz": max(maxes), "samples": len(sms),
+                "reasons": sorted(reasons)}
+
+
+# ------------------------------------------------------------- distributed
+def dist_setup(n_gpus):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    if world > 1:
+        import torch.distributed as dist
+        rank = int(os.environ["RANK"])
+        local = int(os.environ.get("LOCAL_RANK", rank))
+        return dict(world=world, rank=rank, local=local, dist=dist)
+    return dict(world=1, rank=0, local=0, dist=None)
+
+
+def dist_max(ctx, value):
+    """Max over ranks (identity on one rank)."""
+    if ctx["dist"] is None:
+        return value
+    import torch
+    dev = torch.device("cuda", ctx["local"]) if torch.cuda.is_available() else torch.device("cpu")
+    t = torch.tensor([float(value)], dtype=torch.float64, device=dev)
+    ctx["dist"].all_reduce(t, op=ctx["dist"].ReduceOp.MAX)
+    return float(t.item())
+
+
+def dist_barrier(ctx):
+    if ctx["dist"] is not None:
+        ctx["dist"].barrier()
+
+
+# --------------------------------------------------------------- our arm
+def _device_inputs(w, dev, seed):
+    """Seeded synthetic tensors generated on the device (same shapes and
+    distributions as synth.make_inputs; the parity tests use the host ones)."""
+    import torch
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(seed)
+
+    def draw(shape, std):
+        t = torch.randn(*shape, generator=gen, device=dev, dtype=torch.float32)
+        return (t * std).to(torch.bfloat16)
+
+    out = {"x": draw((w.N, w.d), 1.0), "W1": draw((w.d_ff, w.d), w.d ** -0.5)}
+    out["W3"] = draw((w.d_ff, w.d), w.d ** -0.5) if w.act == "swiglu" else None
+    out["W2"] = draw((w.d, w.d_ff), w.d_ff ** -0.5)
+    out["dy"] = None if w.fwd_only else draw((w.N, w.d), 1.0)
+    return out
+
+
+def _kernel_work(w, name):
+    """Algorithmic work of one launch: ('flop', F) or ('byte', B)."""
+    N, d, dff, T = w.N, w.d, w.d_ff, w.T_p
+    wide = 2 * dff if w.act == "swiglu" else dff
+    flops = {"up_swiglu": 2 * N * d * 2 * dff, "up_gelu": 2 * N * d * dff, "down_fused_sum": 2 * N * dff * d,
+             "down_partials": 2 * N * dff * d, "dgrad_h_swiglu": 2 * N * d * dff, "dgrad_h_gelu": 2 * N * d * dff,
+             "dgrad_x_fused_sum": 2 * N * wide * d, "dgrad_x_partials": 2 * N * wide * d,
+             "wgrad_w2": 2 * N * d * dff, "wgrad_w13": 2 * N * wide * d, "wgrad_w1": 2 * N * wide * d}
+    if name in flops:
+        return "flop", flops[name]
+    if name.startswith("shard_sum"):
+        return "byte", T * N * d * 4 + N * d * 2
+    return "byte", 0
+
+
+def run_ours(args, ctx):
+    import torch
+    from synth import WORKLOADS
+    from megatron_tensor_transformer_w1_gb300 import tpffn as abi
+    from megatron_tensor_transformer_w1_gb300.ffn import TensorParallelFFN
+
+    dev = torch.device("cuda", ctx["local"])
+    torch.cuda.set_device(dev)
+    peaks = _peaks()
+    w = WORKLOADS[MAIN]
+    inp = _device_inputs(w, dev, 20260000 + w.seed_index + 1000 * ctx["rank"])
+    ffn = TensorParallelFFN(w.d, w.d_ff, w.T_p, w.act, "bf16", device=dev)
+    fused = args.sum == "fused"
+    flags = abi.TP_SUM_FUSED if fused else 0
+    st = torch.cuda.current_stream(dev)
+    plan = ffn.plan
+    n = w.N
+    w13p = torch.empty(abi.tp_ffn_packed_bytes(plan, abi.TP_PACK_COLUMNS), dtype=torch.uint8, device=dev)
+    w2p = torch.empty(abi.tp_ffn_packed_bytes(plan, abi.TP_PACK_ROWS), dtype=torch.uint8, device=dev)
+    saved = torch.empty(abi.tp_ffn_saved_bytes(plan, n), dtype=torch.uint8, device=dev)
+    ws = torch.empty(abi.tp_ffn_workspace_bytes(plan, n, flags), dtype=torch.uint8, device=dev)
+    y = torch.empty(n, w.d, dtype=torch.bfloat16, device=dev)
+    dx = torch.empty_like(y)
+    dw13p, dw2p = torch.empty_like(w13p), torch.empty_like(w2p)
+    x, dy = inp["x"], inp["dy"]
+    launches = [0]
+
+    def step(f=flags, x=x, dy=dy):
+        abi.check(abi.tp_ffn_shard_columns(plan, inp["W1"], inp["W3"], w13p, st), "shard_columns")
+        abi.check(abi.tp_ffn_shard_rows(plan, inp["W2"], w2p, st), "shard_rows")
+        abi.check(abi.tp_ffn_fwd(plan, n, x, w13p, w2p, None, None, y, None, saved, ws, ws.numel(), f, st), "fwd")
+        c = 2 + abi.tp_ffn_last_launch_count(plan)
+        abi.check(abi.tp_ffn_bwd(plan, n, x, w13p, w2p, saved, dy, dx, None, dw13p, dw2p, None, None, ws,
+                                 ws.numel(), f, st), "bwd")
+        launches[0] += c + abi.tp_ffn_last_launch_count(plan)
+
+    flop_step = w.fwd_flops() + w.bwd_flops()
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize(dev)
+    abi.tp_ffn_kernel_times(plan, 0)  # clear
+    launches[0] = 0
+    dist_barrier(ctx)
+    torch.cuda.synchronize(dev)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with ClockSampler(dev.index) as clk:
+        e0.record(st)
+        for _ in range(args.steps):
+            step(flags | abi.TP_FLAG_TIMING)
+        e1.record(st)
+        torch.cuda.synchronize(dev)
+    dist_barrier(ctx)
+    ms = e0.elapsed_time(e1) / args.steps
+    ms = dist_max(ctx, ms)
+    gpu_launches = launches[0]
+    recs = abi.tp_ffn_kernel_times(plan, 100000)
+
+    # dominant kernel and its roofline, from the per-launch events above
+    per = {}
+    for name, t in recs:
+        per.setdefault(name, []).append(t)
+    dom = max(per, key=lambda k: sum(per[k]))
+    kind, work = _kernel_work(w, dom)
+    avg_ms = sum(per[dom]) / len(per[dom])
+    if kind == "flop":
+        ach = work / (avg_ms * 1e-3) / 1e12
+        roof = {"kernel": dom, "bound": "tensor", "achieved": round(ach, 1), "peak": peaks["bf16_sus"],
+                "unit": "TFLOP/s", "frac": round(ach / peaks["bf16_sus"], 4),
+                "peak_kind": f"bf16 sustained ({peaks['source']})", "traffic": NCU_TRAFFIC.get(dom),
+                "work_per_launch": work, "launch_ms": round(avg_ms, 4)}
+    else:
+        ach = work / (avg_ms * 1e-3) / 1e9
+        roof = {"kernel": dom, "bound": "hbm", "achieved": round(ach, 1), "peak": peaks["hbm"], "unit": "GB/s",
+                "frac": round(ach / peaks["hbm"], 4), "peak_kind": f"HBM copy ({peaks['source']})",
+                "traffic": NCU_TRAFFIC.get(dom), "work_per_launch": work, "launch_ms": round(avg_ms, 4)}
+    kernels = {k: {"launches": len(v), "avg_ms": round(sum(v) / len(v), 4), "share": None} for k, v in per.items()}
+    tot = sum(sum(v) for v in per.values())
+    for k, v in per.items():
+        kernels[k]["share"] = round(sum(v) / tot, 4)
+        kind_k, work_k = _kernel_work(w, k)
+        if work_k:
+            rate = work_k / (kernels[k]["avg_ms"] * 1e-3)
+            kernels[k]["rate"] = round(rate / (1e12 if kind_k == "flop" else 1e9), 1)
+            kernels[k]["rate_unit"] = "TFLOP/s" if kind_k == "flop" else "GB/s"
+
+    # end to end: x, dy in from pinned host memory, y, dx back, every step
+    hx = x.cpu().pin_memory()
+    hdy = dy.cpu().pin_memory()
+    hy = torch.empty(y.shape, dtype=y.dtype).pin_memory()
+    hdx = torch.empty(dx.shape, dtype=dx.dtype).pin_memory()
+    dx_in, ddy_in = torch.empty_like(x), torch.empty_like(dy)
+
+    def e2e_step():
+        dx_in.copy_(hx, non_blocking=True)
+        ddy_in.copy_(hdy, non_blocking=True)
+        step(flags, dx_in, ddy_in)
+        hy.copy_(y, non_blocking=True)
+        hdx.copy_(dx, non_blocking=True)
+
+    k_e2e = max(3, args.steps // 2)
+    for _ in range(2):
+        e2e_step()
+    torch.cuda.synchronize(dev)
+    dist_barrier(ctx)
+    e2, e3 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e2.record(st)
+    for _ in range(k_e2e):
+        e2e_step()
+    e3.record(st)
+    torch.cuda.synchronize(dev)
+    e2e_ms = dist_max(ctx, e2.elapsed_time(e3) / k_e2e)
+    h2d = (x.numel() + dy.numel()) * 2
+    d2h = (y.numel() + dx.numel()) * 2
+
+    decode = run_decode(args, ctx, dev, peaks) if not args.no_decode else None
+
+    value = ctx["world"] * flop_step / (ms * 1e-3) / 1e12
+    line = {
+        "metric": METRIC, "value": round(value, 2), "unit": "TFLOP/s", "n_gpus": ctx["world"],
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 4), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic (seeded on-device normals)",
+        "config": {"workload": MAIN, "tokens": w.N, "d": w.d, "d_ff": w.d_ff, "T_p": w.T_p, "act": w.act,
+                   "shard_sum": args.sum, "step": "shard_columns+shard_rows+fwd+bwd (incl. weight grads)",
+                   "flop_per_step": flop_step, "l2": "no flush: per-step working set ~4.3 GB > 129 MB L2",
+                   "parallelism": f"{w.T_p} virtual TP ranks per GPU; replicas across GPUs"},
+        "frac_of_bf16_peak": {"burst": round(value / ctx['world'] / peaks["bf16"], 4),
+                              "sustained": round(value / ctx['world'] / peaks["bf16_sus"], 4),
+                              "peaks": peaks["source"]},
+        "roofline": roof,
+        "kernels": kernels,
+        "e2e": {"value": round(ctx["world"] * flop_step / (e2e_ms * 1e-3) / 1e12, 2), "unit": "TFLOP/s",
+                "ms_per_step": round(e2e_ms, 4), "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+        "gpu_launches": gpu_launches,
+        "clocks": clk.summary(),
+        "decode": decode,
+    }
+    if ctx["rank"] == 0 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(w, budget_s=args.cpu_budget)
+    return line
+
+
+def run_decode(args, ctx, dev, peaks):
+    import torch
+    from synth import WORKLOADS
+    from megatron_tensor_transformer_w1_gb300 import tpffn as abi
+    from megatron_tensor_transformer_w1_gb300.ffn import TensorParallelFFN
+    w = WORKLOADS[DECODE]
+    inp = _device_inputs(w, dev, 20260000 + w.seed_index)
+    ffn = TensorParallelFFN(w.d, w.d_ff, w.T_p, w.act, "bf16", device=dev)
+    plan, st, n = ffn.plan, torch.cuda.current_stream(dev), w.N
+    w13p, w2p = ffn.pack(inp["W1"], inp["W2"], inp["W3"])
+    ws = torch.empty(abi.tp_ffn_workspace_bytes(plan, n, 0), dtype=torch.uint8, device=dev)
+    y = torch.empty(n, w.d, dtype=torch.bfloat16, device=dev)
+
+    def step(f=0):
+        abi.check(abi.tp_ffn_fwd(plan, n, inp["x"], w13p, w2p, None, None, y, None, None, ws, ws.numel(), f, st),
+                  "decode fwd")
+
+    for _ in range(5):
+        step()
+    torch.cuda.synchronize(dev)
+    abi.tp_ffn_kernel_times(plan, 0)
+    k = max(20, args.steps)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(st)
+    for _ in range(k):
+        step(abi.TP_FLAG_TIMING)
+    e1.record(st)
+    torch.cuda.synchronize(dev)
+    ms = dist_max(ctx, e0.elapsed_time(e1) / k)
+    recs = abi.tp_ffn_kernel_times(plan, 100000)
+    per = {}
+    for name, t in recs:
+        per.setdefault(name, []).append(t)
+    nbytes = w.weight_bytes() + 2 * w.N * w.d * 2  # weights + x + y
+    gbs = ctx["world"] * nbytes / (ms * 1e-3) / 1e9
+    dom = max(per, key=lambda q: sum(per[q]))
+    dom_ms = sum(per[dom]) / len(per[dom])
+    dom_bytes = {"up_swiglu": 2 * w.d_ff * w.d * 2 + w.N * w.d * 2 + w.N * w.d_ff * 2,
+                 "down_partials": w.d_ff * w.d * 2 + w.N * w.d_ff * 2 + w.T_p * w.N * w.d * 4}.get(dom, 0)
+    dach = dom_bytes / (dom_ms * 1e-3) / 1e9
+    return {"workload": DECODE, "value": round(gbs, 1), "unit": "GB/s", "ms_per_step": round(ms, 4),
+            "bytes_per_step": nbytes, "frac_of_hbm_peak": round(gbs / ctx["world"] / peaks["hbm"], 4),
+            "roofline": {"kernel": dom, "bound": "hbm", "achieved": round(dach, 1), "peak": peaks["hbm"],
+                         "unit": "GB/s", "frac": round(dach / peaks["hbm"], 4), "traffic": NCU_TRAFFIC.get(dom),
+                         "launch_ms": round(dom_ms, 4)},
+            "kernels": {q: {"launches": len(v), "avg_ms": round(sum(v) / len(v), 4)} for q, v in per.items()}}
+
+
+# ------------------------------------------------------------ CPU oracle
+def cpu_baseline(w, budget_s=15.0, seed=5):
+    """The float64 oracle as it stands, on a bounded sample of the workload:
+    sharded forward of R token rows, backward (dx) of R/2 rows, and the weight
+    gradients of J hidden units (all their dW1/dW3 rows and dW2 columns).
+    Rate = algorithmic FLOPs of those outputs / wall time."""
+    import numpy as np
+    import oracle
+    from synth import make_inputs, to_f64
+
+    inp = make_inputs(w)
+    f = {k: to_f64(v) for k, v in inp.items()}
+    P = oracle.FFN(f["x"], f["W2"], w.T_p, w.act, W1=f["W1"], W3=f["W3"], b1=f["b1"], b2=f["b2"])
+    rng = np.random.default_rng(seed)
+    per_row_fwd = w.fwd_flops() / w.N
+    per_row_dx = (2 * w.d * w.d_ff) + (2 * w.d * w.d_ff * (2 if w.act == "swiglu" else 1))
+    per_j_wgrad = 2 * w.N * w.d * ((2 if w.act == "swiglu" else 1) + 1)
+    # calibrate on 8 rows, then size the sample to the budget
+    t0 = time.perf_counter()
+    P.forward_sharded(rng.choice(w.N, 8, replace=False))
+    t_row = (time.perf_counter() - t0) / 8
+    R = int(max(8, min(w.N, 0.45 * budget_s / max(t_row, 1e-6))))
+    Rb = max(4, R // 2)
+    J = 16
+    rows = rng.choice(w.N, R, replace=False)
+    t0 = time.perf_counter()
+    P.forward_sharded(rows)
+    P.backward_rows(f["dy"], rows[:Rb])
+    P.wgrad_entries(f["dy"], rng.choice(w.d_ff, J, replace=False), np.arange(w.d), np.arange(w.d))
+    el = time.perf_counter() - t0
+    flops = R * per_row_fwd + Rb * per_row_dx + J * per_j_wgrad
+    return {"value": round(flops / el / 1e12, 6), "unit": "TFLOP/s", "cores": oracle.num_threads(),
+            "kind": "oracle", "seconds": round(el, 2),
+            "sample": f"{w.name}: sharded forward of {R} token rows, dx of {Rb} rows, weight gradients of "
+                      f"{J} hidden units (all d inputs/outputs); float64, OpenMP over independent outputs"}
+
+
+def run_reference(args, ctx):
+    """--impl reference: the oracle, timed per step on a bounded sample."""
+    import numpy as np
+    import oracle
+    from synth import WORKLOADS, make_inputs, to_f64
+    w = WORKLOADS[MAIN]
+    inp = make_inputs(w)
+    f = {k: to_f64(v) for k, v in inp.items()}
+    P = oracle.FFN(f["x"], f["W2"], w.T_p, w.act, W1=f["W1"], W3=f["W3"])
+    rng = np.random.default_rng(1)
+    R, Rb, J = 16, 8, 2
+    per_row_fwd = w.fwd_flops() / w.N
+    per_row_dx = 2 * w.d * w.d_ff * 3
+    per_j = 2 * w.N * w.d * 3
+    flops = R * per_row_fwd + Rb * per_row_dx + J * per_j
+
+    def step():
+        rows = rng.choice(w.N, R, replace=False)
+        P.forward_sharded(rows)
+        P.backward_rows(f["dy"], rows[:Rb])
+        P.wgrad_entries(f["dy"], rng.choice(w.d_ff, J, replace=False), np.arange(w.d), np.arange(w.d))
+
+    for _ in range(args.warmup):
+        step()
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        step()
+    el = (time.perf_counter() - t0) / args.steps
+    value = flops / el / 1e12
+    sample = (f"{w.name}: per step, sharded forward of {R} token rows, dx of {Rb} rows and the weight "
+              f"gradients of {J} hidden units, float64 oracle on host cores")
+    return {"metric": METRIC, "value": round(value, 6), "unit": "TFLOP/s", "n_gpus": ctx["world"],
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(el * 1e3, 2),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic (seeded host normals)",
+            "config": {"workload": MAIN, "tokens": w.N, "d": w.d, "d_ff": w.d_ff, "T_p": w.T_p, "act": w.act,
+                       "flop_per_step": flops},
+            "impl": "reference",
+            "cpu_baseline": {"kind": "oracle", "cores": oracle.num_threads(), "sample": sample,
+                             "value": round(value, 6), "unit": "TFLOP/s"},
+            "e2e": {"value": round(value, 6), "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=150)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--sum", choices=["fused", "standalone"], default="fused")
+    ap.add_argument("--no-decode", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-budget", type=float, default=15.0)
+    args = ap.parse_args()
+    ctx = dist_setup(args.gpus)
+    if args.impl == "reference":
+        if ctx["rank"] != 0:
+            return 0
+        print(json.dumps(run_reference(args, ctx)), flush=True)
+        return 0
+    if ctx["world"] > 1:
+        import torch
+        torch.cuda.set_device(ctx["local"])
+        ctx["dist"].init_process_group("nccl", device_id=torch.device("cuda", ctx["local"]))
+    import importlib
+    importlib.import_module("__graft_entry__").build()
+    line = run_ours(args, ctx)
+    if ctx["rank"] == 0:
+        print(json.dumps(line), flush=True)
+    if ctx["dist"] is not None:
+        ctx["dist"].destroy_process_group()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,635 @@
+// tp_api.cu -- the C ABI of include/tpffn.h: plans, buffer sizes, packing,
+// and the forward/backward orchestration of the shard computations.
+//
+// Forward ("7.9 Tensor and pipeline parallelism (TP, PP)", §2.1 "The FFN,
+// sharded"; SwiGLU per "S17 Tensor & Pipeline Parallelism", listing "the
+// megatron pattern"):
+//   1. up GEMM, all shards in one launch: h^(t) = sigma(x W1^(t)T [+ b1^(t)])
+//      (SwiGLU: a and g from one interleaved tile, h = silu(a) * g)
+//   2. down GEMM: y^(t) = h^(t) W2^(t)T as fp32 partials, then the ordered
+//      shard-sum y = sum_t y^(t) (+ b2)   [standalone], or one GEMM whose
+//      K loop walks shard 0..T_p-1 into the same accumulator    [fused]
+// Backward (g is the identity, f sums dx):
+//   3. dh^(t) = dy W2^(t) with the activation derivative fused (dz, or da|dg)
+//   4. dx = sum_t dz^(t) W1^(t) (+ dg^(t) W3^(t))   [fused or standalone]
+//   5. dW2^(t) = dy^T h^(t);  dW1^(t) (|dW3^(t)) = dz^(t)T x  -- per shard
+//   6. db1 = sum_n dz, db2 = sum_n dy (ordered two-pass column sums)
+// The attention output projection (§2.2 "Attention, sharded") is steps 2, 3
+// and 5 with the concatenated head outputs as h and no activation.
+#include <cuda_runtime.h>
+
+#include <atomic>
+#include <cstdint>
+#include <cstring>
+#include <mutex>
+#include <new>
+#include <string>
+#include <vector>
+
+#include "tp_internal.h"
+#include "tpffn.h"
+
+using namespace tpffn;
+
+struct TimingRec {
+  const char* name;
+  cudaEvent_t start, stop;
+};
+
+struct tp_ffn_plan {
+  int64_t d = 0, d_ff = 0, s = 0, s_pad = 0;
+  int T_p = 1, act = TP_ACT_GELU_TANH, dtype = TP_BF16;
+  int n_heads = 0, n_kv_heads = 0;
+  int64_t head_dim = 0;
+  // diagnostics (host side; not thread-safe when TP_FLAG_TIMING is used)
+  mutable std::vector<TimingRec> events;
+  mutable int n_events = 0;
+  mutable int last_launches = 0;
+  mutable cudaStream_t timing_stream = nullptr;
+};
+
+namespace {
+
+constexpr size_t kAlign = 256;
+inline size_t align_up(size_t v) { return (v + kAlign - 1) / kAlign * kAlign; }
+inline int esz(const tp_ffn_plan* p) { return p->dtype == TP_BF16 ? 2 : 4; }
+inline int64_t hidden_width(const tp_ffn_plan* p) {  // columns per shard of the up GEMM / of dz
+  return p->act == TP_ACT_SWIGLU ? 2 * p->s_pad : p->s_pad;
+}
+inline bool aligned16(const void* q) { return (reinterpret_cast<uintptr_t>(q) & 15u) == 0; }
+
+int num_sms_current() {
+  static std::atomic<int> cache[64];
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 148;
+  if (dev < 0 || dev >= 64) return 148;
+  int v = cache[dev].load();
+  if (v <= 0) {
+    if (cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || v <= 0) v = 148;
+    cache[dev].store(v);
+  }
+  return v;
+}
+
+// Rows per block of the first column-sum pass: 256, more for very long token
+// counts so that the chunk count stays within the grid's y limit.
+int64_t colsum_chunk(int64_t rows) {
+  int64_t c = 256;
+  while ((rows + c - 1) / c > 4096) c *= 2;
+  return c;
+}
+
+struct WsLayout {
+  size_t h = 0, part = 0, D = 0, cs = 0, total = 0;
+  bool has_part = false;
+};
+
+WsLayout ws_layout(const tp_ffn_plan* p, int64_t n, int flags) {
+  WsLayout L;
+  size_t off = kAlign;  // error word + header
+  const size_t e = esz(p);
+  if (p->act != TP_ACT_NONE) {
+    L.h = off;
+    off += align_up(static_cast<size_t>(p->T_p) * n * p->s_pad * e);
+    L.D = off;
+    off += align_up(static_cast<size_t>(p->T_p) * n * hidden_width(p) * e);
+  }
+  if (!(flags & TP_SUM_FUSED)) {
+    L.has_part = true;
+    L.part = off;
+    off += align_up(static_cast<size_t>(p->T_p) * n * p->d * 4);
+  }
+  L.cs = off;
+  const int64_t cs1 = colsum_scratch_floats(p->T_p, n, p->s_pad, colsum_chunk(n));
+  const int64_t cs2 = colsum_scratch_floats(1, n, p->d, colsum_chunk(n));
+  off += align_up(static_cast<size_t>(cs1 > cs2 ? cs1 : cs2) * 4);
+  L.total = off;
+  return L;
+}
+
+struct SavedLayout {
+  size_t act = 0, h = 0, total = 0;
+};
+SavedLayout saved_layout(const tp_ffn_plan* p, int64_t n) {
+  SavedLayout S;
+  if (p->act == TP_ACT_NONE) return S;
+  const size_t e = esz(p);
+  S.act = 0;
+  S.h = align_up(static_cast<size_t>(p->T_p) * n * hidden_width(p) * e);
+  S.total = S.h + align_up(static_cast<size_t>(p->T_p) * n * p->s_pad * e);
+  return S;
+}
+
+// Timing hooks: an event pair per launch, kept in the plan.
+void timing_before(void* user, const char* name) {
+  const tp_ffn_plan* p = static_cast<const tp_ffn_plan*>(user);
+  if (p->n_events >= static_cast<int>(p->events.size())) {
+    TimingRec r{name, nullptr, nullptr};
+    cudaEventCreate(&r.start);
+    cudaEventCreate(&r.stop);
+    p->events.push_back(r);
+  }
+  TimingRec& r = p->events[p->n_events];
+  r.name = name;
+  cudaEventRecord(r.start, p->timing_stream);
+}
+void timing_after(void* user) {
+  const tp_ffn_plan* p = static_cast<const tp_ffn_plan*>(user);
+  cudaEventRecord(p->events[p->n_events].stop, p->timing_stream);
+  p->n_events++;
+}
+
+int make_ctx(const tp_ffn_plan* p, void* workspace, int flags, cudaStream_t stream, LaunchCtx& ctx) {
+  ctx.stream = stream;
+  ctx.err = static_cast<int*>(workspace);
+  ctx.num_sms = num_sms_current();
+  ctx.debug_skip_load = (flags & TP_FLAG_DEBUG_SKIP_LOAD) ? 1 : 0;
+  ctx.timing = (flags & TP_FLAG_TIMING) != 0;
+  if (ctx.timing) {
+    p->timing_stream = stream;
+    ctx.before = timing_before;
+    ctx.after = timing_after;
+    ctx.user = const_cast<tp_ffn_plan*>(p);
+  }
+  if (cudaMemsetAsync(workspace, 0, sizeof(int), stream) != cudaSuccess) return TP_ERR_CUDA;
+  return TP_OK;
+}
+
+int finish_call(const tp_ffn_plan* p, LaunchCtx& ctx, int rc, int flags, void* workspace) {
+  p->last_launches = ctx.launches;
+  if (rc != TP_OK) return rc;
+  if (cudaPeekAtLastError() != cudaSuccess) return TP_ERR_CUDA;
+  if (flags & TP_FLAG_SYNC) return tp_ffn_last_device_error(p, workspace, ctx.stream);
+  return TP_OK;
+}
+
+int run_gemm(const tp_ffn_plan* p, const GemmSpec& g, LaunchCtx& ctx) {
+  return p->dtype == TP_BF16 ? launch_tc_gemm(g, ctx) : launch_simt_gemm(g, ctx);
+}
+
+Operand kmajor(const void* ptr, int64_t inner, int64_t rows, int64_t batch, int64_t rs, int64_t bs, int bsel,
+               int gsel) {
+  Operand o;
+  o.ptr = ptr;
+  o.inner = inner;
+  o.rows = rows;
+  o.batch = batch;
+  o.row_stride = rs;
+  o.batch_stride = bs;
+  o.mn_major = 0;
+  o.bsel = bsel;
+  o.gsel = gsel;
+  return o;
+}
+Operand mnmajor(const void* ptr, int64_t inner, int64_t rows, int64_t batch, int64_t rs, int64_t bs, int bsel,
+                int gsel) {
+  Operand o = kmajor(ptr, inner, rows, batch, rs, bs, bsel, gsel);
+  o.mn_major = 1;
+  return o;
+}
+
+}  // namespace
+
+// ======================================================================= ABI
+extern "C" {
+
+const char* tp_ffn_status_string(int status) {
+  switch (status) {
+    case TP_OK: return "TP_OK";
+    case TP_ERR_INVALID: return "TP_ERR_INVALID: invalid argument";
+    case TP_ERR_UNSUPPORTED: return "TP_ERR_UNSUPPORTED: not supported by this build";
+    case TP_ERR_CUDA: return "TP_ERR_CUDA: CUDA call or kernel launch failed";
+    case TP_ERR_TIMEOUT: return "TP_ERR_TIMEOUT: a device-side bounded wait expired";
+    case TP_ERR_ALIGN: return "TP_ERR_ALIGN: pointer or stride not 16-byte aligned";
+    default: return "unknown status";
+  }
+}
+
+int tp_ffn_plan_create(tp_ffn_plan** out, int64_t d, int64_t d_ff, int T_p, int act, int dtype) {
+  if (!out) return TP_ERR_INVALID;
+  *out = nullptr;
+  if (d < 1 || d_ff < 1 || T_p < 1 || d_ff % T_p != 0) return TP_ERR_INVALID;
+  if (act != TP_ACT_NONE && act != TP_ACT_GELU_TANH && act != TP_ACT_SWIGLU) return TP_ERR_INVALID;
+  if (dtype != TP_BF16 && dtype != TP_F32) return TP_ERR_INVALID;
+  const int64_t s = d_ff / T_p;
+  if (dtype == TP_BF16) {
+    if (d % 8 != 0) return TP_ERR_UNSUPPORTED;
+    if (act == TP_ACT_NONE && s % 8 != 0) return TP_ERR_UNSUPPORTED;
+  }
+  if (d > (int64_t(1) << 30) || d_ff > (int64_t(1) << 30)) return TP_ERR_UNSUPPORTED;
+  tp_ffn_plan* p = new (std::nothrow) tp_ffn_plan();
+  if (!p) return TP_ERR_INVALID;
+  p->d = d;
+  p->d_ff = d_ff;
+  p->T_p = T_p;
+  p->act = act;
+  p->dtype = dtype;
+  p->s = s;
+  if (act == TP_ACT_SWIGLU)
+    p->s_pad = (s + 127) / 128 * 128;
+  else if (act == TP_ACT_NONE)
+    p->s_pad = s;
+  else
+    p->s_pad = (s + 7) / 8 * 8;
+  *out = p;
+  return TP_OK;
+}
+
+int tp_attn_out_plan_create(tp_ffn_plan** out, int64_t d_model, int n_heads, int n_kv_heads, int64_t head_dim,
+                            int T_p, int dtype) {
+  if (!out) return TP_ERR_INVALID;
+  *out = nullptr;
+  if (n_heads < 1 || n_kv_heads < 1 || head_dim < 1 || T_p < 1) return TP_ERR_INVALID;
+  if (n_heads % T_p != 0 || n_kv_heads % T_p != 0) return TP_ERR_INVALID;
+  if (n_heads % n_kv_heads != 0) return TP_ERR_INVALID;
+  int rc = tp_ffn_plan_create(out, d_model, static_cast<int64_t>(n_heads) * head_dim, T_p, TP_ACT_NONE, dtype);
+  if (rc == TP_OK) {
+    (*out)->n_heads = n_heads;
+    (*out)->n_kv_heads = n_kv_heads;
+    (*out)->head_dim = head_dim;
+  }
+  return rc;
+}
+
+void tp_ffn_plan_destroy(tp_ffn_plan* plan) {
+  if (!plan) return;
+  for (auto& r : plan->events) {
+    if (r.start) cudaEventDestroy(r.start);
+    if (r.stop) cudaEventDestroy(r.stop);
+  }
+  delete plan;
+}
+
+int tp_ffn_plan_info(const tp_ffn_plan* p, int64_t* d, int64_t* d_ff, int* T_p, int* act, int* dtype, int64_t* s,
+                     int64_t* s_pad) {
+  if (!p) return TP_ERR_INVALID;
+  if (d) *d = p->d;
+  if (d_ff) *d_ff = p->d_ff;
+  if (T_p) *T_p = p->T_p;
+  if (act) *act = p->act;
+  if (dtype) *dtype = p->dtype;
+  if (s) *s = p->s;
+  if (s_pad) *s_pad = p->s_pad;
+  return TP_OK;
+}
+
+size_t tp_ffn_packed_bytes(const tp_ffn_plan* p, int which) {
+  if (!p) return 0;
+  const size_t e = esz(p);
+  if (which == TP_PACK_COLUMNS)
+    return p->act == TP_ACT_NONE ? 0 : static_cast<size_t>(p->T_p) * hidden_width(p) * p->d * e;
+  if (which == TP_PACK_ROWS) return static_cast<size_t>(p->T_p) * p->d * p->s_pad * e;
+  return 0;
+}
+
+size_t tp_ffn_saved_bytes(const tp_ffn_plan* p, int64_t n) {
+  if (!p || n < 0) return 0;
+  return saved_layout(p, n).total;
+}
+
+size_t tp_ffn_workspace_bytes(const tp_ffn_plan* p, int64_t n, int flags) {
+  if (!p || n < 0) return 0;
+  return ws_layout(p, n, flags).total;
+}
+
+int tp_ffn_shard_columns(const tp_ffn_plan* p, const void* W1, const void* W3, void* packed, tp_stream_t stream) {
+  if (!p || !W1 || !packed || p->act == TP_ACT_NONE) return TP_ERR_INVALID;
+  if (p->act == TP_ACT_SWIGLU && !W3) return TP_ERR_INVALID;
+  return launch_pack_columns(W1, W3, packed, p->T_p, p->s, p->s_pad, p->d, p->act == TP_ACT_SWIGLU, esz(p), 0,
+                             stream);
+}
+
+int tp_ffn_shard_rows(const tp_ffn_plan* p, const void* W2, void* packed, tp_stream_t stream) {
+  if (!p || !W2 || !packed) return TP_ERR_INVALID;
+  return launch_pack_rows(W2, packed, p->T_p, p->s, p->s_pad, p->d, esz(p), 0, stream);
+}
+
+int tp_ffn_unshard_columns(const tp_ffn_plan* p, const void* packed, void* W1, void* W3, tp_stream_t stream) {
+  if (!p || !W1 || !packed || p->act == TP_ACT_NONE) return TP_ERR_INVALID;
+  if (p->act == TP_ACT_SWIGLU && !W3) return TP_ERR_INVALID;
+  return launch_pack_columns(W1, W3, const_cast<void*>(packed), p->T_p, p->s, p->s_pad, p->d,
+                             p->act == TP_ACT_SWIGLU, esz(p), 1, stream);
+}
+
+int tp_ffn_unshard_rows(const tp_ffn_plan* p, const void* packed, void* W2, tp_stream_t stream) {
+  if (!p || !W2 || !packed) return TP_ERR_INVALID;
+  return launch_pack_rows(W2, const_cast<void*>(packed), p->T_p, p->s, p->s_pad, p->d, esz(p), 1, stream);
+}
+
+int tp_ffn_fwd(const tp_ffn_plan* p, int64_t n, const void* x, const void* w13p, const void* w2p, const void* b1,
+               const void* b2, void* y, float* partials, void* saved, void* workspace, size_t workspace_bytes,
+               int flags, tp_stream_t stream) {
+  if (!p || n < 0) return TP_ERR_INVALID;
+  if (n == 0) {
+    p->last_launches = 0;
+    return TP_OK;
+  }
+  const bool none = p->act == TP_ACT_NONE;
+  const bool fused = (flags & TP_SUM_FUSED) != 0;
+  if (!x || !w2p || !y || !workspace) return TP_ERR_INVALID;
+  if (!none && !w13p) return TP_ERR_INVALID;
+  if (fused && partials) return TP_ERR_INVALID;
+  if (b1 && p->act != TP_ACT_GELU_TANH) return TP_ERR_UNSUPPORTED;
+  if (n > (int64_t(1) << 30)) return TP_ERR_UNSUPPORTED;
+  const WsLayout L = ws_layout(p, n, flags);
+  if (workspace_bytes < L.total) return TP_ERR_INVALID;
+  {
+    const void* ptrs[] = {x, w13p, w2p, b1, b2, y, partials, saved, workspace};
+    for (const void* q : ptrs)
+      if (q && !aligned16(q)) return TP_ERR_ALIGN;
+  }
+
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  LaunchCtx ctx;
+  int rc = make_ctx(p, workspace, flags, st, ctx);
+  if (rc) return finish_call(p, ctx, rc, flags, workspace);
+  char* ws = static_cast<char*>(workspace);
+  const SavedLayout S = saved_layout(p, n);
+  const int64_t T = p->T_p, d = p->d, sp = p->s_pad, W = hidden_width(p);
+  const int out_bf16 = p->dtype == TP_BF16;
+
+  // ---- 1. up GEMM (column-sharded W1 / W3) + activation
+  const void* hbuf = x;  // NONE: the head outputs are the hidden activations
+  if (!none) {
+    void* h = saved ? static_cast<char*>(saved) + S.h : ws + L.h;
+    GemmSpec g;
+    g.name = p->act == TP_ACT_SWIGLU ? "up_swiglu" : "up_gelu";
+    g.M = n;
+    g.N = W;
+    g.K = d;
+    g.NB = static_cast<int>(T);
+    g.G = 1;
+    g.A = kmajor(x, d, n, 1, d, n * d, 0, 0);
+    g.B = kmajor(w13p, d, W, T, d, W * d, 1, 0);
+    g.epi = p->act == TP_ACT_SWIGLU ? EPI_SWIGLU_FWD : EPI_GELU_FWD;
+    g.out = h;
+    g.out_bs = n * sp;
+    g.out_rs = sp;
+    if (saved) {
+      g.out2 = static_cast<char*>(saved) + S.act;
+      g.out2_bs = n * W;
+      g.out2_rs = W;
+    }
+    g.bias = b1;
+    g.bias_bs = p->s;
+    g.bias_len = p->s;
+    g.n_store = sp;
+    g.out_bf16 = out_bf16;
+    rc = run_gemm(p, g, ctx);
+    if (rc) return finish_call(p, ctx, rc, flags, workspace);
+    hbuf = h;
+  }
+
+  // ---- 2. down GEMM (row-sharded W2) + g-operator shard-sum
+  GemmSpec g;
+  g.M = n;
+  g.N = d;
+  g.K = sp;
+  if (none)
+    g.A = kmajor(hbuf, p->s, n, T, p->d_ff, p->s, 0, 0);  // heads of shard t: columns [t*s, (t+1)*s)
+  else
+    g.A = kmajor(hbuf, sp, n, T, sp, n * sp, 0, 0);
+  g.B = kmajor(w2p, sp, d, T, sp, d * sp, 0, 0);
+  g.n_store = d;
+  g.out_bf16 = out_bf16;
+  if (fused) {
+    g.name = "down_fused_sum";
+    g.NB = 1;
+    g.G = static_cast<int>(T);
+    g.A.gsel = 1;
+    g.B.gsel = 1;
+    g.epi = EPI_OUT;
+    g.out = y;
+    g.out_bs = 0;
+    g.out_rs = d;
+    g.bias = b2;
+    g.bias_bs = 0;
+    g.bias_len = d;
+    rc = run_gemm(p, g, ctx);
+  } else {
+    float* part = partials ? partials : reinterpret_cast<float*>(ws + L.part);
+    g.name = "down_partials";
+    g.NB = static_cast<int>(T);
+    g.G = 1;
+    g.A.bsel = 1;
+    g.B.bsel = 1;
+    g.epi = EPI_F32;
+    g.out = part;
+    g.out_bs = n * d;
+    g.out_rs = d;
+    rc = run_gemm(p, g, ctx);
+    if (!rc) rc = launch_shard_sum(part, static_cast<int>(T), n, d, b2, y, out_bf16, ctx, "shard_sum_y");
+  }
+  return finish_call(p, ctx, rc, flags, workspace);
+}
+
+int tp_ffn_bwd(const tp_ffn_plan* p, int64_t n, const void* x, const void* w13p, const void* w2p, const void* saved,
+               const void* dy, void* dx, float* dx_partials, void* dw13p, void* dw2p, void* db1, void* db2,
+               void* workspace, size_t workspace_bytes, int flags, tp_stream_t stream) {
+  if (!p || n < 0) return TP_ERR_INVALID;
+  if (n == 0) {
+    p->last_launches = 0;
+    return TP_OK;
+  }
+  const bool none = p->act == TP_ACT_NONE;
+  const bool fused = (flags & TP_SUM_FUSED) != 0;
+  if (!x || !w2p || !dy || !dx || !dw2p || !workspace) return TP_ERR_INVALID;
+  if (!none && (!w13p || !saved || !dw13p)) return TP_ERR_INVALID;
+  if ((fused || none) && dx_partials) return TP_ERR_INVALID;
+  if (db1 && p->act != TP_ACT_GELU_TANH) return TP_ERR_UNSUPPORTED;
+  if (n > (int64_t(1) << 30)) return TP_ERR_UNSUPPORTED;
+  const WsLayout L = ws_layout(p, n, flags);
+  if (workspace_bytes < L.total) return TP_ERR_INVALID;
+  {
+    const void* ptrs[] = {x, w13p, w2p, saved, dy, dx, dx_partials, dw13p, dw2p, db1, db2, workspace};
+    for (const void* q : ptrs)
+      if (q && !aligned16(q)) return TP_ERR_ALIGN;
+  }
+
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  LaunchCtx ctx;
+  int rc = make_ctx(p, workspace, flags, st, ctx);
+  if (rc) return finish_call(p, ctx, rc, flags, workspace);
+  char* ws = static_cast<char*>(workspace);
+  const SavedLayout S = saved_layout(p, n);
+  const int64_t T = p->T_p, d = p->d, sp = p->s_pad, W = hidden_width(p), s = p->s;
+  const int out_bf16 = p->dtype == TP_BF16;
+  float* cs_scratch = reinterpret_cast<float*>(ws + L.cs);
+
+  if (none) {
+    // dc^(t) = dy W_O^(t): each shard writes its own head columns of dx.
+    GemmSpec g;
+    g.name = "dgrad_heads";
+    g.M = n;
+    g.N = s;
+    g.K = d;
+    g.NB = static_cast<int>(T);
+    g.A = kmajor(dy, d, n, 1, d, n * d, 0, 0);
+    g.B = mnmajor(w2p, sp, d, T, sp, d * sp, 1, 0);
+    g.epi = EPI_OUT;
+    g.out = dx;
+    g.out_bs = s;
+    g.out_rs = p->d_ff;
+    g.n_store = s;
+    g.out_bf16 = out_bf16;
+    rc = run_gemm(p, g, ctx);
+    if (rc) return finish_call(p, ctx, rc, flags, workspace);
+    // dW_O^(t) = dy^T c^(t)
+    GemmSpec w;
+    w.name = "wgrad_rows";
+    w.M = d;
+    w.N = s;
+    w.K = n;
+    w.NB = static_cast<int>(T);
+    w.A = mnmajor(dy, d, n, 1, d, n * d, 0, 0);
+    w.B = mnmajor(x, s, n, T, p->d_ff, s, 1, 0);
+    w.epi = EPI_OUT;
+    w.out = dw2p;
+    w.out_bs = d * sp;
+    w.out_rs = sp;
+    w.n_store = s;
+    w.out_bf16 = out_bf16;
+    rc = run_gemm(p, w, ctx);
+    if (!rc && db2)
+      rc = launch_colsum(dy, out_bf16, 1, n, d, d, n * d, db2, out_bf16, 0, cs_scratch, colsum_chunk(n), ctx,
+                         "colsum_db2");
+    return finish_call(p, ctx, rc, flags, workspace);
+  }
+
+  void* D = ws + L.D;
+  const void* hsaved = static_cast<const char*>(saved) + S.h;
+  const void* asaved = static_cast<const char*>(saved) + S.act;
+
+  // ---- 3. dh^(t) = dy W2^(t), activation derivative fused
+  {
+    GemmSpec g;
+    g.name = p->act == TP_ACT_SWIGLU ? "dgrad_h_swiglu" : "dgrad_h_gelu";
+    g.M = n;
+    g.N = sp;
+    g.K = d;
+    g.NB = static_cast<int>(T);
+    g.A = kmajor(dy, d, n, 1, d, n * d, 0, 0);
+    g.B = mnmajor(w2p, sp, d, T, sp, d * sp, 1, 0);
+    g.epi = p->act == TP_ACT_SWIGLU ? EPI_SWIGLU_BWD : EPI_GELU_BWD;
+    g.out = D;
+    g.out_bs = n * W;
+    g.out_rs = W;
+    g.aux = asaved;
+    g.aux_bs = n * W;
+    g.aux_rs = W;
+    g.n_store = sp;
+    g.out_bf16 = out_bf16;
+    rc = run_gemm(p, g, ctx);
+    if (rc) return finish_call(p, ctx, rc, flags, workspace);
+  }
+  // ---- 4. dx = sum_t D^(t) W13^(t)   (f operator)
+  {
+    GemmSpec g;
+    g.M = n;
+    g.N = d;
+    g.K = W;
+    g.A = kmajor(D, W, n, T, W, n * W, 0, 0);
+    g.B = mnmajor(w13p, d, W, T, d, W * d, 0, 0);
+    g.n_store = d;
+    g.out_bf16 = out_bf16;
+    if (fused) {
+      g.name = "dgrad_x_fused_sum";
+      g.NB = 1;
+      g.G = static_cast<int>(T);
+      g.A.gsel = 1;
+      g.B.gsel = 1;
+      g.epi = EPI_OUT;
+      g.out = dx;
+      g.out_bs = 0;
+      g.out_rs = d;
+      rc = run_gemm(p, g, ctx);
+    } else {
+      float* part = dx_partials ? dx_partials : reinterpret_cast<float*>(ws + L.part);
+      g.name = "dgrad_x_partials";
+      g.NB = static_cast<int>(T);
+      g.A.bsel = 1;
+      g.B.bsel = 1;
+      g.epi = EPI_F32;
+      g.out = part;
+      g.out_bs = n * d;
+      g.out_rs = d;
+      rc = run_gemm(p, g, ctx);
+      if (!rc) rc = launch_shard_sum(part, static_cast<int>(T), n, d, nullptr, dx, out_bf16, ctx, "shard_sum_dx");
+    }
+    if (rc) return finish_call(p, ctx, rc, flags, workspace);
+  }
+  // ---- 5. weight gradients, per shard
+  {
+    GemmSpec g;
+    g.name = "wgrad_w2";
+    g.M = d;
+    g.N = sp;
+    g.K = n;
+    g.NB = static_cast<int>(T);
+    g.A = mnmajor(dy, d, n, 1, d, n * d, 0, 0);
+    g.B = mnmajor(hsaved, sp, n, T, sp, n * sp, 1, 0);
+    g.epi = EPI_OUT;
+    g.out = dw2p;
+    g.out_bs = d * sp;
+    g.out_rs = sp;
+    g.n_store = sp;
+    g.out_bf16 = out_bf16;
+    rc = run_gemm(p, g, ctx);
+    if (rc) return finish_call(p, ctx, rc, flags, workspace);
+  }
+  {
+    GemmSpec g;
+    g.name = p->act == TP_ACT_SWIGLU ? "wgrad_w13" : "wgrad_w1";
+    g.M = W;
+    g.N = d;
+    g.K = n;
+    g.NB = static_cast<int>(T);
+    g.A = mnmajor(D, W, n, T, W, n * W, 1, 0);
+    g.B = mnmajor(x, d, n, 1, d, n * d, 0, 0);
+    g.epi = EPI_OUT;
+    g.out = dw13p;
+    g.out_bs = W * d;
+    g.out_rs = d;
+    g.n_store = d;
+    g.out_bf16 = out_bf16;
+    rc = run_gemm(p, g, ctx);
+    if (rc) return finish_call(p, ctx, rc, flags, workspace);
+  }
+  // ---- 6. bias gradients
+  if (db1)
+    rc = launch_colsum(D, out_bf16, T, n, s, W, n * W, db1, out_bf16, s, cs_scratch, colsum_chunk(n), ctx,
+                       "colsum_db1");
+  if (!rc && db2)
+    rc = launch_colsum(dy, out_bf16, 1, n, d, d, n * d, db2, out_bf16, 0, cs_scratch, colsum_chunk(n), ctx,
+                       "colsum_db2");
+  return finish_call(p, ctx, rc, flags, workspace);
+}
+
+int tp_ffn_last_device_error(const tp_ffn_plan* p, const void* workspace, tp_stream_t stream) {
+  if (!p || !workspace) return TP_ERR_INVALID;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  if (cudaStreamSynchronize(st) != cudaSuccess) return TP_ERR_CUDA;
+  int word = 0;
+  if (cudaMemcpy(&word, workspace, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess) return TP_ERR_CUDA;
+  if (word & DEV_ERR_TIMEOUT) return TP_ERR_TIMEOUT;
+  return word ? TP_ERR_CUDA : TP_OK;
+}
+
+int tp_ffn_kernel_times(const tp_ffn_plan* p, int max, const char** names, float* ms) {
+  if (!p) return -1;
+  for (int i = 0; i < p->n_events && i < max; ++i) {
+    const TimingRec& r = p->events[i];
+    cudaEventSynchronize(r.stop);
+    float t = 0.f;
+    cudaEventElapsedTime(&t, r.start, r.stop);
+    if (names) names[i] = r.name;
+    if (ms) ms[i] = t;
+  }
+  const int n = p->n_events;
+  p->n_events = 0;  // read and clear: the next timed call starts a new list
+  return n;
+}
+
+int tp_ffn_last_launch_count(const tp_ffn_plan* p) { return p ? p->last_launches : -1; }
+
+}  // extern "C"

@@ -1,0 +1,686 @@
+// tp_gemm_tc.cu -- the tensor-core GEMM of every bf16 shard computation.
+//
+// Blackwell (sm_103a) design, written for this library:
+//   * one persistent CTA per SM, 192 threads in three roles:
+//       warp 0      : TMA producer (one elected lane) -- cp.async.bulk.tensor
+//                     3-D tiled loads, 128-byte swizzle, into a STAGES-deep
+//                     shared-memory ring guarded by mbarriers;
+//       warp 1      : allocates tensor memory, and one lane issues
+//                     tcgen05.mma (kind::f16, bf16 x bf16 -> fp32, M=128,
+//                     N=BN, K=16 per instruction) and tcgen05.commit;
+//       warps 2..5  : epilogue -- tcgen05.ld of the fp32 accumulator
+//                     (warp w reads TMEM lanes 32*(w%4)..), fused activation
+//                     or derivative, vectorised global stores;
+//   * the accumulator is double-buffered in tensor memory (2 x BN columns),
+//     so the epilogue of one tile overlaps the MMA K-loop of the next;
+//   * every wait on an mbarrier is bounded: after the time limit the waiting
+//     thread sets the device error word and a CTA-wide abort flag, every role
+//     leaves its loop, in-flight copies and MMAs are drained with bounded
+//     waits, and tensor memory is freed before the CTA exits.
+//
+// Operand majorness: K-major tiles are one TMA box {64 (K), rows} and use the
+// canonical 128B-swizzle K-major layout (8-row atoms of 1024 B, SBO = 1024,
+// K advanced inside the atom by 32 B per MMA).  MN-major tiles are boxes
+// {64 (M or N), 64 (K)}: 128-byte rows along M/N, one 8 KB box per 64 M/N
+// (LBO = 8192 between boxes, SBO = 1024 between 8-row K groups, K advanced by
+// 2048 B per MMA).  MN-major serves the backward GEMMs that contract over the
+// hidden or token dimension without transposing any buffer.
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include <atomic>
+#include <mutex>
+
+#include "tp_internal.h"
+#include "tpffn.h"
+
+namespace tpffn {
+namespace tc {
+
+constexpr int BM = 128;
+constexpr int BK = 64;
+constexpr int THREADS = 192;
+
+struct Params {
+  int M, N, K;
+  int NB, G;
+  int tiles_m, tiles_n, k_blocks;
+  int a_bsel, a_gsel, b_bsel, b_gsel;
+  int a_swap, b_swap;
+  void* out;
+  long long out_bs, out_rs;
+  void* out2;
+  long long out2_bs, out2_rs;
+  const void* aux;
+  long long aux_bs, aux_rs;
+  const __nv_bfloat16* bias;
+  long long bias_bs, bias_len;
+  long long n_store;
+  int* err;
+  unsigned long long timeout_ns;
+  int debug_skip;
+};
+
+// ------------------------------------------------------------ PTX wrappers
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count) : "memory");
+}
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)), "r"(bytes)
+               : "memory");
+}
+__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+__device__ __forceinline__ uint64_t global_timer() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
+// Bounded wait.  Returns false on timeout (after raising the error word and
+// the CTA's abort flag) or when another role already aborted.
+__device__ __forceinline__ bool wait_bounded(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
+                                             const Params& p, bool honour_abort = true) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = global_timer();
+  uint32_t n = 0;
+  while (true) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if ((++n & 31u) == 0) {
+      if (honour_abort && *abort_flag) return false;
+      if (global_timer() - t0 > p.timeout_ns) {
+        *abort_flag = 1;
+        atomicOr(p.err, DEV_ERR_TIMEOUT);
+        __threadfence();
+        return false;
+      }
+    }
+  }
+}
+
+__device__ __forceinline__ void tma_load_3d(void* dst, const CUtensorMap* tm, uint64_t* bar, int c0, int c1,
+                                            int c2) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes "
+      "[%0], [%1, {%2, %3, %4}], [%5];" ::"r"(smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(tm)), "r"(c0), "r"(c1), "r"(c2), "r"(smem_u32(bar))
+      : "memory");
+}
+__device__ __forceinline__ void prefetch_tmap(const CUtensorMap* tm) {
+  asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(tm)) : "memory");
+}
+
+__device__ __forceinline__ void tc_fence_before() {
+  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tc_fence_after() {
+  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_alloc(uint32_t* slot, uint32_t ncols) {
+  asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(slot)),
+               "r"(ncols)
+               : "memory");
+  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
+  asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
+}
+__device__ __forceinline__ void umma_bf16(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                                          uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+__device__ __forceinline__ void umma_commit(uint64_t* bar) {
+  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
+                   smem_u32(bar))
+               : "memory");
+}
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+      "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+      "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+        "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]),
+        "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]),
+        "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]),
+        "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+      : "r"(taddr));
+}
+__device__ __forceinline__ void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
+
+// Shared-memory matrix descriptor (tcgen05): start address, leading and
+// stride byte offsets (>> 4), descriptor version 1 (bits 46-47), 128-byte
+// swizzle (layout type 2, bits 61-63).
+template <bool MN>
+__device__ __forceinline__ uint64_t smem_desc(uint32_t tile_addr, int kstep) {
+  const uint32_t addr = tile_addr + (MN ? kstep * 2048u : kstep * 32u);
+  const uint64_t lbo = MN ? 8192u : 16u;
+  const uint64_t sbo = 1024u;
+  return static_cast<uint64_t>((addr & 0x3FFFFu) >> 4) | ((lbo >> 4) << 16) | ((sbo >> 4) << 32) |
+         (1ull << 46) | (2ull << 61);
+}
+
+// Instruction descriptor, kind::f16: D fp32 (bits 4-5 = 1), A and B bf16
+// (bits 7-9, 10-12 = 1), transpose (MN-major) bits 15/16, N>>3 at 17, M>>4 at 24.
+template <int BN, bool AMN, bool BMN>
+__device__ __forceinline__ constexpr uint32_t instr_desc() {
+  return (1u << 4) | (1u << 7) | (1u << 10) | (static_cast<uint32_t>(AMN) << 15) |
+         (static_cast<uint32_t>(BMN) << 16) | (static_cast<uint32_t>(BN >> 3) << 17) |
+         (static_cast<uint32_t>(BM >> 4) << 24);
+}
+
+// ------------------------------------------------------------ activations
+__device__ __forceinline__ float gelu_tanh_f(float z) {
+  const float k = 0.7978845608028654f;  // sqrt(2/pi)
+  return 0.5f * z * (1.0f + tanhf(k * (z + 0.044715f * z * z * z)));
+}
+__device__ __forceinline__ float gelu_tanh_grad_f(float z) {
+  const float k = 0.7978845608028654f;
+  const float t = tanhf(k * (z + 0.044715f * z * z * z));
+  return 0.5f * (1.0f + t) + 0.5f * z * (1.0f - t * t) * k * (1.0f + 3.0f * 0.044715f * z * z);
+}
+__device__ __forceinline__ float sigmoid_f(float a) { return 1.0f / (1.0f + expf(-a)); }
+
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+  __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<uint32_t*>(&v);
+}
+__device__ __forceinline__ void store_bf16x8(__nv_bfloat16* dst, const float* v) {
+  uint4 q;
+  q.x = pack_bf16x2(v[0], v[1]);
+  q.y = pack_bf16x2(v[2], v[3]);
+  q.z = pack_bf16x2(v[4], v[5]);
+  q.w = pack_bf16x2(v[6], v[7]);
+  *reinterpret_cast<uint4*>(dst) = q;
+}
+__device__ __forceinline__ void load_bf16x8(const __nv_bfloat16* src, float* v) {
+  uint4 q = *reinterpret_cast<const uint4*>(src);
+  const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&q);
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    float2 f = __bfloat1622float2(h[i]);
+    v[2 * i] = f.x;
+    v[2 * i + 1] = f.y;
+  }
+}
+
+// ------------------------------------------------------------ tile order
+__device__ __forceinline__ void decode_tile(const Params& p, int tile, int& b, int& mb, int& nb) {
+  const int tpb = p.tiles_m * p.tiles_n;
+  b = tile / tpb;
+  const int r = tile - b * tpb;
+  constexpr int GM = 8;  // m-blocks per raster group (L2 reuse of B tiles)
+  const int group = r / (GM * p.tiles_n);
+  const int first_m = group * GM;
+  const int gm = min(p.tiles_m - first_m, GM);
+  const int in_group = r - group * GM * p.tiles_n;
+  mb = first_m + in_group % gm;
+  nb = in_group / gm;
+}
+
+// ------------------------------------------------------------ epilogues
+// One thread owns one output row of the tile; `taddr` points at its TMEM
+// lane and the first column of the accumulator buffer.
+template <int BN, int EPI>
+__device__ __forceinline__ void epilogue_tile(const Params& p, int b, int row, bool row_ok, int n0, int nb,
+                                              uint32_t taddr) {
+  if constexpr (EPI == EPI_SWIGLU_FWD) {
+    static_assert(BN == 256, "SwiGLU forward tiles hold 128 a-columns then 128 g-columns");
+    __nv_bfloat16* hout = static_cast<__nv_bfloat16*>(p.out) + b * p.out_bs + (long long)row * p.out_rs;
+    __nv_bfloat16* sv = p.out2 ? static_cast<__nv_bfloat16*>(p.out2) + b * p.out2_bs + (long long)row * p.out2_rs
+                               : nullptr;
+#pragma unroll 1
+    for (int c = 0; c < 4; ++c) {
+      uint32_t ra[32], rg[32];
+      __syncwarp();  // tcgen05.ld is warp-collective: reconverge first
+      tmem_ld32(taddr + c * 32, ra);
+      tmem_ld32(taddr + 128 + c * 32, rg);
+      tmem_wait_ld();
+      if (row_ok) {
+        const int hcol = nb * 128 + c * 32;  // hidden unit within the shard
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          float h[8], a[8], g[8];
+#pragma unroll
+          for (int j = 0; j < 8; ++j) {
+            a[j] = __uint_as_float(ra[q * 8 + j]);
+            g[j] = __uint_as_float(rg[q * 8 + j]);
+            h[j] = a[j] * sigmoid_f(a[j]) * g[j];
+          }
+          store_bf16x8(hout + hcol + q * 8, h);
+          if (sv) {
+            store_bf16x8(sv + nb * 256 + c * 32 + q * 8, a);
+            store_bf16x8(sv + nb * 256 + 128 + c * 32 + q * 8, g);
+          }
+        }
+      }
+    }
+    return;
+  } else {
+#pragma unroll 1
+    for (int c = 0; c < BN / 32; ++c) {
+      uint32_t r[32];
+      __syncwarp();  // tcgen05.ld is warp-collective: reconverge first
+      tmem_ld32(taddr + c * 32, r);
+      tmem_wait_ld();
+      const int nc = n0 + c * 32;
+      if (!row_ok || nc >= p.n_store) continue;  // no warp-collective op follows in this iteration
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const int n = nc + q * 8;
+        if (n >= p.n_store) break;  // n_store is a multiple of 8
+        float v[8];
+#pragma unroll
+        for (int j = 0; j < 8; ++j) v[j] = __uint_as_float(r[q * 8 + j]);
+        if constexpr (EPI == EPI_F32) {
+          float* o = static_cast<float*>(p.out) + b * p.out_bs + (long long)row * p.out_rs + n;
+          *reinterpret_cast<float4*>(o) = make_float4(v[0], v[1], v[2], v[3]);
+          *reinterpret_cast<float4*>(o + 4) = make_float4(v[4], v[5], v[6], v[7]);
+        } else if constexpr (EPI == EPI_OUT) {
+          if (p.bias) {
+#pragma unroll
+            for (int j = 0; j < 8; ++j)
+              if (n + j < p.bias_len) v[j] += __bfloat162float(p.bias[b * p.bias_bs + n + j]);
+          }
+          store_bf16x8(static_cast<__nv_bfloat16*>(p.out) + b * p.out_bs + (long long)row * p.out_rs + n, v);
+        } else if constexpr (EPI == EPI_GELU_FWD) {
+          if (p.bias) {
+#pragma unroll
+            for (int j = 0; j < 8; ++j)
+              if (n + j < p.bias_len) v[j] += __bfloat162float(p.bias[b * p.bias_bs + n + j]);
+          }
+          if (p.out2)
+            store_bf16x8(static_cast<__nv_bfloat16*>(p.out2) + b * p.out2_bs + (long long)row * p.out2_rs + n, v);
+          float h[8];
+#pragma unroll
+          for (int j = 0; j < 8; ++j) h[j] = gelu_tanh_f(v[j]);
+          store_bf16x8(static_cast<__nv_bfloat16*>(p.out) + b * p.out_bs + (long long)row * p.out_rs + n, h);
+        } else if constexpr (EPI == EPI_GELU_BWD) {
+          float z[8];
+          load_bf16x8(static_cast<const __nv_bfloat16*>(p.aux) + b * p.aux_bs + (long long)row * p.aux_rs + n, z);
+#pragma unroll
+          for (int j = 0; j < 8; ++j) v[j] *= gelu_tanh_grad_f(z[j]);
+          store_bf16x8(static_cast<__nv_bfloat16*>(p.out) + b * p.out_bs + (long long)row * p.out_rs + n, v);
+        } else if constexpr (EPI == EPI_SWIGLU_BWD) {
+          // hidden unit n lives in 128-block n>>7 of the interleaved [a|g] rows
+          const long long col = (long long)(n >> 7) * 256 + (n & 127);
+          const __nv_bfloat16* ag =
+              static_cast<const __nv_bfloat16*>(p.aux) + b * p.aux_bs + (long long)row * p.aux_rs + col;
+          float a[8], g[8], da[8], dg[8];
+          load_bf16x8(ag, a);
+          load_bf16x8(ag + 128, g);
+#pragma unroll
+          for (int j = 0; j < 8; ++j) {
+            const float sg = sigmoid_f(a[j]);
+            dg[j] = v[j] * a[j] * sg;                          // dh * silu(a)
+            da[j] = v[j] * g[j] * sg * (1.0f + a[j] * (1.0f - sg));  // dh * g * silu'(a)
+          }
+          __nv_bfloat16* o = static_cast<__nv_bfloat16*>(p.out) + b * p.out_bs + (long long)row * p.out_rs + col;
+          store_bf16x8(o, da);
+          store_bf16x8(o + 128, dg);
+        }
+      }
+    }
+  }
+}
+
+// ------------------------------------------------------------ the kernel
+template <int BN, int STAGES>
+struct Layout {
+  static constexpr int A_BYTES = BM * BK * 2;
+  static constexpr int B_BYTES = BN * BK * 2;
+  static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+  static constexpr int BAR_OFF = STAGES * STAGE_BYTES;
+  static constexpr int SMEM = BAR_OFF + 256 + 1024;
+  static constexpr uint32_t TMEM_COLS = 2 * BN;
+  static_assert((2 * STAGES + 5) * 8 <= 232, "barrier area");
+  static_assert(TMEM_COLS >= 32 && TMEM_COLS <= 512 && (TMEM_COLS & (TMEM_COLS - 1)) == 0, "TMEM columns");
+};
+
+template <int BN, int STAGES, int EPI, bool AMN, bool BMN>
+__global__ void __launch_bounds__(THREADS, 1)
+    tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                   const Params p) {
+  using L = Layout<BN, STAGES>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + L::BAR_OFF);
+  uint64_t* empty = full + STAGES;
+  uint64_t* tfull = empty + STAGES;
+  uint64_t* tempty = tfull + 2;
+  uint64_t* drain = tempty + 2;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::BAR_OFF + 240);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::BAR_OFF + 244);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&tfull[i], 1);
+      mbar_init(&tempty[i], 4);  // one arrive per epilogue warp
+    }
+    mbar_init(drain, 1);
+    *abort_flag = 0;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+  }
+  if (warp == 0 && lane == 0) {
+    prefetch_tmap(&tmA);
+    prefetch_tmap(&tmB);
+  }
+  if (warp == 1) tmem_alloc(tmem_slot, L::TMEM_COLS);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+
+  const int num_tiles = p.tiles_m * p.tiles_n * p.NB;
+  const int k_iters = p.G * p.k_blocks;
+
+  if (warp == 0) {
+    // ------------------------------------------------ TMA producer
+    if (lane == 0) {
+      int stage = 0;
+      uint32_t phase = 0;
+      int last_issue_phase[STAGES];
+#pragma unroll
+      for (int s = 0; s < STAGES; ++s) last_issue_phase[s] = -1;
+      bool ok = true;
+      for (int tile = blockIdx.x; tile < num_tiles && ok; tile += gridDim.x) {
+        int b, mb, nb;
+        decode_tile(p, tile, b, mb, nb);
+        const int m0 = mb * BM, n0 = nb * BN;
+        for (int it = 0; it < k_iters; ++it) {
+          const int g = it / p.k_blocks;
+          const int k0 = (it - g * p.k_blocks) * BK;
+          if (!wait_bounded(&empty[stage], phase ^ 1u, abort_flag, p)) {
+            ok = false;
+            break;
+          }
+          const bool skip = p.debug_skip && tile == (int)blockIdx.x && it == 0;
+          if (!skip) {
+            uint8_t* sA = smem + stage * L::STAGE_BYTES;
+            uint8_t* sB = sA + L::A_BYTES;
+            mbar_arrive_expect_tx(&full[stage], L::STAGE_BYTES);
+            const int ab = b * p.a_bsel + g * p.a_gsel;
+            const int bb = b * p.b_bsel + g * p.b_gsel;
+            if (!AMN) {
+              tma_load_3d(sA, &tmA, &full[stage], k0, p.a_swap ? ab : m0, p.a_swap ? m0 : ab);
+            } else {
+#pragma unroll
+              for (int i = 0; i < BM / 64; ++i)
+                tma_load_3d(sA + i * 8192, &tmA, &full[stage], m0 + 64 * i, p.a_swap ? ab : k0,
+                            p.a_swap ? k0 : ab);
+            }
+            if (!BMN) {
+              tma_load_3d(sB, &tmB, &full[stage], k0, p.b_swap ? bb : n0, p.b_swap ? n0 : bb);
+            } else {
+#pragma unroll
+              for (int i = 0; i < BN / 64; ++i)
+                tma_load_3d(sB + i * 8192, &tmB, &full[stage], n0 + 64 * i, p.b_swap ? bb : k0,
+                            p.b_swap ? k0 : bb);
+            }
+            last_issue_phase[stage] = static_cast<int>(phase);
+          }
+          if (++stage == STAGES) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+      }
+      // Drain: every issued copy must have landed before the CTA may exit.
+#pragma unroll 1
+      for (int s = 0; s < STAGES; ++s)
+        if (last_issue_phase[s] >= 0)
+          wait_bounded(&full[s], static_cast<uint32_t>(last_issue_phase[s]), abort_flag, p, false);
+    }
+    __syncwarp();
+  } else if (warp == 1) {
+    // ------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      constexpr uint32_t IDESC = instr_desc<BN, AMN, BMN>();
+      int stage = 0;
+      uint32_t phase = 0;
+      int local = 0;
+      bool ok = true;
+      for (int tile = blockIdx.x; tile < num_tiles && ok; tile += gridDim.x, ++local) {
+        const int buf = local & 1;
+        const uint32_t use = static_cast<uint32_t>(local >> 1);
+        if (!wait_bounded(&tempty[buf], (use & 1u) ^ 1u, abort_flag, p)) break;
+        tc_fence_after();
+        const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(buf * BN);
+        for (int it = 0; it < k_iters; ++it) {
+          if (!wait_bounded(&full[stage], phase, abort_flag, p)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t a_addr = smem_u32(smem + stage * L::STAGE_BYTES);
+          const uint32_t b_addr = a_addr + L::A_BYTES;
+#pragma unroll
+          for (int k = 0; k < BK / 16; ++k)
+            umma_bf16(d_tmem, smem_desc<AMN>(a_addr, k), smem_desc<BMN>(b_addr, k), IDESC,
+                      (it > 0 || k > 0) ? 1u : 0u);
+          umma_commit(&empty[stage]);  // frees the stage once these MMAs have read it
+          if (++stage == STAGES) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+        if (!ok) break;
+        umma_commit(&tfull[buf]);  // accumulator ready for the epilogue
+      }
+      // Drain: all issued MMAs complete before tensor memory is released.
+      umma_commit(drain);
+      wait_bounded(drain, 0u, abort_flag, p, false);
+    }
+    __syncwarp();
+  } else {
+    // ------------------------------------------------ epilogue warps 2..5
+    const int quarter = warp & 3;  // TMEM lanes this warp may access
+    int local = 0;
+    for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x, ++local) {
+      const int buf = local & 1;
+      const uint32_t use = static_cast<uint32_t>(local >> 1);
+      if (!wait_bounded(&tfull[buf], use & 1u, abort_flag, p)) break;
+      tc_fence_after();
+      int b, mb, nb;
+      decode_tile(p, tile, b, mb, nb);
+      const int row = mb * BM + quarter * 32 + lane;
+      const uint32_t taddr = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) +
+                             static_cast<uint32_t>(buf * BN);
+      epilogue_tile<BN, EPI>(p, b, row, row < p.M, nb * BN, nb, taddr);
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&tempty[buf]);
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem_base, L::TMEM_COLS);
+  }
+}
+
+// ------------------------------------------------------------ host side
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+static EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* ptr = nullptr;
+    cudaDriverEntryPointQueryResult q = cudaDriverEntryPointSymbolNotFound;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(ptr);
+  });
+  return fn;
+}
+
+// 3-D bf16 tensor map of an operand.  Dimension order keeps strides
+// increasing: {inner, rows, batch}, or {inner, batch, rows} ("swap") when the
+// batch stride is the smaller one (e.g. heads inside a token row).
+static int make_map(CUtensorMap* m, const Operand& op, int rows_box, int* swap) {
+  const uint64_t es = 2;
+  if (reinterpret_cast<uintptr_t>(op.ptr) % 16) return TP_ERR_ALIGN;
+  if (op.inner < 1 || op.rows < 1 || op.batch < 1) return TP_ERR_INVALID;
+  const int64_t bst = op.batch > 1 ? op.batch_stride : op.row_stride * op.rows;
+  if ((op.row_stride * es) % 16 || (bst * es) % 16) return TP_ERR_ALIGN;
+  const uint32_t rb = op.mn_major ? 64u : static_cast<uint32_t>(rows_box);
+  cuuint64_t dims[3], strides[2];
+  cuuint32_t box[3], estr[3] = {1, 1, 1};
+  *swap = (op.batch > 1 && op.batch_stride < op.row_stride) ? 1 : 0;
+  dims[0] = static_cast<cuuint64_t>(op.inner);
+  box[0] = 64;
+  if (!*swap) {
+    dims[1] = op.rows;
+    dims[2] = op.batch;
+    strides[0] = op.row_stride * es;
+    strides[1] = bst * es;
+    box[1] = rb;
+    box[2] = 1;
+  } else {
+    dims[1] = op.batch;
+    dims[2] = op.rows;
+    strides[0] = op.batch_stride * es;
+    strides[1] = op.row_stride * es;
+    box[1] = 1;
+    box[2] = rb;
+  }
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return TP_ERR_CUDA;
+  CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(op.ptr), dims, strides, box, estr,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? 0 : TP_ERR_CUDA;
+}
+
+template <int BN, int STAGES, int EPI, bool AMN, bool BMN>
+static int launch_inst(const GemmSpec& s, LaunchCtx& ctx) {
+  using L = Layout<BN, STAGES>;
+  CUtensorMap ta, tb;
+  int sa = 0, sb = 0;
+  int rc = make_map(&ta, s.A, BM, &sa);
+  if (rc) return rc;
+  rc = make_map(&tb, s.B, BN, &sb);
+  if (rc) return rc;
+  Params p{};
+  p.M = static_cast<int>(s.M);
+  p.N = static_cast<int>(s.N);
+  p.K = static_cast<int>(s.K);
+  p.NB = s.NB;
+  p.G = s.G;
+  p.tiles_m = static_cast<int>((s.M + BM - 1) / BM);
+  p.tiles_n = static_cast<int>((s.N + BN - 1) / BN);
+  p.k_blocks = static_cast<int>((s.K + BK - 1) / BK);
+  p.a_bsel = s.A.bsel;
+  p.a_gsel = s.A.gsel;
+  p.b_bsel = s.B.bsel;
+  p.b_gsel = s.B.gsel;
+  p.a_swap = sa;
+  p.b_swap = sb;
+  p.out = s.out;
+  p.out_bs = s.out_bs;
+  p.out_rs = s.out_rs;
+  p.out2 = s.out2;
+  p.out2_bs = s.out2_bs;
+  p.out2_rs = s.out2_rs;
+  p.aux = s.aux;
+  p.aux_bs = s.aux_bs;
+  p.aux_rs = s.aux_rs;
+  p.bias = static_cast<const __nv_bfloat16*>(s.bias);
+  p.bias_bs = s.bias_bs;
+  p.bias_len = s.bias_len;
+  p.n_store = s.n_store;
+  p.err = ctx.err;
+  p.timeout_ns = ctx.timeout_ns;
+  p.debug_skip = ctx.debug_skip_load;
+  ctx.debug_skip_load = 0;
+
+  auto kern = tc_gemm_kernel<BN, STAGES, EPI, AMN, BMN>;
+  static std::atomic<uint32_t> attr_done{0};  // one bit per device
+  int dev = 0;
+  cudaGetDevice(&dev);
+  const uint32_t bit = 1u << (dev & 31);
+  if (!(attr_done.load() & bit)) {
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::SMEM) != cudaSuccess)
+      return TP_ERR_CUDA;
+    attr_done.fetch_or(bit);
+  }
+  const long long tiles = static_cast<long long>(p.tiles_m) * p.tiles_n * p.NB;
+  if (tiles <= 0 || p.k_blocks <= 0) return TP_ERR_INVALID;
+  const int grid = static_cast<int>(tiles < ctx.num_sms ? tiles : ctx.num_sms);
+  if (ctx.before) ctx.before(ctx.user, s.name);
+  kern<<<grid, THREADS, L::SMEM, ctx.stream>>>(ta, tb, p);
+  if (ctx.after) ctx.after(ctx.user);
+  ctx.launches++;
+  return cudaPeekAtLastError() == cudaSuccess ? 0 : TP_ERR_CUDA;
+}
+
+}  // namespace tc
+
+int launch_tc_gemm(const GemmSpec& s, LaunchCtx& ctx) {
+  using namespace tc;
+  const bool amn = s.A.mn_major != 0, bmn = s.B.mn_major != 0;
+  if (s.n_store % 8) return TP_ERR_UNSUPPORTED;
+  switch (s.epi) {
+    case EPI_SWIGLU_FWD:
+      if (!amn && !bmn) return launch_inst<256, 4, EPI_SWIGLU_FWD, false, false>(s, ctx);
+      break;
+    case EPI_GELU_FWD:
+      if (!amn && !bmn) return launch_inst<256, 4, EPI_GELU_FWD, false, false>(s, ctx);
+      break;
+    case EPI_F32:
+      if (!amn && !bmn) return launch_inst<256, 4, EPI_F32, false, false>(s, ctx);
+      if (!amn && bmn) return launch_inst<256, 4, EPI_F32, false, true>(s, ctx);
+      break;
+    case EPI_OUT:
+      if (!amn && !bmn) return launch_inst<256, 4, EPI_OUT, false, false>(s, ctx);
+      if (!amn && bmn) return launch_inst<256, 4, EPI_OUT, false, true>(s, ctx);
+      if (amn && bmn) return launch_inst<256, 4, EPI_OUT, true, true>(s, ctx);
+      break;
+    case EPI_GELU_BWD:
+      if (!amn && bmn) return launch_inst<256, 4, EPI_GELU_BWD, false, true>(s, ctx);
+      break;
+    case EPI_SWIGLU_BWD:
+      if (!amn && bmn) return launch_inst<256, 4, EPI_SWIGLU_BWD, false, true>(s, ctx);
+      break;
+    default:
+      break;
+  }
+  return TP_ERR_UNSUPPORTED;
+}
+
+}  // namespace tpffn

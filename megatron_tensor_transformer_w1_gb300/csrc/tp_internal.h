@@ -1,0 +1,93 @@
+// tp_internal.h -- declarations shared by the library's translation units.
+//
+// One GEMM description (GemmSpec) drives both compute back ends: the tcgen05
+// tensor-core kernel (bf16 operands, fp32 accumulation in tensor memory) and
+// the SIMT kernel (fp32 plans).  A GEMM here is
+//
+//   C_b[M, N] = sum_{g < G} A_{b,g}[M, K] * B_{b,g}[N, K]^T      (b < NB)
+//
+// where every operand is a strided 3-D view (inner, rows, batch) of a device
+// buffer.  "K-major" operands keep K in the contiguous (inner) dimension and
+// M (or N) in rows; "MN-major" operands keep M (or N) contiguous and K in
+// rows.  The batch coordinate of operand X for (b, g) is b*X.bsel + g*X.gsel,
+// which expresses the three uses of the shard index: per-shard GEMMs (bsel=1),
+// a shared operand (0,0) and the shard loop of the fused shard-sum (gsel=1).
+#pragma once
+#include <cstddef>
+#include <cstdint>
+
+#include <cuda_runtime.h>
+
+namespace tpffn {
+
+enum EpiKind : int {
+  EPI_F32 = 0,         // out fp32 = acc                          (partials)
+  EPI_OUT = 1,         // out (plan dtype) = acc + bias[n]        (y, dx, dW)
+  EPI_GELU_FWD = 2,    // z = acc + b1; out2 = z (saved); out = gelu_tanh(z)
+  EPI_SWIGLU_FWD = 3,  // acc = [a | g] per 256-col tile; out = silu(a)*g; out2 = a, g
+  EPI_GELU_BWD = 4,    // out = acc * gelu_tanh'(aux)             (dz)
+  EPI_SWIGLU_BWD = 5,  // acc = dh; aux = saved [a|g]; out = [da | dg]
+};
+
+struct Operand {
+  const void* ptr = nullptr;
+  int64_t inner = 0, rows = 0, batch = 1;   // extents (elements)
+  int64_t row_stride = 0, batch_stride = 0; // element strides
+  int mn_major = 0;
+  int bsel = 0, gsel = 0;
+};
+
+struct GemmSpec {
+  const char* name = "gemm";
+  int64_t M = 0, N = 0, K = 0;
+  int NB = 1, G = 1;
+  Operand A, B;
+  int epi = EPI_F32;
+  void* out = nullptr;  int64_t out_bs = 0, out_rs = 0;
+  void* out2 = nullptr; int64_t out2_bs = 0, out2_rs = 0;
+  const void* aux = nullptr; int64_t aux_bs = 0, aux_rs = 0;
+  const void* bias = nullptr; int64_t bias_bs = 0, bias_len = 0;
+  int64_t n_store = 0;   // columns n < n_store of the output are written
+  int out_bf16 = 1;      // plan dtype of out/out2 (EPI_F32 always fp32)
+};
+
+// Launch context of one API call.
+struct LaunchCtx {
+  cudaStream_t stream = nullptr;
+  int* err = nullptr;            // device error word (workspace header)
+  int num_sms = 148;
+  int debug_skip_load = 0;       // test hook (first tensor-core GEMM only)
+  uint64_t timeout_ns = 2000000000ull;
+  bool timing = false;
+  int launches = 0;
+  // timing records are appended by the caller through these hooks
+  void (*before)(void* user, const char* name) = nullptr;
+  void (*after)(void* user) = nullptr;
+  void* user = nullptr;
+};
+
+// Device error bits.
+constexpr int DEV_ERR_TIMEOUT = 1;
+
+// tensor-core GEMM (tp_gemm_tc.cu). Returns 0 or a TP_ERR_* code.
+int launch_tc_gemm(const GemmSpec& s, LaunchCtx& ctx);
+// SIMT fp32 GEMM (tp_kernels.cu).
+int launch_simt_gemm(const GemmSpec& s, LaunchCtx& ctx);
+
+// Streaming kernels (tp_kernels.cu).  esz = element size of the plan dtype.
+int launch_pack_columns(const void* W1, const void* W3, void* out, int T_p, int64_t s,
+                        int64_t s_pad, int64_t d, int swiglu, int esz, int unpack,
+                        cudaStream_t st);
+int launch_pack_rows(const void* W2, void* out, int T_p, int64_t s, int64_t s_pad, int64_t d,
+                     int esz, int unpack, cudaStream_t st);
+int launch_shard_sum(const float* partials, int T_p, int64_t rows, int64_t cols,
+                     const void* bias, void* out, int out_bf16, LaunchCtx& ctx,
+                     const char* name);
+// Column sums of a [batch][rows][cols] view (row stride rs, batch stride bs)
+// into out[b*out_bs + col] for col < cols, deterministic two-pass order.
+int launch_colsum(const void* in, int in_bf16, int64_t batch, int64_t rows, int64_t cols,
+                  int64_t rs, int64_t bs, void* out, int out_bf16, int64_t out_bs,
+                  float* scratch, int64_t chunk_rows, LaunchCtx& ctx, const char* name);
+int64_t colsum_scratch_floats(int64_t batch, int64_t rows, int64_t cols, int64_t chunk_rows);
+
+}  // namespace tpffn

@@ -1,0 +1,403 @@
+// tp_kernels.cu -- the memory-bound kernels of the path and the fp32 GEMM.
+//
+//   pack / unpack  : shard_columns / shard_rows of "S17 Tensor & Pipeline
+//                    Parallelism" (listing "the megatron pattern"), for all
+//                    shards in one launch, into the layouts of tpffn.h
+//   shard_sum      : the g-operator (forward) and f-operator (backward dx)
+//                    all-reduce of "7.9 Tensor and pipeline parallelism
+//                    (TP, PP)", §2.1, as an on-device sum of the fp32 shard
+//                    partials in the fixed order t = 0..T_p-1 (+ bias once)
+//   colsum         : bias gradients (sum over tokens), two fixed-order passes
+//   simt_gemm      : fp32 GEMM with the same epilogues as the tensor-core
+//                    kernel, for fp32 plans (TF32 would not meet fp32
+//                    accuracy, so these use plain FMA)
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include "tp_internal.h"
+#include "tpffn.h"
+
+namespace tpffn {
+
+namespace {
+
+__device__ __forceinline__ float to_f(const void* p, long long i, int bf16) {
+  return bf16 ? __bfloat162float(static_cast<const __nv_bfloat16*>(p)[i]) : static_cast<const float*>(p)[i];
+}
+__device__ __forceinline__ void from_f(void* p, long long i, float v, int bf16) {
+  if (bf16)
+    static_cast<__nv_bfloat16*>(p)[i] = __float2bfloat16_rn(v);
+  else
+    static_cast<float*>(p)[i] = v;
+}
+
+// ------------------------------------------------------------------ packing
+// Copy `n` elements of `esz` bytes; 16-byte vectors when both ends allow.
+__device__ __forceinline__ void copy_row(char* dst, const char* src, long long n, int esz) {
+  const long long bytes = n * esz;
+  if ((reinterpret_cast<uintptr_t>(dst) % 16) == 0 && (reinterpret_cast<uintptr_t>(src) % 16) == 0 &&
+      bytes % 16 == 0) {
+    for (long long i = threadIdx.x; i < bytes / 16; i += blockDim.x)
+      reinterpret_cast<uint4*>(dst)[i] = reinterpret_cast<const uint4*>(src)[i];
+  } else if (esz == 2) {
+    for (long long i = threadIdx.x; i < n; i += blockDim.x)
+      reinterpret_cast<uint16_t*>(dst)[i] = reinterpret_cast<const uint16_t*>(src)[i];
+  } else {
+    for (long long i = threadIdx.x; i < n; i += blockDim.x)
+      reinterpret_cast<uint32_t*>(dst)[i] = reinterpret_cast<const uint32_t*>(src)[i];
+  }
+}
+__device__ __forceinline__ void zero_row(char* dst, long long n, int esz) {
+  const long long bytes = n * esz;
+  if ((reinterpret_cast<uintptr_t>(dst) % 16) == 0 && bytes % 16 == 0) {
+    for (long long i = threadIdx.x; i < bytes / 16; i += blockDim.x) reinterpret_cast<uint4*>(dst)[i] = uint4{0, 0, 0, 0};
+  } else {
+    for (long long i = threadIdx.x; i < bytes; i += blockDim.x) dst[i] = 0;
+  }
+}
+
+// One block per packed row (t, rr).  GELU: rr = hidden unit j.  SwiGLU: rows
+// come in 256-row blocks, 128 of W1 then 128 of W3 for the same hidden units.
+__global__ void pack_columns_kernel(const char* W1, const char* W3, char* out, long long s, long long s_pad,
+                                    long long d, int swiglu, int esz, int unpack) {
+  const long long rows_per_shard = swiglu ? 2 * s_pad : s_pad;
+  const long long t = blockIdx.x / rows_per_shard;
+  const long long rr = blockIdx.x - t * rows_per_shard;
+  long long j = rr;
+  int half = 0;
+  if (swiglu) {
+    half = static_cast<int>((rr >> 7) & 1);
+    j = (rr >> 8) * 128 + (rr & 127);
+  }
+  char* prow = out + (t * rows_per_shard + rr) * d * esz;
+  const bool valid = j < s;
+  const char* base = half ? W3 : W1;
+  if (!unpack) {
+    if (valid)
+      copy_row(prow, base + (t * s + j) * d * esz, d, esz);
+    else
+      zero_row(prow, d, esz);
+  } else if (valid) {
+    copy_row(const_cast<char*>(base) + (t * s + j) * d * esz, prow, d, esz);
+  }
+}
+
+// One block per packed row (t, c): out[t][c][0:s] = W2[c][t*s : (t+1)*s].
+__global__ void pack_rows_kernel(const char* W2, char* out, long long s, long long s_pad, long long d,
+                                 int T_p, int esz, int unpack) {
+  const long long t = blockIdx.x / d;
+  const long long c = blockIdx.x - t * d;
+  const long long d_ff = s * T_p;
+  char* prow = out + (t * d + c) * s_pad * esz;
+  const char* src = W2 + (c * d_ff + t * s) * esz;
+  if (!unpack) {
+    copy_row(prow, src, s, esz);
+    if (s_pad > s) zero_row(prow + s * esz, s_pad - s, esz);
+  } else {
+    copy_row(const_cast<char*>(src), prow, s, esz);
+  }
+}
+
+// ---------------------------------------------------------------- shard-sum
+// y[i] = ((P_0[i] + P_1[i]) + ...) + P_{T-1}[i], then + bias[i % cols].
+// 8 consecutive elements per thread, 16-byte streaming loads.
+template <int OUT_BF16>
+__global__ void __launch_bounds__(256) shard_sum_vec8_kernel(const float* __restrict__ P, int T, long long plane,
+                                                             long long cols, const __nv_bfloat16* bias_bf,
+                                                             const float* bias_f, void* out) {
+  const long long n8 = plane / 8;
+  for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < n8; i += (long long)gridDim.x * blockDim.x) {
+    const float4* p0 = reinterpret_cast<const float4*>(P) + 2 * i;
+    float4 a = __ldcs(p0), b = __ldcs(p0 + 1);
+    for (int t = 1; t < T; ++t) {
+      const float4* pt = reinterpret_cast<const float4*>(P + t * plane) + 2 * i;
+      const float4 c = __ldcs(pt), e = __ldcs(pt + 1);
+      a.x += c.x; a.y += c.y; a.z += c.z; a.w += c.w;
+      b.x += e.x; b.y += e.y; b.z += e.z; b.w += e.w;
+    }
+    float v[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+    const long long col = (i * 8) % cols;
+    if (bias_bf) {
+#pragma unroll
+      for (int j = 0; j < 8; ++j) v[j] += __bfloat162float(bias_bf[col + j]);
+    } else if (bias_f) {
+#pragma unroll
+      for (int j = 0; j < 8; ++j) v[j] += bias_f[col + j];
+    }
+    if (OUT_BF16) {
+      uint4 q;
+      __nv_bfloat162 h0 = __floats2bfloat162_rn(v[0], v[1]), h1 = __floats2bfloat162_rn(v[2], v[3]);
+      __nv_bfloat162 h2 = __floats2bfloat162_rn(v[4], v[5]), h3 = __floats2bfloat162_rn(v[6], v[7]);
+      q.x = *reinterpret_cast<uint32_t*>(&h0);
+      q.y = *reinterpret_cast<uint32_t*>(&h1);
+      q.z = *reinterpret_cast<uint32_t*>(&h2);
+      q.w = *reinterpret_cast<uint32_t*>(&h3);
+      reinterpret_cast<uint4*>(out)[i] = q;
+    } else {
+      float4* o = reinterpret_cast<float4*>(out) + 2 * i;
+      o[0] = make_float4(v[0], v[1], v[2], v[3]);
+      o[1] = make_float4(v[4], v[5], v[6], v[7]);
+    }
+  }
+}
+
+__global__ void shard_sum_scalar_kernel(const float* P, int T, long long plane, long long cols, const void* bias,
+                                        int bias_bf16, void* out, int out_bf16) {
+  for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < plane; i += (long long)gridDim.x * blockDim.x) {
+    float acc = P[i];
+    for (int t = 1; t < T; ++t) acc += P[t * plane + i];
+    if (bias) acc += to_f(bias, i % cols, bias_bf16);
+    from_f(out, i, acc, out_bf16);
+  }
+}
+
+// ------------------------------------------------------------------ colsum
+__global__ void colsum_pass1_kernel(const void* in, int in_bf16, long long rows, long long cols, long long rs,
+                                    long long bs, float* scratch, long long chunk_rows, long long chunks) {
+  const long long col = blockIdx.x * (long long)blockDim.x + threadIdx.x;
+  const long long chunk = blockIdx.y;
+  const long long b = blockIdx.z;
+  if (col >= cols) return;
+  const long long r0 = chunk * chunk_rows;
+  const long long r1 = min(rows, r0 + chunk_rows);
+  float acc = 0.f;
+  for (long long r = r0; r < r1; ++r) acc += to_f(in, b * bs + r * rs + col, in_bf16);
+  scratch[(b * chunks + chunk) * cols + col] = acc;
+}
+__global__ void colsum_pass2_kernel(const float* scratch, long long cols, long long chunks, void* out, int out_bf16,
+                                    long long out_bs) {
+  const long long col = blockIdx.x * (long long)blockDim.x + threadIdx.x;
+  const long long b = blockIdx.y;
+  if (col >= cols) return;
+  float acc = 0.f;
+  for (long long c = 0; c < chunks; ++c) acc += scratch[(b * chunks + c) * cols + col];
+  from_f(out, b * out_bs + col, acc, out_bf16);
+}
+
+// ---------------------------------------------------------------- SIMT GEMM
+struct SimtOp {
+  const float* p;
+  long long inner, rows, rs, bs;
+  int mn, bsel, gsel;
+};
+struct SimtParams {
+  SimtOp A, B;
+  long long M, N, K;
+  int NB, G, epi;
+  float* out;
+  long long out_bs, out_rs;
+  float* out2;
+  long long out2_bs, out2_rs;
+  const float* aux;
+  long long aux_bs, aux_rs;
+  const float* bias;
+  long long bias_bs, bias_len, n_store;
+};
+
+// Element (mn, k) of operand X for batch coordinate bc; zero outside the
+// operand's extents (the same rule as the tensor-core path's zero fill).
+__device__ __forceinline__ float op_at(const SimtOp& X, long long bc, long long mn, long long k) {
+  if (!X.mn) {
+    if (mn >= X.rows || k >= X.inner) return 0.f;
+    return X.p[bc * X.bs + mn * X.rs + k];
+  }
+  if (mn >= X.inner || k >= X.rows) return 0.f;
+  return X.p[bc * X.bs + k * X.rs + mn];
+}
+
+__device__ __forceinline__ float dot_gk(const SimtParams& p, long long b, long long m, long long n) {
+  float acc = 0.f;
+  for (int g = 0; g < p.G; ++g) {
+    const long long ab = b * p.A.bsel + g * p.A.gsel, bb = b * p.B.bsel + g * p.B.gsel;
+    for (long long k = 0; k < p.K; ++k) acc = fmaf(op_at(p.A, ab, m, k), op_at(p.B, bb, n, k), acc);
+  }
+  return acc;
+}
+
+__device__ __forceinline__ float gelu_tanh_f(float z) {
+  const float k = 0.7978845608028654f;
+  return 0.5f * z * (1.0f + tanhf(k * (z + 0.044715f * z * z * z)));
+}
+__device__ __forceinline__ float gelu_tanh_grad_f(float z) {
+  const float k = 0.7978845608028654f;
+  const float t = tanhf(k * (z + 0.044715f * z * z * z));
+  return 0.5f * (1.0f + t) + 0.5f * z * (1.0f - t * t) * k * (1.0f + 3.0f * 0.044715f * z * z);
+}
+__device__ __forceinline__ float sigmoid_f(float a) { return 1.0f / (1.0f + expf(-a)); }
+
+__global__ void simt_gemm_kernel(const SimtParams p) {
+  const long long ncols = (p.epi == EPI_SWIGLU_FWD) ? p.N / 2 : p.N;
+  const long long total = (long long)p.NB * p.M * ncols;
+  for (long long idx = blockIdx.x * (long long)blockDim.x + threadIdx.x; idx < total;
+       idx += (long long)gridDim.x * blockDim.x) {
+    const long long n = idx % ncols;
+    const long long m = (idx / ncols) % p.M;
+    const long long b = idx / (ncols * p.M);
+    if (p.epi == EPI_SWIGLU_FWD) {
+      // hidden unit n: rows (n>>7)*256 + (n&127) (a) and +128 (g) of B
+      const long long ra = (n >> 7) * 256 + (n & 127);
+      const float a = dot_gk(p, b, m, ra), g = dot_gk(p, b, m, ra + 128);
+      p.out[b * p.out_bs + m * p.out_rs + n] = a * sigmoid_f(a) * g;
+      if (p.out2) {
+        p.out2[b * p.out2_bs + m * p.out2_rs + ra] = a;
+        p.out2[b * p.out2_bs + m * p.out2_rs + ra + 128] = g;
+      }
+      continue;
+    }
+    if (n >= p.n_store) continue;
+    float v = dot_gk(p, b, m, n);
+    switch (p.epi) {
+      case EPI_F32:
+        p.out[b * p.out_bs + m * p.out_rs + n] = v;
+        break;
+      case EPI_OUT:
+        if (p.bias && n < p.bias_len) v += p.bias[b * p.bias_bs + n];
+        p.out[b * p.out_bs + m * p.out_rs + n] = v;
+        break;
+      case EPI_GELU_FWD:
+        if (p.bias && n < p.bias_len) v += p.bias[b * p.bias_bs + n];
+        if (p.out2) p.out2[b * p.out2_bs + m * p.out2_rs + n] = v;
+        p.out[b * p.out_bs + m * p.out_rs + n] = gelu_tanh_f(v);
+        break;
+      case EPI_GELU_BWD:
+        p.out[b * p.out_bs + m * p.out_rs + n] = v * gelu_tanh_grad_f(p.aux[b * p.aux_bs + m * p.aux_rs + n]);
+        break;
+      case EPI_SWIGLU_BWD: {
+        const long long col = (n >> 7) * 256 + (n & 127);
+        const float a = p.aux[b * p.aux_bs + m * p.aux_rs + col];
+        const float g = p.aux[b * p.aux_bs + m * p.aux_rs + col + 128];
+        const float sg = sigmoid_f(a);
+        p.out[b * p.out_bs + m * p.out_rs + col] = v * g * sg * (1.0f + a * (1.0f - sg));
+        p.out[b * p.out_bs + m * p.out_rs + col + 128] = v * a * sg;
+        break;
+      }
+      default:
+        break;
+    }
+  }
+}
+
+SimtOp to_simt(const Operand& o) {
+  SimtOp s;
+  s.p = static_cast<const float*>(o.ptr);
+  s.inner = o.inner;
+  s.rows = o.rows;
+  s.rs = o.row_stride;
+  s.bs = o.batch_stride;
+  s.mn = o.mn_major;
+  s.bsel = o.bsel;
+  s.gsel = o.gsel;
+  return s;
+}
+
+int grid_for(long long work, int per_block, int num_sms) {
+  long long g = (work + per_block - 1) / per_block;
+  const long long cap = (long long)num_sms * 16;
+  if (g > cap) g = cap;
+  if (g < 1) g = 1;
+  return static_cast<int>(g);
+}
+
+}  // namespace
+
+int launch_simt_gemm(const GemmSpec& s, LaunchCtx& ctx) {
+  SimtParams p{};
+  p.A = to_simt(s.A);
+  p.B = to_simt(s.B);
+  p.M = s.M;
+  p.N = s.N;
+  p.K = s.K;
+  p.NB = s.NB;
+  p.G = s.G;
+  p.epi = s.epi;
+  p.out = static_cast<float*>(s.out);
+  p.out_bs = s.out_bs;
+  p.out_rs = s.out_rs;
+  p.out2 = static_cast<float*>(s.out2);
+  p.out2_bs = s.out2_bs;
+  p.out2_rs = s.out2_rs;
+  p.aux = static_cast<const float*>(s.aux);
+  p.aux_bs = s.aux_bs;
+  p.aux_rs = s.aux_rs;
+  p.bias = static_cast<const float*>(s.bias);
+  p.bias_bs = s.bias_bs;
+  p.bias_len = s.bias_len;
+  p.n_store = s.n_store;
+  const long long cols = (s.epi == EPI_SWIGLU_FWD) ? s.N / 2 : s.N;
+  const long long total = (long long)s.NB * s.M * cols;
+  if (total <= 0) return 0;
+  if (ctx.before) ctx.before(ctx.user, s.name);
+  simt_gemm_kernel<<<grid_for(total, 256, ctx.num_sms), 256, 0, ctx.stream>>>(p);
+  if (ctx.after) ctx.after(ctx.user);
+  ctx.launches++;
+  return cudaPeekAtLastError() == cudaSuccess ? 0 : TP_ERR_CUDA;
+}
+
+int launch_pack_columns(const void* W1, const void* W3, void* out, int T_p, int64_t s, int64_t s_pad, int64_t d,
+                        int swiglu, int esz, int unpack, cudaStream_t st) {
+  const long long blocks = (long long)T_p * (swiglu ? 2 * s_pad : s_pad);
+  if (blocks <= 0) return 0;
+  pack_columns_kernel<<<static_cast<unsigned>(blocks), 128, 0, st>>>(
+      static_cast<const char*>(W1), static_cast<const char*>(W3), static_cast<char*>(out), s, s_pad, d, swiglu, esz,
+      unpack);
+  return cudaPeekAtLastError() == cudaSuccess ? 0 : TP_ERR_CUDA;
+}
+
+int launch_pack_rows(const void* W2, void* out, int T_p, int64_t s, int64_t s_pad, int64_t d, int esz, int unpack,
+                     cudaStream_t st) {
+  const long long blocks = (long long)T_p * d;
+  if (blocks <= 0) return 0;
+  pack_rows_kernel<<<static_cast<unsigned>(blocks), 128, 0, st>>>(static_cast<const char*>(W2),
+                                                                  static_cast<char*>(out), s, s_pad, d, T_p, esz,
+                                                                  unpack);
+  return cudaPeekAtLastError() == cudaSuccess ? 0 : TP_ERR_CUDA;
+}
+
+int launch_shard_sum(const float* partials, int T_p, int64_t rows, int64_t cols, const void* bias, void* out,
+                     int out_bf16, LaunchCtx& ctx, const char* name) {
+  const long long plane = (long long)rows * cols;
+  if (plane <= 0) return 0;
+  if (ctx.before) ctx.before(ctx.user, name);
+  const bool vec = (cols % 8 == 0) && (reinterpret_cast<uintptr_t>(partials) % 16 == 0) &&
+                   (reinterpret_cast<uintptr_t>(out) % 16 == 0);
+  if (vec) {
+    const int grid = grid_for(plane / 8, 256, ctx.num_sms);
+    if (out_bf16)
+      shard_sum_vec8_kernel<1><<<grid, 256, 0, ctx.stream>>>(partials, T_p, plane, cols,
+                                                            static_cast<const __nv_bfloat16*>(bias), nullptr, out);
+    else
+      shard_sum_vec8_kernel<0><<<grid, 256, 0, ctx.stream>>>(partials, T_p, plane, cols, nullptr,
+                                                            static_cast<const float*>(bias), out);
+  } else {
+    shard_sum_scalar_kernel<<<grid_for(plane, 256, ctx.num_sms), 256, 0, ctx.stream>>>(partials, T_p, plane, cols,
+                                                                                     bias, out_bf16, out, out_bf16);
+  }
+  if (ctx.after) ctx.after(ctx.user);
+  ctx.launches++;
+  return cudaPeekAtLastError() == cudaSuccess ? 0 : TP_ERR_CUDA;
+}
+
+int64_t colsum_scratch_floats(int64_t batch, int64_t rows, int64_t cols, int64_t chunk_rows) {
+  const int64_t chunks = (rows + chunk_rows - 1) / chunk_rows;
+  return batch * (chunks > 0 ? chunks : 1) * cols;
+}
+
+int launch_colsum(const void* in, int in_bf16, int64_t batch, int64_t rows, int64_t cols, int64_t rs, int64_t bs,
+                  void* out, int out_bf16, int64_t out_bs, float* scratch, int64_t chunk_rows, LaunchCtx& ctx,
+                  const char* name) {
+  if (batch <= 0 || cols <= 0) return 0;
+  const int64_t chunks = rows > 0 ? (rows + chunk_rows - 1) / chunk_rows : 0;
+  if (ctx.before) ctx.before(ctx.user, name);
+  if (chunks > 0) {
+    dim3 g1(static_cast<unsigned>((cols + 255) / 256), static_cast<unsigned>(chunks), static_cast<unsigned>(batch));
+    colsum_pass1_kernel<<<g1, 256, 0, ctx.stream>>>(in, in_bf16, rows, cols, rs, bs, scratch, chunk_rows, chunks);
+    ctx.launches++;
+  }
+  dim3 g2(static_cast<unsigned>((cols + 255) / 256), static_cast<unsigned>(batch));
+  colsum_pass2_kernel<<<g2, 256, 0, ctx.stream>>>(scratch, cols, chunks, out, out_bf16, out_bs);
+  ctx.launches++;
+  if (ctx.after) ctx.after(ctx.user);
+  return cudaPeekAtLastError() == cudaSuccess ? 0 : TP_ERR_CUDA;
+}
+
+}  // namespace tpffn

@@ -1,0 +1,174 @@
+"""Parity of the CUDA path (through the C ABI) with the float64 oracle.
+
+Small and ragged shapes are compared element by element with the full
+oracle; the full-size workloads (GPT-2 small, Llama-3-8B, Megatron-8.3B FFN
+and W_O, Llama-3-70B decode) on seeded token rows and weight-gradient entries
+that the oracle computes one by one.  Tolerances: see tests/parity.py.
+"""
+import numpy as np
+import pytest
+import torch
+
+from synth import WORKLOADS, Workload, make_inputs, small_case
+from tests.parity import (BF16_REL, F32_REL, check, oracle_problem, partial_allowance, run_gpu)
+
+pytestmark = pytest.mark.gpu
+
+
+def _full_compare(w, fused):
+    inp = make_inputs(w)
+    got = run_gpu(w, inp, fused=fused, backward=not w.fwd_only)
+    rel = F32_REL if w.dtype == "f32" else BF16_REL
+    exact, f = oracle_problem(w, inp, round_bf16=False)
+    sh = exact.forward_sharded()
+    check(got["y"], sh["y"], rel, f"{w.name} y")
+    rb, _ = oracle_problem(w, inp, round_bf16=(w.dtype == "bf16"))
+    dump = rb.hidden_rows(f["dy"]) if w.act != "none" and w.dtype == "bf16" else None
+    rows = np.arange(w.N)
+    if got["partials"] is not None:
+        ref = rb.forward_sharded()["partials"]
+        extra = partial_allowance(w, f, dump, rows, "y") if dump is not None else None
+        check(got["partials"], ref, F32_REL, f"{w.name} partials", extra)
+    if w.fwd_only:
+        return
+    g = exact.backward_full(f["dy"])
+    check(got["dx"], g["dx"], rel, f"{w.name} dx")
+    check(got["dW2"], g["dW2"], rel, f"{w.name} dW2")
+    if w.act != "none":
+        check(got["dW1"], g["dW1"], rel, f"{w.name} dW1")
+    if w.act == "swiglu":
+        check(got["dW3"], g["dW3"], rel, f"{w.name} dW3")
+    if w.bias:
+        check(got["db2"], g["db2"], rel, f"{w.name} db2")
+        if w.act == "gelu_tanh":
+            check(got["db1"], g["db1"], rel, f"{w.name} db1")
+    if got["dx_partials"] is not None:
+        ref = rb.backward_rows(f["dy"])["dx_partials"]
+        extra = partial_allowance(w, f, dump, rows, "dx") if dump is not None else None
+        check(got["dx_partials"], ref, F32_REL, f"{w.name} dx partials", extra)
+
+
+@pytest.mark.parametrize("fused", [False, True], ids=["standalone", "fused"])
+def test_tiny_fp32_workload(fused):
+    _full_compare(WORKLOADS["tiny_gelu_fp32"], fused)
+
+
+SMALL = [
+    # ragged on every axis: 333 tokens (M tail), d = 264 (K tail), s = 200
+    small_case(333, 264, 600, 3, "gelu_tanh", bias=True, seed=101),
+    small_case(333, 264, 600, 3, "swiglu", seed=102),          # s = 200 -> padded to 256
+    small_case(200, 256, 768, 4, "swiglu", seed=103),          # two 128-blocks per shard
+    small_case(130, 128, 264, 11, "gelu_tanh", seed=104),      # TP11, s = 24
+    small_case(257, 192, 384, 1, "gelu_tanh", bias=True, seed=105),  # TP1 = dense
+    small_case(1, 64, 256, 2, "swiglu", seed=106),             # a single token
+    small_case(300, 136, 96, 2, "gelu_tanh", bias=True, seed=107),   # s = 48 < one tile
+]
+
+
+@pytest.mark.parametrize("fused", [False, True], ids=["standalone", "fused"])
+@pytest.mark.parametrize("w", SMALL, ids=[w.name for w in SMALL])
+def test_small_bf16_against_full_oracle(w, fused):
+    _full_compare(w, fused)
+
+
+def _attn_case(N, d_model, n_heads, head_dim, T_p, seed):
+    return Workload(f"attn_out_{N}x{d_model}_h{n_heads}x{head_dim}_tp{T_p}", N, d_model, n_heads * head_dim, T_p,
+                    "none", "bf16", seed_index=seed, n_heads=n_heads, n_kv_heads=n_heads, head_dim=head_dim)
+
+
+ATTN = [_attn_case(200, 256, 6, 64, 3, 201), _attn_case(77, 136, 8, 16, 4, 202)]
+
+
+@pytest.mark.parametrize("fused", [False, True], ids=["standalone", "fused"])
+@pytest.mark.parametrize("w", ATTN, ids=[w.name for w in ATTN])
+def test_attention_out_projection_against_full_oracle(w, fused):
+    _full_compare(w, fused)
+
+
+def test_empty_token_batch_is_a_no_op():
+    from megatron_tensor_transformer_w1_gb300 import tpffn as abi
+    rc, plan = abi.tp_ffn_plan_create(64, 256, 2, abi.TP_ACT_GELU_TANH, abi.TP_BF16)
+    assert rc == abi.TP_OK
+    try:
+        assert abi.tp_ffn_fwd(plan, 0, None, None, None, None, None, None, None, None, None, 0, 0) == abi.TP_OK
+        assert abi.tp_ffn_last_launch_count(plan) == 0
+        assert abi.tp_ffn_bwd(plan, 0, *([None] * 12), 0, 0) == abi.TP_OK
+    finally:
+        abi.tp_ffn_plan_destroy(plan)
+
+
+@pytest.mark.parametrize("act", ["gelu_tanh", "swiglu"])
+def test_pack_layout_and_roundtrip_bit_exact(act):
+    """Packing is byte work: compare bit for bit with the layout of tpffn.h."""
+    from megatron_tensor_transformer_w1_gb300.ffn import TensorParallelFFN
+    w = small_case(8, 72, 3 * 200, 3, act, seed=301)
+    inp = make_inputs(w)
+    dev = torch.device("cuda", 0)
+    ffn = TensorParallelFFN(w.d, w.d_ff, w.T_p, act, "bf16", device=dev)
+    W1, W2 = inp["W1"].to(dev), inp["W2"].to(dev)
+    W3 = inp["W3"].to(dev) if act == "swiglu" else None
+    w13p, w2p = ffn.pack(W1, W2, W3)
+    s, sp, d, T = ffn.info["s"], ffn.info["s_pad"], w.d, w.T_p
+    cols = w13p.view(torch.bfloat16).cpu().view(torch.int16)
+    rows = w2p.view(torch.bfloat16).cpu().view(torch.int16).reshape(T, d, sp)
+    W1i, W2i = inp["W1"].view(torch.int16), inp["W2"].view(torch.int16)
+    for t in range(T):
+        assert torch.equal(rows[t, :, :s], W2i[:, t * s:(t + 1) * s])
+        assert not rows[t, :, s:].any()
+    if act == "swiglu":
+        W3i = inp["W3"].view(torch.int16)
+        c = cols.reshape(T, sp // 128, 2, 128, d)
+        for t in range(T):
+            for j in range(sp):
+                blk, r = divmod(j, 128)
+                if j < s:
+                    assert torch.equal(c[t, blk, 0, r], W1i[t * s + j])
+                    assert torch.equal(c[t, blk, 1, r], W3i[t * s + j])
+                else:
+                    assert not c[t, blk, :, r].any()
+    else:
+        c = cols.reshape(T, sp, d)
+        for t in range(T):
+            assert torch.equal(c[t, :s], W1i[t * s:(t + 1) * s])
+    U1, U3 = ffn.unpack_columns(w13p)
+    assert torch.equal(U1.cpu().view(torch.int16), W1i)
+    if act == "swiglu":
+        assert torch.equal(U3.cpu().view(torch.int16), inp["W3"].view(torch.int16))
+    assert torch.equal(ffn.unpack_rows(w2p).cpu().view(torch.int16), W2i)
+
+
+@pytest.mark.parametrize("fused", [False, True], ids=["standalone", "fused"])
+def test_bitwise_reproducible_run_to_run(fused):
+    w = small_case(333, 264, 600, 3, "swiglu", seed=401)
+    inp = make_inputs(w)
+    a = run_gpu(w, inp, fused=fused)["_raw"]
+    b = run_gpu(w, inp, fused=fused)["_raw"]
+    for k, v in a.items():
+        if v is not None:
+            assert torch.equal(v.view(torch.uint8) if v.dtype != torch.float32 else v.view(torch.int32),
+                               b[k].view(torch.uint8) if v.dtype != torch.float32 else b[k].view(torch.int32)), k
+
+
+def test_bounded_wait_expires_and_context_survives():
+    """The test hook makes the first GEMM's producer skip a load; the waiting
+    MMA and epilogue warps give up after their time limit, the call reports
+    TP_ERR_TIMEOUT, and the next call on the same context is correct."""
+    from megatron_tensor_transformer_w1_gb300 import tpffn as abi
+    from megatron_tensor_transformer_w1_gb300.ffn import TensorParallelFFN
+    w = small_case(64, 128, 256, 2, "gelu_tanh", seed=501)
+    inp = make_inputs(w)
+    dev = torch.device("cuda", 0)
+    ffn = TensorParallelFFN(w.d, w.d_ff, w.T_p, "gelu_tanh", "bf16", device=dev)
+    g = {k: (None if v is None else v.to(dev)) for k, v in inp.items()}
+    w13p, w2p = ffn.pack(g["W1"], g["W2"])
+    y = torch.empty(w.N, w.d, dtype=torch.bfloat16, device=dev)
+    ws = ffn.workspace(w.N)
+    rc = abi.tp_ffn_fwd(ffn.plan, w.N, g["x"], w13p, w2p, None, None, y, None, None, ws, ws.numel(),
+                        abi.TP_FLAG_SYNC | abi.TP_FLAG_DEBUG_SKIP_LOAD, torch.cuda.current_stream())
+    assert rc == abi.TP_ERR_TIMEOUT
+    assert abi.tp_ffn_last_device_error(ffn.plan, ws, torch.cuda.current_stream()) == abi.TP_ERR_TIMEOUT
+    rc = abi.tp_ffn_fwd(ffn.plan, w.N, g["x"], w13p, w2p, None, None, y, None, None, ws, ws.numel(),
+                        abi.TP_FLAG_SYNC, torch.cuda.current_stream())
+    assert rc == abi.TP_OK
+    exact, _ = oracle_problem(w, inp)
+    check(y.double().cpu().numpy(), exact.forward_sharded()["y"], BF16_REL, "y after timeout")
