@@ -107,6 +107,19 @@ class ClockSampler:
                 "reasons": sorted(reasons)}
 
 
+def _smi_id(dev):
+    """nvidia-smi's id of a CUDA device: its UUID when PyTorch exposes it (the
+    CUDA ordinal differs from nvidia-smi's index under CUDA_VISIBLE_DEVICES)."""
+    import torch
+    try:
+        u = str(torch.cuda.get_device_properties(dev).uuid)
+        return u if u.startswith("GPU-") else "GPU-" + u
+    except Exception:
+        vis = os.environ.get("CUDA_VISIBLE_DEVICES", "")
+        ids = [v for v in vis.split(",") if v.strip()]
+        return ids[dev.index] if dev.index < len(ids) else str(dev.index)
+
+
 # ------------------------------------------------------------- distributed
 def dist_setup(n_gpus):
     world = int(os.environ.get("WORLD_SIZE", "1"))
@@ -213,7 +226,7 @@ def run_ours(args, ctx):
     dist_barrier(ctx)
     torch.cuda.synchronize(dev)
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    with ClockSampler(dev.index) as clk:
+    with ClockSampler(_smi_id(dev)) as clk:
         e0.record(st)
         for _ in range(args.steps):
             step(flags | abi.TP_FLAG_TIMING)
