@@ -191,6 +191,8 @@ def run_ours(args, ctx):
     torch.cuda.set_device(dev)
     peaks = _peaks()
     w = WORKLOADS[MAIN]
+    if args.tokens:
+        w = w.replace(N=args.tokens)  # smaller token batch for profiler captures only
     inp = _device_inputs(w, dev, 20260000 + w.seed_index + 1000 * ctx["rank"])
     ffn = TensorParallelFFN(w.d, w.d_ff, w.T_p, w.act, "bf16", device=dev)
     fused = args.sum == "fused"
@@ -461,6 +463,7 @@ def main():
     ap.add_argument("--no-decode", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-budget", type=float, default=15.0)
+    ap.add_argument("--tokens", type=int, default=0, help="override the token count (profiler captures)")
     args = ap.parse_args()
     ctx = dist_setup(args.gpus)
     if args.impl == "reference":

@@ -2,8 +2,15 @@
 run the oracle on the same seeded inputs, compare.
 
 Tolerances (written here once, used by every parity test):
-  * bf16 outputs (y, dx, weight and bias gradients) against the float64 oracle:
+  * bf16 outputs (y, dx, weight and bias gradients) against the oracle in the
+    workloads' stated precision ("bf16 weights/activations, fp32 accumulate":
+    the oracle rounds the stored activations h, z / a, g and dz / da, dg to
+    bf16 and computes everything else in float64):
         max |gpu - ref| <= 1e-2 * (|ref| + 1)
+    y and dx are also held to the same bound against the pure float64 chain.
+    Weight gradients are not: they sum the rounding noise of the stored bf16
+    activations over all tokens (sigma ~ sqrt(N) * |dy| * |h| * 2^-9 / sqrt(3)),
+    which exceeds 1e-2 * (|ref| + 1) for small entries at any N in the hundreds
   * fp32 outputs and fp32 shard partials:
         max |gpu - ref| <= 1e-4 * (|ref| + 1)  (+ the rounding allowance below)
   * rounding allowance for partials of bf16 workloads: the partials are sums

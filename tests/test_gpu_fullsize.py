@@ -38,16 +38,19 @@ def _reference(name):
     exact, f = oracle_problem(w, inp, round_bf16=False)
     rb, _ = oracle_problem(w, inp, round_bf16=True)
     ref = dict(rows=rows, js=js, ks=ks, cs=cs)
-    ref["y"] = exact.forward_sharded(rows)["y"]
-    ref["partials"] = rb.forward_sharded(rows)["partials"]
+    ref["y_exact"] = exact.forward_sharded(rows)["y"]
+    fs = rb.forward_sharded(rows)
+    ref["y"], ref["partials"] = fs["y"], fs["partials"]
     dump = rb.hidden_rows(f["dy"], rows) if w.act != "none" else None
     ref["partials_extra"] = partial_allowance(w, f, dump, rows, "y") if dump is not None else None
     if not w.fwd_only:
-        ref["dx"] = exact.backward_rows(f["dy"], rows)["dx"]
+        ref["dx_exact"] = exact.backward_rows(f["dy"], rows)["dx"]
+        br = rb.backward_rows(f["dy"], rows)
+        ref["dx"] = br["dx"]
         if w.act != "none":
-            ref["dx_partials"] = rb.backward_rows(f["dy"], rows)["dx_partials"]
+            ref["dx_partials"] = br["dx_partials"]
             ref["dx_extra"] = partial_allowance(w, f, dump, rows, "dx")
-        ref.update(exact.wgrad_entries(f["dy"], js, ks, cs))
+        ref.update(rb.wgrad_entries(f["dy"], js, ks, cs))
     return w, inp, ref
 
 
@@ -60,12 +63,14 @@ def test_full_size_sampled(name, fused):
     rows, js, ks, cs = (torch.as_tensor(ref[k]).cuda() for k in ("rows", "js", "ks", "cs"))
     get = lambda t: t.to(torch.float64).cpu().numpy()
     check(get(out["y"][rows]), ref["y"], BF16_REL, f"{name} y rows")
+    check(get(out["y"][rows]), ref["y_exact"], BF16_REL, f"{name} y rows vs float64 chain")
     if out["partials"] is not None:
         check(get(out["partials"][:, rows]), ref["partials"], F32_REL, f"{name} partials rows",
               ref["partials_extra"])
     if w.fwd_only:
         return
     check(get(out["dx"][rows]), ref["dx"], BF16_REL, f"{name} dx rows")
+    check(get(out["dx"][rows]), ref["dx_exact"], BF16_REL, f"{name} dx rows vs float64 chain")
     if out["dx_partials"] is not None:
         check(get(out["dx_partials"][:, rows]), ref["dx_partials"], F32_REL, f"{name} dx partials rows",
               ref["dx_extra"])
