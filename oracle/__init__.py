@@ -206,23 +206,27 @@ class FFN:
                                   _ptr(out["db1"]), _ptr(out["db2"]))
         return out
 
-    def hidden_rows(self, dy=None, rows=None):
-        """Values of the stored hidden quantities before bf16 rounding, for
-        selected token rows: dict(h_pre, z_pre, g_pre, dz_pre, dg_pre), each
-        [n, d_ff] (the dz/dg entries only when dy is given)."""
+    DUMP_PLANES = ("h_pre", "z_pre", "g_pre", "dh", "dz_pre", "dg_pre", "nz", "ng", "ndh")
+
+    def hidden_dump(self, dy=None, rows=None, cols=None):
+        """Stored hidden quantities at (rows x cols) before bf16 rounding, with
+        the exact dh and the L2 norms of the producing dot products; a dict of
+        [n_rows, n_cols] arrays keyed by DUMP_PLANES (see tpffn_oracle.c)."""
         lib = self.lib()
         n, r = self._rows(rows)
-        out = {k: np.zeros((n, self.d_ff)) for k in ("h_pre", "z_pre", "g_pre", "dz_pre", "dg_pre")}
+        if cols is None:
+            nc, c = self.d_ff, None
+        else:
+            c = _i64(cols)
+            nc = len(c)
+        out = np.zeros((len(self.DUMP_PLANES), n, nc))
         dyp = None
         if dy is not None:
             dyp = _f64(dy)
             assert dyp.shape == (self.N, self.d)
-        lib.orc_ffn_hidden_rows(ctypes.byref(self._s), _ptr(dyp), ctypes.c_int64(n), _ptr(r),
-                                _ptr(out["h_pre"]), _ptr(out["z_pre"]), _ptr(out["g_pre"]),
-                                _ptr(out["dz_pre"]), _ptr(out["dg_pre"]))
-        if dy is None:
-            del out["dz_pre"], out["dg_pre"]
-        return out
+        lib.orc_ffn_hidden_dump(ctypes.byref(self._s), _ptr(dyp), ctypes.c_int64(n), _ptr(r),
+                                ctypes.c_int64(nc), _ptr(c), _ptr(out))
+        return dict(zip(self.DUMP_PLANES, out))
 
     def backward_full(self, dy):
         """All gradients in full (small problems only)."""

@@ -315,28 +315,58 @@ static void hidden_unit_bwd(const orc_ffn* P, const double* dy, int64_t n, int64
   hidden_unit_bwd_ex(P, dy, n, j, h, dz, dg, NULL);
 }
 
-/* Stored hidden quantities of selected token rows together with their
- * values before bf16 rounding, each [n_rows][d_ff] (any pointer may be NULL):
- *   h_pre  : sigma(z) or silu(a) g          z_pre : z (GELU) or a (SwiGLU)
- *   g_pre  : g (SwiGLU)                     dz_pre: dh sigma'(z_saved) or da
- *   dg_pre : dg (SwiGLU)
- * The tests use them to find rounding decisions that lie within float noise
- * of a bf16 midpoint (dy may be NULL when no backward values are wanted). */
-void orc_ffn_hidden_rows(const orc_ffn* P, const double* dy, int64_t n_rows, const int64_t* rows,
-                         double* h_pre, double* z_pre, double* g_pre, double* dz_pre, double* dg_pre) {
-  const int64_t dff = P->d_ff;
+/* Stored hidden quantities at selected (token row, hidden unit) positions,
+ * with their values before bf16 rounding and the magnitudes of the dot
+ * products that produce them.  rows == NULL: all tokens; cols == NULL: all
+ * hidden units.  out holds 9 planes of [n_rows][n_cols]:
+ *   0 h_pre  : sigma(z) or silu(a) g            1 z_pre : z (GELU) or a
+ *   2 g_pre  : g (SwiGLU)                       3 dh    : W2^T dy (exact)
+ *   4 dz_pre : dh sigma'(z_saved), or da        5 dg_pre: dg (SwiGLU)
+ *   6 nz     : sqrt(sum_k (x_k W1_jk)^2)        7 ng    : same for W3
+ *   8 ndh    : sqrt(sum_c (dy_c W2_cj)^2)
+ * The tests use them to find rounding decisions that lie within the GPU's
+ * accumulation error of a bf16 midpoint.  dy may be NULL (planes 3-5, 8 = 0). */
+void orc_ffn_hidden_dump(const orc_ffn* P, const double* dy, int64_t n_rows, const int64_t* rows,
+                         int64_t n_cols, const int64_t* cols, double* out) {
+  const int64_t d = P->d, dff = P->d_ff;
+  const int64_t plane = n_rows * n_cols;
 #pragma omp parallel for schedule(dynamic, 1)
   for (int64_t r = 0; r < n_rows; ++r) {
     int64_t n = rows ? rows[r] : r;
-    for (int64_t j = 0; j < dff; ++j) {
+    for (int64_t q = 0; q < n_cols; ++q) {
+      int64_t j = cols ? cols[q] : q;
       double h, zs, as, gs, pre[3], bpre[2] = {0.0, 0.0}, dz, dg;
       hidden_unit_ex(P, n, j, &h, &zs, &as, &gs, pre);
-      if (dy) hidden_unit_bwd_ex(P, dy, n, j, &h, &dz, &dg, bpre);
-      if (h_pre) h_pre[r * dff + j] = pre[0];
-      if (z_pre) z_pre[r * dff + j] = pre[1];
-      if (g_pre) g_pre[r * dff + j] = pre[2];
-      if (dz_pre) dz_pre[r * dff + j] = bpre[0];
-      if (dg_pre) dg_pre[r * dff + j] = bpre[1];
+      double dh = 0.0, ndh = 0.0, nz = 0.0, ng = 0.0;
+      if (dy) {
+        hidden_unit_bwd_ex(P, dy, n, j, &h, &dz, &dg, bpre);
+        for (int64_t c = 0; c < d; ++c) {
+          double t = dy[n * d + c] * P->W2[c * dff + j];
+          dh += t;
+          ndh += t * t;
+        }
+      }
+      if (P->act != ORC_ACT_NONE) {
+        const double* xn = P->x + n * d;
+        for (int64_t k = 0; k < d; ++k) {
+          double t = xn[k] * P->W1[j * d + k];
+          nz += t * t;
+          if (P->act == ORC_ACT_SWIGLU) {
+            double u = xn[k] * P->W3[j * d + k];
+            ng += u * u;
+          }
+        }
+      }
+      const int64_t o = r * n_cols + q;
+      out[0 * plane + o] = pre[0];
+      out[1 * plane + o] = pre[1];
+      out[2 * plane + o] = pre[2];
+      out[3 * plane + o] = dh;
+      out[4 * plane + o] = bpre[0];
+      out[5 * plane + o] = bpre[1];
+      out[6 * plane + o] = sqrt(nz);
+      out[7 * plane + o] = sqrt(ng);
+      out[8 * plane + o] = sqrt(ndh);
     }
   }
 }

@@ -9,7 +9,8 @@ import pytest
 import torch
 
 from synth import WORKLOADS, make_inputs
-from tests.parity import BF16_REL, F32_REL, check, oracle_problem, partial_allowance, run_gpu_tensors
+from tests.parity import (BF16_REL, F32_REL, allowance_rows, allowance_wgrad, check, oracle_problem,
+                          rounding_weights, run_gpu_tensors)
 
 pytestmark = [pytest.mark.gpu, pytest.mark.slow]
 
@@ -41,15 +42,16 @@ def _reference(name):
     ref["y_exact"] = exact.forward_sharded(rows)["y"]
     fs = rb.forward_sharded(rows)
     ref["y"], ref["partials"] = fs["y"], fs["partials"]
-    dump = rb.hidden_rows(f["dy"], rows) if w.act != "none" else None
-    ref["partials_extra"] = partial_allowance(w, f, dump, rows, "y") if dump is not None else None
+    A, W = {}, {}
+    if w.act != "none":
+        A = allowance_rows(w, f, rounding_weights(w, rb.hidden_dump(f["dy"], rows)))
+        if not w.fwd_only:
+            W = allowance_wgrad(w, f, rounding_weights(w, rb.hidden_dump(f["dy"], None, js)), ks, cs)
+    ref["A"], ref["W"] = A, W
     if not w.fwd_only:
         ref["dx_exact"] = exact.backward_rows(f["dy"], rows)["dx"]
         br = rb.backward_rows(f["dy"], rows)
-        ref["dx"] = br["dx"]
-        if w.act != "none":
-            ref["dx_partials"] = br["dx_partials"]
-            ref["dx_extra"] = partial_allowance(w, f, dump, rows, "dx")
+        ref["dx"], ref["dx_partials"] = br["dx"], br["dx_partials"]
         ref.update(rb.wgrad_entries(f["dy"], js, ks, cs))
     return w, inp, ref
 
@@ -62,23 +64,23 @@ def test_full_size_sampled(name, fused):
     assert n_fwd >= 1
     rows, js, ks, cs = (torch.as_tensor(ref[k]).cuda() for k in ("rows", "js", "ks", "cs"))
     get = lambda t: t.to(torch.float64).cpu().numpy()
-    check(get(out["y"][rows]), ref["y"], BF16_REL, f"{name} y rows")
+    A, W = ref["A"], ref["W"]
+    check(get(out["y"][rows]), ref["y"], BF16_REL, f"{name} y rows", A.get("y"))
     check(get(out["y"][rows]), ref["y_exact"], BF16_REL, f"{name} y rows vs float64 chain")
     if out["partials"] is not None:
-        check(get(out["partials"][:, rows]), ref["partials"], F32_REL, f"{name} partials rows",
-              ref["partials_extra"])
+        check(get(out["partials"][:, rows]), ref["partials"], F32_REL, f"{name} partials rows", A.get("partials"))
     if w.fwd_only:
         return
-    check(get(out["dx"][rows]), ref["dx"], BF16_REL, f"{name} dx rows")
+    check(get(out["dx"][rows]), ref["dx"], BF16_REL, f"{name} dx rows", A.get("dx"))
     check(get(out["dx"][rows]), ref["dx_exact"], BF16_REL, f"{name} dx rows vs float64 chain")
     if out["dx_partials"] is not None:
         check(get(out["dx_partials"][:, rows]), ref["dx_partials"], F32_REL, f"{name} dx partials rows",
-              ref["dx_extra"])
-    check(get(out["dW2"][cs][:, js]), ref["dW2"], BF16_REL, f"{name} dW2 entries")
+              A.get("dx_partials"))
+    check(get(out["dW2"][cs][:, js]), ref["dW2"], BF16_REL, f"{name} dW2 entries", W.get("dW2"))
     if w.act != "none":
-        check(get(out["dW1"][js][:, ks]), ref["dW1"], BF16_REL, f"{name} dW1 entries")
+        check(get(out["dW1"][js][:, ks]), ref["dW1"], BF16_REL, f"{name} dW1 entries", W.get("dW1"))
     if w.act == "swiglu":
-        check(get(out["dW3"][js][:, ks]), ref["dW3"], BF16_REL, f"{name} dW3 entries")
+        check(get(out["dW3"][js][:, ks]), ref["dW3"], BF16_REL, f"{name} dW3 entries", W.get("dW3"))
     if w.bias:
-        check(get(out["db1"][js]), ref["db1"], BF16_REL, f"{name} db1 entries")
+        check(get(out["db1"][js]), ref["db1"], BF16_REL, f"{name} db1 entries", W.get("db1"))
         check(get(out["db2"][cs]), ref["db2"], BF16_REL, f"{name} db2 entries")

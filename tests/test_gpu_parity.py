@@ -10,7 +10,8 @@ import pytest
 import torch
 
 from synth import WORKLOADS, Workload, make_inputs, small_case
-from tests.parity import (BF16_REL, F32_REL, check, oracle_problem, partial_allowance, run_gpu)
+from tests.parity import (BF16_REL, F32_REL, allowance_rows, allowance_wgrad, check, oracle_problem,
+                          rounding_weights, run_gpu)
 
 pytestmark = pytest.mark.gpu
 
@@ -25,31 +26,32 @@ def _full_compare(w, fused):
     rel = BF16_REL if bf else F32_REL
     exact, f = oracle_problem(w, inp, round_bf16=False)
     rb, _ = oracle_problem(w, inp, round_bf16=bf)
+    wts = None
+    if bf and w.act != "none":
+        wts = rounding_weights(w, rb.hidden_dump(f["dy"]))
+    A = allowance_rows(w, f, wts) if wts is not None else {}
+    W = allowance_wgrad(w, f, wts, np.arange(w.d), np.arange(w.d)) if wts is not None and not w.fwd_only else {}
     sh = rb.forward_sharded()
-    check(got["y"], sh["y"], rel, f"{w.name} y")
+    check(got["y"], sh["y"], rel, f"{w.name} y", A.get("y"))
     check(got["y"], exact.forward_sharded()["y"], rel, f"{w.name} y vs float64 chain")
-    dump = rb.hidden_rows(f["dy"]) if w.act != "none" and bf else None
-    rows = np.arange(w.N)
     if got["partials"] is not None:
-        extra = partial_allowance(w, f, dump, rows, "y") if dump is not None else None
-        check(got["partials"], sh["partials"], F32_REL, f"{w.name} partials", extra)
+        check(got["partials"], sh["partials"], F32_REL, f"{w.name} partials", A.get("partials"))
     if w.fwd_only:
         return
     g = rb.backward_full(f["dy"])
-    check(got["dx"], g["dx"], rel, f"{w.name} dx")
+    check(got["dx"], g["dx"], rel, f"{w.name} dx", A.get("dx"))
     check(got["dx"], exact.backward_rows(f["dy"])["dx"], rel, f"{w.name} dx vs float64 chain")
-    check(got["dW2"], g["dW2"], rel, f"{w.name} dW2")
+    check(got["dW2"], g["dW2"], rel, f"{w.name} dW2", W.get("dW2"))
     if w.act != "none":
-        check(got["dW1"], g["dW1"], rel, f"{w.name} dW1")
+        check(got["dW1"], g["dW1"], rel, f"{w.name} dW1", W.get("dW1"))
     if w.act == "swiglu":
-        check(got["dW3"], g["dW3"], rel, f"{w.name} dW3")
+        check(got["dW3"], g["dW3"], rel, f"{w.name} dW3", W.get("dW3"))
     if w.bias:
         check(got["db2"], g["db2"], rel, f"{w.name} db2")
         if w.act == "gelu_tanh":
-            check(got["db1"], g["db1"], rel, f"{w.name} db1")
+            check(got["db1"], g["db1"], rel, f"{w.name} db1", W.get("db1"))
     if got["dx_partials"] is not None:
-        extra = partial_allowance(w, f, dump, rows, "dx") if dump is not None else None
-        check(got["dx_partials"], g["dx_partials"], F32_REL, f"{w.name} dx partials", extra)
+        check(got["dx_partials"], g["dx_partials"], F32_REL, f"{w.name} dx partials", A.get("dx_partials"))
 
 
 @pytest.mark.parametrize("fused", [False, True], ids=["standalone", "fused"])

@@ -287,14 +287,15 @@ def test_bf16_mode_rounds_only_stored_activations():
 
 def test_hidden_dump_rounds_to_stored_values():
     """The pre-rounding dump rounds (RNE, bf16) to exactly the stored values,
-    and equals them in float64 mode."""
+    equals them in float64 mode, its dh is W2^T dy, its norms are those of the
+    products, and a column subset equals the same columns of the full dump."""
     for act in ("gelu_tanh", "swiglu"):
         w = small_case(11, 16, 48, 3, act, dtype="bf16", bias=(act == "gelu_tanh"), seed=43)
         f = {k: to_f64(v) for k, v in make_inputs(w).items()}
         kw = dict(W1=f["W1"], W3=f["W3"], b1=f["b1"], b2=f["b2"])
         for rb in (False, True):
             P = oracle.FFN(f["x"], f["W2"], 3, act, round_bf16=rb, **kw)
-            dump = P.hidden_rows(f["dy"])
+            dump = P.hidden_dump(f["dy"])
             sh = P.forward_sharded()
             # the oracle's own bf16 rounding (pinned above against PyTorch); a
             # float64 -> float32 -> bf16 cast would round twice
@@ -303,10 +304,16 @@ def test_hidden_dump_rounds_to_stored_values():
             if act == "swiglu":
                 np.testing.assert_array_equal(R(dump["z_pre"]), sh["ag_saved"][:, 0])
                 np.testing.assert_array_equal(R(dump["g_pre"]), sh["ag_saved"][:, 1])
+                np.testing.assert_allclose(dump["ng"], np.sqrt((f["x"] ** 2) @ (f["W3"] ** 2).T), rtol=1e-12)
             else:
                 np.testing.assert_array_equal(R(dump["z_pre"]), sh["z_saved"])
+            np.testing.assert_allclose(dump["dh"], f["dy"] @ f["W2"], rtol=1e-12, atol=1e-14)
+            np.testing.assert_allclose(dump["nz"], np.sqrt((f["x"] ** 2) @ (f["W1"] ** 2).T), rtol=1e-12)
+            np.testing.assert_allclose(dump["ndh"], np.sqrt((f["dy"] ** 2) @ (f["W2"] ** 2)), rtol=1e-12)
             js = np.arange(w.d_ff)
             e = P.wgrad_entries(f["dy"], js)
-            # db1 = sum over tokens of the stored dz
-            if act == "gelu_tanh":
+            if act == "gelu_tanh":  # db1 = sum over tokens of the stored dz
                 np.testing.assert_allclose(R(dump["dz_pre"]).sum(0), e["db1"], rtol=1e-12, atol=1e-12)
+            sub = P.hidden_dump(f["dy"], rows=[3, 0], cols=[47, 5, 20])
+            for k in dump:
+                np.testing.assert_array_equal(sub[k], dump[k][np.ix_([3, 0], [47, 5, 20])])
