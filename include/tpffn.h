@@ -219,6 +219,45 @@ TPFFN_API int tp_ffn_bwd(const tp_ffn_plan* plan, int64_t n_tokens, const void* 
                void* dw13p, void* dw2p, void* db1, void* db2, void* workspace,
                size_t workspace_bytes, int flags, tp_stream_t stream);
 
+/* ------------------------------------------------ forward without allocation */
+
+/* Size of the library's static scratch array (32 MiB).  Every GPU that loads
+ * the library reserves this much device memory until the process exits. */
+#define TPFFN_STATIC_SCRATCH_BYTES ((size_t)32 << 20)
+
+/* Forward pass for callers that cannot allocate device memory.
+ *
+ * The pages have no counterpart to this entry point: it exists for callers
+ * that must not call cudaMalloc, or any allocator, when they run the layer.
+ * Examples are a serving engine that reserves all of its device memory at
+ * start-up and forbids allocation while it handles requests, a plugin whose
+ * host framework owns the allocator, or a loop whose latency budget leaves
+ * no room for an allocation that might block.
+ *
+ * It computes what tp_ffn_fwd computes with TP_SUM_STANDALONE, saved = NULL
+ * and partials = NULL.  The caller still passes the inputs (x, w13p, w2p,
+ * b1, b2) and the output y, with the meanings and layouts of tp_ffn_fwd.
+ * The scratch (error word, hidden activations, fp32 shard partials) lives in
+ * one file-scope device array of TPFFN_STATIC_SCRATCH_BYTES.  This call
+ * allocates nothing: no cudaMalloc, no cudaFree, no allocating library call.
+ *   - Limit: returns TP_ERR_UNSUPPORTED, without enqueueing work, when
+ *     tp_ffn_workspace_bytes(plan, n_tokens, TP_SUM_STANDALONE) exceeds
+ *     TPFFN_STATIC_SCRATCH_BYTES (for example at most 77 tokens for the
+ *     Llama-3-70B-shaped decode FFN: d 8192, d_ff 28672, T_p 8, SwiGLU).
+ *   - Set-up: the first call on each device looks up the array's device
+ *     address (cudaGetSymbolAddress, with that device current) and caches
+ *     it.  Make that first call before any stream capture.
+ *   - Sharing: every call, on any stream, uses the same array, which keeps
+ *     the previous call's contents; the call clears the error word it needs
+ *     zeroed, and overwrites the rest.  Calls that overlap on the GPU (for
+ *     example on two streams) race on the array: serialise them.
+ *   - Errors: argument and launch errors as in tp_ffn_fwd.  The device
+ *     error word sits inside the array and is not exposed, so a device-side
+ *     timeout is not reported by this entry point. */
+TPFFN_API int tp_ffn_fwd_static_scratch(const tp_ffn_plan* plan, int64_t n_tokens, const void* x,
+                                        const void* w13p, const void* w2p, const void* b1, const void* b2,
+                                        void* y, tp_stream_t stream);
+
 /* ------------------------------------------------------------- diagnostics */
 
 /* Wait for the stream, then read the error word a previous call left in this

@@ -20,7 +20,7 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(ROOT, "_build", platform.machine())  # objects never cross architectures
 LIB = os.path.join(PKG, "libtpffn.so")
-SOURCES = ["tp_gemm_tc.cu", "tp_kernels.cu", "tp_api.cu"]
+SOURCES = ["tp_gemm_tc.cu", "tp_kernels.cu", "tp_api.cu", "tp_static.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC,-fvisibility=hidden", "-I", INCLUDE, "-I", CSRC]
 

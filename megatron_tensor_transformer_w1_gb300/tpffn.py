@@ -26,7 +26,9 @@ ABI_FUNCTIONS = (
     "tp_ffn_packed_bytes", "tp_ffn_saved_bytes", "tp_ffn_workspace_bytes", "tp_ffn_shard_columns",
     "tp_ffn_shard_rows", "tp_ffn_unshard_columns", "tp_ffn_unshard_rows", "tp_ffn_fwd", "tp_ffn_bwd",
     "tp_ffn_last_device_error", "tp_ffn_status_string", "tp_ffn_kernel_times", "tp_ffn_last_launch_count",
+    "tp_ffn_fwd_static_scratch",
 )
+TPFFN_STATIC_SCRATCH_BYTES = 32 << 20
 
 
 class TPFFNError(RuntimeError):
@@ -65,6 +67,7 @@ _SIGS = {
     "tp_ffn_status_string": (ctypes.c_char_p, [_INT]),
     "tp_ffn_kernel_times": (_INT, [_P, _INT, ctypes.POINTER(ctypes.c_char_p), ctypes.POINTER(ctypes.c_float)]),
     "tp_ffn_last_launch_count": (_INT, [_P]),
+    "tp_ffn_fwd_static_scratch": (_INT, [_P, _I64, _P, _P, _P, _P, _P, _P, _P]),
 }
 for _name, (_res, _args) in _SIGS.items():
     _f = getattr(_lib, _name)
@@ -175,6 +178,14 @@ def tp_ffn_kernel_times(plan, max_records=64):
 
 def tp_ffn_last_launch_count(plan):
     return _lib.tp_ffn_last_launch_count(plan)
+
+
+def tp_ffn_fwd_static_scratch(plan, n_tokens, x, w13p, w2p, b1, b2, y, stream=None):
+    """Forward pass that allocates no device memory (scratch in the library's
+    static array of TPFFN_STATIC_SCRATCH_BYTES); for callers that may not
+    allocate.  See include/tpffn.h for its limit and sharing rules."""
+    return _lib.tp_ffn_fwd_static_scratch(plan, n_tokens, _ptr(x), _ptr(w13p), _ptr(w2p), _ptr(b1), _ptr(b2),
+                                          _ptr(y), _stream(stream))
 
 
 def check(status, where=""):
