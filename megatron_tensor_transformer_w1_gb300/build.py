@@ -18,11 +18,15 @@ PKG = os.path.dirname(os.path.abspath(__file__))
 ROOT = os.path.dirname(PKG)
 CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
-BUILD = os.path.join(ROOT, "_build", platform.machine())  # objects never cross architectures
+BUILD = os.path.join(ROOT, "_build", platform.machine()  # objects never cross architectures
+                     + ("-" + "-".join(x.strip("-").replace("=", "_") for x in os.environ.get("TPFFN_NVCC_EXTRA", "").split())
+                        if os.environ.get("TPFFN_NVCC_EXTRA") else ""))
 LIB = os.path.join(PKG, "libtpffn.so")
 SOURCES = ["tp_gemm_tc.cu", "tp_kernels.cu", "tp_api.cu", "tp_static.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC,-fvisibility=hidden", "-I", INCLUDE, "-I", CSRC]
+# extra nvcc flags (e.g. -DTPFFN_INSTRUMENT for per-CTA wait counters); part of the build stamp
+EXTRA = os.environ.get("TPFFN_NVCC_EXTRA", "").split()
 
 
 def _nvcc():
@@ -39,7 +43,7 @@ def _compile(src, verbose):
     obj = os.path.join(BUILD, os.path.splitext(src)[0] + ".o")
     if os.path.exists(obj) and os.path.getmtime(obj) >= _deps_mtime():
         return obj
-    cmd = [_nvcc(), *ARCH, *FLAGS, "-c", os.path.join(CSRC, src), "-o", obj]
+    cmd = [_nvcc(), *ARCH, *FLAGS, *EXTRA, "-c", os.path.join(CSRC, src), "-o", obj]
     if verbose:
         cmd.insert(1, "-Xptxas=-v")
     r = subprocess.run(cmd, capture_output=True, text=True)

@@ -30,6 +30,8 @@
 #include <cuda_runtime.h>
 
 #include <atomic>
+#include <cstdio>
+#include <cstdlib>
 #include <mutex>
 
 #include "tp_internal.h"
@@ -530,6 +532,347 @@ __global__ void __launch_bounds__(THREADS, 1)
   }
 }
 
+// ------------------------------------------------------------ 2-SM pair kernel
+//
+// Two CTAs of a cluster (one per SM) compute one 256 x 256 output tile with
+// tcgen05.mma.cta_group::2 (M = 256, N = 256, K = 16): CTA r holds rows
+// [128r, 128r + 128) of the A tile and rows [128r, 128r + 128) of the B tile
+// (its half of N) in its own shared memory; the leader CTA (rank 0) issues the
+// MMAs, which read A from both CTAs and B from both halves and write each
+// CTA's 128 output rows into that CTA's tensor memory.  Each SM therefore
+// stages 32 KB per K step of 64 instead of 48 KB, which leaves room for 7
+// stages (more latency hidden) and reads a third less from L2 per SM.
+//
+// Barriers: TMA copies of both CTAs complete on the leader's full[] barrier
+// (cp.async.bulk.tensor .cta_group::2 with the leader's barrier address),
+// which only the leader arms (expect-tx for both CTAs' bytes);
+// the leader's commits arrive on empty[] and tfull[] of both CTAs
+// (multicast); both CTAs' epilogue warps arrive on the leader's tempty[].
+__device__ __forceinline__ uint32_t cluster_rank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+__device__ __forceinline__ uint32_t map_to_rank(uint32_t local_smem, uint32_t rank) {
+  uint32_t remote;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(local_smem), "r"(rank));
+  return remote;
+}
+__device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_addr) {
+  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
+}
+__device__ __forceinline__ void cluster_sync() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tma_load_3d_pair(void* dst, const CUtensorMap* tm, uint32_t leader_bar, int c0,
+                                                 int c1, int c2) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.cta_group::2.shared::cluster.global.tile.mbarrier::complete_tx::bytes "
+      "[%0], [%1, {%2, %3, %4}], [%5];" ::"r"(smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(tm)), "r"(c0), "r"(c1), "r"(c2), "r"(leader_bar)
+      : "memory");
+}
+__device__ __forceinline__ void tmem_alloc_pair(uint32_t* slot, uint32_t ncols) {
+  asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(slot)),
+               "r"(ncols)
+               : "memory");
+  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_dealloc_pair(uint32_t taddr, uint32_t ncols) {
+  asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
+}
+__device__ __forceinline__ void umma_bf16_pair(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                                               uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+__device__ __forceinline__ void umma_commit_pair(uint64_t* bar) {  // arrive on bar in both CTAs
+  const uint16_t mask = 0x3;
+  asm volatile(
+      "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(
+          smem_u32(bar)),
+      "h"(mask)
+      : "memory");
+}
+
+__device__ __forceinline__ void umma_commit_pair_local(uint64_t* bar) {  // arrive on this CTA's bar
+  asm volatile("tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(smem_u32(bar))
+               : "memory");
+}
+
+#ifdef TPFFN_INSTRUMENT
+// Per-CTA cycle counters for performance investigations (not in normal builds):
+// [0] MMA wait on full, [1] MMA wait on tempty, [2] MMA thread total,
+// [3] producer wait on empty, [4] epilogue wait on tfull, [5] epilogue total, [6] k-iterations
+__device__ unsigned long long g_tpffn_dbg[1024][8];
+#define DBG_T0() const long long _t0 = clock64()
+#define DBG_ADD(slot, since) atomicAdd(&g_tpffn_dbg[blockIdx.x & 1023][slot], (unsigned long long)(clock64() - (since)))
+#else
+#define DBG_T0()
+#define DBG_ADD(slot, since)
+#endif
+
+constexpr int PAIR_BN = 256;   // N of the pair tile (each CTA stages half of it)
+constexpr int PAIR_STAGES = 7;
+
+struct PairLayout {
+  static constexpr int A_BYTES = BM * BK * 2;               // this CTA's 128 rows of A
+  static constexpr int B_BYTES = (PAIR_BN / 2) * BK * 2;    // this CTA's half of B
+  static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;     // 32 KB
+  static constexpr int BAR_OFF = PAIR_STAGES * STAGE_BYTES;
+  static constexpr int SMEM = BAR_OFF + 256 + 1024;
+  static constexpr uint32_t TMEM_COLS = 2 * PAIR_BN;
+  static_assert((2 * PAIR_STAGES + 5) * 8 <= 232, "barrier area");
+};
+
+// Pair tile order: like decode_tile, over 256-row M blocks.
+__device__ __forceinline__ void decode_pair_tile(const Params& p, int tile, int& b, int& mp, int& nb) {
+  const int tiles_m2 = (p.tiles_m + 1) >> 1;
+  const int tpb = tiles_m2 * p.tiles_n;
+  b = tile / tpb;
+  const int r = tile - b * tpb;
+  constexpr int GM = 4;
+  const int group = r / (GM * p.tiles_n);
+  const int first_m = group * GM;
+  const int gm = min(tiles_m2 - first_m, GM);
+  const int in_group = r - group * GM * p.tiles_n;
+  mp = first_m + in_group % gm;
+  nb = in_group / gm;
+}
+
+template <int EPI, bool AMN, bool BMN>
+__global__ void __launch_bounds__(THREADS, 1)
+    tc_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                        const Params p) {
+  using L = PairLayout;
+  constexpr int BN = PAIR_BN;
+  constexpr int STAGES = PAIR_STAGES;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + L::BAR_OFF);
+  uint64_t* empty = full + STAGES;
+  uint64_t* tfull = empty + STAGES;
+  uint64_t* tempty = tfull + 2;
+  uint64_t* drain = tempty + 2;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::BAR_OFF + 240);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::BAR_OFF + 244);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const uint32_t rank = cluster_rank();
+  const bool leader = rank == 0;
+  const int cluster_id = blockIdx.x >> 1;
+  const int num_clusters = gridDim.x >> 1;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(&full[s], 1);   // leader: its own arrive + both CTAs' bytes
+      mbar_init(&empty[s], 1);  // one multicast commit of the leader
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&tfull[i], 1);
+      mbar_init(&tempty[i], 8);  // leader: 4 epilogue warps x 2 CTAs
+    }
+    mbar_init(drain, 1);
+    *abort_flag = 0;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+  }
+  if (warp == 0 && lane == 0) {
+    prefetch_tmap(&tmA);
+    prefetch_tmap(&tmB);
+  }
+  if (warp == 1) tmem_alloc_pair(tmem_slot, L::TMEM_COLS);
+  tc_fence_before();
+  cluster_sync();  // barriers of both CTAs initialised before any remote arrive
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+
+  const int tiles_m2 = (p.tiles_m + 1) >> 1;
+  const int num_tiles = tiles_m2 * p.tiles_n * p.NB;
+  const int k_iters = p.G * p.k_blocks;
+
+  if (warp == 0) {
+    // ------------------------------------------------ TMA producer (both CTAs)
+    if (lane == 0) {
+      int stage = 0;
+      uint32_t phase = 0;
+      int last_issue_phase[STAGES];
+#pragma unroll
+      for (int s = 0; s < STAGES; ++s) last_issue_phase[s] = -1;
+      bool ok = true;
+      for (int tile = cluster_id; tile < num_tiles && ok; tile += num_clusters) {
+        int b, mp, nb;
+        decode_pair_tile(p, tile, b, mp, nb);
+        const int m0 = mp * 256 + static_cast<int>(rank) * 128;   // this CTA's A rows
+        const int n0 = nb * BN + static_cast<int>(rank) * (BN / 2);  // this CTA's half of B
+        for (int it = 0; it < k_iters; ++it) {
+          const int g = it / p.k_blocks;
+          const int k0 = (it - g * p.k_blocks) * BK;
+          {
+            DBG_T0();
+            const bool w_ok = wait_bounded(&empty[stage], phase ^ 1u, abort_flag, p);
+            DBG_ADD(3, _t0);
+            if (!w_ok) {
+              ok = false;
+              break;
+            }
+          }
+          const bool skip = p.debug_skip && tile == cluster_id && it == 0;
+          if (!skip) {
+            uint8_t* sA = smem + stage * L::STAGE_BYTES;
+            uint8_t* sB = sA + L::A_BYTES;
+            // Only the leader arms its full barrier, for the bytes of both
+            // CTAs; the peer's copies complete on it directly (its transaction
+            // count may go below zero until the leader arms it).  A peer-side
+            // arrive would need a cluster-scope release per stage, which
+            // serialises the peer's copies.
+            const uint32_t leader_full = map_to_rank(smem_u32(&full[stage]), 0);
+            if (leader) mbar_arrive_expect_tx(&full[stage], 2 * L::STAGE_BYTES);
+            const int ab = b * p.a_bsel + g * p.a_gsel;
+            const int bb = b * p.b_bsel + g * p.b_gsel;
+            if (!AMN) {
+              tma_load_3d_pair(sA, &tmA, leader_full, k0, p.a_swap ? ab : m0, p.a_swap ? m0 : ab);
+            } else {
+#pragma unroll
+              for (int i = 0; i < 2; ++i)
+                tma_load_3d_pair(sA + i * 8192, &tmA, leader_full, m0 + 64 * i, p.a_swap ? ab : k0,
+                                 p.a_swap ? k0 : ab);
+            }
+            if (!BMN) {
+              tma_load_3d_pair(sB, &tmB, leader_full, k0, p.b_swap ? bb : n0, p.b_swap ? n0 : bb);
+            } else {
+#pragma unroll
+              for (int i = 0; i < 2; ++i)
+                tma_load_3d_pair(sB + i * 8192, &tmB, leader_full, n0 + 64 * i, p.b_swap ? bb : k0,
+                                 p.b_swap ? k0 : bb);
+            }
+            last_issue_phase[stage] = static_cast<int>(phase);
+          }
+          if (++stage == STAGES) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+      }
+      // Drain (leader): its full[] barriers count both CTAs' copies.
+      if (leader) {
+#pragma unroll 1
+        for (int s = 0; s < STAGES; ++s)
+          if (last_issue_phase[s] >= 0)
+            wait_bounded(&full[s], static_cast<uint32_t>(last_issue_phase[s]), abort_flag, p, false);
+      }
+    }
+    __syncwarp();
+  } else if (warp == 1) {
+    // ------------------------------------------------ MMA issuer (leader only)
+    if (leader && lane == 0) {
+      // M = 256 (two CTAs), N = 256
+      constexpr uint32_t IDESC = (1u << 4) | (1u << 7) | (1u << 10) | (static_cast<uint32_t>(AMN) << 15) |
+                                 (static_cast<uint32_t>(BMN) << 16) | (static_cast<uint32_t>(BN >> 3) << 17) |
+                                 (static_cast<uint32_t>(256 >> 4) << 24);
+      int stage = 0;
+      uint32_t phase = 0;
+      int local = 0;
+      bool ok = true;
+#ifdef TPFFN_INSTRUMENT
+      const long long t_start = clock64();
+#endif
+      for (int tile = cluster_id; tile < num_tiles && ok; tile += num_clusters, ++local) {
+        const int buf = local & 1;
+        const uint32_t use = static_cast<uint32_t>(local >> 1);
+        {
+          DBG_T0();
+          const bool w_ok = wait_bounded(&tempty[buf], (use & 1u) ^ 1u, abort_flag, p);
+          DBG_ADD(1, _t0);
+          if (!w_ok) break;
+        }
+        tc_fence_after();
+        const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(buf * BN);
+        for (int it = 0; it < k_iters; ++it) {
+          {
+            DBG_T0();
+            const bool w_ok = wait_bounded(&full[stage], phase, abort_flag, p);
+            DBG_ADD(0, _t0);
+            if (!w_ok) {
+              ok = false;
+              break;
+            }
+          }
+#ifdef TPFFN_INSTRUMENT
+          atomicAdd(&g_tpffn_dbg[blockIdx.x & 1023][6], 1ull);
+#endif
+          tc_fence_after();
+          const uint32_t a_addr = smem_u32(smem + stage * L::STAGE_BYTES);
+          const uint32_t b_addr = a_addr + L::A_BYTES;
+#pragma unroll
+          for (int k = 0; k < BK / 16; ++k)
+            umma_bf16_pair(d_tmem, smem_desc<AMN>(a_addr, k), smem_desc<BMN>(b_addr, k), IDESC,
+                           (it > 0 || k > 0) ? 1u : 0u);
+          umma_commit_pair(&empty[stage]);  // frees the stage in both CTAs
+          if (++stage == STAGES) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+        if (!ok) break;
+        umma_commit_pair(&tfull[buf]);  // accumulators of both CTAs ready
+      }
+      umma_commit_pair_local(drain);  // arrives once every MMA issued here has completed
+      wait_bounded(drain, 0u, abort_flag, p, false);
+#ifdef TPFFN_INSTRUMENT
+      DBG_ADD(2, t_start);
+#endif
+    }
+    __syncwarp();
+  } else {
+    // ------------------------------------------------ epilogue warps 2..5 (both CTAs)
+    const int quarter = warp & 3;
+    const uint32_t leader_tempty0 = map_to_rank(smem_u32(&tempty[0]), 0);
+    const uint32_t leader_tempty1 = map_to_rank(smem_u32(&tempty[1]), 0);
+    int local = 0;
+#ifdef TPFFN_INSTRUMENT
+    const long long t_epi = clock64();
+#endif
+    for (int tile = cluster_id; tile < num_tiles; tile += num_clusters, ++local) {
+      const int buf = local & 1;
+      const uint32_t use = static_cast<uint32_t>(local >> 1);
+      bool w_ok;
+      {
+        DBG_T0();
+        w_ok = wait_bounded(&tfull[buf], use & 1u, abort_flag, p);
+        if (warp == 2 && lane == 0) DBG_ADD(4, _t0);
+      }
+      if (!w_ok) break;
+      tc_fence_after();
+      int b, mp, nb;
+      decode_pair_tile(p, tile, b, mp, nb);
+      const int row = mp * 256 + static_cast<int>(rank) * 128 + quarter * 32 + lane;
+      const uint32_t taddr = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) +
+                             static_cast<uint32_t>(buf * BN);
+      epilogue_tile<BN, EPI>(p, b, row, row < p.M, nb * BN, nb, taddr);
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive_cluster(buf ? leader_tempty1 : leader_tempty0);
+    }
+#ifdef TPFFN_INSTRUMENT
+    if (warp == 2 && lane == 0) DBG_ADD(5, t_epi);
+#endif
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  cluster_sync();  // the leader's MMAs and copies into both CTAs have finished
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc_pair(tmem_base, L::TMEM_COLS);
+  }
+}
+
 // ------------------------------------------------------------ host side
 typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
                                   const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
@@ -649,12 +992,146 @@ static int launch_inst(const GemmSpec& s, LaunchCtx& ctx) {
   return cudaPeekAtLastError() == cudaSuccess ? 0 : TP_ERR_CUDA;
 }
 
+template <int EPI, bool AMN, bool BMN>
+static int launch_pair(const GemmSpec& s, LaunchCtx& ctx) {
+  using L = PairLayout;
+  CUtensorMap ta, tb;
+  int sa = 0, sb = 0;
+  int rc = make_map(&ta, s.A, BM, &sa);
+  if (rc) return rc;
+  rc = make_map(&tb, s.B, PAIR_BN / 2, &sb);
+  if (rc) return rc;
+  Params p{};
+  p.M = static_cast<int>(s.M);
+  p.N = static_cast<int>(s.N);
+  p.K = static_cast<int>(s.K);
+  p.NB = s.NB;
+  p.G = s.G;
+  p.tiles_m = static_cast<int>((s.M + BM - 1) / BM);
+  p.tiles_n = static_cast<int>((s.N + PAIR_BN - 1) / PAIR_BN);
+  p.k_blocks = static_cast<int>((s.K + BK - 1) / BK);
+  p.a_bsel = s.A.bsel;
+  p.a_gsel = s.A.gsel;
+  p.b_bsel = s.B.bsel;
+  p.b_gsel = s.B.gsel;
+  p.a_swap = sa;
+  p.b_swap = sb;
+  p.out = s.out;
+  p.out_bs = s.out_bs;
+  p.out_rs = s.out_rs;
+  p.out2 = s.out2;
+  p.out2_bs = s.out2_bs;
+  p.out2_rs = s.out2_rs;
+  p.aux = s.aux;
+  p.aux_bs = s.aux_bs;
+  p.aux_rs = s.aux_rs;
+  p.bias = static_cast<const __nv_bfloat16*>(s.bias);
+  p.bias_bs = s.bias_bs;
+  p.bias_len = s.bias_len;
+  p.n_store = s.n_store;
+  p.err = ctx.err;
+  p.timeout_ns = ctx.timeout_ns;
+  p.debug_skip = ctx.debug_skip_load;
+  ctx.debug_skip_load = 0;
+
+  auto kern = tc_gemm_pair_kernel<EPI, AMN, BMN>;
+  static std::atomic<uint32_t> attr_done{0};
+  static std::atomic<int> max_clusters[32];
+  int dev = 0;
+  cudaGetDevice(&dev);
+  const uint32_t bit = 1u << (dev & 31);
+  if (!(attr_done.load() & bit)) {
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::SMEM) != cudaSuccess)
+      return TP_ERR_CUDA;
+    cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 0);
+    attr_done.fetch_or(bit);
+  }
+  cudaLaunchConfig_t cfg{};
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.blockDim = dim3(THREADS, 1, 1);
+  cfg.dynamicSmemBytes = L::SMEM;
+  cfg.stream = ctx.stream;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  int mc = max_clusters[dev & 31].load();
+  if (mc <= 0) {
+    cfg.gridDim = dim3(2 * (ctx.num_sms / 2), 1, 1);
+    int q = 0;
+    cudaError_t qe = cudaOccupancyMaxActiveClusters(&q, kern, &cfg);
+    mc = (qe == cudaSuccess && q > 0) ? q : ctx.num_sms / 2;
+    if (getenv("TPFFN_VERBOSE"))
+      fprintf(stderr, "tpffn: pair kernel: occupancy query rc=%d clusters=%d -> using %d clusters\n", (int)qe, q, mc);
+    max_clusters[dev & 31].store(mc);
+  }
+  const long long tiles = static_cast<long long>((p.tiles_m + 1) / 2) * p.tiles_n * p.NB;
+  if (tiles <= 0 || p.k_blocks <= 0) return TP_ERR_INVALID;
+  const int clusters = static_cast<int>(tiles < mc ? tiles : mc);
+  cfg.gridDim = dim3(2 * clusters, 1, 1);
+  if (ctx.before) ctx.before(ctx.user, s.name);
+  cudaError_t e = cudaLaunchKernelEx(&cfg, kern, ta, tb, p);
+  if (ctx.after) ctx.after(ctx.user);
+  ctx.launches++;
+  return e == cudaSuccess && cudaPeekAtLastError() == cudaSuccess ? 0 : TP_ERR_CUDA;
+}
+
 }  // namespace tc
+
+#ifdef TPFFN_INSTRUMENT
+extern "C" __attribute__((visibility("default"))) int tpffn_debug_counters(unsigned long long* host, int clear) {
+  if (cudaMemcpyFromSymbol(host, tc::g_tpffn_dbg, sizeof(tc::g_tpffn_dbg)) != cudaSuccess) return 1;
+  if (clear) {
+    static unsigned long long zeros[1024][8];
+    if (cudaMemcpyToSymbol(tc::g_tpffn_dbg, zeros, sizeof(zeros)) != cudaSuccess) return 1;
+  }
+  return 0;
+}
+#endif
+
+// The two-SM kernel serves every GEMM with at least 256 rows; TPFFN_PAIR=0 in
+// the environment selects the one-SM kernel everywhere (for comparisons).
+static bool pair_path_enabled() {
+  static const bool on = [] {
+    const char* v = getenv("TPFFN_PAIR");
+    return !(v && v[0] == '0');
+  }();
+  return on;
+}
 
 int launch_tc_gemm(const GemmSpec& s, LaunchCtx& ctx) {
   using namespace tc;
   const bool amn = s.A.mn_major != 0, bmn = s.B.mn_major != 0;
   if (s.n_store % 8) return TP_ERR_UNSUPPORTED;
+  if (s.M >= 256 && pair_path_enabled()) {
+    switch (s.epi) {
+      case EPI_SWIGLU_FWD:
+        if (!amn && !bmn) return launch_pair<EPI_SWIGLU_FWD, false, false>(s, ctx);
+        break;
+      case EPI_GELU_FWD:
+        if (!amn && !bmn) return launch_pair<EPI_GELU_FWD, false, false>(s, ctx);
+        break;
+      case EPI_F32:
+        if (!amn && !bmn) return launch_pair<EPI_F32, false, false>(s, ctx);
+        if (!amn && bmn) return launch_pair<EPI_F32, false, true>(s, ctx);
+        break;
+      case EPI_OUT:
+        if (!amn && !bmn) return launch_pair<EPI_OUT, false, false>(s, ctx);
+        if (!amn && bmn) return launch_pair<EPI_OUT, false, true>(s, ctx);
+        if (amn && bmn) return launch_pair<EPI_OUT, true, true>(s, ctx);
+        break;
+      case EPI_GELU_BWD:
+        if (!amn && bmn) return launch_pair<EPI_GELU_BWD, false, true>(s, ctx);
+        break;
+      case EPI_SWIGLU_BWD:
+        if (!amn && bmn) return launch_pair<EPI_SWIGLU_BWD, false, true>(s, ctx);
+        break;
+      default:
+        break;
+    }
+  }
   switch (s.epi) {
     case EPI_SWIGLU_FWD:
       if (!amn && !bmn) return launch_inst<256, 4, EPI_SWIGLU_FWD, false, false>(s, ctx);
