@@ -1,16 +1,18 @@
 // tp_gemm_tc.cu -- the tensor-core GEMM of every bf16 shard computation.
 //
 // Blackwell (sm_103a) design, written for this library:
-//   * one persistent CTA per SM, 192 threads in three roles:
+//   * one persistent CTA per SM, 192 or 320 threads in three roles:
 //       warp 0      : TMA producer (one elected lane) -- cp.async.bulk.tensor
 //                     3-D tiled loads, 128-byte swizzle, into a STAGES-deep
 //                     shared-memory ring guarded by mbarriers;
 //       warp 1      : allocates tensor memory, and one lane issues
 //                     tcgen05.mma (kind::f16, bf16 x bf16 -> fp32, M=128,
 //                     N=BN, K=16 per instruction) and tcgen05.commit;
-//       warps 2..5  : epilogue -- tcgen05.ld of the fp32 accumulator
-//                     (warp w reads TMEM lanes 32*(w%4)..), fused activation
-//                     or derivative, vectorised global stores;
+//       warps 2..   : epilogue (4, or 8 for the backward epilogues) --
+//                     tcgen05.ld of the fp32 accumulator (warp w reads TMEM
+//                     lanes 32*(w%4)..; with 8, two warps per lane quarter
+//                     split the columns), fused activation or derivative,
+//                     vectorised global stores;
 //   * the accumulator is double-buffered in tensor memory (2 x BN columns),
 //     so the epilogue of one tile overlaps the MMA K-loop of the next;
 //   * every wait on an mbarrier is bounded: after the time limit the waiting
@@ -42,7 +44,18 @@ namespace tc {
 
 constexpr int BM = 128;
 constexpr int BK = 64;
-constexpr int THREADS = 192;
+// Epilogue warps per CTA: 8 (two per TMEM lane quarter, each taking half the
+// columns) for the backward epilogues, whose global loads of the saved
+// activations are latency-bound; 4 for the others, whose arithmetic would
+// otherwise take issue slots from the producer and MMA threads.
+template <int EPI>
+__host__ __device__ constexpr int epi_warps() {
+  return (EPI == EPI_SWIGLU_BWD || EPI == EPI_GELU_BWD) ? 8 : 4;
+}
+template <int EPI>
+__host__ __device__ constexpr int threads_for() {
+  return 64 + 32 * epi_warps<EPI>();  // producer, MMA, epilogue
+}
 
 struct Params {
   int M, N, K;
@@ -244,16 +257,19 @@ __device__ __forceinline__ void decode_tile(const Params& p, int tile, int& b, i
 // ------------------------------------------------------------ epilogues
 // One thread owns one output row of the tile; `taddr` points at its TMEM
 // lane and the first column of the accumulator buffer.
+// `part` selects which share of the tile's columns this warp handles when a
+// TMEM lane quarter is served by two epilogue warps (part is 0 with one).
 template <int BN, int EPI>
 __device__ __forceinline__ void epilogue_tile(const Params& p, int b, int row, bool row_ok, int n0, int nb,
-                                              uint32_t taddr) {
+                                              uint32_t taddr, int part) {
+  constexpr int NSPLIT = epi_warps<EPI>() / 4;
   if constexpr (EPI == EPI_SWIGLU_FWD) {
     static_assert(BN == 256, "SwiGLU forward tiles hold 128 a-columns then 128 g-columns");
     __nv_bfloat16* hout = static_cast<__nv_bfloat16*>(p.out) + b * p.out_bs + (long long)row * p.out_rs;
     __nv_bfloat16* sv = p.out2 ? static_cast<__nv_bfloat16*>(p.out2) + b * p.out2_bs + (long long)row * p.out2_rs
                                : nullptr;
 #pragma unroll 1
-    for (int c = 0; c < 4; ++c) {
+    for (int c = part * (4 / NSPLIT); c < (part + 1) * (4 / NSPLIT); ++c) {
       uint32_t ra[32], rg[32];
       __syncwarp();  // tcgen05.ld is warp-collective: reconverge first
       tmem_ld32(taddr + c * 32, ra);
@@ -281,7 +297,7 @@ __device__ __forceinline__ void epilogue_tile(const Params& p, int b, int row, b
     return;
   } else {
 #pragma unroll 1
-    for (int c = 0; c < BN / 32; ++c) {
+    for (int c = part * (BN / 32 / NSPLIT); c < (part + 1) * (BN / 32 / NSPLIT); ++c) {
       uint32_t r[32];
       __syncwarp();  // tcgen05.ld is warp-collective: reconverge first
       tmem_ld32(taddr + c * 32, r);
@@ -361,7 +377,7 @@ struct Layout {
 };
 
 template <int BN, int STAGES, int EPI, bool AMN, bool BMN>
-__global__ void __launch_bounds__(THREADS, 1)
+__global__ void __launch_bounds__(threads_for<EPI>(), 1)
     tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                    const Params p) {
   using L = Layout<BN, STAGES>;
@@ -385,7 +401,7 @@ __global__ void __launch_bounds__(THREADS, 1)
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&tfull[i], 1);
-      mbar_init(&tempty[i], 4);  // one arrive per epilogue warp
+      mbar_init(&tempty[i], epi_warps<EPI>());  // one arrive per epilogue warp
     }
     mbar_init(drain, 1);
     *abort_flag = 0;
@@ -504,7 +520,7 @@ __global__ void __launch_bounds__(THREADS, 1)
     }
     __syncwarp();
   } else {
-    // ------------------------------------------------ epilogue warps 2..5
+    // ------------------------------------------------ epilogue warps 2..9
     const int quarter = warp & 3;  // TMEM lanes this warp may access
     int local = 0;
     for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x, ++local) {
@@ -517,7 +533,7 @@ __global__ void __launch_bounds__(THREADS, 1)
       const int row = mb * BM + quarter * 32 + lane;
       const uint32_t taddr = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) +
                              static_cast<uint32_t>(buf * BN);
-      epilogue_tile<BN, EPI>(p, b, row, row < p.M, nb * BN, nb, taddr);
+      epilogue_tile<BN, EPI>(p, b, row, row < p.M, nb * BN, nb, taddr, (warp - 2) >> 2);
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&tempty[buf]);
@@ -645,7 +661,7 @@ __device__ __forceinline__ void decode_pair_tile(const Params& p, int tile, int&
 }
 
 template <int EPI, bool AMN, bool BMN>
-__global__ void __launch_bounds__(THREADS, 1)
+__global__ void __launch_bounds__(threads_for<EPI>(), 1)
     tc_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                         const Params p) {
   using L = PairLayout;
@@ -675,7 +691,7 @@ __global__ void __launch_bounds__(THREADS, 1)
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&tfull[i], 1);
-      mbar_init(&tempty[i], 8);  // leader: 4 epilogue warps x 2 CTAs
+      mbar_init(&tempty[i], 2 * epi_warps<EPI>());  // leader: the epilogue warps of both CTAs
     }
     mbar_init(drain, 1);
     *abort_flag = 0;
@@ -830,7 +846,7 @@ __global__ void __launch_bounds__(THREADS, 1)
     }
     __syncwarp();
   } else {
-    // ------------------------------------------------ epilogue warps 2..5 (both CTAs)
+    // ------------------------------------------------ epilogue warps 2..9 (both CTAs)
     const int quarter = warp & 3;
     const uint32_t leader_tempty0 = map_to_rank(smem_u32(&tempty[0]), 0);
     const uint32_t leader_tempty1 = map_to_rank(smem_u32(&tempty[1]), 0);
@@ -854,7 +870,7 @@ __global__ void __launch_bounds__(THREADS, 1)
       const int row = mp * 256 + static_cast<int>(rank) * 128 + quarter * 32 + lane;
       const uint32_t taddr = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) +
                              static_cast<uint32_t>(buf * BN);
-      epilogue_tile<BN, EPI>(p, b, row, row < p.M, nb * BN, nb, taddr);
+      epilogue_tile<BN, EPI>(p, b, row, row < p.M, nb * BN, nb, taddr, (warp - 2) >> 2);
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive_cluster(buf ? leader_tempty1 : leader_tempty0);
@@ -986,7 +1002,7 @@ static int launch_inst(const GemmSpec& s, LaunchCtx& ctx) {
   if (tiles <= 0 || p.k_blocks <= 0) return TP_ERR_INVALID;
   const int grid = static_cast<int>(tiles < ctx.num_sms ? tiles : ctx.num_sms);
   if (ctx.before) ctx.before(ctx.user, s.name);
-  kern<<<grid, THREADS, L::SMEM, ctx.stream>>>(ta, tb, p);
+  kern<<<grid, threads_for<EPI>(), L::SMEM, ctx.stream>>>(ta, tb, p);
   if (ctx.after) ctx.after(ctx.user);
   ctx.launches++;
   return cudaPeekAtLastError() == cudaSuccess ? 0 : TP_ERR_CUDA;
@@ -1052,7 +1068,7 @@ static int launch_pair(const GemmSpec& s, LaunchCtx& ctx) {
   attr[0].val.clusterDim.x = 2;
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
-  cfg.blockDim = dim3(THREADS, 1, 1);
+  cfg.blockDim = dim3(threads_for<EPI>(), 1, 1);
   cfg.dynamicSmemBytes = L::SMEM;
   cfg.stream = ctx.stream;
   cfg.attrs = attr;
