@@ -154,14 +154,20 @@ def _device_inputs(w, dev, seed):
     import torch
     gen = torch.Generator(device=dev)
     gen.manual_seed(seed)
+    dt = torch.float32 if w.dtype == "f32" else torch.bfloat16
 
     def draw(shape, std):
         t = torch.randn(*shape, generator=gen, device=dev, dtype=torch.float32)
-        return (t * std).to(torch.bfloat16)
+        return (t * std).to(dt)
 
-    out = {"x": draw((w.N, w.d), 1.0), "W1": draw((w.d_ff, w.d), w.d ** -0.5)}
-    out["W3"] = draw((w.d_ff, w.d), w.d ** -0.5) if w.act == "swiglu" else None
-    out["W2"] = draw((w.d, w.d_ff), w.d_ff ** -0.5)
+    s1 = w.w_std if w.w_std is not None else w.d ** -0.5
+    s2 = w.w_std if w.w_std is not None else w.d_ff ** -0.5
+    out = {"x": draw((w.N, w.d_in), 1.0)}
+    out["W1"] = draw((w.d_ff, w.d), s1) if w.act != "none" else None
+    out["W3"] = draw((w.d_ff, w.d), s1) if w.act == "swiglu" else None
+    out["W2"] = draw((w.d, w.d_ff), s2)
+    out["b1"] = draw((w.d_ff,), w.b_std) if w.bias else None
+    out["b2"] = draw((w.d,), w.b_std) if w.bias else None
     out["dy"] = None if w.fwd_only else draw((w.N, w.d), 1.0)
     return out
 
@@ -298,6 +304,8 @@ def run_ours(args, ctx):
     d2h = (y.numel() + dx.numel()) * 2
 
     decode = run_decode(args, ctx, dev, peaks) if not args.no_decode else None
+    standalone = run_standalone_sum(dev, 10, peaks) if not args.no_extras else None
+    workloads = run_all_workloads(dev, 10) if not args.no_extras else None
 
     value = ctx["world"] * flop_step / (ms * 1e-3) / 1e12
     line = {
@@ -318,10 +326,104 @@ def run_ours(args, ctx):
         "gpu_launches": gpu_launches,
         "clocks": clk.summary(),
         "decode": decode,
+        "standalone_shard_sum": standalone,
+        "workloads": workloads,
     }
     if ctx["rank"] == 0 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(w, budget_s=args.cpu_budget)
     return line
+
+
+def time_workload(w, dev, steps, fused, seed=0):
+    """fwd and bwd of one workload through the C ABI: ms per call (CUDA
+    events on the calling stream) and the per-kernel times of the last call."""
+    import torch
+    from megatron_tensor_transformer_w1_gb300 import tpffn as abi
+    from megatron_tensor_transformer_w1_gb300.ffn import TensorParallelFFN
+    inp = _device_inputs(w, dev, 20260000 + w.seed_index + seed)
+    if w.act == "none":
+        ffn = TensorParallelFFN(w.d, w.d_ff, w.T_p, "none", w.dtype, device=dev, n_heads=w.n_heads,
+                                n_kv_heads=w.n_kv_heads, head_dim=w.head_dim)
+    else:
+        ffn = TensorParallelFFN(w.d, w.d_ff, w.T_p, w.act, w.dtype, device=dev)
+    st = torch.cuda.current_stream(dev)
+    w13p, w2p = ffn.pack(inp["W1"], inp["W2"], inp["W3"])
+    res = {}
+
+    def timed(fn):
+        for _ in range(3):
+            fn(0)
+        torch.cuda.synchronize(dev)
+        abi.tp_ffn_kernel_times(ffn.plan, 0)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(st)
+        for _ in range(steps):
+            fn(abi.TP_FLAG_TIMING)
+        e1.record(st)
+        torch.cuda.synchronize(dev)
+        per = {}
+        for name, t in abi.tp_ffn_kernel_times(ffn.plan, 100000):
+            per.setdefault(name, []).append(t)
+        return e0.elapsed_time(e1) / steps, {k: round(sum(v) / len(v), 4) for k, v in per.items()}
+
+    out = {}
+    f = abi.TP_SUM_FUSED if fused else 0
+    saved = None if w.fwd_only or w.act == "none" else torch.empty(
+        abi.tp_ffn_saved_bytes(ffn.plan, w.N), dtype=torch.uint8, device=dev)
+    ws = ffn.workspace(w.N, f)
+    y = torch.empty(w.N, w.d, dtype=ffn.torch_dtype, device=dev)
+
+    def fwd(extra):
+        abi.check(abi.tp_ffn_fwd(ffn.plan, w.N, inp["x"], w13p, w2p, inp["b1"], inp["b2"], y, None, saved, ws,
+                                 ws.numel(), f | extra, st), "fwd")
+
+    out["fwd_ms"], out["fwd_kernels"] = timed(fwd)
+    out["fwd_tflops"] = round(w.fwd_flops() / (out["fwd_ms"] * 1e-3) / 1e12, 3)
+    if not w.fwd_only:
+        dx = torch.empty(w.N, w.d_in, dtype=ffn.torch_dtype, device=dev)
+        dw13p = None if w13p is None else torch.empty_like(w13p)
+        dw2p = torch.empty_like(w2p)
+        db1 = torch.empty(w.d_ff, dtype=ffn.torch_dtype, device=dev) if w.bias and w.act == "gelu_tanh" else None
+        db2 = torch.empty(w.d, dtype=ffn.torch_dtype, device=dev) if w.bias else None
+
+        def bwd(extra):
+            abi.check(abi.tp_ffn_bwd(ffn.plan, w.N, inp["x"], w13p, w2p, saved, inp["dy"], dx, None, dw13p, dw2p,
+                                     db1, db2, ws, ws.numel(), f | extra, st), "bwd")
+
+        out["bwd_ms"], out["bwd_kernels"] = timed(bwd)
+        out["bwd_tflops"] = round(w.bwd_flops() / (out["bwd_ms"] * 1e-3) / 1e12, 3)
+    out["fwd_ms"] = round(out["fwd_ms"], 4)
+    if "bwd_ms" in out:
+        out["bwd_ms"] = round(out["bwd_ms"], 4)
+    return out
+
+
+def run_all_workloads(dev, steps):
+    """fwd and bwd throughput of every workload (fused shard-sum), plus the
+    standalone shard-sum kernel of the Llama-3-8B workload in HBM GB/s."""
+    from synth import WORKLOADS
+    table = {}
+    for name, w in WORKLOADS.items():
+        table[name] = time_workload(w, dev, steps, fused=not w.fwd_only)
+        if w.fwd_only:
+            nbytes = w.weight_bytes() + 2 * w.N * w.d * 2
+            table[name]["fwd_hbm_gbs"] = round(nbytes / (table[name]["fwd_ms"] * 1e-3) / 1e9, 1)
+    return table
+
+
+def run_standalone_sum(dev, steps, peaks):
+    from synth import WORKLOADS
+    w = WORKLOADS[MAIN]
+    r = time_workload(w, dev, steps, fused=False)
+    nbytes = w.T_p * w.N * w.d * 4 + w.N * w.d * 2  # fp32 partials read + bf16 result written
+    out = {"workload": MAIN, "fwd_ms": r["fwd_ms"], "bwd_ms": r["bwd_ms"],
+           "step_tflops_fwd_bwd": round((w.fwd_flops() + w.bwd_flops()) / ((r["fwd_ms"] + r["bwd_ms"]) * 1e-3) / 1e12, 2)}
+    for k, ms in list(r["fwd_kernels"].items()) + list(r["bwd_kernels"].items()):
+        if k.startswith("shard_sum"):
+            gbs = nbytes / (ms * 1e-3) / 1e9
+            out[k] = {"ms": ms, "bytes": nbytes, "achieved_gbs": round(gbs, 1), "peak_gbs": peaks["hbm"],
+                      "frac": round(gbs / peaks["hbm"], 4)}
+    return out
 
 
 def run_decode(args, ctx, dev, peaks):
@@ -462,6 +564,7 @@ def main():
     ap.add_argument("--sum", choices=["fused", "standalone"], default="fused")
     ap.add_argument("--no-decode", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-extras", action="store_true", help="skip the per-workload table and standalone-sum line")
     ap.add_argument("--cpu-budget", type=float, default=15.0)
     ap.add_argument("--tokens", type=int, default=0, help="override the token count (profiler captures)")
     args = ap.parse_args()
