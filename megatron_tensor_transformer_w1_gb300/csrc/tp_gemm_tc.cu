@@ -651,7 +651,9 @@ __device__ __forceinline__ void decode_pair_tile(const Params& p, int tile, int&
   const int tpb = tiles_m2 * p.tiles_n;
   b = tile / tpb;
   const int r = tile - b * tpb;
-  constexpr int GM = 4;
+  // 8 pair-rows per raster group: about 8 x 9.5 tiles run at once, so each K
+  // step fetches ~17.5 distinct operand blocks from DRAM (4 x 19: ~23).
+  constexpr int GM = 8;
   const int group = r / (GM * p.tiles_n);
   const int first_m = group * GM;
   const int gm = min(tiles_m2 - first_m, GM);
