@@ -37,10 +37,19 @@ METRIC = "TP-FFN fwd+bwd TFLOP/s & % BF16 tensor peak; decode-path HBM GB/s"
 MAIN = "llama3_8b_swiglu_bf16"
 DECODE = "llama3_70b_decode_swiglu_bf16"
 
-# DRAM bytes per launch from ncu captures (dram__bytes_read.sum +
-# dram__bytes_write.sum), by kernel name; None until captured for the current
-# kernel code.  Sources are the summaries under profiles/.
-NCU_TRAFFIC = {}
+# DRAM bytes per launch (dram__bytes_read.sum + dram__bytes_write.sum) from
+# one ncu capture of the Llama-3-8B step at full size (8192 tokens, fused
+# sums, two-SM pair GEMMs, raster groups of 8); see
+# profiles/llama3_8b_swiglu_gemm_dram_traffic.md.  To be cleared when the
+# kernels change.
+NCU_TRAFFIC = {
+    "up_swiglu": 1.17e9 + 679.34e6,
+    "down_fused_sum": 1.05e9 + 59.80e6,
+    "dgrad_h_swiglu": 1.48e9 + 447.41e6,
+    "dgrad_x_fused_sum": 2.10e9 + 60.07e6,
+    "wgrad_w2": 1.19e9 + 108.54e6,
+    "wgrad_w13": 2.22e9 + 224.73e6,
+}
 
 
 def _peaks():

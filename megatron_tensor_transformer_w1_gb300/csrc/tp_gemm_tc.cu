@@ -75,6 +75,7 @@ struct Params {
   int* err;
   unsigned long long timeout_ns;
   int debug_skip;
+  int dbg_slot;  // launch slot of the optional wait counters (instrumented builds only)
 };
 
 // ------------------------------------------------------------ PTX wrappers
@@ -624,9 +625,10 @@ __device__ __forceinline__ void umma_commit_pair_local(uint64_t* bar) {  // arri
 // Per-CTA cycle counters for performance investigations (not in normal builds):
 // [0] MMA wait on full, [1] MMA wait on tempty, [2] MMA thread total,
 // [3] producer wait on empty, [4] epilogue wait on tfull, [5] epilogue total, [6] k-iterations
-__device__ unsigned long long g_tpffn_dbg[1024][8];
+__device__ unsigned long long g_tpffn_dbg[8][256][8];  // [launch slot][CTA][counter]
 #define DBG_T0() const long long _t0 = clock64()
-#define DBG_ADD(slot, since) atomicAdd(&g_tpffn_dbg[blockIdx.x & 1023][slot], (unsigned long long)(clock64() - (since)))
+#define DBG_ADD(slot, since) \
+  atomicAdd(&g_tpffn_dbg[p.dbg_slot & 7][blockIdx.x & 255][slot], (unsigned long long)(clock64() - (since)))
 #else
 #define DBG_T0()
 #define DBG_ADD(slot, since)
@@ -822,7 +824,7 @@ __global__ void __launch_bounds__(threads_for<EPI>(), 1)
             }
           }
 #ifdef TPFFN_INSTRUMENT
-          atomicAdd(&g_tpffn_dbg[blockIdx.x & 1023][6], 1ull);
+          atomicAdd(&g_tpffn_dbg[p.dbg_slot & 7][blockIdx.x & 255][6], 1ull);
 #endif
           tc_fence_after();
           const uint32_t a_addr = smem_u32(smem + stage * L::STAGE_BYTES);
@@ -1051,6 +1053,10 @@ static int launch_pair(const GemmSpec& s, LaunchCtx& ctx) {
   p.timeout_ns = ctx.timeout_ns;
   p.debug_skip = ctx.debug_skip_load;
   ctx.debug_skip_load = 0;
+#ifdef TPFFN_INSTRUMENT
+  static int dbg_launch = 0;
+  p.dbg_slot = dbg_launch++ & 7;
+#endif
 
   auto kern = tc_gemm_pair_kernel<EPI, AMN, BMN>;
   static std::atomic<uint32_t> attr_done{0};
@@ -1102,7 +1108,7 @@ static int launch_pair(const GemmSpec& s, LaunchCtx& ctx) {
 extern "C" __attribute__((visibility("default"))) int tpffn_debug_counters(unsigned long long* host, int clear) {
   if (cudaMemcpyFromSymbol(host, tc::g_tpffn_dbg, sizeof(tc::g_tpffn_dbg)) != cudaSuccess) return 1;
   if (clear) {
-    static unsigned long long zeros[1024][8];
+    static unsigned long long zeros[8][256][8];
     if (cudaMemcpyToSymbol(tc::g_tpffn_dbg, zeros, sizeof(zeros)) != cudaSuccess) return 1;
   }
   return 0;
