@@ -343,7 +343,7 @@ def run_ours(args, ctx):
     return line
 
 
-def time_workload(w, dev, steps, fused, seed=0):
+def time_workload(w, dev, steps, fused, seed=0, overlap=False):
     """fwd and bwd of one workload through the C ABI: ms per call (CUDA
     events on the calling stream) and the per-kernel times of the last call."""
     import torch
@@ -376,7 +376,7 @@ def time_workload(w, dev, steps, fused, seed=0):
         return e0.elapsed_time(e1) / steps, {k: round(sum(v) / len(v), 4) for k, v in per.items()}
 
     out = {}
-    f = abi.TP_SUM_FUSED if fused else 0
+    f = (abi.TP_SUM_FUSED if fused else 0) | (abi.TP_SUM_OVERLAP if overlap else 0)
     saved = None if w.fwd_only or w.act == "none" else torch.empty(
         abi.tp_ffn_saved_bytes(ffn.plan, w.N), dtype=torch.uint8, device=dev)
     ws = ffn.workspace(w.N, f)
@@ -421,12 +421,23 @@ def run_all_workloads(dev, steps):
 
 
 def run_standalone_sum(dev, steps, peaks):
+    """The standalone shard-sum kernel in HBM GB/s, and how much of it the
+    overlapped variant (TP_SUM_OVERLAP) hides behind the row-sharded GEMM."""
     from synth import WORKLOADS
     w = WORKLOADS[MAIN]
     r = time_workload(w, dev, steps, fused=False)
+    o = time_workload(w, dev, steps, fused=False, overlap=True)
     nbytes = w.T_p * w.N * w.d * 4 + w.N * w.d * 2  # fp32 partials read + bf16 result written
     out = {"workload": MAIN, "fwd_ms": r["fwd_ms"], "bwd_ms": r["bwd_ms"],
-           "step_tflops_fwd_bwd": round((w.fwd_flops() + w.bwd_flops()) / ((r["fwd_ms"] + r["bwd_ms"]) * 1e-3) / 1e12, 2)}
+           "step_tflops_fwd_bwd": round((w.fwd_flops() + w.bwd_flops()) / ((r["fwd_ms"] + r["bwd_ms"]) * 1e-3) / 1e12, 2),
+           "overlap": {"fwd_ms": o["fwd_ms"], "bwd_ms": o["bwd_ms"],
+                       "step_tflops_fwd_bwd": round((w.fwd_flops() + w.bwd_flops()) /
+                                                    ((o["fwd_ms"] + o["bwd_ms"]) * 1e-3) / 1e12, 2)}}
+    sums = sum(ms for k, ms in list(r["fwd_kernels"].items()) + list(r["bwd_kernels"].items())
+               if k.startswith("shard_sum"))
+    if sums > 0:
+        out["overlap"]["hidden_fraction_of_shard_sum"] = round(
+            ((r["fwd_ms"] + r["bwd_ms"]) - (o["fwd_ms"] + o["bwd_ms"])) / sums, 3)
     for k, ms in list(r["fwd_kernels"].items()) + list(r["bwd_kernels"].items()):
         if k.startswith("shard_sum"):
             gbs = nbytes / (ms * 1e-3) / 1e9

@@ -88,6 +88,17 @@ enum {
                              report device-side errors as the return value   */
   TP_FLAG_TIMING = 4,     /* record CUDA events around every kernel of the
                              call (read with tp_ffn_kernel_times)            */
+  TP_SUM_OVERLAP = 8,     /* standalone sum overlapped with compute: the
+                             row-sharded GEMM and the shard-sum run in 4 token
+                             chunks, the sum of chunk i on a second stream
+                             (owned by the plan) while the GEMM of chunk i+1
+                             runs on the call's stream; the call's stream waits
+                             for the last sum before anything later on it.
+                             Results are bit-identical to TP_SUM_STANDALONE.
+                             TP_ERR_INVALID together with TP_SUM_FUSED.
+                             This puts on the device the "hidden behind
+                             compute" argument of "7.9 Tensor and pipeline
+                             parallelism (TP, PP)", §2.4-2.5              */
   TP_FLAG_DEBUG_SKIP_LOAD = 1 << 16  /* test hook: the first tensor-core GEMM
                              of the call never issues its first operand load,
                              so its consumer's bounded wait expires and the

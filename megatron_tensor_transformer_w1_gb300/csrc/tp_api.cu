@@ -20,6 +20,7 @@
 
 #include <atomic>
 #include <cstdint>
+#include <cstdlib>
 #include <cstring>
 #include <mutex>
 #include <new>
@@ -46,6 +47,12 @@ struct tp_ffn_plan {
   mutable int n_events = 0;
   mutable int last_launches = 0;
   mutable cudaStream_t timing_stream = nullptr;
+  // second stream and events of the overlapped shard-sum (host handles,
+  // created on first use on a device; not thread-safe)
+  mutable int ov_device = -1;
+  mutable cudaStream_t ov_stream = nullptr;
+  mutable std::vector<cudaEvent_t> ov_events;
+  mutable cudaEvent_t ov_join = nullptr;
 };
 
 namespace {
@@ -121,7 +128,7 @@ SavedLayout saved_layout(const tp_ffn_plan* p, int64_t n) {
 }
 
 // Timing hooks: an event pair per launch, kept in the plan.
-void timing_before(void* user, const char* name) {
+void timing_before(void* user, const char* name, cudaStream_t stream) {
   const tp_ffn_plan* p = static_cast<const tp_ffn_plan*>(user);
   if (p->n_events >= static_cast<int>(p->events.size())) {
     TimingRec r{name, nullptr, nullptr};
@@ -131,11 +138,11 @@ void timing_before(void* user, const char* name) {
   }
   TimingRec& r = p->events[p->n_events];
   r.name = name;
-  cudaEventRecord(r.start, p->timing_stream);
+  cudaEventRecord(r.start, stream);
 }
-void timing_after(void* user) {
+void timing_after(void* user, cudaStream_t stream) {
   const tp_ffn_plan* p = static_cast<const tp_ffn_plan*>(user);
-  cudaEventRecord(p->events[p->n_events].stop, p->timing_stream);
+  cudaEventRecord(p->events[p->n_events].stop, stream);
   p->n_events++;
 }
 
@@ -165,6 +172,77 @@ int finish_call(const tp_ffn_plan* p, LaunchCtx& ctx, int rc, int flags, void* w
 
 int run_gemm(const tp_ffn_plan* p, const GemmSpec& g, LaunchCtx& ctx) {
   return p->dtype == TP_BF16 ? launch_tc_gemm(g, ctx) : launch_simt_gemm(g, ctx);
+}
+
+// Token chunks of the overlapped sum.  Measured on GB300 (Llama-3-8B step):
+// 1, 2 and 4 chunks all lose to the plain standalone path, because the
+// persistent GEMM already holds every SM and the sum is HBM-bound either way.
+constexpr int kOverlapChunks = 4;
+
+void release_overlap(const tp_ffn_plan* p) {
+  for (cudaEvent_t e : p->ov_events) cudaEventDestroy(e);
+  p->ov_events.clear();
+  if (p->ov_join) cudaEventDestroy(p->ov_join);
+  if (p->ov_stream) cudaStreamDestroy(p->ov_stream);
+  p->ov_join = nullptr;
+  p->ov_stream = nullptr;
+  p->ov_device = -1;
+}
+
+int ensure_overlap(const tp_ffn_plan* p) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return TP_ERR_CUDA;
+  if (p->ov_device == dev && p->ov_stream) return TP_OK;
+  release_overlap(p);
+  if (cudaStreamCreateWithFlags(&p->ov_stream, cudaStreamNonBlocking) != cudaSuccess) return TP_ERR_CUDA;
+  for (int i = 0; i < kOverlapChunks; ++i) {
+    cudaEvent_t e;
+    if (cudaEventCreateWithFlags(&e, cudaEventDisableTiming) != cudaSuccess) return TP_ERR_CUDA;
+    p->ov_events.push_back(e);
+  }
+  if (cudaEventCreateWithFlags(&p->ov_join, cudaEventDisableTiming) != cudaSuccess) return TP_ERR_CUDA;
+  p->ov_device = dev;
+  return TP_OK;
+}
+
+// Row-sharded GEMM into fp32 partials followed by the ordered shard-sum,
+// split into token chunks: the sum of chunk i runs on the plan's second
+// stream while the GEMM of chunk i+1 runs on the call's stream.  `g` is the
+// whole-problem spec (NB = T_p, EPI_F32, out = partials [T_p][n][d]) whose A
+// operand has the tokens as rows; chunk results are bit-identical to the
+// unchunked path (same per-element arithmetic).
+int gemm_sum_overlapped(const tp_ffn_plan* p, const GemmSpec& g, LaunchCtx& ctx, float* part, int64_t n,
+                        int64_t d, const void* bias, void* out, int out_bf16, const char* sum_name) {
+  int rc = ensure_overlap(p);
+  if (rc) return rc;
+  const size_t esz_in = p->dtype == TP_BF16 ? 2 : 4;
+  const int64_t per = ((n + kOverlapChunks - 1) / kOverlapChunks + 255) / 256 * 256;
+  int i = 0;
+  for (int64_t r0 = 0; r0 < n; r0 += per, ++i) {
+    const int64_t rows = (n - r0) < per ? (n - r0) : per;
+    GemmSpec c = g;
+    c.M = rows;
+    c.A.rows = rows;
+    c.A.ptr = static_cast<const char*>(g.A.ptr) + static_cast<size_t>(r0) * g.A.row_stride * esz_in;
+    c.out = part + r0 * d;
+    rc = run_gemm(p, c, ctx);
+    if (rc) return rc;
+    if (cudaEventRecord(p->ov_events[i], ctx.stream) != cudaSuccess ||
+        cudaStreamWaitEvent(p->ov_stream, p->ov_events[i], 0) != cudaSuccess)
+      return TP_ERR_CUDA;
+    LaunchCtx actx = ctx;
+    actx.stream = p->ov_stream;
+    actx.launches = 0;
+    rc = launch_shard_sum(part + r0 * d, p->T_p, rows, d, bias,
+                          static_cast<char*>(out) + static_cast<size_t>(r0) * d * (out_bf16 ? 2 : 4), out_bf16,
+                          actx, sum_name, n * d);
+    ctx.launches += actx.launches;
+    if (rc) return rc;
+  }
+  if (cudaEventRecord(p->ov_join, p->ov_stream) != cudaSuccess ||
+      cudaStreamWaitEvent(ctx.stream, p->ov_join, 0) != cudaSuccess)
+    return TP_ERR_CUDA;
+  return TP_OK;
 }
 
 Operand kmajor(const void* ptr, int64_t inner, int64_t rows, int64_t batch, int64_t rs, int64_t bs, int bsel,
@@ -253,6 +331,7 @@ int tp_attn_out_plan_create(tp_ffn_plan** out, int64_t d_model, int n_heads, int
 
 void tp_ffn_plan_destroy(tp_ffn_plan* plan) {
   if (!plan) return;
+  release_overlap(plan);
   for (auto& r : plan->events) {
     if (r.start) cudaEventDestroy(r.start);
     if (r.stop) cudaEventDestroy(r.stop);
@@ -329,6 +408,7 @@ int tp_ffn_fwd(const tp_ffn_plan* p, int64_t n, const void* x, const void* w13p,
   if (!x || !w2p || !y || !workspace) return TP_ERR_INVALID;
   if (!none && !w13p) return TP_ERR_INVALID;
   if (fused && partials) return TP_ERR_INVALID;
+  if (fused && (flags & TP_SUM_OVERLAP)) return TP_ERR_INVALID;
   if (b1 && p->act != TP_ACT_GELU_TANH) return TP_ERR_UNSUPPORTED;
   if (n > (int64_t(1) << 30)) return TP_ERR_UNSUPPORTED;
   const WsLayout L = ws_layout(p, n, flags);
@@ -417,8 +497,12 @@ int tp_ffn_fwd(const tp_ffn_plan* p, int64_t n, const void* x, const void* w13p,
     g.out = part;
     g.out_bs = n * d;
     g.out_rs = d;
-    rc = run_gemm(p, g, ctx);
-    if (!rc) rc = launch_shard_sum(part, static_cast<int>(T), n, d, b2, y, out_bf16, ctx, "shard_sum_y");
+    if (flags & TP_SUM_OVERLAP) {
+      rc = gemm_sum_overlapped(p, g, ctx, part, n, d, b2, y, out_bf16, "shard_sum_y");
+    } else {
+      rc = run_gemm(p, g, ctx);
+      if (!rc) rc = launch_shard_sum(part, static_cast<int>(T), n, d, b2, y, out_bf16, ctx, "shard_sum_y");
+    }
   }
   return finish_call(p, ctx, rc, flags, workspace);
 }
@@ -436,6 +520,7 @@ int tp_ffn_bwd(const tp_ffn_plan* p, int64_t n, const void* x, const void* w13p,
   if (!x || !w2p || !dy || !dx || !dw2p || !workspace) return TP_ERR_INVALID;
   if (!none && (!w13p || !saved || !dw13p)) return TP_ERR_INVALID;
   if ((fused || none) && dx_partials) return TP_ERR_INVALID;
+  if (fused && (flags & TP_SUM_OVERLAP)) return TP_ERR_INVALID;
   if (db1 && p->act != TP_ACT_GELU_TANH) return TP_ERR_UNSUPPORTED;
   if (n > (int64_t(1) << 30)) return TP_ERR_UNSUPPORTED;
   const WsLayout L = ws_layout(p, n, flags);
@@ -553,8 +638,12 @@ int tp_ffn_bwd(const tp_ffn_plan* p, int64_t n, const void* x, const void* w13p,
       g.out = part;
       g.out_bs = n * d;
       g.out_rs = d;
-      rc = run_gemm(p, g, ctx);
-      if (!rc) rc = launch_shard_sum(part, static_cast<int>(T), n, d, nullptr, dx, out_bf16, ctx, "shard_sum_dx");
+      if (flags & TP_SUM_OVERLAP) {
+        rc = gemm_sum_overlapped(p, g, ctx, part, n, d, nullptr, dx, out_bf16, "shard_sum_dx");
+      } else {
+        rc = run_gemm(p, g, ctx);
+        if (!rc) rc = launch_shard_sum(part, static_cast<int>(T), n, d, nullptr, dx, out_bf16, ctx, "shard_sum_dx");
+      }
     }
     if (rc) return finish_call(p, ctx, rc, flags, workspace);
   }

@@ -1005,9 +1005,9 @@ static int launch_inst(const GemmSpec& s, LaunchCtx& ctx) {
   const long long tiles = static_cast<long long>(p.tiles_m) * p.tiles_n * p.NB;
   if (tiles <= 0 || p.k_blocks <= 0) return TP_ERR_INVALID;
   const int grid = static_cast<int>(tiles < ctx.num_sms ? tiles : ctx.num_sms);
-  if (ctx.before) ctx.before(ctx.user, s.name);
+  if (ctx.before) ctx.before(ctx.user, s.name, ctx.stream);
   kern<<<grid, threads_for<EPI>(), L::SMEM, ctx.stream>>>(ta, tb, p);
-  if (ctx.after) ctx.after(ctx.user);
+  if (ctx.after) ctx.after(ctx.user, ctx.stream);
   ctx.launches++;
   return cudaPeekAtLastError() == cudaSuccess ? 0 : TP_ERR_CUDA;
 }
@@ -1095,9 +1095,9 @@ static int launch_pair(const GemmSpec& s, LaunchCtx& ctx) {
   if (tiles <= 0 || p.k_blocks <= 0) return TP_ERR_INVALID;
   const int clusters = static_cast<int>(tiles < mc ? tiles : mc);
   cfg.gridDim = dim3(2 * clusters, 1, 1);
-  if (ctx.before) ctx.before(ctx.user, s.name);
+  if (ctx.before) ctx.before(ctx.user, s.name, ctx.stream);
   cudaError_t e = cudaLaunchKernelEx(&cfg, kern, ta, tb, p);
-  if (ctx.after) ctx.after(ctx.user);
+  if (ctx.after) ctx.after(ctx.user, ctx.stream);
   ctx.launches++;
   return e == cudaSuccess && cudaPeekAtLastError() == cudaSuccess ? 0 : TP_ERR_CUDA;
 }

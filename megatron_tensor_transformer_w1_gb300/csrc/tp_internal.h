@@ -61,8 +61,8 @@ struct LaunchCtx {
   bool timing = false;
   int launches = 0;
   // timing records are appended by the caller through these hooks
-  void (*before)(void* user, const char* name) = nullptr;
-  void (*after)(void* user) = nullptr;
+  void (*before)(void* user, const char* name, cudaStream_t stream) = nullptr;
+  void (*after)(void* user, cudaStream_t stream) = nullptr;
   void* user = nullptr;
 };
 
@@ -80,9 +80,10 @@ int launch_pack_columns(const void* W1, const void* W3, void* out, int T_p, int6
                         cudaStream_t st);
 int launch_pack_rows(const void* W2, void* out, int T_p, int64_t s, int64_t s_pad, int64_t d,
                      int esz, int unpack, cudaStream_t st);
+// shard_stride: elements between consecutive shards' partials (0: rows*cols).
 int launch_shard_sum(const float* partials, int T_p, int64_t rows, int64_t cols,
                      const void* bias, void* out, int out_bf16, LaunchCtx& ctx,
-                     const char* name);
+                     const char* name, int64_t shard_stride = 0);
 // Column sums of a [batch][rows][cols] view (row stride rs, batch stride bs)
 // into out[b*out_bs + col] for col < cols, deterministic two-pass order.
 int launch_colsum(const void* in, int in_bf16, int64_t batch, int64_t rows, int64_t cols,

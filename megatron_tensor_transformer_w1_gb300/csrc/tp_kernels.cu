@@ -104,13 +104,13 @@ __global__ void pack_rows_kernel(const char* W2, char* out, long long s, long lo
 template <int OUT_BF16>
 __global__ void __launch_bounds__(256) shard_sum_vec8_kernel(const float* __restrict__ P, int T, long long plane,
                                                              long long cols, const __nv_bfloat16* bias_bf,
-                                                             const float* bias_f, void* out) {
+                                                             const float* bias_f, void* out, long long stride) {
   const long long n8 = plane / 8;
   for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < n8; i += (long long)gridDim.x * blockDim.x) {
     const float4* p0 = reinterpret_cast<const float4*>(P) + 2 * i;
     float4 a = __ldcs(p0), b = __ldcs(p0 + 1);
     for (int t = 1; t < T; ++t) {
-      const float4* pt = reinterpret_cast<const float4*>(P + t * plane) + 2 * i;
+      const float4* pt = reinterpret_cast<const float4*>(P + t * stride) + 2 * i;
       const float4 c = __ldcs(pt), e = __ldcs(pt + 1);
       a.x += c.x; a.y += c.y; a.z += c.z; a.w += c.w;
       b.x += e.x; b.y += e.y; b.z += e.z; b.w += e.w;
@@ -142,10 +142,10 @@ __global__ void __launch_bounds__(256) shard_sum_vec8_kernel(const float* __rest
 }
 
 __global__ void shard_sum_scalar_kernel(const float* P, int T, long long plane, long long cols, const void* bias,
-                                        int bias_bf16, void* out, int out_bf16) {
+                                        int bias_bf16, void* out, int out_bf16, long long stride) {
   for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < plane; i += (long long)gridDim.x * blockDim.x) {
     float acc = P[i];
-    for (int t = 1; t < T; ++t) acc += P[t * plane + i];
+    for (int t = 1; t < T; ++t) acc += P[t * stride + i];
     if (bias) acc += to_f(bias, i % cols, bias_bf16);
     from_f(out, i, acc, out_bf16);
   }
@@ -326,9 +326,9 @@ int launch_simt_gemm(const GemmSpec& s, LaunchCtx& ctx) {
   const long long cols = (s.epi == EPI_SWIGLU_FWD) ? s.N / 2 : s.N;
   const long long total = (long long)s.NB * s.M * cols;
   if (total <= 0) return 0;
-  if (ctx.before) ctx.before(ctx.user, s.name);
+  if (ctx.before) ctx.before(ctx.user, s.name, ctx.stream);
   simt_gemm_kernel<<<grid_for(total, 256, ctx.num_sms), 256, 0, ctx.stream>>>(p);
-  if (ctx.after) ctx.after(ctx.user);
+  if (ctx.after) ctx.after(ctx.user, ctx.stream);
   ctx.launches++;
   return cudaPeekAtLastError() == cudaSuccess ? 0 : TP_ERR_CUDA;
 }
@@ -354,25 +354,27 @@ int launch_pack_rows(const void* W2, void* out, int T_p, int64_t s, int64_t s_pa
 }
 
 int launch_shard_sum(const float* partials, int T_p, int64_t rows, int64_t cols, const void* bias, void* out,
-                     int out_bf16, LaunchCtx& ctx, const char* name) {
+                     int out_bf16, LaunchCtx& ctx, const char* name, int64_t shard_stride) {
   const long long plane = (long long)rows * cols;
   if (plane <= 0) return 0;
-  if (ctx.before) ctx.before(ctx.user, name);
+  const long long stride = shard_stride > 0 ? shard_stride : plane;
+  if (ctx.before) ctx.before(ctx.user, name, ctx.stream);
   const bool vec = (cols % 8 == 0) && (reinterpret_cast<uintptr_t>(partials) % 16 == 0) &&
                    (reinterpret_cast<uintptr_t>(out) % 16 == 0);
   if (vec) {
     const int grid = grid_for(plane / 8, 256, ctx.num_sms);
     if (out_bf16)
       shard_sum_vec8_kernel<1><<<grid, 256, 0, ctx.stream>>>(partials, T_p, plane, cols,
-                                                            static_cast<const __nv_bfloat16*>(bias), nullptr, out);
+                                                            static_cast<const __nv_bfloat16*>(bias), nullptr, out,
+                                                            stride);
     else
       shard_sum_vec8_kernel<0><<<grid, 256, 0, ctx.stream>>>(partials, T_p, plane, cols, nullptr,
-                                                            static_cast<const float*>(bias), out);
+                                                            static_cast<const float*>(bias), out, stride);
   } else {
-    shard_sum_scalar_kernel<<<grid_for(plane, 256, ctx.num_sms), 256, 0, ctx.stream>>>(partials, T_p, plane, cols,
-                                                                                     bias, out_bf16, out, out_bf16);
+    shard_sum_scalar_kernel<<<grid_for(plane, 256, ctx.num_sms), 256, 0, ctx.stream>>>(
+        partials, T_p, plane, cols, bias, out_bf16, out, out_bf16, stride);
   }
-  if (ctx.after) ctx.after(ctx.user);
+  if (ctx.after) ctx.after(ctx.user, ctx.stream);
   ctx.launches++;
   return cudaPeekAtLastError() == cudaSuccess ? 0 : TP_ERR_CUDA;
 }
@@ -387,7 +389,7 @@ int launch_colsum(const void* in, int in_bf16, int64_t batch, int64_t rows, int6
                   const char* name) {
   if (batch <= 0 || cols <= 0) return 0;
   const int64_t chunks = rows > 0 ? (rows + chunk_rows - 1) / chunk_rows : 0;
-  if (ctx.before) ctx.before(ctx.user, name);
+  if (ctx.before) ctx.before(ctx.user, name, ctx.stream);
   if (chunks > 0) {
     dim3 g1(static_cast<unsigned>((cols + 255) / 256), static_cast<unsigned>(chunks), static_cast<unsigned>(batch));
     colsum_pass1_kernel<<<g1, 256, 0, ctx.stream>>>(in, in_bf16, rows, cols, rs, bs, scratch, chunk_rows, chunks);
@@ -396,7 +398,7 @@ int launch_colsum(const void* in, int in_bf16, int64_t batch, int64_t rows, int6
   dim3 g2(static_cast<unsigned>((cols + 255) / 256), static_cast<unsigned>(batch));
   colsum_pass2_kernel<<<g2, 256, 0, ctx.stream>>>(scratch, cols, chunks, out, out_bf16, out_bs);
   ctx.launches++;
-  if (ctx.after) ctx.after(ctx.user);
+  if (ctx.after) ctx.after(ctx.user, ctx.stream);
   return cudaPeekAtLastError() == cudaSuccess ? 0 : TP_ERR_CUDA;
 }
 

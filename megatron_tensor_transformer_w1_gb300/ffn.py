@@ -78,9 +78,11 @@ class TensorParallelFFN:
         return W2
 
     # ------------------------------------------------------------ passes
-    def forward(self, x, w13p, w2p, b1=None, b2=None, save=True, fused=False, want_partials=False, flags=0):
+    def forward(self, x, w13p, w2p, b1=None, b2=None, save=True, fused=False, want_partials=False, flags=0,
+                overlap=False):
         n = x.shape[0]
         flags |= abi.TP_SUM_FUSED if fused else 0
+        flags |= abi.TP_SUM_OVERLAP if overlap else 0
         st = self._stream()
         y = torch.empty(n, self.d, dtype=self.torch_dtype, device=self.device)
         saved = self._bytes(abi.tp_ffn_saved_bytes(self.plan, n)) if save and self.act_name != "none" else None
@@ -90,9 +92,11 @@ class TensorParallelFFN:
                   "fwd")
         return y, saved, part
 
-    def backward(self, x, w13p, w2p, saved, dy, fused=False, want_partials=False, bias=False, flags=0):
+    def backward(self, x, w13p, w2p, saved, dy, fused=False, want_partials=False, bias=False, flags=0,
+                 overlap=False):
         n = dy.shape[0]
         flags |= abi.TP_SUM_FUSED if fused else 0
+        flags |= abi.TP_SUM_OVERLAP if overlap else 0
         st = self._stream()
         d_in = self.d_ff if self.act_name == "none" else self.d
         dx = torch.empty(n, d_in, dtype=self.torch_dtype, device=self.device)

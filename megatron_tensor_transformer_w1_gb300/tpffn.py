@@ -18,7 +18,7 @@ TP_OK, TP_ERR_INVALID, TP_ERR_UNSUPPORTED, TP_ERR_CUDA, TP_ERR_TIMEOUT, TP_ERR_A
 TP_ACT_NONE, TP_ACT_GELU_TANH, TP_ACT_SWIGLU = 0, 1, 2
 TP_F32, TP_BF16 = 0, 1
 TP_PACK_COLUMNS, TP_PACK_ROWS = 0, 1
-TP_SUM_STANDALONE, TP_SUM_FUSED, TP_FLAG_SYNC, TP_FLAG_TIMING = 0, 1, 2, 4
+TP_SUM_STANDALONE, TP_SUM_FUSED, TP_FLAG_SYNC, TP_FLAG_TIMING, TP_SUM_OVERLAP = 0, 1, 2, 4, 8
 TP_FLAG_DEBUG_SKIP_LOAD = 1 << 16
 
 ABI_FUNCTIONS = (

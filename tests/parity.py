@@ -73,7 +73,7 @@ def check(got, ref, rel, what, extra=None):
 
 
 # ------------------------------------------------------------------ GPU side
-def run_gpu_tensors(w, inp, fused=False, want_partials=True, backward=True):
+def run_gpu_tensors(w, inp, fused=False, want_partials=True, backward=True, overlap=False):
     """Runs pack + forward (+ backward) of workload `w` on cuda:0 through the
     C ABI; returns the device tensors (gradients unpacked to [out, in]) and
     the number of kernels the forward call launched."""
@@ -90,12 +90,13 @@ def run_gpu_tensors(w, inp, fused=False, want_partials=True, backward=True):
     w13p, w2p = ffn.pack(g["W1"], g["W2"], g["W3"])
     partials = want_partials and not fused
     y, saved, part = ffn.forward(g["x"], w13p, w2p, b1=g["b1"], b2=g["b2"], save=backward, fused=fused,
-                                 want_partials=partials)
+                                 want_partials=partials, overlap=overlap)
     n_fwd = abi.tp_ffn_last_launch_count(ffn.plan)
     out = dict(y=y, partials=part)
     if backward and g["dy"] is not None:
         gr = ffn.backward(g["x"], w13p, w2p, saved, g["dy"], fused=fused,
-                          want_partials=partials and w.act != "none", bias=w.bias)
+                          want_partials=partials and w.act != "none", bias=w.bias,
+                          overlap=overlap and w.act != "none")
         out.update(dx=gr["dx"], dx_partials=gr["dx_partials"], db1=gr["db1"], db2=gr["db2"])
         if w.act != "none":
             out["dW1"], out["dW3"] = ffn.unpack_columns(gr["dw13p"])
@@ -104,9 +105,9 @@ def run_gpu_tensors(w, inp, fused=False, want_partials=True, backward=True):
     return out, n_fwd
 
 
-def run_gpu(w, inp, fused=False, want_partials=True, backward=True):
+def run_gpu(w, inp, fused=False, want_partials=True, backward=True, overlap=False):
     """run_gpu_tensors, converted to float64 numpy (small workloads)."""
-    out, n_fwd = run_gpu_tensors(w, inp, fused, want_partials, backward)
+    out, n_fwd = run_gpu_tensors(w, inp, fused, want_partials, backward, overlap)
     assert n_fwd >= 1, "the forward pass launched no kernel of libtpffn.so"
     res = {k: (None if v is None else v.to(torch.float64).cpu().numpy()) for k, v in out.items()}
     res["_raw"] = {k: (None if v is None else v.cpu()) for k, v in out.items()}

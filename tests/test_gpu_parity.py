@@ -178,3 +178,30 @@ def test_bounded_wait_expires_and_context_survives():
     assert rc == abi.TP_OK
     rb, _ = oracle_problem(w, inp, round_bf16=True)
     check(y.double().cpu().numpy(), rb.forward_sharded()["y"], BF16_REL, "y after timeout")
+
+
+OVERLAP = [small_case(700, 264, 600, 3, "swiglu", seed=601),             # 3 token chunks of 256 (+ a ragged one)
+           small_case(1300, 192, 768, 4, "gelu_tanh", bias=True, seed=602),
+           _attn_case(600, 256, 6, 64, 3, 603)]
+
+
+@pytest.mark.parametrize("w", OVERLAP, ids=[w.name for w in OVERLAP])
+def test_overlapped_shard_sum_matches_oracle_and_is_bit_identical(w):
+    """TP_SUM_OVERLAP: the chunked GEMM + second-stream sum gives exactly the
+    standalone path's bits, and matches the oracle."""
+    inp = make_inputs(w)
+    ov = run_gpu(w, inp, overlap=True)["_raw"]
+    st = run_gpu(w, inp, overlap=False)["_raw"]
+    for k in ("y", "partials", "dx", "dx_partials"):
+        if st.get(k) is not None:
+            assert torch.equal(ov[k].view(torch.uint8), st[k].view(torch.uint8)), k
+    _full_compare_overlap(w, inp)
+
+
+def _full_compare_overlap(w, inp):
+    got = run_gpu(w, inp, overlap=True)
+    rb, f = oracle_problem(w, inp, round_bf16=True)
+    wts = rounding_weights(w, rb.hidden_dump(f["dy"])) if w.act != "none" else None
+    A = allowance_rows(w, f, wts) if wts is not None else {}
+    check(got["y"], rb.forward_sharded()["y"], BF16_REL, f"{w.name} overlap y", A.get("y"))
+    check(got["dx"], rb.backward_rows(f["dy"])["dx"], BF16_REL, f"{w.name} overlap dx", A.get("dx"))
