@@ -315,6 +315,7 @@ def run_ours(args, ctx):
     decode = run_decode(args, ctx, dev, peaks) if not args.no_decode else None
     standalone = run_standalone_sum(dev, 10, peaks) if not args.no_extras else None
     workloads = run_all_workloads(dev, 10) if not args.no_extras else None
+    seq_parallel = run_seq_parallel(dev, 10, peaks) if not args.no_extras else None
 
     value = ctx["world"] * flop_step / (ms * 1e-3) / 1e12
     line = {
@@ -337,6 +338,7 @@ def run_ours(args, ctx):
         "decode": decode,
         "standalone_shard_sum": standalone,
         "workloads": workloads,
+        "sequence_parallel": seq_parallel,
     }
     if ctx["rank"] == 0 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(w, budget_s=args.cpu_budget)
@@ -443,6 +445,73 @@ def run_standalone_sum(dev, steps, peaks):
             gbs = nbytes / (ms * 1e-3) / 1e9
             out[k] = {"ms": ms, "bytes": nbytes, "achieved_gbs": round(gbs, 1), "peak_gbs": peaks["hbm"],
                       "frac": round(gbs / peaks["hbm"], 4)}
+    return out
+
+
+def run_seq_parallel(dev, steps, peaks):
+    """Sequence-parallel forms of the Llama-3-8B workload: fwd and bwd ms with
+    per-rank token slices (all-gather + reduce-scatter), and the GB/s of the
+    gather and reduce-scatter kernels."""
+    import torch
+    from synth import WORKLOADS
+    from megatron_tensor_transformer_w1_gb300 import tpffn as abi
+    from megatron_tensor_transformer_w1_gb300.ffn import TensorParallelFFN
+    w = WORKLOADS[MAIN]
+    inp = _device_inputs(w, dev, 20260000 + w.seed_index + 7)
+    ffn = TensorParallelFFN(w.d, w.d_ff, w.T_p, w.act, "bf16", device=dev)
+    st = torch.cuda.current_stream(dev)
+    w13p, w2p = ffn.pack(inp["W1"], inp["W2"], inp["W3"])
+    T, ns = w.T_p, w.N // w.T_p
+    xs = [inp["x"][t * ns:(t + 1) * ns].clone() for t in range(T)]
+    dys = [inp["dy"][t * ns:(t + 1) * ns].clone() for t in range(T)]
+    ys = [torch.empty(ns, w.d, dtype=torch.bfloat16, device=dev) for _ in range(T)]
+    dxs = [torch.empty(ns, w.d, dtype=torch.bfloat16, device=dev) for _ in range(T)]
+    saved = torch.empty(abi.tp_ffn_saved_bytes(ffn.plan, w.N), dtype=torch.uint8, device=dev)
+    dw13p, dw2p = torch.empty_like(w13p), torch.empty_like(w2p)
+    out = {"workload": MAIN}
+    for mode, flags in (("reduce_scatter", 0), ("fused_then_scatter", abi.TP_SUM_FUSED)):
+        ws = torch.empty(abi.tp_ffn_seq_parallel_workspace_bytes(ffn.plan, w.N, flags), dtype=torch.uint8,
+                         device=dev)
+
+        def fwd(extra):
+            abi.check(abi.tp_ffn_fwd_seq_parallel(ffn.plan, w.N, xs, w13p, w2p, None, None, ys, saved, ws,
+                                                  ws.numel(), flags | extra, st), "fwd_sp")
+
+        def bwd(extra):
+            abi.check(abi.tp_ffn_bwd_seq_parallel(ffn.plan, w.N, xs, w13p, w2p, saved, dys, dxs, dw13p, dw2p, None,
+                                                  None, ws, ws.numel(), flags | extra, st), "bwd_sp")
+
+        res = {}
+        for name, fn in (("fwd", fwd), ("bwd", bwd)):
+            for _ in range(3):
+                fn(0)
+            torch.cuda.synchronize(dev)
+            abi.tp_ffn_kernel_times(ffn.plan, 0)
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(st)
+            for _ in range(steps):
+                fn(abi.TP_FLAG_TIMING)
+            e1.record(st)
+            torch.cuda.synchronize(dev)
+            res[name + "_ms"] = round(e0.elapsed_time(e1) / steps, 4)
+            per = {}
+            for k, t in abi.tp_ffn_kernel_times(ffn.plan, 100000):
+                per.setdefault(k, []).append(t)
+            for k, v in per.items():
+                ms = sum(v) / len(v)
+                if k.startswith("all_gather"):
+                    nbytes = 2 * w.N * w.d * 2  # read slices + write the gathered tensor
+                elif k.startswith("reduce_scatter"):
+                    nbytes = w.T_p * w.N * w.d * 4 + w.N * w.d * 2
+                elif k.startswith("scatter"):
+                    nbytes = 2 * w.N * w.d * 2
+                else:
+                    continue
+                res[k] = {"ms": round(ms, 4), "gbs": round(nbytes / (ms * 1e-3) / 1e9, 1),
+                          "frac_of_hbm": round(nbytes / (ms * 1e-3) / 1e9 / peaks["hbm"], 4)}
+        res["step_tflops_fwd_bwd"] = round((w.fwd_flops() + w.bwd_flops()) /
+                                           ((res["fwd_ms"] + res["bwd_ms"]) * 1e-3) / 1e12, 2)
+        out[mode] = res
     return out
 
 

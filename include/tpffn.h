@@ -230,6 +230,36 @@ TPFFN_API int tp_ffn_bwd(const tp_ffn_plan* plan, int64_t n_tokens, const void* 
                void* dw13p, void* dw2p, void* db1, void* db2, void* workspace,
                size_t workspace_bytes, int flags, tp_stream_t stream);
 
+/* ------------------------------------------------------- sequence parallel */
+
+/* Sequence-parallel forms ("7.9 Tensor and pipeline parallelism (TP, PP)",
+ * §2.5 "Sequence parallelism"; "Parallelism II: model", "Sequence and context
+ * parallelism"): outside the tensor-parallel region each of the T_p virtual
+ * ranks holds the token slice [t*n/T_p, (t+1)*n/T_p) of the activations, and
+ * the all-reduce becomes an all-gather before the column-sharded GEMM plus a
+ * reduce-scatter after the row-sharded GEMM (the same bytes).
+ *   x_slices, y_slices, dy_slices, dx_slices: host arrays of T_p device
+ *   pointers, slice t = [n/T_p][features] (features: d, or d_ff for act NONE
+ *   inputs and dx).  TP_ERR_INVALID unless n % T_p == 0 and T_p <= 64.
+ * The forward gathers x, runs tp_ffn_fwd's path and writes row-slice t of
+ * y = sum_t y^(t) (+ b2) into y_slices[t]: with TP_SUM_STANDALONE the ordered
+ * shard-sum itself writes each slice (reduce-scatter); with TP_SUM_FUSED the
+ * fused GEMM's result is scattered.  The backward gathers x and dy and
+ * reduce-scatters dx the same way; weight and bias gradients are as in
+ * tp_ffn_bwd.  Results are bit-identical to tp_ffn_fwd / tp_ffn_bwd on the
+ * concatenated tensors.  TP_SUM_OVERLAP is not supported (TP_ERR_INVALID).
+ * workspace: tp_ffn_seq_parallel_workspace_bytes(plan, n, flags) bytes. */
+TPFFN_API size_t tp_ffn_seq_parallel_workspace_bytes(const tp_ffn_plan* plan, int64_t n_tokens, int flags);
+TPFFN_API int tp_ffn_fwd_seq_parallel(const tp_ffn_plan* plan, int64_t n_tokens, const void* const* x_slices,
+                                      const void* w13p, const void* w2p, const void* b1, const void* b2,
+                                      void* const* y_slices, void* saved, void* workspace, size_t workspace_bytes,
+                                      int flags, tp_stream_t stream);
+TPFFN_API int tp_ffn_bwd_seq_parallel(const tp_ffn_plan* plan, int64_t n_tokens, const void* const* x_slices,
+                                      const void* w13p, const void* w2p, const void* saved,
+                                      const void* const* dy_slices, void* const* dx_slices, void* dw13p,
+                                      void* dw2p, void* db1, void* db2, void* workspace, size_t workspace_bytes,
+                                      int flags, tp_stream_t stream);
+
 /* ------------------------------------------------ forward without allocation */
 
 /* Size of the library's static scratch array (32 MiB).  Every GPU that loads

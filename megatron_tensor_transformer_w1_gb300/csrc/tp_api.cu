@@ -395,14 +395,9 @@ int tp_ffn_unshard_rows(const tp_ffn_plan* p, const void* packed, void* W2, tp_s
   return launch_pack_rows(W2, const_cast<void*>(packed), p->T_p, p->s, p->s_pad, p->d, esz(p), 1, stream);
 }
 
-int tp_ffn_fwd(const tp_ffn_plan* p, int64_t n, const void* x, const void* w13p, const void* w2p, const void* b1,
-               const void* b2, void* y, float* partials, void* saved, void* workspace, size_t workspace_bytes,
-               int flags, tp_stream_t stream) {
-  if (!p || n < 0) return TP_ERR_INVALID;
-  if (n == 0) {
-    p->last_launches = 0;
-    return TP_OK;
-  }
+static int validate_fwd(const tp_ffn_plan* p, int64_t n, const void* x, const void* w13p, const void* w2p,
+                        const void* b1, const void* b2, const void* y, const float* partials, const void* saved,
+                        const void* workspace, size_t workspace_bytes, int flags) {
   const bool none = p->act == TP_ACT_NONE;
   const bool fused = (flags & TP_SUM_FUSED) != 0;
   if (!x || !w2p || !y || !workspace) return TP_ERR_INVALID;
@@ -413,16 +408,23 @@ int tp_ffn_fwd(const tp_ffn_plan* p, int64_t n, const void* x, const void* w13p,
   if (n > (int64_t(1) << 30)) return TP_ERR_UNSUPPORTED;
   const WsLayout L = ws_layout(p, n, flags);
   if (workspace_bytes < L.total) return TP_ERR_INVALID;
-  {
-    const void* ptrs[] = {x, w13p, w2p, b1, b2, y, partials, saved, workspace};
-    for (const void* q : ptrs)
-      if (q && !aligned16(q)) return TP_ERR_ALIGN;
-  }
+  const void* ptrs[] = {x, w13p, w2p, b1, b2, y, partials, saved, workspace};
+  for (const void* q : ptrs)
+    if (q && !aligned16(q)) return TP_ERR_ALIGN;
+  return TP_OK;
+}
 
-  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-  LaunchCtx ctx;
-  int rc = make_ctx(p, workspace, flags, st, ctx);
-  if (rc) return finish_call(p, ctx, rc, flags, workspace);
+// Forward on an initialised launch context.  With `sc`, the result rows go to
+// the T_p slice buffers of a sequence-parallel caller: the standalone sum
+// writes each row-slice straight into its buffer (reduce-scatter), the fused
+// GEMM writes `y` (a workspace buffer) and a copy scatters it.
+static int fwd_impl(const tp_ffn_plan* p, int64_t n, const void* x, const void* w13p, const void* w2p,
+                    const void* b1, const void* b2, void* y, float* partials, void* saved, void* workspace,
+                    int flags, LaunchCtx& ctx, const RowSlices* sc) {
+  const bool none = p->act == TP_ACT_NONE;
+  const bool fused = (flags & TP_SUM_FUSED) != 0;
+  const WsLayout L = ws_layout(p, n, flags);
+  int rc = TP_OK;
   char* ws = static_cast<char*>(workspace);
   const SavedLayout S = saved_layout(p, n);
   const int64_t T = p->T_p, d = p->d, sp = p->s_pad, W = hidden_width(p);
@@ -456,7 +458,7 @@ int tp_ffn_fwd(const tp_ffn_plan* p, int64_t n, const void* x, const void* w13p,
     g.n_store = sp;
     g.out_bf16 = out_bf16;
     rc = run_gemm(p, g, ctx);
-    if (rc) return finish_call(p, ctx, rc, flags, workspace);
+    if (rc) return rc;
     hbuf = h;
   }
 
@@ -486,6 +488,7 @@ int tp_ffn_fwd(const tp_ffn_plan* p, int64_t n, const void* x, const void* w13p,
     g.bias_bs = 0;
     g.bias_len = d;
     rc = run_gemm(p, g, ctx);
+    if (!rc && sc) rc = launch_scatter_rows(y, n, d, out_bf16 ? 2 : 4, *sc, ctx, "scatter_y");
   } else {
     float* part = partials ? partials : reinterpret_cast<float*>(ws + L.part);
     g.name = "down_partials";
@@ -501,20 +504,35 @@ int tp_ffn_fwd(const tp_ffn_plan* p, int64_t n, const void* x, const void* w13p,
       rc = gemm_sum_overlapped(p, g, ctx, part, n, d, b2, y, out_bf16, "shard_sum_y");
     } else {
       rc = run_gemm(p, g, ctx);
-      if (!rc) rc = launch_shard_sum(part, static_cast<int>(T), n, d, b2, y, out_bf16, ctx, "shard_sum_y");
+      if (!rc && sc)
+        rc = launch_shard_sum_scatter(part, static_cast<int>(T), n, d, b2, *sc, out_bf16, ctx, "reduce_scatter_y");
+      else if (!rc)
+        rc = launch_shard_sum(part, static_cast<int>(T), n, d, b2, y, out_bf16, ctx, "shard_sum_y");
     }
   }
-  return finish_call(p, ctx, rc, flags, workspace);
+  return rc;
 }
 
-int tp_ffn_bwd(const tp_ffn_plan* p, int64_t n, const void* x, const void* w13p, const void* w2p, const void* saved,
-               const void* dy, void* dx, float* dx_partials, void* dw13p, void* dw2p, void* db1, void* db2,
-               void* workspace, size_t workspace_bytes, int flags, tp_stream_t stream) {
+int tp_ffn_fwd(const tp_ffn_plan* p, int64_t n, const void* x, const void* w13p, const void* w2p, const void* b1,
+               const void* b2, void* y, float* partials, void* saved, void* workspace, size_t workspace_bytes,
+               int flags, tp_stream_t stream) {
   if (!p || n < 0) return TP_ERR_INVALID;
   if (n == 0) {
     p->last_launches = 0;
     return TP_OK;
   }
+  int rc = validate_fwd(p, n, x, w13p, w2p, b1, b2, y, partials, saved, workspace, workspace_bytes, flags);
+  if (rc) return rc;
+  LaunchCtx ctx;
+  rc = make_ctx(p, workspace, flags, reinterpret_cast<cudaStream_t>(stream), ctx);
+  if (!rc) rc = fwd_impl(p, n, x, w13p, w2p, b1, b2, y, partials, saved, workspace, flags, ctx, nullptr);
+  return finish_call(p, ctx, rc, flags, workspace);
+}
+
+static int validate_bwd(const tp_ffn_plan* p, int64_t n, const void* x, const void* w13p, const void* w2p,
+                        const void* saved, const void* dy, const void* dx, const float* dx_partials,
+                        const void* dw13p, const void* dw2p, const void* db1, const void* db2,
+                        const void* workspace, size_t workspace_bytes, int flags) {
   const bool none = p->act == TP_ACT_NONE;
   const bool fused = (flags & TP_SUM_FUSED) != 0;
   if (!x || !w2p || !dy || !dx || !dw2p || !workspace) return TP_ERR_INVALID;
@@ -525,16 +543,20 @@ int tp_ffn_bwd(const tp_ffn_plan* p, int64_t n, const void* x, const void* w13p,
   if (n > (int64_t(1) << 30)) return TP_ERR_UNSUPPORTED;
   const WsLayout L = ws_layout(p, n, flags);
   if (workspace_bytes < L.total) return TP_ERR_INVALID;
-  {
-    const void* ptrs[] = {x, w13p, w2p, saved, dy, dx, dx_partials, dw13p, dw2p, db1, db2, workspace};
-    for (const void* q : ptrs)
-      if (q && !aligned16(q)) return TP_ERR_ALIGN;
-  }
+  const void* ptrs[] = {x, w13p, w2p, saved, dy, dx, dx_partials, dw13p, dw2p, db1, db2, workspace};
+  for (const void* q : ptrs)
+    if (q && !aligned16(q)) return TP_ERR_ALIGN;
+  return TP_OK;
+}
 
-  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-  LaunchCtx ctx;
-  int rc = make_ctx(p, workspace, flags, st, ctx);
-  if (rc) return finish_call(p, ctx, rc, flags, workspace);
+// Backward on an initialised launch context; `sc` as in fwd_impl, for dx.
+static int bwd_impl(const tp_ffn_plan* p, int64_t n, const void* x, const void* w13p, const void* w2p,
+                    const void* saved, const void* dy, void* dx, float* dx_partials, void* dw13p, void* dw2p,
+                    void* db1, void* db2, void* workspace, int flags, LaunchCtx& ctx, const RowSlices* sc) {
+  const bool none = p->act == TP_ACT_NONE;
+  const bool fused = (flags & TP_SUM_FUSED) != 0;
+  const WsLayout L = ws_layout(p, n, flags);
+  int rc = TP_OK;
   char* ws = static_cast<char*>(workspace);
   const SavedLayout S = saved_layout(p, n);
   const int64_t T = p->T_p, d = p->d, sp = p->s_pad, W = hidden_width(p), s = p->s;
@@ -558,7 +580,8 @@ int tp_ffn_bwd(const tp_ffn_plan* p, int64_t n, const void* x, const void* w13p,
     g.n_store = s;
     g.out_bf16 = out_bf16;
     rc = run_gemm(p, g, ctx);
-    if (rc) return finish_call(p, ctx, rc, flags, workspace);
+    if (!rc && sc) rc = launch_scatter_rows(dx, n, p->d_ff, out_bf16 ? 2 : 4, *sc, ctx, "scatter_dx");
+    if (rc) return rc;
     // dW_O^(t) = dy^T c^(t)
     GemmSpec w;
     w.name = "wgrad_rows";
@@ -578,7 +601,7 @@ int tp_ffn_bwd(const tp_ffn_plan* p, int64_t n, const void* x, const void* w13p,
     if (!rc && db2)
       rc = launch_colsum(dy, out_bf16, 1, n, d, d, n * d, db2, out_bf16, 0, cs_scratch, colsum_chunk(n), ctx,
                          "colsum_db2");
-    return finish_call(p, ctx, rc, flags, workspace);
+    return rc;
   }
 
   void* D = ws + L.D;
@@ -605,7 +628,7 @@ int tp_ffn_bwd(const tp_ffn_plan* p, int64_t n, const void* x, const void* w13p,
     g.n_store = sp;
     g.out_bf16 = out_bf16;
     rc = run_gemm(p, g, ctx);
-    if (rc) return finish_call(p, ctx, rc, flags, workspace);
+    if (rc) return rc;
   }
   // ---- 4. dx = sum_t D^(t) W13^(t)   (f operator)
   {
@@ -628,6 +651,7 @@ int tp_ffn_bwd(const tp_ffn_plan* p, int64_t n, const void* x, const void* w13p,
       g.out_bs = 0;
       g.out_rs = d;
       rc = run_gemm(p, g, ctx);
+      if (!rc && sc) rc = launch_scatter_rows(dx, n, d, out_bf16 ? 2 : 4, *sc, ctx, "scatter_dx");
     } else {
       float* part = dx_partials ? dx_partials : reinterpret_cast<float*>(ws + L.part);
       g.name = "dgrad_x_partials";
@@ -642,10 +666,14 @@ int tp_ffn_bwd(const tp_ffn_plan* p, int64_t n, const void* x, const void* w13p,
         rc = gemm_sum_overlapped(p, g, ctx, part, n, d, nullptr, dx, out_bf16, "shard_sum_dx");
       } else {
         rc = run_gemm(p, g, ctx);
-        if (!rc) rc = launch_shard_sum(part, static_cast<int>(T), n, d, nullptr, dx, out_bf16, ctx, "shard_sum_dx");
+        if (!rc && sc)
+          rc = launch_shard_sum_scatter(part, static_cast<int>(T), n, d, nullptr, *sc, out_bf16, ctx,
+                                        "reduce_scatter_dx");
+        else if (!rc)
+          rc = launch_shard_sum(part, static_cast<int>(T), n, d, nullptr, dx, out_bf16, ctx, "shard_sum_dx");
       }
     }
-    if (rc) return finish_call(p, ctx, rc, flags, workspace);
+    if (rc) return rc;
   }
   // ---- 5. weight gradients, per shard
   {
@@ -664,7 +692,7 @@ int tp_ffn_bwd(const tp_ffn_plan* p, int64_t n, const void* x, const void* w13p,
     g.n_store = sp;
     g.out_bf16 = out_bf16;
     rc = run_gemm(p, g, ctx);
-    if (rc) return finish_call(p, ctx, rc, flags, workspace);
+    if (rc) return rc;
   }
   {
     GemmSpec g;
@@ -682,7 +710,7 @@ int tp_ffn_bwd(const tp_ffn_plan* p, int64_t n, const void* x, const void* w13p,
     g.n_store = d;
     g.out_bf16 = out_bf16;
     rc = run_gemm(p, g, ctx);
-    if (rc) return finish_call(p, ctx, rc, flags, workspace);
+    if (rc) return rc;
   }
   // ---- 6. bias gradients
   if (db1)
@@ -691,6 +719,109 @@ int tp_ffn_bwd(const tp_ffn_plan* p, int64_t n, const void* x, const void* w13p,
   if (!rc && db2)
     rc = launch_colsum(dy, out_bf16, 1, n, d, d, n * d, db2, out_bf16, 0, cs_scratch, colsum_chunk(n), ctx,
                        "colsum_db2");
+  return rc;
+}
+
+int tp_ffn_bwd(const tp_ffn_plan* p, int64_t n, const void* x, const void* w13p, const void* w2p, const void* saved,
+               const void* dy, void* dx, float* dx_partials, void* dw13p, void* dw2p, void* db1, void* db2,
+               void* workspace, size_t workspace_bytes, int flags, tp_stream_t stream) {
+  if (!p || n < 0) return TP_ERR_INVALID;
+  if (n == 0) {
+    p->last_launches = 0;
+    return TP_OK;
+  }
+  int rc = validate_bwd(p, n, x, w13p, w2p, saved, dy, dx, dx_partials, dw13p, dw2p, db1, db2, workspace,
+                        workspace_bytes, flags);
+  if (rc) return rc;
+  LaunchCtx ctx;
+  rc = make_ctx(p, workspace, flags, reinterpret_cast<cudaStream_t>(stream), ctx);
+  if (!rc)
+    rc = bwd_impl(p, n, x, w13p, w2p, saved, dy, dx, dx_partials, dw13p, dw2p, db1, db2, workspace, flags, ctx,
+                  nullptr);
+  return finish_call(p, ctx, rc, flags, workspace);
+}
+
+// ------------------------------------------------------ sequence parallel
+static size_t sp_extra_region(const tp_ffn_plan* p, int64_t n) {
+  const int64_t w = p->d > p->d_ff ? p->d : p->d_ff;
+  return align_up(static_cast<size_t>(n) * w * esz(p));
+}
+
+size_t tp_ffn_seq_parallel_workspace_bytes(const tp_ffn_plan* p, int64_t n, int flags) {
+  if (!p || n < 0) return 0;
+  return ws_layout(p, n, flags).total + 3 * sp_extra_region(p, n);
+}
+
+static int sp_slices(const tp_ffn_plan* p, int64_t n, const void* const* ptrs, RowSlices* out) {
+  if (!ptrs || p->T_p > kMaxSlices || n % p->T_p != 0) return TP_ERR_INVALID;
+  out->n = p->T_p;
+  out->rows = n / p->T_p;
+  for (int t = 0; t < p->T_p; ++t) {
+    if (!ptrs[t]) return TP_ERR_INVALID;
+    if (!aligned16(ptrs[t])) return TP_ERR_ALIGN;
+    out->ptr[t] = const_cast<void*>(ptrs[t]);
+  }
+  return TP_OK;
+}
+
+int tp_ffn_fwd_seq_parallel(const tp_ffn_plan* p, int64_t n, const void* const* x_slices, const void* w13p,
+                            const void* w2p, const void* b1, const void* b2, void* const* y_slices, void* saved,
+                            void* workspace, size_t workspace_bytes, int flags, tp_stream_t stream) {
+  if (!p || n < 0) return TP_ERR_INVALID;
+  if (n == 0) {
+    p->last_launches = 0;
+    return TP_OK;
+  }
+  if (flags & TP_SUM_OVERLAP) return TP_ERR_INVALID;
+  RowSlices xs, ys;
+  int rc = sp_slices(p, n, x_slices, &xs);
+  if (!rc) rc = sp_slices(p, n, y_slices, &ys);
+  if (rc) return rc;
+  if (!workspace || workspace_bytes < tp_ffn_seq_parallel_workspace_bytes(p, n, flags)) return TP_ERR_INVALID;
+  const size_t base = ws_layout(p, n, flags).total, extra = sp_extra_region(p, n);
+  char* x_full = static_cast<char*>(workspace) + base;
+  char* y_full = x_full + extra;
+  rc = validate_fwd(p, n, x_full, w13p, w2p, b1, b2, y_full, nullptr, saved, workspace, base, flags);
+  if (rc) return rc;
+  LaunchCtx ctx;
+  rc = make_ctx(p, workspace, flags, reinterpret_cast<cudaStream_t>(stream), ctx);
+  const int64_t d_in = p->act == TP_ACT_NONE ? p->d_ff : p->d;
+  if (!rc) rc = launch_gather_rows(xs, x_full, d_in, esz(p), ctx, "all_gather_x");
+  if (!rc) rc = fwd_impl(p, n, x_full, w13p, w2p, b1, b2, y_full, nullptr, saved, workspace, flags, ctx, &ys);
+  return finish_call(p, ctx, rc, flags, workspace);
+}
+
+int tp_ffn_bwd_seq_parallel(const tp_ffn_plan* p, int64_t n, const void* const* x_slices, const void* w13p,
+                            const void* w2p, const void* saved, const void* const* dy_slices, void* const* dx_slices,
+                            void* dw13p, void* dw2p, void* db1, void* db2, void* workspace, size_t workspace_bytes,
+                            int flags, tp_stream_t stream) {
+  if (!p || n < 0) return TP_ERR_INVALID;
+  if (n == 0) {
+    p->last_launches = 0;
+    return TP_OK;
+  }
+  if (flags & TP_SUM_OVERLAP) return TP_ERR_INVALID;
+  RowSlices xs, dys, dxs;
+  int rc = sp_slices(p, n, x_slices, &xs);
+  if (!rc) rc = sp_slices(p, n, dy_slices, &dys);
+  if (!rc) rc = sp_slices(p, n, dx_slices, &dxs);
+  if (rc) return rc;
+  if (!workspace || workspace_bytes < tp_ffn_seq_parallel_workspace_bytes(p, n, flags)) return TP_ERR_INVALID;
+  const size_t base = ws_layout(p, n, flags).total, extra = sp_extra_region(p, n);
+  char* x_full = static_cast<char*>(workspace) + base;
+  char* dy_full = x_full + extra;
+  char* dx_full = dy_full + extra;
+  rc = validate_bwd(p, n, x_full, w13p, w2p, saved, dy_full, dx_full, nullptr, dw13p, dw2p, db1, db2, workspace,
+                    base, flags);
+  if (rc) return rc;
+  LaunchCtx ctx;
+  rc = make_ctx(p, workspace, flags, reinterpret_cast<cudaStream_t>(stream), ctx);
+  const int64_t d_in = p->act == TP_ACT_NONE ? p->d_ff : p->d;
+  if (!rc) rc = launch_gather_rows(xs, x_full, d_in, esz(p), ctx, "all_gather_x");
+  if (!rc) rc = launch_gather_rows(dys, dy_full, p->d, esz(p), ctx, "all_gather_dy");
+  if (!rc)
+    rc = bwd_impl(p, n, x_full, w13p, w2p, saved, dy_full, dx_full, nullptr, dw13p, dw2p, db1, db2, workspace, flags,
+                  ctx, &dxs);
   return finish_call(p, ctx, rc, flags, workspace);
 }
 

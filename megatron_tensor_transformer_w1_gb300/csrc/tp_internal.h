@@ -66,6 +66,15 @@ struct LaunchCtx {
   void* user = nullptr;
 };
 
+// Row slices of a sequence-parallel caller: rank t's rows [t*rows, (t+1)*rows)
+// of an [n][cols] tensor live in their own buffer ptr[t].
+constexpr int kMaxSlices = 64;
+struct RowSlices {
+  void* ptr[kMaxSlices];
+  int n = 0;
+  int64_t rows = 0;
+};
+
 // Device error bits.
 constexpr int DEV_ERR_TIMEOUT = 1;
 
@@ -84,6 +93,15 @@ int launch_pack_rows(const void* W2, void* out, int T_p, int64_t s, int64_t s_pa
 int launch_shard_sum(const float* partials, int T_p, int64_t rows, int64_t cols,
                      const void* bias, void* out, int out_bf16, LaunchCtx& ctx,
                      const char* name, int64_t shard_stride = 0);
+// Sequence-parallel data movement (tp_kernels.cu): gather the slices into a
+// contiguous [n][cols] buffer (all-gather), scatter a contiguous buffer into
+// the slices, and the ordered shard-sum writing each row-slice into its own
+// buffer (reduce-scatter).  esz = element size in bytes.
+int launch_gather_rows(const RowSlices& src, void* dst, int64_t cols, int esz, LaunchCtx& ctx, const char* name);
+int launch_scatter_rows(const void* src, int64_t n, int64_t cols, int esz, const RowSlices& dst, LaunchCtx& ctx,
+                        const char* name);
+int launch_shard_sum_scatter(const float* partials, int T_p, int64_t rows, int64_t cols, const void* bias,
+                             const RowSlices& out, int out_bf16, LaunchCtx& ctx, const char* name);
 // Column sums of a [batch][rows][cols] view (row stride rs, batch stride bs)
 // into out[b*out_bs + col] for col < cols, deterministic two-pass order.
 int launch_colsum(const void* in, int in_bf16, int64_t batch, int64_t rows, int64_t cols,

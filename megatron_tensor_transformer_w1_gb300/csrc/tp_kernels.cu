@@ -151,6 +151,94 @@ __global__ void shard_sum_scalar_kernel(const float* P, int T, long long plane, 
   }
 }
 
+// ------------------------------------------------------- sequence parallel
+struct SliceTable {
+  char* p[kMaxSlices];
+};
+
+// Copy between T contiguous [rows][row_bytes] slices and one [T*rows] buffer.
+// to_slices = 0: gather (slices -> buffer); 1: scatter (buffer -> slices).
+__global__ void slice_copy_kernel(SliceTable tab, char* buf, long long slice_bytes, long long total_bytes,
+                                  int to_slices) {
+  const long long n16 = total_bytes / 16;
+  for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < n16; i += (long long)gridDim.x * blockDim.x) {
+    const long long o = i * 16;
+    const long long t = o / slice_bytes;
+    uint4* sl = reinterpret_cast<uint4*>(tab.p[t] + (o - t * slice_bytes));
+    uint4* bf = reinterpret_cast<uint4*>(buf + o);
+    if (to_slices)
+      *sl = *bf;
+    else
+      *bf = *sl;
+  }
+}
+__global__ void slice_copy_bytes_kernel(SliceTable tab, char* buf, long long slice_bytes, long long total_bytes,
+                                        int to_slices) {
+  for (long long o = blockIdx.x * (long long)blockDim.x + threadIdx.x; o < total_bytes;
+       o += (long long)gridDim.x * blockDim.x) {
+    const long long t = o / slice_bytes;
+    char* sl = tab.p[t] + (o - t * slice_bytes);
+    if (to_slices)
+      *sl = buf[o];
+    else
+      buf[o] = *sl;
+  }
+}
+
+// Ordered shard-sum whose output row r goes to slice r / rows_per_slice.
+template <int OUT_BF16>
+__global__ void __launch_bounds__(256) shard_sum_scatter_kernel(const float* __restrict__ P, int T, long long plane,
+                                                                long long cols, const void* bias, SliceTable out,
+                                                                long long rows_per_slice) {
+  for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < plane; i += (long long)gridDim.x * blockDim.x) {
+    float acc = P[i];
+    for (int t = 1; t < T; ++t) acc += P[t * plane + i];
+    const long long row = i / cols, col = i - row * cols;
+    if (bias) acc += to_f(bias, col, OUT_BF16);
+    const long long sl = row / rows_per_slice;
+    from_f(out.p[sl], (row - sl * rows_per_slice) * cols + col, acc, OUT_BF16);
+  }
+}
+template <int OUT_BF16>
+__global__ void __launch_bounds__(256) shard_sum_scatter_vec8_kernel(const float* __restrict__ P, int T,
+                                                                     long long plane, long long cols,
+                                                                     const void* bias, SliceTable out,
+                                                                     long long rows_per_slice) {
+  const long long n8 = plane / 8;
+  for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < n8; i += (long long)gridDim.x * blockDim.x) {
+    const float4* p0 = reinterpret_cast<const float4*>(P) + 2 * i;
+    float4 a = __ldcs(p0), b = __ldcs(p0 + 1);
+    for (int t = 1; t < T; ++t) {
+      const float4* pt = reinterpret_cast<const float4*>(P + t * plane) + 2 * i;
+      const float4 c = __ldcs(pt), e = __ldcs(pt + 1);
+      a.x += c.x; a.y += c.y; a.z += c.z; a.w += c.w;
+      b.x += e.x; b.y += e.y; b.z += e.z; b.w += e.w;
+    }
+    float v[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+    const long long e0 = i * 8, row = e0 / cols, col = e0 - row * cols;
+    if (bias) {
+#pragma unroll
+      for (int j = 0; j < 8; ++j) v[j] += to_f(bias, col + j, OUT_BF16);
+    }
+    const long long sl = row / rows_per_slice;
+    const long long o = (row - sl * rows_per_slice) * cols + col;
+    if (OUT_BF16) {
+      uint4 q;
+      __nv_bfloat162 h0 = __floats2bfloat162_rn(v[0], v[1]), h1 = __floats2bfloat162_rn(v[2], v[3]);
+      __nv_bfloat162 h2 = __floats2bfloat162_rn(v[4], v[5]), h3 = __floats2bfloat162_rn(v[6], v[7]);
+      q.x = *reinterpret_cast<uint32_t*>(&h0);
+      q.y = *reinterpret_cast<uint32_t*>(&h1);
+      q.z = *reinterpret_cast<uint32_t*>(&h2);
+      q.w = *reinterpret_cast<uint32_t*>(&h3);
+      *reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(out.p[sl]) + o) = q;
+    } else {
+      float4* dst = reinterpret_cast<float4*>(reinterpret_cast<float*>(out.p[sl]) + o);
+      dst[0] = make_float4(v[0], v[1], v[2], v[3]);
+      dst[1] = make_float4(v[4], v[5], v[6], v[7]);
+    }
+  }
+}
+
 // ------------------------------------------------------------------ colsum
 __global__ void colsum_pass1_kernel(const void* in, int in_bf16, long long rows, long long cols, long long rs,
                                     long long bs, float* scratch, long long chunk_rows, long long chunks) {
@@ -373,6 +461,70 @@ int launch_shard_sum(const float* partials, int T_p, int64_t rows, int64_t cols,
   } else {
     shard_sum_scalar_kernel<<<grid_for(plane, 256, ctx.num_sms), 256, 0, ctx.stream>>>(
         partials, T_p, plane, cols, bias, out_bf16, out, out_bf16, stride);
+  }
+  if (ctx.after) ctx.after(ctx.user, ctx.stream);
+  ctx.launches++;
+  return cudaPeekAtLastError() == cudaSuccess ? 0 : TP_ERR_CUDA;
+}
+
+static SliceTable to_table(const RowSlices& r) {
+  SliceTable t{};
+  for (int i = 0; i < r.n && i < kMaxSlices; ++i) t.p[i] = static_cast<char*>(r.ptr[i]);
+  return t;
+}
+
+static bool all_aligned16(const RowSlices& r) {
+  for (int i = 0; i < r.n; ++i)
+    if (reinterpret_cast<uintptr_t>(r.ptr[i]) % 16) return false;
+  return true;
+}
+
+static int slice_copy(const RowSlices& r, void* buf, int64_t cols, int esz, int to_slices, LaunchCtx& ctx,
+                      const char* name) {
+  const long long slice_bytes = r.rows * cols * esz;
+  const long long total = slice_bytes * r.n;
+  if (total <= 0) return 0;
+  if (ctx.before) ctx.before(ctx.user, name, ctx.stream);
+  if (slice_bytes % 16 == 0 && all_aligned16(r) && reinterpret_cast<uintptr_t>(buf) % 16 == 0)
+    slice_copy_kernel<<<grid_for(total / 16, 256, ctx.num_sms), 256, 0, ctx.stream>>>(
+        to_table(r), static_cast<char*>(buf), slice_bytes, total, to_slices);
+  else
+    slice_copy_bytes_kernel<<<grid_for(total, 256, ctx.num_sms), 256, 0, ctx.stream>>>(
+        to_table(r), static_cast<char*>(buf), slice_bytes, total, to_slices);
+  if (ctx.after) ctx.after(ctx.user, ctx.stream);
+  ctx.launches++;
+  return cudaPeekAtLastError() == cudaSuccess ? 0 : TP_ERR_CUDA;
+}
+
+int launch_gather_rows(const RowSlices& src, void* dst, int64_t cols, int esz, LaunchCtx& ctx, const char* name) {
+  return slice_copy(src, dst, cols, esz, 0, ctx, name);
+}
+
+int launch_scatter_rows(const void* src, int64_t n, int64_t cols, int esz, const RowSlices& dst, LaunchCtx& ctx,
+                        const char* name) {
+  (void)n;
+  return slice_copy(dst, const_cast<void*>(src), cols, esz, 1, ctx, name);
+}
+
+int launch_shard_sum_scatter(const float* partials, int T_p, int64_t rows, int64_t cols, const void* bias,
+                             const RowSlices& out, int out_bf16, LaunchCtx& ctx, const char* name) {
+  const long long plane = (long long)rows * cols;
+  if (plane <= 0) return 0;
+  if (ctx.before) ctx.before(ctx.user, name, ctx.stream);
+  const bool vec = cols % 8 == 0 && reinterpret_cast<uintptr_t>(partials) % 16 == 0 && all_aligned16(out);
+  const SliceTable tab = to_table(out);
+  if (vec) {
+    const int grid = grid_for(plane / 8, 256, ctx.num_sms);
+    if (out_bf16)
+      shard_sum_scatter_vec8_kernel<1><<<grid, 256, 0, ctx.stream>>>(partials, T_p, plane, cols, bias, tab, out.rows);
+    else
+      shard_sum_scatter_vec8_kernel<0><<<grid, 256, 0, ctx.stream>>>(partials, T_p, plane, cols, bias, tab, out.rows);
+  } else {
+    const int grid = grid_for(plane, 256, ctx.num_sms);
+    if (out_bf16)
+      shard_sum_scatter_kernel<1><<<grid, 256, 0, ctx.stream>>>(partials, T_p, plane, cols, bias, tab, out.rows);
+    else
+      shard_sum_scatter_kernel<0><<<grid, 256, 0, ctx.stream>>>(partials, T_p, plane, cols, bias, tab, out.rows);
   }
   if (ctx.after) ctx.after(ctx.user, ctx.stream);
   ctx.launches++;

@@ -26,7 +26,8 @@ ABI_FUNCTIONS = (
     "tp_ffn_packed_bytes", "tp_ffn_saved_bytes", "tp_ffn_workspace_bytes", "tp_ffn_shard_columns",
     "tp_ffn_shard_rows", "tp_ffn_unshard_columns", "tp_ffn_unshard_rows", "tp_ffn_fwd", "tp_ffn_bwd",
     "tp_ffn_last_device_error", "tp_ffn_status_string", "tp_ffn_kernel_times", "tp_ffn_last_launch_count",
-    "tp_ffn_fwd_static_scratch",
+    "tp_ffn_fwd_static_scratch", "tp_ffn_seq_parallel_workspace_bytes", "tp_ffn_fwd_seq_parallel",
+    "tp_ffn_bwd_seq_parallel",
 )
 TPFFN_STATIC_SCRATCH_BYTES = 32 << 20
 
@@ -68,6 +69,9 @@ _SIGS = {
     "tp_ffn_kernel_times": (_INT, [_P, _INT, ctypes.POINTER(ctypes.c_char_p), ctypes.POINTER(ctypes.c_float)]),
     "tp_ffn_last_launch_count": (_INT, [_P]),
     "tp_ffn_fwd_static_scratch": (_INT, [_P, _I64, _P, _P, _P, _P, _P, _P, _P]),
+    "tp_ffn_seq_parallel_workspace_bytes": (_SZ, [_P, _I64, _INT]),
+    "tp_ffn_fwd_seq_parallel": (_INT, [_P, _I64, _P, _P, _P, _P, _P, _P, _P, _P, _SZ, _INT, _P]),
+    "tp_ffn_bwd_seq_parallel": (_INT, [_P, _I64, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _SZ, _INT, _P]),
 }
 for _name, (_res, _args) in _SIGS.items():
     _f = getattr(_lib, _name)
@@ -186,6 +190,34 @@ def tp_ffn_fwd_static_scratch(plan, n_tokens, x, w13p, w2p, b1, b2, y, stream=No
     allocate.  See include/tpffn.h for its limit and sharing rules."""
     return _lib.tp_ffn_fwd_static_scratch(plan, n_tokens, _ptr(x), _ptr(w13p), _ptr(w2p), _ptr(b1), _ptr(b2),
                                           _ptr(y), _stream(stream))
+
+
+def _ptr_array(items):
+    """A host array of device pointers (None -> NULL) for the slice arguments."""
+    if items is None:
+        return None
+    arr = (ctypes.c_void_p * len(items))(*[_ptr(a) for a in items])
+    return ctypes.cast(arr, ctypes.c_void_p), arr  # keep `arr` alive with the call
+
+
+def tp_ffn_seq_parallel_workspace_bytes(plan, n_tokens, flags=0):
+    return _lib.tp_ffn_seq_parallel_workspace_bytes(plan, n_tokens, flags)
+
+
+def tp_ffn_fwd_seq_parallel(plan, n_tokens, x_slices, w13p, w2p, b1, b2, y_slices, saved, workspace,
+                            workspace_bytes, flags=0, stream=None):
+    xs, ys = _ptr_array(x_slices), _ptr_array(y_slices)
+    return _lib.tp_ffn_fwd_seq_parallel(plan, n_tokens, xs and xs[0], _ptr(w13p), _ptr(w2p), _ptr(b1), _ptr(b2),
+                                        ys and ys[0], _ptr(saved), _ptr(workspace), workspace_bytes, flags,
+                                        _stream(stream))
+
+
+def tp_ffn_bwd_seq_parallel(plan, n_tokens, x_slices, w13p, w2p, saved, dy_slices, dx_slices, dw13p, dw2p, db1, db2,
+                            workspace, workspace_bytes, flags=0, stream=None):
+    xs, dys, dxs = _ptr_array(x_slices), _ptr_array(dy_slices), _ptr_array(dx_slices)
+    return _lib.tp_ffn_bwd_seq_parallel(plan, n_tokens, xs and xs[0], _ptr(w13p), _ptr(w2p), _ptr(saved),
+                                        dys and dys[0], dxs and dxs[0], _ptr(dw13p), _ptr(dw2p), _ptr(db1), _ptr(db2),
+                                        _ptr(workspace), workspace_bytes, flags, _stream(stream))
 
 
 def check(status, where=""):
