@@ -15,7 +15,11 @@ computes are stated in that file's header:
   megatron pattern");
 * the backward by the chain rule, with the dx shard-sum (the f operator of §2.1);
 * the row-parallel attention output projection (§2.2 "Attention, sharded"),
-  as activation NONE.
+  as activation NONE;
+* the whole head-sharded attention sublayer of §2.2 (column-sharded Q/K/V with
+  the GQA divisibility rule of "S17 Tensor & Pipeline Parallelism", the scaled
+  dot-product attention of each head, the row-sharded W_O with the ordered
+  shard-sum) and its backward, and the attention core alone (``AttentionCore``).
 """
 from __future__ import annotations
 
@@ -237,6 +241,95 @@ class FFN:
         b = self.backward_rows(dy)
         w.update(b)
         return w
+
+
+class _AttnCore(ctypes.Structure):
+    _fields_ = [("B", ctypes.c_int64), ("S", ctypes.c_int64), ("H", ctypes.c_int64),
+                ("Hkv", ctypes.c_int64), ("hd", ctypes.c_int64), ("causal", ctypes.c_int),
+                ("round_bf16", ctypes.c_int)]
+
+
+class _Attn(ctypes.Structure):
+    _fields_ = [("core", _AttnCore), ("d", ctypes.c_int64), ("T_p", ctypes.c_int),
+                ("x", ctypes.c_void_p), ("Wq", ctypes.c_void_p), ("Wk", ctypes.c_void_p),
+                ("Wv", ctypes.c_void_p), ("Wo", ctypes.c_void_p)]
+
+
+class AttentionCore:
+    """Scaled dot-product attention of B sequences of S tokens, H query heads
+    of width hd reading Hkv key/value heads (query head h reads h // (H/Hkv)).
+
+    q, o : [B*S, H*hd]   k, v : [B*S, Hkv*hd]   (token rows, head columns)
+    """
+
+    def __init__(self, B, S, H, Hkv, hd, causal=True, round_bf16=False, lib=None):
+        if H % Hkv:
+            raise ValueError("H must be a multiple of Hkv")
+        self.B, self.S, self.H, self.Hkv, self.hd = int(B), int(S), int(H), int(Hkv), int(hd)
+        self.causal, self.round_bf16 = bool(causal), bool(round_bf16)
+        self._lib = lib
+        self._s = _AttnCore(self.B, self.S, self.H, self.Hkv, self.hd, int(self.causal), int(self.round_bf16))
+
+    def lib(self):
+        return self._lib if self._lib is not None else _load()
+
+    def forward(self, q, k, v):
+        """Returns (o [B*S, H*hd], lse [B, H, S])."""
+        q, k, v = _f64(q), _f64(k), _f64(v)
+        n = self.B * self.S
+        assert q.shape == (n, self.H * self.hd) and k.shape == v.shape == (n, self.Hkv * self.hd)
+        o = np.empty((n, self.H * self.hd))
+        lse = np.empty((self.B, self.H, self.S))
+        self.lib().orc_attn_core_fwd(ctypes.byref(self._s), _ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse))
+        return o, lse
+
+    def backward(self, q, k, v, dO):
+        """Returns (dq, dk, dv)."""
+        q, k, v, dO = _f64(q), _f64(k), _f64(v), _f64(dO)
+        dq, dk, dv = np.empty_like(q), np.empty_like(k), np.empty_like(v)
+        self.lib().orc_attn_core_bwd(ctypes.byref(self._s), _ptr(q), _ptr(k), _ptr(v), _ptr(dO), _ptr(dq),
+                                     _ptr(dk), _ptr(dv))
+        return dq, dk, dv
+
+
+class Attention:
+    """The head-sharded attention sublayer of one problem.
+
+    x : [B*S, d]   Wq : [H*hd, d]   Wk, Wv : [Hkv*hd, d]   Wo : [d, H*hd]
+    Shard t owns query heads [t*H/T_p, (t+1)*H/T_p) and key/value heads
+    [t*Hkv/T_p, (t+1)*Hkv/T_p); both counts must divide by T_p.
+    """
+
+    def __init__(self, x, Wq, Wk, Wv, Wo, B, S, H, Hkv, hd, T_p, causal=True, round_bf16=False, lib=None):
+        if H % T_p or Hkv % T_p:
+            raise ValueError("the tensor-parallel degree must divide the query and the key/value heads")
+        self.core = AttentionCore(B, S, H, Hkv, hd, causal, round_bf16, lib)
+        self.x, self.Wq, self.Wk, self.Wv, self.Wo = _f64(x), _f64(Wq), _f64(Wk), _f64(Wv), _f64(Wo)
+        self.d = self.x.shape[1]
+        self.T_p = int(T_p)
+        assert self.x.shape[0] == B * S
+        assert self.Wq.shape == (H * hd, self.d) and self.Wk.shape == self.Wv.shape == (Hkv * hd, self.d)
+        assert self.Wo.shape == (self.d, H * hd)
+        self._s = _Attn(self.core._s, self.d, self.T_p, _ptr(self.x), _ptr(self.Wq), _ptr(self.Wk),
+                        _ptr(self.Wv), _ptr(self.Wo))
+
+    def forward(self):
+        """Returns (c [B*S, H*hd] head outputs, y [B*S, d])."""
+        n = self.x.shape[0]
+        c = np.empty((n, self.Wo.shape[1]))
+        y = np.empty((n, self.d))
+        self.core.lib().orc_attn_forward(ctypes.byref(self._s), _ptr(c), _ptr(y))
+        return c, y
+
+    def backward(self, dy):
+        """Returns dict dx, dWq, dWk, dWv, dWo."""
+        dy = _f64(dy)
+        assert dy.shape == (self.x.shape[0], self.d)
+        out = dict(dx=np.empty_like(self.x), dWq=np.empty_like(self.Wq), dWk=np.empty_like(self.Wk),
+                   dWv=np.empty_like(self.Wv), dWo=np.empty_like(self.Wo))
+        self.core.lib().orc_attn_backward(ctypes.byref(self._s), _ptr(dy), _ptr(out["dx"]), _ptr(out["dWq"]),
+                                          _ptr(out["dWk"]), _ptr(out["dWv"]), _ptr(out["dWo"]))
+        return out
 
 
 # -------------------------------------------------------------- scalar API

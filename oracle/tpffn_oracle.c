@@ -507,3 +507,260 @@ int orc_num_threads(void) {
   return 1;
 #endif
 }
+
+/* ================================================================ attention
+ *
+ * Head-sharded self-attention sublayer -- "7.9 Tensor and pipeline
+ * parallelism (TP, PP)", §2.2 "Attention, sharded": shard t owns the query
+ * heads [t*H/T_p, (t+1)*H/T_p) and the key/value heads [t*Hkv/T_p, ...) (the
+ * divisibility rule of "S17 Tensor & Pipeline Parallelism", "Attention shards
+ * by head, and GQA caps the degree"); it computes Q, K, V for its heads, the
+ * scaled dot-product attention of each head (query head h reads key/value
+ * head h / (H/Hkv)), and the row-sharded output projection
+ * y^(t) = c^(t) W_O^(t)T of its heads' outputs c^(t); y = sum_t y^(t) in the
+ * order t = 0..T_p-1.  Per head: s_ij = (q_i . k_j) / sqrt(hd) (j <= i when
+ * causal), p_i = softmax_j(s_i), o_i = sum_j p_ij v_j.
+ *
+ * Layouts (row-major, tokens of sequence b are rows b*S .. b*S+S-1):
+ *   q, o, dq, dO [B*S][H*hd]     k, v, dk, dv [B*S][Hkv*hd]
+ *   weights [out][in]: Wq [H*hd][d], Wk, Wv [Hkv*hd][d], Wo [d][H*hd].
+ * round_bf16: q, k, v and the head outputs o are rounded to bf16 where the
+ * sublayer stores them, and so are dO, dq, dk, dv in the backward; the
+ * probabilities p and the score gradients dS are transient (never stored)
+ * and stay exact, and the key/value gradients of a GQA group are summed over
+ * its query heads before their one rounding. */
+
+typedef struct {
+  int64_t B, S, H, Hkv, hd;
+  int causal, round_bf16;
+} orc_attn_core;
+
+/* Softmax probabilities of query i (global row r = b*S + i) of head h;
+ * p[0..S-1], zero where masked.  Returns the log-sum-exp of the scaled
+ * scores. */
+static double attn_probs(const orc_attn_core* C, const double* q, const double* k, int64_t b, int64_t h,
+                         int64_t i, double* p) {
+  const int64_t S = C->S, hd = C->hd, nq = C->H * hd, nk = C->Hkv * hd;
+  const int64_t hk = h / (C->H / C->Hkv);
+  const double scale = 1.0 / sqrt((double)hd);
+  const int64_t jmax = C->causal ? i : S - 1;
+  const double* qi = q + (b * S + i) * nq + h * hd;
+  double m = -INFINITY;
+  for (int64_t j = 0; j <= jmax; ++j) {
+    p[j] = dot_row(qi, k + (b * S + j) * nk + hk * hd, hd) * scale;
+    if (p[j] > m) m = p[j];
+  }
+  double sum = 0.0;
+  for (int64_t j = 0; j <= jmax; ++j) {
+    p[j] = exp(p[j] - m);
+    sum += p[j];
+  }
+  for (int64_t j = 0; j < S; ++j) p[j] = (j <= jmax) ? p[j] / sum : 0.0;
+  return m + log(sum);
+}
+
+/* Attention core forward: o = softmax(q k^T / sqrt(hd)) v per head;
+ * lse [B][H][S] (may be NULL) receives the log-sum-exp of each row. */
+void orc_attn_core_fwd(const orc_attn_core* C, const double* q, const double* k, const double* v, double* o,
+                       double* lse) {
+  const int64_t B = C->B, S = C->S, H = C->H, hd = C->hd, nq = H * hd, nk = C->Hkv * hd;
+  const int64_t G = H / C->Hkv;
+#pragma omp parallel for schedule(dynamic, 1)
+  for (int64_t bhi = 0; bhi < B * H * S; ++bhi) {
+    const int64_t b = bhi / (H * S), h = (bhi / S) % H, i = bhi % S;
+    double* p = (double*)malloc(sizeof(double) * S);
+    const double l = attn_probs(C, q, k, b, h, i, p);
+    if (lse) lse[(b * H + h) * S + i] = l;
+    for (int64_t jd = 0; jd < hd; ++jd) {
+      double acc = 0.0;
+      for (int64_t j = 0; j < S; ++j) acc += p[j] * v[(b * S + j) * nk + (h / G) * hd + jd];
+      o[(b * S + i) * nq + h * hd + jd] = RND(C->round_bf16, acc);
+    }
+    free(p);
+  }
+}
+
+/* Attention core backward: given dO, dq = dS k, dk = dS^T q, dv = P^T dO
+ * with dS_ij = p_ij (dO_i . v_j - sum_l p_il dO_i . v_l) / sqrt(hd). */
+void orc_attn_core_bwd(const orc_attn_core* C, const double* q, const double* k, const double* v,
+                       const double* dO, double* dq, double* dk, double* dv) {
+  const int R = C->round_bf16;
+  const int64_t B = C->B, S = C->S, H = C->H, Hkv = C->Hkv, hd = C->hd, nq = H * hd, nk = Hkv * hd;
+  const int64_t G = H / Hkv;
+  const double scale = 1.0 / sqrt((double)hd);
+  double* P = (double*)malloc(sizeof(double) * B * H * S * S);
+  double* dS = (double*)malloc(sizeof(double) * B * H * S * S);
+#pragma omp parallel for schedule(dynamic, 1)
+  for (int64_t bhi = 0; bhi < B * H * S; ++bhi) {
+    const int64_t b = bhi / (H * S), h = (bhi / S) % H, i = bhi % S, hk = h / G;
+    double* p = P + bhi * S;
+    double* ds = dS + bhi * S;
+    attn_probs(C, q, k, b, h, i, p);
+    const double* dOi = dO + (b * S + i) * nq + h * hd;
+    double rowdot = 0.0;
+    for (int64_t j = 0; j < S; ++j) {
+      ds[j] = dot_row(dOi, v + (b * S + j) * nk + hk * hd, hd);
+      rowdot += p[j] * ds[j];
+    }
+    for (int64_t j = 0; j < S; ++j) ds[j] = p[j] * (ds[j] - rowdot) * scale;
+  }
+  /* dq */
+#pragma omp parallel for schedule(dynamic, 1)
+  for (int64_t bhi = 0; bhi < B * H * S; ++bhi) {
+    const int64_t b = bhi / (H * S), h = (bhi / S) % H, i = bhi % S, hk = h / G;
+    for (int64_t jd = 0; jd < hd; ++jd) {
+      double acc = 0.0;
+      for (int64_t j = 0; j < S; ++j) acc += dS[bhi * S + j] * k[(b * S + j) * nk + hk * hd + jd];
+      dq[(b * S + i) * nq + h * hd + jd] = RND(R, acc);
+    }
+  }
+  /* dk, dv: key/value head hk collects the G query heads of its group */
+#pragma omp parallel for schedule(dynamic, 1)
+  for (int64_t bki = 0; bki < B * Hkv * S; ++bki) {
+    const int64_t b = bki / (Hkv * S), hk = (bki / S) % Hkv, j = bki % S;
+    for (int64_t jd = 0; jd < hd; ++jd) {
+      double ak = 0.0, av = 0.0;
+      for (int64_t g = 0; g < G; ++g) {
+        const int64_t h = hk * G + g;
+        for (int64_t i = 0; i < S; ++i) {
+          const int64_t row = (b * H + h) * S + i;
+          ak += dS[row * S + j] * q[(b * S + i) * nq + h * hd + jd];
+          av += P[row * S + j] * dO[(b * S + i) * nq + h * hd + jd];
+        }
+      }
+      dk[(b * S + j) * nk + hk * hd + jd] = RND(R, ak);
+      dv[(b * S + j) * nk + hk * hd + jd] = RND(R, av);
+    }
+  }
+  free(dS);
+  free(P);
+}
+
+typedef struct {
+  orc_attn_core core;
+  int64_t d;
+  int T_p;
+  const double* x;   /* [B*S][d] */
+  const double* Wq;  /* [H*hd][d] */
+  const double* Wk;  /* [Hkv*hd][d] */
+  const double* Wv;  /* [Hkv*hd][d] */
+  const double* Wo;  /* [d][H*hd] */
+} orc_attn;
+
+/* q, k, v of every token (rounded where stored). */
+static void attn_project(const orc_attn* A, double* q, double* k, double* v) {
+  const orc_attn_core* C = &A->core;
+  const int R = C->round_bf16;
+  const int64_t n = C->B * C->S, d = A->d, nq = C->H * C->hd, nk = C->Hkv * C->hd;
+#pragma omp parallel for schedule(static)
+  for (int64_t r = 0; r < n; ++r) {
+    const double* xr = A->x + r * d;
+    for (int64_t c = 0; c < nq; ++c) q[r * nq + c] = RND(R, dot_row(xr, A->Wq + c * d, d));
+    for (int64_t c = 0; c < nk; ++c) {
+      k[r * nk + c] = RND(R, dot_row(xr, A->Wk + c * d, d));
+      v[r * nk + c] = RND(R, dot_row(xr, A->Wv + c * d, d));
+    }
+  }
+}
+
+/* Sublayer forward: c [B*S][H*hd] (head outputs), y [B*S][d] = sum over
+ * shards t = 0..T_p-1 of c^(t) Wo^(t)T, Wo^(t) = columns [t*nq/T_p, ...). */
+void orc_attn_forward(const orc_attn* A, double* c_out, double* y_out) {
+  const orc_attn_core* C = &A->core;
+  const int64_t n = C->B * C->S, d = A->d, nq = C->H * C->hd, nk = C->Hkv * C->hd;
+  double* q = (double*)malloc(sizeof(double) * n * nq);
+  double* k = (double*)malloc(sizeof(double) * n * nk);
+  double* v = (double*)malloc(sizeof(double) * n * nk);
+  attn_project(A, q, k, v);
+  orc_attn_core_fwd(C, q, k, v, c_out, NULL);
+  const int T = A->T_p;
+  const int64_t s = nq / T;
+#pragma omp parallel for schedule(static)
+  for (int64_t r = 0; r < n; ++r)
+    for (int64_t o = 0; o < d; ++o) {
+      double acc = 0.0;
+      for (int t = 0; t < T; ++t) {
+        double part = 0.0;
+        for (int64_t jj = t * s; jj < (t + 1) * s; ++jj) part += A->Wo[o * nq + jj] * c_out[r * nq + jj];
+        acc += part;
+      }
+      y_out[r * d + o] = acc;
+    }
+  free(v);
+  free(k);
+  free(q);
+}
+
+/* Sublayer backward given dy [B*S][d]: dx [B*S][d] = sum over shards
+ * t = 0..T_p-1 of (dq^(t) Wq^(t) + dk^(t) Wk^(t) + dv^(t) Wv^(t)), and the
+ * weight gradients dWq [H*hd][d], dWk, dWv [Hkv*hd][d], dWo [d][H*hd]
+ * (each may be NULL), summed over all tokens. */
+void orc_attn_backward(const orc_attn* A, const double* dy, double* dx, double* dWq, double* dWk, double* dWv,
+                       double* dWo) {
+  const orc_attn_core* C = &A->core;
+  const int R = C->round_bf16;
+  const int64_t n = C->B * C->S, d = A->d, nq = C->H * C->hd, nk = C->Hkv * C->hd;
+  double* q = (double*)malloc(sizeof(double) * n * nq);
+  double* k = (double*)malloc(sizeof(double) * n * nk);
+  double* v = (double*)malloc(sizeof(double) * n * nk);
+  double* c = (double*)malloc(sizeof(double) * n * nq);
+  double* dO = (double*)malloc(sizeof(double) * n * nq);
+  double* dq = (double*)malloc(sizeof(double) * n * nq);
+  double* dk = (double*)malloc(sizeof(double) * n * nk);
+  double* dv = (double*)malloc(sizeof(double) * n * nk);
+  attn_project(A, q, k, v);
+  orc_attn_core_fwd(C, q, k, v, c, NULL);
+  /* dO = dy Wo: shard t's head columns only need its own Wo^(t) -- no sum */
+#pragma omp parallel for schedule(static)
+  for (int64_t r = 0; r < n; ++r)
+    for (int64_t col = 0; col < nq; ++col) {
+      double acc = 0.0;
+      for (int64_t o = 0; o < d; ++o) acc += dy[r * d + o] * A->Wo[o * nq + col];
+      dO[r * nq + col] = RND(R, acc);
+    }
+  orc_attn_core_bwd(C, q, k, v, dO, dq, dk, dv);
+  const int T = A->T_p;
+  const int64_t sq = nq / T, sk = nk / T;
+#pragma omp parallel for schedule(static)
+  for (int64_t r = 0; r < n; ++r)
+    for (int64_t kk = 0; kk < d; ++kk) {
+      double acc = 0.0;
+      for (int t = 0; t < T; ++t) {
+        double part = 0.0;
+        for (int64_t c2 = t * sq; c2 < (t + 1) * sq; ++c2) part += dq[r * nq + c2] * A->Wq[c2 * d + kk];
+        for (int64_t c2 = t * sk; c2 < (t + 1) * sk; ++c2) {
+          part += dk[r * nk + c2] * A->Wk[c2 * d + kk];
+          part += dv[r * nk + c2] * A->Wv[c2 * d + kk];
+        }
+        acc += part;
+      }
+      dx[r * d + kk] = acc;
+    }
+#pragma omp parallel for schedule(static)
+  for (int64_t kk = 0; kk < d; ++kk) {
+    for (int64_t c2 = 0; c2 < nq; ++c2) {
+      double acc = 0.0;
+      for (int64_t r = 0; r < n; ++r) acc += dq[r * nq + c2] * A->x[r * d + kk];
+      if (dWq) dWq[c2 * d + kk] = acc;
+    }
+    for (int64_t c2 = 0; c2 < nk; ++c2) {
+      double ak = 0.0, av = 0.0;
+      for (int64_t r = 0; r < n; ++r) {
+        ak += dk[r * nk + c2] * A->x[r * d + kk];
+        av += dv[r * nk + c2] * A->x[r * d + kk];
+      }
+      if (dWk) dWk[c2 * d + kk] = ak;
+      if (dWv) dWv[c2 * d + kk] = av;
+    }
+  }
+  if (dWo) {
+#pragma omp parallel for schedule(static)
+    for (int64_t o = 0; o < d; ++o)
+      for (int64_t col = 0; col < nq; ++col) {
+        double acc = 0.0;
+        for (int64_t r = 0; r < n; ++r) acc += dy[r * d + o] * c[r * nq + col];
+        dWo[o * nq + col] = acc;
+      }
+  }
+  free(dv); free(dk); free(dq); free(dO); free(c); free(v); free(k); free(q);
+}

@@ -145,6 +145,76 @@ def small_case(N, d, d_ff, T_p, act, dtype="bf16", bias=False, seed=7, fwd_only=
                     b_std=(0.02 if bias else 0.0), seed_index=seed)
 
 
+@dataclasses.dataclass(frozen=True)
+class AttnWorkload:
+    """Head-sharded attention sublayer: B sequences of S tokens, model width d,
+    H query heads and Hkv key/value heads of width hd, T_p shards."""
+    name: str
+    B: int
+    S: int
+    d: int
+    H: int
+    Hkv: int
+    hd: int
+    T_p: int
+    causal: bool = True
+    dtype: str = "bf16"
+    seed_index: int = 0
+
+    @property
+    def N(self):
+        return self.B * self.S
+
+    def proj_flops(self):
+        """Q/K/V and output projections, forward."""
+        return 2 * self.N * self.d * (2 * self.H * self.hd + 2 * self.Hkv * self.hd)
+
+    def core_flops(self):
+        """q k^T and p v of every head, forward, counting only the visible
+        (causal: lower-triangle incl. diagonal) score entries."""
+        pairs = self.S * (self.S + 1) // 2 if self.causal else self.S * self.S
+        return 4 * self.B * self.H * pairs * self.hd
+
+    def fwd_flops(self):
+        return self.proj_flops() + self.core_flops()
+
+    def bwd_flops(self):
+        """Projections: 2x forward; core: dV, dP, dS-K, dS-Q = 2.5x forward
+        (recomputing the scores is not counted)."""
+        return 2 * self.proj_flops() + 5 * self.core_flops() // 2
+
+    def replace(self, **kw):
+        return dataclasses.replace(self, **kw)
+
+
+ATTN_WORKLOADS = {
+    w.name: w for w in [
+        AttnWorkload("megatron_8p3b_attention_bf16", 8, 1024, 3072, 24, 24, 128, 8, seed_index=7),
+        AttnWorkload("llama3_8b_attention_bf16", 1, 8192, 4096, 32, 8, 128, 8, seed_index=8),
+    ]
+}
+
+_ATTN_ORDER = ("x", "Wq", "Wk", "Wv", "Wo", "dy")
+
+
+def make_attention_inputs(w: AttnWorkload, seed: int | None = None):
+    """Host tensors of an attention workload: x [N, d] and dy [N, d] ~ N(0, 1);
+    Wq [H*hd, d], Wk, Wv [Hkv*hd, d] ~ N(0, 1/d); Wo [d, H*hd] ~ N(0, 1/(H*hd))."""
+    seed = BASE_SEED + w.seed_index if seed is None else seed
+    streams = np.random.SeedSequence(seed).spawn(len(_ATTN_ORDER))
+    rng = {k: np.random.Generator(np.random.PCG64(s)) for k, s in zip(_ATTN_ORDER, streams)}
+    dt = w.dtype
+    nq, nk = w.H * w.hd, w.Hkv * w.hd
+    return dict(
+        x=_draw(rng["x"], (w.N, w.d), 1.0, dt),
+        Wq=_draw(rng["Wq"], (nq, w.d), 1.0 / np.sqrt(w.d), dt),
+        Wk=_draw(rng["Wk"], (nk, w.d), 1.0 / np.sqrt(w.d), dt),
+        Wv=_draw(rng["Wv"], (nk, w.d), 1.0 / np.sqrt(w.d), dt),
+        Wo=_draw(rng["Wo"], (w.d, nq), 1.0 / np.sqrt(nq), dt),
+        dy=_draw(rng["dy"], (w.N, w.d), 1.0, dt),
+    )
+
+
 def to_f64(t):
     """Exact float64 widening of a host tensor (None passes through)."""
     if t is None:

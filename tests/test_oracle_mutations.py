@@ -11,6 +11,7 @@ import tempfile
 import pytest
 
 import oracle
+import tests.test_oracle_attention_pins as apins
 import tests.test_oracle_pins as pins
 
 _SRC = os.path.join(os.path.dirname(oracle.__file__), "tpffn_oracle.c")
@@ -31,6 +32,18 @@ MUTATIONS = {
                              "return 0.5 * (1.0 + th) + 0.5 * u * (1.0 - th) * dinner;"),
     "dx_skips_last_shard": ("for (int t = 0; t < T; ++t) acc += part[(int64_t)t * d + k];",
                             "for (int t = 0; t + 1 < T; ++t) acc += part[(int64_t)t * d + k];"),
+    # attention sublayer
+    "attn_kv_head_modulo": ("const int64_t hk = h / (C->H / C->Hkv);", "const int64_t hk = h % C->Hkv;"),
+    "attn_scale_without_sqrt": ("const double scale = 1.0 / sqrt((double)hd);", "const double scale = 1.0 / (double)hd;"),
+    "attn_causal_sees_next_key": ("const int64_t jmax = C->causal ? i : S - 1;",
+                                  "const int64_t jmax = C->causal ? (i + 1 < S ? i + 1 : i) : S - 1;"),
+    "attn_drops_rowdot": ("ds[j] = p[j] * (ds[j] - rowdot) * scale;", "ds[j] = p[j] * ds[j] * scale;"),
+    "attn_dv_uses_dS": ("av += P[row * S + j] * dO[(b * S + i) * nq + h * hd + jd];",
+                        "av += dS[row * S + j] * dO[(b * S + i) * nq + h * hd + jd];"),
+    "attn_wo_shard_rotated": ("part += A->Wo[o * nq + jj] * c_out[r * nq + jj];",
+                              "part += A->Wo[o * nq + (jj + s) % nq] * c_out[r * nq + jj];"),
+    "attn_dx_skips_v": ("part += dv[r * nk + c2] * A->Wv[c2 * d + kk];", "part += 0.0 * dv[r * nk + c2];"),
+    "attn_lse_drops_max": ("return m + log(sum);", "return log(sum);"),
 }
 
 
@@ -46,6 +59,16 @@ def _pin_calls():
         calls.append(lambda a=act, b=bias: pins.test_backward_matches_torch_autograd(a, b))
     for act in ("gelu_tanh", "swiglu"):
         calls.append(lambda a=act: pins.test_backward_central_finite_differences(a))
+    for case in apins.CORE_CASES:
+        calls.append(lambda c=case: apins.test_attn_core_matches_torch_sdpa_and_autograd(c))
+        calls.append(lambda c=case: apins.test_attn_core_key_shift_invariance_and_zero_key_gradient_sum(c))
+    for case in apins.SUB_CASES:
+        calls.append(lambda c=case: apins.test_attn_sublayer_matches_torch_linear_sdpa_and_autograd(c))
+    calls += [lambda: apins.test_attn_core_zero_queries_give_visible_means(True),
+              apins.test_attn_core_single_token_returns_value, apins.test_attn_core_central_finite_differences,
+              apins.test_attn_core_bf16_mode_rounds_only_its_outputs,
+              apins.test_attn_sublayer_independent_of_shard_count,
+              apins.test_attn_sublayer_finite_differences_of_x]
     return calls
 
 
