@@ -260,6 +260,94 @@ TPFFN_API int tp_ffn_bwd_seq_parallel(const tp_ffn_plan* plan, int64_t n_tokens,
                                       void* dw2p, void* db1, void* db2, void* workspace, size_t workspace_bytes,
                                       int flags, tp_stream_t stream);
 
+/* ------------------------------------------------------- attention sublayer
+ *
+ * The whole head-sharded self-attention sublayer of "7.9 Tensor and pipeline
+ * parallelism (TP, PP)", §2.2 "Attention, sharded": shard t owns the query
+ * heads [t*H/T_p, (t+1)*H/T_p) and the key/value heads [t*Hkv/T_p, ...) (the
+ * divisibility rule of "S17 Tensor & Pipeline Parallelism", "Attention shards
+ * by head, and GQA caps the degree"; query head h reads key/value head
+ * h / (H/Hkv)).  Per shard: column-sharded projections q, k, v = x W^(t)T,
+ * scaled dot-product attention of each of its heads (s = q k^T / sqrt(hd),
+ * optional causal mask, softmax, o = p v), and the row-sharded output
+ * projection y^(t) = c^(t) W_O^(t)T of its head outputs c^(t); y is the sum
+ * of the T_p shards in the order t = 0..T_p-1 (the g operator).  Backward: dc
+ * per shard (no sum), the attention gradients, dx = sum_t of the shards'
+ * q/k/v input gradients in the order t = 0..T_p-1 (the f operator), and the
+ * weight gradients of every shard.
+ *
+ * Tokens: B sequences of S tokens, sequence b in rows b*S .. b*S+S-1 of every
+ * [B*S][...] buffer.  All buffers bf16 row-major unless stated; every pointer
+ * 16-byte aligned (TP_ERR_ALIGN otherwise).
+ *
+ * Packed projection weights ("wqkv", [T_p * slice][d]): shard t's slice of
+ * slice = (H + 2*Hkv)/T_p * hd rows is [Wq rows of its query heads | Wk rows
+ * of its key heads | Wv rows of its value heads].  The packed q/k/v buffer
+ * ("qkv", [B*S][T_p * slice]) has the same column order: it is x wqkv^T.
+ * The packed output projection is the W_O packing of tp_attn_out_plan_create.
+ */
+typedef struct tp_attn_plan tp_attn_plan;
+
+/* d_model: model width (multiple of 8); head_dim: 128 only (the tensor-core
+ * kernels' tile); causal: 1 for the decoder mask (key j visible to query i
+ * iff j <= i), 0 for none; dtype: TP_BF16 only.
+ * Errors: TP_ERR_INVALID for NULL out, non-positive sizes, or when T_p does
+ * not divide n_heads and n_kv_heads or n_kv_heads does not divide n_heads;
+ * TP_ERR_UNSUPPORTED for head_dim != 128, d_model % 8 != 0 or TP_F32. */
+TPFFN_API int tp_attn_plan_create(tp_attn_plan** out, int64_t d_model, int n_heads, int n_kv_heads,
+                                  int64_t head_dim, int T_p, int causal, int dtype);
+TPFFN_API void tp_attn_plan_destroy(tp_attn_plan* plan);
+/* qkv_width = T_p * slice; slice, and its query / key widths sq = H/T_p*hd,
+ * sk = Hkv/T_p*hd (any pointer may be NULL). */
+TPFFN_API int tp_attn_plan_info(const tp_attn_plan* plan, int64_t* qkv_width, int64_t* slice, int64_t* sq,
+                                int64_t* sk);
+
+/* TP_PACK_COLUMNS: bytes of wqkv; TP_PACK_ROWS: bytes of the packed W_O. */
+TPFFN_API size_t tp_attn_packed_bytes(const tp_attn_plan* plan, int which);
+/* Wq [H*hd][d], Wk, Wv [Hkv*hd][d], Wo [d][H*hd] (row-major [out][in]) into
+ * the packed forms, and back. */
+TPFFN_API int tp_attn_shard_weights(const tp_attn_plan* plan, const void* Wq, const void* Wk, const void* Wv,
+                                    const void* Wo, void* wqkv, void* wo_packed, tp_stream_t stream);
+TPFFN_API int tp_attn_unshard_weights(const tp_attn_plan* plan, const void* wqkv, const void* wo_packed, void* Wq,
+                                      void* Wk, void* Wv, void* Wo, tp_stream_t stream);
+
+/* Activations the forward saves for the backward, in one buffer of
+ * tp_attn_saved_bytes(plan, B, S) bytes: qkv [B*S][qkv_width] at *qkv_off,
+ * the head outputs c [B*S][H*hd] at *c_off, and the log-sum-exp of every
+ * softmax row, fp32 [B*H][S_pad] with S_pad = S rounded up to 128, in the
+ * base-2 domain (log2 of sum_j 2^(s_ij log2 e)), at *lse_off. */
+TPFFN_API size_t tp_attn_saved_bytes(const tp_attn_plan* plan, int64_t B, int64_t S);
+TPFFN_API int tp_attn_saved_offsets(const tp_attn_plan* plan, int64_t B, int64_t S, size_t* qkv_off,
+                                    size_t* c_off, size_t* lse_off);
+/* Workspace of every tp_attn_* pass for this shape and these flags. */
+TPFFN_API size_t tp_attn_workspace_bytes(const tp_attn_plan* plan, int64_t B, int64_t S, int flags);
+
+/* Forward: y [B*S][d] from x [B*S][d]; fills `saved`.  Flags as tp_ffn_fwd
+ * (TP_SUM_* choose how the output projection sums its shards).
+ * Launches: q/k/v GEMM, attention kernel, output-projection GEMM (+ sum). */
+TPFFN_API int tp_attn_fwd(const tp_attn_plan* plan, int64_t B, int64_t S, const void* x, const void* wqkv,
+                          const void* wo_packed, void* y, void* saved, void* workspace, size_t workspace_bytes,
+                          int flags, tp_stream_t stream);
+/* Backward from dy [B*S][d]: dx [B*S][d]; dwqkv (packed like wqkv) and
+ * dwo_packed (packed like W_O) are overwritten with this call's gradients. */
+TPFFN_API int tp_attn_bwd(const tp_attn_plan* plan, int64_t B, int64_t S, const void* x, const void* wqkv,
+                          const void* wo_packed, const void* saved, const void* dy, void* dx, void* dwqkv,
+                          void* dwo_packed, void* workspace, size_t workspace_bytes, int flags, tp_stream_t stream);
+
+/* The attention core alone, on a caller's packed qkv [B*S][qkv_width]:
+ * o [B*S][H*hd] (head h in columns [h*hd, (h+1)*hd)) and lse as in `saved`.
+ * Backward: dqkv [B*S][qkv_width] (packed like qkv) from dO [B*S][H*hd],
+ * given the forward's o and lse.  workspace: tp_attn_workspace_bytes. */
+TPFFN_API int tp_attn_core_fwd(const tp_attn_plan* plan, int64_t B, int64_t S, const void* qkv, void* o,
+                               float* lse, void* workspace, size_t workspace_bytes, int flags, tp_stream_t stream);
+TPFFN_API int tp_attn_core_bwd(const tp_attn_plan* plan, int64_t B, int64_t S, const void* qkv, const void* o,
+                               const float* lse, const void* dO, void* dqkv, void* workspace,
+                               size_t workspace_bytes, int flags, tp_stream_t stream);
+
+/* Diagnostics of attention calls, as their tp_ffn_* counterparts. */
+TPFFN_API int tp_attn_kernel_times(const tp_attn_plan* plan, int max, const char** names, float* ms);
+TPFFN_API int tp_attn_last_launch_count(const tp_attn_plan* plan);
+
 /* ------------------------------------------------ forward without allocation */
 
 /* Size of the library's static scratch array (32 MiB).  Every GPU that loads

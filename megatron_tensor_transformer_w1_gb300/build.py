@@ -22,7 +22,7 @@ BUILD = os.path.join(ROOT, "_build", platform.machine()  # objects never cross a
                      + ("-" + "-".join(x.strip("-").replace("=", "_") for x in os.environ.get("TPFFN_NVCC_EXTRA", "").split())
                         if os.environ.get("TPFFN_NVCC_EXTRA") else ""))
 LIB = os.path.join(PKG, "libtpffn.so")
-SOURCES = ["tp_gemm_tc.cu", "tp_kernels.cu", "tp_api.cu", "tp_static.cu"]
+SOURCES = ["tp_gemm_tc.cu", "tp_attention.cu", "tp_kernels.cu", "tp_api.cu", "tp_static.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC,-fvisibility=hidden", "-I", INCLUDE, "-I", CSRC]
 # extra nvcc flags (e.g. -DTPFFN_INSTRUMENT for per-CTA wait counters); part of the build stamp

@@ -22,6 +22,7 @@
 #include <cstdint>
 #include <cstdlib>
 #include <cstring>
+#include <initializer_list>
 #include <mutex>
 #include <new>
 #include <string>
@@ -851,5 +852,359 @@ int tp_ffn_kernel_times(const tp_ffn_plan* p, int max, const char** names, float
 }
 
 int tp_ffn_last_launch_count(const tp_ffn_plan* p) { return p ? p->last_launches : -1; }
+
+// ------------------------------------------------------ attention sublayer
+// "7.9 Tensor and pipeline parallelism (TP, PP)", §2.2 "Attention, sharded".
+// Forward: qkv = x wqkv^T (one GEMM over all shards' column slices), the
+// attention core, then the row-sharded output projection of the inner
+// act-NONE plan with its ordered shard-sum.  Backward: that projection's
+// backward (dc per shard, dW_O), the attention-core backward (dqkv), dx =
+// sum_t dqkv^(t) wqkv^(t) in shard order (fused K loop or partials + sum), and
+// dwqkv = dqkv^T x (one GEMM: the packed weight is shard-major).
+struct tp_attn_plan {
+  tp_ffn_plan* wo = nullptr;  // output projection (act NONE, d_ff = H * hd)
+  int64_t d = 0, hd = 0;
+  int H = 0, Hkv = 0, T_p = 1, causal = 1;
+  int64_t sq = 0, sk = 0, slice = 0, W = 0;
+};
+
+namespace {
+int64_t seq_pad(int64_t S) { return (S + 127) / 128 * 128; }
+
+struct AttnSaved {
+  size_t qkv = 0, c = 0, lse = 0, total = 0;
+};
+AttnSaved attn_saved(const tp_attn_plan* a, int64_t B, int64_t S) {
+  AttnSaved L;
+  const size_t n = static_cast<size_t>(B) * S;
+  L.qkv = 0;
+  L.c = align_up(n * a->W * 2);
+  L.lse = L.c + align_up(n * a->H * a->hd * 2);
+  L.total = L.lse + align_up(static_cast<size_t>(B) * a->H * seq_pad(S) * 4);
+  return L;
+}
+
+struct AttnWs {
+  size_t wo = 0, wo_bytes = 0, dc = 0, dqkv = 0, Dv = 0, total = 0;
+};
+AttnWs attn_ws(const tp_attn_plan* a, int64_t B, int64_t S, int flags) {
+  AttnWs L;
+  const size_t n = static_cast<size_t>(B) * S;
+  size_t off = kAlign;  // error word
+  L.wo = off;
+  L.wo_bytes = ws_layout(a->wo, static_cast<int64_t>(n), flags).total;
+  off += align_up(L.wo_bytes);
+  L.dc = off;
+  off += align_up(n * a->H * a->hd * 2);
+  L.dqkv = off;
+  off += align_up(n * a->W * 2);
+  L.Dv = off;
+  off += align_up(static_cast<size_t>(B) * a->H * seq_pad(S) * 4);
+  L.total = off;
+  return L;
+}
+
+AttnSpec attn_spec(const tp_attn_plan* a, int64_t B, int64_t S) {
+  AttnSpec sp;
+  sp.B = static_cast<int>(B);
+  sp.S = static_cast<int>(S);
+  sp.H = a->H;
+  sp.Hkv = a->Hkv;
+  sp.T_p = a->T_p;
+  sp.causal = a->causal;
+  sp.hd = a->hd;
+  sp.qkv_rs = a->W;
+  sp.o_rs = a->H * a->hd;
+  sp.do_rs = a->H * a->hd;
+  sp.s_pad = seq_pad(S);
+  return sp;
+}
+
+int attn_check(const tp_attn_plan* a, int64_t B, int64_t S, size_t ws_bytes, const void* workspace, int flags,
+               std::initializer_list<const void*> ptrs) {
+  if (!a || B < 0 || S < 0 || !workspace) return TP_ERR_INVALID;
+  if (B > (int64_t(1) << 24) || S > (int64_t(1) << 24) || B * S > (int64_t(1) << 30)) return TP_ERR_UNSUPPORTED;
+  if ((flags & TP_SUM_FUSED) && (flags & TP_SUM_OVERLAP)) return TP_ERR_INVALID;
+  if (ws_bytes < attn_ws(a, B, S, flags).total) return TP_ERR_INVALID;
+  for (const void* q : ptrs) {
+    if (!q) return TP_ERR_INVALID;
+    if (!aligned16(q)) return TP_ERR_ALIGN;
+  }
+  if (!aligned16(workspace)) return TP_ERR_ALIGN;
+  return TP_OK;
+}
+}  // namespace
+
+int tp_attn_plan_create(tp_attn_plan** out, int64_t d_model, int n_heads, int n_kv_heads, int64_t head_dim, int T_p,
+                        int causal, int dtype) {
+  if (!out) return TP_ERR_INVALID;
+  *out = nullptr;
+  if (d_model < 1 || n_heads < 1 || n_kv_heads < 1 || head_dim < 1 || T_p < 1) return TP_ERR_INVALID;
+  if (n_heads % T_p || n_kv_heads % T_p || n_heads % n_kv_heads) return TP_ERR_INVALID;
+  if (dtype != TP_BF16 && dtype != TP_F32) return TP_ERR_INVALID;
+  if (dtype != TP_BF16 || head_dim != 128 || d_model % 8) return TP_ERR_UNSUPPORTED;
+  tp_attn_plan* a = new (std::nothrow) tp_attn_plan();
+  if (!a) return TP_ERR_INVALID;
+  int rc = tp_attn_out_plan_create(&a->wo, d_model, n_heads, n_kv_heads, head_dim, T_p, dtype);
+  if (rc) {
+    delete a;
+    return rc;
+  }
+  a->d = d_model;
+  a->hd = head_dim;
+  a->H = n_heads;
+  a->Hkv = n_kv_heads;
+  a->T_p = T_p;
+  a->causal = causal ? 1 : 0;
+  a->sq = static_cast<int64_t>(n_heads / T_p) * head_dim;
+  a->sk = static_cast<int64_t>(n_kv_heads / T_p) * head_dim;
+  a->slice = a->sq + 2 * a->sk;
+  a->W = a->slice * T_p;
+  *out = a;
+  return TP_OK;
+}
+
+void tp_attn_plan_destroy(tp_attn_plan* a) {
+  if (!a) return;
+  tp_ffn_plan_destroy(a->wo);
+  delete a;
+}
+
+int tp_attn_plan_info(const tp_attn_plan* a, int64_t* qkv_width, int64_t* slice, int64_t* sq, int64_t* sk) {
+  if (!a) return TP_ERR_INVALID;
+  if (qkv_width) *qkv_width = a->W;
+  if (slice) *slice = a->slice;
+  if (sq) *sq = a->sq;
+  if (sk) *sk = a->sk;
+  return TP_OK;
+}
+
+size_t tp_attn_packed_bytes(const tp_attn_plan* a, int which) {
+  if (!a) return 0;
+  if (which == TP_PACK_COLUMNS) return static_cast<size_t>(a->W) * a->d * 2;
+  if (which == TP_PACK_ROWS) return tp_ffn_packed_bytes(a->wo, TP_PACK_ROWS);
+  return 0;
+}
+
+int tp_attn_shard_weights(const tp_attn_plan* a, const void* Wq, const void* Wk, const void* Wv, const void* Wo,
+                          void* wqkv, void* wo_packed, tp_stream_t stream) {
+  if (!a || !Wo || !wo_packed) return TP_ERR_INVALID;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  int rc = launch_pack_qkv(Wq, Wk, Wv, wqkv, a->T_p, a->sq, a->sk, a->d, 0, st);
+  return rc ? rc : tp_ffn_shard_rows(a->wo, Wo, wo_packed, stream);
+}
+
+int tp_attn_unshard_weights(const tp_attn_plan* a, const void* wqkv, const void* wo_packed, void* Wq, void* Wk,
+                            void* Wv, void* Wo, tp_stream_t stream) {
+  if (!a || !Wo || !wo_packed) return TP_ERR_INVALID;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  int rc = launch_pack_qkv(Wq, Wk, Wv, const_cast<void*>(wqkv), a->T_p, a->sq, a->sk, a->d, 1, st);
+  return rc ? rc : tp_ffn_unshard_rows(a->wo, wo_packed, Wo, stream);
+}
+
+size_t tp_attn_saved_bytes(const tp_attn_plan* a, int64_t B, int64_t S) {
+  if (!a || B < 0 || S < 0) return 0;
+  return attn_saved(a, B, S).total;
+}
+
+int tp_attn_saved_offsets(const tp_attn_plan* a, int64_t B, int64_t S, size_t* qkv_off, size_t* c_off,
+                          size_t* lse_off) {
+  if (!a || B < 0 || S < 0) return TP_ERR_INVALID;
+  const AttnSaved L = attn_saved(a, B, S);
+  if (qkv_off) *qkv_off = L.qkv;
+  if (c_off) *c_off = L.c;
+  if (lse_off) *lse_off = L.lse;
+  return TP_OK;
+}
+
+size_t tp_attn_workspace_bytes(const tp_attn_plan* a, int64_t B, int64_t S, int flags) {
+  if (!a || B < 0 || S < 0) return 0;
+  return attn_ws(a, B, S, flags).total;
+}
+
+int tp_attn_fwd(const tp_attn_plan* a, int64_t B, int64_t S, const void* x, const void* wqkv, const void* wo_packed,
+                void* y, void* saved, void* workspace, size_t workspace_bytes, int flags, tp_stream_t stream) {
+  int rc = attn_check(a, B, S, workspace_bytes, workspace, flags, {x, wqkv, wo_packed, y, saved});
+  if (rc) return rc;
+  const int64_t n = B * S;
+  if (n == 0) {
+    a->wo->last_launches = 0;
+    return TP_OK;
+  }
+  LaunchCtx ctx;
+  rc = make_ctx(a->wo, workspace, flags, reinterpret_cast<cudaStream_t>(stream), ctx);
+  if (rc) return rc;
+  const AttnSaved SV = attn_saved(a, B, S);
+  const AttnWs L = attn_ws(a, B, S, flags);
+  char* sv = static_cast<char*>(saved);
+  char* ws = static_cast<char*>(workspace);
+  // q, k, v of every shard: one GEMM over the shard-major packed weight
+  GemmSpec g;
+  g.name = "qkv_proj";
+  g.M = n;
+  g.N = a->W;
+  g.K = a->d;
+  g.A = kmajor(x, a->d, n, 1, a->d, n * a->d, 0, 0);
+  g.B = kmajor(wqkv, a->d, a->W, 1, a->d, a->W * a->d, 0, 0);
+  g.epi = EPI_OUT;
+  g.out = sv + SV.qkv;
+  g.out_rs = a->W;
+  g.n_store = a->W;
+  g.out_bf16 = 1;
+  rc = run_gemm(a->wo, g, ctx);
+  if (!rc) {
+    AttnSpec sp = attn_spec(a, B, S);
+    sp.qkv = sv + SV.qkv;
+    sp.o = sv + SV.c;
+    sp.lse = reinterpret_cast<float*>(sv + SV.lse);
+    rc = launch_attn_fwd(sp, ctx);
+  }
+  if (!rc)
+    rc = fwd_impl(a->wo, n, sv + SV.c, nullptr, wo_packed, nullptr, nullptr, y, nullptr, nullptr, ws + L.wo, flags,
+                  ctx, nullptr);
+  return finish_call(a->wo, ctx, rc, flags, workspace);
+}
+
+int tp_attn_bwd(const tp_attn_plan* a, int64_t B, int64_t S, const void* x, const void* wqkv, const void* wo_packed,
+                const void* saved, const void* dy, void* dx, void* dwqkv, void* dwo_packed, void* workspace,
+                size_t workspace_bytes, int flags, tp_stream_t stream) {
+  int rc = attn_check(a, B, S, workspace_bytes, workspace, flags,
+                      {x, wqkv, wo_packed, saved, dy, dx, dwqkv, dwo_packed});
+  if (rc) return rc;
+  const int64_t n = B * S;
+  if (n == 0) {
+    a->wo->last_launches = 0;
+    return TP_OK;
+  }
+  LaunchCtx ctx;
+  rc = make_ctx(a->wo, workspace, flags, reinterpret_cast<cudaStream_t>(stream), ctx);
+  if (rc) return rc;
+  const AttnSaved SV = attn_saved(a, B, S);
+  const AttnWs L = attn_ws(a, B, S, flags);
+  const char* sv = static_cast<const char*>(saved);
+  char* ws = static_cast<char*>(workspace);
+  const bool fused = (flags & TP_SUM_FUSED) != 0;
+  const int64_t T = a->T_p, d = a->d, W = a->W, sl = a->slice;
+  // 1. output projection backward: dc per shard (no sum), dW_O
+  rc = bwd_impl(a->wo, n, sv + SV.c, nullptr, wo_packed, nullptr, dy, ws + L.dc, nullptr, nullptr, dwo_packed,
+                nullptr, nullptr, ws + L.wo, flags, ctx, nullptr);
+  // 2. attention core backward -> dqkv
+  if (!rc) {
+    AttnSpec sp = attn_spec(a, B, S);
+    sp.qkv = sv + SV.qkv;
+    sp.o = const_cast<char*>(sv + SV.c);
+    sp.lse = reinterpret_cast<float*>(const_cast<char*>(sv + SV.lse));
+    sp.dO = ws + L.dc;
+    sp.Dv = reinterpret_cast<float*>(ws + L.Dv);
+    sp.dqkv = ws + L.dqkv;
+    rc = launch_attn_bwd(sp, ctx);
+  }
+  // 3. dx = sum_t dqkv^(t) wqkv^(t)   (f operator, shard order)
+  if (!rc) {
+    const void* dq = ws + L.dqkv;
+    GemmSpec g;
+    g.M = n;
+    g.N = d;
+    g.K = sl;
+    g.A = kmajor(dq, sl, n, T, W, sl, 0, 0);
+    g.B = mnmajor(wqkv, d, sl, T, d, sl * d, 0, 0);
+    g.n_store = d;
+    g.out_bf16 = 1;
+    if (fused) {
+      g.name = "attn_dgrad_x_fused_sum";
+      g.NB = 1;
+      g.G = static_cast<int>(T);
+      g.A.gsel = 1;
+      g.B.gsel = 1;
+      g.epi = EPI_OUT;
+      g.out = dx;
+      g.out_rs = d;
+      rc = run_gemm(a->wo, g, ctx);
+    } else {
+      // the output projection's partial buffer is free again: reuse it
+      float* part = reinterpret_cast<float*>(ws + L.wo + ws_layout(a->wo, n, flags).part);
+      g.name = "attn_dgrad_x_partials";
+      g.NB = static_cast<int>(T);
+      g.A.bsel = 1;
+      g.B.bsel = 1;
+      g.epi = EPI_F32;
+      g.out = part;
+      g.out_bs = n * d;
+      g.out_rs = d;
+      if (flags & TP_SUM_OVERLAP) {
+        rc = gemm_sum_overlapped(a->wo, g, ctx, part, n, d, nullptr, dx, 1, "attn_shard_sum_dx");
+      } else {
+        rc = run_gemm(a->wo, g, ctx);
+        if (!rc) rc = launch_shard_sum(part, static_cast<int>(T), n, d, nullptr, dx, 1, ctx, "attn_shard_sum_dx");
+      }
+    }
+  }
+  // 4. dwqkv = dqkv^T x, every shard's slice in one GEMM
+  if (!rc) {
+    GemmSpec g;
+    g.name = "attn_wgrad_qkv";
+    g.M = W;
+    g.N = d;
+    g.K = n;
+    g.A = mnmajor(ws + L.dqkv, W, n, 1, W, n * W, 0, 0);
+    g.B = mnmajor(x, d, n, 1, d, n * d, 0, 0);
+    g.epi = EPI_OUT;
+    g.out = dwqkv;
+    g.out_rs = d;
+    g.n_store = d;
+    g.out_bf16 = 1;
+    rc = run_gemm(a->wo, g, ctx);
+  }
+  return finish_call(a->wo, ctx, rc, flags, workspace);
+}
+
+int tp_attn_core_fwd(const tp_attn_plan* a, int64_t B, int64_t S, const void* qkv, void* o, float* lse,
+                     void* workspace, size_t workspace_bytes, int flags, tp_stream_t stream) {
+  int rc = attn_check(a, B, S, workspace_bytes, workspace, flags, {qkv, o, lse});
+  if (rc) return rc;
+  if (B * S == 0) {
+    a->wo->last_launches = 0;
+    return TP_OK;
+  }
+  LaunchCtx ctx;
+  rc = make_ctx(a->wo, workspace, flags, reinterpret_cast<cudaStream_t>(stream), ctx);
+  if (rc) return rc;
+  AttnSpec sp = attn_spec(a, B, S);
+  sp.qkv = qkv;
+  sp.o = o;
+  sp.lse = lse;
+  rc = launch_attn_fwd(sp, ctx);
+  return finish_call(a->wo, ctx, rc, flags, workspace);
+}
+
+int tp_attn_core_bwd(const tp_attn_plan* a, int64_t B, int64_t S, const void* qkv, const void* o, const float* lse,
+                     const void* dO, void* dqkv, void* workspace, size_t workspace_bytes, int flags,
+                     tp_stream_t stream) {
+  int rc = attn_check(a, B, S, workspace_bytes, workspace, flags, {qkv, o, lse, dO, dqkv});
+  if (rc) return rc;
+  if (B * S == 0) {
+    a->wo->last_launches = 0;
+    return TP_OK;
+  }
+  LaunchCtx ctx;
+  rc = make_ctx(a->wo, workspace, flags, reinterpret_cast<cudaStream_t>(stream), ctx);
+  if (rc) return rc;
+  const AttnWs L = attn_ws(a, B, S, flags);
+  AttnSpec sp = attn_spec(a, B, S);
+  sp.qkv = qkv;
+  sp.o = const_cast<void*>(o);
+  sp.lse = const_cast<float*>(lse);
+  sp.dO = dO;
+  sp.Dv = reinterpret_cast<float*>(static_cast<char*>(workspace) + L.Dv);
+  sp.dqkv = dqkv;
+  rc = launch_attn_bwd(sp, ctx);
+  return finish_call(a->wo, ctx, rc, flags, workspace);
+}
+
+int tp_attn_kernel_times(const tp_attn_plan* a, int max, const char** names, float* ms) {
+  return a ? tp_ffn_kernel_times(a->wo, max, names, ms) : -1;
+}
+
+int tp_attn_last_launch_count(const tp_attn_plan* a) { return a ? a->wo->last_launches : -1; }
 
 }  // extern "C"

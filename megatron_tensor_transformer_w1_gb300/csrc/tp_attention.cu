@@ -1,0 +1,1165 @@
+// tp_attention.cu -- the attention core of the head-sharded attention sublayer.
+//
+// "7.9 Tensor and pipeline parallelism (TP, PP)", §2.2 "Attention, sharded":
+// each shard owns H/T_p query heads and Hkv/T_p key/value heads (the GQA
+// divisibility rule of "S17 Tensor & Pipeline Parallelism", "Attention shards
+// by head, and GQA caps the degree"), and computes the scaled dot-product
+// attention of its heads from its own Q/K/V columns -- no exchange happens
+// before the row-sharded output projection.  Per head, with hd = 128:
+//   s_ij = q_i . k_j / sqrt(hd)  (j <= i when causal),  p_i = softmax(s_i),
+//   o_i = sum_j p_ij v_j;
+// backward: dP_ij = dO_i . v_j, D_i = dO_i . o_i, dS_ij = p_ij (dP_ij - D_i),
+//   dq = dS k / sqrt(hd), dk = dS^T q / sqrt(hd), dv = P^T dO.
+//
+// Blackwell design (sm_103a), three persistent kernels of 192 threads, one
+// CTA per SM:  warp 0 issues TMA copies (128-byte swizzle, zero fill past the
+// end of a sequence), one lane of warp 1 issues tcgen05.mma (bf16 in, fp32
+// accumulators in tensor memory), warps 2..5 own one TMEM lane -- one row of
+// the 128-row tile -- each, so every row reduction (max, sum) stays in one
+// thread.  Probabilities and score gradients are written by those threads to
+// shared memory in the swizzled K-major layout the MMA reads; nothing of size
+// S x S ever reaches global memory.
+//
+//  * forward (per query head and 128-query block): S = Q K^T into one of two
+//    TMEM buffers while the softmax threads work on the other; online softmax
+//    in the log2 domain with a lazy rescale (the running maximum only moves
+//    when it grew by more than 2^8, so the O accumulator in TMEM is rarely
+//    read back); O += P V; output o / l in bf16 and the log-sum-exp.
+//  * dq (per query head and 128-query block, 64-key blocks): S and dP into
+//    double-buffered TMEM, p recomputed from the log-sum-exp, dS to shared
+//    memory, dQ += dS K in TMEM.
+//  * dk/dv (per key/value head and 128-key block, 64-query blocks of every
+//    query head of its GQA group): S^T and dP^T, P^T and dS^T to shared
+//    memory, dV += P^T dO and dK += dS^T Q in TMEM -- the whole group's sum
+//    stays in fp32 and is rounded once.
+// No atomics anywhere: the results are bit-identical run to run.
+//
+// Every mbarrier wait is bounded (device error word + CTA abort flag, then
+// in-flight copies and MMAs are drained and tensor memory is freed).
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include <atomic>
+#include <cmath>
+#include <cstdint>
+
+#include "tc_ptx.cuh"
+#include "tp_internal.h"
+#include "tpffn.h"
+
+namespace tpffn {
+namespace attn {
+using namespace tc;
+
+constexpr int HD = 128;            // head width
+constexpr int TILE = 128 * HD * 2; // [128 rows][128 cols] bf16: two 64-column boxes
+constexpr int NT = 192;            // producer warp, MMA warp, 4 softmax warps
+constexpr int NSM = 128;           // softmax threads
+
+// Column geometry of the packed q/k/v buffer (see AttnSpec).
+struct Geo {
+  int hq_per, hk_per, sq, sk, slice;
+  __device__ __forceinline__ int qcol(int h) const { return (h / hq_per) * slice + (h % hq_per) * HD; }
+  __device__ __forceinline__ int kcol(int hk) const { return (hk / hk_per) * slice + sq + (hk % hk_per) * HD; }
+  __device__ __forceinline__ int vcol(int hk) const { return kcol(hk) + sk; }
+};
+
+struct Params {
+  Geo g;
+  int B, S, H, Hkv, G, causal;
+  int n_qb;    // 128-row blocks per sequence
+  int n_b64;   // 64-row blocks per sequence
+  int items;
+  __nv_bfloat16* o;
+  long long o_rs;
+  const __nv_bfloat16* dO;
+  long long do_rs;
+  float* lse;
+  long long s_pad;
+  float* Dv;
+  __nv_bfloat16* dqkv;
+  long long dqkv_rs;
+  float scale_log2;  // log2(e) / sqrt(hd)
+  float scale;       // 1 / sqrt(hd)
+  int* err;
+  unsigned long long timeout_ns;
+};
+
+// ------------------------------------------------------------ PTX helpers
+__device__ __forceinline__ uint8_t* align1024(uint8_t* p) {
+  return reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(p) + 1023) & ~uintptr_t(1023));
+}
+__device__ __forceinline__ void fence_async_smem() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
+__device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
+  asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c), "r"(d) : "memory");
+}
+__device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(smem_u32(bar))
+      : "memory");
+}
+__device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], "
+      "{%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,"
+      "%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};" ::"r"(taddr),
+      "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]),
+      "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15]), "r"(r[16]),
+      "r"(r[17]), "r"(r[18]), "r"(r[19]), "r"(r[20]), "r"(r[21]), "r"(r[22]), "r"(r[23]), "r"(r[24]),
+      "r"(r[25]), "r"(r[26]), "r"(r[27]), "r"(r[28]), "r"(r[29]), "r"(r[30]), "r"(r[31])
+      : "memory");
+}
+__device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
+
+// Shared-memory descriptor of a 128-byte-swizzled tile (version 1, SBO 1024).
+__device__ __forceinline__ uint64_t sw128_desc(uint32_t addr, uint32_t lbo) {
+  return static_cast<uint64_t>((addr & 0x3FFFFu) >> 4) | (static_cast<uint64_t>(lbo >> 4) << 16) |
+         (static_cast<uint64_t>(1024u >> 4) << 32) | (1ull << 46) | (2ull << 61);
+}
+// K-major operand: `rows` rows x 128 K-columns held as two 64-column boxes of
+// rows*128 bytes; K step ks covers columns [16 ks, 16 ks + 16).
+__device__ __forceinline__ uint64_t kdesc(uint32_t tile, int rows, int ks) {
+  return sw128_desc(tile + static_cast<uint32_t>((ks >> 2) * rows * 128 + (ks & 3) * 32), 16);
+}
+// MN-major operand: `krows` rows along K, 128 M/N columns held as two boxes
+// of krows*128 bytes; K step ks covers rows [16 ks, 16 ks + 16).
+__device__ __forceinline__ uint64_t mndesc(uint32_t tile, int krows, int ks) {
+  return sw128_desc(tile + static_cast<uint32_t>(ks * 2048), static_cast<uint32_t>(krows * 128));
+}
+// Instruction descriptor, kind::f16, M = 128, bf16 x bf16 -> fp32.
+__host__ __device__ constexpr uint32_t idesc(int N, int amn, int bmn) {
+  return (1u << 4) | (1u << 7) | (1u << 10) | (static_cast<uint32_t>(amn) << 15) |
+         (static_cast<uint32_t>(bmn) << 16) | (static_cast<uint32_t>(N >> 3) << 17) | (8u << 24);
+}
+// Address of 16-byte chunk col8 (= column / 8) of row r of a thread-written
+// K-major swizzled tile of `rows` rows (the layout TMA's 128-byte swizzle
+// gives: chunk index XOR row mod 8 inside each 1024-byte group of 8 rows).
+__device__ __forceinline__ uint32_t sw_chunk(uint32_t tile, int rows, int r, int col8) {
+  return tile + static_cast<uint32_t>((col8 >> 3) * rows * 128 + r * 128 + (((col8 & 7) ^ (r & 7)) << 4));
+}
+
+struct Waiter {
+  volatile int* abort_flag;
+  int* err;
+  unsigned long long timeout_ns;
+  __device__ __forceinline__ bool operator()(uint64_t* bar, uint32_t parity) const {
+    return wait_bounded_raw(bar, parity, abort_flag, err, timeout_ns, true);
+  }
+  // drain wait: ignores the abort flag
+  __device__ __forceinline__ void drain(uint64_t* bar, uint32_t parity) const {
+    wait_bounded_raw(bar, parity, abort_flag, err, timeout_ns, false);
+  }
+  // warp-uniform wait of the softmax warps
+  __device__ __forceinline__ bool warp(uint64_t* bar, uint32_t parity) const {
+    const bool ok = wait_bounded_raw(bar, parity, abort_flag, err, timeout_ns, true);
+    return __all_sync(0xffffffffu, ok) != 0;
+  }
+};
+
+// Query-major items, heaviest first under the causal mask: item ->
+// (128-row block, sequence, head).
+__device__ __forceinline__ void decode_item(const Params& p, int item, int heads, bool heavy_last_block, int& blk,
+                                            int& b, int& h) {
+  const int per = p.B * heads;
+  const int r = item / per;
+  blk = heavy_last_block ? p.n_qb - 1 - r : r;
+  const int bh = item - r * per;
+  b = bh / heads;
+  h = bh - b * heads;
+}
+
+__device__ __forceinline__ void store_row_bf16(__nv_bfloat16* dst, const uint32_t (&r)[32], float mul) {
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    uint4 v;
+    v.x = pack_bf16x2(__uint_as_float(r[q * 8 + 0]) * mul, __uint_as_float(r[q * 8 + 1]) * mul);
+    v.y = pack_bf16x2(__uint_as_float(r[q * 8 + 2]) * mul, __uint_as_float(r[q * 8 + 3]) * mul);
+    v.z = pack_bf16x2(__uint_as_float(r[q * 8 + 4]) * mul, __uint_as_float(r[q * 8 + 5]) * mul);
+    v.w = pack_bf16x2(__uint_as_float(r[q * 8 + 6]) * mul, __uint_as_float(r[q * 8 + 7]) * mul);
+    *reinterpret_cast<uint4*>(dst + q * 8) = v;
+  }
+}
+
+// ================================================================ forward
+constexpr int F_Q = 0;
+constexpr int F_K = F_Q + TILE;       // 2 stages
+constexpr int F_V = F_K + 2 * TILE;   // 2 stages
+constexpr int F_P = F_V + 2 * TILE;   // P [128 q][128 keys]
+constexpr int F_BAR = F_P + TILE;
+constexpr int F_SMEM = F_BAR + 256 + 1024;
+
+__global__ void __launch_bounds__(NT, 1) attn_fwd_kernel(const __grid_constant__ CUtensorMap tq, const Params p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = align1024(smem_raw);
+  uint64_t* bar = reinterpret_cast<uint64_t*>(smem + F_BAR);
+  uint64_t* q_full = bar + 0;
+  uint64_t* q_empty = bar + 1;
+  uint64_t* k_full = bar + 2;
+  uint64_t* k_empty = bar + 4;
+  uint64_t* v_full = bar + 6;
+  uint64_t* v_empty = bar + 8;
+  uint64_t* s_full = bar + 10;
+  uint64_t* s_empty = bar + 12;
+  uint64_t* p_full = bar + 14;
+  uint64_t* pv_done = bar + 15;
+  uint64_t* o_empty = bar + 16;
+  uint64_t* drain = bar + 17;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bar + 18);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(bar + 18) + 1;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+  if (threadIdx.x == 0) {
+    mbar_init(q_full, 1);
+    mbar_init(q_empty, 1);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&k_full[i], 1);
+      mbar_init(&k_empty[i], 1);
+      mbar_init(&v_full[i], 1);
+      mbar_init(&v_empty[i], 1);
+      mbar_init(&s_full[i], 1);
+      mbar_init(&s_empty[i], NSM);
+    }
+    mbar_init(p_full, NSM);
+    mbar_init(pv_done, 1);
+    mbar_init(o_empty, NSM);
+    mbar_init(drain, 1);
+    *abort_flag = 0;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+  }
+  if (warp == 0 && lane == 0) prefetch_tmap(&tq);
+  if (warp == 1) tmem_alloc(tmem_slot, 512);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;  // S buffers at columns 0 and 128, O at 256
+  const Waiter W{abort_flag, p.err, p.timeout_ns};
+
+  if (warp == 0) {
+    // ------------------------------------------------ TMA producer
+    if (lane == 0) {
+      int q_last = -1, k_last[2] = {-1, -1}, v_last[2] = {-1, -1};
+      uint32_t kv = 0, it = 0;
+      bool ok = true;
+      for (int item = blockIdx.x; item < p.items && ok; item += gridDim.x, ++it) {
+        int qb, b, h;
+        decode_item(p, item, p.H, p.causal != 0, qb, b, h);
+        const int nkb = p.causal ? qb + 1 : p.n_qb;
+        if (!W(q_empty, (it & 1u) ^ 1u)) break;
+        mbar_arrive_expect_tx(q_full, TILE);
+        const int qc = p.g.qcol(h);
+        tma_load_3d(smem + F_Q, &tq, q_full, qc, qb * 128, b);
+        tma_load_3d(smem + F_Q + TILE / 2, &tq, q_full, qc + 64, qb * 128, b);
+        q_last = static_cast<int>(it & 1u);
+        const int hk = h / p.G, kc = p.g.kcol(hk), vc = p.g.vcol(hk);
+        for (int j = 0; j < nkb; ++j, ++kv) {
+          const int st = kv & 1;
+          const uint32_t ph = (kv >> 1) & 1u;
+          if (!W(&k_empty[st], ph ^ 1u)) { ok = false; break; }
+          uint8_t* kd = smem + F_K + st * TILE;
+          mbar_arrive_expect_tx(&k_full[st], TILE);
+          tma_load_3d(kd, &tq, &k_full[st], kc, j * 128, b);
+          tma_load_3d(kd + TILE / 2, &tq, &k_full[st], kc + 64, j * 128, b);
+          k_last[st] = static_cast<int>(ph);
+          if (!W(&v_empty[st], ph ^ 1u)) { ok = false; break; }
+          uint8_t* vd = smem + F_V + st * TILE;
+          mbar_arrive_expect_tx(&v_full[st], TILE);
+          tma_load_3d(vd, &tq, &v_full[st], vc, j * 128, b);
+          tma_load_3d(vd + TILE / 2, &tq, &v_full[st], vc + 64, j * 128, b);
+          v_last[st] = static_cast<int>(ph);
+        }
+      }
+      // every issued copy lands before the CTA may exit
+      if (q_last >= 0) W.drain(q_full, static_cast<uint32_t>(q_last));
+      for (int s = 0; s < 2; ++s) {
+        if (k_last[s] >= 0) W.drain(&k_full[s], static_cast<uint32_t>(k_last[s]));
+        if (v_last[s] >= 0) W.drain(&v_full[s], static_cast<uint32_t>(v_last[s]));
+      }
+    }
+    __syncwarp();
+  } else if (warp == 1) {
+    // ------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      constexpr uint32_t ID_S = idesc(128, 0, 0);   // S = Q K^T
+      constexpr uint32_t ID_PV = idesc(128, 0, 1);  // O += P V (V: N = hd contiguous)
+      const uint32_t qa = smem_u32(smem + F_Q), pa = smem_u32(smem + F_P);
+      uint32_t kv = 0, sc = 0, pc = 0, it = 0;
+      bool ok = true;
+      for (int item = blockIdx.x; item < p.items && ok; item += gridDim.x, ++it) {
+        int qb, b, h;
+        decode_item(p, item, p.H, p.causal != 0, qb, b, h);
+        const int nkb = p.causal ? qb + 1 : p.n_qb;
+        if (!W(q_full, it & 1u)) break;
+        tc_fence_after();
+        auto issue_s = [&](int j) -> bool {
+          const uint32_t n = kv + j;
+          const int st = n & 1;
+          if (!W(&k_full[st], (n >> 1) & 1u)) return false;
+          const uint32_t buf = (sc + j) & 1u, use = (sc + j) >> 1;
+          if (!W(&s_empty[buf], (use & 1u) ^ 1u)) return false;
+          tc_fence_after();
+          const uint32_t ka = smem_u32(smem + F_K + st * TILE);
+#pragma unroll
+          for (int ks = 0; ks < 8; ++ks)
+            umma_bf16(tmem + buf * 128, kdesc(qa, 128, ks), kdesc(ka, 128, ks), ID_S, ks > 0 ? 1u : 0u);
+          umma_commit(&s_full[buf]);
+          umma_commit(&k_empty[st]);
+          if (j == nkb - 1) umma_commit(q_empty);  // Q free once the item's last S is done
+          return true;
+        };
+        if (!issue_s(0)) break;
+        for (int j = 0; j < nkb; ++j) {
+          if (j + 1 < nkb && !issue_s(j + 1)) { ok = false; break; }
+          if (!W(p_full, pc & 1u)) { ok = false; break; }
+          if (j == 0 && !W(o_empty, (it & 1u) ^ 1u)) { ok = false; break; }
+          const uint32_t n = kv + j;
+          const int st = n & 1;
+          if (!W(&v_full[st], (n >> 1) & 1u)) { ok = false; break; }
+          tc_fence_after();
+          const uint32_t va = smem_u32(smem + F_V + st * TILE);
+#pragma unroll
+          for (int ks = 0; ks < 8; ++ks)
+            umma_bf16(tmem + 256, kdesc(pa, 128, ks), mndesc(va, 128, ks), ID_PV, (j > 0 || ks > 0) ? 1u : 0u);
+          umma_commit(&v_empty[st]);
+          umma_commit(pv_done);
+          ++pc;
+        }
+        kv += nkb;
+        sc += nkb;
+      }
+      umma_commit(drain);  // all issued MMAs complete before tensor memory is released
+      W.drain(drain, 0u);
+    }
+    __syncwarp();
+  } else {
+    // ------------------------------------------------ softmax warps 2..5
+    const int quarter = warp & 3;
+    const int row = quarter * 32 + lane;
+    const uint32_t tl = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
+    const uint32_t pt = smem_u32(smem + F_P);
+    uint32_t sc = 0, pvw = 0, it = 0;
+    for (int item = blockIdx.x; item < p.items; item += gridDim.x, ++it) {
+      int qb, b, h;
+      decode_item(p, item, p.H, p.causal != 0, qb, b, h);
+      const int nkb = p.causal ? qb + 1 : p.n_qb;
+      const int qpos = qb * 128 + row;
+      float m_used = -INFINITY, l = 0.f;
+      bool ok = true;
+      for (int j = 0; j < nkb; ++j) {
+        const uint32_t buf = sc & 1u, use = sc >> 1;
+        ++sc;
+        if (!W.warp(&s_full[buf], use & 1u)) { ok = false; break; }
+        tc_fence_after();
+        uint32_t r[128];
+#pragma unroll
+        for (int c = 0; c < 4; ++c)
+          tmem_ld32(tl + buf * 128 + c * 32, *reinterpret_cast<uint32_t(*)[32]>(&r[c * 32]));
+        tmem_wait_ld();
+        tc_fence_before();
+        mbar_arrive(&s_empty[buf]);
+        const int kbase = j * 128;
+        float mx = -INFINITY;
+#pragma unroll
+        for (int c = 0; c < 128; ++c) {
+          const int key = kbase + c;
+          const bool vis = key < p.S && (!p.causal || key <= qpos);
+          const float x = vis ? __uint_as_float(r[c]) * p.scale_log2 : -INFINITY;
+          r[c] = __float_as_uint(x);
+          mx = fmaxf(mx, x);
+        }
+        float alpha = 1.f;
+        bool rescale = false;
+        if (j == 0) {
+          m_used = mx;
+        } else if (mx > m_used + 8.f) {  // lazy rescale: p stays <= 2^8 otherwise
+          alpha = exp2f(m_used - mx);
+          m_used = mx;
+          rescale = true;
+        }
+        l *= alpha;
+        uint32_t pk[64];
+#pragma unroll
+        for (int c = 0; c < 64; ++c) {
+          const float p0 = exp2f(__uint_as_float(r[2 * c]) - m_used);
+          const float p1 = exp2f(__uint_as_float(r[2 * c + 1]) - m_used);
+          l += p0 + p1;
+          pk[c] = pack_bf16x2(p0, p1);
+        }
+        if (j > 0) {  // PV of the previous block done: P buffer free, O current
+          if (!W.warp(pv_done, pvw & 1u)) { ok = false; break; }
+          ++pvw;
+          tc_fence_after();
+        }
+        if (__any_sync(0xffffffffu, rescale)) {
+#pragma unroll 1
+          for (int c = 0; c < 4; ++c) {
+            uint32_t o[32];
+            tmem_ld32(tl + 256 + c * 32, o);
+            tmem_wait_ld();
+#pragma unroll
+            for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
+            tmem_st32(tl + 256 + c * 32, o);
+          }
+          tmem_wait_st();
+        }
+#pragma unroll
+        for (int c8 = 0; c8 < 16; ++c8)
+          st_shared_v4(sw_chunk(pt, 128, row, c8), pk[4 * c8], pk[4 * c8 + 1], pk[4 * c8 + 2], pk[4 * c8 + 3]);
+        fence_async_smem();
+        tc_fence_before();
+        mbar_arrive(p_full);
+      }
+      if (!ok) break;
+      if (!W.warp(pv_done, pvw & 1u)) break;
+      ++pvw;
+      tc_fence_after();
+      const bool row_ok = qpos < p.S;
+      const float inv = 1.f / l;
+      __nv_bfloat16* orow = p.o + (static_cast<long long>(b) * p.S + qpos) * p.o_rs + h * HD;
+#pragma unroll 1
+      for (int c = 0; c < 4; ++c) {
+        uint32_t o[32];
+        tmem_ld32(tl + 256 + c * 32, o);
+        tmem_wait_ld();
+        if (row_ok) store_row_bf16(orow + c * 32, o, inv);
+      }
+      if (row_ok) p.lse[(static_cast<long long>(b) * p.H + h) * p.s_pad + qpos] = m_used + log2f(l);
+      tc_fence_before();
+      mbar_arrive(o_empty);
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
+// ================================================================ D = rowsum(dO * o)
+__global__ void attn_prep_kernel(const Params p) {
+  const long long idx = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
+  const long long total = static_cast<long long>(p.B) * p.S * p.H;
+  if (idx >= total) return;
+  const int h = static_cast<int>(idx % p.H);
+  const long long tok = idx / p.H;
+  const int b = static_cast<int>(tok / p.S), i = static_cast<int>(tok % p.S);
+  const __nv_bfloat16* o = p.o + tok * p.o_rs + h * HD;
+  const __nv_bfloat16* g = p.dO + tok * p.do_rs + h * HD;
+  float acc = 0.f;
+#pragma unroll 4
+  for (int c = 0; c < HD; c += 8) {
+    const uint4 a = *reinterpret_cast<const uint4*>(o + c);
+    const uint4 d = *reinterpret_cast<const uint4*>(g + c);
+    const __nv_bfloat162* ah = reinterpret_cast<const __nv_bfloat162*>(&a);
+    const __nv_bfloat162* dh = reinterpret_cast<const __nv_bfloat162*>(&d);
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const float2 af = __bfloat1622float2(ah[k]), df = __bfloat1622float2(dh[k]);
+      acc = fmaf(af.x, df.x, acc);
+      acc = fmaf(af.y, df.y, acc);
+    }
+  }
+  p.Dv[(static_cast<long long>(b) * p.H + h) * p.s_pad + i] = acc;
+}
+
+// ================================================================ dq
+constexpr int KB = 64 * HD * 2;        // [64 rows][128 cols] bf16: two 8 KB boxes
+constexpr int Q_Q = 0;
+constexpr int Q_DO = Q_Q + TILE;
+constexpr int Q_K = Q_DO + TILE;       // 3 stages
+constexpr int Q_V = Q_K + 3 * KB;      // 3 stages
+constexpr int Q_DS = Q_V + 3 * KB;     // dS [128 q][64 keys]
+constexpr int Q_BAR = Q_DS + KB;
+constexpr int Q_SMEM = Q_BAR + 256 + 1024;
+
+__global__ void __launch_bounds__(NT, 1) attn_dq_kernel(const __grid_constant__ CUtensorMap tq128,
+                                                        const __grid_constant__ CUtensorMap tq64,
+                                                        const __grid_constant__ CUtensorMap tdo128, const Params p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = align1024(smem_raw);
+  uint64_t* bar = reinterpret_cast<uint64_t*>(smem + Q_BAR);
+  uint64_t* qdo_full = bar + 0;
+  uint64_t* qdo_empty = bar + 1;
+  uint64_t* k_full = bar + 2;    // [3]
+  uint64_t* k_empty = bar + 5;   // [3]
+  uint64_t* v_full = bar + 8;    // [3]
+  uint64_t* v_empty = bar + 11;  // [3]
+  uint64_t* sdp_full = bar + 14; // [2]
+  uint64_t* sdp_empty = bar + 16;// [2]
+  uint64_t* ds_full = bar + 18;
+  uint64_t* ds_free = bar + 19;
+  uint64_t* dq_full = bar + 20;
+  uint64_t* dq_empty = bar + 21;
+  uint64_t* drain = bar + 22;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bar + 23);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(bar + 23) + 1;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+  if (threadIdx.x == 0) {
+    mbar_init(qdo_full, 1);
+    mbar_init(qdo_empty, 1);
+    for (int i = 0; i < 3; ++i) {
+      mbar_init(&k_full[i], 1);
+      mbar_init(&k_empty[i], 1);
+      mbar_init(&v_full[i], 1);
+      mbar_init(&v_empty[i], 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&sdp_full[i], 1);
+      mbar_init(&sdp_empty[i], NSM);
+    }
+    mbar_init(ds_full, NSM);
+    mbar_init(ds_free, 1);
+    mbar_init(dq_full, 1);
+    mbar_init(dq_empty, NSM);
+    mbar_init(drain, 1);
+    *abort_flag = 0;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+  }
+  if (warp == 0 && lane == 0) {
+    prefetch_tmap(&tq128);
+    prefetch_tmap(&tq64);
+    prefetch_tmap(&tdo128);
+  }
+  if (warp == 1) tmem_alloc(tmem_slot, 512);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;  // S at 0/64, dP at 128/192, dQ at 256
+  const Waiter W{abort_flag, p.err, p.timeout_ns};
+
+  auto nkb_of = [&](int qb) { return p.causal ? min(2 * qb + 2, p.n_b64) : p.n_b64; };
+
+  if (warp == 0) {
+    if (lane == 0) {
+      int qdo_last = -1, k_last[3] = {-1, -1, -1}, v_last[3] = {-1, -1, -1};
+      uint32_t kc = 0, it = 0;
+      bool ok = true;
+      for (int item = blockIdx.x; item < p.items && ok; item += gridDim.x, ++it) {
+        int qb, b, h;
+        decode_item(p, item, p.H, p.causal != 0, qb, b, h);
+        const int nkb = nkb_of(qb);
+        if (!W(qdo_empty, (it & 1u) ^ 1u)) break;
+        mbar_arrive_expect_tx(qdo_full, 2 * TILE);
+        const int qc = p.g.qcol(h);
+        tma_load_3d(smem + Q_Q, &tq128, qdo_full, qc, qb * 128, b);
+        tma_load_3d(smem + Q_Q + TILE / 2, &tq128, qdo_full, qc + 64, qb * 128, b);
+        tma_load_3d(smem + Q_DO, &tdo128, qdo_full, h * HD, qb * 128, b);
+        tma_load_3d(smem + Q_DO + TILE / 2, &tdo128, qdo_full, h * HD + 64, qb * 128, b);
+        qdo_last = static_cast<int>(it & 1u);
+        const int hk = h / p.G, kcol = p.g.kcol(hk), vcol = p.g.vcol(hk);
+        for (int j = 0; j < nkb; ++j, ++kc) {
+          const int st = kc % 3;
+          const uint32_t ph = (kc / 3) & 1u;
+          if (!W(&k_empty[st], ph ^ 1u)) { ok = false; break; }
+          uint8_t* kd = smem + Q_K + st * KB;
+          mbar_arrive_expect_tx(&k_full[st], KB);
+          tma_load_3d(kd, &tq64, &k_full[st], kcol, j * 64, b);
+          tma_load_3d(kd + KB / 2, &tq64, &k_full[st], kcol + 64, j * 64, b);
+          k_last[st] = static_cast<int>(ph);
+          if (!W(&v_empty[st], ph ^ 1u)) { ok = false; break; }
+          uint8_t* vd = smem + Q_V + st * KB;
+          mbar_arrive_expect_tx(&v_full[st], KB);
+          tma_load_3d(vd, &tq64, &v_full[st], vcol, j * 64, b);
+          tma_load_3d(vd + KB / 2, &tq64, &v_full[st], vcol + 64, j * 64, b);
+          v_last[st] = static_cast<int>(ph);
+        }
+      }
+      if (qdo_last >= 0) W.drain(qdo_full, static_cast<uint32_t>(qdo_last));
+      for (int s = 0; s < 3; ++s) {
+        if (k_last[s] >= 0) W.drain(&k_full[s], static_cast<uint32_t>(k_last[s]));
+        if (v_last[s] >= 0) W.drain(&v_full[s], static_cast<uint32_t>(v_last[s]));
+      }
+    }
+    __syncwarp();
+  } else if (warp == 1) {
+    if (lane == 0) {
+      constexpr uint32_t ID_S = idesc(64, 0, 0);    // S = Q K^T, dP = dO V^T
+      constexpr uint32_t ID_DQ = idesc(128, 0, 1);  // dQ += dS K (K: N = hd contiguous)
+      const uint32_t qa = smem_u32(smem + Q_Q), da = smem_u32(smem + Q_DO), dsa = smem_u32(smem + Q_DS);
+      uint32_t kc = 0, sc = 0, dsc = 0, it = 0;
+      bool ok = true;
+      for (int item = blockIdx.x; item < p.items && ok; item += gridDim.x, ++it) {
+        int qb, b, h;
+        decode_item(p, item, p.H, p.causal != 0, qb, b, h);
+        const int nkb = nkb_of(qb);
+        if (!W(qdo_full, it & 1u)) break;
+        tc_fence_after();
+        auto issue_sdp = [&](int j) -> bool {
+          const uint32_t n = kc + j;
+          const int st = n % 3;
+          const uint32_t ph = (n / 3) & 1u;
+          if (!W(&k_full[st], ph) || !W(&v_full[st], ph)) return false;
+          const uint32_t buf = (sc + j) & 1u, use = (sc + j) >> 1;
+          if (!W(&sdp_empty[buf], (use & 1u) ^ 1u)) return false;
+          tc_fence_after();
+          const uint32_t ka = smem_u32(smem + Q_K + st * KB), va = smem_u32(smem + Q_V + st * KB);
+#pragma unroll
+          for (int ks = 0; ks < 8; ++ks)
+            umma_bf16(tmem + buf * 64, kdesc(qa, 128, ks), kdesc(ka, 64, ks), ID_S, ks > 0 ? 1u : 0u);
+#pragma unroll
+          for (int ks = 0; ks < 8; ++ks)
+            umma_bf16(tmem + 128 + buf * 64, kdesc(da, 128, ks), kdesc(va, 64, ks), ID_S, ks > 0 ? 1u : 0u);
+          umma_commit(&sdp_full[buf]);
+          umma_commit(&v_empty[st]);
+          if (j == nkb - 1) umma_commit(qdo_empty);
+          return true;
+        };
+        if (!issue_sdp(0)) break;
+        for (int j = 0; j < nkb; ++j) {
+          if (j + 1 < nkb && !issue_sdp(j + 1)) { ok = false; break; }
+          if (!W(ds_full, dsc & 1u)) { ok = false; break; }
+          if (j == 0 && !W(dq_empty, (it & 1u) ^ 1u)) { ok = false; break; }
+          tc_fence_after();
+          const int st = (kc + j) % 3;
+          const uint32_t ka = smem_u32(smem + Q_K + st * KB);
+#pragma unroll
+          for (int ks = 0; ks < 4; ++ks)
+            umma_bf16(tmem + 256, kdesc(dsa, 128, ks), mndesc(ka, 64, ks), ID_DQ, (j > 0 || ks > 0) ? 1u : 0u);
+          umma_commit(&k_empty[st]);
+          umma_commit(ds_free);
+          ++dsc;
+        }
+        if (!ok) break;
+        umma_commit(dq_full);
+        kc += nkb;
+        sc += nkb;
+      }
+      umma_commit(drain);
+      W.drain(drain, 0u);
+    }
+    __syncwarp();
+  } else {
+    const int quarter = warp & 3;
+    const int row = quarter * 32 + lane;
+    const uint32_t tl = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
+    const uint32_t dst = smem_u32(smem + Q_DS);
+    uint32_t sc = 0, dsbase = 0, it = 0;
+    for (int item = blockIdx.x; item < p.items; item += gridDim.x, ++it) {
+      int qb, b, h;
+      decode_item(p, item, p.H, p.causal != 0, qb, b, h);
+      const int nkb = nkb_of(qb);
+      const int qpos = qb * 128 + row;
+      const bool row_ok = qpos < p.S;
+      const long long vrow = (static_cast<long long>(b) * p.H + h) * p.s_pad + qpos;
+      const float lse_r = row_ok ? p.lse[vrow] : 0.f;
+      const float d_r = row_ok ? p.Dv[vrow] : 0.f;
+      bool ok = true;
+      for (int j = 0; j < nkb; ++j) {
+        const uint32_t buf = sc & 1u, use = sc >> 1;
+        ++sc;
+        if (!W.warp(&sdp_full[buf], use & 1u)) { ok = false; break; }
+        tc_fence_after();
+        uint32_t rs[64], rp[64];
+        tmem_ld32(tl + buf * 64, *reinterpret_cast<uint32_t(*)[32]>(&rs[0]));
+        tmem_ld32(tl + buf * 64 + 32, *reinterpret_cast<uint32_t(*)[32]>(&rs[32]));
+        tmem_ld32(tl + 128 + buf * 64, *reinterpret_cast<uint32_t(*)[32]>(&rp[0]));
+        tmem_ld32(tl + 128 + buf * 64 + 32, *reinterpret_cast<uint32_t(*)[32]>(&rp[32]));
+        tmem_wait_ld();
+        tc_fence_before();
+        mbar_arrive(&sdp_empty[buf]);
+        uint32_t pk[32];
+#pragma unroll
+        for (int c = 0; c < 64; c += 2) {
+          float ds[2];
+#pragma unroll
+          for (int e = 0; e < 2; ++e) {
+            const int key = j * 64 + c + e;
+            const bool vis = row_ok && key < p.S && (!p.causal || key <= qpos);
+            const float pr = vis ? exp2f(__uint_as_float(rs[c + e]) * p.scale_log2 - lse_r) : 0.f;
+            ds[e] = pr * (__uint_as_float(rp[c + e]) - d_r) * p.scale;
+          }
+          pk[c / 2] = pack_bf16x2(ds[0], ds[1]);
+        }
+        if (j > 0 && !W.warp(ds_free, (dsbase + j - 1) & 1u)) { ok = false; break; }
+#pragma unroll
+        for (int c8 = 0; c8 < 8; ++c8)
+          st_shared_v4(sw_chunk(dst, 128, row, c8), pk[4 * c8], pk[4 * c8 + 1], pk[4 * c8 + 2], pk[4 * c8 + 3]);
+        fence_async_smem();
+        tc_fence_before();
+        mbar_arrive(ds_full);
+      }
+      if (!ok) break;
+      if (!W.warp(dq_full, it & 1u)) break;
+      tc_fence_after();
+      __nv_bfloat16* out = p.dqkv + (static_cast<long long>(b) * p.S + qpos) * p.dqkv_rs + p.g.qcol(h);
+#pragma unroll 1
+      for (int c = 0; c < 4; ++c) {
+        uint32_t o[32];
+        tmem_ld32(tl + 256 + c * 32, o);
+        tmem_wait_ld();
+        if (row_ok) store_row_bf16(out + c * 32, o, 1.f);
+      }
+      tc_fence_before();
+      mbar_arrive(dq_empty);
+      dsbase += nkb;
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
+// ================================================================ dk, dv
+constexpr int V_K = 0;
+constexpr int V_V = V_K + TILE;
+constexpr int V_Q = V_V + TILE;        // 3 stages of [64 q][128]
+constexpr int V_DO = V_Q + 3 * KB;     // 3 stages
+constexpr int V_PT = V_DO + 3 * KB;     // P^T [128 keys][64 q]
+constexpr int V_DST = V_PT + 16384;     // dS^T [128 keys][64 q]
+constexpr int V_VEC = V_DST + 16384;   // 3 stages x (64 lse + 64 D) floats
+constexpr int V_BAR = V_VEC + 3 * 512;
+constexpr int V_SMEM = V_BAR + 256 + 1024;
+
+__global__ void __launch_bounds__(NT, 1) attn_dkdv_kernel(const __grid_constant__ CUtensorMap tq128,
+                                                          const __grid_constant__ CUtensorMap tq64,
+                                                          const __grid_constant__ CUtensorMap tdo64, const Params p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = align1024(smem_raw);
+  uint64_t* bar = reinterpret_cast<uint64_t*>(smem + V_BAR);
+  uint64_t* kv_full = bar + 0;
+  uint64_t* kv_empty = bar + 1;
+  uint64_t* q_full = bar + 2;     // [3]
+  uint64_t* q_empty = bar + 5;    // [3]
+  uint64_t* do_full = bar + 8;    // [3]
+  uint64_t* do_empty = bar + 11;  // [3]
+  uint64_t* sdp_full = bar + 14;  // [2]
+  uint64_t* sdp_empty = bar + 16; // [2]
+  uint64_t* p_full = bar + 18;
+  uint64_t* p_free = bar + 19;
+  uint64_t* ds_full = bar + 20;
+  uint64_t* ds_free = bar + 21;
+  uint64_t* dkv_full = bar + 22;
+  uint64_t* dkv_empty = bar + 23;
+  uint64_t* drain = bar + 24;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bar + 25);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(bar + 25) + 1;
+  float* vec = reinterpret_cast<float*>(smem + V_VEC);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+  if (threadIdx.x == 0) {
+    mbar_init(kv_full, 1);
+    mbar_init(kv_empty, 1);
+    for (int i = 0; i < 3; ++i) {
+      mbar_init(&q_full[i], 1);
+      mbar_init(&q_empty[i], 1);
+      mbar_init(&do_full[i], 1);
+      mbar_init(&do_empty[i], 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&sdp_full[i], 1);
+      mbar_init(&sdp_empty[i], NSM);
+    }
+    mbar_init(p_full, NSM);
+    mbar_init(p_free, 1);
+    mbar_init(ds_full, NSM);
+    mbar_init(ds_free, 1);
+    mbar_init(dkv_full, 1);
+    mbar_init(dkv_empty, NSM);
+    mbar_init(drain, 1);
+    *abort_flag = 0;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+  }
+  if (warp == 0 && lane == 0) {
+    prefetch_tmap(&tq128);
+    prefetch_tmap(&tq64);
+    prefetch_tmap(&tdo64);
+  }
+  if (warp == 1) tmem_alloc(tmem_slot, 512);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;  // S^T at 0/64, dP^T at 128/192, dV at 256, dK at 384
+  const Waiter W{abort_flag, p.err, p.timeout_ns};
+
+  // causal: key block kb sees the 64-query blocks from 2 kb on
+  auto q0_of = [&](int kb) { return p.causal ? 2 * kb : 0; };
+
+  if (warp == 0) {
+    if (lane == 0) {
+      int kv_last = -1, q_last[3] = {-1, -1, -1}, do_last[3] = {-1, -1, -1};
+      uint32_t qc = 0, it = 0;
+      bool ok = true;
+      for (int item = blockIdx.x; item < p.items && ok; item += gridDim.x, ++it) {
+        int kb, b, hk;
+        decode_item(p, item, p.Hkv, false, kb, b, hk);
+        if (!W(kv_empty, (it & 1u) ^ 1u)) break;
+        mbar_arrive_expect_tx(kv_full, 2 * TILE);
+        const int kcol = p.g.kcol(hk), vcol = p.g.vcol(hk);
+        tma_load_3d(smem + V_K, &tq128, kv_full, kcol, kb * 128, b);
+        tma_load_3d(smem + V_K + TILE / 2, &tq128, kv_full, kcol + 64, kb * 128, b);
+        tma_load_3d(smem + V_V, &tq128, kv_full, vcol, kb * 128, b);
+        tma_load_3d(smem + V_V + TILE / 2, &tq128, kv_full, vcol + 64, kb * 128, b);
+        kv_last = static_cast<int>(it & 1u);
+        const int i0 = q0_of(kb);
+        for (int g = 0; g < p.G && ok; ++g) {
+          const int h = hk * p.G + g;
+          const int qcol = p.g.qcol(h);
+          const float* lse_row = p.lse + (static_cast<long long>(b) * p.H + h) * p.s_pad;
+          const float* d_row = p.Dv + (static_cast<long long>(b) * p.H + h) * p.s_pad;
+          for (int i = i0; i < p.n_b64; ++i, ++qc) {
+            const int st = qc % 3;
+            const uint32_t ph = (qc / 3) & 1u;
+            if (!W(&q_empty[st], ph ^ 1u)) { ok = false; break; }
+            uint8_t* qd = smem + V_Q + st * KB;
+            mbar_arrive_expect_tx(&q_full[st], KB + 512);
+            tma_load_3d(qd, &tq64, &q_full[st], qcol, i * 64, b);
+            tma_load_3d(qd + KB / 2, &tq64, &q_full[st], qcol + 64, i * 64, b);
+            bulk_g2s(vec + st * 128, lse_row + i * 64, 256, &q_full[st]);
+            bulk_g2s(vec + st * 128 + 64, d_row + i * 64, 256, &q_full[st]);
+            q_last[st] = static_cast<int>(ph);
+            if (!W(&do_empty[st], ph ^ 1u)) { ok = false; break; }
+            uint8_t* dd = smem + V_DO + st * KB;
+            mbar_arrive_expect_tx(&do_full[st], KB);
+            tma_load_3d(dd, &tdo64, &do_full[st], h * HD, i * 64, b);
+            tma_load_3d(dd + KB / 2, &tdo64, &do_full[st], h * HD + 64, i * 64, b);
+            do_last[st] = static_cast<int>(ph);
+          }
+        }
+      }
+      if (kv_last >= 0) W.drain(kv_full, static_cast<uint32_t>(kv_last));
+      for (int s = 0; s < 3; ++s) {
+        if (q_last[s] >= 0) W.drain(&q_full[s], static_cast<uint32_t>(q_last[s]));
+        if (do_last[s] >= 0) W.drain(&do_full[s], static_cast<uint32_t>(do_last[s]));
+      }
+    }
+    __syncwarp();
+  } else if (warp == 1) {
+    if (lane == 0) {
+      constexpr uint32_t ID_S = idesc(64, 0, 0);    // S^T = K Q^T, dP^T = V dO^T
+      constexpr uint32_t ID_G = idesc(128, 0, 1);   // dV += P^T dO, dK += dS^T Q
+      const uint32_t ka = smem_u32(smem + V_K), va = smem_u32(smem + V_V);
+      const uint32_t pta = smem_u32(smem + V_PT), dsa = smem_u32(smem + V_DST);
+      uint32_t qc = 0, sc = 0, pc = 0, it = 0;
+      bool ok = true;
+      for (int item = blockIdx.x; item < p.items && ok; item += gridDim.x, ++it) {
+        int kb, b, hk;
+        decode_item(p, item, p.Hkv, false, kb, b, hk);
+        const int nq = p.n_b64 - q0_of(kb);
+        const int n_it = p.G * nq;
+        if (!W(kv_full, it & 1u)) break;
+        tc_fence_after();
+        auto issue_sdp = [&](int t) -> bool {
+          const uint32_t n = qc + t;
+          const int st = n % 3;
+          const uint32_t ph = (n / 3) & 1u;
+          if (!W(&q_full[st], ph) || !W(&do_full[st], ph)) return false;
+          const uint32_t buf = (sc + t) & 1u, use = (sc + t) >> 1;
+          if (!W(&sdp_empty[buf], (use & 1u) ^ 1u)) return false;
+          tc_fence_after();
+          const uint32_t qa = smem_u32(smem + V_Q + st * KB), da = smem_u32(smem + V_DO + st * KB);
+#pragma unroll
+          for (int ks = 0; ks < 8; ++ks)
+            umma_bf16(tmem + buf * 64, kdesc(ka, 128, ks), kdesc(qa, 64, ks), ID_S, ks > 0 ? 1u : 0u);
+#pragma unroll
+          for (int ks = 0; ks < 8; ++ks)
+            umma_bf16(tmem + 128 + buf * 64, kdesc(va, 128, ks), kdesc(da, 64, ks), ID_S, ks > 0 ? 1u : 0u);
+          umma_commit(&sdp_full[buf]);
+          return true;
+        };
+        if (n_it > 0 && !issue_sdp(0)) break;
+        for (int t = 0; t < n_it; ++t) {
+          if (t + 1 < n_it && !issue_sdp(t + 1)) { ok = false; break; }
+          const int st = (qc + t) % 3;
+          if (!W(p_full, pc & 1u)) { ok = false; break; }
+          if (t == 0 && !W(dkv_empty, (it & 1u) ^ 1u)) { ok = false; break; }
+          tc_fence_after();
+          const uint32_t qa = smem_u32(smem + V_Q + st * KB), da = smem_u32(smem + V_DO + st * KB);
+#pragma unroll
+          for (int ks = 0; ks < 4; ++ks)
+            umma_bf16(tmem + 256, kdesc(pta, 128, ks), mndesc(da, 64, ks), ID_G, (t > 0 || ks > 0) ? 1u : 0u);
+          umma_commit(&do_empty[st]);
+          umma_commit(p_free);
+          if (!W(ds_full, pc & 1u)) { ok = false; break; }
+          tc_fence_after();
+#pragma unroll
+          for (int ks = 0; ks < 4; ++ks)
+            umma_bf16(tmem + 384, kdesc(dsa, 128, ks), mndesc(qa, 64, ks), ID_G, (t > 0 || ks > 0) ? 1u : 0u);
+          umma_commit(&q_empty[st]);
+          umma_commit(ds_free);
+          ++pc;
+        }
+        if (!ok) break;
+        umma_commit(dkv_full);
+        umma_commit(kv_empty);
+        qc += n_it;
+        sc += n_it;
+      }
+      umma_commit(drain);
+      W.drain(drain, 0u);
+    }
+    __syncwarp();
+  } else {
+    const int quarter = warp & 3;
+    const int row = quarter * 32 + lane;
+    const uint32_t tl = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
+    const uint32_t pts = smem_u32(smem + V_PT), dss = smem_u32(smem + V_DST);
+    uint32_t qc = 0, sc = 0, pbase = 0, it = 0;
+    for (int item = blockIdx.x; item < p.items; item += gridDim.x, ++it) {
+      int kb, b, hk;
+      decode_item(p, item, p.Hkv, false, kb, b, hk);
+      const int i0 = q0_of(kb), nq = p.n_b64 - i0;
+      const int n_it = p.G * nq;
+      const int kpos = kb * 128 + row;
+      const bool row_ok = kpos < p.S;
+      bool ok = true;
+      for (int t = 0; t < n_it; ++t) {
+        const int i = i0 + t % nq;
+        const uint32_t n = qc + t;
+        const int st = n % 3;
+        const uint32_t ph = (n / 3) & 1u;
+        const uint32_t buf = sc & 1u, use = sc >> 1;
+        ++sc;
+        if (!W.warp(&sdp_full[buf], use & 1u)) { ok = false; break; }
+        tc_fence_after();
+        uint32_t rs[64], rp[64];
+        tmem_ld32(tl + buf * 64, *reinterpret_cast<uint32_t(*)[32]>(&rs[0]));
+        tmem_ld32(tl + buf * 64 + 32, *reinterpret_cast<uint32_t(*)[32]>(&rs[32]));
+        tmem_ld32(tl + 128 + buf * 64, *reinterpret_cast<uint32_t(*)[32]>(&rp[0]));
+        tmem_ld32(tl + 128 + buf * 64 + 32, *reinterpret_cast<uint32_t(*)[32]>(&rp[32]));
+        tmem_wait_ld();
+        tc_fence_before();
+        mbar_arrive(&sdp_empty[buf]);
+        if (!W.warp(&q_full[st], ph)) { ok = false; break; }  // lse / D of this block landed
+        const float* lse_v = vec + st * 128;
+        const float* d_v = lse_v + 64;
+        uint32_t pp[32], pd[32];
+#pragma unroll
+        for (int c = 0; c < 64; c += 2) {
+          float pr[2], ds[2];
+#pragma unroll
+          for (int e = 0; e < 2; ++e) {
+            const int qpos = i * 64 + c + e;
+            const bool vis = row_ok && qpos < p.S && (!p.causal || kpos <= qpos);
+            pr[e] = vis ? exp2f(__uint_as_float(rs[c + e]) * p.scale_log2 - lse_v[c + e]) : 0.f;
+            ds[e] = pr[e] * (__uint_as_float(rp[c + e]) - d_v[c + e]) * p.scale;
+          }
+          pp[c / 2] = pack_bf16x2(pr[0], pr[1]);
+          pd[c / 2] = pack_bf16x2(ds[0], ds[1]);
+        }
+        if (t > 0 && !W.warp(p_free, (pbase + t - 1) & 1u)) { ok = false; break; }
+#pragma unroll
+        for (int c8 = 0; c8 < 8; ++c8)
+          st_shared_v4(sw_chunk(pts, 128, row, c8), pp[4 * c8], pp[4 * c8 + 1], pp[4 * c8 + 2], pp[4 * c8 + 3]);
+        fence_async_smem();
+        tc_fence_before();
+        mbar_arrive(p_full);
+        if (t > 0 && !W.warp(ds_free, (pbase + t - 1) & 1u)) { ok = false; break; }
+#pragma unroll
+        for (int c8 = 0; c8 < 8; ++c8)
+          st_shared_v4(sw_chunk(dss, 128, row, c8), pd[4 * c8], pd[4 * c8 + 1], pd[4 * c8 + 2], pd[4 * c8 + 3]);
+        fence_async_smem();
+        tc_fence_before();
+        mbar_arrive(ds_full);
+      }
+      if (!ok) break;
+      if (!W.warp(dkv_full, it & 1u)) break;
+      tc_fence_after();
+      __nv_bfloat16* out = p.dqkv + (static_cast<long long>(b) * p.S + kpos) * p.dqkv_rs;
+      const int vcol = p.g.vcol(hk), kcol = p.g.kcol(hk);
+#pragma unroll 1
+      for (int c = 0; c < 4; ++c) {
+        uint32_t o[32];
+        tmem_ld32(tl + 256 + c * 32, o);
+        tmem_wait_ld();
+        if (row_ok) store_row_bf16(out + vcol + c * 32, o, 1.f);
+      }
+#pragma unroll 1
+      for (int c = 0; c < 4; ++c) {
+        uint32_t o[32];
+        tmem_ld32(tl + 384 + c * 32, o);
+        tmem_wait_ld();
+        if (row_ok) store_row_bf16(out + kcol + c * 32, o, 1.f);
+      }
+      tc_fence_before();
+      mbar_arrive(dkv_empty);
+      qc += n_it;
+      pbase += n_it;
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
+// ================================================================ packing
+__global__ void pack_qkv_kernel(const __nv_bfloat16* Wq, const __nv_bfloat16* Wk, const __nv_bfloat16* Wv,
+                                __nv_bfloat16* packed, int T, long long sq, long long sk, long long d, int unpack) {
+  const long long slice = sq + 2 * sk;
+  const long long rows = T * slice;
+  for (long long r = blockIdx.x; r < rows; r += gridDim.x) {
+    const long long t = r / slice, c = r - t * slice;
+    const __nv_bfloat16* src;
+    if (c < sq)
+      src = Wq + (t * sq + c) * d;
+    else if (c < sq + sk)
+      src = Wk + (t * sk + c - sq) * d;
+    else
+      src = Wv + (t * sk + c - sq - sk) * d;
+    __nv_bfloat16* dst = packed + r * d;
+    const uint4* s4 = reinterpret_cast<const uint4*>(unpack ? dst : src);
+    uint4* d4 = reinterpret_cast<uint4*>(unpack ? const_cast<__nv_bfloat16*>(src) : dst);
+    for (long long k = threadIdx.x; k < d / 8; k += blockDim.x) d4[k] = s4[k];
+  }
+}
+
+// ================================================================ host
+Params make_params(const AttnSpec& a, const LaunchCtx& ctx) {
+  Params p{};
+  p.g.hq_per = a.H / a.T_p;
+  p.g.hk_per = a.Hkv / a.T_p;
+  p.g.sq = p.g.hq_per * HD;
+  p.g.sk = p.g.hk_per * HD;
+  p.g.slice = p.g.sq + 2 * p.g.sk;
+  p.B = a.B;
+  p.S = a.S;
+  p.H = a.H;
+  p.Hkv = a.Hkv;
+  p.G = a.H / a.Hkv;
+  p.causal = a.causal ? 1 : 0;
+  p.n_qb = (a.S + 127) / 128;
+  p.n_b64 = (a.S + 63) / 64;
+  p.o = static_cast<__nv_bfloat16*>(a.o);
+  p.o_rs = a.o_rs;
+  p.dO = static_cast<const __nv_bfloat16*>(a.dO);
+  p.do_rs = a.do_rs;
+  p.lse = a.lse;
+  p.s_pad = a.s_pad;
+  p.Dv = a.Dv;
+  p.dqkv = static_cast<__nv_bfloat16*>(a.dqkv);
+  p.dqkv_rs = a.qkv_rs;
+  p.scale = static_cast<float>(1.0 / std::sqrt(static_cast<double>(HD)));
+  p.scale_log2 = static_cast<float>(1.4426950408889634 / std::sqrt(static_cast<double>(HD)));
+  p.err = ctx.err;
+  p.timeout_ns = ctx.timeout_ns;
+  return p;
+}
+
+int check_spec(const AttnSpec& a) {
+  if (a.hd != HD) return TP_ERR_UNSUPPORTED;
+  if (a.B < 1 || a.S < 1 || a.H < 1 || a.Hkv < 1 || a.T_p < 1) return TP_ERR_INVALID;
+  if (a.H % a.T_p || a.Hkv % a.T_p || a.H % a.Hkv) return TP_ERR_INVALID;
+  if (a.qkv_rs < static_cast<int64_t>(a.H + 2 * a.Hkv) * HD || a.qkv_rs % 8) return TP_ERR_INVALID;
+  if (a.s_pad < (a.S + 127) / 128 * 128 || a.s_pad % 128) return TP_ERR_INVALID;
+  if (a.o_rs < static_cast<int64_t>(a.H) * HD || a.o_rs % 8) return TP_ERR_INVALID;
+  const long long blocks = static_cast<long long>((a.S + 127) / 128) * a.B * a.H;
+  if (blocks > (1ll << 30) || static_cast<long long>(a.B) * a.S > (1ll << 30)) return TP_ERR_UNSUPPORTED;
+  return TP_OK;
+}
+
+int map_rows(CUtensorMap* m, const void* ptr, int64_t rs, int S, int B, uint32_t box_rows) {
+  const uint64_t dims[3] = {static_cast<uint64_t>(rs), static_cast<uint64_t>(S), static_cast<uint64_t>(B)};
+  const uint64_t str[2] = {static_cast<uint64_t>(rs) * 2, static_cast<uint64_t>(rs) * 2 * static_cast<uint64_t>(S)};
+  const uint32_t box[3] = {64, box_rows, 1};
+  return encode_map_3d_bf16(m, ptr, dims, str, box);
+}
+
+template <typename K>
+int set_smem_once(K kern, int bytes, std::atomic<uint32_t>& done) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return TP_ERR_CUDA;
+  const uint32_t bit = 1u << (dev & 31);
+  if (!(done.load() & bit)) {
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes) != cudaSuccess)
+      return TP_ERR_CUDA;
+    done.fetch_or(bit);
+  }
+  return TP_OK;
+}
+
+int grid_for(long long items, int sms) { return static_cast<int>(items < sms ? items : sms); }
+
+}  // namespace attn
+
+int launch_attn_fwd(const AttnSpec& a, LaunchCtx& ctx) {
+  using namespace attn;
+  int rc = check_spec(a);
+  if (rc) return rc;
+  if (!a.qkv || !a.o || !a.lse) return TP_ERR_INVALID;
+  CUtensorMap tq;
+  if ((rc = map_rows(&tq, a.qkv, a.qkv_rs, a.S, a.B, 128))) return rc;
+  Params p = make_params(a, ctx);
+  p.items = p.n_qb * a.B * a.H;
+  static std::atomic<uint32_t> done{0};
+  if ((rc = set_smem_once(attn_fwd_kernel, F_SMEM, done))) return rc;
+  if (ctx.before) ctx.before(ctx.user, "attn_fwd", ctx.stream);
+  attn_fwd_kernel<<<grid_for(p.items, ctx.num_sms), NT, F_SMEM, ctx.stream>>>(tq, p);
+  if (ctx.after) ctx.after(ctx.user, ctx.stream);
+  ctx.launches++;
+  return cudaPeekAtLastError() == cudaSuccess ? TP_OK : TP_ERR_CUDA;
+}
+
+int launch_attn_bwd(const AttnSpec& a, LaunchCtx& ctx) {
+  using namespace attn;
+  int rc = check_spec(a);
+  if (rc) return rc;
+  if (!a.qkv || !a.o || !a.lse || !a.dO || !a.Dv || !a.dqkv) return TP_ERR_INVALID;
+  if (a.do_rs < static_cast<int64_t>(a.H) * HD || a.do_rs % 8) return TP_ERR_INVALID;
+  CUtensorMap tq128, tq64, tdo128, tdo64;
+  if ((rc = map_rows(&tq128, a.qkv, a.qkv_rs, a.S, a.B, 128))) return rc;
+  if ((rc = map_rows(&tq64, a.qkv, a.qkv_rs, a.S, a.B, 64))) return rc;
+  if ((rc = map_rows(&tdo128, a.dO, a.do_rs, a.S, a.B, 128))) return rc;
+  if ((rc = map_rows(&tdo64, a.dO, a.do_rs, a.S, a.B, 64))) return rc;
+  Params p = make_params(a, ctx);
+
+  // D = rowsum(dO * o)
+  {
+    const long long total = static_cast<long long>(a.B) * a.S * a.H;
+    const int threads = 256;
+    const long long blocks = (total + threads - 1) / threads;
+    if (ctx.before) ctx.before(ctx.user, "attn_bwd_prep", ctx.stream);
+    attn_prep_kernel<<<static_cast<unsigned>(blocks), threads, 0, ctx.stream>>>(p);
+    if (ctx.after) ctx.after(ctx.user, ctx.stream);
+    ctx.launches++;
+  }
+  {
+    p.items = p.n_qb * a.B * a.H;
+    static std::atomic<uint32_t> done{0};
+    if ((rc = set_smem_once(attn_dq_kernel, Q_SMEM, done))) return rc;
+    if (ctx.before) ctx.before(ctx.user, "attn_bwd_dq", ctx.stream);
+    attn_dq_kernel<<<grid_for(p.items, ctx.num_sms), NT, Q_SMEM, ctx.stream>>>(tq128, tq64, tdo128, p);
+    if (ctx.after) ctx.after(ctx.user, ctx.stream);
+    ctx.launches++;
+  }
+  {
+    p.items = p.n_qb * a.B * a.Hkv;
+    static std::atomic<uint32_t> done{0};
+    if ((rc = set_smem_once(attn_dkdv_kernel, V_SMEM, done))) return rc;
+    if (ctx.before) ctx.before(ctx.user, "attn_bwd_dkdv", ctx.stream);
+    attn_dkdv_kernel<<<grid_for(p.items, ctx.num_sms), NT, V_SMEM, ctx.stream>>>(tq128, tq64, tdo64, p);
+    if (ctx.after) ctx.after(ctx.user, ctx.stream);
+    ctx.launches++;
+  }
+  return cudaPeekAtLastError() == cudaSuccess ? TP_OK : TP_ERR_CUDA;
+}
+
+int launch_pack_qkv(const void* Wq, const void* Wk, const void* Wv, void* packed, int T_p, int64_t sq, int64_t sk,
+                    int64_t d, int unpack, cudaStream_t st) {
+  if (!Wq || !Wk || !Wv || !packed || d % 8) return TP_ERR_INVALID;
+  const void* ptrs[] = {Wq, Wk, Wv, packed};
+  for (const void* q : ptrs)
+    if (reinterpret_cast<uintptr_t>(q) % 16) return TP_ERR_ALIGN;
+  const long long rows = static_cast<long long>(T_p) * (sq + 2 * sk);
+  const int grid = static_cast<int>(rows < 65535 ? rows : 65535);
+  attn::pack_qkv_kernel<<<grid, 128, 0, st>>>(static_cast<const __nv_bfloat16*>(Wq),
+                                              static_cast<const __nv_bfloat16*>(Wk),
+                                              static_cast<const __nv_bfloat16*>(Wv),
+                                              static_cast<__nv_bfloat16*>(packed), T_p, sq, sk, d, unpack);
+  return cudaPeekAtLastError() == cudaSuccess ? TP_OK : TP_ERR_CUDA;
+}
+
+}  // namespace tpffn

@@ -109,4 +109,27 @@ int launch_colsum(const void* in, int in_bf16, int64_t batch, int64_t rows, int6
                   float* scratch, int64_t chunk_rows, LaunchCtx& ctx, const char* name);
 int64_t colsum_scratch_floats(int64_t batch, int64_t rows, int64_t cols, int64_t chunk_rows);
 
+// Attention core of the head-sharded attention sublayer (tp_attention.cu).
+// Tokens of sequence b are rows b*S .. b*S+S-1.  The projected queries, keys
+// and values live in one bf16 buffer `qkv` [B*S][qkv_rs] holding the T_p
+// shard slices side by side; slice t (columns [t*slice, (t+1)*slice),
+// slice = (H + 2*Hkv) / T_p * hd) is [query heads of shard t | key heads |
+// value heads], each head hd columns wide.  `dqkv` has the same layout.
+struct AttnSpec {
+  int B = 0, S = 0, H = 0, Hkv = 0, T_p = 1, causal = 1;
+  int64_t hd = 128;
+  const void* qkv = nullptr; int64_t qkv_rs = 0;
+  void* o = nullptr; int64_t o_rs = 0;          // head outputs [B*S][o_rs], head h at column h*hd
+  float* lse = nullptr; int64_t s_pad = 0;      // log2-domain log-sum-exp [B*H][s_pad]
+  const void* dO = nullptr; int64_t do_rs = 0;  // gradient of the head outputs
+  float* Dv = nullptr;                          // rowsum(dO * o) [B*H][s_pad] (scratch)
+  void* dqkv = nullptr;
+};
+int launch_attn_fwd(const AttnSpec& a, LaunchCtx& ctx);
+int launch_attn_bwd(const AttnSpec& a, LaunchCtx& ctx);
+// Pack Wq [H*hd][d], Wk, Wv [Hkv*hd][d] into shard slices [T_p][slice][d]
+// (unpack = 1 reverses it).
+int launch_pack_qkv(const void* Wq, const void* Wk, const void* Wv, void* packed, int T_p, int64_t sq, int64_t sk,
+                    int64_t d, int unpack, cudaStream_t st);
+
 }  // namespace tpffn

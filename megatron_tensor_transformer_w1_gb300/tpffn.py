@@ -28,6 +28,10 @@ ABI_FUNCTIONS = (
     "tp_ffn_last_device_error", "tp_ffn_status_string", "tp_ffn_kernel_times", "tp_ffn_last_launch_count",
     "tp_ffn_fwd_static_scratch", "tp_ffn_seq_parallel_workspace_bytes", "tp_ffn_fwd_seq_parallel",
     "tp_ffn_bwd_seq_parallel",
+    "tp_attn_plan_create", "tp_attn_plan_destroy", "tp_attn_plan_info", "tp_attn_packed_bytes",
+    "tp_attn_shard_weights", "tp_attn_unshard_weights", "tp_attn_saved_bytes", "tp_attn_saved_offsets",
+    "tp_attn_workspace_bytes", "tp_attn_fwd", "tp_attn_bwd", "tp_attn_core_fwd", "tp_attn_core_bwd",
+    "tp_attn_kernel_times", "tp_attn_last_launch_count",
 )
 TPFFN_STATIC_SCRATCH_BYTES = 32 << 20
 
@@ -72,6 +76,21 @@ _SIGS = {
     "tp_ffn_seq_parallel_workspace_bytes": (_SZ, [_P, _I64, _INT]),
     "tp_ffn_fwd_seq_parallel": (_INT, [_P, _I64, _P, _P, _P, _P, _P, _P, _P, _P, _SZ, _INT, _P]),
     "tp_ffn_bwd_seq_parallel": (_INT, [_P, _I64, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _SZ, _INT, _P]),
+    "tp_attn_plan_create": (_INT, [ctypes.POINTER(_P), _I64, _INT, _INT, _I64, _INT, _INT, _INT]),
+    "tp_attn_plan_destroy": (None, [_P]),
+    "tp_attn_plan_info": (_INT, [_P] + [ctypes.POINTER(_I64)] * 4),
+    "tp_attn_packed_bytes": (_SZ, [_P, _INT]),
+    "tp_attn_shard_weights": (_INT, [_P, _P, _P, _P, _P, _P, _P, _P]),
+    "tp_attn_unshard_weights": (_INT, [_P, _P, _P, _P, _P, _P, _P, _P]),
+    "tp_attn_saved_bytes": (_SZ, [_P, _I64, _I64]),
+    "tp_attn_saved_offsets": (_INT, [_P, _I64, _I64] + [ctypes.POINTER(_SZ)] * 3),
+    "tp_attn_workspace_bytes": (_SZ, [_P, _I64, _I64, _INT]),
+    "tp_attn_fwd": (_INT, [_P, _I64, _I64, _P, _P, _P, _P, _P, _P, _SZ, _INT, _P]),
+    "tp_attn_bwd": (_INT, [_P, _I64, _I64, _P, _P, _P, _P, _P, _P, _P, _P, _P, _SZ, _INT, _P]),
+    "tp_attn_core_fwd": (_INT, [_P, _I64, _I64, _P, _P, _P, _P, _SZ, _INT, _P]),
+    "tp_attn_core_bwd": (_INT, [_P, _I64, _I64, _P, _P, _P, _P, _P, _P, _SZ, _INT, _P]),
+    "tp_attn_kernel_times": (_INT, [_P, _INT, ctypes.POINTER(ctypes.c_char_p), ctypes.POINTER(ctypes.c_float)]),
+    "tp_attn_last_launch_count": (_INT, [_P]),
 }
 for _name, (_res, _args) in _SIGS.items():
     _f = getattr(_lib, _name)
@@ -218,6 +237,88 @@ def tp_ffn_bwd_seq_parallel(plan, n_tokens, x_slices, w13p, w2p, saved, dy_slice
     return _lib.tp_ffn_bwd_seq_parallel(plan, n_tokens, xs and xs[0], _ptr(w13p), _ptr(w2p), _ptr(saved),
                                         dys and dys[0], dxs and dxs[0], _ptr(dw13p), _ptr(dw2p), _ptr(db1), _ptr(db2),
                                         _ptr(workspace), workspace_bytes, flags, _stream(stream))
+
+
+# ------------------------------------------------------------ attention sublayer
+def tp_attn_plan_create(d_model, n_heads, n_kv_heads, head_dim, T_p, causal, dtype):
+    """Returns (status, plan handle or None)."""
+    h = _P()
+    rc = _lib.tp_attn_plan_create(ctypes.byref(h), d_model, n_heads, n_kv_heads, head_dim, T_p, int(causal), dtype)
+    return rc, (h.value if rc == TP_OK else None)
+
+
+def tp_attn_plan_destroy(plan):
+    _lib.tp_attn_plan_destroy(plan)
+
+
+def tp_attn_plan_info(plan):
+    vals = [_I64() for _ in range(4)]
+    rc = _lib.tp_attn_plan_info(plan, *[ctypes.byref(v) for v in vals])
+    if rc != TP_OK:
+        raise TPFFNError(rc, "tp_attn_plan_info")
+    return dict(zip(("qkv_width", "slice", "sq", "sk"), (v.value for v in vals)))
+
+
+def tp_attn_packed_bytes(plan, which):
+    return _lib.tp_attn_packed_bytes(plan, which)
+
+
+def tp_attn_shard_weights(plan, Wq, Wk, Wv, Wo, wqkv, wo_packed, stream=None):
+    return _lib.tp_attn_shard_weights(plan, _ptr(Wq), _ptr(Wk), _ptr(Wv), _ptr(Wo), _ptr(wqkv), _ptr(wo_packed),
+                                      _stream(stream))
+
+
+def tp_attn_unshard_weights(plan, wqkv, wo_packed, Wq, Wk, Wv, Wo, stream=None):
+    return _lib.tp_attn_unshard_weights(plan, _ptr(wqkv), _ptr(wo_packed), _ptr(Wq), _ptr(Wk), _ptr(Wv), _ptr(Wo),
+                                        _stream(stream))
+
+
+def tp_attn_saved_bytes(plan, B, S):
+    return _lib.tp_attn_saved_bytes(plan, B, S)
+
+
+def tp_attn_saved_offsets(plan, B, S):
+    vals = [_SZ() for _ in range(3)]
+    rc = _lib.tp_attn_saved_offsets(plan, B, S, *[ctypes.byref(v) for v in vals])
+    if rc != TP_OK:
+        raise TPFFNError(rc, "tp_attn_saved_offsets")
+    return dict(zip(("qkv", "c", "lse"), (v.value for v in vals)))
+
+
+def tp_attn_workspace_bytes(plan, B, S, flags=0):
+    return _lib.tp_attn_workspace_bytes(plan, B, S, flags)
+
+
+def tp_attn_fwd(plan, B, S, x, wqkv, wo_packed, y, saved, workspace, workspace_bytes, flags=0, stream=None):
+    return _lib.tp_attn_fwd(plan, B, S, _ptr(x), _ptr(wqkv), _ptr(wo_packed), _ptr(y), _ptr(saved), _ptr(workspace),
+                            workspace_bytes, flags, _stream(stream))
+
+
+def tp_attn_bwd(plan, B, S, x, wqkv, wo_packed, saved, dy, dx, dwqkv, dwo_packed, workspace, workspace_bytes,
+                flags=0, stream=None):
+    return _lib.tp_attn_bwd(plan, B, S, _ptr(x), _ptr(wqkv), _ptr(wo_packed), _ptr(saved), _ptr(dy), _ptr(dx),
+                            _ptr(dwqkv), _ptr(dwo_packed), _ptr(workspace), workspace_bytes, flags, _stream(stream))
+
+
+def tp_attn_core_fwd(plan, B, S, qkv, o, lse, workspace, workspace_bytes, flags=0, stream=None):
+    return _lib.tp_attn_core_fwd(plan, B, S, _ptr(qkv), _ptr(o), _ptr(lse), _ptr(workspace), workspace_bytes, flags,
+                                 _stream(stream))
+
+
+def tp_attn_core_bwd(plan, B, S, qkv, o, lse, dO, dqkv, workspace, workspace_bytes, flags=0, stream=None):
+    return _lib.tp_attn_core_bwd(plan, B, S, _ptr(qkv), _ptr(o), _ptr(lse), _ptr(dO), _ptr(dqkv), _ptr(workspace),
+                                 workspace_bytes, flags, _stream(stream))
+
+
+def tp_attn_kernel_times(plan, max_records=64):
+    names = (ctypes.c_char_p * max_records)()
+    ms = (ctypes.c_float * max_records)()
+    n = _lib.tp_attn_kernel_times(plan, max_records, names, ms)
+    return [(names[i].decode(), ms[i]) for i in range(min(n, max_records))]
+
+
+def tp_attn_last_launch_count(plan):
+    return _lib.tp_attn_last_launch_count(plan)
 
 
 def check(status, where=""):

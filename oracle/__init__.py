@@ -291,6 +291,15 @@ class AttentionCore:
                                      _ptr(dk), _ptr(dv))
         return dq, dk, dv
 
+    def allowance(self, q, k, v, dO, u):
+        """Per-element rounding allowances (a_o, a_dq, a_dk, a_dv) of a bf16
+        computation of this core; see orc_attn_core_allowance."""
+        q, k, v, dO = _f64(q), _f64(k), _f64(v), _f64(dO)
+        out = [np.empty_like(q), np.empty_like(q), np.empty_like(k), np.empty_like(v)]
+        self.lib().orc_attn_core_allowance(ctypes.byref(self._s), _ptr(q), _ptr(k), _ptr(v), _ptr(dO),
+                                           ctypes.c_double(u), *[_ptr(a) for a in out])
+        return tuple(out)
+
 
 class Attention:
     """The head-sharded attention sublayer of one problem.
@@ -320,6 +329,17 @@ class Attention:
         y = np.empty((n, self.d))
         self.core.lib().orc_attn_forward(ctypes.byref(self._s), _ptr(c), _ptr(y))
         return c, y
+
+    def intermediates(self, dy):
+        """The stored intermediates: dict q, k, v, c (head outputs), dO."""
+        dy = _f64(dy)
+        n = self.x.shape[0]
+        nq, nk = self.Wq.shape[0], self.Wk.shape[0]
+        out = dict(q=np.empty((n, nq)), k=np.empty((n, nk)), v=np.empty((n, nk)), c=np.empty((n, nq)),
+                   dO=np.empty((n, nq)))
+        self.core.lib().orc_attn_intermediates(ctypes.byref(self._s), _ptr(dy),
+                                               *[_ptr(out[m]) for m in ("q", "k", "v", "c", "dO")])
+        return out
 
     def backward(self, dy):
         """Returns dict dx, dWq, dWk, dWv, dWo."""

@@ -764,3 +764,109 @@ void orc_attn_backward(const orc_attn* A, const double* dy, double* dx, double* 
   }
   free(dv); free(dk); free(dq); free(dO); free(c); free(v); free(k); free(q);
 }
+
+/* Rounding allowances of a bf16 attention core (test infrastructure, not a
+ * result).  A computation that stores q, k, v, o, dq, dk, dv in bf16, feeds
+ * the probabilities p and the score gradients dS to its products in bf16, and
+ * forms D_i = dO_i . o_i from the stored o strays from the exact values by
+ * rounding alone.  With u one bf16 unit (relative) this returns, per output
+ * element, the root-sum-square of the rounding of every term of its sum plus
+ * the coherent error that the error of D_i adds to every dS_ij of a row:
+ *   a_o  = u (rss_j p_ij v_jd + |o_id|)
+ *   dD_i = u sum_d |dO_id| (|o_id| + rss_j p_ij v_jd)
+ *   a_dq = rss_j (u dS_ij k_jd) + dD_i |sum_j p_ij k_jd| / sqrt(hd) + u |dq_id|
+ *   a_dk = rss_(h in group, i) ((u |dS_ij| + p_ij dD_i / sqrt(hd)) q_id) + u |dk_jd|
+ *   a_dv = rss_(h in group, i) (u p_ij dO_id) + u |dv_jd|
+ * (dS includes the 1/sqrt(hd) of the scores).  Layouts as the core. */
+void orc_attn_core_allowance(const orc_attn_core* C, const double* q, const double* k, const double* v,
+                             const double* dO, double u, double* a_o, double* a_dq, double* a_dk, double* a_dv) {
+  const int64_t B = C->B, S = C->S, H = C->H, Hkv = C->Hkv, hd = C->hd, nq = H * hd, nk = Hkv * hd;
+  const int64_t G = H / Hkv;
+  const double scale = 1.0 / sqrt((double)hd);
+  double* P = (double*)malloc(sizeof(double) * B * H * S * S);
+  double* dS = (double*)malloc(sizeof(double) * B * H * S * S);
+  double* dD = (double*)malloc(sizeof(double) * B * H * S);
+#pragma omp parallel for schedule(dynamic, 1)
+  for (int64_t bhi = 0; bhi < B * H * S; ++bhi) {
+    const int64_t b = bhi / (H * S), h = (bhi / S) % H, i = bhi % S, hk = h / G;
+    double* p = P + bhi * S;
+    double* ds = dS + bhi * S;
+    attn_probs(C, q, k, b, h, i, p);
+    const double* dOi = dO + (b * S + i) * nq + h * hd;
+    double rowdot = 0.0, dd = 0.0;
+    for (int64_t j = 0; j < S; ++j) {
+      ds[j] = dot_row(dOi, v + (b * S + j) * nk + hk * hd, hd);
+      rowdot += p[j] * ds[j];
+    }
+    for (int64_t jd = 0; jd < hd; ++jd) {
+      double o = 0.0, r2 = 0.0;
+      for (int64_t j = 0; j < S; ++j) {
+        const double t = p[j] * v[(b * S + j) * nk + hk * hd + jd];
+        o += t;
+        r2 += t * t;
+      }
+      a_o[(b * S + i) * nq + h * hd + jd] = u * (sqrt(r2) + fabs(o));
+      dd += fabs(dOi[jd]) * (fabs(o) + sqrt(r2));
+    }
+    dD[bhi] = u * dd;
+    for (int64_t j = 0; j < S; ++j) ds[j] = p[j] * (ds[j] - rowdot) * scale;
+  }
+#pragma omp parallel for schedule(dynamic, 1)
+  for (int64_t bhi = 0; bhi < B * H * S; ++bhi) {
+    const int64_t b = bhi / (H * S), h = (bhi / S) % H, i = bhi % S, hk = h / G;
+    for (int64_t jd = 0; jd < hd; ++jd) {
+      double r2 = 0.0, pk = 0.0, dq = 0.0;
+      for (int64_t j = 0; j < S; ++j) {
+        const double kk = k[(b * S + j) * nk + hk * hd + jd];
+        const double t = u * dS[bhi * S + j] * kk;
+        r2 += t * t;
+        pk += P[bhi * S + j] * kk;
+        dq += dS[bhi * S + j] * kk;
+      }
+      a_dq[(b * S + i) * nq + h * hd + jd] = sqrt(r2) + dD[bhi] * scale * fabs(pk) + u * fabs(dq);
+    }
+  }
+#pragma omp parallel for schedule(dynamic, 1)
+  for (int64_t bki = 0; bki < B * Hkv * S; ++bki) {
+    const int64_t b = bki / (Hkv * S), hk = (bki / S) % Hkv, j = bki % S;
+    for (int64_t jd = 0; jd < hd; ++jd) {
+      double rk = 0.0, rv = 0.0, dk = 0.0, dv = 0.0;
+      for (int64_t g = 0; g < G; ++g) {
+        const int64_t h = hk * G + g;
+        for (int64_t i = 0; i < S; ++i) {
+          const int64_t row = (b * H + h) * S + i;
+          const double pij = P[row * S + j], dsij = dS[row * S + j];
+          const double qq = q[(b * S + i) * nq + h * hd + jd], gg = dO[(b * S + i) * nq + h * hd + jd];
+          const double tk = (u * fabs(dsij) + pij * dD[row] * scale) * qq;
+          const double tv = u * pij * gg;
+          rk += tk * tk;
+          rv += tv * tv;
+          dk += dsij * qq;
+          dv += pij * gg;
+        }
+      }
+      a_dk[(b * S + j) * nk + hk * hd + jd] = sqrt(rk) + u * fabs(dk);
+      a_dv[(b * S + j) * nk + hk * hd + jd] = sqrt(rv) + u * fabs(dv);
+    }
+  }
+  free(dD);
+  free(dS);
+  free(P);
+}
+
+/* The sublayer's stored intermediates: q, k, v (rounded as stored), the head
+ * outputs c, and dO = dy Wo (rounded as stored). */
+void orc_attn_intermediates(const orc_attn* A, const double* dy, double* q, double* k, double* v, double* c,
+                            double* dO) {
+  const orc_attn_core* C = &A->core;
+  const int64_t n = C->B * C->S, d = A->d, nq = C->H * C->hd;
+  attn_project(A, q, k, v);
+  orc_attn_core_fwd(C, q, k, v, c, NULL);
+#pragma omp parallel for schedule(static)
+  for (int64_t r = 0; r < n; ++r)
+    for (int64_t col = 0; col < nq; ++col) {
+      double acc = 0.0;
+      for (int64_t o = 0; o < d; ++o) acc += dy[r * d + o] * A->Wo[o * nq + col];
+      dO[r * nq + col] = RND(C->round_bf16, acc);
+    }
+}

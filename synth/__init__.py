@@ -215,6 +215,17 @@ def make_attention_inputs(w: AttnWorkload, seed: int | None = None):
     )
 
 
+def make_core_inputs(B, S, H, Hkv, hd, seed, q_scale=1.0):
+    """bf16 host tensors q [B*S, H*hd] ~ N(0, q_scale^2), k, v [B*S, Hkv*hd] and
+    dO [B*S, H*hd] ~ N(0, 1) for the attention core alone (q_scale > 1 sharpens
+    the softmax)."""
+    streams = np.random.SeedSequence(BASE_SEED + 1000 + seed).spawn(4)
+    rng = [np.random.Generator(np.random.PCG64(s)) for s in streams]
+    n = B * S
+    return dict(q=_draw(rng[0], (n, H * hd), q_scale, "bf16"), k=_draw(rng[1], (n, Hkv * hd), 1.0, "bf16"),
+                v=_draw(rng[2], (n, Hkv * hd), 1.0, "bf16"), dO=_draw(rng[3], (n, H * hd), 1.0, "bf16"))
+
+
 def to_f64(t):
     """Exact float64 widening of a host tensor (None passes through)."""
     if t is None:

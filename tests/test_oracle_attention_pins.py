@@ -263,3 +263,58 @@ def test_attn_gqa_divisibility_golden():
         else:
             with pytest.raises(ValueError):
                 oracle.Attention(*args)
+
+
+# ------------------------------------------------------------------ tolerance model
+def _bf16(a):
+    return torch.from_numpy(np.asarray(a, dtype=np.float32)).to(torch.bfloat16).double().numpy()
+
+
+def _emulate_bf16_core(q, k, v, dO, B, S, H, Hkv, hd, causal):
+    """A bf16 attention core written with numpy: unnormalised probabilities
+    rounded before p v, o rounded, D from the rounded o, dS rounded before its
+    products, every output rounded (the rounding points the allowance models)."""
+    G = H // Hkv
+    sc = 1 / math.sqrt(hd)
+    o, dq = np.zeros_like(q), np.zeros_like(q)
+    dk, dv = np.zeros_like(k), np.zeros_like(v)
+    for b in range(B):
+        rows = slice(b * S, (b + 1) * S)
+        for h in range(H):
+            hk = h // G
+            Q, K, V = q[rows, h * hd:(h + 1) * hd], k[rows, hk * hd:(hk + 1) * hd], v[rows, hk * hd:(hk + 1) * hd]
+            s = (Q @ K.T) * sc
+            if causal:
+                s = np.where(np.tril(np.ones((S, S))) > 0, s, -np.inf)
+            e = np.exp(s - s.max(1, keepdims=True))
+            l = e.sum(1, keepdims=True)
+            ob = _bf16((_bf16(e) @ V) / l)
+            o[rows, h * hd:(h + 1) * hd] = ob
+            P = e / l
+            g = dO[rows, h * hd:(h + 1) * hd]
+            dS = _bf16(P * (g @ V.T - (g * ob).sum(1, keepdims=True)) * sc)
+            dq[rows, h * hd:(h + 1) * hd] = dS @ K
+            dk[rows, hk * hd:(hk + 1) * hd] += dS.T @ Q
+            dv[rows, hk * hd:(hk + 1) * hd] += _bf16(P).T @ g
+    return o, _bf16(dq), _bf16(dk), _bf16(dv)
+
+
+@pytest.mark.parametrize("case", [(2, 40, 4, 2, 16, True, 1.0), (1, 64, 2, 2, 32, False, 4.0)])
+def test_attn_allowance_bounds_a_bf16_computation(case):
+    """The rounding allowance used by the GPU parity tests bounds how far a
+    bf16 computation of the same steps strays from the exact result (here a
+    numpy emulation of those rounding points), with the factor those tests
+    use; and it is not vacuous: it stays within 10% of the values' RMS."""
+    B, S, H, Hkv, hd, causal, qs = case
+    rng = np.random.default_rng(21)
+    q = _bf16(rng.standard_normal((B * S, H * hd)) * qs)
+    k, v = (_bf16(rng.standard_normal((B * S, Hkv * hd))) for _ in range(2))
+    dO = _bf16(rng.standard_normal((B * S, H * hd)))
+    C = oracle.AttentionCore(B, S, H, Hkv, hd, causal=causal, round_bf16=True)
+    o, _ = C.forward(q, k, v)
+    exact = (o,) + C.backward(q, k, v, dO)
+    allow = C.allowance(q, k, v, dO, 2.0 ** -8)
+    emul = _emulate_bf16_core(q, k, v, dO, B, S, H, Hkv, hd, causal)
+    for name, e, r, a in zip(("o", "dq", "dk", "dv"), emul, exact, allow):
+        assert np.all(np.abs(e - r) <= 1e-2 * (np.abs(r) + 1) + 3 * a), name
+        assert np.sqrt(np.mean(a ** 2)) < 0.1 * np.sqrt(np.mean(r ** 2)), name
