@@ -316,6 +316,7 @@ def run_ours(args, ctx):
     standalone = run_standalone_sum(dev, 10, peaks) if not args.no_extras else None
     workloads = run_all_workloads(dev, 10) if not args.no_extras else None
     seq_parallel = run_seq_parallel(dev, 10, peaks) if not args.no_extras else None
+    attention = run_attention(dev, 10, peaks, args.sum) if not args.no_extras else None
 
     value = ctx["world"] * flop_step / (ms * 1e-3) / 1e12
     line = {
@@ -339,6 +340,7 @@ def run_ours(args, ctx):
         "standalone_shard_sum": standalone,
         "workloads": workloads,
         "sequence_parallel": seq_parallel,
+        "attention_sublayer": attention,
     }
     if ctx["rank"] == 0 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(w, budget_s=args.cpu_budget)
@@ -512,6 +514,99 @@ def run_seq_parallel(dev, steps, peaks):
         res["step_tflops_fwd_bwd"] = round((w.fwd_flops() + w.bwd_flops()) /
                                            ((res["fwd_ms"] + res["bwd_ms"]) * 1e-3) / 1e12, 2)
         out[mode] = res
+    return out
+
+
+def _attn_kernel_work(w, name):
+    """FLOPs one launch of the attention sublayer executes (visible score
+    entries only for the attention kernels: the dq kernel recomputes S and dP
+    and forms dQ -- 3 products; the dk/dv kernel recomputes S^T and dP^T and
+    forms dV and dK -- 4 products; the forward forms S and PV -- 2)."""
+    n, d, nq, nk = w.N, w.d, w.H * w.hd, w.Hkv * w.hd
+    half = w.core_flops() // 2  # one product over the visible pairs
+    table = {"qkv_proj": 2 * n * d * (nq + 2 * nk), "attn_fwd": 2 * half, "down_fused_sum": 2 * n * nq * d,
+             "down_partials": 2 * n * nq * d, "dgrad_heads": 2 * n * d * nq, "wgrad_rows": 2 * n * d * nq,
+             "attn_bwd_dq": 3 * half, "attn_bwd_dkdv": 4 * half,
+             "attn_dgrad_x_fused_sum": 2 * n * (nq + 2 * nk) * d, "attn_dgrad_x_partials": 2 * n * (nq + 2 * nk) * d,
+             "attn_wgrad_qkv": 2 * n * (nq + 2 * nk) * d}
+    return table.get(name)
+
+
+def run_attention(dev, steps, peaks, sum_mode="fused"):
+    """The whole head-sharded attention sublayer (fwd + bwd incl. weight
+    gradients) on its two workloads: ms, TFLOP/s (FlashAttention counting:
+    backward core = 2.5x forward core) and per-kernel times and rates."""
+    import torch
+    from synth import ATTN_WORKLOADS
+    from megatron_tensor_transformer_w1_gb300 import tpffn as abi
+    from megatron_tensor_transformer_w1_gb300.attention import TensorParallelAttention
+    out = {}
+    for name, w in ATTN_WORKLOADS.items():
+        gen = torch.Generator(device=dev)
+        gen.manual_seed(20260000 + w.seed_index)
+
+        def draw(shape, std):
+            return (torch.randn(*shape, generator=gen, device=dev) * std).to(torch.bfloat16)
+
+        nq, nk = w.H * w.hd, w.Hkv * w.hd
+        x, dy = draw((w.N, w.d), 1.0), draw((w.N, w.d), 1.0)
+        attn = TensorParallelAttention(w.d, w.H, w.Hkv, w.hd, w.T_p, causal=w.causal, device=dev)
+        wqkv, wo = attn.pack(draw((nq, w.d), w.d ** -0.5), draw((nk, w.d), w.d ** -0.5),
+                             draw((nk, w.d), w.d ** -0.5), draw((w.d, nq), nq ** -0.5))
+        st = torch.cuda.current_stream(dev)
+        flags = abi.TP_SUM_FUSED if sum_mode == "fused" else 0
+        y = torch.empty(w.N, w.d, dtype=torch.bfloat16, device=dev)
+        dx = torch.empty_like(y)
+        saved = torch.empty(abi.tp_attn_saved_bytes(attn.plan, w.B, w.S), dtype=torch.uint8, device=dev)
+        dwqkv, dwo = torch.empty_like(wqkv), torch.empty_like(wo)
+        ws = attn.workspace(w.B, w.S, flags)
+
+        def fwd(extra=0):
+            abi.check(abi.tp_attn_fwd(attn.plan, w.B, w.S, x, wqkv, wo, y, saved, ws, ws.numel(), flags | extra, st),
+                      "attn_fwd")
+
+        def bwd(extra=0):
+            abi.check(abi.tp_attn_bwd(attn.plan, w.B, w.S, x, wqkv, wo, saved, dy, dx, dwqkv, dwo, ws, ws.numel(),
+                                      flags | extra, st), "attn_bwd")
+
+        res = {"B": w.B, "S": w.S, "d": w.d, "heads": w.H, "kv_heads": w.Hkv, "head_dim": w.hd, "T_p": w.T_p,
+               "causal": w.causal, "shard_sum": sum_mode}
+        for ph, fn in (("fwd", fwd), ("bwd", bwd)):
+            for _ in range(3):
+                fwd()
+                fn()
+            torch.cuda.synchronize(dev)
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(st)
+            for _ in range(steps):
+                fn()
+            e1.record(st)
+            torch.cuda.synchronize(dev)
+            res[ph + "_ms"] = round(e0.elapsed_time(e1) / steps, 4)
+        flop = w.fwd_flops() + w.bwd_flops()
+        res["flop_per_step"] = flop
+        res["step_tflops_fwd_bwd"] = round(flop / ((res["fwd_ms"] + res["bwd_ms"]) * 1e-3) / 1e12, 2)
+        res["frac_of_bf16_peak"] = round(res["step_tflops_fwd_bwd"] / peaks["bf16"], 4)
+        # per-kernel breakdown (events around every launch)
+        abi.tp_attn_kernel_times(attn.plan, 0)
+        for _ in range(steps):
+            fwd(abi.TP_FLAG_TIMING)
+            bwd(abi.TP_FLAG_TIMING)
+        per = {}
+        for k, t in abi.tp_attn_kernel_times(attn.plan, 100000):
+            per.setdefault(k, []).append(t)
+        kern = {}
+        for k, v in per.items():
+            ms = sum(v) / len(v)
+            e = {"ms": round(ms, 4)}
+            f = _attn_kernel_work(w, k)
+            if f:
+                e["tflops"] = round(f / (ms * 1e-3) / 1e12, 1)
+                e["frac_of_bf16_peak"] = round(f / (ms * 1e-3) / 1e12 / peaks["bf16"], 4)
+            kern[k] = e
+        res["kernels"] = kern
+        out[name] = res
+        del attn
     return out
 
 

@@ -54,8 +54,9 @@ using namespace tc;
 
 constexpr int HD = 128;            // head width
 constexpr int TILE = 128 * HD * 2; // [128 rows][128 cols] bf16: two 64-column boxes
-constexpr int NT = 192;            // producer warp, MMA warp, 4 softmax warps
-constexpr int NSM = 128;           // softmax threads
+constexpr int NT = 320;            // producer warp, MMA warp, 8 softmax warps
+constexpr int NSM = 256;           // softmax threads: two warps per TMEM lane quarter,
+                                   // each taking half of the tile's columns
 
 // Column geometry of the packed q/k/v buffer (see AttnSpec).
 struct Geo {
@@ -112,6 +113,13 @@ __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32
       : "memory");
 }
 __device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
+// 2^x by the SFU instruction (ex2.approx, flush-to-zero): a few ulp, far
+// below the bf16 rounding the probabilities get next; 2^-inf = 0.
+__device__ __forceinline__ float ex2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
 
 // Shared-memory descriptor of a 128-byte-swizzled tile (version 1, SBO 1024).
 __device__ __forceinline__ uint64_t sw128_desc(uint32_t addr, uint32_t lbo) {
@@ -186,28 +194,35 @@ __device__ __forceinline__ void store_row_bf16(__nv_bfloat16* dst, const uint32_
 constexpr int F_Q = 0;
 constexpr int F_K = F_Q + TILE;       // 2 stages
 constexpr int F_V = F_K + 2 * TILE;   // 2 stages
-constexpr int F_P = F_V + 2 * TILE;   // P [128 q][128 keys]
-constexpr int F_BAR = F_P + TILE;
+constexpr int F_P = F_V + 2 * TILE;   // 2 buffers of P [128 q][128 keys]
+constexpr int F_X = F_P + 2 * TILE;   // row max / sum exchange [2 halves][128 rows] fp32
+constexpr int F_BAR = F_X + 1024;
 constexpr int F_SMEM = F_BAR + 256 + 1024;
 
+// P buffers and their "PV done" barriers are indexed by the running count g
+// of P blocks of the CTA (g & 1): the softmax threads may fill buffer g & 1
+// once PV g-2 has read it, so they overlap the exponentials of one block with
+// the PV product of the previous one.
 __global__ void __launch_bounds__(NT, 1) attn_fwd_kernel(const __grid_constant__ CUtensorMap tq, const Params p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = align1024(smem_raw);
   uint64_t* bar = reinterpret_cast<uint64_t*>(smem + F_BAR);
   uint64_t* q_full = bar + 0;
   uint64_t* q_empty = bar + 1;
-  uint64_t* k_full = bar + 2;
-  uint64_t* k_empty = bar + 4;
-  uint64_t* v_full = bar + 6;
-  uint64_t* v_empty = bar + 8;
-  uint64_t* s_full = bar + 10;
-  uint64_t* s_empty = bar + 12;
+  uint64_t* k_full = bar + 2;   // [2]
+  uint64_t* k_empty = bar + 4;  // [2]
+  uint64_t* v_full = bar + 6;   // [2]
+  uint64_t* v_empty = bar + 8;  // [2]
+  uint64_t* s_full = bar + 10;  // [2]
+  uint64_t* s_empty = bar + 12; // [2]
   uint64_t* p_full = bar + 14;
-  uint64_t* pv_done = bar + 15;
-  uint64_t* o_empty = bar + 16;
-  uint64_t* drain = bar + 17;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bar + 18);
-  volatile int* abort_flag = reinterpret_cast<volatile int*>(bar + 18) + 1;
+  uint64_t* pv_done = bar + 15; // [2]
+  uint64_t* o_empty = bar + 17;
+  uint64_t* drain = bar + 18;
+  uint64_t* pair_x = bar + 19;  // [4] both halves of a row wrote their value
+  uint64_t* pair_r = bar + 23;  // [4] both halves read their partner's value
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bar + 27);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(bar + 27) + 1;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
   if (threadIdx.x == 0) {
@@ -220,11 +235,15 @@ __global__ void __launch_bounds__(NT, 1) attn_fwd_kernel(const __grid_constant__
       mbar_init(&v_empty[i], 1);
       mbar_init(&s_full[i], 1);
       mbar_init(&s_empty[i], NSM);
+      mbar_init(&pv_done[i], 1);
     }
     mbar_init(p_full, NSM);
-    mbar_init(pv_done, 1);
     mbar_init(o_empty, NSM);
     mbar_init(drain, 1);
+    for (int i = 0; i < 4; ++i) {
+      mbar_init(&pair_x[i], 64);
+      mbar_init(&pair_r[i], 64);
+    }
     *abort_flag = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
@@ -284,8 +303,8 @@ __global__ void __launch_bounds__(NT, 1) attn_fwd_kernel(const __grid_constant__
     if (lane == 0) {
       constexpr uint32_t ID_S = idesc(128, 0, 0);   // S = Q K^T
       constexpr uint32_t ID_PV = idesc(128, 0, 1);  // O += P V (V: N = hd contiguous)
-      const uint32_t qa = smem_u32(smem + F_Q), pa = smem_u32(smem + F_P);
-      uint32_t kv = 0, sc = 0, pc = 0, it = 0;
+      const uint32_t qa = smem_u32(smem + F_Q);
+      uint32_t kv = 0, sc = 0, pg = 0, it = 0;
       bool ok = true;
       for (int item = blockIdx.x; item < p.items && ok; item += gridDim.x, ++it) {
         int qb, b, h;
@@ -312,19 +331,20 @@ __global__ void __launch_bounds__(NT, 1) attn_fwd_kernel(const __grid_constant__
         if (!issue_s(0)) break;
         for (int j = 0; j < nkb; ++j) {
           if (j + 1 < nkb && !issue_s(j + 1)) { ok = false; break; }
-          if (!W(p_full, pc & 1u)) { ok = false; break; }
+          if (!W(p_full, pg & 1u)) { ok = false; break; }
           if (j == 0 && !W(o_empty, (it & 1u) ^ 1u)) { ok = false; break; }
           const uint32_t n = kv + j;
           const int st = n & 1;
           if (!W(&v_full[st], (n >> 1) & 1u)) { ok = false; break; }
           tc_fence_after();
           const uint32_t va = smem_u32(smem + F_V + st * TILE);
+          const uint32_t pa = smem_u32(smem + F_P + (pg & 1u) * TILE);
 #pragma unroll
           for (int ks = 0; ks < 8; ++ks)
             umma_bf16(tmem + 256, kdesc(pa, 128, ks), mndesc(va, 128, ks), ID_PV, (j > 0 || ks > 0) ? 1u : 0u);
           umma_commit(&v_empty[st]);
-          umma_commit(pv_done);
-          ++pc;
+          umma_commit(&pv_done[pg & 1u]);
+          ++pg;
         }
         kv += nkb;
         sc += nkb;
@@ -334,98 +354,135 @@ __global__ void __launch_bounds__(NT, 1) attn_fwd_kernel(const __grid_constant__
     }
     __syncwarp();
   } else {
-    // ------------------------------------------------ softmax warps 2..5
-    const int quarter = warp & 3;
+    // ------------------------------------------------ softmax warps 2..9
+    // warp w serves TMEM lanes 32 (w % 4) .. (rows of the tile) and the
+    // columns [64 half, 64 half + 64) of the S and O accumulators
+    const int quarter = warp & 3, half = (warp - 2) >> 2;
     const int row = quarter * 32 + lane;
     const uint32_t tl = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
-    const uint32_t pt = smem_u32(smem + F_P);
-    uint32_t sc = 0, pvw = 0, it = 0;
+    float* xs = reinterpret_cast<float*>(smem + F_X);
+    uint32_t xe = 0;  // exchanges done with the partner warp
+    // swap a per-row value with the partner half (bounded waits)
+    auto exchange = [&](float mine, float& theirs) -> bool {
+      if (xe > 0 && !W.warp(&pair_r[quarter], (xe - 1) & 1u)) return false;
+      xs[half * 128 + row] = mine;
+      mbar_arrive(&pair_x[quarter]);
+      if (!W.warp(&pair_x[quarter], xe & 1u)) return false;
+      theirs = xs[(1 - half) * 128 + row];
+      mbar_arrive(&pair_r[quarter]);
+      ++xe;
+      return true;
+    };
+    uint32_t sc = 0, pg = 0, it = 0;
     for (int item = blockIdx.x; item < p.items; item += gridDim.x, ++it) {
       int qb, b, h;
       decode_item(p, item, p.H, p.causal != 0, qb, b, h);
       const int nkb = p.causal ? qb + 1 : p.n_qb;
       const int qpos = qb * 128 + row;
-      float m_used = -INFINITY, l = 0.f;
+      float m_used = -INFINITY, l = 0.f;  // l: this half's share of the row sum
       bool ok = true;
       for (int j = 0; j < nkb; ++j) {
         const uint32_t buf = sc & 1u, use = sc >> 1;
         ++sc;
         if (!W.warp(&s_full[buf], use & 1u)) { ok = false; break; }
         tc_fence_after();
-        uint32_t r[128];
-#pragma unroll
-        for (int c = 0; c < 4; ++c)
-          tmem_ld32(tl + buf * 128 + c * 32, *reinterpret_cast<uint32_t(*)[32]>(&r[c * 32]));
+        uint32_t r[64];
+        tmem_ld32(tl + buf * 128 + half * 64, *reinterpret_cast<uint32_t(*)[32]>(&r[0]));
+        tmem_ld32(tl + buf * 128 + half * 64 + 32, *reinterpret_cast<uint32_t(*)[32]>(&r[32]));
         tmem_wait_ld();
         tc_fence_before();
         mbar_arrive(&s_empty[buf]);
-        const int kbase = j * 128;
-        float mx = -INFINITY;
+        const int kbase = j * 128 + half * 64;
+        // only the diagonal block (causal) and a block past the end of the
+        // sequence hold invisible keys; elsewhere every key is visible
+        if ((p.causal && j * 128 + 127 > qb * 128) || j * 128 + 128 > p.S) {
 #pragma unroll
-        for (int c = 0; c < 128; ++c) {
-          const int key = kbase + c;
-          const bool vis = key < p.S && (!p.causal || key <= qpos);
-          const float x = vis ? __uint_as_float(r[c]) * p.scale_log2 : -INFINITY;
-          r[c] = __float_as_uint(x);
-          mx = fmaxf(mx, x);
+          for (int c = 0; c < 64; ++c) {
+            const int key = kbase + c;
+            const bool vis = key < p.S && (!p.causal || key <= qpos);
+            r[c] = vis ? r[c] : __float_as_uint(-INFINITY);
+          }
         }
+        // row maximum of the raw scores: eight chains, then the partner's half
+        float m8[8];
+#pragma unroll
+        for (int c = 0; c < 8; ++c) m8[c] = __uint_as_float(r[c]);
+#pragma unroll
+        for (int c = 8; c < 64; ++c) m8[c & 7] = fmaxf(m8[c & 7], __uint_as_float(r[c]));
+        const float mh = fmaxf(fmaxf(fmaxf(m8[0], m8[1]), fmaxf(m8[2], m8[3])),
+                               fmaxf(fmaxf(m8[4], m8[5]), fmaxf(m8[6], m8[7])));
+        float mo;
+        if (!exchange(mh, mo)) { ok = false; break; }
+        const float mx = fmaxf(mh, mo) * p.scale_log2;
         float alpha = 1.f;
         bool rescale = false;
         if (j == 0) {
           m_used = mx;
         } else if (mx > m_used + 8.f) {  // lazy rescale: p stays <= 2^8 otherwise
-          alpha = exp2f(m_used - mx);
+          alpha = ex2(m_used - mx);
           m_used = mx;
           rescale = true;
         }
-        l *= alpha;
-        uint32_t pk[64];
-#pragma unroll
-        for (int c = 0; c < 64; ++c) {
-          const float p0 = exp2f(__uint_as_float(r[2 * c]) - m_used);
-          const float p1 = exp2f(__uint_as_float(r[2 * c + 1]) - m_used);
-          l += p0 + p1;
-          pk[c] = pack_bf16x2(p0, p1);
-        }
-        if (j > 0) {  // PV of the previous block done: P buffer free, O current
-          if (!W.warp(pv_done, pvw & 1u)) { ok = false; break; }
-          ++pvw;
-          tc_fence_after();
-        }
+        const uint32_t g = pg + j;
         if (__any_sync(0xffffffffu, rescale)) {
+          // O must hold PV g-1 before it is rescaled
+          const uint32_t gp = g - 1;
+          if (!W.warp(&pv_done[gp & 1u], (gp >> 1) & 1u)) { ok = false; break; }
+          tc_fence_after();
 #pragma unroll 1
-          for (int c = 0; c < 4; ++c) {
+          for (int c = 0; c < 2; ++c) {
             uint32_t o[32];
-            tmem_ld32(tl + 256 + c * 32, o);
+            const uint32_t ta = tl + 256 + half * 64 + c * 32;
+            tmem_ld32(ta, o);
             tmem_wait_ld();
 #pragma unroll
             for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
-            tmem_st32(tl + 256 + c * 32, o);
+            tmem_st32(ta, o);
           }
           tmem_wait_st();
         }
+        // P buffer g & 1 is free once PV g-2 has read it
+        if (!W.warp(&pv_done[g & 1u], ((g >> 1) & 1u) ^ 1u)) { ok = false; break; }
+        const uint32_t pt = smem_u32(smem + F_P + (g & 1u) * TILE);
+        const float neg_m = -m_used;
+        float l8[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-        for (int c8 = 0; c8 < 16; ++c8)
-          st_shared_v4(sw_chunk(pt, 128, row, c8), pk[4 * c8], pk[4 * c8 + 1], pk[4 * c8 + 2], pk[4 * c8 + 3]);
+        for (int c8 = 0; c8 < 8; ++c8) {
+          float e[8];
+#pragma unroll
+          for (int q = 0; q < 8; ++q) {
+            e[q] = ex2(fmaf(__uint_as_float(r[c8 * 8 + q]), p.scale_log2, neg_m));
+            l8[q] += e[q];
+          }
+          st_shared_v4(sw_chunk(pt, 128, row, half * 8 + c8), pack_bf16x2(e[0], e[1]), pack_bf16x2(e[2], e[3]),
+                       pack_bf16x2(e[4], e[5]), pack_bf16x2(e[6], e[7]));
+        }
+        l = l * alpha + (((l8[0] + l8[1]) + (l8[2] + l8[3])) + ((l8[4] + l8[5]) + (l8[6] + l8[7])));
         fence_async_smem();
         tc_fence_before();
         mbar_arrive(p_full);
       }
       if (!ok) break;
-      if (!W.warp(pv_done, pvw & 1u)) break;
-      ++pvw;
+      const uint32_t glast = pg + nkb - 1;
+      pg += nkb;
+      float lo;
+      if (!exchange(l, lo)) break;
+      const float lsum = l + lo;
+      if (!W.warp(&pv_done[glast & 1u], (glast >> 1) & 1u)) break;
       tc_fence_after();
       const bool row_ok = qpos < p.S;
-      const float inv = 1.f / l;
-      __nv_bfloat16* orow = p.o + (static_cast<long long>(b) * p.S + qpos) * p.o_rs + h * HD;
+      const float inv = 1.f / lsum;
+      __nv_bfloat16* orow = p.o + (static_cast<long long>(b) * p.S + qpos) * p.o_rs + h * HD + half * 64;
 #pragma unroll 1
-      for (int c = 0; c < 4; ++c) {
+      for (int c = 0; c < 2; ++c) {
         uint32_t o[32];
-        tmem_ld32(tl + 256 + c * 32, o);
+        tmem_ld32(tl + 256 + half * 64 + c * 32, o);
         tmem_wait_ld();
         if (row_ok) store_row_bf16(orow + c * 32, o, inv);
       }
-      if (row_ok) p.lse[(static_cast<long long>(b) * p.H + h) * p.s_pad + qpos] = m_used + log2f(l);
+      // rows past the sequence get lse = +inf: the backward reads them as p = 0
+      if (half == 0)
+        p.lse[(static_cast<long long>(b) * p.H + h) * p.s_pad + qpos] = row_ok ? m_used + log2f(lsum) : INFINITY;
       tc_fence_before();
       mbar_arrive(o_empty);
     }
@@ -441,29 +498,34 @@ __global__ void __launch_bounds__(NT, 1) attn_fwd_kernel(const __grid_constant__
 
 // ================================================================ D = rowsum(dO * o)
 __global__ void attn_prep_kernel(const Params p) {
+  // one thread per (sequence, head, padded position); positions past the
+  // sequence get D = 0
   const long long idx = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
-  const long long total = static_cast<long long>(p.B) * p.S * p.H;
+  const long long total = static_cast<long long>(p.B) * p.H * p.s_pad;
   if (idx >= total) return;
-  const int h = static_cast<int>(idx % p.H);
-  const long long tok = idx / p.H;
-  const int b = static_cast<int>(tok / p.S), i = static_cast<int>(tok % p.S);
-  const __nv_bfloat16* o = p.o + tok * p.o_rs + h * HD;
-  const __nv_bfloat16* g = p.dO + tok * p.do_rs + h * HD;
+  const int i = static_cast<int>(idx % p.s_pad);
+  const long long bh = idx / p.s_pad;
+  const int h = static_cast<int>(bh % p.H), b = static_cast<int>(bh / p.H);
   float acc = 0.f;
+  if (i < p.S) {
+    const long long tok = static_cast<long long>(b) * p.S + i;
+    const __nv_bfloat16* o = p.o + tok * p.o_rs + h * HD;
+    const __nv_bfloat16* g = p.dO + tok * p.do_rs + h * HD;
 #pragma unroll 4
-  for (int c = 0; c < HD; c += 8) {
-    const uint4 a = *reinterpret_cast<const uint4*>(o + c);
-    const uint4 d = *reinterpret_cast<const uint4*>(g + c);
-    const __nv_bfloat162* ah = reinterpret_cast<const __nv_bfloat162*>(&a);
-    const __nv_bfloat162* dh = reinterpret_cast<const __nv_bfloat162*>(&d);
+    for (int c = 0; c < HD; c += 8) {
+      const uint4 a = *reinterpret_cast<const uint4*>(o + c);
+      const uint4 d = *reinterpret_cast<const uint4*>(g + c);
+      const __nv_bfloat162* ah = reinterpret_cast<const __nv_bfloat162*>(&a);
+      const __nv_bfloat162* dh = reinterpret_cast<const __nv_bfloat162*>(&d);
 #pragma unroll
-    for (int k = 0; k < 4; ++k) {
-      const float2 af = __bfloat1622float2(ah[k]), df = __bfloat1622float2(dh[k]);
-      acc = fmaf(af.x, df.x, acc);
-      acc = fmaf(af.y, df.y, acc);
+      for (int k = 0; k < 4; ++k) {
+        const float2 af = __bfloat1622float2(ah[k]), df = __bfloat1622float2(dh[k]);
+        acc = fmaf(af.x, df.x, acc);
+        acc = fmaf(af.y, df.y, acc);
+      }
     }
   }
-  p.Dv[(static_cast<long long>(b) * p.H + h) * p.s_pad + i] = acc;
+  p.Dv[idx] = acc;
 }
 
 // ================================================================ dq
@@ -635,7 +697,9 @@ __global__ void __launch_bounds__(NT, 1) attn_dq_kernel(const __grid_constant__ 
     }
     __syncwarp();
   } else {
-    const int quarter = warp & 3;
+    // warp w: TMEM lanes 32 (w % 4) .., columns [32 half, 32 half + 32) of
+    // the 64-key S and dP blocks and [64 half, 64 half + 64) of dQ
+    const int quarter = warp & 3, half = (warp - 2) >> 2;
     const int row = quarter * 32 + lane;
     const uint32_t tl = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
     const uint32_t dst = smem_u32(smem + Q_DS);
@@ -647,39 +711,45 @@ __global__ void __launch_bounds__(NT, 1) attn_dq_kernel(const __grid_constant__ 
       const int qpos = qb * 128 + row;
       const bool row_ok = qpos < p.S;
       const long long vrow = (static_cast<long long>(b) * p.H + h) * p.s_pad + qpos;
-      const float lse_r = row_ok ? p.lse[vrow] : 0.f;
-      const float d_r = row_ok ? p.Dv[vrow] : 0.f;
+      // rows past the sequence read lse = +inf (written by the forward): p = 0
+      const float lse_r = p.lse[vrow];
+      const float ds_off = p.Dv[vrow] * p.scale;
       bool ok = true;
       for (int j = 0; j < nkb; ++j) {
         const uint32_t buf = sc & 1u, use = sc >> 1;
         ++sc;
         if (!W.warp(&sdp_full[buf], use & 1u)) { ok = false; break; }
         tc_fence_after();
-        uint32_t rs[64], rp[64];
-        tmem_ld32(tl + buf * 64, *reinterpret_cast<uint32_t(*)[32]>(&rs[0]));
-        tmem_ld32(tl + buf * 64 + 32, *reinterpret_cast<uint32_t(*)[32]>(&rs[32]));
-        tmem_ld32(tl + 128 + buf * 64, *reinterpret_cast<uint32_t(*)[32]>(&rp[0]));
-        tmem_ld32(tl + 128 + buf * 64 + 32, *reinterpret_cast<uint32_t(*)[32]>(&rp[32]));
+        uint32_t rs[32], rp[32];
+        tmem_ld32(tl + buf * 64 + half * 32, rs);
+        tmem_ld32(tl + 128 + buf * 64 + half * 32, rp);
         tmem_wait_ld();
         tc_fence_before();
         mbar_arrive(&sdp_empty[buf]);
-        uint32_t pk[32];
+        // keys past the sequence need no mask here: their K rows are zero
+        // filled, so they add nothing to dQ; only the causal diagonal does
+        const int kbase = j * 64 + half * 32;
+        if (p.causal && j * 64 + 63 > qb * 128) {
 #pragma unroll
-        for (int c = 0; c < 64; c += 2) {
+          for (int c = 0; c < 32; ++c)
+            rs[c] = (kbase + c <= qpos) ? rs[c] : __float_as_uint(-INFINITY);
+        }
+        uint32_t pk[16];
+#pragma unroll
+        for (int c = 0; c < 32; c += 2) {
           float ds[2];
 #pragma unroll
           for (int e = 0; e < 2; ++e) {
-            const int key = j * 64 + c + e;
-            const bool vis = row_ok && key < p.S && (!p.causal || key <= qpos);
-            const float pr = vis ? exp2f(__uint_as_float(rs[c + e]) * p.scale_log2 - lse_r) : 0.f;
-            ds[e] = pr * (__uint_as_float(rp[c + e]) - d_r) * p.scale;
+            const float pr = ex2(fmaf(__uint_as_float(rs[c + e]), p.scale_log2, -lse_r));
+            ds[e] = pr * fmaf(__uint_as_float(rp[c + e]), p.scale, -ds_off);
           }
           pk[c / 2] = pack_bf16x2(ds[0], ds[1]);
         }
         if (j > 0 && !W.warp(ds_free, (dsbase + j - 1) & 1u)) { ok = false; break; }
 #pragma unroll
-        for (int c8 = 0; c8 < 8; ++c8)
-          st_shared_v4(sw_chunk(dst, 128, row, c8), pk[4 * c8], pk[4 * c8 + 1], pk[4 * c8 + 2], pk[4 * c8 + 3]);
+        for (int c8 = 0; c8 < 4; ++c8)
+          st_shared_v4(sw_chunk(dst, 128, row, half * 4 + c8), pk[4 * c8], pk[4 * c8 + 1], pk[4 * c8 + 2],
+                       pk[4 * c8 + 3]);
         fence_async_smem();
         tc_fence_before();
         mbar_arrive(ds_full);
@@ -687,11 +757,12 @@ __global__ void __launch_bounds__(NT, 1) attn_dq_kernel(const __grid_constant__ 
       if (!ok) break;
       if (!W.warp(dq_full, it & 1u)) break;
       tc_fence_after();
-      __nv_bfloat16* out = p.dqkv + (static_cast<long long>(b) * p.S + qpos) * p.dqkv_rs + p.g.qcol(h);
+      __nv_bfloat16* out =
+          p.dqkv + (static_cast<long long>(b) * p.S + qpos) * p.dqkv_rs + p.g.qcol(h) + half * 64;
 #pragma unroll 1
-      for (int c = 0; c < 4; ++c) {
+      for (int c = 0; c < 2; ++c) {
         uint32_t o[32];
-        tmem_ld32(tl + 256 + c * 32, o);
+        tmem_ld32(tl + 256 + half * 64 + c * 32, o);
         tmem_wait_ld();
         if (row_ok) store_row_bf16(out + c * 32, o, 1.f);
       }
@@ -900,7 +971,10 @@ __global__ void __launch_bounds__(NT, 1) attn_dkdv_kernel(const __grid_constant_
     }
     __syncwarp();
   } else {
-    const int quarter = warp & 3;
+    // warp w: TMEM lanes 32 (w % 4) .. (keys of the tile), query columns
+    // [32 half, 32 half + 32) of each 64-query block, and columns
+    // [64 half, 64 half + 64) of dV and dK
+    const int quarter = warp & 3, half = (warp - 2) >> 2;
     const int row = quarter * 32 + lane;
     const uint32_t tl = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
     const uint32_t pts = smem_u32(smem + V_PT), dss = smem_u32(smem + V_DST);
@@ -922,42 +996,53 @@ __global__ void __launch_bounds__(NT, 1) attn_dkdv_kernel(const __grid_constant_
         ++sc;
         if (!W.warp(&sdp_full[buf], use & 1u)) { ok = false; break; }
         tc_fence_after();
-        uint32_t rs[64], rp[64];
-        tmem_ld32(tl + buf * 64, *reinterpret_cast<uint32_t(*)[32]>(&rs[0]));
-        tmem_ld32(tl + buf * 64 + 32, *reinterpret_cast<uint32_t(*)[32]>(&rs[32]));
-        tmem_ld32(tl + 128 + buf * 64, *reinterpret_cast<uint32_t(*)[32]>(&rp[0]));
-        tmem_ld32(tl + 128 + buf * 64 + 32, *reinterpret_cast<uint32_t(*)[32]>(&rp[32]));
+        uint32_t rs[32], rp[32];
+        tmem_ld32(tl + buf * 64 + half * 32, rs);
+        tmem_ld32(tl + 128 + buf * 64 + half * 32, rp);
         tmem_wait_ld();
         tc_fence_before();
         mbar_arrive(&sdp_empty[buf]);
         if (!W.warp(&q_full[st], ph)) { ok = false; break; }  // lse / D of this block landed
-        const float* lse_v = vec + st * 128;
+        const float* lse_v = vec + st * 128 + half * 32;
         const float* d_v = lse_v + 64;
-        uint32_t pp[32], pd[32];
+        // queries past the sequence read lse = +inf and D = 0 (p = 0); keys
+        // past it are never stored; only the causal diagonal needs a mask
+        const int qbase = i * 64 + half * 32;
+        if (p.causal && i * 64 < kb * 128 + 127) {
 #pragma unroll
-        for (int c = 0; c < 64; c += 2) {
-          float pr[2], ds[2];
+          for (int c = 0; c < 32; ++c)
+            rs[c] = (kpos <= qbase + c) ? rs[c] : __float_as_uint(-INFINITY);
+        }
+        uint32_t pp[16], pd[16];
 #pragma unroll
-          for (int e = 0; e < 2; ++e) {
-            const int qpos = i * 64 + c + e;
-            const bool vis = row_ok && qpos < p.S && (!p.causal || kpos <= qpos);
-            pr[e] = vis ? exp2f(__uint_as_float(rs[c + e]) * p.scale_log2 - lse_v[c + e]) : 0.f;
-            ds[e] = pr[e] * (__uint_as_float(rp[c + e]) - d_v[c + e]) * p.scale;
+        for (int c = 0; c < 32; c += 4) {
+          const float4 lv = *reinterpret_cast<const float4*>(lse_v + c);
+          const float4 dv = *reinterpret_cast<const float4*>(d_v + c);
+          const float l4[4] = {lv.x, lv.y, lv.z, lv.w}, d4[4] = {dv.x, dv.y, dv.z, dv.w};
+          float pr[4], ds[4];
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            pr[e] = ex2(fmaf(__uint_as_float(rs[c + e]), p.scale_log2, -l4[e]));
+            ds[e] = pr[e] * ((__uint_as_float(rp[c + e]) - d4[e]) * p.scale);
           }
           pp[c / 2] = pack_bf16x2(pr[0], pr[1]);
+          pp[c / 2 + 1] = pack_bf16x2(pr[2], pr[3]);
           pd[c / 2] = pack_bf16x2(ds[0], ds[1]);
+          pd[c / 2 + 1] = pack_bf16x2(ds[2], ds[3]);
         }
         if (t > 0 && !W.warp(p_free, (pbase + t - 1) & 1u)) { ok = false; break; }
 #pragma unroll
-        for (int c8 = 0; c8 < 8; ++c8)
-          st_shared_v4(sw_chunk(pts, 128, row, c8), pp[4 * c8], pp[4 * c8 + 1], pp[4 * c8 + 2], pp[4 * c8 + 3]);
+        for (int c8 = 0; c8 < 4; ++c8)
+          st_shared_v4(sw_chunk(pts, 128, row, half * 4 + c8), pp[4 * c8], pp[4 * c8 + 1], pp[4 * c8 + 2],
+                       pp[4 * c8 + 3]);
         fence_async_smem();
         tc_fence_before();
         mbar_arrive(p_full);
         if (t > 0 && !W.warp(ds_free, (pbase + t - 1) & 1u)) { ok = false; break; }
 #pragma unroll
-        for (int c8 = 0; c8 < 8; ++c8)
-          st_shared_v4(sw_chunk(dss, 128, row, c8), pd[4 * c8], pd[4 * c8 + 1], pd[4 * c8 + 2], pd[4 * c8 + 3]);
+        for (int c8 = 0; c8 < 4; ++c8)
+          st_shared_v4(sw_chunk(dss, 128, row, half * 4 + c8), pd[4 * c8], pd[4 * c8 + 1], pd[4 * c8 + 2],
+                       pd[4 * c8 + 3]);
         fence_async_smem();
         tc_fence_before();
         mbar_arrive(ds_full);
@@ -965,19 +1050,19 @@ __global__ void __launch_bounds__(NT, 1) attn_dkdv_kernel(const __grid_constant_
       if (!ok) break;
       if (!W.warp(dkv_full, it & 1u)) break;
       tc_fence_after();
-      __nv_bfloat16* out = p.dqkv + (static_cast<long long>(b) * p.S + kpos) * p.dqkv_rs;
+      __nv_bfloat16* out = p.dqkv + (static_cast<long long>(b) * p.S + kpos) * p.dqkv_rs + half * 64;
       const int vcol = p.g.vcol(hk), kcol = p.g.kcol(hk);
 #pragma unroll 1
-      for (int c = 0; c < 4; ++c) {
+      for (int c = 0; c < 2; ++c) {
         uint32_t o[32];
-        tmem_ld32(tl + 256 + c * 32, o);
+        tmem_ld32(tl + 256 + half * 64 + c * 32, o);
         tmem_wait_ld();
         if (row_ok) store_row_bf16(out + vcol + c * 32, o, 1.f);
       }
 #pragma unroll 1
-      for (int c = 0; c < 4; ++c) {
+      for (int c = 0; c < 2; ++c) {
         uint32_t o[32];
-        tmem_ld32(tl + 384 + c * 32, o);
+        tmem_ld32(tl + 384 + half * 64 + c * 32, o);
         tmem_wait_ld();
         if (row_ok) store_row_bf16(out + kcol + c * 32, o, 1.f);
       }
@@ -1118,7 +1203,7 @@ int launch_attn_bwd(const AttnSpec& a, LaunchCtx& ctx) {
 
   // D = rowsum(dO * o)
   {
-    const long long total = static_cast<long long>(a.B) * a.S * a.H;
+    const long long total = static_cast<long long>(a.B) * a.H * a.s_pad;
     const int threads = 256;
     const long long blocks = (total + threads - 1) / threads;
     if (ctx.before) ctx.before(ctx.user, "attn_bwd_prep", ctx.stream);
