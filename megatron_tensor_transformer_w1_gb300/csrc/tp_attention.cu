@@ -121,6 +121,19 @@ __device__ __forceinline__ float ex2(float x) {
   return y;
 }
 
+// tcgen05.mma with the A operand in tensor memory: for kind::f16 each 32-bit
+// TMEM cell of a lane holds two consecutive K elements of that row (the
+// lower K index in the low half), so one K = 16 step spans 8 columns.
+__device__ __forceinline__ void umma_bf16_ta(uint32_t d_tmem, uint32_t a_tmem, uint64_t bdesc, uint32_t idesc,
+                                             uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(bdesc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
 // Shared-memory descriptor of a 128-byte-swizzled tile (version 1, SBO 1024).
 __device__ __forceinline__ uint64_t sw128_desc(uint32_t addr, uint32_t lbo) {
   return static_cast<uint64_t>((addr & 0x3FFFFu) >> 4) | (static_cast<uint64_t>(lbo >> 4) << 16) |
@@ -166,6 +179,19 @@ struct Waiter {
   }
 };
 
+#ifdef TPFFN_INSTRUMENT
+// Per-CTA cycle counters of the forward kernel, for performance work only
+// (not in normal builds): see tpffn_attn_debug_counters.
+__device__ unsigned long long g_attn_dbg[256][24];
+#define AT_T0(v) const long long v = clock64()
+#define AT_ADD(slot, since) atomicAdd(&g_attn_dbg[blockIdx.x & 255][slot], (unsigned long long)(clock64() - (since)))
+#define AT_CNT(slot) atomicAdd(&g_attn_dbg[blockIdx.x & 255][slot], 1ull)
+#else
+#define AT_T0(v)
+#define AT_ADD(slot, since)
+#define AT_CNT(slot)
+#endif
+
 // Query-major items, heaviest first under the causal mask: item ->
 // (128-row block, sequence, head).
 __device__ __forceinline__ void decode_item(const Params& p, int item, int heads, bool heavy_last_block, int& blk,
@@ -194,15 +220,17 @@ __device__ __forceinline__ void store_row_bf16(__nv_bfloat16* dst, const uint32_
 constexpr int F_Q = 0;
 constexpr int F_K = F_Q + TILE;       // 2 stages
 constexpr int F_V = F_K + 2 * TILE;   // 2 stages
-constexpr int F_P = F_V + 2 * TILE;   // 2 buffers of P [128 q][128 keys]
-constexpr int F_X = F_P + 2 * TILE;   // row max / sum exchange [2 halves][128 rows] fp32
+constexpr int F_X = F_V + 2 * TILE;   // row max / sum exchange [2 halves][128 rows] fp32
 constexpr int F_BAR = F_X + 1024;
 constexpr int F_SMEM = F_BAR + 256 + 1024;
 
-// P buffers and their "PV done" barriers are indexed by the running count g
-// of P blocks of the CTA (g & 1): the softmax threads may fill buffer g & 1
-// once PV g-2 has read it, so they overlap the exponentials of one block with
-// the PV product of the previous one.
+// P never leaves the chip: the softmax threads write it in bf16 over the S
+// block it came from (64 of the buffer's 128 columns, two probabilities per
+// 32-bit cell), and the PV product reads its A operand from tensor memory.
+// tcgen05 products of the CTA execute in issue order, so S_{j+2}, issued
+// after PV_j, overwrites that buffer only after PV_j has read it.  The "PV
+// done" barriers, indexed by the running count g of P blocks (g & 1), serve
+// the lazy rescale of O and the final read of O.
 __global__ void __launch_bounds__(NT, 1) attn_fwd_kernel(const __grid_constant__ CUtensorMap tq, const Params p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = align1024(smem_raw);
@@ -266,7 +294,9 @@ __global__ void __launch_bounds__(NT, 1) attn_fwd_kernel(const __grid_constant__
         int qb, b, h;
         decode_item(p, item, p.H, p.causal != 0, qb, b, h);
         const int nkb = p.causal ? qb + 1 : p.n_qb;
+        AT_T0(t16);
         if (!W(q_empty, (it & 1u) ^ 1u)) break;
+        AT_ADD(16, t16);
         mbar_arrive_expect_tx(q_full, TILE);
         const int qc = p.g.qcol(h);
         tma_load_3d(smem + F_Q, &tq, q_full, qc, qb * 128, b);
@@ -276,13 +306,17 @@ __global__ void __launch_bounds__(NT, 1) attn_fwd_kernel(const __grid_constant__
         for (int j = 0; j < nkb; ++j, ++kv) {
           const int st = kv & 1;
           const uint32_t ph = (kv >> 1) & 1u;
+          AT_T0(t17);
           if (!W(&k_empty[st], ph ^ 1u)) { ok = false; break; }
+          AT_ADD(17, t17);
           uint8_t* kd = smem + F_K + st * TILE;
           mbar_arrive_expect_tx(&k_full[st], TILE);
           tma_load_3d(kd, &tq, &k_full[st], kc, j * 128, b);
           tma_load_3d(kd + TILE / 2, &tq, &k_full[st], kc + 64, j * 128, b);
           k_last[st] = static_cast<int>(ph);
+          AT_T0(t18);
           if (!W(&v_empty[st], ph ^ 1u)) { ok = false; break; }
+          AT_ADD(18, t18);
           uint8_t* vd = smem + F_V + st * TILE;
           mbar_arrive_expect_tx(&v_full[st], TILE);
           tma_load_3d(vd, &tq, &v_full[st], vc, j * 128, b);
@@ -306,6 +340,7 @@ __global__ void __launch_bounds__(NT, 1) attn_fwd_kernel(const __grid_constant__
       const uint32_t qa = smem_u32(smem + F_Q);
       uint32_t kv = 0, sc = 0, pg = 0, it = 0;
       bool ok = true;
+      AT_T0(t_mma);
       for (int item = blockIdx.x; item < p.items && ok; item += gridDim.x, ++it) {
         int qb, b, h;
         decode_item(p, item, p.H, p.causal != 0, qb, b, h);
@@ -315,9 +350,13 @@ __global__ void __launch_bounds__(NT, 1) attn_fwd_kernel(const __grid_constant__
         auto issue_s = [&](int j) -> bool {
           const uint32_t n = kv + j;
           const int st = n & 1;
+          AT_T0(t0);
           if (!W(&k_full[st], (n >> 1) & 1u)) return false;
+          AT_ADD(0, t0);
           const uint32_t buf = (sc + j) & 1u, use = (sc + j) >> 1;
+          AT_T0(t1);
           if (!W(&s_empty[buf], (use & 1u) ^ 1u)) return false;
+          AT_ADD(1, t1);
           tc_fence_after();
           const uint32_t ka = smem_u32(smem + F_K + st * TILE);
 #pragma unroll
@@ -331,17 +370,24 @@ __global__ void __launch_bounds__(NT, 1) attn_fwd_kernel(const __grid_constant__
         if (!issue_s(0)) break;
         for (int j = 0; j < nkb; ++j) {
           if (j + 1 < nkb && !issue_s(j + 1)) { ok = false; break; }
+          AT_T0(t2);
           if (!W(p_full, pg & 1u)) { ok = false; break; }
+          AT_ADD(2, t2);
+          AT_T0(t3);
           if (j == 0 && !W(o_empty, (it & 1u) ^ 1u)) { ok = false; break; }
+          AT_ADD(3, t3);
           const uint32_t n = kv + j;
           const int st = n & 1;
+          AT_T0(t4);
           if (!W(&v_full[st], (n >> 1) & 1u)) { ok = false; break; }
+          AT_ADD(4, t4);
+          AT_CNT(6);
           tc_fence_after();
           const uint32_t va = smem_u32(smem + F_V + st * TILE);
-          const uint32_t pa = smem_u32(smem + F_P + (pg & 1u) * TILE);
+          const uint32_t pa = tmem + ((sc + j) & 1u) * 128;  // P over the S block it came from
 #pragma unroll
           for (int ks = 0; ks < 8; ++ks)
-            umma_bf16(tmem + 256, kdesc(pa, 128, ks), mndesc(va, 128, ks), ID_PV, (j > 0 || ks > 0) ? 1u : 0u);
+            umma_bf16_ta(tmem + 256, pa + ks * 8, mndesc(va, 128, ks), ID_PV, (j > 0 || ks > 0) ? 1u : 0u);
           umma_commit(&v_empty[st]);
           umma_commit(&pv_done[pg & 1u]);
           ++pg;
@@ -349,6 +395,7 @@ __global__ void __launch_bounds__(NT, 1) attn_fwd_kernel(const __grid_constant__
         kv += nkb;
         sc += nkb;
       }
+      AT_ADD(5, t_mma);
       umma_commit(drain);  // all issued MMAs complete before tensor memory is released
       W.drain(drain, 0u);
     }
@@ -374,6 +421,10 @@ __global__ void __launch_bounds__(NT, 1) attn_fwd_kernel(const __grid_constant__
       return true;
     };
     uint32_t sc = 0, pg = 0, it = 0;
+#ifdef TPFFN_INSTRUMENT
+    const bool rec = warp == 2 && lane == 0;
+    const long long t_sm = clock64();
+#endif
     for (int item = blockIdx.x; item < p.items; item += gridDim.x, ++it) {
       int qb, b, h;
       decode_item(p, item, p.H, p.causal != 0, qb, b, h);
@@ -384,7 +435,12 @@ __global__ void __launch_bounds__(NT, 1) attn_fwd_kernel(const __grid_constant__
       for (int j = 0; j < nkb; ++j) {
         const uint32_t buf = sc & 1u, use = sc >> 1;
         ++sc;
+        AT_T0(t7);
         if (!W.warp(&s_full[buf], use & 1u)) { ok = false; break; }
+#ifdef TPFFN_INSTRUMENT
+        if (rec) AT_ADD(7, t7);
+#endif
+        AT_T0(t8);
         tc_fence_after();
         uint32_t r[64];
         tmem_ld32(tl + buf * 128 + half * 64, *reinterpret_cast<uint32_t(*)[32]>(&r[0]));
@@ -392,6 +448,10 @@ __global__ void __launch_bounds__(NT, 1) attn_fwd_kernel(const __grid_constant__
         tmem_wait_ld();
         tc_fence_before();
         mbar_arrive(&s_empty[buf]);
+#ifdef TPFFN_INSTRUMENT
+        if (rec) AT_ADD(8, t8);
+#endif
+        AT_T0(t9);
         const int kbase = j * 128 + half * 64;
         // only the diagonal block (causal) and a block past the end of the
         // sequence hold invisible keys; elsewhere every key is visible
@@ -412,7 +472,14 @@ __global__ void __launch_bounds__(NT, 1) attn_fwd_kernel(const __grid_constant__
         const float mh = fmaxf(fmaxf(fmaxf(m8[0], m8[1]), fmaxf(m8[2], m8[3])),
                                fmaxf(fmaxf(m8[4], m8[5]), fmaxf(m8[6], m8[7])));
         float mo;
+#ifdef TPFFN_INSTRUMENT
+        if (rec) AT_ADD(9, t9);
+#endif
+        AT_T0(t10);
         if (!exchange(mh, mo)) { ok = false; break; }
+#ifdef TPFFN_INSTRUMENT
+        if (rec) AT_ADD(10, t10);
+#endif
         const float mx = fmaxf(mh, mo) * p.scale_log2;
         float alpha = 1.f;
         bool rescale = false;
@@ -441,28 +508,34 @@ __global__ void __launch_bounds__(NT, 1) attn_fwd_kernel(const __grid_constant__
           }
           tmem_wait_st();
         }
-        // P buffer g & 1 is free once PV g-2 has read it
-        if (!W.warp(&pv_done[g & 1u], ((g >> 1) & 1u) ^ 1u)) { ok = false; break; }
-        const uint32_t pt = smem_u32(smem + F_P + (g & 1u) * TILE);
+        // P (bf16 pairs) over columns [32 half, 32 half + 32) of this S
+        // buffer; both halves have read their S values (the exchange above)
+        AT_T0(t12);
         const float neg_m = -m_used;
         float l8[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+        uint32_t pk[32];
 #pragma unroll
-        for (int c8 = 0; c8 < 8; ++c8) {
-          float e[8];
-#pragma unroll
-          for (int q = 0; q < 8; ++q) {
-            e[q] = ex2(fmaf(__uint_as_float(r[c8 * 8 + q]), p.scale_log2, neg_m));
-            l8[q] += e[q];
-          }
-          st_shared_v4(sw_chunk(pt, 128, row, half * 8 + c8), pack_bf16x2(e[0], e[1]), pack_bf16x2(e[2], e[3]),
-                       pack_bf16x2(e[4], e[5]), pack_bf16x2(e[6], e[7]));
+        for (int c = 0; c < 32; ++c) {
+          const float e0 = ex2(fmaf(__uint_as_float(r[2 * c]), p.scale_log2, neg_m));
+          const float e1 = ex2(fmaf(__uint_as_float(r[2 * c + 1]), p.scale_log2, neg_m));
+          l8[c & 7] += e0 + e1;
+          pk[c] = pack_bf16x2(e0, e1);
         }
+        tc_fence_after();  // orders this store after the partner's S load (exchange)
+        tmem_st32(tl + buf * 128 + half * 32, pk);
+        tmem_wait_st();
         l = l * alpha + (((l8[0] + l8[1]) + (l8[2] + l8[3])) + ((l8[4] + l8[5]) + (l8[6] + l8[7])));
-        fence_async_smem();
         tc_fence_before();
         mbar_arrive(p_full);
+#ifdef TPFFN_INSTRUMENT
+        if (rec) {
+          AT_ADD(12, t12);
+          if (rescale) AT_CNT(13);
+        }
+#endif
       }
       if (!ok) break;
+      AT_T0(t14);
       const uint32_t glast = pg + nkb - 1;
       pg += nkb;
       float lo;
@@ -485,7 +558,13 @@ __global__ void __launch_bounds__(NT, 1) attn_fwd_kernel(const __grid_constant__
         p.lse[(static_cast<long long>(b) * p.H + h) * p.s_pad + qpos] = row_ok ? m_used + log2f(lsum) : INFINITY;
       tc_fence_before();
       mbar_arrive(o_empty);
+#ifdef TPFFN_INSTRUMENT
+      if (rec) AT_ADD(14, t14);
+#endif
     }
+#ifdef TPFFN_INSTRUMENT
+    if (rec) AT_ADD(15, t_sm);
+#endif
   }
 
   tc_fence_before();
@@ -1169,6 +1248,17 @@ int set_smem_once(K kern, int bytes, std::atomic<uint32_t>& done) {
 int grid_for(long long items, int sms) { return static_cast<int>(items < sms ? items : sms); }
 
 }  // namespace attn
+
+#ifdef TPFFN_INSTRUMENT
+extern "C" __attribute__((visibility("default"))) int tpffn_attn_debug_counters(unsigned long long* host, int clear) {
+  if (cudaMemcpyFromSymbol(host, attn::g_attn_dbg, sizeof(attn::g_attn_dbg)) != cudaSuccess) return 1;
+  if (clear) {
+    static unsigned long long zeros[256][24];
+    if (cudaMemcpyToSymbol(attn::g_attn_dbg, zeros, sizeof(zeros)) != cudaSuccess) return 1;
+  }
+  return 0;
+}
+#endif
 
 int launch_attn_fwd(const AttnSpec& a, LaunchCtx& ctx) {
   using namespace attn;
