@@ -301,6 +301,30 @@ class AttentionCore:
         return tuple(out)
 
 
+def _attn_core_sample(core, q, k, v, dO, u, rows, kv_rows):
+    q, k, v, dO = _f64(q), _f64(k), _f64(v), _f64(dO)
+    rows = np.asarray(rows, dtype=np.int64).reshape(-1, 3)
+    kv_rows = np.asarray(kv_rows, dtype=np.int64).reshape(-1, 3)
+    nr, nkv, hd = len(rows), len(kv_rows), core.hd
+    rb, rh, ri = (np.ascontiguousarray(rows[:, c]) for c in range(3))
+    kb, kh, kj = (np.ascontiguousarray(kv_rows[:, c]) for c in range(3))
+    out = {n: np.zeros((nr, hd)) for n in ("o", "dq", "a_o", "a_dq")}
+    out["lse"] = np.zeros(nr)
+    out.update({n: np.zeros((nkv, hd)) for n in ("dk", "dv", "a_dk", "a_dv")})
+    core.lib().orc_attn_core_sample(ctypes.byref(core._s), _ptr(q), _ptr(k), _ptr(v), _ptr(dO), ctypes.c_double(u),
+                                    ctypes.c_int64(nr), _ptr(rb), _ptr(rh), _ptr(ri), _ptr(out["o"]),
+                                    _ptr(out["lse"]), _ptr(out["dq"]), _ptr(out["a_o"]), _ptr(out["a_dq"]),
+                                    ctypes.c_int64(nkv), _ptr(kb), _ptr(kh), _ptr(kj), _ptr(out["dk"]),
+                                    _ptr(out["dv"]), _ptr(out["a_dk"]), _ptr(out["a_dv"]))
+    return out
+
+
+AttentionCore.sample = lambda self, q, k, v, dO, u, rows, kv_rows: _attn_core_sample(self, q, k, v, dO, u, rows,
+                                                                                      kv_rows)
+AttentionCore.sample.__doc__ = """Sampled rows: rows = [(b, h, i)] give o, lse, dq (+ a_o, a_dq);
+kv_rows = [(b, hk, j)] give dk, dv (+ a_dk, a_dv).  Unrounded values."""
+
+
 class Attention:
     """The head-sharded attention sublayer of one problem.
 

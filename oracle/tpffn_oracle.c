@@ -870,3 +870,126 @@ void orc_attn_intermediates(const orc_attn* A, const double* dy, double* q, doub
       dO[r * nq + col] = RND(C->round_bf16, acc);
     }
 }
+
+/* Sampled rows of the attention core with their rounding allowances (test
+ * infrastructure for full-size shapes, where the whole core is too slow).
+ * Query samples (rb, rh, ri): o row, lse (natural log) and dq row of query ri
+ * of head rh in sequence rb.  Key samples (kb, khk, kj): dk and dv rows of key
+ * kj of key/value head khk in sequence kb.  Values and allowances are those
+ * of orc_attn_core_fwd / orc_attn_core_bwd / orc_attn_core_allowance at the
+ * same positions (D_i is taken as dO_i . o_i, equal to sum_j p_ij dO_i . v_j).
+ * Row statistics are computed per (sequence, head, query) in parallel and
+ * accumulated in a fixed order, so results do not depend on the thread count. */
+typedef struct {
+  double lse, D, dD;
+} attn_rowstat;
+
+static void attn_row_stats(const orc_attn_core* C, const double* q, const double* k, const double* v,
+                           const double* dO, double u, int64_t b, int64_t h, int64_t i, double* p, double* o,
+                           double* rss_o, attn_rowstat* st) {
+  const int64_t S = C->S, hd = C->hd, nq = C->H * hd, nk = C->Hkv * hd;
+  const int64_t hk = h / (C->H / C->Hkv);
+  st->lse = attn_probs(C, q, k, b, h, i, p);
+  const double* dOi = dO + (b * S + i) * nq + h * hd;
+  double D = 0.0, dd = 0.0;
+  for (int64_t jd = 0; jd < hd; ++jd) {
+    double acc = 0.0, r2 = 0.0;
+    for (int64_t j = 0; j < S; ++j) {
+      const double t = p[j] * v[(b * S + j) * nk + hk * hd + jd];
+      acc += t;
+      r2 += t * t;
+    }
+    o[jd] = acc;
+    rss_o[jd] = sqrt(r2);
+    D += dOi[jd] * acc;
+    dd += fabs(dOi[jd]) * (fabs(acc) + sqrt(r2));
+  }
+  st->D = D;
+  st->dD = u * dd;
+}
+
+void orc_attn_core_sample(const orc_attn_core* C, const double* q, const double* k, const double* v,
+                          const double* dO, double u, int64_t nr, const int64_t* rb, const int64_t* rh,
+                          const int64_t* ri, double* o_out, double* lse_out, double* dq_out, double* a_o,
+                          double* a_dq, int64_t nkv, const int64_t* kb, const int64_t* khk, const int64_t* kj,
+                          double* dk_out, double* dv_out, double* a_dk, double* a_dv) {
+  const int64_t S = C->S, hd = C->hd, H = C->H, Hkv = C->Hkv, nq = H * hd, nk = Hkv * hd;
+  const int64_t G = H / Hkv;
+  const double scale = 1.0 / sqrt((double)hd);
+  /* query samples */
+#pragma omp parallel for schedule(dynamic, 1)
+  for (int64_t s = 0; s < nr; ++s) {
+    const int64_t b = rb[s], h = rh[s], i = ri[s], hk = h / G;
+    double* p = (double*)malloc(sizeof(double) * S);
+    double* o = o_out + s * hd;
+    double* rss = (double*)malloc(sizeof(double) * hd);
+    attn_rowstat st;
+    attn_row_stats(C, q, k, v, dO, u, b, h, i, p, o, rss, &st);
+    lse_out[s] = st.lse;
+    const double* dOi = dO + (b * S + i) * nq + h * hd;
+    double* ds = (double*)malloc(sizeof(double) * S);
+    for (int64_t j = 0; j < S; ++j)
+      ds[j] = p[j] * (dot_row(dOi, v + (b * S + j) * nk + hk * hd, hd) - st.D) * scale;
+    for (int64_t jd = 0; jd < hd; ++jd) {
+      double dq = 0.0, r2 = 0.0, pk = 0.0;
+      for (int64_t j = 0; j < S; ++j) {
+        const double kk = k[(b * S + j) * nk + hk * hd + jd];
+        dq += ds[j] * kk;
+        r2 += (u * ds[j] * kk) * (u * ds[j] * kk);
+        pk += p[j] * kk;
+      }
+      dq_out[s * hd + jd] = dq;
+      a_dq[s * hd + jd] = sqrt(r2) + st.dD * scale * fabs(pk) + u * fabs(dq);
+      a_o[s * hd + jd] = u * (rss[jd] + fabs(o[jd]));
+    }
+    free(ds);
+    free(rss);
+    free(p);
+  }
+  /* key samples: each needs p_ij, dS_ij and dD_i of every visible query i of
+   * every query head of the group */
+  for (int64_t s = 0; s < nkv; ++s) {
+    const int64_t b = kb[s], hk = khk[s], j = kj[s];
+    const int64_t i0 = C->causal ? j : 0;
+    const int64_t ni = S - i0;
+    double* pij = (double*)malloc(sizeof(double) * G * ni);
+    double* dsij = (double*)malloc(sizeof(double) * G * ni);
+    double* ddi = (double*)malloc(sizeof(double) * G * ni);
+#pragma omp parallel for schedule(dynamic, 4)
+    for (int64_t gi = 0; gi < G * ni; ++gi) {
+      const int64_t g = gi / ni, i = i0 + gi % ni, h = hk * G + g;
+      double* p = (double*)malloc(sizeof(double) * S);
+      double* o = (double*)malloc(sizeof(double) * hd);
+      double* rss = (double*)malloc(sizeof(double) * hd);
+      attn_rowstat st;
+      attn_row_stats(C, q, k, v, dO, u, b, h, i, p, o, rss, &st);
+      const double dp = dot_row(dO + (b * S + i) * nq + h * hd, v + (b * S + j) * nk + hk * hd, hd);
+      pij[gi] = p[j];
+      dsij[gi] = p[j] * (dp - st.D) * scale;
+      ddi[gi] = st.dD;
+      free(rss);
+      free(o);
+      free(p);
+    }
+    for (int64_t jd = 0; jd < hd; ++jd) {
+      double dk = 0.0, dv = 0.0, rk = 0.0, rv = 0.0;
+      for (int64_t gi = 0; gi < G * ni; ++gi) {
+        const int64_t g = gi / ni, i = i0 + gi % ni, h = hk * G + g;
+        const double qq = q[(b * S + i) * nq + h * hd + jd], gg = dO[(b * S + i) * nq + h * hd + jd];
+        dk += dsij[gi] * qq;
+        dv += pij[gi] * gg;
+        const double tk = (u * fabs(dsij[gi]) + pij[gi] * ddi[gi] * scale) * qq;
+        const double tv = u * pij[gi] * gg;
+        rk += tk * tk;
+        rv += tv * tv;
+      }
+      dk_out[s * hd + jd] = dk;
+      dv_out[s * hd + jd] = dv;
+      a_dk[s * hd + jd] = sqrt(rk) + u * fabs(dk);
+      a_dv[s * hd + jd] = sqrt(rv) + u * fabs(dv);
+    }
+    free(ddi);
+    free(dsij);
+    free(pij);
+  }
+}

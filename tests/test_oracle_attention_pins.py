@@ -318,3 +318,32 @@ def test_attn_allowance_bounds_a_bf16_computation(case):
     for name, e, r, a in zip(("o", "dq", "dk", "dv"), emul, exact, allow):
         assert np.all(np.abs(e - r) <= 1e-2 * (np.abs(r) + 1) + 3 * a), name
         assert np.sqrt(np.mean(a ** 2)) < 0.1 * np.sqrt(np.mean(r ** 2)), name
+
+
+@pytest.mark.parametrize("causal", [True, False])
+def test_attn_sampled_rows_equal_full_computation(causal):
+    """The sampled-row function (used at full sizes) returns exactly what the
+    full core, backward and allowance give at the same positions."""
+    B, S, H, Hkv, hd = 2, 21, 4, 2, 8
+    q, k, v, dO = _core_inputs(B, S, H, Hkv, hd, seed=31)
+    C = oracle.AttentionCore(B, S, H, Hkv, hd, causal=causal)
+    u = 2.0 ** -8
+    o, lse = C.forward(q, k, v)
+    dq, dk, dv = C.backward(q, k, v, dO)
+    a_o, a_dq, a_dk, a_dv = C.allowance(q, k, v, dO, u)
+    rows = [(0, 0, 0), (1, 3, 20), (0, 2, 7), (1, 1, 13)]
+    kv_rows = [(0, 0, 0), (1, 1, 20), (1, 0, 5), (0, 1, 11)]
+    smp = C.sample(q, k, v, dO, u, rows, kv_rows)
+    for s, (b, h, i) in enumerate(rows):
+        sl = (b * S + i, slice(h * hd, (h + 1) * hd))
+        np.testing.assert_allclose(smp["o"][s], o[sl], rtol=0, atol=1e-13)
+        np.testing.assert_allclose(smp["dq"][s], dq[sl], rtol=0, atol=1e-13)
+        np.testing.assert_allclose(smp["a_o"][s], a_o[sl], rtol=1e-12, atol=1e-15)
+        np.testing.assert_allclose(smp["a_dq"][s], a_dq[sl], rtol=1e-10, atol=1e-15)
+        assert abs(smp["lse"][s] - lse[b, h, i]) < 1e-13
+    for s, (b, hk, j) in enumerate(kv_rows):
+        sl = (b * S + j, slice(hk * hd, (hk + 1) * hd))
+        np.testing.assert_allclose(smp["dk"][s], dk[sl], rtol=0, atol=1e-13)
+        np.testing.assert_allclose(smp["dv"][s], dv[sl], rtol=0, atol=1e-13)
+        np.testing.assert_allclose(smp["a_dk"][s], a_dk[sl], rtol=1e-10, atol=1e-15)
+        np.testing.assert_allclose(smp["a_dv"][s], a_dv[sl], rtol=1e-10, atol=1e-15)
