@@ -112,6 +112,14 @@ __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32
       "r"(r[25]), "r"(r[26]), "r"(r[27]), "r"(r[28]), "r"(r[29]), "r"(r[30]), "r"(r[31])
       : "memory");
 }
+__device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&r)[16]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], "
+      "{%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};" ::"r"(taddr),
+      "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]),
+      "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15])
+      : "memory");
+}
 __device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
 // 2^x by the SFU instruction (ex2.approx, flush-to-zero): a few ulp, far
 // below the bf16 rounding the probabilities get next; 2^-inf = 0.
@@ -243,14 +251,17 @@ __global__ void __launch_bounds__(NT, 1) attn_fwd_kernel(const __grid_constant__
   uint64_t* v_empty = bar + 8;  // [2]
   uint64_t* s_full = bar + 10;  // [2]
   uint64_t* s_empty = bar + 12; // [2]
-  uint64_t* p_full = bar + 14;
-  uint64_t* pv_done = bar + 15; // [2]
-  uint64_t* o_empty = bar + 17;
-  uint64_t* drain = bar + 18;
-  uint64_t* pair_x = bar + 19;  // [4] both halves of a row wrote their value
-  uint64_t* pair_r = bar + 23;  // [4] both halves read their partner's value
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bar + 27);
-  volatile int* abort_flag = reinterpret_cast<volatile int*>(bar + 27) + 1;
+  // one "P written" barrier per S buffer: the softmax warps may run a block
+  // ahead of the MMA thread's wait, and a single barrier would then advance
+  // two phases before the wait sees the first
+  uint64_t* p_full = bar + 14;  // [2]
+  uint64_t* pv_done = bar + 16; // [2]
+  uint64_t* o_empty = bar + 18;
+  uint64_t* drain = bar + 19;
+  uint64_t* pair_x = bar + 20;  // [4] both halves of a row wrote their value
+  uint64_t* pair_r = bar + 24;  // [4] both halves read their partner's value
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bar + 28);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(bar + 28) + 1;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
   if (threadIdx.x == 0) {
@@ -264,8 +275,8 @@ __global__ void __launch_bounds__(NT, 1) attn_fwd_kernel(const __grid_constant__
       mbar_init(&s_full[i], 1);
       mbar_init(&s_empty[i], NSM);
       mbar_init(&pv_done[i], 1);
+      mbar_init(&p_full[i], NSM);
     }
-    mbar_init(p_full, NSM);
     mbar_init(o_empty, NSM);
     mbar_init(drain, 1);
     for (int i = 0; i < 4; ++i) {
@@ -371,7 +382,7 @@ __global__ void __launch_bounds__(NT, 1) attn_fwd_kernel(const __grid_constant__
         for (int j = 0; j < nkb; ++j) {
           if (j + 1 < nkb && !issue_s(j + 1)) { ok = false; break; }
           AT_T0(t2);
-          if (!W(p_full, pg & 1u)) { ok = false; break; }
+          if (!W(&p_full[pg & 1u], (pg >> 1) & 1u)) { ok = false; break; }
           AT_ADD(2, t2);
           AT_T0(t3);
           if (j == 0 && !W(o_empty, (it & 1u) ^ 1u)) { ok = false; break; }
@@ -526,7 +537,7 @@ __global__ void __launch_bounds__(NT, 1) attn_fwd_kernel(const __grid_constant__
         tmem_wait_st();
         l = l * alpha + (((l8[0] + l8[1]) + (l8[2] + l8[3])) + ((l8[4] + l8[5]) + (l8[6] + l8[7])));
         tc_fence_before();
-        mbar_arrive(p_full);
+        mbar_arrive(&p_full[g & 1u]);
 #ifdef TPFFN_INSTRUMENT
         if (rec) {
           AT_ADD(12, t12);
@@ -608,13 +619,26 @@ __global__ void attn_prep_kernel(const Params p) {
 }
 
 // ================================================================ dq
+// The backward kernels keep the bf16 products of the softmax warps (dS, P^T,
+// dS^T) in tensor memory: each thread writes its two-per-cell bf16 values
+// over the first half of its own fp32 columns of the block's S (or dP)
+// buffer -- no other warp reads those columns -- and the tcgen05 products
+// read them as the A operand, one K = 16 step at a time (8 columns per
+// step; the two warps of a row hold K steps {0, 1} and {2, 3}).  A stage of
+// tensor memory is refilled only by a product issued after the ones that
+// read it, and tcgen05 products execute in issue order.
+__device__ __forceinline__ uint32_t a_step(uint32_t base, int ks) {
+  return base + static_cast<uint32_t>((ks >> 1) * 32 + (ks & 1) * 8);
+}
+
 constexpr int KB = 64 * HD * 2;        // [64 rows][128 cols] bf16: two 8 KB boxes
+constexpr int DQ_ST = 3;               // S/dP stages in tensor memory (128 columns each)
+constexpr int DQ_KV = 4;               // key/value stages in shared memory
 constexpr int Q_Q = 0;
 constexpr int Q_DO = Q_Q + TILE;
-constexpr int Q_K = Q_DO + TILE;       // 3 stages
-constexpr int Q_V = Q_K + 3 * KB;      // 3 stages
-constexpr int Q_DS = Q_V + 3 * KB;     // dS [128 q][64 keys]
-constexpr int Q_BAR = Q_DS + KB;
+constexpr int Q_K = Q_DO + TILE;
+constexpr int Q_V = Q_K + DQ_KV * KB;
+constexpr int Q_BAR = Q_V + DQ_KV * KB;
 constexpr int Q_SMEM = Q_BAR + 256 + 1024;
 
 __global__ void __launch_bounds__(NT, 1) attn_dq_kernel(const __grid_constant__ CUtensorMap tq128,
@@ -625,36 +649,32 @@ __global__ void __launch_bounds__(NT, 1) attn_dq_kernel(const __grid_constant__ 
   uint64_t* bar = reinterpret_cast<uint64_t*>(smem + Q_BAR);
   uint64_t* qdo_full = bar + 0;
   uint64_t* qdo_empty = bar + 1;
-  uint64_t* k_full = bar + 2;    // [3]
-  uint64_t* k_empty = bar + 5;   // [3]
-  uint64_t* v_full = bar + 8;    // [3]
-  uint64_t* v_empty = bar + 11;  // [3]
-  uint64_t* sdp_full = bar + 14; // [2]
-  uint64_t* sdp_empty = bar + 16;// [2]
-  uint64_t* ds_full = bar + 18;
-  uint64_t* ds_free = bar + 19;
-  uint64_t* dq_full = bar + 20;
-  uint64_t* dq_empty = bar + 21;
-  uint64_t* drain = bar + 22;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bar + 23);
-  volatile int* abort_flag = reinterpret_cast<volatile int*>(bar + 23) + 1;
+  uint64_t* k_full = bar + 2;     // [DQ_KV]
+  uint64_t* k_empty = bar + 6;    // [DQ_KV]
+  uint64_t* v_full = bar + 10;    // [DQ_KV]
+  uint64_t* v_empty = bar + 14;   // [DQ_KV]
+  uint64_t* sdp_full = bar + 18;  // [DQ_ST]
+  uint64_t* ds_full = bar + 21;   // [DQ_ST] one per stage (see the forward's p_full)
+  uint64_t* dq_full = bar + 24;
+  uint64_t* dq_empty = bar + 25;
+  uint64_t* drain = bar + 26;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bar + 27);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(bar + 27) + 1;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
   if (threadIdx.x == 0) {
     mbar_init(qdo_full, 1);
     mbar_init(qdo_empty, 1);
-    for (int i = 0; i < 3; ++i) {
+    for (int i = 0; i < DQ_KV; ++i) {
       mbar_init(&k_full[i], 1);
       mbar_init(&k_empty[i], 1);
       mbar_init(&v_full[i], 1);
       mbar_init(&v_empty[i], 1);
     }
-    for (int i = 0; i < 2; ++i) {
+    for (int i = 0; i < DQ_ST; ++i) {
       mbar_init(&sdp_full[i], 1);
-      mbar_init(&sdp_empty[i], NSM);
+      mbar_init(&ds_full[i], NSM);
     }
-    mbar_init(ds_full, NSM);
-    mbar_init(ds_free, 1);
     mbar_init(dq_full, 1);
     mbar_init(dq_empty, NSM);
     mbar_init(drain, 1);
@@ -671,14 +691,15 @@ __global__ void __launch_bounds__(NT, 1) attn_dq_kernel(const __grid_constant__ 
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  const uint32_t tmem = *tmem_slot;  // S at 0/64, dP at 128/192, dQ at 256
+  const uint32_t tmem = *tmem_slot;  // stage s: S at 128 s, dP at 128 s + 64; dQ at 384
   const Waiter W{abort_flag, p.err, p.timeout_ns};
 
   auto nkb_of = [&](int qb) { return p.causal ? min(2 * qb + 2, p.n_b64) : p.n_b64; };
 
   if (warp == 0) {
     if (lane == 0) {
-      int qdo_last = -1, k_last[3] = {-1, -1, -1}, v_last[3] = {-1, -1, -1};
+      int qdo_last = -1, k_last[DQ_KV], v_last[DQ_KV];
+      for (int i = 0; i < DQ_KV; ++i) k_last[i] = v_last[i] = -1;
       uint32_t kc = 0, it = 0;
       bool ok = true;
       for (int item = blockIdx.x; item < p.items && ok; item += gridDim.x, ++it) {
@@ -695,8 +716,8 @@ __global__ void __launch_bounds__(NT, 1) attn_dq_kernel(const __grid_constant__ 
         qdo_last = static_cast<int>(it & 1u);
         const int hk = h / p.G, kcol = p.g.kcol(hk), vcol = p.g.vcol(hk);
         for (int j = 0; j < nkb; ++j, ++kc) {
-          const int st = kc % 3;
-          const uint32_t ph = (kc / 3) & 1u;
+          const int st = kc % DQ_KV;
+          const uint32_t ph = (kc / DQ_KV) & 1u;
           if (!W(&k_empty[st], ph ^ 1u)) { ok = false; break; }
           uint8_t* kd = smem + Q_K + st * KB;
           mbar_arrive_expect_tx(&k_full[st], KB);
@@ -712,18 +733,18 @@ __global__ void __launch_bounds__(NT, 1) attn_dq_kernel(const __grid_constant__ 
         }
       }
       if (qdo_last >= 0) W.drain(qdo_full, static_cast<uint32_t>(qdo_last));
-      for (int s = 0; s < 3; ++s) {
-        if (k_last[s] >= 0) W.drain(&k_full[s], static_cast<uint32_t>(k_last[s]));
-        if (v_last[s] >= 0) W.drain(&v_full[s], static_cast<uint32_t>(v_last[s]));
+      for (int s2 = 0; s2 < DQ_KV; ++s2) {
+        if (k_last[s2] >= 0) W.drain(&k_full[s2], static_cast<uint32_t>(k_last[s2]));
+        if (v_last[s2] >= 0) W.drain(&v_full[s2], static_cast<uint32_t>(v_last[s2]));
       }
     }
     __syncwarp();
   } else if (warp == 1) {
     if (lane == 0) {
       constexpr uint32_t ID_S = idesc(64, 0, 0);    // S = Q K^T, dP = dO V^T
-      constexpr uint32_t ID_DQ = idesc(128, 0, 1);  // dQ += dS K (K: N = hd contiguous)
-      const uint32_t qa = smem_u32(smem + Q_Q), da = smem_u32(smem + Q_DO), dsa = smem_u32(smem + Q_DS);
-      uint32_t kc = 0, sc = 0, dsc = 0, it = 0;
+      constexpr uint32_t ID_DQ = idesc(128, 0, 1);  // dQ += dS K (dS in TMEM, K: N = hd contiguous)
+      const uint32_t qa = smem_u32(smem + Q_Q), da = smem_u32(smem + Q_DO);
+      uint32_t kc = 0, sc = 0, it = 0;
       bool ok = true;
       for (int item = blockIdx.x; item < p.items && ok; item += gridDim.x, ++it) {
         int qb, b, h;
@@ -733,38 +754,37 @@ __global__ void __launch_bounds__(NT, 1) attn_dq_kernel(const __grid_constant__ 
         tc_fence_after();
         auto issue_sdp = [&](int j) -> bool {
           const uint32_t n = kc + j;
-          const int st = n % 3;
-          const uint32_t ph = (n / 3) & 1u;
+          const int st = n % DQ_KV;
+          const uint32_t ph = (n / DQ_KV) & 1u;
           if (!W(&k_full[st], ph) || !W(&v_full[st], ph)) return false;
-          const uint32_t buf = (sc + j) & 1u, use = (sc + j) >> 1;
-          if (!W(&sdp_empty[buf], (use & 1u) ^ 1u)) return false;
           tc_fence_after();
+          const uint32_t sbase = tmem + ((sc + j) % DQ_ST) * 128;
           const uint32_t ka = smem_u32(smem + Q_K + st * KB), va = smem_u32(smem + Q_V + st * KB);
 #pragma unroll
           for (int ks = 0; ks < 8; ++ks)
-            umma_bf16(tmem + buf * 64, kdesc(qa, 128, ks), kdesc(ka, 64, ks), ID_S, ks > 0 ? 1u : 0u);
+            umma_bf16(sbase, kdesc(qa, 128, ks), kdesc(ka, 64, ks), ID_S, ks > 0 ? 1u : 0u);
 #pragma unroll
           for (int ks = 0; ks < 8; ++ks)
-            umma_bf16(tmem + 128 + buf * 64, kdesc(da, 128, ks), kdesc(va, 64, ks), ID_S, ks > 0 ? 1u : 0u);
-          umma_commit(&sdp_full[buf]);
+            umma_bf16(sbase + 64, kdesc(da, 128, ks), kdesc(va, 64, ks), ID_S, ks > 0 ? 1u : 0u);
+          umma_commit(&sdp_full[(sc + j) % DQ_ST]);
           umma_commit(&v_empty[st]);
           if (j == nkb - 1) umma_commit(qdo_empty);
           return true;
         };
-        if (!issue_sdp(0)) break;
-        for (int j = 0; j < nkb; ++j) {
-          if (j + 1 < nkb && !issue_sdp(j + 1)) { ok = false; break; }
-          if (!W(ds_full, dsc & 1u)) { ok = false; break; }
+        for (int j = 0; j < nkb && j < DQ_ST && ok; ++j) ok = issue_sdp(j);
+        for (int j = 0; j < nkb && ok; ++j) {
+          const uint32_t gs = sc + j;
+          if (!W(&ds_full[gs % DQ_ST], (gs / DQ_ST) & 1u)) { ok = false; break; }
           if (j == 0 && !W(dq_empty, (it & 1u) ^ 1u)) { ok = false; break; }
           tc_fence_after();
-          const int st = (kc + j) % 3;
+          const int st = (kc + j) % DQ_KV;
+          const uint32_t sbase = tmem + ((sc + j) % DQ_ST) * 128;
           const uint32_t ka = smem_u32(smem + Q_K + st * KB);
 #pragma unroll
           for (int ks = 0; ks < 4; ++ks)
-            umma_bf16(tmem + 256, kdesc(dsa, 128, ks), mndesc(ka, 64, ks), ID_DQ, (j > 0 || ks > 0) ? 1u : 0u);
+            umma_bf16_ta(tmem + 384, a_step(sbase, ks), mndesc(ka, 64, ks), ID_DQ, (j > 0 || ks > 0) ? 1u : 0u);
           umma_commit(&k_empty[st]);
-          umma_commit(ds_free);
-          ++dsc;
+          if (j + DQ_ST < nkb && !issue_sdp(j + DQ_ST)) { ok = false; break; }
         }
         if (!ok) break;
         umma_commit(dq_full);
@@ -781,8 +801,7 @@ __global__ void __launch_bounds__(NT, 1) attn_dq_kernel(const __grid_constant__ 
     const int quarter = warp & 3, half = (warp - 2) >> 2;
     const int row = quarter * 32 + lane;
     const uint32_t tl = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
-    const uint32_t dst = smem_u32(smem + Q_DS);
-    uint32_t sc = 0, dsbase = 0, it = 0;
+    uint32_t sc = 0, it = 0;
     for (int item = blockIdx.x; item < p.items; item += gridDim.x, ++it) {
       int qb, b, h;
       decode_item(p, item, p.H, p.causal != 0, qb, b, h);
@@ -795,16 +814,14 @@ __global__ void __launch_bounds__(NT, 1) attn_dq_kernel(const __grid_constant__ 
       const float ds_off = p.Dv[vrow] * p.scale;
       bool ok = true;
       for (int j = 0; j < nkb; ++j) {
-        const uint32_t buf = sc & 1u, use = sc >> 1;
-        ++sc;
-        if (!W.warp(&sdp_full[buf], use & 1u)) { ok = false; break; }
+        const uint32_t g = sc + j, stage = g % DQ_ST, use = g / DQ_ST;
+        if (!W.warp(&sdp_full[stage], use & 1u)) { ok = false; break; }
         tc_fence_after();
+        const uint32_t sb = tl + stage * 128 + half * 32;
         uint32_t rs[32], rp[32];
-        tmem_ld32(tl + buf * 64 + half * 32, rs);
-        tmem_ld32(tl + 128 + buf * 64 + half * 32, rp);
+        tmem_ld32(sb, rs);
+        tmem_ld32(sb + 64, rp);
         tmem_wait_ld();
-        tc_fence_before();
-        mbar_arrive(&sdp_empty[buf]);
         // keys past the sequence need no mask here: their K rows are zero
         // filled, so they add nothing to dQ; only the causal diagonal does
         const int kbase = j * 64 + half * 32;
@@ -824,14 +841,10 @@ __global__ void __launch_bounds__(NT, 1) attn_dq_kernel(const __grid_constant__ 
           }
           pk[c / 2] = pack_bf16x2(ds[0], ds[1]);
         }
-        if (j > 0 && !W.warp(ds_free, (dsbase + j - 1) & 1u)) { ok = false; break; }
-#pragma unroll
-        for (int c8 = 0; c8 < 4; ++c8)
-          st_shared_v4(sw_chunk(dst, 128, row, half * 4 + c8), pk[4 * c8], pk[4 * c8 + 1], pk[4 * c8 + 2],
-                       pk[4 * c8 + 3]);
-        fence_async_smem();
+        tmem_st16(sb, pk);  // dS over this thread's own S columns
+        tmem_wait_st();
         tc_fence_before();
-        mbar_arrive(ds_full);
+        mbar_arrive(&ds_full[stage]);
       }
       if (!ok) break;
       if (!W.warp(dq_full, it & 1u)) break;
@@ -841,13 +854,13 @@ __global__ void __launch_bounds__(NT, 1) attn_dq_kernel(const __grid_constant__ 
 #pragma unroll 1
       for (int c = 0; c < 2; ++c) {
         uint32_t o[32];
-        tmem_ld32(tl + 256 + half * 64 + c * 32, o);
+        tmem_ld32(tl + 384 + half * 64 + c * 32, o);
         tmem_wait_ld();
         if (row_ok) store_row_bf16(out + c * 32, o, 1.f);
       }
       tc_fence_before();
       mbar_arrive(dq_empty);
-      dsbase += nkb;
+      sc += nkb;
     }
   }
 
@@ -864,9 +877,7 @@ constexpr int V_K = 0;
 constexpr int V_V = V_K + TILE;
 constexpr int V_Q = V_V + TILE;        // 3 stages of [64 q][128]
 constexpr int V_DO = V_Q + 3 * KB;     // 3 stages
-constexpr int V_PT = V_DO + 3 * KB;     // P^T [128 keys][64 q]
-constexpr int V_DST = V_PT + 16384;     // dS^T [128 keys][64 q]
-constexpr int V_VEC = V_DST + 16384;   // 3 stages x (64 lse + 64 D) floats
+constexpr int V_VEC = V_DO + 3 * KB;   // 3 stages x (64 lse + 64 D) floats
 constexpr int V_BAR = V_VEC + 3 * 512;
 constexpr int V_SMEM = V_BAR + 256 + 1024;
 
@@ -883,16 +894,12 @@ __global__ void __launch_bounds__(NT, 1) attn_dkdv_kernel(const __grid_constant_
   uint64_t* do_full = bar + 8;    // [3]
   uint64_t* do_empty = bar + 11;  // [3]
   uint64_t* sdp_full = bar + 14;  // [2]
-  uint64_t* sdp_empty = bar + 16; // [2]
-  uint64_t* p_full = bar + 18;
-  uint64_t* p_free = bar + 19;
-  uint64_t* ds_full = bar + 20;
-  uint64_t* ds_free = bar + 21;
-  uint64_t* dkv_full = bar + 22;
-  uint64_t* dkv_empty = bar + 23;
-  uint64_t* drain = bar + 24;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bar + 25);
-  volatile int* abort_flag = reinterpret_cast<volatile int*>(bar + 25) + 1;
+  uint64_t* pd_full = bar + 16;   // [2] one per stage (see the forward's p_full)
+  uint64_t* dkv_full = bar + 18;
+  uint64_t* dkv_empty = bar + 19;
+  uint64_t* drain = bar + 20;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bar + 21);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(bar + 21) + 1;
   float* vec = reinterpret_cast<float*>(smem + V_VEC);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
@@ -907,12 +914,8 @@ __global__ void __launch_bounds__(NT, 1) attn_dkdv_kernel(const __grid_constant_
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&sdp_full[i], 1);
-      mbar_init(&sdp_empty[i], NSM);
+      mbar_init(&pd_full[i], NSM);
     }
-    mbar_init(p_full, NSM);
-    mbar_init(p_free, 1);
-    mbar_init(ds_full, NSM);
-    mbar_init(ds_free, 1);
     mbar_init(dkv_full, 1);
     mbar_init(dkv_empty, NSM);
     mbar_init(drain, 1);
@@ -929,7 +932,7 @@ __global__ void __launch_bounds__(NT, 1) attn_dkdv_kernel(const __grid_constant_
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  const uint32_t tmem = *tmem_slot;  // S^T at 0/64, dP^T at 128/192, dV at 256, dK at 384
+  const uint32_t tmem = *tmem_slot;  // stage s: S^T at 128 s, dP^T at 128 s + 64; dV at 256, dK at 384
   const Waiter W{abort_flag, p.err, p.timeout_ns};
 
   // causal: key block kb sees the 64-query blocks from 2 kb on
@@ -978,19 +981,18 @@ __global__ void __launch_bounds__(NT, 1) attn_dkdv_kernel(const __grid_constant_
         }
       }
       if (kv_last >= 0) W.drain(kv_full, static_cast<uint32_t>(kv_last));
-      for (int s = 0; s < 3; ++s) {
-        if (q_last[s] >= 0) W.drain(&q_full[s], static_cast<uint32_t>(q_last[s]));
-        if (do_last[s] >= 0) W.drain(&do_full[s], static_cast<uint32_t>(do_last[s]));
+      for (int s2 = 0; s2 < 3; ++s2) {
+        if (q_last[s2] >= 0) W.drain(&q_full[s2], static_cast<uint32_t>(q_last[s2]));
+        if (do_last[s2] >= 0) W.drain(&do_full[s2], static_cast<uint32_t>(do_last[s2]));
       }
     }
     __syncwarp();
   } else if (warp == 1) {
     if (lane == 0) {
       constexpr uint32_t ID_S = idesc(64, 0, 0);    // S^T = K Q^T, dP^T = V dO^T
-      constexpr uint32_t ID_G = idesc(128, 0, 1);   // dV += P^T dO, dK += dS^T Q
+      constexpr uint32_t ID_G = idesc(128, 0, 1);   // dV += P^T dO, dK += dS^T Q (A in TMEM)
       const uint32_t ka = smem_u32(smem + V_K), va = smem_u32(smem + V_V);
-      const uint32_t pta = smem_u32(smem + V_PT), dsa = smem_u32(smem + V_DST);
-      uint32_t qc = 0, sc = 0, pc = 0, it = 0;
+      uint32_t qc = 0, sc = 0, it = 0;
       bool ok = true;
       for (int item = blockIdx.x; item < p.items && ok; item += gridDim.x, ++it) {
         int kb, b, hk;
@@ -1004,40 +1006,37 @@ __global__ void __launch_bounds__(NT, 1) attn_dkdv_kernel(const __grid_constant_
           const int st = n % 3;
           const uint32_t ph = (n / 3) & 1u;
           if (!W(&q_full[st], ph) || !W(&do_full[st], ph)) return false;
-          const uint32_t buf = (sc + t) & 1u, use = (sc + t) >> 1;
-          if (!W(&sdp_empty[buf], (use & 1u) ^ 1u)) return false;
           tc_fence_after();
+          const uint32_t sbase = tmem + ((sc + t) & 1u) * 128;
           const uint32_t qa = smem_u32(smem + V_Q + st * KB), da = smem_u32(smem + V_DO + st * KB);
 #pragma unroll
           for (int ks = 0; ks < 8; ++ks)
-            umma_bf16(tmem + buf * 64, kdesc(ka, 128, ks), kdesc(qa, 64, ks), ID_S, ks > 0 ? 1u : 0u);
+            umma_bf16(sbase, kdesc(ka, 128, ks), kdesc(qa, 64, ks), ID_S, ks > 0 ? 1u : 0u);
 #pragma unroll
           for (int ks = 0; ks < 8; ++ks)
-            umma_bf16(tmem + 128 + buf * 64, kdesc(va, 128, ks), kdesc(da, 64, ks), ID_S, ks > 0 ? 1u : 0u);
-          umma_commit(&sdp_full[buf]);
+            umma_bf16(sbase + 64, kdesc(va, 128, ks), kdesc(da, 64, ks), ID_S, ks > 0 ? 1u : 0u);
+          umma_commit(&sdp_full[(sc + t) & 1u]);
           return true;
         };
         if (n_it > 0 && !issue_sdp(0)) break;
         for (int t = 0; t < n_it; ++t) {
           if (t + 1 < n_it && !issue_sdp(t + 1)) { ok = false; break; }
-          const int st = (qc + t) % 3;
-          if (!W(p_full, pc & 1u)) { ok = false; break; }
+          const uint32_t gs = sc + t;
+          if (!W(&pd_full[gs & 1u], (gs >> 1) & 1u)) { ok = false; break; }
           if (t == 0 && !W(dkv_empty, (it & 1u) ^ 1u)) { ok = false; break; }
           tc_fence_after();
+          const int st = (qc + t) % 3;
+          const uint32_t sbase = tmem + ((sc + t) & 1u) * 128;
           const uint32_t qa = smem_u32(smem + V_Q + st * KB), da = smem_u32(smem + V_DO + st * KB);
 #pragma unroll
           for (int ks = 0; ks < 4; ++ks)
-            umma_bf16(tmem + 256, kdesc(pta, 128, ks), mndesc(da, 64, ks), ID_G, (t > 0 || ks > 0) ? 1u : 0u);
+            umma_bf16_ta(tmem + 256, a_step(sbase, ks), mndesc(da, 64, ks), ID_G, (t > 0 || ks > 0) ? 1u : 0u);
           umma_commit(&do_empty[st]);
-          umma_commit(p_free);
-          if (!W(ds_full, pc & 1u)) { ok = false; break; }
-          tc_fence_after();
 #pragma unroll
           for (int ks = 0; ks < 4; ++ks)
-            umma_bf16(tmem + 384, kdesc(dsa, 128, ks), mndesc(qa, 64, ks), ID_G, (t > 0 || ks > 0) ? 1u : 0u);
+            umma_bf16_ta(tmem + 384, a_step(sbase + 64, ks), mndesc(qa, 64, ks), ID_G,
+                         (t > 0 || ks > 0) ? 1u : 0u);
           umma_commit(&q_empty[st]);
-          umma_commit(ds_free);
-          ++pc;
         }
         if (!ok) break;
         umma_commit(dkv_full);
@@ -1056,8 +1055,7 @@ __global__ void __launch_bounds__(NT, 1) attn_dkdv_kernel(const __grid_constant_
     const int quarter = warp & 3, half = (warp - 2) >> 2;
     const int row = quarter * 32 + lane;
     const uint32_t tl = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
-    const uint32_t pts = smem_u32(smem + V_PT), dss = smem_u32(smem + V_DST);
-    uint32_t qc = 0, sc = 0, pbase = 0, it = 0;
+    uint32_t qc = 0, sc = 0, it = 0;
     for (int item = blockIdx.x; item < p.items; item += gridDim.x, ++it) {
       int kb, b, hk;
       decode_item(p, item, p.Hkv, false, kb, b, hk);
@@ -1071,19 +1069,17 @@ __global__ void __launch_bounds__(NT, 1) attn_dkdv_kernel(const __grid_constant_
         const uint32_t n = qc + t;
         const int st = n % 3;
         const uint32_t ph = (n / 3) & 1u;
-        const uint32_t buf = sc & 1u, use = sc >> 1;
-        ++sc;
-        if (!W.warp(&sdp_full[buf], use & 1u)) { ok = false; break; }
+        const uint32_t g = sc + t, stage = g & 1u, use = g >> 1;
+        if (!W.warp(&sdp_full[stage], use & 1u)) { ok = false; break; }
         tc_fence_after();
+        const uint32_t sb = tl + stage * 128 + half * 32;
         uint32_t rs[32], rp[32];
-        tmem_ld32(tl + buf * 64 + half * 32, rs);
-        tmem_ld32(tl + 128 + buf * 64 + half * 32, rp);
+        tmem_ld32(sb, rs);
+        tmem_ld32(sb + 64, rp);
         tmem_wait_ld();
-        tc_fence_before();
-        mbar_arrive(&sdp_empty[buf]);
         if (!W.warp(&q_full[st], ph)) { ok = false; break; }  // lse / D of this block landed
         const float* lse_v = vec + st * 128 + half * 32;
-        const float* d_v = lse_v + 64;
+        const float* d_v = vec + st * 128 + 64 + half * 32;
         // queries past the sequence read lse = +inf and D = 0 (p = 0); keys
         // past it are never stored; only the causal diagonal needs a mask
         const int qbase = i * 64 + half * 32;
@@ -1109,22 +1105,11 @@ __global__ void __launch_bounds__(NT, 1) attn_dkdv_kernel(const __grid_constant_
           pd[c / 2] = pack_bf16x2(ds[0], ds[1]);
           pd[c / 2 + 1] = pack_bf16x2(ds[2], ds[3]);
         }
-        if (t > 0 && !W.warp(p_free, (pbase + t - 1) & 1u)) { ok = false; break; }
-#pragma unroll
-        for (int c8 = 0; c8 < 4; ++c8)
-          st_shared_v4(sw_chunk(pts, 128, row, half * 4 + c8), pp[4 * c8], pp[4 * c8 + 1], pp[4 * c8 + 2],
-                       pp[4 * c8 + 3]);
-        fence_async_smem();
+        tmem_st16(sb, pp);       // P^T over this thread's own S^T columns
+        tmem_st16(sb + 64, pd);  // dS^T over its own dP^T columns
+        tmem_wait_st();
         tc_fence_before();
-        mbar_arrive(p_full);
-        if (t > 0 && !W.warp(ds_free, (pbase + t - 1) & 1u)) { ok = false; break; }
-#pragma unroll
-        for (int c8 = 0; c8 < 4; ++c8)
-          st_shared_v4(sw_chunk(dss, 128, row, half * 4 + c8), pd[4 * c8], pd[4 * c8 + 1], pd[4 * c8 + 2],
-                       pd[4 * c8 + 3]);
-        fence_async_smem();
-        tc_fence_before();
-        mbar_arrive(ds_full);
+        mbar_arrive(&pd_full[stage]);
       }
       if (!ok) break;
       if (!W.warp(dkv_full, it & 1u)) break;
@@ -1148,7 +1133,7 @@ __global__ void __launch_bounds__(NT, 1) attn_dkdv_kernel(const __grid_constant_
       tc_fence_before();
       mbar_arrive(dkv_empty);
       qc += n_it;
-      pbase += n_it;
+      sc += n_it;
     }
   }
 
