@@ -191,13 +191,19 @@ struct Waiter {
 // Per-CTA cycle counters of the forward kernel, for performance work only
 // (not in normal builds): see tpffn_attn_debug_counters.
 __device__ unsigned long long g_attn_dbg[256][24];
+__device__ unsigned long long g_attn_bwd_dbg[2][256][16];  // [dq, dk/dv][CTA][counter]
 #define AT_T0(v) const long long v = clock64()
 #define AT_ADD(slot, since) atomicAdd(&g_attn_dbg[blockIdx.x & 255][slot], (unsigned long long)(clock64() - (since)))
 #define AT_CNT(slot) atomicAdd(&g_attn_dbg[blockIdx.x & 255][slot], 1ull)
+#define BW_ADD(k, slot, since) \
+  atomicAdd(&g_attn_bwd_dbg[k][blockIdx.x & 255][slot], (unsigned long long)(clock64() - (since)))
+#define BW_CNT(k, slot) atomicAdd(&g_attn_bwd_dbg[k][blockIdx.x & 255][slot], 1ull)
 #else
 #define AT_T0(v)
 #define AT_ADD(slot, since)
 #define AT_CNT(slot)
+#define BW_ADD(k, slot, since)
+#define BW_CNT(k, slot)
 #endif
 
 // Query-major items, heaviest first under the causal mask: item ->
@@ -746,6 +752,7 @@ __global__ void __launch_bounds__(NT, 1) attn_dq_kernel(const __grid_constant__ 
       const uint32_t qa = smem_u32(smem + Q_Q), da = smem_u32(smem + Q_DO);
       uint32_t kc = 0, sc = 0, it = 0;
       bool ok = true;
+      AT_T0(t_mma);
       for (int item = blockIdx.x; item < p.items && ok; item += gridDim.x, ++it) {
         int qb, b, h;
         decode_item(p, item, p.H, p.causal != 0, qb, b, h);
@@ -756,7 +763,10 @@ __global__ void __launch_bounds__(NT, 1) attn_dq_kernel(const __grid_constant__ 
           const uint32_t n = kc + j;
           const int st = n % DQ_KV;
           const uint32_t ph = (n / DQ_KV) & 1u;
+          AT_T0(t0);
           if (!W(&k_full[st], ph) || !W(&v_full[st], ph)) return false;
+          BW_ADD(0, 0, t0);
+          AT_T0(t1);
           tc_fence_after();
           const uint32_t sbase = tmem + ((sc + j) % DQ_ST) * 128;
           const uint32_t ka = smem_u32(smem + Q_K + st * KB), va = smem_u32(smem + Q_V + st * KB);
@@ -769,13 +779,20 @@ __global__ void __launch_bounds__(NT, 1) attn_dq_kernel(const __grid_constant__ 
           umma_commit(&sdp_full[(sc + j) % DQ_ST]);
           umma_commit(&v_empty[st]);
           if (j == nkb - 1) umma_commit(qdo_empty);
+          BW_ADD(0, 1, t1);
           return true;
         };
         for (int j = 0; j < nkb && j < DQ_ST && ok; ++j) ok = issue_sdp(j);
         for (int j = 0; j < nkb && ok; ++j) {
           const uint32_t gs = sc + j;
+          AT_T0(t2);
           if (!W(&ds_full[gs % DQ_ST], (gs / DQ_ST) & 1u)) { ok = false; break; }
+          BW_ADD(0, 2, t2);
+          AT_T0(t3);
           if (j == 0 && !W(dq_empty, (it & 1u) ^ 1u)) { ok = false; break; }
+          BW_ADD(0, 3, t3);
+          BW_CNT(0, 4);
+          AT_T0(t5);
           tc_fence_after();
           const int st = (kc + j) % DQ_KV;
           const uint32_t sbase = tmem + ((sc + j) % DQ_ST) * 128;
@@ -784,6 +801,7 @@ __global__ void __launch_bounds__(NT, 1) attn_dq_kernel(const __grid_constant__ 
           for (int ks = 0; ks < 4; ++ks)
             umma_bf16_ta(tmem + 384, a_step(sbase, ks), mndesc(ka, 64, ks), ID_DQ, (j > 0 || ks > 0) ? 1u : 0u);
           umma_commit(&k_empty[st]);
+          BW_ADD(0, 5, t5);
           if (j + DQ_ST < nkb && !issue_sdp(j + DQ_ST)) { ok = false; break; }
         }
         if (!ok) break;
@@ -791,6 +809,7 @@ __global__ void __launch_bounds__(NT, 1) attn_dq_kernel(const __grid_constant__ 
         kc += nkb;
         sc += nkb;
       }
+      BW_ADD(0, 6, t_mma);
       umma_commit(drain);
       W.drain(drain, 0u);
     }
@@ -815,7 +834,12 @@ __global__ void __launch_bounds__(NT, 1) attn_dq_kernel(const __grid_constant__ 
       bool ok = true;
       for (int j = 0; j < nkb; ++j) {
         const uint32_t g = sc + j, stage = g % DQ_ST, use = g / DQ_ST;
+        AT_T0(t7);
         if (!W.warp(&sdp_full[stage], use & 1u)) { ok = false; break; }
+#ifdef TPFFN_INSTRUMENT
+        if (warp == 2 && lane == 0) BW_ADD(0, 7, t7);
+#endif
+        AT_T0(t8);
         tc_fence_after();
         const uint32_t sb = tl + stage * 128 + half * 32;
         uint32_t rs[32], rp[32];
@@ -845,6 +869,9 @@ __global__ void __launch_bounds__(NT, 1) attn_dq_kernel(const __grid_constant__ 
         tmem_wait_st();
         tc_fence_before();
         mbar_arrive(&ds_full[stage]);
+#ifdef TPFFN_INSTRUMENT
+        if (warp == 2 && lane == 0) BW_ADD(0, 8, t8);
+#endif
       }
       if (!ok) break;
       if (!W.warp(dq_full, it & 1u)) break;
@@ -994,6 +1021,7 @@ __global__ void __launch_bounds__(NT, 1) attn_dkdv_kernel(const __grid_constant_
       const uint32_t ka = smem_u32(smem + V_K), va = smem_u32(smem + V_V);
       uint32_t qc = 0, sc = 0, it = 0;
       bool ok = true;
+      AT_T0(t_mma);
       for (int item = blockIdx.x; item < p.items && ok; item += gridDim.x, ++it) {
         int kb, b, hk;
         decode_item(p, item, p.Hkv, false, kb, b, hk);
@@ -1005,7 +1033,10 @@ __global__ void __launch_bounds__(NT, 1) attn_dkdv_kernel(const __grid_constant_
           const uint32_t n = qc + t;
           const int st = n % 3;
           const uint32_t ph = (n / 3) & 1u;
+          AT_T0(t0);
           if (!W(&q_full[st], ph) || !W(&do_full[st], ph)) return false;
+          BW_ADD(1, 0, t0);
+          AT_T0(t1);
           tc_fence_after();
           const uint32_t sbase = tmem + ((sc + t) & 1u) * 128;
           const uint32_t qa = smem_u32(smem + V_Q + st * KB), da = smem_u32(smem + V_DO + st * KB);
@@ -1016,14 +1047,21 @@ __global__ void __launch_bounds__(NT, 1) attn_dkdv_kernel(const __grid_constant_
           for (int ks = 0; ks < 8; ++ks)
             umma_bf16(sbase + 64, kdesc(va, 128, ks), kdesc(da, 64, ks), ID_S, ks > 0 ? 1u : 0u);
           umma_commit(&sdp_full[(sc + t) & 1u]);
+          BW_ADD(1, 1, t1);
           return true;
         };
         if (n_it > 0 && !issue_sdp(0)) break;
         for (int t = 0; t < n_it; ++t) {
           if (t + 1 < n_it && !issue_sdp(t + 1)) { ok = false; break; }
           const uint32_t gs = sc + t;
+          AT_T0(t2);
           if (!W(&pd_full[gs & 1u], (gs >> 1) & 1u)) { ok = false; break; }
+          BW_ADD(1, 2, t2);
+          AT_T0(t3);
           if (t == 0 && !W(dkv_empty, (it & 1u) ^ 1u)) { ok = false; break; }
+          BW_ADD(1, 3, t3);
+          BW_CNT(1, 4);
+          AT_T0(t5);
           tc_fence_after();
           const int st = (qc + t) % 3;
           const uint32_t sbase = tmem + ((sc + t) & 1u) * 128;
@@ -1037,6 +1075,7 @@ __global__ void __launch_bounds__(NT, 1) attn_dkdv_kernel(const __grid_constant_
             umma_bf16_ta(tmem + 384, a_step(sbase + 64, ks), mndesc(qa, 64, ks), ID_G,
                          (t > 0 || ks > 0) ? 1u : 0u);
           umma_commit(&q_empty[st]);
+          BW_ADD(1, 5, t5);
         }
         if (!ok) break;
         umma_commit(dkv_full);
@@ -1044,6 +1083,7 @@ __global__ void __launch_bounds__(NT, 1) attn_dkdv_kernel(const __grid_constant_
         qc += n_it;
         sc += n_it;
       }
+      BW_ADD(1, 6, t_mma);
       umma_commit(drain);
       W.drain(drain, 0u);
     }
@@ -1070,7 +1110,12 @@ __global__ void __launch_bounds__(NT, 1) attn_dkdv_kernel(const __grid_constant_
         const int st = n % 3;
         const uint32_t ph = (n / 3) & 1u;
         const uint32_t g = sc + t, stage = g & 1u, use = g >> 1;
+        AT_T0(t7);
         if (!W.warp(&sdp_full[stage], use & 1u)) { ok = false; break; }
+#ifdef TPFFN_INSTRUMENT
+        if (warp == 2 && lane == 0) BW_ADD(1, 7, t7);
+#endif
+        AT_T0(t8);
         tc_fence_after();
         const uint32_t sb = tl + stage * 128 + half * 32;
         uint32_t rs[32], rp[32];
@@ -1110,6 +1155,9 @@ __global__ void __launch_bounds__(NT, 1) attn_dkdv_kernel(const __grid_constant_
         tmem_wait_st();
         tc_fence_before();
         mbar_arrive(&pd_full[stage]);
+#ifdef TPFFN_INSTRUMENT
+        if (warp == 2 && lane == 0) BW_ADD(1, 8, t8);
+#endif
       }
       if (!ok) break;
       if (!W.warp(dkv_full, it & 1u)) break;
@@ -1235,6 +1283,15 @@ int grid_for(long long items, int sms) { return static_cast<int>(items < sms ? i
 }  // namespace attn
 
 #ifdef TPFFN_INSTRUMENT
+extern "C" __attribute__((visibility("default"))) int tpffn_attn_bwd_debug_counters(unsigned long long* host,
+                                                                                   int clear) {
+  if (cudaMemcpyFromSymbol(host, attn::g_attn_bwd_dbg, sizeof(attn::g_attn_bwd_dbg)) != cudaSuccess) return 1;
+  if (clear) {
+    static unsigned long long zeros[2][256][16];
+    if (cudaMemcpyToSymbol(attn::g_attn_bwd_dbg, zeros, sizeof(zeros)) != cudaSuccess) return 1;
+  }
+  return 0;
+}
 extern "C" __attribute__((visibility("default"))) int tpffn_attn_debug_counters(unsigned long long* host, int clear) {
   if (cudaMemcpyFromSymbol(host, attn::g_attn_dbg, sizeof(attn::g_attn_dbg)) != cudaSuccess) return 1;
   if (clear) {
