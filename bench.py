@@ -610,6 +610,34 @@ def run_attention(dev, steps, peaks, sum_mode="fused"):
     return out
 
 
+def profile_attention(args):
+    """A plain loop of attention-sublayer steps for profiler captures: no
+    timing, no extras; --attn-batch shrinks the sequence count."""
+    import torch
+    from synth import ATTN_WORKLOADS
+    from megatron_tensor_transformer_w1_gb300.attention import TensorParallelAttention
+    w = ATTN_WORKLOADS[args.profile_attention]
+    if args.attn_batch:
+        w = w.replace(B=args.attn_batch)
+    dev = torch.device("cuda", 0)
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(20260000 + w.seed_index)
+
+    def draw(shape, std):
+        return (torch.randn(*shape, generator=gen, device=dev) * std).to(torch.bfloat16)
+
+    nq, nk = w.H * w.hd, w.Hkv * w.hd
+    attn = TensorParallelAttention(w.d, w.H, w.Hkv, w.hd, w.T_p, causal=w.causal, device=dev)
+    wqkv, wo = attn.pack(draw((nq, w.d), w.d ** -0.5), draw((nk, w.d), w.d ** -0.5), draw((nk, w.d), w.d ** -0.5),
+                         draw((w.d, nq), nq ** -0.5))
+    x, dy = draw((w.N, w.d), 1.0), draw((w.N, w.d), 1.0)
+    for _ in range(args.warmup + args.steps):
+        y, saved = attn.forward(x, w.B, w.S, wqkv, wo, fused=args.sum == "fused")
+        attn.backward(x, w.B, w.S, wqkv, wo, saved, dy, fused=args.sum == "fused")
+    torch.cuda.synchronize(dev)
+    return {"profile_attention": w.name, "B": w.B, "S": w.S, "steps": args.steps, "warmup": args.warmup}
+
+
 def run_decode(args, ctx, dev, peaks):
     import torch
     from synth import WORKLOADS
@@ -751,6 +779,9 @@ def main():
     ap.add_argument("--no-extras", action="store_true", help="skip the per-workload table and standalone-sum line")
     ap.add_argument("--cpu-budget", type=float, default=15.0)
     ap.add_argument("--tokens", type=int, default=0, help="override the token count (profiler captures)")
+    ap.add_argument("--profile-attention", default="", metavar="WORKLOAD",
+                    help="only run --steps fwd+bwd steps of this attention workload (profiler captures)")
+    ap.add_argument("--attn-batch", type=int, default=0, help="override the attention workload's sequence count")
     args = ap.parse_args()
     ctx = dist_setup(args.gpus)
     if args.impl == "reference":
@@ -764,6 +795,9 @@ def main():
         ctx["dist"].init_process_group("nccl", device_id=torch.device("cuda", ctx["local"]))
     import importlib
     importlib.import_module("__graft_entry__").build()
+    if args.profile_attention:
+        print(json.dumps(profile_attention(args)), flush=True)
+        return 0
     line = run_ours(args, ctx)
     if ctx["rank"] == 0:
         print(json.dumps(line), flush=True)

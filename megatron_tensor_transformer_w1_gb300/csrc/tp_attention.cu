@@ -80,7 +80,8 @@ struct Params {
   long long s_pad;
   float* Dv;
   __nv_bfloat16* dqkv;
-  long long dqkv_rs;
+  long long dqkv_rs;      // row stride of qkv and dqkv
+  const __nv_bfloat16* dqkv_src;  // the packed q/k/v (read by the dq kernel's Q copy)
   float scale_log2;  // log2(e) / sqrt(hd)
   float scale;       // 1 / sqrt(hd)
   int* err;
@@ -638,49 +639,66 @@ __device__ __forceinline__ uint32_t a_step(uint32_t base, int ks) {
 }
 
 constexpr int KB = 64 * HD * 2;        // [64 rows][128 cols] bf16: two 8 KB boxes
-constexpr int DQ_ST = 3;               // S/dP stages in tensor memory (128 columns each)
-constexpr int DQ_KV = 4;               // key/value stages in shared memory
-constexpr int Q_Q = 0;
-constexpr int Q_DO = Q_Q + TILE;
-constexpr int Q_K = Q_DO + TILE;
-constexpr int Q_V = Q_K + DQ_KV * KB;
-constexpr int Q_BAR = Q_V + DQ_KV * KB;
+constexpr int DQ_KV = 3;               // key/value stages of 128 keys in shared memory
+constexpr int Q_K = 0;
+constexpr int Q_V = Q_K + DQ_KV * TILE;
+constexpr int Q_DS = Q_V + DQ_KV * TILE;  // dS [128 q][128 keys] bf16, K-major
+constexpr int Q_BAR = Q_DS + TILE;
 constexpr int Q_SMEM = Q_BAR + 256 + 1024;
+constexpr uint32_t DQ_S = 0, DQ_DP = 128, DQ_ACC = 256, DQ_QA = 384, DQ_DOA = 448;  // TMEM columns
 
-__global__ void __launch_bounds__(NT, 1) attn_dq_kernel(const __grid_constant__ CUtensorMap tq128,
-                                                        const __grid_constant__ CUtensorMap tq64,
-                                                        const __grid_constant__ CUtensorMap tdo128, const Params p) {
+// Blocks of 128 keys: S = Q K^T and dP = dO V^T are N = 128 products (an
+// N = 64 tcgen05.mma costs as many cycles as ~90 % of an N = 128 one), with
+// Q and dO, fixed for the item, as A operands in tensor memory (bf16 pairs,
+// 64 columns each; the softmax warps copy them in at the start of each item,
+// after the previous item's last S/dP has completed).  S and dP are freed as
+// soon as the softmax warps have read them, so the next block's products run
+// while they compute dS; dS goes to shared memory for dQ += dS K.
+__device__ __forceinline__ void load_row_pairs(const __nv_bfloat16* src, bool ok, uint32_t (&r)[32]) {
+#pragma unroll
+  for (int c = 0; c < 8; ++c) {
+    uint4 v = ok ? *reinterpret_cast<const uint4*>(src + c * 8) : make_uint4(0u, 0u, 0u, 0u);
+    r[4 * c] = v.x;
+    r[4 * c + 1] = v.y;
+    r[4 * c + 2] = v.z;
+    r[4 * c + 3] = v.w;
+  }
+}
+
+__global__ void __launch_bounds__(NT, 1) attn_dq_kernel(const __grid_constant__ CUtensorMap tq128, const Params p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = align1024(smem_raw);
   uint64_t* bar = reinterpret_cast<uint64_t*>(smem + Q_BAR);
-  uint64_t* qdo_full = bar + 0;
-  uint64_t* qdo_empty = bar + 1;
+  uint64_t* qdo_ready = bar + 0;  // softmax warps wrote Q and dO of the item into TMEM
+  uint64_t* qdo_free = bar + 1;   // the item's last S/dP has completed
   uint64_t* k_full = bar + 2;     // [DQ_KV]
-  uint64_t* k_empty = bar + 6;    // [DQ_KV]
-  uint64_t* v_full = bar + 10;    // [DQ_KV]
-  uint64_t* v_empty = bar + 14;   // [DQ_KV]
-  uint64_t* sdp_full = bar + 18;  // [DQ_ST]
-  uint64_t* ds_full = bar + 21;   // [DQ_ST] one per stage (see the forward's p_full)
-  uint64_t* dq_full = bar + 24;
-  uint64_t* dq_empty = bar + 25;
-  uint64_t* drain = bar + 26;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bar + 27);
-  volatile int* abort_flag = reinterpret_cast<volatile int*>(bar + 27) + 1;
+  uint64_t* k_empty = bar + 5;    // [DQ_KV]
+  uint64_t* v_full = bar + 8;     // [DQ_KV]
+  uint64_t* v_empty = bar + 11;   // [DQ_KV]
+  uint64_t* sdp_full = bar + 14;
+  uint64_t* sdp_empty = bar + 15;
+  uint64_t* ds_full = bar + 16;
+  uint64_t* ds_free = bar + 17;
+  uint64_t* dq_full = bar + 18;
+  uint64_t* dq_empty = bar + 19;
+  uint64_t* drain = bar + 20;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bar + 21);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(bar + 21) + 1;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
   if (threadIdx.x == 0) {
-    mbar_init(qdo_full, 1);
-    mbar_init(qdo_empty, 1);
+    mbar_init(qdo_ready, NSM);
+    mbar_init(qdo_free, 1);
     for (int i = 0; i < DQ_KV; ++i) {
       mbar_init(&k_full[i], 1);
       mbar_init(&k_empty[i], 1);
       mbar_init(&v_full[i], 1);
       mbar_init(&v_empty[i], 1);
     }
-    for (int i = 0; i < DQ_ST; ++i) {
-      mbar_init(&sdp_full[i], 1);
-      mbar_init(&ds_full[i], NSM);
-    }
+    mbar_init(sdp_full, 1);
+    mbar_init(sdp_empty, NSM);
+    mbar_init(ds_full, NSM);
+    mbar_init(ds_free, 1);
     mbar_init(dq_full, 1);
     mbar_init(dq_empty, NSM);
     mbar_init(drain, 1);
@@ -688,57 +706,44 @@ __global__ void __launch_bounds__(NT, 1) attn_dq_kernel(const __grid_constant__ 
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
   }
-  if (warp == 0 && lane == 0) {
-    prefetch_tmap(&tq128);
-    prefetch_tmap(&tq64);
-    prefetch_tmap(&tdo128);
-  }
+  if (warp == 0 && lane == 0) prefetch_tmap(&tq128);
   if (warp == 1) tmem_alloc(tmem_slot, 512);
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  const uint32_t tmem = *tmem_slot;  // stage s: S at 128 s, dP at 128 s + 64; dQ at 384
+  const uint32_t tmem = *tmem_slot;
   const Waiter W{abort_flag, p.err, p.timeout_ns};
 
-  auto nkb_of = [&](int qb) { return p.causal ? min(2 * qb + 2, p.n_b64) : p.n_b64; };
+  auto nkb_of = [&](int qb) { return p.causal ? qb + 1 : p.n_qb; };
 
   if (warp == 0) {
     if (lane == 0) {
-      int qdo_last = -1, k_last[DQ_KV], v_last[DQ_KV];
+      int k_last[DQ_KV], v_last[DQ_KV];
       for (int i = 0; i < DQ_KV; ++i) k_last[i] = v_last[i] = -1;
-      uint32_t kc = 0, it = 0;
+      uint32_t kc = 0;
       bool ok = true;
-      for (int item = blockIdx.x; item < p.items && ok; item += gridDim.x, ++it) {
+      for (int item = blockIdx.x; item < p.items && ok; item += gridDim.x) {
         int qb, b, h;
         decode_item(p, item, p.H, p.causal != 0, qb, b, h);
         const int nkb = nkb_of(qb);
-        if (!W(qdo_empty, (it & 1u) ^ 1u)) break;
-        mbar_arrive_expect_tx(qdo_full, 2 * TILE);
-        const int qc = p.g.qcol(h);
-        tma_load_3d(smem + Q_Q, &tq128, qdo_full, qc, qb * 128, b);
-        tma_load_3d(smem + Q_Q + TILE / 2, &tq128, qdo_full, qc + 64, qb * 128, b);
-        tma_load_3d(smem + Q_DO, &tdo128, qdo_full, h * HD, qb * 128, b);
-        tma_load_3d(smem + Q_DO + TILE / 2, &tdo128, qdo_full, h * HD + 64, qb * 128, b);
-        qdo_last = static_cast<int>(it & 1u);
         const int hk = h / p.G, kcol = p.g.kcol(hk), vcol = p.g.vcol(hk);
         for (int j = 0; j < nkb; ++j, ++kc) {
           const int st = kc % DQ_KV;
           const uint32_t ph = (kc / DQ_KV) & 1u;
           if (!W(&k_empty[st], ph ^ 1u)) { ok = false; break; }
-          uint8_t* kd = smem + Q_K + st * KB;
-          mbar_arrive_expect_tx(&k_full[st], KB);
-          tma_load_3d(kd, &tq64, &k_full[st], kcol, j * 64, b);
-          tma_load_3d(kd + KB / 2, &tq64, &k_full[st], kcol + 64, j * 64, b);
+          uint8_t* kd = smem + Q_K + st * TILE;
+          mbar_arrive_expect_tx(&k_full[st], TILE);
+          tma_load_3d(kd, &tq128, &k_full[st], kcol, j * 128, b);
+          tma_load_3d(kd + TILE / 2, &tq128, &k_full[st], kcol + 64, j * 128, b);
           k_last[st] = static_cast<int>(ph);
           if (!W(&v_empty[st], ph ^ 1u)) { ok = false; break; }
-          uint8_t* vd = smem + Q_V + st * KB;
-          mbar_arrive_expect_tx(&v_full[st], KB);
-          tma_load_3d(vd, &tq64, &v_full[st], vcol, j * 64, b);
-          tma_load_3d(vd + KB / 2, &tq64, &v_full[st], vcol + 64, j * 64, b);
+          uint8_t* vd = smem + Q_V + st * TILE;
+          mbar_arrive_expect_tx(&v_full[st], TILE);
+          tma_load_3d(vd, &tq128, &v_full[st], vcol, j * 128, b);
+          tma_load_3d(vd + TILE / 2, &tq128, &v_full[st], vcol + 64, j * 128, b);
           v_last[st] = static_cast<int>(ph);
         }
       }
-      if (qdo_last >= 0) W.drain(qdo_full, static_cast<uint32_t>(qdo_last));
       for (int s2 = 0; s2 < DQ_KV; ++s2) {
         if (k_last[s2] >= 0) W.drain(&k_full[s2], static_cast<uint32_t>(k_last[s2]));
         if (v_last[s2] >= 0) W.drain(&v_full[s2], static_cast<uint32_t>(v_last[s2]));
@@ -747,17 +752,17 @@ __global__ void __launch_bounds__(NT, 1) attn_dq_kernel(const __grid_constant__ 
     __syncwarp();
   } else if (warp == 1) {
     if (lane == 0) {
-      constexpr uint32_t ID_S = idesc(64, 0, 0);    // S = Q K^T, dP = dO V^T
-      constexpr uint32_t ID_DQ = idesc(128, 0, 1);  // dQ += dS K (dS in TMEM, K: N = hd contiguous)
-      const uint32_t qa = smem_u32(smem + Q_Q), da = smem_u32(smem + Q_DO);
-      uint32_t kc = 0, sc = 0, it = 0;
+      constexpr uint32_t ID_S = idesc(128, 0, 0);   // S = Q K^T, dP = dO V^T (A in TMEM)
+      constexpr uint32_t ID_DQ = idesc(128, 0, 1);  // dQ += dS K (K: N = hd contiguous)
+      const uint32_t dsa = smem_u32(smem + Q_DS);
+      uint32_t kc = 0, it = 0, blk = 0;
       bool ok = true;
       AT_T0(t_mma);
       for (int item = blockIdx.x; item < p.items && ok; item += gridDim.x, ++it) {
         int qb, b, h;
         decode_item(p, item, p.H, p.causal != 0, qb, b, h);
         const int nkb = nkb_of(qb);
-        if (!W(qdo_full, it & 1u)) break;
+        if (!W(qdo_ready, it & 1u)) break;
         tc_fence_after();
         auto issue_sdp = [&](int j) -> bool {
           const uint32_t n = kc + j;
@@ -765,28 +770,30 @@ __global__ void __launch_bounds__(NT, 1) attn_dq_kernel(const __grid_constant__ 
           const uint32_t ph = (n / DQ_KV) & 1u;
           AT_T0(t0);
           if (!W(&k_full[st], ph) || !W(&v_full[st], ph)) return false;
+          // S/dP buffer free once the softmax warps have read the previous block
+          if (blk > 0 && !W(sdp_empty, (blk - 1) & 1u)) return false;
           BW_ADD(0, 0, t0);
           AT_T0(t1);
           tc_fence_after();
-          const uint32_t sbase = tmem + ((sc + j) % DQ_ST) * 128;
-          const uint32_t ka = smem_u32(smem + Q_K + st * KB), va = smem_u32(smem + Q_V + st * KB);
+          const uint32_t ka = smem_u32(smem + Q_K + st * TILE), va = smem_u32(smem + Q_V + st * TILE);
 #pragma unroll
           for (int ks = 0; ks < 8; ++ks)
-            umma_bf16(sbase, kdesc(qa, 128, ks), kdesc(ka, 64, ks), ID_S, ks > 0 ? 1u : 0u);
+            umma_bf16_ta(tmem + DQ_S, tmem + DQ_QA + ks * 8, kdesc(ka, 128, ks), ID_S, ks > 0 ? 1u : 0u);
 #pragma unroll
           for (int ks = 0; ks < 8; ++ks)
-            umma_bf16(sbase + 64, kdesc(da, 128, ks), kdesc(va, 64, ks), ID_S, ks > 0 ? 1u : 0u);
-          umma_commit(&sdp_full[(sc + j) % DQ_ST]);
+            umma_bf16_ta(tmem + DQ_DP, tmem + DQ_DOA + ks * 8, kdesc(va, 128, ks), ID_S, ks > 0 ? 1u : 0u);
+          umma_commit(sdp_full);
           umma_commit(&v_empty[st]);
-          if (j == nkb - 1) umma_commit(qdo_empty);
+          if (j == nkb - 1) umma_commit(qdo_free);  // Q, dO of the item no longer read
+          ++blk;
           BW_ADD(0, 1, t1);
           return true;
         };
-        for (int j = 0; j < nkb && j < DQ_ST && ok; ++j) ok = issue_sdp(j);
+        if (!issue_sdp(0)) break;
         for (int j = 0; j < nkb && ok; ++j) {
-          const uint32_t gs = sc + j;
+          if (j + 1 < nkb && !issue_sdp(j + 1)) { ok = false; break; }
           AT_T0(t2);
-          if (!W(&ds_full[gs % DQ_ST], (gs / DQ_ST) & 1u)) { ok = false; break; }
+          if (!W(ds_full, (blk - (j + 1 < nkb ? 2 : 1)) & 1u)) { ok = false; break; }
           BW_ADD(0, 2, t2);
           AT_T0(t3);
           if (j == 0 && !W(dq_empty, (it & 1u) ^ 1u)) { ok = false; break; }
@@ -795,19 +802,17 @@ __global__ void __launch_bounds__(NT, 1) attn_dq_kernel(const __grid_constant__ 
           AT_T0(t5);
           tc_fence_after();
           const int st = (kc + j) % DQ_KV;
-          const uint32_t sbase = tmem + ((sc + j) % DQ_ST) * 128;
-          const uint32_t ka = smem_u32(smem + Q_K + st * KB);
+          const uint32_t ka = smem_u32(smem + Q_K + st * TILE);
 #pragma unroll
-          for (int ks = 0; ks < 4; ++ks)
-            umma_bf16_ta(tmem + 384, a_step(sbase, ks), mndesc(ka, 64, ks), ID_DQ, (j > 0 || ks > 0) ? 1u : 0u);
+          for (int ks = 0; ks < 8; ++ks)
+            umma_bf16(tmem + DQ_ACC, kdesc(dsa, 128, ks), mndesc(ka, 128, ks), ID_DQ, (j > 0 || ks > 0) ? 1u : 0u);
           umma_commit(&k_empty[st]);
+          umma_commit(ds_free);
           BW_ADD(0, 5, t5);
-          if (j + DQ_ST < nkb && !issue_sdp(j + DQ_ST)) { ok = false; break; }
         }
         if (!ok) break;
         umma_commit(dq_full);
         kc += nkb;
-        sc += nkb;
       }
       BW_ADD(0, 6, t_mma);
       umma_commit(drain);
@@ -815,12 +820,13 @@ __global__ void __launch_bounds__(NT, 1) attn_dq_kernel(const __grid_constant__ 
     }
     __syncwarp();
   } else {
-    // warp w: TMEM lanes 32 (w % 4) .., columns [32 half, 32 half + 32) of
-    // the 64-key S and dP blocks and [64 half, 64 half + 64) of dQ
+    // warp w: TMEM lanes 32 (w % 4) .., columns [64 half, 64 half + 64) of
+    // the 128-key S and dP blocks and of dQ, and half of the row's Q and dO
     const int quarter = warp & 3, half = (warp - 2) >> 2;
     const int row = quarter * 32 + lane;
     const uint32_t tl = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
-    uint32_t sc = 0, it = 0;
+    const uint32_t dst = smem_u32(smem + Q_DS);
+    uint32_t it = 0, blk = 0;
     for (int item = blockIdx.x; item < p.items; item += gridDim.x, ++it) {
       int qb, b, h;
       decode_item(p, item, p.H, p.causal != 0, qb, b, h);
@@ -831,44 +837,68 @@ __global__ void __launch_bounds__(NT, 1) attn_dq_kernel(const __grid_constant__ 
       // rows past the sequence read lse = +inf (written by the forward): p = 0
       const float lse_r = p.lse[vrow];
       const float ds_off = p.Dv[vrow] * p.scale;
+      // Q and dO of this row into tensor memory, once the previous item's
+      // products no longer read them
+      if (!W.warp(qdo_free, (it & 1u) ^ 1u)) break;
+      tc_fence_after();
+      {
+        const long long tok = static_cast<long long>(b) * p.S + qpos;
+        uint32_t r[32];
+        load_row_pairs(p.dqkv_src + tok * p.dqkv_rs + p.g.qcol(h) + half * 64, row_ok, r);
+        tmem_st32(tl + DQ_QA + half * 32, r);
+        load_row_pairs(p.dO + tok * p.do_rs + h * HD + half * 64, row_ok, r);
+        tmem_st32(tl + DQ_DOA + half * 32, r);
+        tmem_wait_st();
+      }
+      tc_fence_before();
+      mbar_arrive(qdo_ready);
       bool ok = true;
-      for (int j = 0; j < nkb; ++j) {
-        const uint32_t g = sc + j, stage = g % DQ_ST, use = g / DQ_ST;
+      for (int j = 0; j < nkb; ++j, ++blk) {
         AT_T0(t7);
-        if (!W.warp(&sdp_full[stage], use & 1u)) { ok = false; break; }
+        if (!W.warp(sdp_full, blk & 1u)) { ok = false; break; }
 #ifdef TPFFN_INSTRUMENT
         if (warp == 2 && lane == 0) BW_ADD(0, 7, t7);
 #endif
         AT_T0(t8);
         tc_fence_after();
-        const uint32_t sb = tl + stage * 128 + half * 32;
-        uint32_t rs[32], rp[32];
-        tmem_ld32(sb, rs);
-        tmem_ld32(sb + 64, rp);
-        tmem_wait_ld();
         // keys past the sequence need no mask here: their K rows are zero
         // filled, so they add nothing to dQ; only the causal diagonal does
-        const int kbase = j * 64 + half * 32;
-        if (p.causal && j * 64 + 63 > qb * 128) {
+        const bool diag = p.causal && j == qb;
+        uint32_t pk[32];
 #pragma unroll
-          for (int c = 0; c < 32; ++c)
-            rs[c] = (kbase + c <= qpos) ? rs[c] : __float_as_uint(-INFINITY);
-        }
-        uint32_t pk[16];
+        for (int c2 = 0; c2 < 2; ++c2) {
+          uint32_t rs[32], rp[32];
+          tmem_ld32(tl + DQ_S + half * 64 + c2 * 32, rs);
+          tmem_ld32(tl + DQ_DP + half * 64 + c2 * 32, rp);
+          tmem_wait_ld();
+          const int kbase = j * 128 + half * 64 + c2 * 32;
+          if (diag) {
 #pragma unroll
-        for (int c = 0; c < 32; c += 2) {
-          float ds[2];
-#pragma unroll
-          for (int e = 0; e < 2; ++e) {
-            const float pr = ex2(fmaf(__uint_as_float(rs[c + e]), p.scale_log2, -lse_r));
-            ds[e] = pr * fmaf(__uint_as_float(rp[c + e]), p.scale, -ds_off);
+            for (int c = 0; c < 32; ++c)
+              rs[c] = (kbase + c <= qpos) ? rs[c] : __float_as_uint(-INFINITY);
           }
-          pk[c / 2] = pack_bf16x2(ds[0], ds[1]);
+#pragma unroll
+          for (int c = 0; c < 32; c += 2) {
+            float ds[2];
+#pragma unroll
+            for (int e = 0; e < 2; ++e) {
+              const float pr = ex2(fmaf(__uint_as_float(rs[c + e]), p.scale_log2, -lse_r));
+              ds[e] = pr * fmaf(__uint_as_float(rp[c + e]), p.scale, -ds_off);
+            }
+            pk[c2 * 16 + c / 2] = pack_bf16x2(ds[0], ds[1]);
+          }
         }
-        tmem_st16(sb, pk);  // dS over this thread's own S columns
-        tmem_wait_st();
         tc_fence_before();
-        mbar_arrive(&ds_full[stage]);
+        mbar_arrive(sdp_empty);  // S and dP read: the next block's products may start
+        // dS buffer free once the previous block's dQ has read it
+        if (blk > 0 && !W.warp(ds_free, (blk - 1) & 1u)) { ok = false; break; }
+#pragma unroll
+        for (int c8 = 0; c8 < 8; ++c8)
+          st_shared_v4(sw_chunk(dst, 128, row, half * 8 + c8), pk[4 * c8], pk[4 * c8 + 1], pk[4 * c8 + 2],
+                       pk[4 * c8 + 3]);
+        fence_async_smem();
+        tc_fence_before();
+        mbar_arrive(ds_full);
 #ifdef TPFFN_INSTRUMENT
         if (warp == 2 && lane == 0) BW_ADD(0, 8, t8);
 #endif
@@ -881,13 +911,12 @@ __global__ void __launch_bounds__(NT, 1) attn_dq_kernel(const __grid_constant__ 
 #pragma unroll 1
       for (int c = 0; c < 2; ++c) {
         uint32_t o[32];
-        tmem_ld32(tl + 384 + half * 64 + c * 32, o);
+        tmem_ld32(tl + DQ_ACC + half * 64 + c * 32, o);
         tmem_wait_ld();
         if (row_ok) store_row_bf16(out + c * 32, o, 1.f);
       }
       tc_fence_before();
       mbar_arrive(dq_empty);
-      sc += nkb;
     }
   }
 
@@ -1214,6 +1243,12 @@ __global__ void pack_qkv_kernel(const __nv_bfloat16* Wq, const __nv_bfloat16* Wk
   }
 }
 
+// barrier areas (mbarriers + TMEM slot + abort flag) fit their reserved bytes
+static_assert(F_SMEM - F_BAR - 1024 >= 28 * 8 + 8, "forward barrier area");
+static_assert(Q_SMEM - Q_BAR - 1024 >= 21 * 8 + 8, "dq barrier area");
+static_assert(V_SMEM - V_BAR - 1024 >= 21 * 8 + 8, "dk/dv barrier area");
+static_assert(F_SMEM <= 232448 && Q_SMEM <= 232448 && V_SMEM <= 232448, "shared memory per CTA");
+
 // ================================================================ host
 Params make_params(const AttnSpec& a, const LaunchCtx& ctx) {
   Params p{};
@@ -1239,6 +1274,7 @@ Params make_params(const AttnSpec& a, const LaunchCtx& ctx) {
   p.Dv = a.Dv;
   p.dqkv = static_cast<__nv_bfloat16*>(a.dqkv);
   p.dqkv_rs = a.qkv_rs;
+  p.dqkv_src = static_cast<const __nv_bfloat16*>(a.qkv);
   p.scale = static_cast<float>(1.0 / std::sqrt(static_cast<double>(HD)));
   p.scale_log2 = static_cast<float>(1.4426950408889634 / std::sqrt(static_cast<double>(HD)));
   p.err = ctx.err;
@@ -1326,10 +1362,9 @@ int launch_attn_bwd(const AttnSpec& a, LaunchCtx& ctx) {
   if (rc) return rc;
   if (!a.qkv || !a.o || !a.lse || !a.dO || !a.Dv || !a.dqkv) return TP_ERR_INVALID;
   if (a.do_rs < static_cast<int64_t>(a.H) * HD || a.do_rs % 8) return TP_ERR_INVALID;
-  CUtensorMap tq128, tq64, tdo128, tdo64;
+  CUtensorMap tq128, tq64, tdo64;
   if ((rc = map_rows(&tq128, a.qkv, a.qkv_rs, a.S, a.B, 128))) return rc;
   if ((rc = map_rows(&tq64, a.qkv, a.qkv_rs, a.S, a.B, 64))) return rc;
-  if ((rc = map_rows(&tdo128, a.dO, a.do_rs, a.S, a.B, 128))) return rc;
   if ((rc = map_rows(&tdo64, a.dO, a.do_rs, a.S, a.B, 64))) return rc;
   Params p = make_params(a, ctx);
 
@@ -1348,7 +1383,7 @@ int launch_attn_bwd(const AttnSpec& a, LaunchCtx& ctx) {
     static std::atomic<uint32_t> done{0};
     if ((rc = set_smem_once(attn_dq_kernel, Q_SMEM, done))) return rc;
     if (ctx.before) ctx.before(ctx.user, "attn_bwd_dq", ctx.stream);
-    attn_dq_kernel<<<grid_for(p.items, ctx.num_sms), NT, Q_SMEM, ctx.stream>>>(tq128, tq64, tdo128, p);
+    attn_dq_kernel<<<grid_for(p.items, ctx.num_sms), NT, Q_SMEM, ctx.stream>>>(tq128, p);
     if (ctx.after) ctx.after(ctx.user, ctx.stream);
     ctx.launches++;
   }
