@@ -43,12 +43,12 @@ DECODE = "llama3_70b_decode_swiglu_bf16"
 # profiles/llama3_8b_swiglu_gemm_dram_traffic.md.  To be cleared when the
 # kernels change.
 NCU_TRAFFIC = {
-    "up_swiglu": 1.17e9 + 679.34e6,
-    "down_fused_sum": 1.05e9 + 59.80e6,
-    "dgrad_h_swiglu": 1.48e9 + 447.41e6,
-    "dgrad_x_fused_sum": 2.10e9 + 60.07e6,
-    "wgrad_w2": 1.19e9 + 108.54e6,
-    "wgrad_w13": 2.22e9 + 224.73e6,
+    "up_swiglu": 1.29e9 + 679.03e6,
+    "down_fused_sum": 1.05e9 + 59.91e6,
+    "dgrad_h_swiglu": 1.52e9 + 447.99e6,
+    "dgrad_x_fused_sum": 2.41e9 + 60.22e6,
+    "wgrad_w2": 1.18e9 + 107.72e6,
+    "wgrad_w13": 2.23e9 + 225.02e6,
 }
 
 

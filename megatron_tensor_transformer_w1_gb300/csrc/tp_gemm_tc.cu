@@ -63,7 +63,7 @@ struct Params {
   int NB, G;
   int tiles_m, tiles_n, k_blocks;
   int a_bsel, a_gsel, b_bsel, b_gsel;
-  int a_swap, b_swap;
+  int a_swap, b_swap;  // 0: {inner, rows, batch}; 1: {inner, batch, rows}; 2: 4-D MN-major groups
   void* out;
   long long out_bs, out_rs;
   void* out2;
@@ -336,18 +336,24 @@ __global__ void __launch_bounds__(threads_for<EPI>(), 1)
             if (!AMN) {
               tma_load_3d(sA, &tmA, &full[stage], k0, p.a_swap ? ab : m0, p.a_swap ? m0 : ab);
             } else {
+              if (p.a_swap == 2)
+                tma_load_4d(sA, &tmA, &full[stage], 0, k0, m0 / 64, ab);
+              else
 #pragma unroll
-              for (int i = 0; i < BM / 64; ++i)
-                tma_load_3d(sA + i * 8192, &tmA, &full[stage], m0 + 64 * i, p.a_swap ? ab : k0,
-                            p.a_swap ? k0 : ab);
+                for (int i = 0; i < BM / 64; ++i)
+                  tma_load_3d(sA + i * 8192, &tmA, &full[stage], m0 + 64 * i, p.a_swap ? ab : k0,
+                              p.a_swap ? k0 : ab);
             }
             if (!BMN) {
               tma_load_3d(sB, &tmB, &full[stage], k0, p.b_swap ? bb : n0, p.b_swap ? n0 : bb);
             } else {
+              if (p.b_swap == 2)
+                tma_load_4d(sB, &tmB, &full[stage], 0, k0, n0 / 64, bb);
+              else
 #pragma unroll
-              for (int i = 0; i < BN / 64; ++i)
-                tma_load_3d(sB + i * 8192, &tmB, &full[stage], n0 + 64 * i, p.b_swap ? bb : k0,
-                            p.b_swap ? k0 : bb);
+                for (int i = 0; i < BN / 64; ++i)
+                  tma_load_3d(sB + i * 8192, &tmB, &full[stage], n0 + 64 * i, p.b_swap ? bb : k0,
+                              p.b_swap ? k0 : bb);
             }
             last_issue_phase[stage] = static_cast<int>(phase);
           }
@@ -464,6 +470,14 @@ __device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_addr) {
 }
 __device__ __forceinline__ void cluster_sync() {
   asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tma_load_4d_pair(void* dst, const CUtensorMap* tm, uint32_t leader_bar, int c0,
+                                                 int c1, int c2, int c3) {
+  asm volatile(
+      "cp.async.bulk.tensor.4d.cta_group::2.shared::cluster.global.tile.mbarrier::complete_tx::bytes "
+      "[%0], [%1, {%2, %3, %4, %5}], [%6];" ::"r"(smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(tm)), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(leader_bar)
+      : "memory");
 }
 __device__ __forceinline__ void tma_load_3d_pair(void* dst, const CUtensorMap* tm, uint32_t leader_bar, int c0,
                                                  int c1, int c2) {
@@ -642,18 +656,26 @@ __global__ void __launch_bounds__(threads_for<EPI>(), 1)
             if (!AMN) {
               tma_load_3d_pair(sA, &tmA, leader_full, k0, p.a_swap ? ab : m0, p.a_swap ? m0 : ab);
             } else {
+              if (p.a_swap == 2) {
+                tma_load_4d_pair(sA, &tmA, leader_full, 0, k0, m0 / 64, ab);
+              } else {
 #pragma unroll
-              for (int i = 0; i < 2; ++i)
-                tma_load_3d_pair(sA + i * 8192, &tmA, leader_full, m0 + 64 * i, p.a_swap ? ab : k0,
-                                 p.a_swap ? k0 : ab);
+                for (int i = 0; i < 2; ++i)
+                  tma_load_3d_pair(sA + i * 8192, &tmA, leader_full, m0 + 64 * i, p.a_swap ? ab : k0,
+                                   p.a_swap ? k0 : ab);
+              }
             }
             if (!BMN) {
               tma_load_3d_pair(sB, &tmB, leader_full, k0, p.b_swap ? bb : n0, p.b_swap ? n0 : bb);
             } else {
+              if (p.b_swap == 2) {
+                tma_load_4d_pair(sB, &tmB, leader_full, 0, k0, n0 / 64, bb);
+              } else {
 #pragma unroll
-              for (int i = 0; i < 2; ++i)
-                tma_load_3d_pair(sB + i * 8192, &tmB, leader_full, n0 + 64 * i, p.b_swap ? bb : k0,
-                                 p.b_swap ? k0 : bb);
+                for (int i = 0; i < 2; ++i)
+                  tma_load_3d_pair(sB + i * 8192, &tmB, leader_full, n0 + 64 * i, p.b_swap ? bb : k0,
+                                   p.b_swap ? k0 : bb);
+              }
             }
             last_issue_phase[stage] = static_cast<int>(phase);
           }
@@ -778,6 +800,13 @@ __global__ void __launch_bounds__(threads_for<EPI>(), 1)
 }
 
 // ------------------------------------------------------------ host side
+// TPFFN_MN4D=0 in the environment selects the 3-D maps (one request per
+// 64-element group) for MN-major operands, for comparisons.
+static bool getenv_flag_off(const char* name) {
+  const char* v = getenv(name);
+  return v && v[0] == '0';
+}
+
 typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
                                   const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
@@ -825,6 +854,25 @@ static int make_map(CUtensorMap* m, const Operand& op, int rows_box, int* swap) 
   cuuint64_t dims[3], strides[2];
   cuuint32_t box[3], estr[3] = {1, 1, 1};
   *swap = (op.batch > 1 && op.batch_stride < op.row_stride) ? 1 : 0;
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return TP_ERR_CUDA;
+  // MN-major operands whose M/N extent is whole 64-element groups: a 4-D view
+  // {64 (M/N within a group), K rows, groups, batch} lets one request fetch
+  // every group of the tile in the layout the MMA reads (group i at +8 KB i).
+  if (op.mn_major && !*swap && op.inner % 64 == 0 && rows_box % 64 == 0 && !getenv_flag_off("TPFFN_MN4D")) {
+    cuuint64_t d4[4] = {64, static_cast<cuuint64_t>(op.rows), static_cast<cuuint64_t>(op.inner / 64),
+                        static_cast<cuuint64_t>(op.batch)};
+    cuuint64_t s4[3] = {static_cast<cuuint64_t>(op.row_stride * es), 64 * es, static_cast<cuuint64_t>(bst * es)};
+    cuuint32_t b4[4] = {64, 64, static_cast<cuuint32_t>(rows_box / 64), 1}, e4[4] = {1, 1, 1, 1};
+    CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(op.ptr), d4, s4, b4, e4,
+                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r == CUDA_SUCCESS) {
+      *swap = 2;
+      return 0;
+    }
+    // otherwise the 3-D map below (one request per 64-element group)
+  }
   dims[0] = static_cast<cuuint64_t>(op.inner);
   box[0] = 64;
   if (!*swap) {
@@ -842,8 +890,6 @@ static int make_map(CUtensorMap* m, const Operand& op, int rows_box, int* swap) 
     box[1] = 1;
     box[2] = rb;
   }
-  EncodeTiledFn fn = encode_fn();
-  if (!fn) return TP_ERR_CUDA;
   CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(op.ptr), dims, strides, box, estr,
                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
