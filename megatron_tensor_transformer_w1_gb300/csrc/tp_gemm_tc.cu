@@ -524,6 +524,7 @@ __device__ __forceinline__ void umma_commit_pair_local(uint64_t* bar) {  // arri
 // [0] MMA wait on full, [1] MMA wait on tempty, [2] MMA thread total,
 // [3] producer wait on empty, [4] epilogue wait on tfull, [5] epilogue total, [6] k-iterations
 __device__ unsigned long long g_tpffn_dbg[8][256][8];  // [launch slot][CTA][counter]
+static int g_dbg_launch = 0;                           // pair-GEMM launches since the last clear
 #define DBG_T0() const long long _t0 = clock64()
 #define DBG_ADD(slot, since) \
   atomicAdd(&g_tpffn_dbg[p.dbg_slot & 7][blockIdx.x & 255][slot], (unsigned long long)(clock64() - (since)))
@@ -1000,8 +1001,7 @@ static int launch_pair(const GemmSpec& s, LaunchCtx& ctx) {
   p.debug_skip = ctx.debug_skip_load;
   ctx.debug_skip_load = 0;
 #ifdef TPFFN_INSTRUMENT
-  static int dbg_launch = 0;
-  p.dbg_slot = dbg_launch++ & 7;
+  p.dbg_slot = g_dbg_launch++ & 7;
 #endif
 
   auto kern = tc_gemm_pair_kernel<EPI, AMN, BMN>;
@@ -1052,6 +1052,7 @@ static int launch_pair(const GemmSpec& s, LaunchCtx& ctx) {
 
 #ifdef TPFFN_INSTRUMENT
 extern "C" __attribute__((visibility("default"))) int tpffn_debug_counters(unsigned long long* host, int clear) {
+  if (clear) tc::g_dbg_launch = 0;  // the next pair GEMM records into slot 0
   if (cudaMemcpyFromSymbol(host, tc::g_tpffn_dbg, sizeof(tc::g_tpffn_dbg)) != cudaSuccess) return 1;
   if (clear) {
     static unsigned long long zeros[8][256][8];
