@@ -681,7 +681,9 @@ def run_decode(args, ctx, dev, peaks):
     return {"workload": DECODE, "value": round(gbs, 1), "unit": "GB/s", "ms_per_step": round(ms, 4),
             "bytes_per_step": nbytes, "frac_of_hbm_peak": round(gbs / ctx["world"] / peaks["hbm"], 4),
             "roofline": {"kernel": dom, "bound": "hbm", "achieved": round(dach, 1), "peak": peaks["hbm"],
-                         "unit": "GB/s", "frac": round(dach / peaks["hbm"], 4), "traffic": NCU_TRAFFIC.get(dom),
+                         "unit": "GB/s", "frac": round(dach / peaks["hbm"], 4),
+                         # the DRAM captures above are of the training step's launches
+                         "traffic": None,
                          "launch_ms": round(dom_ms, 4)},
             "kernels": {q: {"launches": len(v), "avg_ms": round(sum(v) / len(v), 4)} for q, v in per.items()}}
 

@@ -951,7 +951,14 @@ static int launch_inst(const GemmSpec& s, LaunchCtx& ctx) {
   }
   const long long tiles = static_cast<long long>(p.tiles_m) * p.tiles_n * p.NB;
   if (tiles <= 0 || p.k_blocks <= 0) return TP_ERR_INVALID;
-  const int grid = static_cast<int>(tiles < ctx.num_sms ? tiles : ctx.num_sms);
+  int grid = static_cast<int>(tiles < ctx.num_sms ? tiles : ctx.num_sms);
+  // A single row of M tiles (decode-sized token counts) streams weights and
+  // is HBM-bound: spread the tiles evenly -- every CTA gets the same number
+  // of tiles -- rather than leaving a last wave on a fraction of the SMs.
+  if (p.tiles_m == 1 && tiles > grid) {
+    const long long waves = (tiles + grid - 1) / grid;
+    grid = static_cast<int>((tiles + waves - 1) / waves);
+  }
   if (ctx.before) ctx.before(ctx.user, s.name, ctx.stream);
   kern<<<grid, threads_for<EPI>(), L::SMEM, ctx.stream>>>(ta, tb, p);
   if (ctx.after) ctx.after(ctx.user, ctx.stream);
