@@ -96,6 +96,10 @@ CORE_CASES = [  # B, S, H, Hkv, T_p, causal, q_scale
     (1, 129, 4, 4, 4, False, 1.0),
     (2, 384, 2, 2, 1, True, 4.0),
     (1, 520, 4, 2, 2, False, 3.0),
+    (1, 257, 16, 2, 2, True, 1.0),   # GQA groups of 8, a one-row tail tile
+    (3, 97, 2, 1, 1, False, 2.0),    # T_p 1, ragged non-causal
+    (2, 2, 4, 4, 2, True, 1.0),      # two tokens
+    (1, 640, 2, 2, 2, True, 1.0),    # odd number of 128-row tiles (5)
 ]
 
 
@@ -129,6 +133,7 @@ SUB_CASES = [  # B, S, d, H, Hkv, T_p, causal, fused
     (2, 160, 256, 4, 2, 2, True, True),
     (1, 200, 384, 8, 8, 4, False, False),
     (3, 70, 128, 4, 4, 4, True, True),
+    (1, 130, 256, 16, 2, 2, True, False),  # GQA groups of 8
 ]
 
 
