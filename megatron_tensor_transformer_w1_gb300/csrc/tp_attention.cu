@@ -232,12 +232,12 @@ __device__ __forceinline__ void store_row_bf16(__nv_bfloat16* dst, const uint32_
 }
 
 // ================================================================ forward
-constexpr int F_Q = 0;
-constexpr int F_K = F_Q + TILE;       // 2 stages
+constexpr int F_Q = 0;                // 2 buffers: the next item's Q loads during this one
+constexpr int F_K = F_Q + 2 * TILE;   // 2 stages
 constexpr int F_V = F_K + 2 * TILE;   // 2 stages
 constexpr int F_X = F_V + 2 * TILE;   // row max / sum exchange [2 halves][128 rows] fp32
 constexpr int F_BAR = F_X + 1024;
-constexpr int F_SMEM = F_BAR + 256 + 1024;
+constexpr int F_SMEM = F_BAR + 512 + 1024;
 
 // P never leaves the chip: the softmax threads write it in bf16 over the S
 // block it came from (64 of the buffer's 128 columns, two probabilities per
@@ -250,8 +250,8 @@ __global__ void __launch_bounds__(NT, 1) attn_fwd_kernel(const __grid_constant__
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = align1024(smem_raw);
   uint64_t* bar = reinterpret_cast<uint64_t*>(smem + F_BAR);
-  uint64_t* q_full = bar + 0;
-  uint64_t* q_empty = bar + 1;
+  uint64_t* q_full = bar + 29;  // [2] (placed after the others)
+  uint64_t* q_empty = bar + 31; // [2]
   uint64_t* k_full = bar + 2;   // [2]
   uint64_t* k_empty = bar + 4;  // [2]
   uint64_t* v_full = bar + 6;   // [2]
@@ -267,14 +267,14 @@ __global__ void __launch_bounds__(NT, 1) attn_fwd_kernel(const __grid_constant__
   uint64_t* drain = bar + 19;
   uint64_t* pair_x = bar + 20;  // [4] both halves of a row wrote their value
   uint64_t* pair_r = bar + 24;  // [4] both halves read their partner's value
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bar + 28);
-  volatile int* abort_flag = reinterpret_cast<volatile int*>(bar + 28) + 1;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bar + 33);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(bar + 33) + 1;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
   if (threadIdx.x == 0) {
-    mbar_init(q_full, 1);
-    mbar_init(q_empty, 1);
     for (int i = 0; i < 2; ++i) {
+      mbar_init(&q_full[i], 1);
+      mbar_init(&q_empty[i], 1);
       mbar_init(&k_full[i], 1);
       mbar_init(&k_empty[i], 1);
       mbar_init(&v_full[i], 1);
@@ -305,21 +305,23 @@ __global__ void __launch_bounds__(NT, 1) attn_fwd_kernel(const __grid_constant__
   if (warp == 0) {
     // ------------------------------------------------ TMA producer
     if (lane == 0) {
-      int q_last = -1, k_last[2] = {-1, -1}, v_last[2] = {-1, -1};
+      int q_last[2] = {-1, -1}, k_last[2] = {-1, -1}, v_last[2] = {-1, -1};
       uint32_t kv = 0, it = 0;
       bool ok = true;
       for (int item = blockIdx.x; item < p.items && ok; item += gridDim.x, ++it) {
         int qb, b, h;
         decode_item(p, item, p.H, p.causal != 0, qb, b, h);
         const int nkb = p.causal ? qb + 1 : p.n_qb;
+        const int qbuf = it & 1;
+        const uint32_t qph = (it >> 1) & 1u;
         AT_T0(t16);
-        if (!W(q_empty, (it & 1u) ^ 1u)) break;
+        if (!W(&q_empty[qbuf], qph ^ 1u)) break;
         AT_ADD(16, t16);
-        mbar_arrive_expect_tx(q_full, TILE);
+        mbar_arrive_expect_tx(&q_full[qbuf], TILE);
         const int qc = p.g.qcol(h);
-        tma_load_3d(smem + F_Q, &tq, q_full, qc, qb * 128, b);
-        tma_load_3d(smem + F_Q + TILE / 2, &tq, q_full, qc + 64, qb * 128, b);
-        q_last = static_cast<int>(it & 1u);
+        tma_load_3d(smem + F_Q + qbuf * TILE, &tq, &q_full[qbuf], qc, qb * 128, b);
+        tma_load_3d(smem + F_Q + qbuf * TILE + TILE / 2, &tq, &q_full[qbuf], qc + 64, qb * 128, b);
+        q_last[qbuf] = static_cast<int>(qph);
         const int hk = h / p.G, kc = p.g.kcol(hk), vc = p.g.vcol(hk);
         for (int j = 0; j < nkb; ++j, ++kv) {
           const int st = kv & 1;
@@ -343,8 +345,8 @@ __global__ void __launch_bounds__(NT, 1) attn_fwd_kernel(const __grid_constant__
         }
       }
       // every issued copy lands before the CTA may exit
-      if (q_last >= 0) W.drain(q_full, static_cast<uint32_t>(q_last));
       for (int s = 0; s < 2; ++s) {
+        if (q_last[s] >= 0) W.drain(&q_full[s], static_cast<uint32_t>(q_last[s]));
         if (k_last[s] >= 0) W.drain(&k_full[s], static_cast<uint32_t>(k_last[s]));
         if (v_last[s] >= 0) W.drain(&v_full[s], static_cast<uint32_t>(v_last[s]));
       }
@@ -355,7 +357,6 @@ __global__ void __launch_bounds__(NT, 1) attn_fwd_kernel(const __grid_constant__
     if (lane == 0) {
       constexpr uint32_t ID_S = idesc(128, 0, 0);   // S = Q K^T
       constexpr uint32_t ID_PV = idesc(128, 0, 1);  // O += P V (V: N = hd contiguous)
-      const uint32_t qa = smem_u32(smem + F_Q);
       uint32_t kv = 0, sc = 0, pg = 0, it = 0;
       bool ok = true;
       AT_T0(t_mma);
@@ -363,8 +364,10 @@ __global__ void __launch_bounds__(NT, 1) attn_fwd_kernel(const __grid_constant__
         int qb, b, h;
         decode_item(p, item, p.H, p.causal != 0, qb, b, h);
         const int nkb = p.causal ? qb + 1 : p.n_qb;
-        if (!W(q_full, it & 1u)) break;
+        const int qbuf = it & 1;
+        if (!W(&q_full[qbuf], (it >> 1) & 1u)) break;
         tc_fence_after();
+        const uint32_t qa = smem_u32(smem + F_Q + qbuf * TILE);
         auto issue_s = [&](int j) -> bool {
           const uint32_t n = kv + j;
           const int st = n & 1;
@@ -382,7 +385,7 @@ __global__ void __launch_bounds__(NT, 1) attn_fwd_kernel(const __grid_constant__
             umma_bf16(tmem + buf * 128, kdesc(qa, 128, ks), kdesc(ka, 128, ks), ID_S, ks > 0 ? 1u : 0u);
           umma_commit(&s_full[buf]);
           umma_commit(&k_empty[st]);
-          if (j == nkb - 1) umma_commit(q_empty);  // Q free once the item's last S is done
+          if (j == nkb - 1) umma_commit(&q_empty[qbuf]);  // Q free once the item's last S is done
           return true;
         };
         if (!issue_s(0)) break;
@@ -929,12 +932,16 @@ __global__ void __launch_bounds__(NT, 1) attn_dq_kernel(const __grid_constant__ 
 }
 
 // ================================================================ dk, dv
+// Query/dO ring depth: a stage is held from the S^T / dP^T products until the
+// dK / dV products of the same block, so the ring must cover the TMA round
+// trip beyond that (3 stages left about one block of slack).
+constexpr int QST = 4;
 constexpr int V_K = 0;
 constexpr int V_V = V_K + TILE;
-constexpr int V_Q = V_V + TILE;        // 3 stages of [64 q][128]
-constexpr int V_DO = V_Q + 3 * KB;     // 3 stages
-constexpr int V_VEC = V_DO + 3 * KB;   // 3 stages x (64 lse + 64 D) floats
-constexpr int V_BAR = V_VEC + 3 * 512;
+constexpr int V_Q = V_V + TILE;          // QST stages of [64 q][128]
+constexpr int V_DO = V_Q + QST * KB;     // QST stages
+constexpr int V_VEC = V_DO + QST * KB;   // QST stages x (64 lse + 64 D) floats
+constexpr int V_BAR = V_VEC + QST * 512;
 constexpr int V_SMEM = V_BAR + 256 + 1024;
 
 __global__ void __launch_bounds__(NT, 1) attn_dkdv_kernel(const __grid_constant__ CUtensorMap tq128,
@@ -945,24 +952,24 @@ __global__ void __launch_bounds__(NT, 1) attn_dkdv_kernel(const __grid_constant_
   uint64_t* bar = reinterpret_cast<uint64_t*>(smem + V_BAR);
   uint64_t* kv_full = bar + 0;
   uint64_t* kv_empty = bar + 1;
-  uint64_t* q_full = bar + 2;     // [3]
-  uint64_t* q_empty = bar + 5;    // [3]
-  uint64_t* do_full = bar + 8;    // [3]
-  uint64_t* do_empty = bar + 11;  // [3]
-  uint64_t* sdp_full = bar + 14;  // [2]
-  uint64_t* pd_full = bar + 16;   // [2] one per stage (see the forward's p_full)
-  uint64_t* dkv_full = bar + 18;
-  uint64_t* dkv_empty = bar + 19;
-  uint64_t* drain = bar + 20;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bar + 21);
-  volatile int* abort_flag = reinterpret_cast<volatile int*>(bar + 21) + 1;
+  uint64_t* q_full = bar + 2;                // [QST]
+  uint64_t* q_empty = q_full + QST;          // [QST]
+  uint64_t* do_full = q_empty + QST;         // [QST]
+  uint64_t* do_empty = do_full + QST;        // [QST]
+  uint64_t* sdp_full = do_empty + QST;       // [2]
+  uint64_t* pd_full = sdp_full + 2;          // [2] one per stage (see the forward's p_full)
+  uint64_t* dkv_full = pd_full + 2;
+  uint64_t* dkv_empty = dkv_full + 1;
+  uint64_t* drain = dkv_empty + 1;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(drain + 1) + 1;
   float* vec = reinterpret_cast<float*>(smem + V_VEC);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
   if (threadIdx.x == 0) {
     mbar_init(kv_full, 1);
     mbar_init(kv_empty, 1);
-    for (int i = 0; i < 3; ++i) {
+    for (int i = 0; i < QST; ++i) {
       mbar_init(&q_full[i], 1);
       mbar_init(&q_empty[i], 1);
       mbar_init(&do_full[i], 1);
@@ -996,7 +1003,8 @@ __global__ void __launch_bounds__(NT, 1) attn_dkdv_kernel(const __grid_constant_
 
   if (warp == 0) {
     if (lane == 0) {
-      int kv_last = -1, q_last[3] = {-1, -1, -1}, do_last[3] = {-1, -1, -1};
+      int kv_last = -1, q_last[QST], do_last[QST];
+      for (int i = 0; i < QST; ++i) q_last[i] = do_last[i] = -1;
       uint32_t qc = 0, it = 0;
       bool ok = true;
       for (int item = blockIdx.x; item < p.items && ok; item += gridDim.x, ++it) {
@@ -1017,8 +1025,8 @@ __global__ void __launch_bounds__(NT, 1) attn_dkdv_kernel(const __grid_constant_
           const float* lse_row = p.lse + (static_cast<long long>(b) * p.H + h) * p.s_pad;
           const float* d_row = p.Dv + (static_cast<long long>(b) * p.H + h) * p.s_pad;
           for (int i = i0; i < p.n_b64; ++i, ++qc) {
-            const int st = qc % 3;
-            const uint32_t ph = (qc / 3) & 1u;
+            const int st = qc % QST;
+            const uint32_t ph = (qc / QST) & 1u;
             if (!W(&q_empty[st], ph ^ 1u)) { ok = false; break; }
             uint8_t* qd = smem + V_Q + st * KB;
             mbar_arrive_expect_tx(&q_full[st], KB + 512);
@@ -1037,7 +1045,7 @@ __global__ void __launch_bounds__(NT, 1) attn_dkdv_kernel(const __grid_constant_
         }
       }
       if (kv_last >= 0) W.drain(kv_full, static_cast<uint32_t>(kv_last));
-      for (int s2 = 0; s2 < 3; ++s2) {
+      for (int s2 = 0; s2 < QST; ++s2) {
         if (q_last[s2] >= 0) W.drain(&q_full[s2], static_cast<uint32_t>(q_last[s2]));
         if (do_last[s2] >= 0) W.drain(&do_full[s2], static_cast<uint32_t>(do_last[s2]));
       }
@@ -1060,8 +1068,8 @@ __global__ void __launch_bounds__(NT, 1) attn_dkdv_kernel(const __grid_constant_
         tc_fence_after();
         auto issue_sdp = [&](int t) -> bool {
           const uint32_t n = qc + t;
-          const int st = n % 3;
-          const uint32_t ph = (n / 3) & 1u;
+          const int st = n % QST;
+          const uint32_t ph = (n / QST) & 1u;
           AT_T0(t0);
           if (!W(&q_full[st], ph) || !W(&do_full[st], ph)) return false;
           BW_ADD(1, 0, t0);
@@ -1092,7 +1100,7 @@ __global__ void __launch_bounds__(NT, 1) attn_dkdv_kernel(const __grid_constant_
           BW_CNT(1, 4);
           AT_T0(t5);
           tc_fence_after();
-          const int st = (qc + t) % 3;
+          const int st = (qc + t) % QST;
           const uint32_t sbase = tmem + ((sc + t) & 1u) * 128;
           const uint32_t qa = smem_u32(smem + V_Q + st * KB), da = smem_u32(smem + V_DO + st * KB);
 #pragma unroll
@@ -1136,8 +1144,8 @@ __global__ void __launch_bounds__(NT, 1) attn_dkdv_kernel(const __grid_constant_
       for (int t = 0; t < n_it; ++t) {
         const int i = i0 + t % nq;
         const uint32_t n = qc + t;
-        const int st = n % 3;
-        const uint32_t ph = (n / 3) & 1u;
+        const int st = n % QST;
+        const uint32_t ph = (n / QST) & 1u;
         const uint32_t g = sc + t, stage = g & 1u, use = g >> 1;
         AT_T0(t7);
         if (!W.warp(&sdp_full[stage], use & 1u)) { ok = false; break; }
@@ -1244,9 +1252,9 @@ __global__ void pack_qkv_kernel(const __nv_bfloat16* Wq, const __nv_bfloat16* Wk
 }
 
 // barrier areas (mbarriers + TMEM slot + abort flag) fit their reserved bytes
-static_assert(F_SMEM - F_BAR - 1024 >= 28 * 8 + 8, "forward barrier area");
+static_assert(F_SMEM - F_BAR - 1024 >= 33 * 8 + 8, "forward barrier area");
 static_assert(Q_SMEM - Q_BAR - 1024 >= 21 * 8 + 8, "dq barrier area");
-static_assert(V_SMEM - V_BAR - 1024 >= 21 * 8 + 8, "dk/dv barrier area");
+static_assert(V_SMEM - V_BAR - 1024 >= (9 + 4 * QST) * 8 + 8, "dk/dv barrier area");
 static_assert(F_SMEM <= 232448 && Q_SMEM <= 232448 && V_SMEM <= 232448, "shared memory per CTA");
 
 // ================================================================ host
