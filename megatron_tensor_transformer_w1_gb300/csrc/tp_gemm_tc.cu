@@ -34,6 +34,7 @@
 #include <atomic>
 #include <cstdio>
 #include <cstdlib>
+#include <cstring>
 #include <mutex>
 
 #include "tc_ptx.cuh"
@@ -116,6 +117,16 @@ __device__ __forceinline__ void store_bf16x8(__nv_bfloat16* dst, const float* v)
 }
 __device__ __forceinline__ void load_bf16x8(const __nv_bfloat16* src, float* v) {
   uint4 q = *reinterpret_cast<const uint4*>(src);
+  const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&q);
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    float2 f = __bfloat1622float2(h[i]);
+    v[2 * i] = f.x;
+    v[2 * i + 1] = f.y;
+  }
+}
+
+__device__ __forceinline__ void unpack_bf16x8(const uint4 q, float* v) {
   const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&q);
 #pragma unroll
   for (int i = 0; i < 4; ++i) {
@@ -534,17 +545,48 @@ static int g_dbg_launch = 0;                           // pair-GEMM launches sin
 #endif
 
 constexpr int PAIR_BN = 256;   // N of the pair tile (each CTA stages half of it)
-constexpr int PAIR_STAGES = 7;
 
+// The backward epilogues read saved activations (z, or a|g) for every output
+// element.  Fetched by the epilogue threads themselves, one row per thread,
+// those loads slowed the tensor pipe of the same SM by ~15 % (measured: the
+// same kernel with the loads removed ran 1250 -> 1480 TFLOP/s, with the
+// arithmetic kept); staged by TMA into shared memory they cost little.  Each
+// epilogue warp owns a 4 KB slot: per 32-column chunk of its 32 rows, the
+// 32 x 32 bf16 block of z (2 KB), or of a and of g (2 x 2 KB), with 64-byte
+// swizzle.  The slots take one operand stage.
+template <int EPI>
+__host__ __device__ constexpr bool aux_staged() {
+  return EPI == EPI_SWIGLU_BWD || EPI == EPI_GELU_BWD;
+}
+
+template <int EPI>
 struct PairLayout {
+  static constexpr int STAGES = aux_staged<EPI>() ? 6 : 7;
   static constexpr int A_BYTES = BM * BK * 2;               // this CTA's 128 rows of A
   static constexpr int B_BYTES = (PAIR_BN / 2) * BK * 2;    // this CTA's half of B
   static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;     // 32 KB
-  static constexpr int BAR_OFF = PAIR_STAGES * STAGE_BYTES;
+  static constexpr int AUX_SLOT = 4096;                     // per epilogue warp
+  static constexpr int AUX_OFF = STAGES * STAGE_BYTES;
+  static constexpr int AUX_BYTES = aux_staged<EPI>() ? epi_warps<EPI>() * AUX_SLOT : 0;
+  static constexpr int BAR_OFF = AUX_OFF + AUX_BYTES;
   static constexpr int SMEM = BAR_OFF + 256 + 1024;
   static constexpr uint32_t TMEM_COLS = 2 * PAIR_BN;
-  static_assert((2 * PAIR_STAGES + 5) * 8 <= 232, "barrier area");
+  // full/empty per stage, tfull/tempty x2, drain, one slot barrier per epilogue warp
+  static_assert((2 * STAGES + 5 + (aux_staged<EPI>() ? epi_warps<EPI>() : 0)) * 8 <= 240, "barrier area");
+  static_assert(SMEM <= 232448, "shared memory per CTA");
 };
+
+// Swizzled 16-byte chunk k of row r in a slot block of 64-byte rows (the
+// 64-byte TMA swizzle: chunk bits 4..5 of the address XOR bits 7..8).
+__device__ __forceinline__ uint32_t sw64(uint32_t base, int r, int k) {
+  return base + static_cast<uint32_t>(r * 64) + (static_cast<uint32_t>(k ^ ((r >> 1) & 3)) << 4);
+}
+__device__ __forceinline__ uint4 lds128(uint32_t addr) {
+  uint4 v;
+  asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(addr)
+               : "memory");
+  return v;
+}
 
 // Pair tile order: like decode_tile, over 256-row M blocks.
 __device__ __forceinline__ void decode_pair_tile(const Params& p, int tile, int& b, int& mp, int& nb) {
@@ -566,10 +608,10 @@ __device__ __forceinline__ void decode_pair_tile(const Params& p, int tile, int&
 template <int EPI, bool AMN, bool BMN>
 __global__ void __launch_bounds__(threads_for<EPI>(), 1)
     tc_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                        const Params p) {
-  using L = PairLayout;
+                        const __grid_constant__ CUtensorMap tmX, const Params p) {
+  using L = PairLayout<EPI>;
   constexpr int BN = PAIR_BN;
-  constexpr int STAGES = PAIR_STAGES;
+  constexpr int STAGES = L::STAGES;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + L::BAR_OFF);
@@ -577,6 +619,7 @@ __global__ void __launch_bounds__(threads_for<EPI>(), 1)
   uint64_t* tfull = empty + STAGES;
   uint64_t* tempty = tfull + 2;
   uint64_t* drain = tempty + 2;
+  uint64_t* xbar = drain + 1;  // saved-activation slots (backward epilogues)
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::BAR_OFF + 240);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::BAR_OFF + 244);
 
@@ -597,6 +640,8 @@ __global__ void __launch_bounds__(threads_for<EPI>(), 1)
       mbar_init(&tempty[i], 2 * epi_warps<EPI>());  // leader: the epilogue warps of both CTAs
     }
     mbar_init(drain, 1);
+    if constexpr (aux_staged<EPI>())
+      for (int i = 0; i < epi_warps<EPI>(); ++i) mbar_init(&xbar[i], 1);
     *abort_flag = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
@@ -604,6 +649,7 @@ __global__ void __launch_bounds__(threads_for<EPI>(), 1)
   if (warp == 0 && lane == 0) {
     prefetch_tmap(&tmA);
     prefetch_tmap(&tmB);
+    if constexpr (aux_staged<EPI>()) prefetch_tmap(&tmX);
   }
   if (warp == 1) tmem_alloc_pair(tmem_slot, L::TMEM_COLS);
   tc_fence_before();
@@ -765,26 +811,144 @@ __global__ void __launch_bounds__(threads_for<EPI>(), 1)
 #ifdef TPFFN_INSTRUMENT
     const long long t_epi = clock64();
 #endif
-    for (int tile = cluster_id; tile < num_tiles; tile += num_clusters, ++local) {
-      const int buf = local & 1;
-      const uint32_t use = static_cast<uint32_t>(local >> 1);
-      bool w_ok;
-      {
-        DBG_T0();
-        w_ok = wait_bounded(&tfull[buf], use & 1u, abort_flag, p);
-        if (warp == 2 && lane == 0) DBG_ADD(4, _t0);
+    if constexpr (aux_staged<EPI>()) {
+      // Backward epilogue with the saved activations staged by TMA: chunk c
+      // of this warp's 32 rows lands in its slot while chunk c-1 is
+      // computed; the chunk after the tile's last is the next tile's first.
+      constexpr int CPW = BN / 32 / 2;  // 32-column chunks per warp (two warps per lane quarter)
+      constexpr uint32_t XBYTES = EPI == EPI_SWIGLU_BWD ? 4096u : 2048u;
+      const int part = (warp - 2) >> 2;
+      const int c0 = part * CPW;
+      uint8_t* xslot = smem + L::AUX_OFF + (warp - 2) * L::AUX_SLOT;
+      const uint32_t xs = smem_u32(xslot);
+      uint64_t* xb = &xbar[warp - 2];
+      uint32_t xph = 0;
+      bool pending = false;
+      auto issue = [&](int t, int c) {  // lane 0
+        int b, mp, nb;
+        decode_pair_tile(p, t, b, mp, nb);
+        const int row0 = mp * 256 + static_cast<int>(rank) * 128 + quarter * 32;
+        const int n = nb * BN + c * 32;
+        mbar_arrive_expect_tx(xb, XBYTES);
+        if constexpr (EPI == EPI_SWIGLU_BWD) {
+          // hidden unit n lives in 128-block n>>7 of the interleaved [a|g] rows
+          const int col = (n >> 7) * 256 + (n & 127);
+          tma_load_3d(xslot, &tmX, xb, col, row0, b);
+          tma_load_3d(xslot + 2048, &tmX, xb, col + 128, row0, b);
+        } else {
+          tma_load_3d(xslot, &tmX, xb, n, row0, b);
+        }
+      };
+      if (cluster_id < num_tiles) {
+        if (lane == 0) issue(cluster_id, c0);
+        pending = true;
       }
-      if (!w_ok) break;
-      tc_fence_after();
-      int b, mp, nb;
-      decode_pair_tile(p, tile, b, mp, nb);
-      const int row = mp * 256 + static_cast<int>(rank) * 128 + quarter * 32 + lane;
-      const uint32_t taddr = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) +
-                             static_cast<uint32_t>(buf * BN);
-      epilogue_tile<BN, EPI>(p, b, row, row < p.M, nb * BN, nb, taddr, (warp - 2) >> 2);
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive_cluster(buf ? leader_tempty1 : leader_tempty0);
+      bool ok = true;
+      for (int tile = cluster_id; tile < num_tiles && ok; tile += num_clusters, ++local) {
+        const int buf = local & 1;
+        const uint32_t use = static_cast<uint32_t>(local >> 1);
+        {
+          DBG_T0();
+          ok = wait_bounded(&tfull[buf], use & 1u, abort_flag, p);
+          if (warp == 2 && lane == 0) DBG_ADD(4, _t0);
+        }
+        if (!ok) break;
+        tc_fence_after();
+        int b, mp, nb;
+        decode_pair_tile(p, tile, b, mp, nb);
+        const int row = mp * 256 + static_cast<int>(rank) * 128 + quarter * 32 + lane;
+        const bool row_ok = row < p.M;
+        const uint32_t taddr = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) +
+                               static_cast<uint32_t>(buf * BN);
+        __nv_bfloat16* out = static_cast<__nv_bfloat16*>(p.out) + b * p.out_bs + (long long)row * p.out_rs;
+#pragma unroll 1
+        for (int c = c0; c < c0 + CPW; ++c) {
+          if (!wait_bounded(xb, xph, abort_flag, p)) {
+            ok = false;
+            break;
+          }
+          pending = false;
+          xph ^= 1u;
+          uint4 za[4], gg[4];
+#pragma unroll
+          for (int k = 0; k < 4; ++k) {
+            za[k] = lds128(sw64(xs, lane, k));
+            if constexpr (EPI == EPI_SWIGLU_BWD) gg[k] = lds128(sw64(xs + 2048, lane, k));
+          }
+          // the slot's reads are ordered before the next copy into it
+          asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+          __syncwarp();
+          int nt = tile, ncc = c + 1;
+          if (ncc == c0 + CPW) {
+            nt = tile + num_clusters;
+            ncc = c0;
+          }
+          if (nt < num_tiles) {
+            if (lane == 0) issue(nt, ncc);
+            pending = true;
+          }
+          uint32_t r[32];
+          __syncwarp();  // tcgen05.ld is warp-collective: reconverge first
+          tmem_ld32(taddr + c * 32, r);
+          tmem_wait_ld();
+          const int nc = nb * BN + c * 32;
+          if (!row_ok || nc >= p.n_store) continue;
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            const int n = nc + q * 8;
+            if (n >= p.n_store) break;  // n_store is a multiple of 8
+            float v[8], a[8];
+#pragma unroll
+            for (int j = 0; j < 8; ++j) v[j] = __uint_as_float(r[q * 8 + j]);
+            unpack_bf16x8(za[q], a);
+            if constexpr (EPI == EPI_GELU_BWD) {
+#pragma unroll
+              for (int j = 0; j < 8; ++j) v[j] *= gelu_tanh_grad_f(a[j]);
+              store_bf16x8(out + n, v);
+            } else {
+              float g[8], da[8], dg[8];
+              unpack_bf16x8(gg[q], g);
+#pragma unroll
+              for (int j = 0; j < 8; ++j) {
+                const float sg = sigmoid_f(a[j]);
+                dg[j] = v[j] * a[j] * sg;                                // dh * silu(a)
+                da[j] = v[j] * g[j] * sg * (1.0f + a[j] * (1.0f - sg));  // dh * g * silu'(a)
+              }
+              const long long col = (long long)(n >> 7) * 256 + (n & 127);
+              store_bf16x8(out + col, da);
+              store_bf16x8(out + col + 128, dg);
+            }
+          }
+        }
+        if (!ok) break;
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive_cluster(buf ? leader_tempty1 : leader_tempty0);
+      }
+      // a copy still in flight into the slot completes before the CTA exits
+      if (pending) wait_bounded(xb, xph, abort_flag, p, false);
+    } else {
+      for (int tile = cluster_id; tile < num_tiles; tile += num_clusters, ++local) {
+        const int buf = local & 1;
+        const uint32_t use = static_cast<uint32_t>(local >> 1);
+        bool w_ok;
+        {
+          DBG_T0();
+          w_ok = wait_bounded(&tfull[buf], use & 1u, abort_flag, p);
+          if (warp == 2 && lane == 0) DBG_ADD(4, _t0);
+        }
+        if (!w_ok) break;
+        tc_fence_after();
+        int b, mp, nb;
+        decode_pair_tile(p, tile, b, mp, nb);
+        const int row = mp * 256 + static_cast<int>(rank) * 128 + quarter * 32 + lane;
+        const uint32_t taddr = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) +
+                               static_cast<uint32_t>(buf * BN);
+        epilogue_tile<BN, EPI>(p, b, row, row < p.M, nb * BN, nb, taddr, (warp - 2) >> 2);
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive_cluster(buf ? leader_tempty1 : leader_tempty0);
+      }
     }
 #ifdef TPFFN_INSTRUMENT
     if (warp == 2 && lane == 0) DBG_ADD(5, t_epi);
@@ -966,15 +1130,38 @@ static int launch_inst(const GemmSpec& s, LaunchCtx& ctx) {
   return cudaPeekAtLastError() == cudaSuccess ? 0 : TP_ERR_CUDA;
 }
 
+// Saved activations of a backward epilogue, {columns, rows, batch}: a
+// 32 x 32 box per copy, 64-byte swizzle, zero fill past the rows / columns.
+static int make_aux_map(CUtensorMap* m, const GemmSpec& s) {
+  if (!s.aux || reinterpret_cast<uintptr_t>(s.aux) % 16) return TP_ERR_ALIGN;
+  if ((s.aux_rs * 2) % 16 || (s.aux_bs * 2) % 16) return TP_ERR_ALIGN;
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return TP_ERR_CUDA;
+  const int64_t nb = s.NB > 1 ? s.NB : 1;
+  cuuint64_t dims[3] = {static_cast<cuuint64_t>(s.aux_rs), static_cast<cuuint64_t>(s.M), static_cast<cuuint64_t>(nb)};
+  cuuint64_t strides[2] = {static_cast<cuuint64_t>(s.aux_rs * 2),
+                           static_cast<cuuint64_t>(nb > 1 ? s.aux_bs * 2 : s.aux_rs * 2 * s.M)};
+  cuuint32_t box[3] = {32, 32, 1}, estr[3] = {1, 1, 1};
+  CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(s.aux), dims, strides, box, estr,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? 0 : TP_ERR_CUDA;
+}
+
 template <int EPI, bool AMN, bool BMN>
 static int launch_pair(const GemmSpec& s, LaunchCtx& ctx) {
-  using L = PairLayout;
-  CUtensorMap ta, tb;
+  using L = PairLayout<EPI>;
+  CUtensorMap ta, tb, tx;
   int sa = 0, sb = 0;
   int rc = make_map(&ta, s.A, BM, &sa);
   if (rc) return rc;
   rc = make_map(&tb, s.B, PAIR_BN / 2, &sb);
   if (rc) return rc;
+  memset(&tx, 0, sizeof(tx));
+  if constexpr (aux_staged<EPI>()) {
+    rc = make_aux_map(&tx, s);
+    if (rc) return rc;
+  }
   Params p{};
   p.M = static_cast<int>(s.M);
   p.N = static_cast<int>(s.N);
@@ -1049,7 +1236,7 @@ static int launch_pair(const GemmSpec& s, LaunchCtx& ctx) {
   const int clusters = static_cast<int>(tiles < mc ? tiles : mc);
   cfg.gridDim = dim3(2 * clusters, 1, 1);
   if (ctx.before) ctx.before(ctx.user, s.name, ctx.stream);
-  cudaError_t e = cudaLaunchKernelEx(&cfg, kern, ta, tb, p);
+  cudaError_t e = cudaLaunchKernelEx(&cfg, kern, ta, tb, tx, p);
   if (ctx.after) ctx.after(ctx.user, ctx.stream);
   ctx.launches++;
   return e == cudaSuccess && cudaPeekAtLastError() == cudaSuccess ? 0 : TP_ERR_CUDA;

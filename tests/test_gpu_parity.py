@@ -68,6 +68,7 @@ SMALL = [
     small_case(257, 192, 384, 1, "gelu_tanh", bias=True, seed=105),  # TP1 = dense
     small_case(1, 64, 256, 2, "swiglu", seed=106),             # a single token
     small_case(300, 136, 96, 2, "gelu_tanh", bias=True, seed=107),   # s = 48 < one tile
+    small_case(520, 192, 900, 3, "swiglu", seed=108),          # s = 300 -> 384: the second N tile half empty
 ]
 
 
