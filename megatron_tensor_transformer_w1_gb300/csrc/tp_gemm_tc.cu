@@ -260,9 +260,15 @@ __device__ __forceinline__ void epilogue_tile(const Params& p, int b, int row, b
 }
 
 // ------------------------------------------------------------ the kernel
-template <int BN, int STAGES>
+// AR: rows of A staged per K block.  Decode-sized token counts stage only
+// their 32 rows; the M = 128 product still reads 128 rows of A, and rows
+// 32..127 then come from the B tile that follows in the same stage -- rows
+// whose outputs are never stored (each output row depends on its A row
+// only).  The stage shrinks from 48 to 36 KB, so six stages instead of four
+// keep 50 % more weight bytes in flight per SM.
+template <int BN, int STAGES, int AR = BM>
 struct Layout {
-  static constexpr int A_BYTES = BM * BK * 2;
+  static constexpr int A_BYTES = AR * BK * 2;
   static constexpr int B_BYTES = BN * BK * 2;
   static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
   static constexpr int BAR_OFF = STAGES * STAGE_BYTES;
@@ -272,11 +278,13 @@ struct Layout {
   static_assert(TMEM_COLS >= 32 && TMEM_COLS <= 512 && (TMEM_COLS & (TMEM_COLS - 1)) == 0, "TMEM columns");
 };
 
-template <int BN, int STAGES, int EPI, bool AMN, bool BMN>
+template <int BN, int STAGES, int EPI, bool AMN, bool BMN, int AR = BM>
 __global__ void __launch_bounds__(threads_for<EPI>(), 1)
     tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                    const Params p) {
-  using L = Layout<BN, STAGES>;
+  using L = Layout<BN, STAGES, AR>;
+  static_assert(AR == BM || (!AMN && AR % 8 == 0 && L::STAGE_BYTES >= BM * BK * 2),
+                "a short A tile is K-major and the product's 128 rows stay inside the stage");
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + L::BAR_OFF);
@@ -1061,12 +1069,13 @@ static int make_map(CUtensorMap* m, const Operand& op, int rows_box, int* swap) 
   return r == CUDA_SUCCESS ? 0 : TP_ERR_CUDA;
 }
 
-template <int BN, int STAGES, int EPI, bool AMN, bool BMN>
+template <int BN, int STAGES, int EPI, bool AMN, bool BMN, int AR = BM>
 static int launch_inst(const GemmSpec& s, LaunchCtx& ctx) {
-  using L = Layout<BN, STAGES>;
+  using L = Layout<BN, STAGES, AR>;
+  if (AR < BM && s.M > AR) return TP_ERR_INVALID;
   CUtensorMap ta, tb;
   int sa = 0, sb = 0;
-  int rc = make_map(&ta, s.A, BM, &sa);
+  int rc = make_map(&ta, s.A, AR, &sa);
   if (rc) return rc;
   rc = make_map(&tb, s.B, BN, &sb);
   if (rc) return rc;
@@ -1103,7 +1112,7 @@ static int launch_inst(const GemmSpec& s, LaunchCtx& ctx) {
   p.debug_skip = ctx.debug_skip_load;
   ctx.debug_skip_load = 0;
 
-  auto kern = tc_gemm_kernel<BN, STAGES, EPI, AMN, BMN>;
+  auto kern = tc_gemm_kernel<BN, STAGES, EPI, AMN, BMN, AR>;
   static std::atomic<uint32_t> attr_done{0};  // one bit per device
   int dev = 0;
   cudaGetDevice(&dev);
@@ -1296,6 +1305,10 @@ int launch_tc_gemm(const GemmSpec& s, LaunchCtx& ctx) {
       default:
         break;
     }
+  }
+  if (s.M <= 32 && !amn && !bmn) {  // decode: weights stream from HBM
+    if (s.epi == EPI_SWIGLU_FWD) return launch_inst<256, 6, EPI_SWIGLU_FWD, false, false, 32>(s, ctx);
+    if (s.epi == EPI_F32) return launch_inst<256, 6, EPI_F32, false, false, 32>(s, ctx);
   }
   switch (s.epi) {
     case EPI_SWIGLU_FWD:

@@ -69,6 +69,8 @@ SMALL = [
     small_case(1, 64, 256, 2, "swiglu", seed=106),             # a single token
     small_case(300, 136, 96, 2, "gelu_tanh", bias=True, seed=107),   # s = 48 < one tile
     small_case(520, 192, 900, 3, "swiglu", seed=108),          # s = 300 -> 384: the second N tile half empty
+    small_case(32, 256, 1536, 4, "swiglu", seed=109),          # decode-sized: 32-row A tiles
+    small_case(17, 200, 600, 3, "swiglu", seed=110),           # decode-sized, ragged: 17 of 32 rows
 ]
 
 
