@@ -200,6 +200,20 @@ __device__ __forceinline__ void epilogue_tile(const Params& p, int b, int row, b
       tmem_wait_ld();
       const int nc = n0 + c * 32;
       if (!row_ok || nc >= p.n_store) continue;  // no warp-collective op follows in this iteration
+      // the chunk's 32 bias values, read once (one round trip per chunk)
+      float bv[32];
+      if constexpr (EPI == EPI_OUT || EPI == EPI_GELU_FWD) {
+        if (p.bias) {
+          const __nv_bfloat16* bp = p.bias + b * p.bias_bs + nc;
+          if (nc + 32 <= p.bias_len && (reinterpret_cast<uintptr_t>(bp) & 15) == 0) {
+#pragma unroll
+            for (int q = 0; q < 4; ++q) load_bf16x8(bp + q * 8, bv + q * 8);
+          } else {
+#pragma unroll
+            for (int j = 0; j < 32; ++j) bv[j] = nc + j < p.bias_len ? __bfloat162float(bp[j]) : 0.f;
+          }
+        }
+      }
 #pragma unroll
       for (int q = 0; q < 4; ++q) {
         const int n = nc + q * 8;
@@ -214,15 +228,13 @@ __device__ __forceinline__ void epilogue_tile(const Params& p, int b, int row, b
         } else if constexpr (EPI == EPI_OUT) {
           if (p.bias) {
 #pragma unroll
-            for (int j = 0; j < 8; ++j)
-              if (n + j < p.bias_len) v[j] += __bfloat162float(p.bias[b * p.bias_bs + n + j]);
+            for (int j = 0; j < 8; ++j) v[j] += bv[q * 8 + j];
           }
           store_bf16x8(static_cast<__nv_bfloat16*>(p.out) + b * p.out_bs + (long long)row * p.out_rs + n, v);
         } else if constexpr (EPI == EPI_GELU_FWD) {
           if (p.bias) {
 #pragma unroll
-            for (int j = 0; j < 8; ++j)
-              if (n + j < p.bias_len) v[j] += __bfloat162float(p.bias[b * p.bias_bs + n + j]);
+            for (int j = 0; j < 8; ++j) v[j] += bv[q * 8 + j];
           }
           if (p.out2)
             store_bf16x8(static_cast<__nv_bfloat16*>(p.out2) + b * p.out2_bs + (long long)row * p.out2_rs + n, v);
