@@ -79,10 +79,11 @@ int num_sms_current() {
   return v;
 }
 
-// Rows per block of the first column-sum pass: 256, more for very long token
+// Rows per block of the first column-sum pass: 64 (enough blocks to spread
+// a short token axis over the SMs), more for very long token
 // counts so that the chunk count stays within the grid's y limit.
 int64_t colsum_chunk(int64_t rows) {
-  int64_t c = 256;
+  int64_t c = 64;
   while ((rows + c - 1) / c > 4096) c *= 2;
   return c;
 }

@@ -240,17 +240,49 @@ __global__ void __launch_bounds__(256) shard_sum_scatter_vec8_kernel(const float
 }
 
 // ------------------------------------------------------------------ colsum
-__global__ void colsum_pass1_kernel(const void* in, int in_bf16, long long rows, long long cols, long long rs,
-                                    long long bs, float* scratch, long long chunk_rows, long long chunks) {
-  const long long col = blockIdx.x * (long long)blockDim.x + threadIdx.x;
+// Pass 1: a block covers 256 columns of one chunk of rows: 32 column groups
+// of 8 (16-byte loads of bf16 rows where the layout allows) times 8 row
+// lanes, lane l taking rows l, l+8, ...; the lanes' partial sums are then
+// added in lane order, so the result is fixed for a given chunking.
+__global__ void __launch_bounds__(256) colsum_pass1_kernel(const void* in, int in_bf16, long long rows,
+                                                           long long cols, long long rs, long long bs,
+                                                           float* scratch, long long chunk_rows, long long chunks) {
+  __shared__ float part[8][256 + 4];
+  const int cg = threadIdx.x & 31, lane = threadIdx.x >> 5;
+  const long long c0 = blockIdx.x * 256LL + cg * 8;
   const long long chunk = blockIdx.y;
   const long long b = blockIdx.z;
-  if (col >= cols) return;
   const long long r0 = chunk * chunk_rows;
   const long long r1 = min(rows, r0 + chunk_rows);
-  float acc = 0.f;
-  for (long long r = r0; r < r1; ++r) acc += to_f(in, b * bs + r * rs + col, in_bf16);
-  scratch[(b * chunks + chunk) * cols + col] = acc;
+  const bool vec = in_bf16 && rs % 8 == 0 && bs % 8 == 0 && (reinterpret_cast<uintptr_t>(in) & 15) == 0 &&
+                   c0 + 8 <= cols;
+  float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+  for (long long r = r0 + lane; r < r1; r += 8) {
+    const long long base = b * bs + r * rs + c0;
+    if (vec) {
+      const uint4 q = *reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(in) + base);
+      const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&q);
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        const float2 f = __bfloat1622float2(h[k]);
+        acc[2 * k] += f.x;
+        acc[2 * k + 1] += f.y;
+      }
+    } else {
+#pragma unroll
+      for (int j = 0; j < 8; ++j)
+        if (c0 + j < cols) acc[j] += to_f(in, base + j, in_bf16);
+    }
+  }
+#pragma unroll
+  for (int j = 0; j < 8; ++j) part[lane][cg * 8 + j] = acc[j];
+  __syncthreads();
+  const long long col = blockIdx.x * 256LL + threadIdx.x;
+  if (col >= cols) return;
+  float sum = 0.f;
+#pragma unroll
+  for (int l = 0; l < 8; ++l) sum += part[l][threadIdx.x];
+  scratch[(b * chunks + chunk) * cols + col] = sum;
 }
 __global__ void colsum_pass2_kernel(const float* scratch, long long cols, long long chunks, void* out, int out_bf16,
                                     long long out_bs) {
