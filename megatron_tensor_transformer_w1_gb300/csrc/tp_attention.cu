@@ -70,7 +70,6 @@ struct Params {
   Geo g;
   int B, S, H, Hkv, G, causal;
   int n_qb;    // 128-row blocks per sequence
-  int n_b64;   // 64-row blocks per sequence
   int items;
   __nv_bfloat16* o;
   long long o_rs;
@@ -629,19 +628,6 @@ __global__ void attn_prep_kernel(const Params p) {
 }
 
 // ================================================================ dq
-// The backward kernels keep the bf16 products of the softmax warps (dS, P^T,
-// dS^T) in tensor memory: each thread writes its two-per-cell bf16 values
-// over the first half of its own fp32 columns of the block's S (or dP)
-// buffer -- no other warp reads those columns -- and the tcgen05 products
-// read them as the A operand, one K = 16 step at a time (8 columns per
-// step; the two warps of a row hold K steps {0, 1} and {2, 3}).  A stage of
-// tensor memory is refilled only by a product issued after the ones that
-// read it, and tcgen05 products execute in issue order.
-__device__ __forceinline__ uint32_t a_step(uint32_t base, int ks) {
-  return base + static_cast<uint32_t>((ks >> 1) * 32 + (ks & 1) * 8);
-}
-
-constexpr int KB = 64 * HD * 2;        // [64 rows][128 cols] bf16: two 8 KB boxes
 constexpr int DQ_KV = 3;               // key/value stages of 128 keys in shared memory
 constexpr int Q_K = 0;
 constexpr int Q_V = Q_K + DQ_KV * TILE;
@@ -932,32 +918,48 @@ __global__ void __launch_bounds__(NT, 1) attn_dq_kernel(const __grid_constant__ 
 }
 
 // ================================================================ dk, dv
-// Query/dO ring depth: a stage is held from the S^T / dP^T products until the
-// dK / dV products of the same block, so the ring must cover the TMA round
-// trip beyond that (3 stages left about one block of slack).
-constexpr int QST = 4;
+// Blocks of 128 queries: S^T = K Q^T and dP^T = V dO^T are N = 128 products
+// (full rate; N = 64 ones sit at the per-instruction floor), and dV += P^T dO,
+// dK += dS^T Q contract over the block's 128 queries.  Tensor memory: S^T at
+// columns 0..127, dP^T at 128..255, dV at 256..383, dK at 384..511 -- one
+// S^T / dP^T stage, so a block's S^T / dP^T products follow the previous
+// block's dV / dK products, which read the P^T / dS^T written over S^T / dP^T
+// (tcgen05 products execute in issue order).  The softmax warps hand the block
+// over in two halves (queries {0..31, 64..95}, then {32..63, 96..127}); the
+// dV / dK products of the first half run while the second is computed.
+constexpr int VST = 2;                    // query / dO stages of 128 rows
 constexpr int V_K = 0;
 constexpr int V_V = V_K + TILE;
-constexpr int V_Q = V_V + TILE;          // QST stages of [64 q][128]
-constexpr int V_DO = V_Q + QST * KB;     // QST stages
-constexpr int V_VEC = V_DO + QST * KB;   // QST stages x (64 lse + 64 D) floats
-constexpr int V_BAR = V_VEC + QST * 512;
+constexpr int V_Q = V_V + TILE;           // VST stages of [128 q][128]
+constexpr int V_DO = V_Q + VST * TILE;    // VST stages
+constexpr int V_VEC = V_DO + VST * TILE;  // VST stages x (128 lse + 128 D) floats
+constexpr int V_BAR = V_VEC + VST * 1024;
 constexpr int V_SMEM = V_BAR + 256 + 1024;
 
+// The softmax warps keep P^T and dS^T in tensor memory: each thread writes
+// its bf16 pairs (two per 32-bit cell, lower K in the low half) over the
+// first half of its own fp32 columns of S^T / dP^T -- no other warp reads
+// them -- and the dV / dK products read them as the A operand, one K = 16
+// step (8 columns) at a time.  Tensor-memory column of K step ks within its
+// S^T / dP^T block: the warps of half h own queries [64 h, 64 h + 64).
+__device__ __forceinline__ uint32_t a_step128(uint32_t base, int ks) {
+  return base + static_cast<uint32_t>((ks >> 2) * 64 + (ks & 3) * 8);
+}
+
 __global__ void __launch_bounds__(NT, 1) attn_dkdv_kernel(const __grid_constant__ CUtensorMap tq128,
-                                                          const __grid_constant__ CUtensorMap tq64,
-                                                          const __grid_constant__ CUtensorMap tdo64, const Params p) {
+                                                          const __grid_constant__ CUtensorMap tdo128,
+                                                          const Params p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = align1024(smem_raw);
   uint64_t* bar = reinterpret_cast<uint64_t*>(smem + V_BAR);
   uint64_t* kv_full = bar + 0;
   uint64_t* kv_empty = bar + 1;
-  uint64_t* q_full = bar + 2;                // [QST]
-  uint64_t* q_empty = q_full + QST;          // [QST]
-  uint64_t* do_full = q_empty + QST;         // [QST]
-  uint64_t* do_empty = do_full + QST;        // [QST]
-  uint64_t* sdp_full = do_empty + QST;       // [2]
-  uint64_t* pd_full = sdp_full + 2;          // [2] one per stage (see the forward's p_full)
+  uint64_t* q_full = bar + 2;                // [VST]
+  uint64_t* q_empty = q_full + VST;          // [VST]
+  uint64_t* do_full = q_empty + VST;         // [VST]
+  uint64_t* do_empty = do_full + VST;        // [VST]
+  uint64_t* sdp_full = do_empty + VST;
+  uint64_t* pd_full = sdp_full + 1;          // [2] one per half-block hand-over
   uint64_t* dkv_full = pd_full + 2;
   uint64_t* dkv_empty = dkv_full + 1;
   uint64_t* drain = dkv_empty + 1;
@@ -969,16 +971,15 @@ __global__ void __launch_bounds__(NT, 1) attn_dkdv_kernel(const __grid_constant_
   if (threadIdx.x == 0) {
     mbar_init(kv_full, 1);
     mbar_init(kv_empty, 1);
-    for (int i = 0; i < QST; ++i) {
+    for (int i = 0; i < VST; ++i) {
       mbar_init(&q_full[i], 1);
       mbar_init(&q_empty[i], 1);
       mbar_init(&do_full[i], 1);
       mbar_init(&do_empty[i], 1);
     }
-    for (int i = 0; i < 2; ++i) {
-      mbar_init(&sdp_full[i], 1);
-      mbar_init(&pd_full[i], NSM);
-    }
+    mbar_init(sdp_full, 1);
+    mbar_init(&pd_full[0], NSM);
+    mbar_init(&pd_full[1], NSM);
     mbar_init(dkv_full, 1);
     mbar_init(dkv_empty, NSM);
     mbar_init(drain, 1);
@@ -988,23 +989,22 @@ __global__ void __launch_bounds__(NT, 1) attn_dkdv_kernel(const __grid_constant_
   }
   if (warp == 0 && lane == 0) {
     prefetch_tmap(&tq128);
-    prefetch_tmap(&tq64);
-    prefetch_tmap(&tdo64);
+    prefetch_tmap(&tdo128);
   }
   if (warp == 1) tmem_alloc(tmem_slot, 512);
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  const uint32_t tmem = *tmem_slot;  // stage s: S^T at 128 s, dP^T at 128 s + 64; dV at 256, dK at 384
+  const uint32_t tmem = *tmem_slot;
   const Waiter W{abort_flag, p.err, p.timeout_ns};
 
-  // causal: key block kb sees the 64-query blocks from 2 kb on
-  auto q0_of = [&](int kb) { return p.causal ? 2 * kb : 0; };
+  // causal: key block kb sees the query blocks from kb on
+  auto q0_of = [&](int kb) { return p.causal ? kb : 0; };
 
   if (warp == 0) {
     if (lane == 0) {
-      int kv_last = -1, q_last[QST], do_last[QST];
-      for (int i = 0; i < QST; ++i) q_last[i] = do_last[i] = -1;
+      int kv_last = -1, q_last[VST], do_last[VST];
+      for (int i = 0; i < VST; ++i) q_last[i] = do_last[i] = -1;
       uint32_t qc = 0, it = 0;
       bool ok = true;
       for (int item = blockIdx.x; item < p.items && ok; item += gridDim.x, ++it) {
@@ -1024,28 +1024,28 @@ __global__ void __launch_bounds__(NT, 1) attn_dkdv_kernel(const __grid_constant_
           const int qcol = p.g.qcol(h);
           const float* lse_row = p.lse + (static_cast<long long>(b) * p.H + h) * p.s_pad;
           const float* d_row = p.Dv + (static_cast<long long>(b) * p.H + h) * p.s_pad;
-          for (int i = i0; i < p.n_b64; ++i, ++qc) {
-            const int st = qc % QST;
-            const uint32_t ph = (qc / QST) & 1u;
+          for (int i = i0; i < p.n_qb; ++i, ++qc) {
+            const int st = qc % VST;
+            const uint32_t ph = (qc / VST) & 1u;
             if (!W(&q_empty[st], ph ^ 1u)) { ok = false; break; }
-            uint8_t* qd = smem + V_Q + st * KB;
-            mbar_arrive_expect_tx(&q_full[st], KB + 512);
-            tma_load_3d(qd, &tq64, &q_full[st], qcol, i * 64, b);
-            tma_load_3d(qd + KB / 2, &tq64, &q_full[st], qcol + 64, i * 64, b);
-            bulk_g2s(vec + st * 128, lse_row + i * 64, 256, &q_full[st]);
-            bulk_g2s(vec + st * 128 + 64, d_row + i * 64, 256, &q_full[st]);
+            uint8_t* qd = smem + V_Q + st * TILE;
+            mbar_arrive_expect_tx(&q_full[st], TILE + 1024);
+            tma_load_3d(qd, &tq128, &q_full[st], qcol, i * 128, b);
+            tma_load_3d(qd + TILE / 2, &tq128, &q_full[st], qcol + 64, i * 128, b);
+            bulk_g2s(vec + st * 256, lse_row + i * 128, 512, &q_full[st]);
+            bulk_g2s(vec + st * 256 + 128, d_row + i * 128, 512, &q_full[st]);
             q_last[st] = static_cast<int>(ph);
             if (!W(&do_empty[st], ph ^ 1u)) { ok = false; break; }
-            uint8_t* dd = smem + V_DO + st * KB;
-            mbar_arrive_expect_tx(&do_full[st], KB);
-            tma_load_3d(dd, &tdo64, &do_full[st], h * HD, i * 64, b);
-            tma_load_3d(dd + KB / 2, &tdo64, &do_full[st], h * HD + 64, i * 64, b);
+            uint8_t* dd = smem + V_DO + st * TILE;
+            mbar_arrive_expect_tx(&do_full[st], TILE);
+            tma_load_3d(dd, &tdo128, &do_full[st], h * HD, i * 128, b);
+            tma_load_3d(dd + TILE / 2, &tdo128, &do_full[st], h * HD + 64, i * 128, b);
             do_last[st] = static_cast<int>(ph);
           }
         }
       }
       if (kv_last >= 0) W.drain(kv_full, static_cast<uint32_t>(kv_last));
-      for (int s2 = 0; s2 < QST; ++s2) {
+      for (int s2 = 0; s2 < VST; ++s2) {
         if (q_last[s2] >= 0) W.drain(&q_full[s2], static_cast<uint32_t>(q_last[s2]));
         if (do_last[s2] >= 0) W.drain(&do_full[s2], static_cast<uint32_t>(do_last[s2]));
       }
@@ -1053,7 +1053,7 @@ __global__ void __launch_bounds__(NT, 1) attn_dkdv_kernel(const __grid_constant_
     __syncwarp();
   } else if (warp == 1) {
     if (lane == 0) {
-      constexpr uint32_t ID_S = idesc(64, 0, 0);    // S^T = K Q^T, dP^T = V dO^T
+      constexpr uint32_t ID_S = idesc(128, 0, 0);   // S^T = K Q^T, dP^T = V dO^T
       constexpr uint32_t ID_G = idesc(128, 0, 1);   // dV += P^T dO, dK += dS^T Q (A in TMEM)
       const uint32_t ka = smem_u32(smem + V_K), va = smem_u32(smem + V_V);
       uint32_t qc = 0, sc = 0, it = 0;
@@ -1062,57 +1062,55 @@ __global__ void __launch_bounds__(NT, 1) attn_dkdv_kernel(const __grid_constant_
       for (int item = blockIdx.x; item < p.items && ok; item += gridDim.x, ++it) {
         int kb, b, hk;
         decode_item(p, item, p.Hkv, false, kb, b, hk);
-        const int nq = p.n_b64 - q0_of(kb);
-        const int n_it = p.G * nq;
+        const int n_it = p.G * (p.n_qb - q0_of(kb));
         if (!W(kv_full, it & 1u)) break;
         tc_fence_after();
-        auto issue_sdp = [&](int t) -> bool {
-          const uint32_t n = qc + t;
-          const int st = n % QST;
-          const uint32_t ph = (n / QST) & 1u;
+        for (int t = 0; t < n_it; ++t) {
+          const uint32_t n = qc + t, g = sc + t;
+          const int st = n % VST;
+          const uint32_t ph = (n / VST) & 1u;
           AT_T0(t0);
-          if (!W(&q_full[st], ph) || !W(&do_full[st], ph)) return false;
+          if (!W(&q_full[st], ph) || !W(&do_full[st], ph)) { ok = false; break; }
           BW_ADD(1, 0, t0);
           AT_T0(t1);
           tc_fence_after();
-          const uint32_t sbase = tmem + ((sc + t) & 1u) * 128;
-          const uint32_t qa = smem_u32(smem + V_Q + st * KB), da = smem_u32(smem + V_DO + st * KB);
+          const uint32_t qa = smem_u32(smem + V_Q + st * TILE), da = smem_u32(smem + V_DO + st * TILE);
 #pragma unroll
           for (int ks = 0; ks < 8; ++ks)
-            umma_bf16(sbase, kdesc(ka, 128, ks), kdesc(qa, 64, ks), ID_S, ks > 0 ? 1u : 0u);
+            umma_bf16(tmem, kdesc(ka, 128, ks), kdesc(qa, 128, ks), ID_S, ks > 0 ? 1u : 0u);
 #pragma unroll
           for (int ks = 0; ks < 8; ++ks)
-            umma_bf16(sbase + 64, kdesc(va, 128, ks), kdesc(da, 64, ks), ID_S, ks > 0 ? 1u : 0u);
-          umma_commit(&sdp_full[(sc + t) & 1u]);
+            umma_bf16(tmem + 128, kdesc(va, 128, ks), kdesc(da, 128, ks), ID_S, ks > 0 ? 1u : 0u);
+          umma_commit(sdp_full);
           BW_ADD(1, 1, t1);
-          return true;
-        };
-        if (n_it > 0 && !issue_sdp(0)) break;
-        for (int t = 0; t < n_it; ++t) {
-          if (t + 1 < n_it && !issue_sdp(t + 1)) { ok = false; break; }
-          const uint32_t gs = sc + t;
-          AT_T0(t2);
-          if (!W(&pd_full[gs & 1u], (gs >> 1) & 1u)) { ok = false; break; }
-          BW_ADD(1, 2, t2);
           AT_T0(t3);
           if (t == 0 && !W(dkv_empty, (it & 1u) ^ 1u)) { ok = false; break; }
           BW_ADD(1, 3, t3);
           BW_CNT(1, 4);
-          AT_T0(t5);
-          tc_fence_after();
-          const int st = (qc + t) % QST;
-          const uint32_t sbase = tmem + ((sc + t) & 1u) * 128;
-          const uint32_t qa = smem_u32(smem + V_Q + st * KB), da = smem_u32(smem + V_DO + st * KB);
+          for (int c = 0; c < 2; ++c) {
+            AT_T0(t2);
+            if (!W(&pd_full[c], g & 1u)) { ok = false; break; }
+            BW_ADD(1, 2, t2);
+            AT_T0(t5);
+            tc_fence_after();
+            // K steps of this half-block: queries 32c .. 32c + 31 and 64 + 32c .. 64 + 32c + 31
 #pragma unroll
-          for (int ks = 0; ks < 4; ++ks)
-            umma_bf16_ta(tmem + 256, a_step(sbase, ks), mndesc(da, 64, ks), ID_G, (t > 0 || ks > 0) ? 1u : 0u);
+            for (int e = 0; e < 4; ++e) {
+              const int ks = (e >> 1) * 4 + 2 * c + (e & 1);
+              umma_bf16_ta(tmem + 256, a_step128(tmem, ks), mndesc(da, 128, ks), ID_G,
+                           (t > 0 || c > 0 || e > 0) ? 1u : 0u);
+            }
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              const int ks = (e >> 1) * 4 + 2 * c + (e & 1);
+              umma_bf16_ta(tmem + 384, a_step128(tmem + 128, ks), mndesc(qa, 128, ks), ID_G,
+                           (t > 0 || c > 0 || e > 0) ? 1u : 0u);
+            }
+            BW_ADD(1, 5, t5);
+          }
+          if (!ok) break;
           umma_commit(&do_empty[st]);
-#pragma unroll
-          for (int ks = 0; ks < 4; ++ks)
-            umma_bf16_ta(tmem + 384, a_step(sbase + 64, ks), mndesc(qa, 64, ks), ID_G,
-                         (t > 0 || ks > 0) ? 1u : 0u);
           umma_commit(&q_empty[st]);
-          BW_ADD(1, 5, t5);
         }
         if (!ok) break;
         umma_commit(dkv_full);
@@ -1126,9 +1124,9 @@ __global__ void __launch_bounds__(NT, 1) attn_dkdv_kernel(const __grid_constant_
     }
     __syncwarp();
   } else {
-    // warp w: TMEM lanes 32 (w % 4) .. (keys of the tile), query columns
-    // [32 half, 32 half + 32) of each 64-query block, and columns
-    // [64 half, 64 half + 64) of dV and dK
+    // warp w: TMEM lanes 32 (w % 4) .. (keys of the tile), queries
+    // [64 half, 64 half + 64) of each block (two 32-query pieces), and
+    // columns [64 half, 64 half + 64) of dV and dK
     const int quarter = warp & 3, half = (warp - 2) >> 2;
     const int row = quarter * 32 + lane;
     const uint32_t tl = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
@@ -1136,62 +1134,65 @@ __global__ void __launch_bounds__(NT, 1) attn_dkdv_kernel(const __grid_constant_
     for (int item = blockIdx.x; item < p.items; item += gridDim.x, ++it) {
       int kb, b, hk;
       decode_item(p, item, p.Hkv, false, kb, b, hk);
-      const int i0 = q0_of(kb), nq = p.n_b64 - i0;
+      const int i0 = q0_of(kb), nq = p.n_qb - i0;
       const int n_it = p.G * nq;
       const int kpos = kb * 128 + row;
       const bool row_ok = kpos < p.S;
       bool ok = true;
       for (int t = 0; t < n_it; ++t) {
         const int i = i0 + t % nq;
-        const uint32_t n = qc + t;
-        const int st = n % QST;
-        const uint32_t ph = (n / QST) & 1u;
-        const uint32_t g = sc + t, stage = g & 1u, use = g >> 1;
+        const uint32_t n = qc + t, g = sc + t;
+        const int st = n % VST;
+        const uint32_t ph = (n / VST) & 1u;
         AT_T0(t7);
-        if (!W.warp(&sdp_full[stage], use & 1u)) { ok = false; break; }
+        if (!W.warp(sdp_full, g & 1u)) { ok = false; break; }
 #ifdef TPFFN_INSTRUMENT
         if (warp == 2 && lane == 0) BW_ADD(1, 7, t7);
 #endif
         AT_T0(t8);
         tc_fence_after();
-        const uint32_t sb = tl + stage * 128 + half * 32;
-        uint32_t rs[32], rp[32];
-        tmem_ld32(sb, rs);
-        tmem_ld32(sb + 64, rp);
-        tmem_wait_ld();
         if (!W.warp(&q_full[st], ph)) { ok = false; break; }  // lse / D of this block landed
-        const float* lse_v = vec + st * 128 + half * 32;
-        const float* d_v = vec + st * 128 + 64 + half * 32;
-        // queries past the sequence read lse = +inf and D = 0 (p = 0); keys
-        // past it are never stored; only the causal diagonal needs a mask
-        const int qbase = i * 64 + half * 32;
-        if (p.causal && i * 64 < kb * 128 + 127) {
+        for (int c = 0; c < 2; ++c) {
+          const int col = half * 64 + c * 32;  // first query of this piece within the block
+          uint32_t rs[32], rp[32];
+          tmem_ld32(tl + col, rs);
+          tmem_ld32(tl + 128 + col, rp);
+          tmem_wait_ld();
+          const float* lse_v = vec + st * 256 + col;
+          const float* d_v = vec + st * 256 + 128 + col;
+          // queries past the sequence read lse = +inf and D = 0 (p = 0); keys
+          // past it are never stored; only the causal diagonal needs a mask
+          const int qbase = i * 128 + col;
+          if (p.causal && i == kb) {
 #pragma unroll
-          for (int c = 0; c < 32; ++c)
-            rs[c] = (kpos <= qbase + c) ? rs[c] : __float_as_uint(-INFINITY);
-        }
-        uint32_t pp[16], pd[16];
-#pragma unroll
-        for (int c = 0; c < 32; c += 4) {
-          const float4 lv = *reinterpret_cast<const float4*>(lse_v + c);
-          const float4 dv = *reinterpret_cast<const float4*>(d_v + c);
-          const float l4[4] = {lv.x, lv.y, lv.z, lv.w}, d4[4] = {dv.x, dv.y, dv.z, dv.w};
-          float pr[4], ds[4];
-#pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            pr[e] = ex2(fmaf(__uint_as_float(rs[c + e]), p.scale_log2, -l4[e]));
-            ds[e] = pr[e] * ((__uint_as_float(rp[c + e]) - d4[e]) * p.scale);
+            for (int e = 0; e < 32; ++e)
+              rs[e] = (kpos <= qbase + e) ? rs[e] : __float_as_uint(-INFINITY);
           }
-          pp[c / 2] = pack_bf16x2(pr[0], pr[1]);
-          pp[c / 2 + 1] = pack_bf16x2(pr[2], pr[3]);
-          pd[c / 2] = pack_bf16x2(ds[0], ds[1]);
-          pd[c / 2 + 1] = pack_bf16x2(ds[2], ds[3]);
+          uint32_t pp[16], pd[16];
+#pragma unroll
+          for (int e = 0; e < 32; e += 4) {
+            const float4 lv = *reinterpret_cast<const float4*>(lse_v + e);
+            const float4 dv = *reinterpret_cast<const float4*>(d_v + e);
+            const float l4[4] = {lv.x, lv.y, lv.z, lv.w}, d4[4] = {dv.x, dv.y, dv.z, dv.w};
+            float pr[4], ds[4];
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+              pr[k] = ex2(fmaf(__uint_as_float(rs[e + k]), p.scale_log2, -l4[k]));
+              ds[k] = pr[k] * ((__uint_as_float(rp[e + k]) - d4[k]) * p.scale);
+            }
+            pp[e / 2] = pack_bf16x2(pr[0], pr[1]);
+            pp[e / 2 + 1] = pack_bf16x2(pr[2], pr[3]);
+            pd[e / 2] = pack_bf16x2(ds[0], ds[1]);
+            pd[e / 2 + 1] = pack_bf16x2(ds[2], ds[3]);
+          }
+          // P^T / dS^T of K steps 4 half + 2c, +1: columns 64 half + 16 c ..
+          // +15, inside this thread's own (already read) S^T / dP^T columns
+          tmem_st16(tl + half * 64 + c * 16, pp);
+          tmem_st16(tl + 128 + half * 64 + c * 16, pd);
+          tmem_wait_st();
+          tc_fence_before();
+          mbar_arrive(&pd_full[c]);
         }
-        tmem_st16(sb, pp);       // P^T over this thread's own S^T columns
-        tmem_st16(sb + 64, pd);  // dS^T over its own dP^T columns
-        tmem_wait_st();
-        tc_fence_before();
-        mbar_arrive(&pd_full[stage]);
 #ifdef TPFFN_INSTRUMENT
         if (warp == 2 && lane == 0) BW_ADD(1, 8, t8);
 #endif
@@ -1254,7 +1255,7 @@ __global__ void pack_qkv_kernel(const __nv_bfloat16* Wq, const __nv_bfloat16* Wk
 // barrier areas (mbarriers + TMEM slot + abort flag) fit their reserved bytes
 static_assert(F_SMEM - F_BAR - 1024 >= 33 * 8 + 8, "forward barrier area");
 static_assert(Q_SMEM - Q_BAR - 1024 >= 21 * 8 + 8, "dq barrier area");
-static_assert(V_SMEM - V_BAR - 1024 >= (9 + 4 * QST) * 8 + 8, "dk/dv barrier area");
+static_assert(V_SMEM - V_BAR - 1024 >= (8 + 4 * VST) * 8 + 8, "dk/dv barrier area");
 static_assert(F_SMEM <= 232448 && Q_SMEM <= 232448 && V_SMEM <= 232448, "shared memory per CTA");
 
 // ================================================================ host
@@ -1272,7 +1273,6 @@ Params make_params(const AttnSpec& a, const LaunchCtx& ctx) {
   p.G = a.H / a.Hkv;
   p.causal = a.causal ? 1 : 0;
   p.n_qb = (a.S + 127) / 128;
-  p.n_b64 = (a.S + 63) / 64;
   p.o = static_cast<__nv_bfloat16*>(a.o);
   p.o_rs = a.o_rs;
   p.dO = static_cast<const __nv_bfloat16*>(a.dO);
@@ -1370,10 +1370,9 @@ int launch_attn_bwd(const AttnSpec& a, LaunchCtx& ctx) {
   if (rc) return rc;
   if (!a.qkv || !a.o || !a.lse || !a.dO || !a.Dv || !a.dqkv) return TP_ERR_INVALID;
   if (a.do_rs < static_cast<int64_t>(a.H) * HD || a.do_rs % 8) return TP_ERR_INVALID;
-  CUtensorMap tq128, tq64, tdo64;
+  CUtensorMap tq128, tdo128;
   if ((rc = map_rows(&tq128, a.qkv, a.qkv_rs, a.S, a.B, 128))) return rc;
-  if ((rc = map_rows(&tq64, a.qkv, a.qkv_rs, a.S, a.B, 64))) return rc;
-  if ((rc = map_rows(&tdo64, a.dO, a.do_rs, a.S, a.B, 64))) return rc;
+  if ((rc = map_rows(&tdo128, a.dO, a.do_rs, a.S, a.B, 128))) return rc;
   Params p = make_params(a, ctx);
 
   // D = rowsum(dO * o)
@@ -1400,7 +1399,7 @@ int launch_attn_bwd(const AttnSpec& a, LaunchCtx& ctx) {
     static std::atomic<uint32_t> done{0};
     if ((rc = set_smem_once(attn_dkdv_kernel, V_SMEM, done))) return rc;
     if (ctx.before) ctx.before(ctx.user, "attn_bwd_dkdv", ctx.stream);
-    attn_dkdv_kernel<<<grid_for(p.items, ctx.num_sms), NT, V_SMEM, ctx.stream>>>(tq128, tq64, tdo64, p);
+    attn_dkdv_kernel<<<grid_for(p.items, ctx.num_sms), NT, V_SMEM, ctx.stream>>>(tq128, tdo128, p);
     if (ctx.after) ctx.after(ctx.user, ctx.stream);
     ctx.launches++;
   }
