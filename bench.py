@@ -39,16 +39,22 @@ DECODE = "llama3_70b_decode_swiglu_bf16"
 
 # DRAM bytes per launch (dram__bytes_read.sum + dram__bytes_write.sum) from
 # one ncu capture of the Llama-3-8B step at full size (8192 tokens, fused
-# sums, two-SM pair GEMMs, raster groups of 8); see
-# profiles/llama3_8b_swiglu_gemm_dram_traffic.md.  To be cleared when the
+# sums, two-SM pair GEMMs, raster groups of 8, TMA-staged backward epilogue);
+# see profiles/llama3_8b_swiglu_gemm_dram_traffic.md.  To be cleared when the
 # kernels change.
 NCU_TRAFFIC = {
-    "up_swiglu": 1.29e9 + 679.03e6,
-    "down_fused_sum": 1.05e9 + 59.91e6,
-    "dgrad_h_swiglu": 1.52e9 + 447.99e6,
-    "dgrad_x_fused_sum": 2.41e9 + 60.22e6,
-    "wgrad_w2": 1.18e9 + 107.72e6,
-    "wgrad_w13": 2.23e9 + 225.02e6,
+    "up_swiglu": 1.142e9 + 678.07e6,
+    "down_fused_sum": 1.048e9 + 59.79e6,
+    "dgrad_h_swiglu": 1.704e9 + 440.65e6,
+    "dgrad_x_fused_sum": 2.110e9 + 59.83e6,
+    "wgrad_w2": 1.187e9 + 107.47e6,
+    "wgrad_w13": 2.213e9 + 224.10e6,
+}
+# The same for the decode-sized forward (Llama-3-70B shapes, 32 tokens,
+# one-SM kernel with 32-row A tiles); same profile file.
+NCU_TRAFFIC_DECODE = {
+    "up_swiglu": 940.65e6 + 4.42e6,
+    "down_partials": 471.64e6 + 4.32e6,
 }
 
 
@@ -682,8 +688,7 @@ def run_decode(args, ctx, dev, peaks):
             "bytes_per_step": nbytes, "frac_of_hbm_peak": round(gbs / ctx["world"] / peaks["hbm"], 4),
             "roofline": {"kernel": dom, "bound": "hbm", "achieved": round(dach, 1), "peak": peaks["hbm"],
                          "unit": "GB/s", "frac": round(dach / peaks["hbm"], 4),
-                         # the DRAM captures above are of the training step's launches
-                         "traffic": None,
+                         "traffic": NCU_TRAFFIC_DECODE.get(dom),
                          "launch_ms": round(dom_ms, 4)},
             "kernels": {q: {"launches": len(v), "avg_ms": round(sum(v) / len(v), 4)} for q, v in per.items()}}
 
