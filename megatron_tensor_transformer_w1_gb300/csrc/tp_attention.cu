@@ -239,12 +239,18 @@ constexpr int F_BAR = F_X + 1024;
 constexpr int F_SMEM = F_BAR + 512 + 1024;
 
 // P never leaves the chip: the softmax threads write it in bf16 over the S
-// block it came from (64 of the buffer's 128 columns, two probabilities per
-// 32-bit cell), and the PV product reads its A operand from tensor memory.
-// tcgen05 products of the CTA execute in issue order, so S_{j+2}, issued
-// after PV_j, overwrites that buffer only after PV_j has read it.  The "PV
-// done" barriers, indexed by the running count g of P blocks (g & 1), serve
-// the lazy rescale of O and the final read of O.
+// block it came from (two probabilities per 32-bit cell), and the PV product
+// reads its A operand from tensor memory.  tcgen05 products of the CTA
+// execute in issue order, so S_{j+2}, issued after PV_j, overwrites that
+// buffer only after PV_j has read it.  The "PV done" barriers, indexed by the
+// running count g of P blocks (g & 1), serve the lazy rescale of O and the
+// final read of O.
+// The two softmax warps of a row split each key block into halves, and each
+// half is an independent online softmax: its own running maximum, row sum
+// and O accumulator (O_0 at columns 256.., O_1 at 384..; its P over the
+// first 32 of its own 64 S columns).  The halves meet once per work item,
+// when O = (O_0 2^{m_0 - m} + O_1 2^{m_1 - m}) / l is written out, instead of
+// exchanging their maxima for every block.
 __global__ void __launch_bounds__(NT, 1) attn_fwd_kernel(const __grid_constant__ CUtensorMap tq, const Params p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = align1024(smem_raw);
@@ -298,7 +304,7 @@ __global__ void __launch_bounds__(NT, 1) attn_fwd_kernel(const __grid_constant__
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  const uint32_t tmem = *tmem_slot;  // S buffers at columns 0 and 128, O at 256
+  const uint32_t tmem = *tmem_slot;  // S buffers at columns 0 and 128, O_0 at 256, O_1 at 384
   const Waiter W{abort_flag, p.err, p.timeout_ns};
 
   if (warp == 0) {
@@ -404,10 +410,12 @@ __global__ void __launch_bounds__(NT, 1) attn_fwd_kernel(const __grid_constant__
           AT_CNT(6);
           tc_fence_after();
           const uint32_t va = smem_u32(smem + F_V + st * TILE);
-          const uint32_t pa = tmem + ((sc + j) & 1u) * 128;  // P over the S block it came from
+          // key half kh: its P over the first 32 of S columns [64 kh, 64 kh + 64), into O_kh
+          const uint32_t pa = tmem + ((sc + j) & 1u) * 128;
 #pragma unroll
           for (int ks = 0; ks < 8; ++ks)
-            umma_bf16_ta(tmem + 256, pa + ks * 8, mndesc(va, 128, ks), ID_PV, (j > 0 || ks > 0) ? 1u : 0u);
+            umma_bf16_ta(tmem + 256 + (ks >> 2) * 128, pa + (ks >> 2) * 64 + (ks & 3) * 8, mndesc(va, 128, ks),
+                         ID_PV, (j > 0 || (ks & 3) > 0) ? 1u : 0u);
           umma_commit(&v_empty[st]);
           umma_commit(&pv_done[pg & 1u]);
           ++pg;
@@ -450,7 +458,7 @@ __global__ void __launch_bounds__(NT, 1) attn_fwd_kernel(const __grid_constant__
       decode_item(p, item, p.H, p.causal != 0, qb, b, h);
       const int nkb = p.causal ? qb + 1 : p.n_qb;
       const int qpos = qb * 128 + row;
-      float m_used = -INFINITY, l = 0.f;  // l: this half's share of the row sum
+      float m_used = -INFINITY, l = 0.f;  // this key half's running maximum (log2 units) and row sum
       bool ok = true;
       for (int j = 0; j < nkb; ++j) {
         const uint32_t buf = sc & 1u, use = sc >> 1;
@@ -483,7 +491,7 @@ __global__ void __launch_bounds__(NT, 1) attn_fwd_kernel(const __grid_constant__
             r[c] = vis ? r[c] : __float_as_uint(-INFINITY);
           }
         }
-        // row maximum of the raw scores: eight chains, then the partner's half
+        // this half's maximum of the raw scores: eight chains
         float m8[8];
 #pragma unroll
         for (int c = 0; c < 8; ++c) m8[c] = __uint_as_float(r[c]);
@@ -491,20 +499,14 @@ __global__ void __launch_bounds__(NT, 1) attn_fwd_kernel(const __grid_constant__
         for (int c = 8; c < 64; ++c) m8[c & 7] = fmaxf(m8[c & 7], __uint_as_float(r[c]));
         const float mh = fmaxf(fmaxf(fmaxf(m8[0], m8[1]), fmaxf(m8[2], m8[3])),
                                fmaxf(fmaxf(m8[4], m8[5]), fmaxf(m8[6], m8[7])));
-        float mo;
 #ifdef TPFFN_INSTRUMENT
         if (rec) AT_ADD(9, t9);
 #endif
-        AT_T0(t10);
-        if (!exchange(mh, mo)) { ok = false; break; }
-#ifdef TPFFN_INSTRUMENT
-        if (rec) AT_ADD(10, t10);
-#endif
-        const float mx = fmaxf(mh, mo) * p.scale_log2;
+        const float mx = mh * p.scale_log2;
         float alpha = 1.f;
         bool rescale = false;
-        if (j == 0) {
-          m_used = mx;
+        if (m_used == -INFINITY) {
+          m_used = mx;  // first visible key of this half (O and l are still zero)
         } else if (mx > m_used + 8.f) {  // lazy rescale: p stays <= 2^8 otherwise
           alpha = ex2(m_used - mx);
           m_used = mx;
@@ -512,14 +514,14 @@ __global__ void __launch_bounds__(NT, 1) attn_fwd_kernel(const __grid_constant__
         }
         const uint32_t g = pg + j;
         if (__any_sync(0xffffffffu, rescale)) {
-          // O must hold PV g-1 before it is rescaled
+          // O_half must hold PV g-1 before it is rescaled
           const uint32_t gp = g - 1;
           if (!W.warp(&pv_done[gp & 1u], (gp >> 1) & 1u)) { ok = false; break; }
           tc_fence_after();
 #pragma unroll 1
-          for (int c = 0; c < 2; ++c) {
+          for (int c = 0; c < 4; ++c) {
             uint32_t o[32];
-            const uint32_t ta = tl + 256 + half * 64 + c * 32;
+            const uint32_t ta = tl + 256 + half * 128 + c * 32;
             tmem_ld32(ta, o);
             tmem_wait_ld();
 #pragma unroll
@@ -528,10 +530,10 @@ __global__ void __launch_bounds__(NT, 1) attn_fwd_kernel(const __grid_constant__
           }
           tmem_wait_st();
         }
-        // P (bf16 pairs) over columns [32 half, 32 half + 32) of this S
-        // buffer; both halves have read their S values (the exchange above)
+        // P (bf16 pairs) over the first 32 of this half's 64 S columns, which
+        // this thread has already read
         AT_T0(t12);
-        const float neg_m = -m_used;
+        const float neg_m = m_used == -INFINITY ? 0.f : -m_used;  // no visible key yet: every p is 0
         float l8[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
         uint32_t pk[32];
 #pragma unroll
@@ -541,8 +543,7 @@ __global__ void __launch_bounds__(NT, 1) attn_fwd_kernel(const __grid_constant__
           l8[c & 7] += e0 + e1;
           pk[c] = pack_bf16x2(e0, e1);
         }
-        tc_fence_after();  // orders this store after the partner's S load (exchange)
-        tmem_st32(tl + buf * 128 + half * 32, pk);
+        tmem_st32(tl + buf * 128 + half * 64, pk);
         tmem_wait_st();
         l = l * alpha + (((l8[0] + l8[1]) + (l8[2] + l8[3])) + ((l8[4] + l8[5]) + (l8[6] + l8[7])));
         tc_fence_before();
@@ -558,9 +559,13 @@ __global__ void __launch_bounds__(NT, 1) attn_fwd_kernel(const __grid_constant__
       AT_T0(t14);
       const uint32_t glast = pg + nkb - 1;
       pg += nkb;
-      float lo;
-      if (!exchange(l, lo)) break;
-      const float lsum = l + lo;
+      // the two halves meet: m = max(m_0, m_1), l = sum of l_h 2^{m_h - m}
+      float mo, lo;
+      if (!exchange(m_used, mo) || !exchange(l, lo)) break;
+      const float m = fmaxf(m_used, mo);  // finite: every row sees at least one key
+      const float f_mine = ex2(m_used - m), f_other = ex2(mo - m);
+      const float lsum = l * f_mine + lo * f_other;
+      const float f0 = half == 0 ? f_mine : f_other, f1 = half == 0 ? f_other : f_mine;
       if (!W.warp(&pv_done[glast & 1u], (glast >> 1) & 1u)) break;
       tc_fence_after();
       const bool row_ok = qpos < p.S;
@@ -568,14 +573,18 @@ __global__ void __launch_bounds__(NT, 1) attn_fwd_kernel(const __grid_constant__
       __nv_bfloat16* orow = p.o + (static_cast<long long>(b) * p.S + qpos) * p.o_rs + h * HD + half * 64;
 #pragma unroll 1
       for (int c = 0; c < 2; ++c) {
-        uint32_t o[32];
-        tmem_ld32(tl + 256 + half * 64 + c * 32, o);
+        uint32_t o0[32], o1[32];
+        tmem_ld32(tl + 256 + half * 64 + c * 32, o0);
+        tmem_ld32(tl + 384 + half * 64 + c * 32, o1);
         tmem_wait_ld();
-        if (row_ok) store_row_bf16(orow + c * 32, o, inv);
+#pragma unroll
+        for (int i = 0; i < 32; ++i)
+          o0[i] = __float_as_uint(fmaf(__uint_as_float(o0[i]), f0, __uint_as_float(o1[i]) * f1));
+        if (row_ok) store_row_bf16(orow + c * 32, o0, inv);
       }
       // rows past the sequence get lse = +inf: the backward reads them as p = 0
       if (half == 0)
-        p.lse[(static_cast<long long>(b) * p.H + h) * p.s_pad + qpos] = row_ok ? m_used + log2f(lsum) : INFINITY;
+        p.lse[(static_cast<long long>(b) * p.H + h) * p.s_pad + qpos] = row_ok ? m + log2f(lsum) : INFINITY;
       tc_fence_before();
       mbar_arrive(o_empty);
 #ifdef TPFFN_INSTRUMENT
