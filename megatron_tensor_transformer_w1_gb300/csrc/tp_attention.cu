@@ -262,7 +262,9 @@ __global__ void __launch_bounds__(NT, 1) attn_fwd_kernel(const __grid_constant__
   uint64_t* v_full = bar + 6;   // [2]
   uint64_t* v_empty = bar + 8;  // [2]
   uint64_t* s_full = bar + 10;  // [2]
-  uint64_t* s_empty = bar + 12; // [2]
+  // (bar + 12, 13 unused: an S buffer is rewritten only by an S product issued
+  // after the PV product of the block it held, which waited for that block's P,
+  // so the softmax warps have read it)
   // one "P written" barrier per S buffer: the softmax warps may run a block
   // ahead of the MMA thread's wait, and a single barrier would then advance
   // two phases before the wait sees the first
@@ -285,7 +287,6 @@ __global__ void __launch_bounds__(NT, 1) attn_fwd_kernel(const __grid_constant__
       mbar_init(&v_full[i], 1);
       mbar_init(&v_empty[i], 1);
       mbar_init(&s_full[i], 1);
-      mbar_init(&s_empty[i], NSM);
       mbar_init(&pv_done[i], 1);
       mbar_init(&p_full[i], NSM);
     }
@@ -379,10 +380,7 @@ __global__ void __launch_bounds__(NT, 1) attn_fwd_kernel(const __grid_constant__
           AT_T0(t0);
           if (!W(&k_full[st], (n >> 1) & 1u)) return false;
           AT_ADD(0, t0);
-          const uint32_t buf = (sc + j) & 1u, use = (sc + j) >> 1;
-          AT_T0(t1);
-          if (!W(&s_empty[buf], (use & 1u) ^ 1u)) return false;
-          AT_ADD(1, t1);
+          const uint32_t buf = (sc + j) & 1u;
           tc_fence_after();
           const uint32_t ka = smem_u32(smem + F_K + st * TILE);
 #pragma unroll
@@ -474,8 +472,6 @@ __global__ void __launch_bounds__(NT, 1) attn_fwd_kernel(const __grid_constant__
         tmem_ld32(tl + buf * 128 + half * 64, *reinterpret_cast<uint32_t(*)[32]>(&r[0]));
         tmem_ld32(tl + buf * 128 + half * 64 + 32, *reinterpret_cast<uint32_t(*)[32]>(&r[32]));
         tmem_wait_ld();
-        tc_fence_before();
-        mbar_arrive(&s_empty[buf]);
 #ifdef TPFFN_INSTRUMENT
         if (rec) AT_ADD(8, t8);
 #endif
