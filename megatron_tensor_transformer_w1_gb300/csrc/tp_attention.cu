@@ -258,9 +258,10 @@ __global__ void __launch_bounds__(NT, 1) attn_fwd_kernel(const __grid_constant__
   uint64_t* q_full = bar + 29;  // [2] (placed after the others)
   uint64_t* q_empty = bar + 31; // [2]
   uint64_t* k_full = bar + 2;   // [2]
-  uint64_t* k_empty = bar + 4;  // [2]
+  // (bar + 4, 5 and 8, 9 unused: a K stage is free once the S product that read
+  // it completes -- s_full of the same index, as K, V, S and PV all count the
+  // same blocks -- and a V stage once its PV completes -- pv_done)
   uint64_t* v_full = bar + 6;   // [2]
-  uint64_t* v_empty = bar + 8;  // [2]
   uint64_t* s_full = bar + 10;  // [2]
   // (bar + 12, 13 unused: an S buffer is rewritten only by an S product issued
   // after the PV product of the block it held, which waited for that block's P,
@@ -283,9 +284,7 @@ __global__ void __launch_bounds__(NT, 1) attn_fwd_kernel(const __grid_constant__
       mbar_init(&q_full[i], 1);
       mbar_init(&q_empty[i], 1);
       mbar_init(&k_full[i], 1);
-      mbar_init(&k_empty[i], 1);
       mbar_init(&v_full[i], 1);
-      mbar_init(&v_empty[i], 1);
       mbar_init(&s_full[i], 1);
       mbar_init(&pv_done[i], 1);
       mbar_init(&p_full[i], NSM);
@@ -333,7 +332,7 @@ __global__ void __launch_bounds__(NT, 1) attn_fwd_kernel(const __grid_constant__
           const int st = kv & 1;
           const uint32_t ph = (kv >> 1) & 1u;
           AT_T0(t17);
-          if (!W(&k_empty[st], ph ^ 1u)) { ok = false; break; }
+          if (!W(&s_full[st], ph ^ 1u)) { ok = false; break; }  // S of block kv-2 has read K
           AT_ADD(17, t17);
           uint8_t* kd = smem + F_K + st * TILE;
           mbar_arrive_expect_tx(&k_full[st], TILE);
@@ -341,7 +340,7 @@ __global__ void __launch_bounds__(NT, 1) attn_fwd_kernel(const __grid_constant__
           tma_load_3d(kd + TILE / 2, &tq, &k_full[st], kc + 64, j * 128, b);
           k_last[st] = static_cast<int>(ph);
           AT_T0(t18);
-          if (!W(&v_empty[st], ph ^ 1u)) { ok = false; break; }
+          if (!W(&pv_done[st], ph ^ 1u)) { ok = false; break; }  // PV of block kv-2 has read V
           AT_ADD(18, t18);
           uint8_t* vd = smem + F_V + st * TILE;
           mbar_arrive_expect_tx(&v_full[st], TILE);
@@ -387,7 +386,6 @@ __global__ void __launch_bounds__(NT, 1) attn_fwd_kernel(const __grid_constant__
           for (int ks = 0; ks < 8; ++ks)
             umma_bf16(tmem + buf * 128, kdesc(qa, 128, ks), kdesc(ka, 128, ks), ID_S, ks > 0 ? 1u : 0u);
           umma_commit(&s_full[buf]);
-          umma_commit(&k_empty[st]);
           if (j == nkb - 1) umma_commit(&q_empty[qbuf]);  // Q free once the item's last S is done
           return true;
         };
@@ -414,7 +412,6 @@ __global__ void __launch_bounds__(NT, 1) attn_fwd_kernel(const __grid_constant__
           for (int ks = 0; ks < 8; ++ks)
             umma_bf16_ta(tmem + 256 + (ks >> 2) * 128, pa + (ks >> 2) * 64 + (ks & 3) * 8, mndesc(va, 128, ks),
                          ID_PV, (j > 0 || (ks & 3) > 0) ? 1u : 0u);
-          umma_commit(&v_empty[st]);
           umma_commit(&pv_done[pg & 1u]);
           ++pg;
         }
