@@ -187,6 +187,16 @@ struct Waiter {
   }
 };
 
+// Softmax-side hand-overs arrive once per warp (NSW arrivals complete a
+// phase): every lane has finished its tensor-memory / shared-memory writes and
+// the fence that publishes them, the warp reconverges, and lane 0 arrives.
+// 256 per-thread arrivals on one barrier serialise on its shared-memory word.
+constexpr int NSW = NSM / 32;
+__device__ __forceinline__ void warp_arrive(uint64_t* bar) {
+  __syncwarp();
+  if ((threadIdx.x & 31) == 0) mbar_arrive(bar);
+}
+
 #ifdef TPFFN_INSTRUMENT
 // Per-CTA cycle counters of the forward kernel, for performance work only
 // (not in normal builds): see tpffn_attn_debug_counters.
@@ -287,9 +297,9 @@ __global__ void __launch_bounds__(NT, 1) attn_fwd_kernel(const __grid_constant__
       mbar_init(&v_full[i], 1);
       mbar_init(&s_full[i], 1);
       mbar_init(&pv_done[i], 1);
-      mbar_init(&p_full[i], NSM);
+      mbar_init(&p_full[i], NSW);
     }
-    mbar_init(o_empty, NSM);
+    mbar_init(o_empty, NSW);
     mbar_init(drain, 1);
     for (int i = 0; i < 4; ++i) {
       mbar_init(&pair_x[i], 64);
@@ -540,7 +550,7 @@ __global__ void __launch_bounds__(NT, 1) attn_fwd_kernel(const __grid_constant__
         tmem_wait_st();
         l = l * alpha + (((l8[0] + l8[1]) + (l8[2] + l8[3])) + ((l8[4] + l8[5]) + (l8[6] + l8[7])));
         tc_fence_before();
-        mbar_arrive(&p_full[g & 1u]);
+        warp_arrive(&p_full[g & 1u]);
 #ifdef TPFFN_INSTRUMENT
         if (rec) {
           AT_ADD(12, t12);
@@ -579,7 +589,7 @@ __global__ void __launch_bounds__(NT, 1) attn_fwd_kernel(const __grid_constant__
       if (half == 0)
         p.lse[(static_cast<long long>(b) * p.H + h) * p.s_pad + qpos] = row_ok ? m + log2f(lsum) : INFINITY;
       tc_fence_before();
-      mbar_arrive(o_empty);
+      warp_arrive(o_empty);
 #ifdef TPFFN_INSTRUMENT
       if (rec) AT_ADD(14, t14);
 #endif
@@ -678,7 +688,7 @@ __global__ void __launch_bounds__(NT, 1) attn_dq_kernel(const __grid_constant__ 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
   if (threadIdx.x == 0) {
-    mbar_init(qdo_ready, NSM);
+    mbar_init(qdo_ready, NSW);
     mbar_init(qdo_free, 1);
     for (int i = 0; i < DQ_KV; ++i) {
       mbar_init(&k_full[i], 1);
@@ -687,11 +697,11 @@ __global__ void __launch_bounds__(NT, 1) attn_dq_kernel(const __grid_constant__ 
       mbar_init(&v_empty[i], 1);
     }
     mbar_init(sdp_full, 1);
-    mbar_init(sdp_empty, NSM);
-    mbar_init(ds_full, NSM);
+    mbar_init(sdp_empty, NSW);
+    mbar_init(ds_full, NSW);
     mbar_init(ds_free, 1);
     mbar_init(dq_full, 1);
-    mbar_init(dq_empty, NSM);
+    mbar_init(dq_empty, NSW);
     mbar_init(drain, 1);
     *abort_flag = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
@@ -842,7 +852,7 @@ __global__ void __launch_bounds__(NT, 1) attn_dq_kernel(const __grid_constant__ 
         tmem_wait_st();
       }
       tc_fence_before();
-      mbar_arrive(qdo_ready);
+      warp_arrive(qdo_ready);
       bool ok = true;
       for (int j = 0; j < nkb; ++j, ++blk) {
         AT_T0(t7);
@@ -880,7 +890,7 @@ __global__ void __launch_bounds__(NT, 1) attn_dq_kernel(const __grid_constant__ 
           }
         }
         tc_fence_before();
-        mbar_arrive(sdp_empty);  // S and dP read: the next block's products may start
+        warp_arrive(sdp_empty);  // S and dP read: the next block's products may start
         // dS buffer free once the previous block's dQ has read it
         if (blk > 0 && !W.warp(ds_free, (blk - 1) & 1u)) { ok = false; break; }
 #pragma unroll
@@ -889,7 +899,7 @@ __global__ void __launch_bounds__(NT, 1) attn_dq_kernel(const __grid_constant__ 
                        pk[4 * c8 + 3]);
         fence_async_smem();
         tc_fence_before();
-        mbar_arrive(ds_full);
+        warp_arrive(ds_full);
 #ifdef TPFFN_INSTRUMENT
         if (warp == 2 && lane == 0) BW_ADD(0, 8, t8);
 #endif
@@ -907,7 +917,7 @@ __global__ void __launch_bounds__(NT, 1) attn_dq_kernel(const __grid_constant__ 
         if (row_ok) store_row_bf16(out + c * 32, o, 1.f);
       }
       tc_fence_before();
-      mbar_arrive(dq_empty);
+      warp_arrive(dq_empty);
     }
   }
 
@@ -980,10 +990,10 @@ __global__ void __launch_bounds__(NT, 1) attn_dkdv_kernel(const __grid_constant_
       mbar_init(&do_empty[i], 1);
     }
     mbar_init(sdp_full, 1);
-    mbar_init(&pd_full[0], NSM);
-    mbar_init(&pd_full[1], NSM);
+    mbar_init(&pd_full[0], NSW);
+    mbar_init(&pd_full[1], NSW);
     mbar_init(dkv_full, 1);
-    mbar_init(dkv_empty, NSM);
+    mbar_init(dkv_empty, NSW);
     mbar_init(drain, 1);
     *abort_flag = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
@@ -1193,7 +1203,7 @@ __global__ void __launch_bounds__(NT, 1) attn_dkdv_kernel(const __grid_constant_
           tmem_st16(tl + 128 + half * 64 + c * 16, pd);
           tmem_wait_st();
           tc_fence_before();
-          mbar_arrive(&pd_full[c]);
+          warp_arrive(&pd_full[c]);
         }
 #ifdef TPFFN_INSTRUMENT
         if (warp == 2 && lane == 0) BW_ADD(1, 8, t8);
@@ -1219,7 +1229,7 @@ __global__ void __launch_bounds__(NT, 1) attn_dkdv_kernel(const __grid_constant_
         if (row_ok) store_row_bf16(out + kcol + c * 32, o, 1.f);
       }
       tc_fence_before();
-      mbar_arrive(dkv_empty);
+      warp_arrive(dkv_empty);
       qc += n_it;
       sc += n_it;
     }
