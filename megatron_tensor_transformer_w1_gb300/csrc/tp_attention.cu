@@ -679,7 +679,8 @@ __global__ void __launch_bounds__(NT, 1) attn_dq_kernel(const __grid_constant__ 
   uint64_t* sdp_full = bar + 14;
   uint64_t* sdp_empty = bar + 15;
   uint64_t* ds_full = bar + 16;
-  uint64_t* ds_free = bar + 17;
+  // (bar + 17 unused: the dS buffer is free once the previous block's dQ
+  // product has read it, and that product's commit frees its K stage too)
   uint64_t* dq_full = bar + 18;
   uint64_t* dq_empty = bar + 19;
   uint64_t* drain = bar + 20;
@@ -699,7 +700,6 @@ __global__ void __launch_bounds__(NT, 1) attn_dq_kernel(const __grid_constant__ 
     mbar_init(sdp_full, 1);
     mbar_init(sdp_empty, NSW);
     mbar_init(ds_full, NSW);
-    mbar_init(ds_free, 1);
     mbar_init(dq_full, 1);
     mbar_init(dq_empty, NSW);
     mbar_init(drain, 1);
@@ -807,8 +807,7 @@ __global__ void __launch_bounds__(NT, 1) attn_dq_kernel(const __grid_constant__ 
 #pragma unroll
           for (int ks = 0; ks < 8; ++ks)
             umma_bf16(tmem + DQ_ACC, kdesc(dsa, 128, ks), mndesc(ka, 128, ks), ID_DQ, (j > 0 || ks > 0) ? 1u : 0u);
-          umma_commit(&k_empty[st]);
-          umma_commit(ds_free);
+          umma_commit(&k_empty[st]);  // also tells the softmax warps the dS buffer is free
           BW_ADD(0, 5, t5);
         }
         if (!ok) break;
@@ -892,7 +891,7 @@ __global__ void __launch_bounds__(NT, 1) attn_dq_kernel(const __grid_constant__ 
         tc_fence_before();
         warp_arrive(sdp_empty);  // S and dP read: the next block's products may start
         // dS buffer free once the previous block's dQ has read it
-        if (blk > 0 && !W.warp(ds_free, (blk - 1) & 1u)) { ok = false; break; }
+        if (blk > 0 && !W.warp(&k_empty[(blk - 1) % DQ_KV], ((blk - 1) / DQ_KV) & 1u)) { ok = false; break; }
 #pragma unroll
         for (int c8 = 0; c8 < 8; ++c8)
           st_shared_v4(sw_chunk(dst, 128, row, half * 8 + c8), pk[4 * c8], pk[4 * c8 + 1], pk[4 * c8 + 2],
@@ -966,11 +965,9 @@ __global__ void __launch_bounds__(NT, 1) attn_dkdv_kernel(const __grid_constant_
   uint64_t* bar = reinterpret_cast<uint64_t*>(smem + V_BAR);
   uint64_t* kv_full = bar + 0;
   uint64_t* kv_empty = bar + 1;
-  uint64_t* q_full = bar + 2;                // [VST]
-  uint64_t* q_empty = q_full + VST;          // [VST]
-  uint64_t* do_full = q_empty + VST;         // [VST]
-  uint64_t* do_empty = do_full + VST;        // [VST]
-  uint64_t* sdp_full = do_empty + VST;
+  uint64_t* qdo_full = bar + 2;              // [VST] Q, dO, lse and D of a block landed
+  uint64_t* qdo_empty = qdo_full + VST;      // [VST] its dV / dK products completed
+  uint64_t* sdp_full = qdo_empty + VST;
   uint64_t* pd_full = sdp_full + 1;          // [2] one per half-block hand-over
   uint64_t* dkv_full = pd_full + 2;
   uint64_t* dkv_empty = dkv_full + 1;
@@ -984,10 +981,8 @@ __global__ void __launch_bounds__(NT, 1) attn_dkdv_kernel(const __grid_constant_
     mbar_init(kv_full, 1);
     mbar_init(kv_empty, 1);
     for (int i = 0; i < VST; ++i) {
-      mbar_init(&q_full[i], 1);
-      mbar_init(&q_empty[i], 1);
-      mbar_init(&do_full[i], 1);
-      mbar_init(&do_empty[i], 1);
+      mbar_init(&qdo_full[i], 1);
+      mbar_init(&qdo_empty[i], 1);
     }
     mbar_init(sdp_full, 1);
     mbar_init(&pd_full[0], NSW);
@@ -1015,8 +1010,8 @@ __global__ void __launch_bounds__(NT, 1) attn_dkdv_kernel(const __grid_constant_
 
   if (warp == 0) {
     if (lane == 0) {
-      int kv_last = -1, q_last[VST], do_last[VST];
-      for (int i = 0; i < VST; ++i) q_last[i] = do_last[i] = -1;
+      int kv_last = -1, q_last[VST];
+      for (int i = 0; i < VST; ++i) q_last[i] = -1;
       uint32_t qc = 0, it = 0;
       bool ok = true;
       for (int item = blockIdx.x; item < p.items && ok; item += gridDim.x, ++it) {
@@ -1039,28 +1034,23 @@ __global__ void __launch_bounds__(NT, 1) attn_dkdv_kernel(const __grid_constant_
           for (int i = i0; i < p.n_qb; ++i, ++qc) {
             const int st = qc % VST;
             const uint32_t ph = (qc / VST) & 1u;
-            if (!W(&q_empty[st], ph ^ 1u)) { ok = false; break; }
+            if (!W(&qdo_empty[st], ph ^ 1u)) { ok = false; break; }
             uint8_t* qd = smem + V_Q + st * TILE;
-            mbar_arrive_expect_tx(&q_full[st], TILE + 1024);
-            tma_load_3d(qd, &tq128, &q_full[st], qcol, i * 128, b);
-            tma_load_3d(qd + TILE / 2, &tq128, &q_full[st], qcol + 64, i * 128, b);
-            bulk_g2s(vec + st * 256, lse_row + i * 128, 512, &q_full[st]);
-            bulk_g2s(vec + st * 256 + 128, d_row + i * 128, 512, &q_full[st]);
-            q_last[st] = static_cast<int>(ph);
-            if (!W(&do_empty[st], ph ^ 1u)) { ok = false; break; }
             uint8_t* dd = smem + V_DO + st * TILE;
-            mbar_arrive_expect_tx(&do_full[st], TILE);
-            tma_load_3d(dd, &tdo128, &do_full[st], h * HD, i * 128, b);
-            tma_load_3d(dd + TILE / 2, &tdo128, &do_full[st], h * HD + 64, i * 128, b);
-            do_last[st] = static_cast<int>(ph);
+            mbar_arrive_expect_tx(&qdo_full[st], 2 * TILE + 1024);
+            tma_load_3d(qd, &tq128, &qdo_full[st], qcol, i * 128, b);
+            tma_load_3d(qd + TILE / 2, &tq128, &qdo_full[st], qcol + 64, i * 128, b);
+            bulk_g2s(vec + st * 256, lse_row + i * 128, 512, &qdo_full[st]);
+            bulk_g2s(vec + st * 256 + 128, d_row + i * 128, 512, &qdo_full[st]);
+            tma_load_3d(dd, &tdo128, &qdo_full[st], h * HD, i * 128, b);
+            tma_load_3d(dd + TILE / 2, &tdo128, &qdo_full[st], h * HD + 64, i * 128, b);
+            q_last[st] = static_cast<int>(ph);
           }
         }
       }
       if (kv_last >= 0) W.drain(kv_full, static_cast<uint32_t>(kv_last));
-      for (int s2 = 0; s2 < VST; ++s2) {
-        if (q_last[s2] >= 0) W.drain(&q_full[s2], static_cast<uint32_t>(q_last[s2]));
-        if (do_last[s2] >= 0) W.drain(&do_full[s2], static_cast<uint32_t>(do_last[s2]));
-      }
+      for (int s2 = 0; s2 < VST; ++s2)
+        if (q_last[s2] >= 0) W.drain(&qdo_full[s2], static_cast<uint32_t>(q_last[s2]));
     }
     __syncwarp();
   } else if (warp == 1) {
@@ -1082,7 +1072,7 @@ __global__ void __launch_bounds__(NT, 1) attn_dkdv_kernel(const __grid_constant_
           const int st = n % VST;
           const uint32_t ph = (n / VST) & 1u;
           AT_T0(t0);
-          if (!W(&q_full[st], ph) || !W(&do_full[st], ph)) { ok = false; break; }
+          if (!W(&qdo_full[st], ph)) { ok = false; break; }
           BW_ADD(1, 0, t0);
           AT_T0(t1);
           tc_fence_after();
@@ -1121,8 +1111,7 @@ __global__ void __launch_bounds__(NT, 1) attn_dkdv_kernel(const __grid_constant_
             BW_ADD(1, 5, t5);
           }
           if (!ok) break;
-          umma_commit(&do_empty[st]);
-          umma_commit(&q_empty[st]);
+          umma_commit(&qdo_empty[st]);
         }
         if (!ok) break;
         umma_commit(dkv_full);
@@ -1163,7 +1152,7 @@ __global__ void __launch_bounds__(NT, 1) attn_dkdv_kernel(const __grid_constant_
 #endif
         AT_T0(t8);
         tc_fence_after();
-        if (!W.warp(&q_full[st], ph)) { ok = false; break; }  // lse / D of this block landed
+        if (!W.warp(&qdo_full[st], ph)) { ok = false; break; }  // lse / D of this block landed
         for (int c = 0; c < 2; ++c) {
           const int col = half * 64 + c * 32;  // first query of this piece within the block
           uint32_t rs[32], rp[32];
@@ -1267,7 +1256,7 @@ __global__ void pack_qkv_kernel(const __nv_bfloat16* Wq, const __nv_bfloat16* Wk
 // barrier areas (mbarriers + TMEM slot + abort flag) fit their reserved bytes
 static_assert(F_SMEM - F_BAR - 1024 >= 33 * 8 + 8, "forward barrier area");
 static_assert(Q_SMEM - Q_BAR - 1024 >= 21 * 8 + 8, "dq barrier area");
-static_assert(V_SMEM - V_BAR - 1024 >= (8 + 4 * VST) * 8 + 8, "dk/dv barrier area");
+static_assert(V_SMEM - V_BAR - 1024 >= (8 + 2 * VST) * 8 + 8, "dk/dv barrier area");
 static_assert(F_SMEM <= 232448 && Q_SMEM <= 232448 && V_SMEM <= 232448, "shared memory per CTA");
 
 // ================================================================ host
