@@ -392,11 +392,15 @@ __global__ void __launch_bounds__(NT, 1) attn_fwd_kernel(const __grid_constant__
           const uint32_t buf = (sc + j) & 1u;
           tc_fence_after();
           const uint32_t ka = smem_u32(smem + F_K + st * TILE);
+          AT_T0(t19);
 #pragma unroll
           for (int ks = 0; ks < 8; ++ks)
             umma_bf16(tmem + buf * 128, kdesc(qa, 128, ks), kdesc(ka, 128, ks), ID_S, ks > 0 ? 1u : 0u);
+          AT_ADD(19, t19);
+          AT_T0(t20);
           umma_commit(&s_full[buf]);
           if (j == nkb - 1) umma_commit(&q_empty[qbuf]);  // Q free once the item's last S is done
+          AT_ADD(20, t20);
           return true;
         };
         if (!issue_s(0)) break;
@@ -418,11 +422,15 @@ __global__ void __launch_bounds__(NT, 1) attn_fwd_kernel(const __grid_constant__
           const uint32_t va = smem_u32(smem + F_V + st * TILE);
           // key half kh: its P over the first 32 of S columns [64 kh, 64 kh + 64), into O_kh
           const uint32_t pa = tmem + ((sc + j) & 1u) * 128;
+          AT_T0(t21);
 #pragma unroll
           for (int ks = 0; ks < 8; ++ks)
             umma_bf16_ta(tmem + 256 + (ks >> 2) * 128, pa + (ks >> 2) * 64 + (ks & 3) * 8, mndesc(va, 128, ks),
                          ID_PV, (j > 0 || (ks & 3) > 0) ? 1u : 0u);
+          AT_ADD(21, t21);
+          AT_T0(t22);
           umma_commit(&pv_done[pg & 1u]);
+          AT_ADD(22, t22);
           ++pg;
         }
         kv += nkb;
