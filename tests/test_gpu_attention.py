@@ -128,6 +128,36 @@ def test_attention_core_matches_oracle(case):
     both(to_f64(dv), dv_ref, "dv", a_dv)
 
 
+def test_attention_forward_lazy_rescale_path():
+    """Keys whose scale grows along the sequence make each row's running
+    maximum (per 64-key half of a 128-key block, in log2 units) rise by more
+    than 2^8 after its first block, so the forward's lazy rescale of its O
+    accumulators runs; checked on the inputs before the comparison."""
+    B, S, H, Hkv, T = 1, 512, 2, 2, 1
+    inp = make_core_inputs(B, S, H, Hkv, HD, seed=77, q_scale=2.0)
+    ramp = torch.from_numpy(1.0 + 3.0 * np.arange(S, dtype=np.float64) / S).to(torch.float32)[:, None]
+    inp["k"] = (inp["k"].to(torch.float32) * ramp).to(torch.bfloat16)
+    q64, k64, v64, dO64 = (to_f64(inp[n]) for n in ("q", "k", "v", "dO"))
+    scale_log2 = math.log2(math.e) / math.sqrt(HD)
+    rises = 0
+    for hh in range(H):
+        sc = q64[:, hh * HD:(hh + 1) * HD] @ k64[:, hh * HD:(hh + 1) * HD].T * scale_log2  # [S, S]
+        for half in range(2):
+            blk = np.stack([sc[:, j * 128 + half * 64:j * 128 + half * 64 + 64].max(1) for j in range(S // 128)], 1)
+            rises += int((np.maximum.accumulate(blk, 1)[:, 1:] > blk[:, :1] + 8.0).any(1).sum())
+    assert rises > 0, "the inputs do not exercise the lazy rescale"
+    attn = _attn_mod()(d=128, n_heads=H, n_kv_heads=Hkv, head_dim=HD, T_p=T, causal=False)
+    qkv = pack_qkv(inp["q"], inp["k"], inp["v"], H, Hkv, T).cuda()
+    o, lse = attn.core_forward(qkv, B, S)
+    torch.cuda.synchronize()
+    core = oracle.AttentionCore(B, S, H, Hkv, HD, causal=False, round_bf16=True)
+    o_ref, lse_ref = core.forward(q64, k64, v64)
+    a_o, _, _, _ = core.allowance(q64, k64, v64, dO64, U)
+    both(to_f64(o.cpu()), o_ref, "o", a_o)
+    lse_nat = lse.cpu().double().numpy()[:, :S].reshape(B, H, S) * math.log(2.0)
+    check(lse_nat, lse_ref, F32_REL, "lse")
+
+
 SUB_CASES = [  # B, S, d, H, Hkv, T_p, causal, fused
     (2, 160, 256, 4, 2, 2, True, False),
     (2, 160, 256, 4, 2, 2, True, True),
