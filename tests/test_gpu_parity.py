@@ -80,6 +80,32 @@ def test_small_bf16_against_full_oracle(w, fused):
     _full_compare(w, fused)
 
 
+def _sweep_cases(n=10, seed=20261202):
+    """Seeded random shapes across both kernel paths (token counts of at most
+    32, under 256 and above), both activations, biases on or off, ragged
+    d and hidden widths (multiples of 8), and T_p from 1 to 8."""
+    rng = np.random.default_rng(seed)
+    out = []
+    for i in range(n):
+        N = int(rng.choice([rng.integers(1, 33), rng.integers(33, 256), rng.integers(256, 700)]))
+        d = 8 * int(rng.integers(1, 41))
+        T = int(rng.choice([1, 2, 3, 4, 5, 8]))
+        s = 8 * int(rng.integers(1, 41))
+        act = "swiglu" if i % 2 else "gelu_tanh"
+        bias = act == "gelu_tanh" and bool(rng.integers(0, 2))
+        out.append(small_case(N, d, s * T, T, act, bias=bias, seed=300 + i))
+    return out
+
+
+SWEEP = _sweep_cases()
+
+
+@pytest.mark.parametrize("fused", [False, True], ids=["standalone", "fused"])
+@pytest.mark.parametrize("w", SWEEP, ids=[w.name for w in SWEEP])
+def test_seeded_shape_sweep_against_full_oracle(w, fused):
+    _full_compare(w, fused)
+
+
 def _attn_case(N, d_model, n_heads, head_dim, T_p, seed):
     return Workload(f"attn_out_{N}x{d_model}_h{n_heads}x{head_dim}_tp{T_p}", N, d_model, n_heads * head_dim, T_p,
                     "none", "bf16", seed_index=seed, n_heads=n_heads, n_kv_heads=n_heads, head_dim=head_dim)
