@@ -103,6 +103,24 @@ CORE_CASES = [  # B, S, H, Hkv, T_p, causal, q_scale
 ]
 
 
+def _core_sweep(n=6, seed=20261203):
+    """Seeded random attention-core shapes: sequence lengths across tile
+    boundaries, GQA groups of 1 to 4, T_p dividing the key/value heads,
+    causal or not, and sharper or flatter softmaxes."""
+    rng = np.random.default_rng(seed)
+    out = []
+    for _ in range(n):
+        Hkv = int(rng.choice([1, 2, 4]))
+        G = int(rng.choice([1, 2, 4]))
+        T = int(rng.choice([t for t in (1, 2, 4) if Hkv % t == 0]))
+        out.append((int(rng.integers(1, 4)), int(rng.integers(1, 600)), Hkv * G, Hkv, T, bool(rng.integers(0, 2)),
+                    float(rng.choice([0.5, 1.0, 2.0, 3.0]))))
+    return out
+
+
+CORE_CASES = CORE_CASES + _core_sweep()
+
+
 @pytest.mark.parametrize("case", CORE_CASES, ids=lambda c: "B%d_S%d_H%d_kv%d_tp%d_%s_q%g" % (
     c[0], c[1], c[2], c[3], c[4], "causal" if c[5] else "full", c[6]))
 def test_attention_core_matches_oracle(case):
