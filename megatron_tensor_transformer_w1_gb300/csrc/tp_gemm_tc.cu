@@ -333,6 +333,11 @@ __global__ void __launch_bounds__(threads_for<EPI>(), 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
+  // launched as a programmatic dependent of the previous kernel (decode-sized
+  // GEMMs): everything above overlapped its tail; no global memory is touched
+  // before its results are visible
+  grid_dep_launch();
+  grid_dep_wait();
 
   const int num_tiles = p.tiles_m * p.tiles_n * p.NB;
   const int k_iters = p.G * p.k_blocks;
@@ -1145,7 +1150,17 @@ static int launch_inst(const GemmSpec& s, LaunchCtx& ctx) {
     grid = static_cast<int>((tiles + waves - 1) / waves);
   }
   if (ctx.before) ctx.before(ctx.user, s.name, ctx.stream);
-  kern<<<grid, threads_for<EPI>(), L::SMEM, ctx.stream>>>(ta, tb, p);
+  cudaLaunchConfig_t cfg{};
+  cfg.gridDim = dim3(static_cast<unsigned>(grid));
+  cfg.blockDim = dim3(threads_for<EPI>());
+  cfg.dynamicSmemBytes = L::SMEM;
+  cfg.stream = ctx.stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  if (cudaLaunchKernelEx(&cfg, kern, ta, tb, p) != cudaSuccess) return TP_ERR_CUDA;
   if (ctx.after) ctx.after(ctx.user, ctx.stream);
   ctx.launches++;
   return cudaPeekAtLastError() == cudaSuccess ? 0 : TP_ERR_CUDA;

@@ -105,6 +105,8 @@ template <int OUT_BF16>
 __global__ void __launch_bounds__(256) shard_sum_vec8_kernel(const float* __restrict__ P, int T, long long plane,
                                                              long long cols, const __nv_bfloat16* bias_bf,
                                                              const float* bias_f, void* out, long long stride) {
+  // a programmatic dependent of the GEMM that wrote the partials
+  asm volatile("griddepcontrol.wait;" ::: "memory");
   const long long n8 = plane / 8;
   for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < n8; i += (long long)gridDim.x * blockDim.x) {
     const float4* p0 = reinterpret_cast<const float4*>(P) + 2 * i;
@@ -473,6 +475,23 @@ int launch_pack_rows(const void* W2, void* out, int T_p, int64_t s, int64_t s_pa
   return cudaPeekAtLastError() == cudaSuccess ? 0 : TP_ERR_CUDA;
 }
 
+// Launch as a programmatic dependent of the stream's previous kernel (the
+// kernel waits for its results with griddepcontrol.wait).
+template <typename... KArgs, typename... Args>
+static void launch_pdl(void (*kern)(KArgs...), int grid, int block, cudaStream_t stream, Args... args) {
+  cudaLaunchConfig_t cfg{};
+  cfg.gridDim = dim3(static_cast<unsigned>(grid));
+  cfg.blockDim = dim3(static_cast<unsigned>(block));
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  cudaLaunchKernelEx(&cfg, kern, static_cast<KArgs>(args)...);
+}
+
 int launch_shard_sum(const float* partials, int T_p, int64_t rows, int64_t cols, const void* bias, void* out,
                      int out_bf16, LaunchCtx& ctx, const char* name, int64_t shard_stride) {
   const long long plane = (long long)rows * cols;
@@ -484,12 +503,11 @@ int launch_shard_sum(const float* partials, int T_p, int64_t rows, int64_t cols,
   if (vec) {
     const int grid = grid_for(plane / 8, 256, ctx.num_sms);
     if (out_bf16)
-      shard_sum_vec8_kernel<1><<<grid, 256, 0, ctx.stream>>>(partials, T_p, plane, cols,
-                                                            static_cast<const __nv_bfloat16*>(bias), nullptr, out,
-                                                            stride);
+      launch_pdl(shard_sum_vec8_kernel<1>, grid, 256, ctx.stream, partials, T_p, plane, cols,
+                 static_cast<const __nv_bfloat16*>(bias), static_cast<const float*>(nullptr), out, stride);
     else
-      shard_sum_vec8_kernel<0><<<grid, 256, 0, ctx.stream>>>(partials, T_p, plane, cols, nullptr,
-                                                            static_cast<const float*>(bias), out, stride);
+      launch_pdl(shard_sum_vec8_kernel<0>, grid, 256, ctx.stream, partials, T_p, plane, cols,
+                 static_cast<const __nv_bfloat16*>(nullptr), static_cast<const float*>(bias), out, stride);
   } else {
     shard_sum_scalar_kernel<<<grid_for(plane, 256, ctx.num_sms), 256, 0, ctx.stream>>>(
         partials, T_p, plane, cols, bias, out_bf16, out, out_bf16, stride);
