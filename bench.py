@@ -53,8 +53,8 @@ NCU_TRAFFIC = {
 # The same for the decode-sized forward (Llama-3-70B shapes, 32 tokens,
 # one-SM kernel with 32-row A tiles); same profile file.
 NCU_TRAFFIC_DECODE = {
-    "up_swiglu": 940.65e6 + 4.42e6,
-    "down_partials": 471.64e6 + 4.32e6,
+    "up_swiglu": 940.62e6 + 4.36e6,
+    "down_partials": 471.63e6 + 4.32e6,
 }
 
 
