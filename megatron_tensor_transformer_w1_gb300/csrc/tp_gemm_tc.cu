@@ -681,6 +681,11 @@ __global__ void __launch_bounds__(threads_for<EPI>(), 1)
   cluster_sync();  // barriers of both CTAs initialised before any remote arrive
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
+  // a programmatic dependent of the previous kernel: the set-up above
+  // overlapped its tail; no global memory is touched before its results are
+  // visible
+  grid_dep_launch();
+  grid_dep_wait();
 
   const int tiles_m2 = (p.tiles_m + 1) >> 1;
   const int num_tiles = tiles_m2 * p.tiles_n * p.NB;
@@ -1247,16 +1252,18 @@ static int launch_pair(const GemmSpec& s, LaunchCtx& ctx) {
     attr_done.fetch_or(bit);
   }
   cudaLaunchConfig_t cfg{};
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeClusterDimension;
   attr[0].val.clusterDim.x = 2;
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.blockDim = dim3(threads_for<EPI>(), 1, 1);
   cfg.dynamicSmemBytes = L::SMEM;
   cfg.stream = ctx.stream;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = 2;
   int mc = max_clusters[dev & 31].load();
   if (mc <= 0) {
     cfg.gridDim = dim3(2 * (ctx.num_sms / 2), 1, 1);
