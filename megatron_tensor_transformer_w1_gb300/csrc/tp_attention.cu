@@ -1092,6 +1092,8 @@ __global__ void __launch_bounds__(NT, 1) attn_dkdv_kernel(const __grid_constant_
           for (int ks = 0; ks < 8; ++ks)
             umma_bf16(tmem + 128, kdesc(va, 128, ks), kdesc(da, 128, ks), ID_S, ks > 0 ? 1u : 0u);
           umma_commit(sdp_full);
+          // K and V are read only by S^T / dP^T: the next item's copies may start
+          if (t == n_it - 1) umma_commit(kv_empty);
           BW_ADD(1, 1, t1);
           AT_T0(t3);
           if (t == 0 && !W(dkv_empty, (it & 1u) ^ 1u)) { ok = false; break; }
@@ -1123,7 +1125,6 @@ __global__ void __launch_bounds__(NT, 1) attn_dkdv_kernel(const __grid_constant_
         }
         if (!ok) break;
         umma_commit(dkv_full);
-        umma_commit(kv_empty);
         qc += n_it;
         sc += n_it;
       }
