@@ -834,8 +834,30 @@ __global__ void __launch_bounds__(NT, 1) attn_dq_kernel(const __grid_constant__ 
     const int row = quarter * 32 + lane;
     const uint32_t tl = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
     const uint32_t dst = smem_u32(smem + Q_DS);
+    // Q and dO of work item `item` (the it-th of this CTA) into tensor
+    // memory, once the previous item's products no longer read them; done
+    // for the next item before this one's dQ is written out, so the next
+    // item's first S / dP products run during that write-out
+    auto copy_qdo = [&](int item, uint32_t it) -> bool {
+      int qb, b, h;
+      decode_item(p, item, p.H, p.causal != 0, qb, b, h);
+      const int qpos = qb * 128 + row;
+      if (!W.warp(qdo_free, (it & 1u) ^ 1u)) return false;
+      tc_fence_after();
+      const long long tok = static_cast<long long>(b) * p.S + qpos;
+      uint32_t r[32];
+      load_row_pairs(p.dqkv_src + tok * p.dqkv_rs + p.g.qcol(h) + half * 64, qpos < p.S, r);
+      tmem_st32(tl + DQ_QA + half * 32, r);
+      load_row_pairs(p.dO + tok * p.do_rs + h * HD + half * 64, qpos < p.S, r);
+      tmem_st32(tl + DQ_DOA + half * 32, r);
+      tmem_wait_st();
+      tc_fence_before();
+      warp_arrive(qdo_ready);
+      return true;
+    };
     uint32_t it = 0, blk = 0;
-    for (int item = blockIdx.x; item < p.items; item += gridDim.x, ++it) {
+    const bool started = static_cast<int>(blockIdx.x) >= p.items || copy_qdo(blockIdx.x, 0);
+    for (int item = blockIdx.x; started && item < p.items; item += gridDim.x, ++it) {
       int qb, b, h;
       decode_item(p, item, p.H, p.causal != 0, qb, b, h);
       const int nkb = nkb_of(qb);
@@ -845,21 +867,6 @@ __global__ void __launch_bounds__(NT, 1) attn_dq_kernel(const __grid_constant__ 
       // rows past the sequence read lse = +inf (written by the forward): p = 0
       const float lse_r = p.lse[vrow];
       const float ds_off = p.Dv[vrow] * p.scale;
-      // Q and dO of this row into tensor memory, once the previous item's
-      // products no longer read them
-      if (!W.warp(qdo_free, (it & 1u) ^ 1u)) break;
-      tc_fence_after();
-      {
-        const long long tok = static_cast<long long>(b) * p.S + qpos;
-        uint32_t r[32];
-        load_row_pairs(p.dqkv_src + tok * p.dqkv_rs + p.g.qcol(h) + half * 64, row_ok, r);
-        tmem_st32(tl + DQ_QA + half * 32, r);
-        load_row_pairs(p.dO + tok * p.do_rs + h * HD + half * 64, row_ok, r);
-        tmem_st32(tl + DQ_DOA + half * 32, r);
-        tmem_wait_st();
-      }
-      tc_fence_before();
-      warp_arrive(qdo_ready);
       bool ok = true;
       for (int j = 0; j < nkb; ++j, ++blk) {
         AT_T0(t7);
@@ -912,6 +919,7 @@ __global__ void __launch_bounds__(NT, 1) attn_dq_kernel(const __grid_constant__ 
 #endif
       }
       if (!ok) break;
+      if (item + static_cast<int>(gridDim.x) < p.items && !copy_qdo(item + gridDim.x, it + 1)) break;
       if (!W.warp(dq_full, it & 1u)) break;
       tc_fence_after();
       __nv_bfloat16* out =
