@@ -372,40 +372,59 @@ __global__ void __launch_bounds__(NT, 1) attn_fwd_kernel(const __grid_constant__
     if (lane == 0) {
       constexpr uint32_t ID_S = idesc(128, 0, 0);   // S = Q K^T
       constexpr uint32_t ID_PV = idesc(128, 0, 1);  // O += P V (V: N = hd contiguous)
-      uint32_t kv = 0, sc = 0, pg = 0, it = 0;
+      uint32_t kv = 0, pg = 0, it = 0;
       bool ok = true;
       AT_T0(t_mma);
+      // S = Q K^T of K/V block n (the n-th block of this CTA, all items in
+      // turn) into S buffer n & 1; `last`: the item's last block, after which
+      // its Q buffer is free
+      auto issue_s = [&](uint32_t n, uint32_t qa, bool last, int qbuf) -> bool {
+        const int st = n & 1;
+        AT_T0(t0);
+        if (!W(&k_full[st], (n >> 1) & 1u)) return false;
+        AT_ADD(0, t0);
+        tc_fence_after();
+        const uint32_t ka = smem_u32(smem + F_K + st * TILE);
+        AT_T0(t19);
+#pragma unroll
+        for (int ks = 0; ks < 8; ++ks)
+          umma_bf16(tmem + (n & 1u) * 128, kdesc(qa, 128, ks), kdesc(ka, 128, ks), ID_S, ks > 0 ? 1u : 0u);
+        AT_ADD(19, t19);
+        AT_T0(t20);
+        umma_commit(&s_full[n & 1u]);
+        if (last) umma_commit(&q_empty[qbuf]);  // Q free once the item's last S is done
+        AT_ADD(20, t20);
+        return true;
+      };
+      auto q_addr = [&](int qbuf) { return smem_u32(smem + F_Q + qbuf * TILE); };
+      bool s0_issued = false;  // this item's first S went out during the previous item
       for (int item = blockIdx.x; item < p.items && ok; item += gridDim.x, ++it) {
         int qb, b, h;
         decode_item(p, item, p.H, p.causal != 0, qb, b, h);
         const int nkb = p.causal ? qb + 1 : p.n_qb;
         const int qbuf = it & 1;
-        if (!W(&q_full[qbuf], (it >> 1) & 1u)) break;
-        tc_fence_after();
-        const uint32_t qa = smem_u32(smem + F_Q + qbuf * TILE);
-        auto issue_s = [&](int j) -> bool {
-          const uint32_t n = kv + j;
-          const int st = n & 1;
-          AT_T0(t0);
-          if (!W(&k_full[st], (n >> 1) & 1u)) return false;
-          AT_ADD(0, t0);
-          const uint32_t buf = (sc + j) & 1u;
+        if (!s0_issued) {
+          if (!W(&q_full[qbuf], (it >> 1) & 1u)) break;
           tc_fence_after();
-          const uint32_t ka = smem_u32(smem + F_K + st * TILE);
-          AT_T0(t19);
-#pragma unroll
-          for (int ks = 0; ks < 8; ++ks)
-            umma_bf16(tmem + buf * 128, kdesc(qa, 128, ks), kdesc(ka, 128, ks), ID_S, ks > 0 ? 1u : 0u);
-          AT_ADD(19, t19);
-          AT_T0(t20);
-          umma_commit(&s_full[buf]);
-          if (j == nkb - 1) umma_commit(&q_empty[qbuf]);  // Q free once the item's last S is done
-          AT_ADD(20, t20);
-          return true;
-        };
-        if (!issue_s(0)) break;
+          if (!issue_s(kv, q_addr(qbuf), nkb == 1, qbuf)) break;
+        }
+        s0_issued = false;
+        const uint32_t qa = q_addr(qbuf);
         for (int j = 0; j < nkb; ++j) {
-          if (j + 1 < nkb && !issue_s(j + 1)) { ok = false; break; }
+          if (j + 1 < nkb) {
+            if (!issue_s(kv + j + 1, qa, j + 2 == nkb, qbuf)) { ok = false; break; }
+          } else if (item + static_cast<int>(gridDim.x) < p.items) {
+            // the next item's first S, ahead of this item's last PV: the
+            // softmax warps take it before they read this item's O out
+            int qb2, b2, h2;
+            decode_item(p, item + gridDim.x, p.H, p.causal != 0, qb2, b2, h2);
+            const int nkb2 = p.causal ? qb2 + 1 : p.n_qb;
+            const int qbuf2 = (it + 1) & 1;
+            if (!W(&q_full[qbuf2], ((it + 1) >> 1) & 1u)) { ok = false; break; }
+            tc_fence_after();
+            if (!issue_s(kv + nkb, q_addr(qbuf2), nkb2 == 1, qbuf2)) { ok = false; break; }
+            s0_issued = true;
+          }
           AT_T0(t2);
           if (!W(&p_full[pg & 1u], (pg >> 1) & 1u)) { ok = false; break; }
           AT_ADD(2, t2);
@@ -421,7 +440,7 @@ __global__ void __launch_bounds__(NT, 1) attn_fwd_kernel(const __grid_constant__
           tc_fence_after();
           const uint32_t va = smem_u32(smem + F_V + st * TILE);
           // key half kh: its P over the first 32 of S columns [64 kh, 64 kh + 64), into O_kh
-          const uint32_t pa = tmem + ((sc + j) & 1u) * 128;
+          const uint32_t pa = tmem + (n & 1u) * 128;
           AT_T0(t21);
 #pragma unroll
           for (int ks = 0; ks < 8; ++ks)
@@ -434,7 +453,6 @@ __global__ void __launch_bounds__(NT, 1) attn_fwd_kernel(const __grid_constant__
           ++pg;
         }
         kv += nkb;
-        sc += nkb;
       }
       AT_ADD(5, t_mma);
       umma_commit(drain);  // all issued MMAs complete before tensor memory is released
@@ -461,114 +479,150 @@ __global__ void __launch_bounds__(NT, 1) attn_fwd_kernel(const __grid_constant__
       ++xe;
       return true;
     };
-    uint32_t sc = 0, pg = 0, it = 0;
+    uint32_t sc = 0, pg = 0;
 #ifdef TPFFN_INSTRUMENT
     const bool rec = warp == 2 && lane == 0;
     const long long t_sm = clock64();
 #endif
-    for (int item = blockIdx.x; item < p.items; item += gridDim.x, ++it) {
-      int qb, b, h;
-      decode_item(p, item, p.H, p.causal != 0, qb, b, h);
-      const int nkb = p.causal ? qb + 1 : p.n_qb;
+    // Each item's O is read out after the next item's block 0 (the MMA thread
+    // issued that S ahead of the item's last PV), so that the tensor pipe
+    // has the next P block during the read-out; a final pass without blocks
+    // reads out the last item.
+    bool pend = false;  // a read-out is pending
+    float pf0 = 0.f, pf1 = 0.f, pinv = 1.f, plse = 0.f;
+    int pb = 0, ph = 0, pqpos = 0;
+    uint32_t pglast = 0;
+    for (int item = blockIdx.x;; item += gridDim.x) {
+      const bool has = item < p.items;
+      int qb = 0, b = 0, h = 0;
+      if (has) decode_item(p, item, p.H, p.causal != 0, qb, b, h);
+      const int nkb = !has ? 1 : (p.causal ? qb + 1 : p.n_qb);
       const int qpos = qb * 128 + row;
       float m_used = -INFINITY, l = 0.f;  // this key half's running maximum (log2 units) and row sum
       bool ok = true;
       for (int j = 0; j < nkb; ++j) {
-        const uint32_t buf = sc & 1u, use = sc >> 1;
-        ++sc;
-        AT_T0(t7);
-        if (!W.warp(&s_full[buf], use & 1u)) { ok = false; break; }
+        if (has) {
+          const uint32_t g = pg + j;
+          const uint32_t buf = sc & 1u, use = sc >> 1;
+          ++sc;
+          AT_T0(t7);
+          if (!W.warp(&s_full[buf], use & 1u)) { ok = false; break; }
 #ifdef TPFFN_INSTRUMENT
-        if (rec) AT_ADD(7, t7);
+          if (rec) AT_ADD(7, t7);
 #endif
-        AT_T0(t8);
-        tc_fence_after();
-        uint32_t r[64];
-        tmem_ld32(tl + buf * 128 + half * 64, *reinterpret_cast<uint32_t(*)[32]>(&r[0]));
-        tmem_ld32(tl + buf * 128 + half * 64 + 32, *reinterpret_cast<uint32_t(*)[32]>(&r[32]));
-        tmem_wait_ld();
-#ifdef TPFFN_INSTRUMENT
-        if (rec) AT_ADD(8, t8);
-#endif
-        AT_T0(t9);
-        const int kbase = j * 128 + half * 64;
-        // only the diagonal block (causal) and a block past the end of the
-        // sequence hold invisible keys; elsewhere every key is visible
-        if ((p.causal && j * 128 + 127 > qb * 128) || j * 128 + 128 > p.S) {
-#pragma unroll
-          for (int c = 0; c < 64; ++c) {
-            const int key = kbase + c;
-            const bool vis = key < p.S && (!p.causal || key <= qpos);
-            r[c] = vis ? r[c] : __float_as_uint(-INFINITY);
-          }
-        }
-        // this half's maximum of the raw scores: eight chains
-        float m8[8];
-#pragma unroll
-        for (int c = 0; c < 8; ++c) m8[c] = __uint_as_float(r[c]);
-#pragma unroll
-        for (int c = 8; c < 64; ++c) m8[c & 7] = fmaxf(m8[c & 7], __uint_as_float(r[c]));
-        const float mh = fmaxf(fmaxf(fmaxf(m8[0], m8[1]), fmaxf(m8[2], m8[3])),
-                               fmaxf(fmaxf(m8[4], m8[5]), fmaxf(m8[6], m8[7])));
-#ifdef TPFFN_INSTRUMENT
-        if (rec) AT_ADD(9, t9);
-#endif
-        const float mx = mh * p.scale_log2;
-        float alpha = 1.f;
-        bool rescale = false;
-        if (m_used == -INFINITY) {
-          m_used = mx;  // first visible key of this half (O and l are still zero)
-        } else if (mx > m_used + 8.f) {  // lazy rescale: p stays <= 2^8 otherwise
-          alpha = ex2(m_used - mx);
-          m_used = mx;
-          rescale = true;
-        }
-        const uint32_t g = pg + j;
-        if (__any_sync(0xffffffffu, rescale)) {
-          // O_half must hold PV g-1 before it is rescaled
-          const uint32_t gp = g - 1;
-          if (!W.warp(&pv_done[gp & 1u], (gp >> 1) & 1u)) { ok = false; break; }
+          AT_T0(t8);
           tc_fence_after();
+          uint32_t r[64];
+          tmem_ld32(tl + buf * 128 + half * 64, *reinterpret_cast<uint32_t(*)[32]>(&r[0]));
+          tmem_ld32(tl + buf * 128 + half * 64 + 32, *reinterpret_cast<uint32_t(*)[32]>(&r[32]));
+          tmem_wait_ld();
+#ifdef TPFFN_INSTRUMENT
+          if (rec) AT_ADD(8, t8);
+#endif
+          AT_T0(t9);
+          const int kbase = j * 128 + half * 64;
+          // only the diagonal block (causal) and a block past the end of the
+          // sequence hold invisible keys; elsewhere every key is visible
+          if ((p.causal && j * 128 + 127 > qb * 128) || j * 128 + 128 > p.S) {
+#pragma unroll
+            for (int c = 0; c < 64; ++c) {
+              const int key = kbase + c;
+              const bool vis = key < p.S && (!p.causal || key <= qpos);
+              r[c] = vis ? r[c] : __float_as_uint(-INFINITY);
+            }
+          }
+          // this half's maximum of the raw scores: eight chains
+          float m8[8];
+#pragma unroll
+          for (int c = 0; c < 8; ++c) m8[c] = __uint_as_float(r[c]);
+#pragma unroll
+          for (int c = 8; c < 64; ++c) m8[c & 7] = fmaxf(m8[c & 7], __uint_as_float(r[c]));
+          const float mh = fmaxf(fmaxf(fmaxf(m8[0], m8[1]), fmaxf(m8[2], m8[3])),
+                                 fmaxf(fmaxf(m8[4], m8[5]), fmaxf(m8[6], m8[7])));
+#ifdef TPFFN_INSTRUMENT
+          if (rec) AT_ADD(9, t9);
+#endif
+          const float mx = mh * p.scale_log2;
+          float alpha = 1.f;
+          bool rescale = false;
+          if (m_used == -INFINITY) {
+            m_used = mx;  // first visible key of this half (O and l are still zero)
+          } else if (mx > m_used + 8.f) {  // lazy rescale: p stays <= 2^8 otherwise
+            alpha = ex2(m_used - mx);
+            m_used = mx;
+            rescale = true;
+          }
+          if (__any_sync(0xffffffffu, rescale)) {
+            // O_half must hold PV g-1 before it is rescaled
+            const uint32_t gp = g - 1;
+            if (!W.warp(&pv_done[gp & 1u], (gp >> 1) & 1u)) { ok = false; break; }
+            tc_fence_after();
 #pragma unroll 1
-          for (int c = 0; c < 4; ++c) {
-            uint32_t o[32];
-            const uint32_t ta = tl + 256 + half * 128 + c * 32;
-            tmem_ld32(ta, o);
+            for (int c = 0; c < 4; ++c) {
+              uint32_t o[32];
+              const uint32_t ta = tl + 256 + half * 128 + c * 32;
+              tmem_ld32(ta, o);
+              tmem_wait_ld();
+#pragma unroll
+              for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
+              tmem_st32(ta, o);
+            }
+            tmem_wait_st();
+          }
+          // P (bf16 pairs) over the first 32 of this half's 64 S columns, which
+          // this thread has already read
+          AT_T0(t12);
+          const float neg_m = m_used == -INFINITY ? 0.f : -m_used;  // no visible key yet: every p is 0
+          float l8[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+          uint32_t pk[32];
+#pragma unroll
+          for (int c = 0; c < 32; ++c) {
+            const float e0 = ex2(fmaf(__uint_as_float(r[2 * c]), p.scale_log2, neg_m));
+            const float e1 = ex2(fmaf(__uint_as_float(r[2 * c + 1]), p.scale_log2, neg_m));
+            l8[c & 7] += e0 + e1;
+            pk[c] = pack_bf16x2(e0, e1);
+          }
+          tmem_st32(tl + buf * 128 + half * 64, pk);
+          tmem_wait_st();
+          l = l * alpha + (((l8[0] + l8[1]) + (l8[2] + l8[3])) + ((l8[4] + l8[5]) + (l8[6] + l8[7])));
+          tc_fence_before();
+          warp_arrive(&p_full[g & 1u]);
+#ifdef TPFFN_INSTRUMENT
+          if (rec) {
+            AT_ADD(12, t12);
+            if (rescale) AT_CNT(13);
+          }
+#endif
+        }
+        if (j == 0 && pend) {
+          AT_T0(t14);
+          pend = false;
+          if (!W.warp(&pv_done[pglast & 1u], (pglast >> 1) & 1u)) { ok = false; break; }
+          tc_fence_after();
+          const bool row_ok = pqpos < p.S;
+          __nv_bfloat16* orow = p.o + (static_cast<long long>(pb) * p.S + pqpos) * p.o_rs + ph * HD + half * 64;
+#pragma unroll 1
+          for (int c = 0; c < 2; ++c) {
+            uint32_t o0[32], o1[32];
+            tmem_ld32(tl + 256 + half * 64 + c * 32, o0);
+            tmem_ld32(tl + 384 + half * 64 + c * 32, o1);
             tmem_wait_ld();
 #pragma unroll
-            for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
-            tmem_st32(ta, o);
+            for (int i = 0; i < 32; ++i)
+              o0[i] = __float_as_uint(fmaf(__uint_as_float(o0[i]), pf0, __uint_as_float(o1[i]) * pf1));
+            if (row_ok) store_row_bf16(orow + c * 32, o0, pinv);
           }
-          tmem_wait_st();
-        }
-        // P (bf16 pairs) over the first 32 of this half's 64 S columns, which
-        // this thread has already read
-        AT_T0(t12);
-        const float neg_m = m_used == -INFINITY ? 0.f : -m_used;  // no visible key yet: every p is 0
-        float l8[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-        uint32_t pk[32];
-#pragma unroll
-        for (int c = 0; c < 32; ++c) {
-          const float e0 = ex2(fmaf(__uint_as_float(r[2 * c]), p.scale_log2, neg_m));
-          const float e1 = ex2(fmaf(__uint_as_float(r[2 * c + 1]), p.scale_log2, neg_m));
-          l8[c & 7] += e0 + e1;
-          pk[c] = pack_bf16x2(e0, e1);
-        }
-        tmem_st32(tl + buf * 128 + half * 64, pk);
-        tmem_wait_st();
-        l = l * alpha + (((l8[0] + l8[1]) + (l8[2] + l8[3])) + ((l8[4] + l8[5]) + (l8[6] + l8[7])));
-        tc_fence_before();
-        warp_arrive(&p_full[g & 1u]);
+          // rows past the sequence get lse = +inf: the backward reads them as p = 0
+          if (half == 0) p.lse[(static_cast<long long>(pb) * p.H + ph) * p.s_pad + pqpos] = row_ok ? plse : INFINITY;
+          tc_fence_before();
+          warp_arrive(o_empty);
 #ifdef TPFFN_INSTRUMENT
-        if (rec) {
-          AT_ADD(12, t12);
-          if (rescale) AT_CNT(13);
-        }
+          if (rec) AT_ADD(14, t14);
 #endif
+        }
       }
-      if (!ok) break;
-      AT_T0(t14);
-      const uint32_t glast = pg + nkb - 1;
+      if (!ok || !has) break;
+      pglast = pg + nkb - 1;
       pg += nkb;
       // the two halves meet: m = max(m_0, m_1), l = sum of l_h 2^{m_h - m}
       float mo, lo;
@@ -576,31 +630,14 @@ __global__ void __launch_bounds__(NT, 1) attn_fwd_kernel(const __grid_constant__
       const float m = fmaxf(m_used, mo);  // finite: every row sees at least one key
       const float f_mine = ex2(m_used - m), f_other = ex2(mo - m);
       const float lsum = l * f_mine + lo * f_other;
-      const float f0 = half == 0 ? f_mine : f_other, f1 = half == 0 ? f_other : f_mine;
-      if (!W.warp(&pv_done[glast & 1u], (glast >> 1) & 1u)) break;
-      tc_fence_after();
-      const bool row_ok = qpos < p.S;
-      const float inv = 1.f / lsum;
-      __nv_bfloat16* orow = p.o + (static_cast<long long>(b) * p.S + qpos) * p.o_rs + h * HD + half * 64;
-#pragma unroll 1
-      for (int c = 0; c < 2; ++c) {
-        uint32_t o0[32], o1[32];
-        tmem_ld32(tl + 256 + half * 64 + c * 32, o0);
-        tmem_ld32(tl + 384 + half * 64 + c * 32, o1);
-        tmem_wait_ld();
-#pragma unroll
-        for (int i = 0; i < 32; ++i)
-          o0[i] = __float_as_uint(fmaf(__uint_as_float(o0[i]), f0, __uint_as_float(o1[i]) * f1));
-        if (row_ok) store_row_bf16(orow + c * 32, o0, inv);
-      }
-      // rows past the sequence get lse = +inf: the backward reads them as p = 0
-      if (half == 0)
-        p.lse[(static_cast<long long>(b) * p.H + h) * p.s_pad + qpos] = row_ok ? m + log2f(lsum) : INFINITY;
-      tc_fence_before();
-      warp_arrive(o_empty);
-#ifdef TPFFN_INSTRUMENT
-      if (rec) AT_ADD(14, t14);
-#endif
+      pf0 = half == 0 ? f_mine : f_other;
+      pf1 = half == 0 ? f_other : f_mine;
+      pinv = 1.f / lsum;
+      plse = m + log2f(lsum);
+      pb = b;
+      ph = h;
+      pqpos = qpos;
+      pend = true;
     }
 #ifdef TPFFN_INSTRUMENT
     if (rec) AT_ADD(15, t_sm);
