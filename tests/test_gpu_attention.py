@@ -100,6 +100,7 @@ CORE_CASES = [  # B, S, H, Hkv, T_p, causal, q_scale
     (3, 97, 2, 1, 1, False, 2.0),    # T_p 1, ragged non-causal
     (2, 2, 4, 4, 2, True, 1.0),      # two tokens
     (1, 640, 2, 2, 2, True, 1.0),    # odd number of 128-row tiles (5)
+    (2, 768, 16, 4, 4, True, 1.0),   # 192 work items: CTAs take a second item (item-to-item hand-over)
 ]
 
 
