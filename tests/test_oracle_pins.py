@@ -317,3 +317,29 @@ def test_hidden_dump_rounds_to_stored_values():
             sub = P.hidden_dump(f["dy"], rows=[3, 0], cols=[47, 5, 20])
             for k in dump:
                 np.testing.assert_array_equal(sub[k], dump[k][np.ix_([3, 0], [47, 5, 20])])
+
+
+def test_chain_noise_bounds_bf16_storage_and_is_not_vacuous():
+    """The widening that the GPU parity tests give the comparison of y and dx
+    with the pure float64 chain (tests.parity.chain_noise) covers what bf16
+    storage of the hidden activations does to them: the rounded oracle stays
+    within 1e-2 (|ref| + 1) plus that bound of the float64 chain, for both
+    activations and a hidden width in the thousands; and the bound is of the
+    size of that noise, not a blanket pass: measured in the bound's standard
+    deviation (bound / 6), the rounded oracle's distances have a root mean
+    square between 0.1 and 1 (about 0.75 for y, whose h is rounded once)."""
+    from tests.parity import chain_noise
+    for act, (N, d, d_ff, T) in (("swiglu", (96, 64, 2048, 4)), ("gelu_tanh", (96, 64, 4096, 4))):
+        w = small_case(N, d, d_ff, T, act, dtype="bf16", seed=47)
+        f = {k: to_f64(v) for k, v in make_inputs(w).items()}
+        kw = dict(W1=f["W1"], W3=f["W3"], b1=f["b1"], b2=f["b2"])
+        P = oracle.FFN(f["x"], f["W2"], T, act, round_bf16=True, **kw)
+        E = oracle.FFN(f["x"], f["W2"], T, act, round_bf16=False, **kw)
+        C = chain_noise(w, f, E.hidden_dump(f["dy"]))
+        got = dict(y=P.forward_sharded()["y"], dx=P.backward_rows(f["dy"])["dx"])
+        ref = dict(y=E.forward_sharded()["y"], dx=E.backward_rows(f["dy"])["dx"])
+        for k in ("y", "dx"):
+            err = np.abs(got[k] - ref[k])
+            assert np.all(err <= 1e-2 * (np.abs(ref[k]) + 1.0) + C[k]), (act, k)
+            z = np.sqrt(np.mean((err / (C[k] / 6.0)) ** 2))
+            assert 0.1 < z < 1.0, (act, k, z)
