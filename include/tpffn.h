@@ -371,7 +371,7 @@ TPFFN_API int tp_attn_last_launch_count(const tp_attn_plan* plan);
  * allocates nothing: no cudaMalloc, no cudaFree, no allocating library call.
  *   - Limit: returns TP_ERR_UNSUPPORTED, without enqueueing work, when
  *     tp_ffn_workspace_bytes(plan, n_tokens, TP_SUM_STANDALONE) exceeds
- *     TPFFN_STATIC_SCRATCH_BYTES (for example at most 77 tokens for the
+ *     TPFFN_STATIC_SCRATCH_BYTES (for example above 76 tokens for the
  *     Llama-3-70B-shaped decode FFN: d 8192, d_ff 28672, T_p 8, SwiGLU).
  *   - Set-up: the first call on each device looks up the array's device
  *     address (cudaGetSymbolAddress, with that device current) and caches

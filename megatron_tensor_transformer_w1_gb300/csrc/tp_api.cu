@@ -89,9 +89,35 @@ int64_t colsum_chunk(int64_t rows) {
 }
 
 struct WsLayout {
-  size_t h = 0, part = 0, D = 0, cs = 0, total = 0;
-  bool has_part = false;
+  size_t h = 0, part = 0, D = 0, cs = 0, ks = 0, total = 0;
+  bool has_part = false, has_ks = false;
 };
+
+// Decode-sized SwiGLU forwards (at most 32 tokens: one 32-row A tile) may
+// split the up GEMM's K: its T_p x ceil(W / 256) weight tiles are too few to
+// give every SM the same number, and two K parts per tile fill the GPU
+// evenly; the fp32 parts are summed, in order, by the SwiGLU combine kernel.
+constexpr int kMaxKsplit = 2;
+bool ksplit_shape(const tp_ffn_plan* p, int64_t n) {
+  return p->act == TP_ACT_SWIGLU && p->dtype == TP_BF16 && n >= 1 && n <= 32;
+}
+int choose_ksplit(const tp_ffn_plan* p, int64_t n, int num_sms) {
+  static const bool off = [] {
+    const char* v = getenv("TPFFN_KSPLIT");
+    return v && v[0] == '0';
+  }();
+  if (off || !ksplit_shape(p, n) || num_sms < 1) return 1;
+  const int64_t k_blocks = (p->d + 63) / 64;
+  const int64_t tiles = p->T_p * ((hidden_width(p) + 255) / 256);
+  auto eff = [&](int64_t units) {  // share of the SM-unit slots the busiest wave count leaves in use
+    const int64_t waves = (units + num_sms - 1) / num_sms;
+    return static_cast<double>(units) / static_cast<double>(waves * num_sms);
+  };
+  int best = 1;
+  for (int k = 2; k <= kMaxKsplit; ++k)
+    if (k_blocks >= 16 * k && eff(tiles * k) > eff(tiles * best) + 0.05) best = k;
+  return best;
+}
 
 WsLayout ws_layout(const tp_ffn_plan* p, int64_t n, int flags) {
   WsLayout L;
@@ -107,6 +133,11 @@ WsLayout ws_layout(const tp_ffn_plan* p, int64_t n, int flags) {
     L.has_part = true;
     L.part = off;
     off += align_up(static_cast<size_t>(p->T_p) * n * p->d * 4);
+  }
+  if (ksplit_shape(p, n)) {
+    L.has_ks = true;
+    L.ks = off;
+    off += align_up(static_cast<size_t>(kMaxKsplit) * p->T_p * n * hidden_width(p) * 4);
   }
   L.cs = off;
   const int64_t cs1 = colsum_scratch_floats(p->T_p, n, p->s_pad, colsum_chunk(n));
@@ -459,7 +490,24 @@ static int fwd_impl(const tp_ffn_plan* p, int64_t n, const void* x, const void* 
     g.bias_len = p->s;
     g.n_store = sp;
     g.out_bf16 = out_bf16;
-    rc = run_gemm(p, g, ctx);
+    const int ks = L.has_ks ? choose_ksplit(p, n, ctx.num_sms) : 1;
+    if (ks > 1) {
+      // fp32 parts of a and g, then the SwiGLU combine
+      float* parts = reinterpret_cast<float*>(ws + L.ks);
+      g.epi = EPI_F32;
+      g.ksplit = ks;
+      g.out = parts;
+      g.out_bs = n * W;
+      g.out_rs = W;
+      g.out2 = nullptr;
+      g.n_store = W;
+      rc = run_gemm(p, g, ctx);
+      if (!rc)
+        rc = launch_swiglu_combine(parts, ks, static_cast<int>(T), n, sp, h,
+                                   saved ? static_cast<char*>(saved) + S.act : nullptr, ctx, "swiglu_combine");
+    } else {
+      rc = run_gemm(p, g, ctx);
+    }
     if (rc) return rc;
     hbuf = h;
   }

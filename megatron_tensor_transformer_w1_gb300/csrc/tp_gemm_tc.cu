@@ -78,7 +78,20 @@ struct Params {
   unsigned long long timeout_ns;
   int debug_skip;
   int dbg_slot;  // launch slot of the optional wait counters (instrumented builds only)
+  int ksplit;    // one-SM kernel: K split into this many parts (1: none)
 };
+
+// Work unit u of the one-SM kernel: tile u mod (tiles per split) over its
+// part u / (tiles per split) of the K blocks -- [kb0, kb0 + nkb).
+__device__ __forceinline__ int unit_split(const Params& p, int u, int& tile, int& kb0, int& nkb) {
+  const int per = p.tiles_m * p.tiles_n * p.NB;
+  const int kh = p.ksplit > 1 ? u / per : 0;
+  tile = u - kh * per;
+  const int kbs = (p.k_blocks + p.ksplit - 1) / p.ksplit;
+  kb0 = kh * kbs;
+  nkb = min(p.k_blocks - kb0, kbs);
+  return kh;
+}
 
 // Bounded wait (see wait_bounded_raw).
 __device__ __forceinline__ bool wait_bounded(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
@@ -339,8 +352,8 @@ __global__ void __launch_bounds__(threads_for<EPI>(), 1)
   grid_dep_launch();
   grid_dep_wait();
 
-  const int num_tiles = p.tiles_m * p.tiles_n * p.NB;
-  const int k_iters = p.G * p.k_blocks;
+  const int num_tiles = p.tiles_m * p.tiles_n * p.NB * p.ksplit;  // work units
+  const int k_iters_all = p.G * p.k_blocks;
 
   if (warp == 0) {
     // ------------------------------------------------ TMA producer
@@ -351,18 +364,21 @@ __global__ void __launch_bounds__(threads_for<EPI>(), 1)
 #pragma unroll
       for (int s = 0; s < STAGES; ++s) last_issue_phase[s] = -1;
       bool ok = true;
-      for (int tile = blockIdx.x; tile < num_tiles && ok; tile += gridDim.x) {
+      for (int unit = blockIdx.x; unit < num_tiles && ok; unit += gridDim.x) {
+        int tile, kb0, k_iters;
+        unit_split(p, unit, tile, kb0, k_iters);
+        if (p.ksplit == 1) k_iters = k_iters_all;
         int b, mb, nb;
         decode_tile(p, tile, b, mb, nb);
         const int m0 = mb * BM, n0 = nb * BN;
         for (int it = 0; it < k_iters; ++it) {
           const int g = it / p.k_blocks;
-          const int k0 = (it - g * p.k_blocks) * BK;
+          const int k0 = (kb0 + it - g * p.k_blocks) * BK;
           if (!wait_bounded(&empty[stage], phase ^ 1u, abort_flag, p)) {
             ok = false;
             break;
           }
-          const bool skip = p.debug_skip && tile == (int)blockIdx.x && it == 0;
+          const bool skip = p.debug_skip && unit == (int)blockIdx.x && it == 0;
           if (!skip) {
             uint8_t* sA = smem + stage * L::STAGE_BYTES;
             uint8_t* sB = sA + L::A_BYTES;
@@ -414,7 +430,10 @@ __global__ void __launch_bounds__(threads_for<EPI>(), 1)
       uint32_t phase = 0;
       int local = 0;
       bool ok = true;
-      for (int tile = blockIdx.x; tile < num_tiles && ok; tile += gridDim.x, ++local) {
+      for (int unit = blockIdx.x; unit < num_tiles && ok; unit += gridDim.x, ++local) {
+        int tile, kb0, k_iters;
+        unit_split(p, unit, tile, kb0, k_iters);
+        if (p.ksplit == 1) k_iters = k_iters_all;
         const int buf = local & 1;
         const uint32_t use = static_cast<uint32_t>(local >> 1);
         if (!wait_bounded(&tempty[buf], (use & 1u) ^ 1u, abort_flag, p)) break;
@@ -450,13 +469,16 @@ __global__ void __launch_bounds__(threads_for<EPI>(), 1)
     // ------------------------------------------------ epilogue warps 2..9
     const int quarter = warp & 3;  // TMEM lanes this warp may access
     int local = 0;
-    for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x, ++local) {
+    for (int unit = blockIdx.x; unit < num_tiles; unit += gridDim.x, ++local) {
       const int buf = local & 1;
       const uint32_t use = static_cast<uint32_t>(local >> 1);
       if (!wait_bounded(&tfull[buf], use & 1u, abort_flag, p)) break;
       tc_fence_after();
+      int tile, kb0, nkb;
+      const int kh = unit_split(p, unit, tile, kb0, nkb);
       int b, mb, nb;
       decode_tile(p, tile, b, mb, nb);
+      b += kh * p.NB;  // K part kh: fp32 batch kh * NB + b (EPI_F32 only)
       const int row = mb * BM + quarter * 32 + lane;
       const uint32_t taddr = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) +
                              static_cast<uint32_t>(buf * BN);
@@ -1144,7 +1166,10 @@ static int launch_inst(const GemmSpec& s, LaunchCtx& ctx) {
       return TP_ERR_CUDA;
     attr_done.fetch_or(bit);
   }
-  const long long tiles = static_cast<long long>(p.tiles_m) * p.tiles_n * p.NB;
+  p.ksplit = s.ksplit;
+  if (s.ksplit < 1 || (s.ksplit > 1 && (EPI != EPI_F32 || s.G != 1 || p.k_blocks < 2 * s.ksplit)))
+    return TP_ERR_INVALID;
+  const long long tiles = static_cast<long long>(p.tiles_m) * p.tiles_n * p.NB * s.ksplit;  // work units
   if (tiles <= 0 || p.k_blocks <= 0) return TP_ERR_INVALID;
   int grid = static_cast<int>(tiles < ctx.num_sms ? tiles : ctx.num_sms);
   // A single row of M tiles (decode-sized token counts) streams weights and
@@ -1203,7 +1228,9 @@ static int launch_pair(const GemmSpec& s, LaunchCtx& ctx) {
     rc = make_aux_map(&tx, s);
     if (rc) return rc;
   }
+  if (s.ksplit != 1) return TP_ERR_INVALID;  // the K split serves decode-sized GEMMs only
   Params p{};
+  p.ksplit = 1;
   p.M = static_cast<int>(s.M);
   p.N = static_cast<int>(s.N);
   p.K = static_cast<int>(s.K);

@@ -49,6 +49,9 @@ struct GemmSpec {
   const void* bias = nullptr; int64_t bias_bs = 0, bias_len = 0;
   int64_t n_store = 0;   // columns n < n_store of the output are written
   int out_bf16 = 1;      // plan dtype of out/out2 (EPI_F32 always fp32)
+  // K split (EPI_F32, G = 1, decode-sized M only): part k of the K blocks is
+  // accumulated on its own and written as fp32 batch k * NB + b of `out`
+  int ksplit = 1;
 };
 
 // Launch context of one API call.
@@ -90,6 +93,9 @@ int launch_pack_columns(const void* W1, const void* W3, void* out, int T_p, int6
 int launch_pack_rows(const void* W2, void* out, int T_p, int64_t s, int64_t s_pad, int64_t d,
                      int esz, int unpack, cudaStream_t st);
 // shard_stride: elements between consecutive shards' partials (0: rows*cols).
+// SwiGLU of the ksplit fp32 parts of a K-split up GEMM (see tp_kernels.cu).
+int launch_swiglu_combine(const float* parts, int ksplit, int T_p, int64_t rows, int64_t s_pad, void* h,
+                          void* saved, LaunchCtx& ctx, const char* name);
 int launch_shard_sum(const float* partials, int T_p, int64_t rows, int64_t cols,
                      const void* bias, void* out, int out_bf16, LaunchCtx& ctx,
                      const char* name, int64_t shard_stride = 0);

@@ -517,6 +517,77 @@ int launch_shard_sum(const float* partials, int T_p, int64_t rows, int64_t cols,
   return cudaPeekAtLastError() == cudaSuccess ? 0 : TP_ERR_CUDA;
 }
 
+// SwiGLU of a K-split up GEMM (decode-sized token counts): the fp32 parts
+// P[k][t][m][c] (k < ksplit, t < T, m < rows, c < W = 2 s_pad, hidden unit u
+// of shard t at column (u / 128) 256 + u % 128 for a and + 128 for g) are
+// summed in the order k = 0, 1, ..; then h = silu(a) g, as the GEMM's own
+// SwiGLU epilogue forms it, in bf16 at h[t][m][u], and, when `saved` is
+// given, a and g in bf16 at saved[t][m][c].  One thread per 8 hidden units.
+__global__ void __launch_bounds__(256) swiglu_combine_kernel(const float* __restrict__ P, int ksplit, long long part,
+                                                             int T, long long rows, long long s_pad,
+                                                             __nv_bfloat16* h, __nv_bfloat16* saved) {
+  // a programmatic dependent of the GEMM that wrote the parts
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  const long long W = 2 * s_pad;
+  const long long u8 = s_pad / 8;
+  const long long total = (long long)T * rows * u8;
+  for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < total;
+       i += (long long)gridDim.x * blockDim.x) {
+    const long long tm = i / u8;  // t * rows + m
+    const long long u = (i - tm * u8) * 8;
+    const long long ca = (u >> 7) * 256 + (u & 127);
+    const float* pa = P + tm * W + ca;
+    float a[8], g[8];
+    {
+      const float4 a0 = reinterpret_cast<const float4*>(pa)[0], a1 = reinterpret_cast<const float4*>(pa)[1];
+      const float4 g0 = reinterpret_cast<const float4*>(pa + 128)[0], g1 = reinterpret_cast<const float4*>(pa + 128)[1];
+      a[0] = a0.x; a[1] = a0.y; a[2] = a0.z; a[3] = a0.w; a[4] = a1.x; a[5] = a1.y; a[6] = a1.z; a[7] = a1.w;
+      g[0] = g0.x; g[1] = g0.y; g[2] = g0.z; g[3] = g0.w; g[4] = g1.x; g[5] = g1.y; g[6] = g1.z; g[7] = g1.w;
+    }
+    for (int k = 1; k < ksplit; ++k) {
+      const float* q = pa + k * part;
+      const float4 a0 = reinterpret_cast<const float4*>(q)[0], a1 = reinterpret_cast<const float4*>(q)[1];
+      const float4 g0 = reinterpret_cast<const float4*>(q + 128)[0], g1 = reinterpret_cast<const float4*>(q + 128)[1];
+      a[0] += a0.x; a[1] += a0.y; a[2] += a0.z; a[3] += a0.w; a[4] += a1.x; a[5] += a1.y; a[6] += a1.z; a[7] += a1.w;
+      g[0] += g0.x; g[1] += g0.y; g[2] += g0.z; g[3] += g0.w; g[4] += g1.x; g[5] += g1.y; g[6] += g1.z; g[7] += g1.w;
+    }
+    float hv[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) hv[j] = a[j] * sigmoid_f(a[j]) * g[j];
+    auto pack8 = [](const float* v) {
+      uint4 q;
+      __nv_bfloat162 x0 = __floats2bfloat162_rn(v[0], v[1]), x1 = __floats2bfloat162_rn(v[2], v[3]);
+      __nv_bfloat162 x2 = __floats2bfloat162_rn(v[4], v[5]), x3 = __floats2bfloat162_rn(v[6], v[7]);
+      q.x = *reinterpret_cast<uint32_t*>(&x0);
+      q.y = *reinterpret_cast<uint32_t*>(&x1);
+      q.z = *reinterpret_cast<uint32_t*>(&x2);
+      q.w = *reinterpret_cast<uint32_t*>(&x3);
+      return q;
+    };
+    *reinterpret_cast<uint4*>(h + tm * s_pad + u) = pack8(hv);
+    if (saved) {
+      *reinterpret_cast<uint4*>(saved + tm * W + ca) = pack8(a);
+      *reinterpret_cast<uint4*>(saved + tm * W + ca + 128) = pack8(g);
+    }
+  }
+}
+
+int launch_swiglu_combine(const float* parts, int ksplit, int T_p, int64_t rows, int64_t s_pad, void* h,
+                          void* saved, LaunchCtx& ctx, const char* name) {
+  const long long total = (long long)T_p * rows * (s_pad / 8);
+  if (total <= 0) return 0;
+  if (s_pad % 128 || reinterpret_cast<uintptr_t>(parts) % 16 || reinterpret_cast<uintptr_t>(h) % 16 ||
+      reinterpret_cast<uintptr_t>(saved) % 16)
+    return TP_ERR_ALIGN;
+  if (ctx.before) ctx.before(ctx.user, name, ctx.stream);
+  launch_pdl(swiglu_combine_kernel, grid_for(total, 256, ctx.num_sms), 256, ctx.stream, parts, ksplit,
+             (long long)T_p * rows * 2 * s_pad, T_p, rows, s_pad, static_cast<__nv_bfloat16*>(h),
+             static_cast<__nv_bfloat16*>(saved));
+  if (ctx.after) ctx.after(ctx.user, ctx.stream);
+  ctx.launches++;
+  return cudaPeekAtLastError() == cudaSuccess ? 0 : TP_ERR_CUDA;
+}
+
 static SliceTable to_table(const RowSlices& r) {
   SliceTable t{};
   for (int i = 0; i < r.n && i < kMaxSlices; ++i) t.p[i] = static_cast<char*>(r.ptr[i]);
