@@ -53,8 +53,9 @@ NCU_TRAFFIC = {
 # The same for the decode-sized forward (Llama-3-70B shapes, 32 tokens,
 # one-SM kernel with 32-row A tiles); same profile file.
 NCU_TRAFFIC_DECODE = {
-    "up_swiglu": 940.62e6 + 4.36e6,
-    "down_partials": 471.63e6 + 4.32e6,
+    "up_swiglu": 940.66e6 + 12.82e6,  # K split in two fp32 parts
+    "swiglu_combine": 14.72e6 + 0.0,
+    "down_partials": 471.64e6 + 4.33e6,
 }
 
 
