@@ -109,3 +109,22 @@ def test_status_strings(abi):
     for code in range(6):
         assert abi.tp_ffn_status_string(code).startswith("TP_")
     assert abi.tp_ffn_status_string(99) == "unknown status"
+
+
+def test_static_scratch_limit_and_decode_split_workspace(abi):
+    """The header's example: for the Llama-3-70B-shaped decode FFN the static
+    scratch serves up to 76 tokens and refuses more.  Decode-sized SwiGLU
+    calls (at most 32 tokens) also hold two fp32 K parts of the up GEMM
+    (T_p x n x 2 s_pad floats each) in their workspace, and still fit."""
+    rc, plan = abi.tp_ffn_plan_create(8192, 28672, 8, abi.TP_ACT_SWIGLU, abi.TP_BF16)
+    assert rc == abi.TP_OK
+    try:
+        ws = lambda n: abi.tp_ffn_workspace_bytes(plan, n, abi.TP_SUM_STANDALONE)
+        lim = abi.TPFFN_STATIC_SCRATCH_BYTES
+        assert all(ws(n) <= lim for n in range(1, 77))
+        assert ws(77) > lim
+        parts = 2 * 8 * 32 * (2 * 3584) * 4
+        # at 32 tokens the parts are there; at 33 (no split) they are not
+        assert ws(32) - ws(33) * 32 / 33 > 0.9 * parts
+    finally:
+        abi.tp_ffn_plan_destroy(plan)
