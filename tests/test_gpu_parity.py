@@ -74,6 +74,7 @@ SMALL = [
     small_case(32, 256, 1536, 4, "swiglu", seed=109),          # decode-sized: 32-row A tiles
     small_case(17, 200, 600, 3, "swiglu", seed=110),           # decode-sized, ragged: 17 of 32 rows
     small_case(17, 2048, 1024, 2, "swiglu", seed=112),         # decode-sized up GEMM split in two K parts
+    small_case(1, 2048, 1024, 2, "swiglu", seed=113),          # one token through the K split
 ]
 
 
