@@ -37,26 +37,41 @@ METRIC = "TP-FFN fwd+bwd TFLOP/s & % BF16 tensor peak; decode-path HBM GB/s"
 MAIN = "llama3_8b_swiglu_bf16"
 DECODE = "llama3_70b_decode_swiglu_bf16"
 
-# DRAM bytes per launch (dram__bytes_read.sum + dram__bytes_write.sum) from
-# one ncu capture of the Llama-3-8B step at full size (8192 tokens, fused
-# sums, two-SM pair GEMMs, raster groups of 8, TMA-staged backward epilogue);
-# see profiles/llama3_8b_swiglu_gemm_dram_traffic.md.  To be cleared when the
-# kernels change.
-NCU_TRAFFIC = {
-    "up_swiglu": 1.142e9 + 678.07e6,
-    "down_fused_sum": 1.048e9 + 59.79e6,
-    "dgrad_h_swiglu": 1.704e9 + 440.65e6,
-    "dgrad_x_fused_sum": 2.110e9 + 59.83e6,
-    "wgrad_w2": 1.187e9 + 107.47e6,
-    "wgrad_w13": 2.213e9 + 224.10e6,
-}
-# The same for the decode-sized forward (Llama-3-70B shapes, 32 tokens,
-# one-SM kernel with 32-row A tiles); same profile file.
-NCU_TRAFFIC_DECODE = {
-    "up_swiglu": 940.66e6 + 12.82e6,  # K split in two fp32 parts
-    "swiglu_combine": 14.72e6 + 0.0,
-    "down_partials": 471.64e6 + 4.33e6,
-}
+# DRAM bytes per launch (dram__bytes_read.sum + dram__bytes_write.sum) come
+# from a committed ncu summary whose JSON block records them together with a
+# hash of the kernel sources they were captured from; when the sources have
+# changed since, the roofline's traffic is null (stale counters are not
+# reported).
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "dram_traffic_per_launch.md")
+CSRC = os.path.join(ROOT, "megatron_tensor_transformer_w1_gb300", "csrc")
+
+
+def kernel_source_sha16():
+    """sha256 (first 16 hex digits) over every kernel source file, in name order."""
+    import hashlib
+    h = hashlib.sha256()
+    for name in sorted(os.listdir(CSRC)):
+        path = os.path.join(CSRC, name)
+        if os.path.isfile(path):
+            h.update(name.encode())
+            h.update(open(path, "rb").read())
+    return h.hexdigest()[:16]
+
+
+def ncu_traffic(workload):
+    """{kernel name: DRAM bytes per launch} of `workload` from the committed
+    capture, or ({}, reason) when there is none for the current sources."""
+    if not os.path.exists(TRAFFIC_FILE):
+        return {}, "no committed capture"
+    text = open(TRAFFIC_FILE).read()
+    try:
+        block = text.split("```json", 1)[1].split("```", 1)[0]
+        d = json.loads(block)
+    except (IndexError, ValueError):
+        return {}, "capture summary unreadable"
+    if d.get("source_sha16") != kernel_source_sha16():
+        return {}, "kernels changed since the capture"
+    return d.get("per_launch_bytes", {}).get(workload, {}), "ncu capture " + d.get("source_sha16", "")
 
 
 def _peaks():
@@ -269,17 +284,23 @@ def run_ours(args, ctx):
     dom = max(per, key=lambda k: sum(per[k]))
     kind, work = _kernel_work(w, dom)
     avg_ms = sum(per[dom]) / len(per[dom])
+    traffic, traffic_src = ncu_traffic(MAIN if w.N == WORKLOADS[MAIN].N else f"{MAIN}@{w.N}")
     if kind == "flop":
+        # a kernel of about a millisecond, timed inside a 5 ms step: the burst
+        # peak is the denominator; the fraction of the sustained peak (a
+        # seconds-long GEMM loop under the power cap) is given beside it
         ach = work / (avg_ms * 1e-3) / 1e12
-        roof = {"kernel": dom, "bound": "tensor", "achieved": round(ach, 1), "peak": peaks["bf16_sus"],
-                "unit": "TFLOP/s", "frac": round(ach / peaks["bf16_sus"], 4),
-                "peak_kind": f"bf16 sustained ({peaks['source']})", "traffic": NCU_TRAFFIC.get(dom),
-                "work_per_launch": work, "launch_ms": round(avg_ms, 4)}
+        roof = {"kernel": dom, "bound": "tensor", "achieved": round(ach, 1), "peak": peaks["bf16"],
+                "unit": "TFLOP/s", "frac": round(ach / peaks["bf16"], 4),
+                "peak_kind": f"bf16 burst ({peaks['source']})",
+                "frac_of_sustained": round(ach / peaks["bf16_sus"], 4), "traffic": traffic.get(dom),
+                "traffic_source": traffic_src, "work_per_launch": work, "launch_ms": round(avg_ms, 4)}
     else:
         ach = work / (avg_ms * 1e-3) / 1e9
         roof = {"kernel": dom, "bound": "hbm", "achieved": round(ach, 1), "peak": peaks["hbm"], "unit": "GB/s",
                 "frac": round(ach / peaks["hbm"], 4), "peak_kind": f"HBM copy ({peaks['source']})",
-                "traffic": NCU_TRAFFIC.get(dom), "work_per_launch": work, "launch_ms": round(avg_ms, 4)}
+                "traffic": traffic.get(dom), "traffic_source": traffic_src, "work_per_launch": work,
+                "launch_ms": round(avg_ms, 4)}
     kernels = {k: {"launches": len(v), "avg_ms": round(sum(v) / len(v), 4), "share": None} for k, v in per.items()}
     tot = sum(sum(v) for v in per.values())
     for k, v in per.items():
@@ -353,6 +374,9 @@ def run_ours(args, ctx):
     attention = run_attention(dev, 10, peaks, args.sum) if not args.no_extras else None
 
     value = ctx["world"] * flop_step / (ms * 1e-3) / 1e12
+    # Key order: the long tables first, the headline blocks (roofline,
+    # e2e, decode, cpu_baseline) last, so that a reader of the line's tail
+    # sees them.
     line = {
         "metric": METRIC, "value": round(value, 2), "unit": "TFLOP/s", "n_gpus": ctx["world"],
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 4), "higher_is_better": True,
@@ -361,21 +385,21 @@ def run_ours(args, ctx):
                    "shard_sum": args.sum, "step": "shard_columns+shard_rows+fwd+bwd (incl. weight grads)",
                    "flop_per_step": flop_step, "l2": "no flush: per-step working set ~4.3 GB > 129 MB L2",
                    "parallelism": f"{w.T_p} virtual TP ranks per GPU; replicas across GPUs"},
+        "attention_sublayer": attention,
+        "sequence_parallel": seq_parallel,
+        "workloads": workloads,
+        "standalone_shard_sum": standalone,
+        "kernels": kernels,
+        "gpu_launches": gpu_launches,
+        "clocks": clk.summary(),
+        "e2e": {"value": round(ctx["world"] * flop_step / (e2e_ms * 1e-3) / 1e12, 2), "unit": "TFLOP/s",
+                "ms_per_step": round(e2e_ms, 4), "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                "copies": "pinned host buffers; a second stream, two device buffer sets (overlapped with compute)"},
         "frac_of_bf16_peak": {"burst": round(value / ctx['world'] / peaks["bf16"], 4),
                               "sustained": round(value / ctx['world'] / peaks["bf16_sus"], 4),
                               "peaks": peaks["source"]},
         "roofline": roof,
-        "kernels": kernels,
-        "e2e": {"value": round(ctx["world"] * flop_step / (e2e_ms * 1e-3) / 1e12, 2), "unit": "TFLOP/s",
-                "ms_per_step": round(e2e_ms, 4), "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-                "copies": "pinned host buffers; a second stream, two device buffer sets (overlapped with compute)"},
-        "gpu_launches": gpu_launches,
-        "clocks": clk.summary(),
         "decode": decode,
-        "standalone_shard_sum": standalone,
-        "workloads": workloads,
-        "sequence_parallel": seq_parallel,
-        "attention_sublayer": attention,
     }
     if ctx["rank"] == 0 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(w, budget_s=args.cpu_budget)
@@ -673,6 +697,46 @@ def profile_attention(args):
     return {"profile_attention": w.name, "B": w.B, "S": w.S, "steps": args.steps, "warmup": args.warmup}
 
 
+def profile_ffn(args):
+    """A plain loop of FFN steps for profiler captures: the Llama-3-8B shapes
+    (--tokens overrides the token count), pack + forward + backward with the
+    --sum mode, or with --profile-decode the decode-shaped forward alone; no
+    timing, no extras, nothing else launched."""
+    import torch
+    from synth import WORKLOADS
+    from megatron_tensor_transformer_w1_gb300 import tpffn as abi
+    from megatron_tensor_transformer_w1_gb300.ffn import TensorParallelFFN
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    w = WORKLOADS[DECODE if args.profile_decode else MAIN]
+    if args.tokens and not args.profile_decode:
+        w = w.replace(N=args.tokens)
+    inp = _device_inputs(w, dev, 20260000 + w.seed_index)
+    ffn = TensorParallelFFN(w.d, w.d_ff, w.T_p, w.act, "bf16", device=dev)
+    st, plan, n = torch.cuda.current_stream(dev), ffn.plan, w.N
+    flags = abi.TP_SUM_FUSED if (args.sum == "fused" and not args.profile_decode) else 0
+    w13p, w2p = ffn.pack(inp["W1"], inp["W2"], inp["W3"])
+    ws = ffn.workspace(n, flags)
+    y = torch.empty(n, w.d, dtype=torch.bfloat16, device=dev)
+    if args.profile_decode:
+        for _ in range(args.warmup + args.steps):
+            abi.check(abi.tp_ffn_fwd(plan, n, inp["x"], w13p, w2p, None, None, y, None, None, ws, ws.numel(), 0, st),
+                      "decode fwd")
+    else:
+        saved = torch.empty(abi.tp_ffn_saved_bytes(plan, n), dtype=torch.uint8, device=dev)
+        dx = torch.empty_like(y)
+        dw13p, dw2p = torch.empty_like(w13p), torch.empty_like(w2p)
+        for _ in range(args.warmup + args.steps):
+            abi.check(abi.tp_ffn_shard_columns(plan, inp["W1"], inp["W3"], w13p, st), "shard_columns")
+            abi.check(abi.tp_ffn_shard_rows(plan, inp["W2"], w2p, st), "shard_rows")
+            abi.check(abi.tp_ffn_fwd(plan, n, inp["x"], w13p, w2p, None, None, y, None, saved, ws, ws.numel(), flags,
+                                     st), "fwd")
+            abi.check(abi.tp_ffn_bwd(plan, n, inp["x"], w13p, w2p, saved, inp["dy"], dx, None, dw13p, dw2p, None,
+                                     None, ws, ws.numel(), flags, st), "bwd")
+    torch.cuda.synchronize(dev)
+    return {"profile": w.name, "tokens": n, "sum": args.sum, "steps": args.steps, "warmup": args.warmup}
+
+
 def run_decode(args, ctx, dev, peaks):
     import torch
     from synth import WORKLOADS
@@ -719,12 +783,13 @@ def run_decode(args, ctx, dev, peaks):
     dom_bytes = {"up_swiglu": 2 * w.d_ff * w.d * 2 + w.N * w.d * 2 + w.N * w.d_ff * 2,
                  "down_partials": w.d_ff * w.d * 2 + w.N * w.d_ff * 2 + w.T_p * w.N * w.d * 4}.get(dom, 0)
     dach = dom_bytes / (dom_ms * 1e-3) / 1e9
+    dtraffic, dsrc = ncu_traffic(DECODE)
     return {"workload": DECODE, "value": round(gbs, 1), "unit": "GB/s", "ms_per_step": round(ms, 4),
             "timing": "step time from a loop without per-kernel events; kernel times from a second loop with them",
             "bytes_per_step": nbytes, "frac_of_hbm_peak": round(gbs / ctx["world"] / peaks["hbm"], 4),
             "roofline": {"kernel": dom, "bound": "hbm", "achieved": round(dach, 1), "peak": peaks["hbm"],
                          "unit": "GB/s", "frac": round(dach / peaks["hbm"], 4),
-                         "traffic": NCU_TRAFFIC_DECODE.get(dom),
+                         "traffic": dtraffic.get(dom), "traffic_source": dsrc,
                          "launch_ms": round(dom_ms, 4)},
             "kernels": {q: {"launches": len(v), "avg_ms": round(sum(v) / len(v), 4)} for q, v in per.items()}}
 
@@ -825,6 +890,10 @@ def main():
     ap.add_argument("--profile-attention", default="", metavar="WORKLOAD",
                     help="only run --steps fwd+bwd steps of this attention workload (profiler captures)")
     ap.add_argument("--attn-batch", type=int, default=0, help="override the attention workload's sequence count")
+    ap.add_argument("--profile-ffn", action="store_true",
+                    help="only run --warmup + --steps plain FFN steps (profiler captures)")
+    ap.add_argument("--profile-decode", action="store_true",
+                    help="with --profile-ffn: the decode-shaped forward instead of the training step")
     args = ap.parse_args()
     ctx = dist_setup(args.gpus)
     if args.impl == "reference":
@@ -840,6 +909,9 @@ def main():
     importlib.import_module("__graft_entry__").build()
     if args.profile_attention:
         print(json.dumps(profile_attention(args)), flush=True)
+        return 0
+    if args.profile_ffn:
+        print(json.dumps(profile_ffn(args)), flush=True)
         return 0
     line = run_ours(args, ctx)
     if ctx["rank"] == 0:

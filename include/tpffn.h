@@ -350,8 +350,9 @@ TPFFN_API int tp_attn_last_launch_count(const tp_attn_plan* plan);
 
 /* ------------------------------------------------ forward without allocation */
 
-/* Size of the library's static scratch array (32 MiB).  Every GPU that loads
- * the library reserves this much device memory until the process exits. */
+/* Size of the library's static scratch array (32 MiB).  A GPU holds this
+ * much device memory from the moment the library's static-scratch module is
+ * loaded on it until the process exits (see "Set-up" below). */
 #define TPFFN_STATIC_SCRATCH_BYTES ((size_t)32 << 20)
 
 /* Forward pass for callers that cannot allocate device memory.
@@ -364,25 +365,36 @@ TPFFN_API int tp_attn_last_launch_count(const tp_attn_plan* plan);
  * no room for an allocation that might block.
  *
  * It computes what tp_ffn_fwd computes with TP_SUM_STANDALONE, saved = NULL
- * and partials = NULL.  The caller still passes the inputs (x, w13p, w2p,
- * b1, b2) and the output y, with the meanings and layouts of tp_ffn_fwd.
- * The scratch (error word, hidden activations, fp32 shard partials) lives in
- * one file-scope device array of TPFFN_STATIC_SCRATCH_BYTES.  This call
- * allocates nothing: no cudaMalloc, no cudaFree, no allocating library call.
+ * and partials = NULL, with the same kernels, so its y is bit-identical to
+ * that call's.  The caller still passes the inputs (x, w13p, w2p, b1, b2)
+ * and the output y, with the meanings and layouts of tp_ffn_fwd.  The
+ * scratch (error word, hidden activations, fp32 shard partials, the decode
+ * K-split parts) lives in one file-scope device array of
+ * TPFFN_STATIC_SCRATCH_BYTES.  This call allocates nothing: no cudaMalloc,
+ * no cudaFree, no allocating library call.
  *   - Limit: returns TP_ERR_UNSUPPORTED, without enqueueing work, when
  *     tp_ffn_workspace_bytes(plan, n_tokens, TP_SUM_STANDALONE) exceeds
  *     TPFFN_STATIC_SCRATCH_BYTES (for example above 76 tokens for the
  *     Llama-3-70B-shaped decode FFN: d 8192, d_ff 28672, T_p 8, SwiGLU).
- *   - Set-up: the first call on each device looks up the array's device
- *     address (cudaGetSymbolAddress, with that device current) and caches
- *     it.  Make that first call before any stream capture.
+ *   - Set-up: every call looks up the array's device address
+ *     (cudaGetSymbolAddress, on the current device).  Under CUDA's lazy
+ *     module loading, the runtime's default, the first look-up on a device
+ *     loads the module that holds the array, and the device reserves
+ *     TPFFN_STATIC_SCRATCH_BYTES then.  A call with n_tokens = 0 does only
+ *     that set-up (x, w13p, w2p, b1, b2, y and stream are not read) and
+ *     returns TP_OK: make it once per device, with that device current,
+ *     during start-up -- before the caller reserves its device memory and
+ *     before any stream capture.  Likewise, kernels of the library that
+ *     have not run yet on a device are loaded on their first launch; one
+ *     ordinary call at start-up (tp_ffn_fwd, or this one) loads them.
  *   - Sharing: every call, on any stream, uses the same array, which keeps
  *     the previous call's contents; the call clears the error word it needs
  *     zeroed, and overwrites the rest.  Calls that overlap on the GPU (for
  *     example on two streams) race on the array: serialise them.
- *   - Errors: argument and launch errors as in tp_ffn_fwd.  The device
- *     error word sits inside the array and is not exposed, so a device-side
- *     timeout is not reported by this entry point. */
+ *   - Errors: argument and launch errors as in tp_ffn_fwd; TP_ERR_CUDA when
+ *     the address look-up fails.  The device error word sits inside the
+ *     array and is not exposed, so a device-side timeout is not reported by
+ *     this entry point. */
 TPFFN_API int tp_ffn_fwd_static_scratch(const tp_ffn_plan* plan, int64_t n_tokens, const void* x,
                                         const void* w13p, const void* w2p, const void* b1, const void* b2,
                                         void* y, tp_stream_t stream);

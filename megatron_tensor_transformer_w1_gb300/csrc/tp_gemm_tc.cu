@@ -38,6 +38,7 @@
 #include <mutex>
 
 #include "tc_ptx.cuh"
+#include "tp_act.cuh"
 #include "tp_internal.h"
 #include "tpffn.h"
 
@@ -107,18 +108,6 @@ __device__ __forceinline__ constexpr uint32_t instr_desc() {
          (static_cast<uint32_t>(BMN) << 16) | (static_cast<uint32_t>(BN >> 3) << 17) |
          (static_cast<uint32_t>(BM >> 4) << 24);
 }
-
-// ------------------------------------------------------------ activations
-__device__ __forceinline__ float gelu_tanh_f(float z) {
-  const float k = 0.7978845608028654f;  // sqrt(2/pi)
-  return 0.5f * z * (1.0f + tanhf(k * (z + 0.044715f * z * z * z)));
-}
-__device__ __forceinline__ float gelu_tanh_grad_f(float z) {
-  const float k = 0.7978845608028654f;
-  const float t = tanhf(k * (z + 0.044715f * z * z * z));
-  return 0.5f * (1.0f + t) + 0.5f * z * (1.0f - t * t) * k * (1.0f + 3.0f * 0.044715f * z * z);
-}
-__device__ __forceinline__ float sigmoid_f(float a) { return 1.0f / (1.0f + expf(-a)); }
 
 __device__ __forceinline__ void store_bf16x8(__nv_bfloat16* dst, const float* v) {
   uint4 q;

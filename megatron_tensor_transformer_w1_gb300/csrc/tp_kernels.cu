@@ -14,6 +14,7 @@
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
+#include "tp_act.cuh"
 #include "tp_internal.h"
 #include "tpffn.h"
 
@@ -335,17 +336,6 @@ __device__ __forceinline__ float dot_gk(const SimtParams& p, long long b, long l
   }
   return acc;
 }
-
-__device__ __forceinline__ float gelu_tanh_f(float z) {
-  const float k = 0.7978845608028654f;
-  return 0.5f * z * (1.0f + tanhf(k * (z + 0.044715f * z * z * z)));
-}
-__device__ __forceinline__ float gelu_tanh_grad_f(float z) {
-  const float k = 0.7978845608028654f;
-  const float t = tanhf(k * (z + 0.044715f * z * z * z));
-  return 0.5f * (1.0f + t) + 0.5f * z * (1.0f - t * t) * k * (1.0f + 3.0f * 0.044715f * z * z);
-}
-__device__ __forceinline__ float sigmoid_f(float a) { return 1.0f / (1.0f + expf(-a)); }
 
 __global__ void simt_gemm_kernel(const SimtParams p) {
   const long long ncols = (p.epi == EPI_SWIGLU_FWD) ? p.N / 2 : p.N;

@@ -9,14 +9,20 @@
 // needs (the device error word, the hidden activations h^(t) and the fp32
 // shard partials y^(t)) comes from the file-scope array below.
 //
-// The array is static device memory of the library's module: every GPU that
-// loads the library holds TPFFN_STATIC_SCRATCH_BYTES until the process exits.
-// In host code its name only stands in for the symbol; the device address is
-// obtained with cudaGetSymbolAddress once per device (with that device
-// current) and cached, and that address is what the kernels receive.
+// The array is static device memory of this file's module.  A device holds
+// TPFFN_STATIC_SCRATCH_BYTES of it from the moment the module is loaded on
+// that device until the process exits.  Under CUDA's lazy module loading
+// (the runtime's default) that moment is the first cudaGetSymbolAddress of
+// the array on the device, which is why a call with n_tokens = 0 performs
+// exactly that look-up: a caller that must not allocate later makes it at
+// start-up, before reserving its memory.
+//
+// In host code the array's name only stands in for the symbol; the device
+// address comes from cudaGetSymbolAddress with the device current, and that
+// address is what the kernels receive.  It is looked up on every call (a
+// host-side table look-up once the module is loaded), so no address survives
+// a device reset or outlives the context it belongs to.
 #include <cuda_runtime.h>
-
-#include <mutex>
 
 #include "tp_internal.h"
 #include "tpffn.h"
@@ -25,28 +31,15 @@ namespace {
 
 __device__ __align__(256) unsigned char g_static_scratch[TPFFN_STATIC_SCRATCH_BYTES];
 
-constexpr int kMaxDevices = 64;
-std::mutex g_mu;
-void* g_addr[kMaxDevices] = {};
-
-// Device address of g_static_scratch on the current device (set-up on the
-// first call per device).  Returns nullptr and sets *rc on failure.
-void* scratch_address(int* rc) {
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
-    *rc = TP_ERR_CUDA;
+// Device address of g_static_scratch on the current device.  Returns nullptr
+// (and clears the runtime's error state) when the look-up fails.
+void* scratch_address() {
+  void* p = nullptr;
+  if (cudaGetSymbolAddress(&p, g_static_scratch) != cudaSuccess || !p) {
+    cudaGetLastError();
     return nullptr;
   }
-  std::lock_guard<std::mutex> lock(g_mu);
-  if (!g_addr[dev]) {
-    void* p = nullptr;
-    if (cudaGetSymbolAddress(&p, g_static_scratch) != cudaSuccess || !p) {
-      *rc = TP_ERR_CUDA;
-      return nullptr;
-    }
-    g_addr[dev] = p;
-  }
-  return g_addr[dev];
+  return p;
 }
 
 }  // namespace
@@ -55,14 +48,13 @@ extern "C" int tp_ffn_fwd_static_scratch(const tp_ffn_plan* plan, int64_t n_toke
                                          const void* w13p, const void* w2p, const void* b1, const void* b2,
                                          void* y, tp_stream_t stream) {
   if (!plan || n_tokens < 0) return TP_ERR_INVALID;
-  if (n_tokens == 0) return TP_OK;
   // The standalone shard-sum path: error word + h (no saved activations) +
   // fp32 partials must fit in the static array.
   const size_t need = tp_ffn_workspace_bytes(plan, n_tokens, TP_SUM_STANDALONE);
-  if (need == 0 || need > TPFFN_STATIC_SCRATCH_BYTES) return TP_ERR_UNSUPPORTED;
-  int rc = TP_OK;
-  void* scratch = scratch_address(&rc);
-  if (!scratch) return rc;
+  if (n_tokens > 0 && (need == 0 || need > TPFFN_STATIC_SCRATCH_BYTES)) return TP_ERR_UNSUPPORTED;
+  void* scratch = scratch_address();
+  if (!scratch) return TP_ERR_CUDA;
+  if (n_tokens == 0) return TP_OK;  // set-up only: the array is now resident on this device
   return tp_ffn_fwd(plan, n_tokens, x, w13p, w2p, b1, b2, y, nullptr, nullptr, scratch,
                     TPFFN_STATIC_SCRATCH_BYTES, TP_SUM_STANDALONE, stream);
 }

@@ -52,6 +52,7 @@ class Workload:
     n_heads: int = 0     # act "none": heads feeding the projection
     n_kv_heads: int = 0
     head_dim: int = 0
+    x_std: float = 1.0   # std of x (activation-tail cases scale it up)
 
     @property
     def s(self):
@@ -122,7 +123,7 @@ def make_inputs(w: Workload, seed: int | None = None):
     rng = {k: np.random.Generator(np.random.PCG64(s)) for k, s in zip(_ORDER, streams)}
     dt = w.dtype
     out = dict.fromkeys(_ORDER)
-    out["x"] = _draw(rng["x"], (w.N, w.d_in), 1.0, dt)
+    out["x"] = _draw(rng["x"], (w.N, w.d_in), w.x_std, dt)
     if w.act != "none":
         std1 = w.w_std if w.w_std is not None else 1.0 / np.sqrt(w.d)
         out["W1"] = _draw(rng["W1"], (w.d_ff, w.d), std1, dt)
@@ -138,11 +139,14 @@ def make_inputs(w: Workload, seed: int | None = None):
     return out
 
 
-def small_case(N, d, d_ff, T_p, act, dtype="bf16", bias=False, seed=7, fwd_only=False):
-    """A small workload of the same value distributions (for full-oracle parity)."""
-    return Workload(f"small_{act}_{dtype}_{N}x{d}x{d_ff}_tp{T_p}", N, d, d_ff, T_p, act, dtype,
+def small_case(N, d, d_ff, T_p, act, dtype="bf16", bias=False, seed=7, fwd_only=False, x_std=1.0, b_std=None):
+    """A small workload of the same value distributions (for full-oracle parity).
+    x_std > 1 (or a large b_std) drives the pre-activations into the tails of
+    the activation functions."""
+    tag = "" if x_std == 1.0 and b_std is None else f"_xs{x_std:g}" + ("" if b_std is None else f"_bs{b_std:g}")
+    return Workload(f"small_{act}_{dtype}_{N}x{d}x{d_ff}_tp{T_p}{tag}", N, d, d_ff, T_p, act, dtype,
                     bias=bias, fwd_only=fwd_only, w_std=(0.05 if bias else None),
-                    b_std=(0.02 if bias else 0.0), seed_index=seed)
+                    b_std=(b_std if b_std is not None else 0.02) if bias else 0.0, seed_index=seed, x_std=x_std)
 
 
 @dataclasses.dataclass(frozen=True)

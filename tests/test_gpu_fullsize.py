@@ -19,14 +19,19 @@ FULL = ["gpt2_small_gelu_bf16", "llama3_8b_swiglu_bf16", "megatron_8p3b_gelu_bf1
 
 
 def _samples(w):
+    """Seeded sample positions: 64 token rows (both ends included) of y, dx
+    and the partials; 64 hidden units (both ends of the first and last shard
+    and the two units either side of every interior shard boundary) by 64
+    inputs and 64 outputs, i.e. 4096 entries of each of dW1, dW3 and dW2."""
     rng = np.random.default_rng(9000 + w.seed_index)
-    n_rows = min(w.N, 40)
+    n_rows = min(w.N, 64)
     rows = np.unique(np.concatenate([[0, w.N - 1], rng.choice(w.N, n_rows - 2, replace=False)]))
-    # hidden units: include both ends of every shard
     s = w.s
-    js = np.unique(np.concatenate([[0, s - 1, w.d_ff - 1, (w.T_p - 1) * s], rng.choice(w.d_ff, 12, replace=False)]))
-    ks = np.unique(np.concatenate([[0, w.d - 1], rng.choice(w.d, 14, replace=False)]))
-    cs = np.unique(np.concatenate([[0, w.d - 1], rng.choice(w.d, 14, replace=False)]))
+    edges = [0, w.d_ff - 1] + [e for t in range(1, w.T_p) for e in (t * s - 1, t * s)]
+    rest = np.setdiff1d(np.arange(w.d_ff), edges)
+    js = np.unique(np.concatenate([edges, rng.choice(rest, 64 - len(edges), replace=False)]))
+    ks = np.unique(np.concatenate([[0, w.d - 1], rng.choice(np.arange(1, w.d - 1), 62, replace=False)]))
+    cs = np.unique(np.concatenate([[0, w.d - 1], rng.choice(np.arange(1, w.d - 1), 62, replace=False)]))
     return rows, js, ks, cs
 
 
@@ -84,3 +89,33 @@ def test_full_size_sampled(name, fused):
     if w.bias:
         check(get(out["db1"][js]), ref["db1"], BF16_REL, f"{name} db1 entries", W.get("db1"))
         check(get(out["db2"][cs]), ref["db2"], BF16_REL, f"{name} db2 entries")
+
+
+def _bits(t):
+    return t.view(torch.int32) if t.dtype == torch.float32 else t.view(torch.int16)
+
+
+@pytest.mark.parametrize("fused", [False, True], ids=["standalone", "fused"])
+@pytest.mark.parametrize("name", FULL)
+def test_full_size_bitwise_reproducible(name, fused):
+    """Two runs of the whole benchmarked step (pack, forward, backward) on the
+    same inputs, each with freshly allocated buffers, give the same bits in
+    every output: y, the fp32 partials, dx and its partials, every weight and
+    bias gradient.  Covers the fused shard K-loop of the persistent pair GEMMs
+    under programmatic dependent launch, the standalone ordered sums, the
+    ordered column sums of the bias gradients and, for the decode shapes, the
+    split up GEMM with its combine kernel."""
+    w = WORKLOADS[name]
+    inp = make_inputs(w)
+    a, _ = run_gpu_tensors(w, inp, fused=fused, backward=not w.fwd_only)
+    b, _ = run_gpu_tensors(w, inp, fused=fused, backward=not w.fwd_only)
+    compared = []
+    for k, v in a.items():
+        if v is None:
+            continue
+        assert torch.equal(_bits(v), _bits(b[k])), f"{name}: {k} differs between two runs"
+        compared.append(k)
+    expect = {"y"} | ({"partials"} if not fused else set())
+    if not w.fwd_only:
+        expect |= {"dx", "dW2"} | ({"dx_partials"} if not fused and w.act != "none" else set())
+    assert expect <= set(compared), (expect, compared)

@@ -73,9 +73,52 @@ SMALL = [
     small_case(520, 192, 900, 3, "swiglu", seed=108),          # s = 300 -> 384: the second N tile half empty
     small_case(32, 256, 1536, 4, "swiglu", seed=109),          # decode-sized: 32-row A tiles
     small_case(17, 200, 600, 3, "swiglu", seed=110),           # decode-sized, ragged: 17 of 32 rows
-    small_case(17, 2048, 1024, 2, "swiglu", seed=112),         # decode-sized up GEMM split in two K parts
-    small_case(1, 2048, 1024, 2, "swiglu", seed=113),          # one token through the K split
+    small_case(17, 2048, 3072, 3, "swiglu", seed=112),         # decode-sized up GEMM split in two K parts
+    small_case(1, 2048, 3072, 3, "swiglu", seed=113),          # one token through the K split
 ]
+# The K split is taken when it spreads the up GEMM's weight tiles over clearly
+# more SMs: with 3 x 8 = 24 tiles it doubles the SMs in use on any GPU of up to
+# several hundred SMs, so these two cases exercise it on every GB300.
+KSPLIT = [w for w in SMALL if w.N <= 32 and w.d >= 2048]
+
+
+@pytest.mark.parametrize("w", KSPLIT, ids=[w.name for w in KSPLIT])
+def test_decode_ksplit_is_taken(w):
+    """The decode-sized cases above really run the split up GEMM and the
+    SwiGLU combine kernel (the launch records name it)."""
+    from megatron_tensor_transformer_w1_gb300 import tpffn as abi
+    from megatron_tensor_transformer_w1_gb300.ffn import TensorParallelFFN
+    dev = torch.device("cuda", 0)
+    g = {k: (None if v is None else v.to(dev)) for k, v in make_inputs(w).items()}
+    ffn = TensorParallelFFN(w.d, w.d_ff, w.T_p, w.act, "bf16", device=dev)
+    w13p, w2p = ffn.pack(g["W1"], g["W2"], g["W3"])
+    for fused in (False, True):
+        ffn.forward(g["x"], w13p, w2p, fused=fused, flags=abi.TP_FLAG_TIMING)
+        names = [n for n, _ in abi.tp_ffn_kernel_times(ffn.plan, 1000)]
+        assert names[:2] == ["up_swiglu", "swiglu_combine"], names
+
+
+# Pre-activations driven into the tails of the activation functions: x ~
+# N(0, 16^2) puts z (or a and g) at |z| up to ~70 on both signs, where tanh
+# saturates, the z^3 term dominates and gelu', silu' are formed from
+# cancelling terms; a large b1 holds a hidden unit's z deep in one tail for
+# every token; x ~ N(0, 48^2) takes |a| past 88, where e^-a overflows in fp32.
+# Every output of both sum modes is compared element by element.
+TAILS = [
+    small_case(300, 256, 768, 3, "gelu_tanh", seed=701, x_std=16.0),
+    small_case(300, 256, 768, 3, "gelu_tanh", bias=True, seed=702, b_std=16.0),
+    small_case(300, 256, 768, 3, "swiglu", seed=703, x_std=16.0),
+    small_case(300, 256, 768, 3, "swiglu", seed=704, x_std=48.0),
+    small_case(17, 2048, 3072, 3, "swiglu", seed=705, x_std=16.0),       # through the decode K split
+    small_case(40, 64, 256, 2, "gelu_tanh", dtype="f32", seed=706, x_std=16.0),
+    small_case(40, 64, 256, 2, "swiglu", dtype="f32", seed=707, x_std=16.0),
+]
+
+
+@pytest.mark.parametrize("fused", [False, True], ids=["standalone", "fused"])
+@pytest.mark.parametrize("w", TAILS, ids=[w.name for w in TAILS])
+def test_activation_tails_against_full_oracle(w, fused):
+    _full_compare(w, fused)
 
 
 @pytest.mark.parametrize("fused", [False, True], ids=["standalone", "fused"])
