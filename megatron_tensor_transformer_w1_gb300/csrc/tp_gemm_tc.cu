@@ -80,7 +80,18 @@ struct Params {
   int debug_skip;
   int dbg_slot;  // launch slot of the optional wait counters (instrumented builds only)
   int ksplit;    // one-SM kernel: K split into this many parts (1: none)
+  int raster;    // pair kernel tile order (RASTER_*)
 };
+
+// Pair-kernel tile orders.  A per-shard GEMM whose other operand is shared
+// by every shard (x in the up GEMM and in dW1|dW3, dy in dh and dW2) walks
+// the shared operand's blocks fastest, over its whole extent: the tiles that
+// run at the same time then read a few per-shard blocks between them, once
+// each, and the shared operand (64-67 MB at 8192 tokens) stays resident in L2
+// across the whole launch.  Other GEMMs take grouped raster order.
+constexpr int RASTER_GROUPED = 0;  // groups of 8 M blocks, N within a group
+constexpr int RASTER_M_FAST = 1;   // A shared by every batch: all M blocks of one N block in turn
+constexpr int RASTER_N_FAST = 2;   // B shared by every batch: all N blocks of one M block in turn
 
 // Work unit u of the one-SM kernel: tile u mod (tiles per split) over its
 // part u / (tiles per split) of the K blocks -- [kb0, kb0 + nkb).
@@ -624,12 +635,23 @@ __device__ __forceinline__ uint4 lds128(uint32_t addr) {
   return v;
 }
 
-// Pair tile order: like decode_tile, over 256-row M blocks.
+// Pair tile order (RASTER_*), over 256-row M blocks; the batch (shard) is
+// the outermost coordinate in every order.
 __device__ __forceinline__ void decode_pair_tile(const Params& p, int tile, int& b, int& mp, int& nb) {
   const int tiles_m2 = (p.tiles_m + 1) >> 1;
   const int tpb = tiles_m2 * p.tiles_n;
   b = tile / tpb;
   const int r = tile - b * tpb;
+  if (p.raster == RASTER_M_FAST) {
+    nb = r / tiles_m2;
+    mp = r - nb * tiles_m2;
+    return;
+  }
+  if (p.raster == RASTER_N_FAST) {
+    mp = r / p.tiles_n;
+    nb = r - mp * p.tiles_n;
+    return;
+  }
   // 8 pair-rows per raster group: about 8 x 9.5 tiles run at once, so each K
   // step fetches ~17.5 distinct operand blocks from DRAM (4 x 19: ~23).
   constexpr int GM = 8;
@@ -1203,6 +1225,13 @@ static int make_aux_map(CUtensorMap* m, const GemmSpec& s) {
   return r == CUDA_SUCCESS ? 0 : TP_ERR_CUDA;
 }
 
+// TPFFN_RASTER=0 in the environment keeps the grouped order for every pair
+// GEMM (for comparisons).
+static bool raster_by_sharing() {
+  static const bool on = !getenv_flag_off("TPFFN_RASTER");
+  return on;
+}
+
 template <int EPI, bool AMN, bool BMN>
 static int launch_pair(const GemmSpec& s, LaunchCtx& ctx) {
   using L = PairLayout<EPI>;
@@ -1220,6 +1249,11 @@ static int launch_pair(const GemmSpec& s, LaunchCtx& ctx) {
   if (s.ksplit != 1) return TP_ERR_INVALID;  // the K split serves decode-sized GEMMs only
   Params p{};
   p.ksplit = 1;
+  p.raster = RASTER_GROUPED;
+  if (s.NB > 1 && s.G == 1 && raster_by_sharing()) {
+    if (s.A.bsel == 0 && s.B.bsel != 0) p.raster = RASTER_M_FAST;
+    if (s.B.bsel == 0 && s.A.bsel != 0) p.raster = RASTER_N_FAST;
+  }
   p.M = static_cast<int>(s.M);
   p.N = static_cast<int>(s.N);
   p.K = static_cast<int>(s.K);

@@ -110,8 +110,7 @@ TAILS = [
     small_case(300, 256, 768, 3, "swiglu", seed=703, x_std=16.0),
     small_case(300, 256, 768, 3, "swiglu", seed=704, x_std=48.0),
     small_case(17, 2048, 3072, 3, "swiglu", seed=705, x_std=16.0),       # through the decode K split
-    small_case(40, 64, 256, 2, "gelu_tanh", dtype="f32", seed=706, x_std=16.0),
-    small_case(40, 64, 256, 2, "swiglu", dtype="f32", seed=707, x_std=16.0),
+    small_case(40, 64, 256, 2, "gelu_tanh", dtype="f32", seed=706, x_std=16.0),   # the fp32 (SIMT) path
 ]
 
 
