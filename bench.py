@@ -406,9 +406,11 @@ def run_ours(args, ctx):
     return line
 
 
-def time_workload(w, dev, steps, fused, seed=0, overlap=False):
+def time_workload(w, dev, steps, fused, seed=0, overlap=False, graphs=True):
     """fwd and bwd of one workload through the C ABI: ms per call (CUDA
-    events on the calling stream) and the per-kernel times of the last call."""
+    events on the calling stream, around a plain loop of calls), the average
+    per-kernel times (a second loop with an event pair around every launch),
+    and ms per replay of the call captured in a CUDA graph."""
     import torch
     from megatron_tensor_transformer_w1_gb300 import tpffn as abi
     from megatron_tensor_transformer_w1_gb300.ffn import TensorParallelFFN
@@ -423,20 +425,44 @@ def time_workload(w, dev, steps, fused, seed=0, overlap=False):
     res = {}
 
     def timed(fn):
+        """ms per call from a plain loop (no per-launch events), the
+        per-kernel times from a second loop with them, and ms per replay of
+        the call captured once in a CUDA graph (no host launch cost)."""
         for _ in range(3):
             fn(0)
         torch.cuda.synchronize(dev)
-        abi.tp_ffn_kernel_times(ffn.plan, 0)
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         e0.record(st)
         for _ in range(steps):
-            fn(abi.TP_FLAG_TIMING)
+            fn(0)
         e1.record(st)
+        torch.cuda.synchronize(dev)
+        ms = e0.elapsed_time(e1) / steps
+        abi.tp_ffn_kernel_times(ffn.plan, 0)
+        for _ in range(steps):
+            fn(abi.TP_FLAG_TIMING)
         torch.cuda.synchronize(dev)
         per = {}
         for name, t in abi.tp_ffn_kernel_times(ffn.plan, 100000):
             per.setdefault(name, []).append(t)
-        return e0.elapsed_time(e1) / steps, {k: round(sum(v) / len(v), 4) for k, v in per.items()}
+        graph_ms = None
+        if graphs:
+            try:
+                g = torch.cuda.CUDAGraph()
+                with torch.cuda.graph(g):
+                    fn(0)
+                g.replay()
+                torch.cuda.synchronize(dev)
+                e0.record(st)
+                for _ in range(steps):
+                    g.replay()
+                e1.record(st)
+                torch.cuda.synchronize(dev)
+                graph_ms = round(e0.elapsed_time(e1) / steps, 4)
+                del g
+            except Exception as exc:  # report, do not fail the bench line
+                graph_ms = f"capture failed: {type(exc).__name__}: {exc}"[:160]
+        return ms, {k: round(sum(v) / len(v), 4) for k, v in per.items()}, graph_ms
 
     out = {}
     f = (abi.TP_SUM_FUSED if fused else 0) | (abi.TP_SUM_OVERLAP if overlap else 0)
@@ -447,10 +473,12 @@ def time_workload(w, dev, steps, fused, seed=0, overlap=False):
 
     def fwd(extra):
         abi.check(abi.tp_ffn_fwd(ffn.plan, w.N, inp["x"], w13p, w2p, inp["b1"], inp["b2"], y, None, saved, ws,
-                                 ws.numel(), f | extra, st), "fwd")
+                                 ws.numel(), f | extra, torch.cuda.current_stream(dev)), "fwd")
 
-    out["fwd_ms"], out["fwd_kernels"] = timed(fwd)
+    out["fwd_ms"], out["fwd_kernels"], out["fwd_graph_ms"] = timed(fwd)
     out["fwd_tflops"] = round(w.fwd_flops() / (out["fwd_ms"] * 1e-3) / 1e12, 3)
+    if isinstance(out["fwd_graph_ms"], float):
+        out["fwd_graph_tflops"] = round(w.fwd_flops() / (out["fwd_graph_ms"] * 1e-3) / 1e12, 3)
     if not w.fwd_only:
         dx = torch.empty(w.N, w.d_in, dtype=ffn.torch_dtype, device=dev)
         dw13p = None if w13p is None else torch.empty_like(w13p)
@@ -460,10 +488,12 @@ def time_workload(w, dev, steps, fused, seed=0, overlap=False):
 
         def bwd(extra):
             abi.check(abi.tp_ffn_bwd(ffn.plan, w.N, inp["x"], w13p, w2p, saved, inp["dy"], dx, None, dw13p, dw2p,
-                                     db1, db2, ws, ws.numel(), f | extra, st), "bwd")
+                                     db1, db2, ws, ws.numel(), f | extra, torch.cuda.current_stream(dev)), "bwd")
 
-        out["bwd_ms"], out["bwd_kernels"] = timed(bwd)
+        out["bwd_ms"], out["bwd_kernels"], out["bwd_graph_ms"] = timed(bwd)
         out["bwd_tflops"] = round(w.bwd_flops() / (out["bwd_ms"] * 1e-3) / 1e12, 3)
+        if isinstance(out["bwd_graph_ms"], float):
+            out["bwd_graph_tflops"] = round(w.bwd_flops() / (out["bwd_graph_ms"] * 1e-3) / 1e12, 3)
     out["fwd_ms"] = round(out["fwd_ms"], 4)
     if "bwd_ms" in out:
         out["bwd_ms"] = round(out["bwd_ms"], 4)
@@ -488,8 +518,8 @@ def run_standalone_sum(dev, steps, peaks):
     overlapped variant (TP_SUM_OVERLAP) hides behind the row-sharded GEMM."""
     from synth import WORKLOADS
     w = WORKLOADS[MAIN]
-    r = time_workload(w, dev, steps, fused=False)
-    o = time_workload(w, dev, steps, fused=False, overlap=True)
+    r = time_workload(w, dev, steps, fused=False, graphs=False)
+    o = time_workload(w, dev, steps, fused=False, overlap=True, graphs=False)
     nbytes = w.T_p * w.N * w.d * 4 + w.N * w.d * 2  # fp32 partials read + bf16 result written
     out = {"workload": MAIN, "fwd_ms": r["fwd_ms"], "bwd_ms": r["bwd_ms"],
            "step_tflops_fwd_bwd": round((w.fwd_flops() + w.bwd_flops()) / ((r["fwd_ms"] + r["bwd_ms"]) * 1e-3) / 1e12, 2),
