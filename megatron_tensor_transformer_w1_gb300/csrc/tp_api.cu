@@ -90,8 +90,6 @@ int64_t colsum_chunk(int64_t rows) {
 
 struct WsLayout {
   size_t h = 0, part = 0, D = 0, cs = 0, ks = 0, total = 0;
-  size_t cnt = 0;     // per-tile part counters of the K-split up GEMM (in the header)
-  size_t clear = 0;   // header bytes every call zeroes: the error word (and the counters)
   bool has_part = false, has_ks = false;
 };
 
@@ -121,31 +119,9 @@ int choose_ksplit(const tp_ffn_plan* p, int64_t n, int num_sms) {
   return best;
 }
 
-// Tiles of the K-split up GEMM (one counter each): T_p x ceil(W / 256).
-int64_t ksplit_tiles(const tp_ffn_plan* p) { return p->T_p * ((hidden_width(p) + 255) / 256); }
-
-// The K-split up GEMM forms h itself (EPI_SWIGLU_KSPLIT); TPFFN_KSPLIT_FOLD=0
-// in the environment selects the separate combine kernel instead (for
-// comparisons; the results are bit-identical).
-bool ksplit_fold_enabled() {
-  static const bool on = [] {
-    const char* v = getenv("TPFFN_KSPLIT_FOLD");
-    return !(v && v[0] == '0');
-  }();
-  return on;
-}
-
 WsLayout ws_layout(const tp_ffn_plan* p, int64_t n, int flags) {
   WsLayout L;
-  // header: the error word at 0; for decode-sized SwiGLU calls the K-split
-  // part counters from byte 16.  Every call zeroes `clear` bytes of it.
-  L.clear = sizeof(int);
-  size_t off = kAlign;
-  if (ksplit_shape(p, n)) {
-    L.cnt = 16;
-    L.clear = 16 + static_cast<size_t>(ksplit_tiles(p)) * sizeof(int);
-    off = align_up(L.clear);
-  }
+  size_t off = kAlign;  // error word + header
   const size_t e = esz(p);
   if (p->act != TP_ACT_NONE) {
     L.h = off;
@@ -203,8 +179,7 @@ void timing_after(void* user, cudaStream_t stream) {
   p->n_events++;
 }
 
-int make_ctx(const tp_ffn_plan* p, void* workspace, int flags, cudaStream_t stream, LaunchCtx& ctx,
-             size_t clear_bytes = sizeof(int)) {
+int make_ctx(const tp_ffn_plan* p, void* workspace, int flags, cudaStream_t stream, LaunchCtx& ctx) {
   ctx.stream = stream;
   ctx.err = static_cast<int*>(workspace);
   ctx.num_sms = num_sms_current();
@@ -216,7 +191,7 @@ int make_ctx(const tp_ffn_plan* p, void* workspace, int flags, cudaStream_t stre
     ctx.after = timing_after;
     ctx.user = const_cast<tp_ffn_plan*>(p);
   }
-  if (cudaMemsetAsync(workspace, 0, clear_bytes, stream) != cudaSuccess) return TP_ERR_CUDA;
+  if (cudaMemsetAsync(workspace, 0, sizeof(int), stream) != cudaSuccess) return TP_ERR_CUDA;
   return TP_OK;
 }
 
@@ -517,30 +492,19 @@ static int fwd_impl(const tp_ffn_plan* p, int64_t n, const void* x, const void* 
     g.out_bf16 = out_bf16;
     const int ks = L.has_ks ? choose_ksplit(p, n, ctx.num_sms) : 1;
     if (ks > 1) {
-      // fp32 parts of a and g; the unit that finishes a tile's last part
-      // forms h (and the saved a, g) from them -- or, with the fold turned
-      // off, a separate combine kernel does
+      // fp32 parts of a and g, then the SwiGLU combine
       float* parts = reinterpret_cast<float*>(ws + L.ks);
-      void* ag = saved ? static_cast<char*>(saved) + S.act : nullptr;
+      g.epi = EPI_F32;
       g.ksplit = ks;
       g.out = parts;
       g.out_bs = n * W;
       g.out_rs = W;
+      g.out2 = nullptr;
       g.n_store = W;
-      if (ksplit_fold_enabled()) {
-        g.epi = EPI_SWIGLU_KSPLIT;
-        g.out2 = h;
-        g.out2_bs = n * sp;
-        g.out2_rs = sp;
-        g.aux_out = ag;
-        g.counters = reinterpret_cast<int*>(ws + L.cnt);
-        rc = run_gemm(p, g, ctx);
-      } else {
-        g.epi = EPI_F32;
-        g.out2 = nullptr;
-        rc = run_gemm(p, g, ctx);
-        if (!rc) rc = launch_swiglu_combine(parts, ks, static_cast<int>(T), n, sp, h, ag, ctx, "swiglu_combine");
-      }
+      rc = run_gemm(p, g, ctx);
+      if (!rc)
+        rc = launch_swiglu_combine(parts, ks, static_cast<int>(T), n, sp, h,
+                                   saved ? static_cast<char*>(saved) + S.act : nullptr, ctx, "swiglu_combine");
     } else {
       rc = run_gemm(p, g, ctx);
     }
@@ -610,7 +574,7 @@ int tp_ffn_fwd(const tp_ffn_plan* p, int64_t n, const void* x, const void* w13p,
   int rc = validate_fwd(p, n, x, w13p, w2p, b1, b2, y, partials, saved, workspace, workspace_bytes, flags);
   if (rc) return rc;
   LaunchCtx ctx;
-  rc = make_ctx(p, workspace, flags, reinterpret_cast<cudaStream_t>(stream), ctx, ws_layout(p, n, flags).clear);
+  rc = make_ctx(p, workspace, flags, reinterpret_cast<cudaStream_t>(stream), ctx);
   if (!rc) rc = fwd_impl(p, n, x, w13p, w2p, b1, b2, y, partials, saved, workspace, flags, ctx, nullptr);
   return finish_call(p, ctx, rc, flags, workspace);
 }
@@ -870,7 +834,7 @@ int tp_ffn_fwd_seq_parallel(const tp_ffn_plan* p, int64_t n, const void* const* 
   rc = validate_fwd(p, n, x_full, w13p, w2p, b1, b2, y_full, nullptr, saved, workspace, base, flags);
   if (rc) return rc;
   LaunchCtx ctx;
-  rc = make_ctx(p, workspace, flags, reinterpret_cast<cudaStream_t>(stream), ctx, ws_layout(p, n, flags).clear);
+  rc = make_ctx(p, workspace, flags, reinterpret_cast<cudaStream_t>(stream), ctx);
   const int64_t d_in = p->act == TP_ACT_NONE ? p->d_ff : p->d;
   if (!rc) rc = launch_gather_rows(xs, x_full, d_in, esz(p), ctx, "all_gather_x");
   if (!rc) rc = fwd_impl(p, n, x_full, w13p, w2p, b1, b2, y_full, nullptr, saved, workspace, flags, ctx, &ys);

@@ -81,9 +81,6 @@ struct Params {
   int dbg_slot;  // launch slot of the optional wait counters (instrumented builds only)
   int ksplit;    // one-SM kernel: K split into this many parts (1: none)
   int raster;    // pair kernel tile order (RASTER_*)
-  int* cnt;      // EPI_SWIGLU_KSPLIT: per-tile count of finished K parts (zeroed by the caller)
-  void* ag_out;  // EPI_SWIGLU_KSPLIT: saved [a | g] (bf16, strides of out) or nullptr
-  int aux_prefetch;  // backward epilogues: prefetch the next tile's saved activations into L2
 };
 
 // Pair-kernel tile orders.  Grouped raster order (the default) lets the
@@ -276,109 +273,15 @@ __device__ __forceinline__ void epilogue_tile(const Params& p, int b, int row, b
           load_bf16x8(ag + 128, g);
 #pragma unroll
           for (int j = 0; j < 8; ++j) {
-            const float sg = sigmoid_f(a[j]);
-            dg[j] = v[j] * a[j] * sg;                          // dh * silu(a)
-            da[j] = v[j] * g[j] * sg * (1.0f + a[j] * (1.0f - sg));  // dh * g * silu'(a)
+            float sg, om;
+            sigmoid_pair(a[j], sg, om);
+            dg[j] = v[j] * a[j] * sg;                     // dh * silu(a)
+            da[j] = v[j] * g[j] * sg * (1.0f + a[j] * om);  // dh * g * silu'(a)
           }
           __nv_bfloat16* o = static_cast<__nv_bfloat16*>(p.out) + b * p.out_bs + (long long)row * p.out_rs + col;
           store_bf16x8(o, da);
           store_bf16x8(o + 128, dg);
         }
-      }
-    }
-  }
-}
-
-// K-split SwiGLU forward (one-SM kernel, decode-sized token counts: M <= 32,
-// so every live row is in TMEM lane quarter 0 and one warp holds them all;
-// the other epilogue warps have nothing to do here).  Work unit (tile, kh)
-// accumulates K part kh of a 256-column [a | g] tile.  The warp writes the
-// fp32 part to batch kh * NB + b of `out`; the unit that completes the tile's
-// count of parts then sums the parts in the order k = 0, 1, .. (its own from
-// tensor memory, the others from global memory) and forms h = silu(a) g --
-// the same arithmetic, in the same order, as the separate combine kernel --
-// into out2 (and a, g into ag_out).  Only warp-level synchronisation is used.
-__device__ __forceinline__ void epilogue_ksplit_swiglu(const Params& p, int tile, int kh, int b, int row0, int lane,
-                                                       int nb, uint32_t taddr) {
-  if (row0 >= p.M) return;  // no live row in this lane quarter
-  const int row = row0 + lane;
-  const bool row_ok = row < p.M;
-  const long long prow = (long long)row * p.out_rs + nb * 256;  // this row's tile columns within a part
-  float* own = static_cast<float*>(p.out) + (long long)(kh * p.NB + b) * p.out_bs + prow;
-#pragma unroll 1
-  for (int c = 0; c < 8; ++c) {
-    uint32_t r[32];
-    __syncwarp();
-    tmem_ld32(taddr + c * 32, r);
-    tmem_wait_ld();
-    if (row_ok) {
-#pragma unroll
-      for (int q = 0; q < 8; ++q)
-        *reinterpret_cast<float4*>(own + c * 32 + q * 4) =
-            make_float4(__uint_as_float(r[q * 4]), __uint_as_float(r[q * 4 + 1]), __uint_as_float(r[q * 4 + 2]),
-                        __uint_as_float(r[q * 4 + 3]));
-    }
-  }
-  // publish this part, then count it (fence, then atomic: the writes above
-  // are visible to whichever unit observes the final count)
-  __threadfence();
-  __syncwarp();
-  int last = 0;
-  if (lane == 0) last = atomicAdd(p.cnt + tile, 1) == p.ksplit - 1;
-  last = __shfl_sync(0xffffffffu, last, 0);
-  if (!last) return;
-  __threadfence();
-  __nv_bfloat16* hout = static_cast<__nv_bfloat16*>(p.out2) + b * p.out2_bs + (long long)row * p.out2_rs + nb * 128;
-  __nv_bfloat16* sv = p.ag_out ? static_cast<__nv_bfloat16*>(p.ag_out) + b * p.out_bs + prow : nullptr;
-#pragma unroll 1
-  for (int c = 0; c < 4; ++c) {
-    uint32_t ra[32], rg[32];
-    __syncwarp();
-    tmem_ld32(taddr + c * 32, ra);
-    tmem_ld32(taddr + 128 + c * 32, rg);
-    tmem_wait_ld();
-    if (!row_ok) continue;
-#pragma unroll
-    for (int q = 0; q < 4; ++q) {
-      float a[8], g[8], h[8];
-#pragma unroll 1
-      for (int k = 0; k < p.ksplit; ++k) {
-        float pa[8], pg[8];
-        if (k == kh) {
-#pragma unroll
-          for (int j = 0; j < 8; ++j) {
-            pa[j] = __uint_as_float(ra[q * 8 + j]);
-            pg[j] = __uint_as_float(rg[q * 8 + j]);
-          }
-        } else {
-          const float* src =
-              static_cast<const float*>(p.out) + (long long)(k * p.NB + b) * p.out_bs + prow + c * 32 + q * 8;
-#pragma unroll
-          for (int i = 0; i < 2; ++i) {
-            const float4 va = __ldcg(reinterpret_cast<const float4*>(src) + i);
-            const float4 vg = __ldcg(reinterpret_cast<const float4*>(src + 128) + i);
-            pa[4 * i] = va.x;
-            pa[4 * i + 1] = va.y;
-            pa[4 * i + 2] = va.z;
-            pa[4 * i + 3] = va.w;
-            pg[4 * i] = vg.x;
-            pg[4 * i + 1] = vg.y;
-            pg[4 * i + 2] = vg.z;
-            pg[4 * i + 3] = vg.w;
-          }
-        }
-#pragma unroll
-        for (int j = 0; j < 8; ++j) {
-          a[j] = k == 0 ? pa[j] : a[j] + pa[j];
-          g[j] = k == 0 ? pg[j] : g[j] + pg[j];
-        }
-      }
-#pragma unroll
-      for (int j = 0; j < 8; ++j) h[j] = a[j] * sigmoid_f(a[j]) * g[j];
-      store_bf16x8(hout + c * 32 + q * 8, h);
-      if (sv) {
-        store_bf16x8(sv + c * 32 + q * 8, a);
-        store_bf16x8(sv + 128 + c * 32 + q * 8, g);
       }
     }
   }
@@ -578,15 +481,11 @@ __global__ void __launch_bounds__(threads_for<EPI>(), 1)
       const int kh = unit_split(p, unit, tile, kb0, nkb);
       int b, mb, nb;
       decode_tile(p, tile, b, mb, nb);
+      b += kh * p.NB;  // K part kh: fp32 batch kh * NB + b (EPI_F32 only)
       const int row = mb * BM + quarter * 32 + lane;
       const uint32_t taddr = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) +
                              static_cast<uint32_t>(buf * BN);
-      if constexpr (EPI == EPI_SWIGLU_KSPLIT) {
-        epilogue_ksplit_swiglu(p, tile, kh, b, mb * BM + quarter * 32, lane, nb, taddr);
-      } else {
-        b += kh * p.NB;  // K part kh: fp32 batch kh * NB + b (EPI_F32 only)
-        epilogue_tile<BN, EPI>(p, b, row, row < p.M, nb * BN, nb, taddr, (warp - 2) >> 2);
-      }
+      epilogue_tile<BN, EPI>(p, b, row, row < p.M, nb * BN, nb, taddr, (warp - 2) >> 2);
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&tempty[buf]);
@@ -989,7 +888,6 @@ __global__ void __launch_bounds__(threads_for<EPI>(), 1)
       uint8_t* xslot = smem + L::AUX_OFF + (warp - 2) * L::AUX_SLOT;
       const uint32_t xs = smem_u32(xslot);
       uint64_t* xb = &xbar[warp - 2];
-      const bool aux_prefetch_on = p.aux_prefetch != 0;
       uint32_t xph = 0;
       bool pending = false;
       auto issue = [&](int t, int c) {  // lane 0
@@ -1007,34 +905,12 @@ __global__ void __launch_bounds__(threads_for<EPI>(), 1)
           tma_load_3d(xslot, &tmX, xb, n, row0, b);
         }
       };
-      // this warp's blocks of tile t, from DRAM into L2: issued one tile
-      // ahead, so that the slot copies of a tile find their data in L2
-      // instead of waiting a DRAM round trip per chunk
-      auto prefetch_tile = [&](int t) {  // lane 0
-        int b, mp, nb;
-        decode_pair_tile(p, t, b, mp, nb);
-        const int row0 = mp * 256 + static_cast<int>(rank) * 128 + quarter * 32;
-        for (int c = c0; c < c0 + CPW; ++c) {
-          const int n = nb * BN + c * 32;
-          if constexpr (EPI == EPI_SWIGLU_BWD) {
-            const int col = (n >> 7) * 256 + (n & 127);
-            tma_prefetch_l2_3d(&tmX, col, row0, b);
-            tma_prefetch_l2_3d(&tmX, col + 128, row0, b);
-          } else {
-            tma_prefetch_l2_3d(&tmX, n, row0, b);
-          }
-        }
-      };
       if (cluster_id < num_tiles) {
-        if (lane == 0) {
-          issue(cluster_id, c0);
-          if (aux_prefetch_on) prefetch_tile(cluster_id);
-        }
+        if (lane == 0) issue(cluster_id, c0);
         pending = true;
       }
       bool ok = true;
       for (int tile = cluster_id; tile < num_tiles && ok; tile += num_clusters, ++local) {
-        if (aux_prefetch_on && lane == 0 && tile + num_clusters < num_tiles) prefetch_tile(tile + num_clusters);
         const int buf = local & 1;
         const uint32_t use = static_cast<uint32_t>(local >> 1);
         {
@@ -1100,9 +976,10 @@ __global__ void __launch_bounds__(threads_for<EPI>(), 1)
               unpack_bf16x8(gg[q], g);
 #pragma unroll
               for (int j = 0; j < 8; ++j) {
-                const float sg = sigmoid_f(a[j]);
-                dg[j] = v[j] * a[j] * sg;                                // dh * silu(a)
-                da[j] = v[j] * g[j] * sg * (1.0f + a[j] * (1.0f - sg));  // dh * g * silu'(a)
+                float sg, om;
+                sigmoid_pair(a[j], sg, om);
+                dg[j] = v[j] * a[j] * sg;                     // dh * silu(a)
+                da[j] = v[j] * g[j] * sg * (1.0f + a[j] * om);  // dh * g * silu'(a)
               }
               const long long col = (long long)(n >> 7) * 256 + (n & 127);
               store_bf16x8(out + col, da);
@@ -1305,15 +1182,8 @@ static int launch_inst(const GemmSpec& s, LaunchCtx& ctx) {
     attr_done.fetch_or(bit);
   }
   p.ksplit = s.ksplit;
-  if (s.ksplit < 1 || (s.ksplit > 1 && ((EPI != EPI_F32 && EPI != EPI_SWIGLU_KSPLIT) || s.G != 1 ||
-                                        p.k_blocks < 2 * s.ksplit)))
+  if (s.ksplit < 1 || (s.ksplit > 1 && (EPI != EPI_F32 || s.G != 1 || p.k_blocks < 2 * s.ksplit)))
     return TP_ERR_INVALID;
-  if (EPI == EPI_SWIGLU_KSPLIT) {
-    // one live lane quarter (M <= 32) and a per-tile count of finished parts
-    if (s.M > 32 || !s.counters || !s.out2 || BN != 256) return TP_ERR_INVALID;
-    p.cnt = s.counters;
-    p.ag_out = s.aux_out;
-  }
   const long long tiles = static_cast<long long>(p.tiles_m) * p.tiles_n * p.NB * s.ksplit;  // work units
   if (tiles <= 0 || p.k_blocks <= 0) return TP_ERR_INVALID;
   int grid = static_cast<int>(tiles < ctx.num_sms ? tiles : ctx.num_sms);
@@ -1359,13 +1229,6 @@ static int make_aux_map(CUtensorMap* m, const GemmSpec& s) {
   return r == CUDA_SUCCESS ? 0 : TP_ERR_CUDA;
 }
 
-// TPFFN_AUX_PREFETCH=0 in the environment turns off the L2 prefetch of the
-// next tile's saved activations in the backward epilogues (for comparisons).
-static bool aux_prefetch_enabled() {
-  static const bool on = !getenv_flag_off("TPFFN_AUX_PREFETCH");
-  return on;
-}
-
 // TPFFN_RASTER=1 in the environment selects the shared-operand-fastest
 // orders for the per-shard GEMMs (for comparisons).
 static bool raster_by_sharing() {
@@ -1393,7 +1256,6 @@ static int launch_pair(const GemmSpec& s, LaunchCtx& ctx) {
   if (s.ksplit != 1) return TP_ERR_INVALID;  // the K split serves decode-sized GEMMs only
   Params p{};
   p.ksplit = 1;
-  p.aux_prefetch = aux_prefetch_enabled() ? 1 : 0;
   p.raster = RASTER_GROUPED;
   if (s.NB > 1 && s.G == 1 && raster_by_sharing()) {
     if (s.A.bsel == 0 && s.B.bsel != 0) p.raster = RASTER_M_FAST;
@@ -1538,7 +1400,6 @@ int launch_tc_gemm(const GemmSpec& s, LaunchCtx& ctx) {
   if (s.M <= 32 && !amn && !bmn) {  // decode: weights stream from HBM
     if (s.epi == EPI_SWIGLU_FWD) return launch_inst<256, 6, EPI_SWIGLU_FWD, false, false, 32>(s, ctx);
     if (s.epi == EPI_F32) return launch_inst<256, 6, EPI_F32, false, false, 32>(s, ctx);
-    if (s.epi == EPI_SWIGLU_KSPLIT) return launch_inst<256, 6, EPI_SWIGLU_KSPLIT, false, false, 32>(s, ctx);
   }
   switch (s.epi) {
     case EPI_SWIGLU_FWD:

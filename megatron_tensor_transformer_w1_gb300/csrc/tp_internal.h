@@ -27,11 +27,6 @@ enum EpiKind : int {
   EPI_SWIGLU_FWD = 3,  // acc = [a | g] per 256-col tile; out = silu(a)*g; out2 = a, g
   EPI_GELU_BWD = 4,    // out = acc * gelu_tanh'(aux)             (dz)
   EPI_SWIGLU_BWD = 5,  // acc = dh; aux = saved [a|g]; out = [da | dg]
-  // K-split SwiGLU forward (decode-sized one-SM kernel): each K part writes
-  // its fp32 [a | g] to `out` (batch k * NB + b), and the part that completes
-  // a tile (per-tile counter) sums the parts in the order k = 0, 1, .. and
-  // writes h = silu(a) g to out2 and, when aux_out is set, a and g
-  EPI_SWIGLU_KSPLIT = 6,
 };
 
 struct Operand {
@@ -57,10 +52,6 @@ struct GemmSpec {
   // K split (EPI_F32, G = 1, decode-sized M only): part k of the K blocks is
   // accumulated on its own and written as fp32 batch k * NB + b of `out`
   int ksplit = 1;
-  // EPI_SWIGLU_KSPLIT: one zeroed int per (batch, N tile), and the saved-
-  // activation output [a | g] (bf16, with the strides of `out`) or nullptr
-  int* counters = nullptr;
-  void* aux_out = nullptr;
 };
 
 // Launch context of one API call.

@@ -378,8 +378,9 @@ __global__ void simt_gemm_kernel(const SimtParams p) {
         const long long col = (n >> 7) * 256 + (n & 127);
         const float a = p.aux[b * p.aux_bs + m * p.aux_rs + col];
         const float g = p.aux[b * p.aux_bs + m * p.aux_rs + col + 128];
-        const float sg = sigmoid_f(a);
-        p.out[b * p.out_bs + m * p.out_rs + col] = v * g * sg * (1.0f + a * (1.0f - sg));
+        float sg, om;
+        sigmoid_pair(a, sg, om);
+        p.out[b * p.out_bs + m * p.out_rs + col] = v * g * sg * (1.0f + a * om);
         p.out[b * p.out_bs + m * p.out_rs + col + 128] = v * a * sg;
         break;
       }
