@@ -273,10 +273,9 @@ __device__ __forceinline__ void epilogue_tile(const Params& p, int b, int row, b
           load_bf16x8(ag + 128, g);
 #pragma unroll
           for (int j = 0; j < 8; ++j) {
-            float sg, om;
-            sigmoid_pair(a[j], sg, om);
-            dg[j] = v[j] * a[j] * sg;                     // dh * silu(a)
-            da[j] = v[j] * g[j] * sg * (1.0f + a[j] * om);  // dh * g * silu'(a)
+            const float sg = sigmoid_f(a[j]);
+            dg[j] = v[j] * a[j] * sg;                          // dh * silu(a)
+            da[j] = v[j] * g[j] * sg * (1.0f + a[j] * (1.0f - sg));  // dh * g * silu'(a)
           }
           __nv_bfloat16* o = static_cast<__nv_bfloat16*>(p.out) + b * p.out_bs + (long long)row * p.out_rs + col;
           store_bf16x8(o, da);
@@ -976,10 +975,9 @@ __global__ void __launch_bounds__(threads_for<EPI>(), 1)
               unpack_bf16x8(gg[q], g);
 #pragma unroll
               for (int j = 0; j < 8; ++j) {
-                float sg, om;
-                sigmoid_pair(a[j], sg, om);
-                dg[j] = v[j] * a[j] * sg;                     // dh * silu(a)
-                da[j] = v[j] * g[j] * sg * (1.0f + a[j] * om);  // dh * g * silu'(a)
+                const float sg = sigmoid_f(a[j]);
+                dg[j] = v[j] * a[j] * sg;                                // dh * silu(a)
+                da[j] = v[j] * g[j] * sg * (1.0f + a[j] * (1.0f - sg));  // dh * g * silu'(a)
               }
               const long long col = (long long)(n >> 7) * 256 + (n & 127);
               store_bf16x8(out + col, da);

@@ -251,6 +251,9 @@ __global__ void __launch_bounds__(256) colsum_pass1_kernel(const void* in, int i
                                                            long long cols, long long rs, long long bs,
                                                            float* scratch, long long chunk_rows, long long chunks) {
   __shared__ float part[8][256 + 4];
+  // a programmatic dependent of the kernel that wrote `in`
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   const int cg = threadIdx.x & 31, lane = threadIdx.x >> 5;
   const long long c0 = blockIdx.x * 256LL + cg * 8;
   const long long chunk = blockIdx.y;
@@ -289,6 +292,8 @@ __global__ void __launch_bounds__(256) colsum_pass1_kernel(const void* in, int i
 }
 __global__ void colsum_pass2_kernel(const float* scratch, long long cols, long long chunks, void* out, int out_bf16,
                                     long long out_bs) {
+  asm volatile("griddepcontrol.wait;" ::: "memory");  // pass 1's chunk sums are visible
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   const long long col = blockIdx.x * (long long)blockDim.x + threadIdx.x;
   const long long b = blockIdx.y;
   if (col >= cols) return;
@@ -378,9 +383,8 @@ __global__ void simt_gemm_kernel(const SimtParams p) {
         const long long col = (n >> 7) * 256 + (n & 127);
         const float a = p.aux[b * p.aux_bs + m * p.aux_rs + col];
         const float g = p.aux[b * p.aux_bs + m * p.aux_rs + col + 128];
-        float sg, om;
-        sigmoid_pair(a, sg, om);
-        p.out[b * p.out_bs + m * p.out_rs + col] = v * g * sg * (1.0f + a * om);
+        const float sg = sigmoid_f(a);
+        p.out[b * p.out_bs + m * p.out_rs + col] = v * g * sg * (1.0f + a * (1.0f - sg));
         p.out[b * p.out_bs + m * p.out_rs + col + 128] = v * a * sg;
         break;
       }
@@ -469,9 +473,9 @@ int launch_pack_rows(const void* W2, void* out, int T_p, int64_t s, int64_t s_pa
 // Launch as a programmatic dependent of the stream's previous kernel (the
 // kernel waits for its results with griddepcontrol.wait).
 template <typename... KArgs, typename... Args>
-static void launch_pdl(void (*kern)(KArgs...), int grid, int block, cudaStream_t stream, Args... args) {
+static void launch_pdl(void (*kern)(KArgs...), dim3 grid, int block, cudaStream_t stream, Args... args) {
   cudaLaunchConfig_t cfg{};
-  cfg.gridDim = dim3(static_cast<unsigned>(grid));
+  cfg.gridDim = grid;
   cfg.blockDim = dim3(static_cast<unsigned>(block));
   cfg.dynamicSmemBytes = 0;
   cfg.stream = stream;
@@ -494,10 +498,10 @@ int launch_shard_sum(const float* partials, int T_p, int64_t rows, int64_t cols,
   if (vec) {
     const int grid = grid_for(plane / 8, 256, ctx.num_sms);
     if (out_bf16)
-      launch_pdl(shard_sum_vec8_kernel<1>, grid, 256, ctx.stream, partials, T_p, plane, cols,
+      launch_pdl(shard_sum_vec8_kernel<1>, dim3(grid), 256, ctx.stream, partials, T_p, plane, cols,
                  static_cast<const __nv_bfloat16*>(bias), static_cast<const float*>(nullptr), out, stride);
     else
-      launch_pdl(shard_sum_vec8_kernel<0>, grid, 256, ctx.stream, partials, T_p, plane, cols,
+      launch_pdl(shard_sum_vec8_kernel<0>, dim3(grid), 256, ctx.stream, partials, T_p, plane, cols,
                  static_cast<const __nv_bfloat16*>(nullptr), static_cast<const float*>(bias), out, stride);
   } else {
     shard_sum_scalar_kernel<<<grid_for(plane, 256, ctx.num_sms), 256, 0, ctx.stream>>>(
@@ -571,7 +575,7 @@ int launch_swiglu_combine(const float* parts, int ksplit, int T_p, int64_t rows,
       reinterpret_cast<uintptr_t>(saved) % 16)
     return TP_ERR_ALIGN;
   if (ctx.before) ctx.before(ctx.user, name, ctx.stream);
-  launch_pdl(swiglu_combine_kernel, grid_for(total, 256, ctx.num_sms), 256, ctx.stream, parts, ksplit,
+  launch_pdl(swiglu_combine_kernel, dim3(grid_for(total, 256, ctx.num_sms)), 256, ctx.stream, parts, ksplit,
              (long long)T_p * rows * 2 * s_pad, T_p, rows, s_pad, static_cast<__nv_bfloat16*>(h),
              static_cast<__nv_bfloat16*>(saved));
   if (ctx.after) ctx.after(ctx.user, ctx.stream);
@@ -656,11 +660,12 @@ int launch_colsum(const void* in, int in_bf16, int64_t batch, int64_t rows, int6
   if (ctx.before) ctx.before(ctx.user, name, ctx.stream);
   if (chunks > 0) {
     dim3 g1(static_cast<unsigned>((cols + 255) / 256), static_cast<unsigned>(chunks), static_cast<unsigned>(batch));
-    colsum_pass1_kernel<<<g1, 256, 0, ctx.stream>>>(in, in_bf16, rows, cols, rs, bs, scratch, chunk_rows, chunks);
+    launch_pdl(colsum_pass1_kernel, g1, 256, ctx.stream, in, in_bf16, rows, cols, rs, bs, scratch, chunk_rows,
+               chunks);
     ctx.launches++;
   }
   dim3 g2(static_cast<unsigned>((cols + 255) / 256), static_cast<unsigned>(batch));
-  colsum_pass2_kernel<<<g2, 256, 0, ctx.stream>>>(scratch, cols, chunks, out, out_bf16, out_bs);
+  launch_pdl(colsum_pass2_kernel, g2, 256, ctx.stream, scratch, cols, chunks, out, out_bf16, out_bs);
   ctx.launches++;
   if (ctx.after) ctx.after(ctx.user, ctx.stream);
   return cudaPeekAtLastError() == cudaSuccess ? 0 : TP_ERR_CUDA;

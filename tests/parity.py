@@ -40,11 +40,12 @@ F32_REL = 1e-4
 # exact sums of bf16 products for K = 256 .. 16384: the largest error seen was
 # about 5.6e-9 * K * ||p||_2 (p = the K products).  The model below, 2^-26 * K
 # * ||p||_2, is 2.7 times that.  EVAL_ERR and EVAL_ERR_D cover the fp32
-# evaluation of the activation functions in the kernels (the logistic forms
-# with the SFU's ex2 / rcp): relative errors of at most 2^-19 for the values
-# h, silu(a) and 2^-15 for the derivative factors gelu', silu' -- the bounds
-# tests/test_gpu_activation_accuracy.py holds the kernels to (measured
-# 9.3e-7 and 1.4e-5).
+# evaluation of the activation functions in the kernels (GELU in logistic
+# form with the SFU's ex2 / rcp, SwiGLU's logistic with expf and an IEEE
+# division): relative errors of at most 2^-19 for the values h, silu(a) and
+# 2^-15 for the derivative factors gelu', silu' -- the bounds that
+# tests/test_gpu_activation_accuracy.py holds the kernels to (measured at
+# most 9.3e-7 and 1.4e-5).
 ACC_ERR = 2.0 ** -26
 EVAL_ERR = 2.0 ** -19
 EVAL_ERR_D = 2.0 ** -15
