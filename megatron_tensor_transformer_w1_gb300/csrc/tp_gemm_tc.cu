@@ -81,6 +81,7 @@ struct Params {
   int dbg_slot;  // launch slot of the optional wait counters (instrumented builds only)
   int ksplit;    // one-SM kernel: K split into this many parts (1: none)
   int raster;    // pair kernel tile order (RASTER_*)
+  int o_swap;    // pair kernel TMA stores: output maps are {cols, batch, rows} (batch stride < row stride)
 };
 
 // Pair-kernel tile orders.  Grouped raster order (the default) lets the
@@ -608,15 +609,22 @@ __host__ __device__ constexpr bool aux_staged() {
   return EPI == EPI_SWIGLU_BWD || EPI == EPI_GELU_BWD;
 }
 
-template <int EPI>
+// Epilogues that write their tile through shared memory with TMA stores:
+// each epilogue warp stages its 32 rows x 32 columns per output in an 8 KB
+// buffer (64-byte swizzled bf16 boxes, 128-byte swizzled fp32 boxes) and one
+// lane stores them as whole lines, instead of 32 rows x 16 bytes per store
+// instruction from the threads.  The buffers take one operand stage.
+constexpr int OUT_BUF = 8192;  // per epilogue warp
+
+template <int EPI, bool TMA>
 struct PairLayout {
-  static constexpr int STAGES = aux_staged<EPI>() ? 6 : 7;
+  static constexpr int STAGES = (aux_staged<EPI>() || TMA) ? 6 : 7;
   static constexpr int A_BYTES = BM * BK * 2;               // this CTA's 128 rows of A
   static constexpr int B_BYTES = (PAIR_BN / 2) * BK * 2;    // this CTA's half of B
   static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;     // 32 KB
   static constexpr int AUX_SLOT = 4096;                     // per epilogue warp
   static constexpr int AUX_OFF = STAGES * STAGE_BYTES;
-  static constexpr int AUX_BYTES = aux_staged<EPI>() ? epi_warps<EPI>() * AUX_SLOT : 0;
+  static constexpr int AUX_BYTES = aux_staged<EPI>() ? epi_warps<EPI>() * AUX_SLOT : (TMA ? 4 * OUT_BUF : 0);
   static constexpr int BAR_OFF = AUX_OFF + AUX_BYTES;
   static constexpr int SMEM = BAR_OFF + 256 + 1024;
   static constexpr uint32_t TMEM_COLS = 2 * PAIR_BN;
@@ -665,11 +673,164 @@ __device__ __forceinline__ void decode_pair_tile(const Params& p, int tile, int&
   nb = in_group / gm;
 }
 
-template <int EPI, bool AMN, bool BMN>
+// Shared-memory address of 16-byte chunk k of row r in a staged box with
+// 128-byte rows (128-byte TMA swizzle: chunk bits 4..6 XOR row bits 0..2).
+__device__ __forceinline__ uint32_t sw128(uint32_t base, int r, int k) {
+  return base + static_cast<uint32_t>(r * 128) + (static_cast<uint32_t>(k ^ (r & 7)) << 4);
+}
+__device__ __forceinline__ void sts128(uint32_t addr, uint4 v) {
+  asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w)
+               : "memory");
+}
+__device__ __forceinline__ uint4 pack8_bf16(const float* v) {
+  uint4 q;
+  q.x = pack_bf16x2(v[0], v[1]);
+  q.y = pack_bf16x2(v[2], v[3]);
+  q.z = pack_bf16x2(v[4], v[5]);
+  q.w = pack_bf16x2(v[6], v[7]);
+  return q;
+}
+
+// One tile's epilogue through TMA stores (pair kernel, one warp per TMEM lane
+// quarter).  The warp's 32 rows start at row0; lane = its row within them.
+// Rows past M and columns past n_store lie outside the output maps and are
+// not written.  `k` counts this warp's staged chunks (buffer rotation).
+template <int EPI>
+__device__ __forceinline__ void epilogue_tile_tma(const Params& p, const CUtensorMap* tmO, const CUtensorMap* tmO2,
+                                                  int b, int row0, int lane, int n0, int nb, uint32_t taddr,
+                                                  uint8_t* sbuf, uint32_t& k) {
+  const uint32_t sb = smem_u32(sbuf);
+  if constexpr (EPI == EPI_SWIGLU_FWD) {
+    // chunk c: 32 hidden units -> h (2 KB box), a and g (2 KB boxes); one 6 KB buffer
+#pragma unroll 1
+    for (int c = 0; c < 4; ++c) {
+      uint32_t ra[32], rg[32];
+      __syncwarp();
+      tmem_ld32(taddr + c * 32, ra);
+      tmem_ld32(taddr + 128 + c * 32, rg);
+      tmem_wait_ld();
+      if (lane == 0) bulk_wait_read<0>();  // the previous chunk's boxes have left the buffer
+      __syncwarp();
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        float h[8], a[8], g[8];
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          a[j] = __uint_as_float(ra[q * 8 + j]);
+          g[j] = __uint_as_float(rg[q * 8 + j]);
+          h[j] = a[j] * sigmoid_f(a[j]) * g[j];
+        }
+        sts128(sw64(sb, lane, q), pack8_bf16(h));
+        if (p.out2) {
+          sts128(sw64(sb + 2048, lane, q), pack8_bf16(a));
+          sts128(sw64(sb + 4096, lane, q), pack8_bf16(g));
+        }
+      }
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) {
+        const int hcol = nb * 128 + c * 32, acol = nb * 256 + c * 32;
+        if (row0 >= p.M) {
+          // every row of this warp lies past M: nothing to store (an empty
+          // group keeps the buffer accounting)
+        } else if (!p.o_swap) {
+          tma_store_3d(tmO, sbuf, hcol, row0, b);
+          if (p.out2) {
+            tma_store_3d(tmO2, sbuf + 2048, acol, row0, b);
+            tma_store_3d(tmO2, sbuf + 4096, acol + 128, row0, b);
+          }
+        } else {
+          tma_store_3d(tmO, sbuf, hcol, b, row0);
+          if (p.out2) {
+            tma_store_3d(tmO2, sbuf + 2048, acol, b, row0);
+            tma_store_3d(tmO2, sbuf + 4096, acol + 128, b, row0);
+          }
+        }
+        bulk_commit();
+      }
+      ++k;
+    }
+    return;
+  } else {
+    // EPI_OUT / EPI_F32 / EPI_GELU_FWD: chunk c = 32 columns; two 4 KB buffers
+    constexpr int NBUF = 2;
+#pragma unroll 1
+    for (int c = 0; c < PAIR_BN / 32; ++c) {
+      const int nc = n0 + c * 32;
+      if (nc >= p.n_store) break;  // columns past n_store: nothing to store (n_store is a multiple of 8)
+      uint32_t r[32];
+      __syncwarp();
+      tmem_ld32(taddr + c * 32, r);
+      tmem_wait_ld();
+      float bv[32];
+      if constexpr (EPI == EPI_OUT || EPI == EPI_GELU_FWD) {
+        if (p.bias) {
+          const __nv_bfloat16* bp = p.bias + b * p.bias_bs + nc;
+          if (nc + 32 <= p.bias_len && (reinterpret_cast<uintptr_t>(bp) & 15) == 0) {
+#pragma unroll
+            for (int q = 0; q < 4; ++q) load_bf16x8(bp + q * 8, bv + q * 8);
+          } else {
+#pragma unroll
+            for (int j = 0; j < 32; ++j) bv[j] = nc + j < p.bias_len ? __bfloat162float(bp[j]) : 0.f;
+          }
+        }
+      }
+      const uint32_t buf = sb + (k % NBUF) * 4096;
+      if (lane == 0) bulk_wait_read<NBUF - 1>();  // this buffer's previous boxes have left it
+      __syncwarp();
+      if constexpr (EPI == EPI_F32) {
+#pragma unroll
+        for (int q = 0; q < 8; ++q)
+          sts128(sw128(buf, lane, q), make_uint4(r[q * 4], r[q * 4 + 1], r[q * 4 + 2], r[q * 4 + 3]));
+      } else {
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          float v[8];
+#pragma unroll
+          for (int j = 0; j < 8; ++j) v[j] = __uint_as_float(r[q * 8 + j]);
+          if (p.bias) {
+#pragma unroll
+            for (int j = 0; j < 8; ++j) v[j] += bv[q * 8 + j];
+          }
+          if constexpr (EPI == EPI_OUT) {
+            sts128(sw64(buf, lane, q), pack8_bf16(v));
+          } else {  // EPI_GELU_FWD: h, and the saved z beside it
+            if (p.out2) sts128(sw64(buf + 2048, lane, q), pack8_bf16(v));
+            float h[8];
+#pragma unroll
+            for (int j = 0; j < 8; ++j) h[j] = gelu_tanh_f(v[j]);
+            sts128(sw64(buf, lane, q), pack8_bf16(h));
+          }
+        }
+      }
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) {
+        const uint8_t* src = sbuf + (k % NBUF) * 4096;
+        if (row0 >= p.M) {
+          // every row of this warp lies past M: nothing to store (an empty
+          // group keeps the buffer accounting)
+        } else if (!p.o_swap) {
+          tma_store_3d(tmO, src, nc, row0, b);
+          if (EPI == EPI_GELU_FWD && p.out2) tma_store_3d(tmO2, src + 2048, nc, row0, b);
+        } else {
+          tma_store_3d(tmO, src, nc, b, row0);
+          if (EPI == EPI_GELU_FWD && p.out2) tma_store_3d(tmO2, src + 2048, nc, b, row0);
+        }
+        bulk_commit();
+      }
+      ++k;
+    }
+  }
+}
+
+template <int EPI, bool AMN, bool BMN, bool TMA = false>
 __global__ void __launch_bounds__(threads_for<EPI>(), 1)
     tc_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                        const __grid_constant__ CUtensorMap tmX, const Params p) {
-  using L = PairLayout<EPI>;
+                        const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmO,
+                        const __grid_constant__ CUtensorMap tmO2, const Params p) {
+  static_assert(!TMA || !aux_staged<EPI>(), "the backward epilogues store from registers");
+  using L = PairLayout<EPI, TMA>;
   constexpr int BN = PAIR_BN;
   constexpr int STAGES = L::STAGES;
   extern __shared__ uint8_t smem_raw[];
@@ -710,6 +871,10 @@ __global__ void __launch_bounds__(threads_for<EPI>(), 1)
     prefetch_tmap(&tmA);
     prefetch_tmap(&tmB);
     if constexpr (aux_staged<EPI>()) prefetch_tmap(&tmX);
+    if constexpr (TMA) {
+      prefetch_tmap(&tmO);
+      if (p.out2) prefetch_tmap(&tmO2);
+    }
   }
   if (warp == 1) tmem_alloc_pair(tmem_slot, L::TMEM_COLS);
   tc_fence_before();
@@ -993,6 +1158,7 @@ __global__ void __launch_bounds__(threads_for<EPI>(), 1)
       // a copy still in flight into the slot completes before the CTA exits
       if (pending) wait_bounded(xb, xph, abort_flag, p, false);
     } else {
+      uint32_t staged = 0;  // TMA-store epilogue: chunks this warp has staged
       for (int tile = cluster_id; tile < num_tiles; tile += num_clusters, ++local) {
         const int buf = local & 1;
         const uint32_t use = static_cast<uint32_t>(local >> 1);
@@ -1006,14 +1172,23 @@ __global__ void __launch_bounds__(threads_for<EPI>(), 1)
         tc_fence_after();
         int b, mp, nb;
         decode_pair_tile(p, tile, b, mp, nb);
-        const int row = mp * 256 + static_cast<int>(rank) * 128 + quarter * 32 + lane;
+        const int row0 = mp * 256 + static_cast<int>(rank) * 128 + quarter * 32;
         const uint32_t taddr = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) +
                                static_cast<uint32_t>(buf * BN);
-        epilogue_tile<BN, EPI>(p, b, row, row < p.M, nb * BN, nb, taddr, (warp - 2) >> 2);
+        if constexpr (TMA) {
+          epilogue_tile_tma<EPI>(p, &tmO, &tmO2, b, row0, lane, nb * BN, nb, taddr,
+                                 smem + L::AUX_OFF + (warp - 2) * OUT_BUF, staged);
+        } else {
+          const int row = row0 + lane;
+          epilogue_tile<BN, EPI>(p, b, row, row < p.M, nb * BN, nb, taddr, (warp - 2) >> 2);
+        }
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive_cluster(buf ? leader_tempty1 : leader_tempty0);
       }
+      // the stores this warp issued have completed before the CTA exits
+      if (TMA && lane == 0) bulk_wait_all();
+      __syncwarp();
     }
 #ifdef TPFFN_INSTRUMENT
     if (warp == 2 && lane == 0) DBG_ADD(5, t_epi);
@@ -1237,16 +1412,117 @@ static bool raster_by_sharing() {
   return on;
 }
 
+// Output tensor map of a TMA-store epilogue: {cols, rows, batch} (or
+// {cols, batch, rows} when the batch stride is the smaller one), 32 x 32
+// boxes, 64-byte swizzle for bf16 (64-byte box rows), 128-byte for fp32.
+// Columns from `cols` and rows from `rows` on lie outside the map, so a store
+// never writes them.  Returns 0 or a TP_ERR_* code.
+static int make_out_map(CUtensorMap* m, const void* ptr, bool fp32, int64_t cols, int64_t rows, int64_t nb,
+                        int64_t rs, int64_t bs, int* swap) {
+  const uint64_t es = fp32 ? 4 : 2;
+  if (!ptr || reinterpret_cast<uintptr_t>(ptr) % 16 || cols < 1 || rows < 1) return TP_ERR_ALIGN;
+  nb = nb > 1 ? nb : 1;
+  const int64_t bst = nb > 1 ? bs : rs * rows;
+  if ((rs * es) % 16 || (bst * es) % 16 || bst <= 0) return TP_ERR_ALIGN;
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return TP_ERR_CUDA;
+  *swap = (nb > 1 && bs < rs) ? 1 : 0;
+  cuuint64_t dims[3], strides[2];
+  cuuint32_t box[3], estr[3] = {1, 1, 1};
+  dims[0] = static_cast<cuuint64_t>(cols);
+  box[0] = 32;
+  if (!*swap) {
+    dims[1] = rows;
+    dims[2] = nb;
+    strides[0] = rs * es;
+    strides[1] = bst * es;
+    box[1] = 32;
+    box[2] = 1;
+  } else {
+    dims[1] = nb;
+    dims[2] = rows;
+    strides[0] = bs * es;
+    strides[1] = rs * es;
+    box[1] = 1;
+    box[2] = 32;
+  }
+  CUresult r = fn(m, fp32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3,
+                  const_cast<void*>(ptr), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                  fp32 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B, CU_TENSOR_MAP_L2_PROMOTION_NONE,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? 0 : TP_ERR_CUDA;
+}
+
+// TPFFN_TMA_STORE=0 in the environment makes the pair GEMMs' epilogues store
+// from registers, as the backward epilogues do (for comparisons).
+static bool tma_store_enabled() {
+  static const bool on = !getenv_flag_off("TPFFN_TMA_STORE");
+  return on;
+}
+
+// Launch of one pair-kernel instance (its own attribute set-up and cluster
+// occupancy query per device).
+template <int EPI, bool AMN, bool BMN, bool TMA>
+static int launch_pair_inst(const GemmSpec& s, LaunchCtx& ctx, const CUtensorMap& ta, const CUtensorMap& tb,
+                            const CUtensorMap& tx, const CUtensorMap& to, const CUtensorMap& to2, const Params& p) {
+  using L = PairLayout<EPI, TMA>;
+  auto kern = tc_gemm_pair_kernel<EPI, AMN, BMN, TMA>;
+  static std::atomic<uint32_t> attr_done{0};
+  static std::atomic<int> max_clusters[32];
+  int dev = 0;
+  cudaGetDevice(&dev);
+  const uint32_t bit = 1u << (dev & 31);
+  if (!(attr_done.load() & bit)) {
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::SMEM) != cudaSuccess)
+      return TP_ERR_CUDA;
+    cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 0);
+    attr_done.fetch_or(bit);
+  }
+  cudaLaunchConfig_t cfg{};
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
+  cfg.blockDim = dim3(threads_for<EPI>(), 1, 1);
+  cfg.dynamicSmemBytes = L::SMEM;
+  cfg.stream = ctx.stream;
+  cfg.attrs = attr;
+  cfg.numAttrs = 2;
+  int mc = max_clusters[dev & 31].load();
+  if (mc <= 0) {
+    cfg.gridDim = dim3(2 * (ctx.num_sms / 2), 1, 1);
+    int q = 0;
+    cudaError_t qe = cudaOccupancyMaxActiveClusters(&q, kern, &cfg);
+    mc = (qe == cudaSuccess && q > 0) ? q : ctx.num_sms / 2;
+    if (getenv("TPFFN_VERBOSE"))
+      fprintf(stderr, "tpffn: pair kernel: occupancy query rc=%d clusters=%d -> using %d clusters\n", (int)qe, q, mc);
+    max_clusters[dev & 31].store(mc);
+  }
+  const long long tiles = static_cast<long long>((p.tiles_m + 1) / 2) * p.tiles_n * p.NB;
+  if (tiles <= 0 || p.k_blocks <= 0) return TP_ERR_INVALID;
+  const int clusters = static_cast<int>(tiles < mc ? tiles : mc);
+  cfg.gridDim = dim3(2 * clusters, 1, 1);
+  if (ctx.before) ctx.before(ctx.user, s.name, ctx.stream);
+  cudaError_t e = cudaLaunchKernelEx(&cfg, kern, ta, tb, tx, to, to2, p);
+  if (ctx.after) ctx.after(ctx.user, ctx.stream);
+  ctx.launches++;
+  return e == cudaSuccess && cudaPeekAtLastError() == cudaSuccess ? 0 : TP_ERR_CUDA;
+}
+
 template <int EPI, bool AMN, bool BMN>
 static int launch_pair(const GemmSpec& s, LaunchCtx& ctx) {
-  using L = PairLayout<EPI>;
-  CUtensorMap ta, tb, tx;
+  CUtensorMap ta, tb, tx, to, to2;
   int sa = 0, sb = 0;
   int rc = make_map(&ta, s.A, BM, &sa);
   if (rc) return rc;
   rc = make_map(&tb, s.B, PAIR_BN / 2, &sb);
   if (rc) return rc;
   memset(&tx, 0, sizeof(tx));
+  memset(&to, 0, sizeof(to));
+  memset(&to2, 0, sizeof(to2));
   if constexpr (aux_staged<EPI>()) {
     rc = make_aux_map(&tx, s);
     if (rc) return rc;
@@ -1293,51 +1569,27 @@ static int launch_pair(const GemmSpec& s, LaunchCtx& ctx) {
 #ifdef TPFFN_INSTRUMENT
   p.dbg_slot = g_dbg_launch++ & 7;
 #endif
-
-  auto kern = tc_gemm_pair_kernel<EPI, AMN, BMN>;
-  static std::atomic<uint32_t> attr_done{0};
-  static std::atomic<int> max_clusters[32];
-  int dev = 0;
-  cudaGetDevice(&dev);
-  const uint32_t bit = 1u << (dev & 31);
-  if (!(attr_done.load() & bit)) {
-    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::SMEM) != cudaSuccess)
-      return TP_ERR_CUDA;
-    cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 0);
-    attr_done.fetch_or(bit);
+  if constexpr (!aux_staged<EPI>()) {
+    if (tma_store_enabled()) {
+      // output maps: out (h for the forward epilogues; fp32 for EPI_F32) and
+      // out2 (a|g rows, or z); any map that cannot be made keeps the register
+      // stores of the plain epilogue
+      const bool f32 = EPI == EPI_F32;
+      int sw1 = 0, sw2 = 0;
+      const int64_t nb = s.NB > 1 ? s.NB : 1;
+      const int64_t cols1 = EPI == EPI_SWIGLU_FWD ? s.out_rs : s.n_store;
+      bool ok = make_out_map(&to, s.out, f32, cols1, s.M, nb, s.out_rs, s.out_bs, &sw1) == 0;
+      if (ok && s.out2) {
+        const int64_t cols2 = EPI == EPI_SWIGLU_FWD ? s.out2_rs : s.n_store;
+        ok = make_out_map(&to2, s.out2, false, cols2, s.M, nb, s.out2_rs, s.out2_bs, &sw2) == 0 && sw2 == sw1;
+      }
+      if (ok) {
+        p.o_swap = sw1;
+        return launch_pair_inst<EPI, AMN, BMN, true>(s, ctx, ta, tb, tx, to, to2, p);
+      }
+    }
   }
-  cudaLaunchConfig_t cfg{};
-  cudaLaunchAttribute attr[2];
-  attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = 2;
-  attr[0].val.clusterDim.y = 1;
-  attr[0].val.clusterDim.z = 1;
-  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[1].val.programmaticStreamSerializationAllowed = 1;
-  cfg.blockDim = dim3(threads_for<EPI>(), 1, 1);
-  cfg.dynamicSmemBytes = L::SMEM;
-  cfg.stream = ctx.stream;
-  cfg.attrs = attr;
-  cfg.numAttrs = 2;
-  int mc = max_clusters[dev & 31].load();
-  if (mc <= 0) {
-    cfg.gridDim = dim3(2 * (ctx.num_sms / 2), 1, 1);
-    int q = 0;
-    cudaError_t qe = cudaOccupancyMaxActiveClusters(&q, kern, &cfg);
-    mc = (qe == cudaSuccess && q > 0) ? q : ctx.num_sms / 2;
-    if (getenv("TPFFN_VERBOSE"))
-      fprintf(stderr, "tpffn: pair kernel: occupancy query rc=%d clusters=%d -> using %d clusters\n", (int)qe, q, mc);
-    max_clusters[dev & 31].store(mc);
-  }
-  const long long tiles = static_cast<long long>((p.tiles_m + 1) / 2) * p.tiles_n * p.NB;
-  if (tiles <= 0 || p.k_blocks <= 0) return TP_ERR_INVALID;
-  const int clusters = static_cast<int>(tiles < mc ? tiles : mc);
-  cfg.gridDim = dim3(2 * clusters, 1, 1);
-  if (ctx.before) ctx.before(ctx.user, s.name, ctx.stream);
-  cudaError_t e = cudaLaunchKernelEx(&cfg, kern, ta, tb, tx, p);
-  if (ctx.after) ctx.after(ctx.user, ctx.stream);
-  ctx.launches++;
-  return e == cudaSuccess && cudaPeekAtLastError() == cudaSuccess ? 0 : TP_ERR_CUDA;
+  return launch_pair_inst<EPI, AMN, BMN, false>(s, ctx, ta, tb, tx, to, to2, p);
 }
 
 }  // namespace tc
