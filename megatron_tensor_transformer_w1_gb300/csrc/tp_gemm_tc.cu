@@ -616,20 +616,27 @@ __host__ __device__ constexpr bool aux_staged() {
 // instruction from the threads.  The buffers take one operand stage.
 constexpr int OUT_BUF = 8192;  // per epilogue warp
 
+// With TMA stores the backward epilogues give each warp two 4 KB slots: the
+// next chunk's saved activations land in one while the other, once read,
+// takes the current chunk's results for the store.  They take two operand
+// stages (five remain).
 template <int EPI, bool TMA>
 struct PairLayout {
-  static constexpr int STAGES = (aux_staged<EPI>() || TMA) ? 6 : 7;
+  static constexpr bool AUX = aux_staged<EPI>();
+  static constexpr int STAGES = AUX ? (TMA ? 5 : 6) : (TMA ? 6 : 7);
   static constexpr int A_BYTES = BM * BK * 2;               // this CTA's 128 rows of A
   static constexpr int B_BYTES = (PAIR_BN / 2) * BK * 2;    // this CTA's half of B
   static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;     // 32 KB
-  static constexpr int AUX_SLOT = 4096;                     // per epilogue warp
+  static constexpr int AUX_SLOT = 4096;                     // one slot
+  static constexpr int SLOTS = AUX ? (TMA ? 2 : 1) : 0;     // slots per epilogue warp
   static constexpr int AUX_OFF = STAGES * STAGE_BYTES;
-  static constexpr int AUX_BYTES = aux_staged<EPI>() ? epi_warps<EPI>() * AUX_SLOT : (TMA ? 4 * OUT_BUF : 0);
+  static constexpr int AUX_BYTES = AUX ? epi_warps<EPI>() * SLOTS * AUX_SLOT : (TMA ? 4 * OUT_BUF : 0);
   static constexpr int BAR_OFF = AUX_OFF + AUX_BYTES;
-  static constexpr int SMEM = BAR_OFF + 256 + 1024;
+  static constexpr int BAR_AREA = 512;  // barriers, then the TMEM address and the abort flag at 496, 500
+  static constexpr int SMEM = BAR_OFF + BAR_AREA + 1024;
   static constexpr uint32_t TMEM_COLS = 2 * PAIR_BN;
-  // full/empty per stage, tfull/tempty x2, drain, one slot barrier per epilogue warp
-  static_assert((2 * STAGES + 5 + (aux_staged<EPI>() ? epi_warps<EPI>() : 0)) * 8 <= 240, "barrier area");
+  // full/empty per stage, tfull/tempty x2, drain, the slot barriers
+  static_assert((2 * STAGES + 5 + epi_warps<EPI>() * SLOTS) * 8 <= 496, "barrier area");
   static_assert(SMEM <= 232448, "shared memory per CTA");
 };
 
@@ -829,7 +836,6 @@ __global__ void __launch_bounds__(threads_for<EPI>(), 1)
     tc_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                         const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmO,
                         const __grid_constant__ CUtensorMap tmO2, const Params p) {
-  static_assert(!TMA || !aux_staged<EPI>(), "the backward epilogues store from registers");
   using L = PairLayout<EPI, TMA>;
   constexpr int BN = PAIR_BN;
   constexpr int STAGES = L::STAGES;
@@ -841,8 +847,8 @@ __global__ void __launch_bounds__(threads_for<EPI>(), 1)
   uint64_t* tempty = tfull + 2;
   uint64_t* drain = tempty + 2;
   uint64_t* xbar = drain + 1;  // saved-activation slots (backward epilogues)
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::BAR_OFF + 240);
-  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::BAR_OFF + 244);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::BAR_OFF + 496);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::BAR_OFF + 500);
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -862,7 +868,7 @@ __global__ void __launch_bounds__(threads_for<EPI>(), 1)
     }
     mbar_init(drain, 1);
     if constexpr (aux_staged<EPI>())
-      for (int i = 0; i < epi_warps<EPI>(); ++i) mbar_init(&xbar[i], 1);
+      for (int i = 0; i < epi_warps<EPI>() * L::SLOTS; ++i) mbar_init(&xbar[i], 1);
     *abort_flag = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
@@ -873,7 +879,7 @@ __global__ void __launch_bounds__(threads_for<EPI>(), 1)
     if constexpr (aux_staged<EPI>()) prefetch_tmap(&tmX);
     if constexpr (TMA) {
       prefetch_tmap(&tmO);
-      if (p.out2) prefetch_tmap(&tmO2);
+      if (!aux_staged<EPI>() && p.out2) prefetch_tmap(&tmO2);
     }
   }
   if (warp == 1) tmem_alloc_pair(tmem_slot, L::TMEM_COLS);
@@ -1041,7 +1047,137 @@ __global__ void __launch_bounds__(threads_for<EPI>(), 1)
 #ifdef TPFFN_INSTRUMENT
     const long long t_epi = clock64();
 #endif
-    if constexpr (aux_staged<EPI>()) {
+    if constexpr (aux_staged<EPI>() && TMA) {
+      // Backward epilogue, TMA in and out: chunk k of this warp (its c-th
+      // 32-column chunk of a tile) finds its saved activations in slot k & 1;
+      // before waiting for them the warp sends the next chunk's copy into the
+      // other slot (once the store that last read that slot has read it).  The
+      // chunk's results replace the activations in slot k & 1 -- each lane
+      // writes only its own row, which it has read -- and one lane stores
+      // them.  The chunk after a tile's last is the next tile's first.
+      constexpr int CPW = BN / 32 / 2;  // 32-column chunks per warp (two warps per lane quarter)
+      constexpr uint32_t XBYTES = EPI == EPI_SWIGLU_BWD ? 4096u : 2048u;
+      const int part = (warp - 2) >> 2;
+      const int c0 = part * CPW;
+      uint8_t* slots = smem + L::AUX_OFF + (warp - 2) * 2 * L::AUX_SLOT;
+      uint64_t* xbw = &xbar[(warp - 2) * 2];
+      uint32_t xph = 0, pendm = 0;  // per-slot phase and copy-in-flight bits
+      uint32_t kc = 0;              // chunks done by this warp
+      auto issue = [&](int t, int c, int sl) {  // lane 0
+        int b, mp, nb;
+        decode_pair_tile(p, t, b, mp, nb);
+        const int row0 = mp * 256 + static_cast<int>(rank) * 128 + quarter * 32;
+        const int n = nb * BN + c * 32;
+        uint8_t* dst = slots + sl * L::AUX_SLOT;
+        mbar_arrive_expect_tx(&xbw[sl], XBYTES);
+        if constexpr (EPI == EPI_SWIGLU_BWD) {
+          const int col = (n >> 7) * 256 + (n & 127);
+          tma_load_3d(dst, &tmX, &xbw[sl], col, row0, b);
+          tma_load_3d(dst + 2048, &tmX, &xbw[sl], col + 128, row0, b);
+        } else {
+          tma_load_3d(dst, &tmX, &xbw[sl], n, row0, b);
+        }
+      };
+      if (cluster_id < num_tiles) {
+        if (lane == 0) issue(cluster_id, c0, 0);
+        pendm |= 1u;
+      }
+      bool ok = true;
+      for (int tile = cluster_id; tile < num_tiles && ok; tile += num_clusters, ++local) {
+        const int buf = local & 1;
+        const uint32_t use = static_cast<uint32_t>(local >> 1);
+        ok = wait_bounded(&tfull[buf], use & 1u, abort_flag, p);
+        if (!ok) break;
+        tc_fence_after();
+        int b, mp, nb;
+        decode_pair_tile(p, tile, b, mp, nb);
+        const int row0 = mp * 256 + static_cast<int>(rank) * 128 + quarter * 32;
+        const uint32_t taddr = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) +
+                               static_cast<uint32_t>(buf * BN);
+#pragma unroll 1
+        for (int c = c0; c < c0 + CPW; ++c, ++kc) {
+          const int sl = static_cast<int>(kc & 1u);
+          int nt = tile, ncc = c + 1;
+          if (ncc == c0 + CPW) {
+            nt = tile + num_clusters;
+            ncc = c0;
+          }
+          if (nt < num_tiles) {
+            if (lane == 0) {
+              bulk_wait_read<0>();  // the store that last read the other slot is done with it
+              issue(nt, ncc, sl ^ 1);
+            }
+            pendm |= 1u << (sl ^ 1);
+          }
+          if (!wait_bounded(&xbw[sl], (xph >> sl) & 1u, abort_flag, p)) {
+            ok = false;
+            break;
+          }
+          pendm &= ~(1u << sl);
+          xph ^= 1u << sl;
+          const uint32_t xs = smem_u32(slots + sl * L::AUX_SLOT);
+          uint4 za[4], gg[4];
+#pragma unroll
+          for (int k = 0; k < 4; ++k) {
+            za[k] = lds128(sw64(xs, lane, k));
+            if constexpr (EPI == EPI_SWIGLU_BWD) gg[k] = lds128(sw64(xs + 2048, lane, k));
+          }
+          uint32_t r[32];
+          __syncwarp();  // tcgen05.ld is warp-collective: reconverge first
+          tmem_ld32(taddr + c * 32, r);
+          tmem_wait_ld();
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            float v[8], a[8];
+#pragma unroll
+            for (int j = 0; j < 8; ++j) v[j] = __uint_as_float(r[q * 8 + j]);
+            unpack_bf16x8(za[q], a);
+            if constexpr (EPI == EPI_GELU_BWD) {
+#pragma unroll
+              for (int j = 0; j < 8; ++j) v[j] *= gelu_tanh_grad_f(a[j]);
+              sts128(sw64(xs, lane, q), pack8_bf16(v));
+            } else {
+              float g[8], da[8], dg[8];
+              unpack_bf16x8(gg[q], g);
+#pragma unroll
+              for (int j = 0; j < 8; ++j) {
+                const float sg = sigmoid_f(a[j]);
+                dg[j] = v[j] * a[j] * sg;                                // dh * silu(a)
+                da[j] = v[j] * g[j] * sg * (1.0f + a[j] * (1.0f - sg));  // dh * g * silu'(a)
+              }
+              sts128(sw64(xs, lane, q), pack8_bf16(da));
+              sts128(sw64(xs + 2048, lane, q), pack8_bf16(dg));
+            }
+          }
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) {
+            const int n = nb * BN + c * 32;
+            if (row0 < p.M && n < p.n_store) {
+              const uint8_t* src = slots + sl * L::AUX_SLOT;
+              if constexpr (EPI == EPI_SWIGLU_BWD) {
+                const int col = (n >> 7) * 256 + (n & 127);
+                tma_store_3d(&tmO, src, col, row0, b);
+                tma_store_3d(&tmO, src + 2048, col + 128, row0, b);
+              } else {
+                tma_store_3d(&tmO, src, n, row0, b);
+              }
+            }
+            bulk_commit();  // (an empty group when nothing is stored)
+          }
+        }
+        if (!ok) break;
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive_cluster(buf ? leader_tempty1 : leader_tempty0);
+      }
+      // copies still in flight into the slots, and the stores, complete
+      // before the CTA exits
+      for (int sl = 0; sl < 2; ++sl)
+        if (pendm & (1u << sl)) wait_bounded(&xbw[sl], (xph >> sl) & 1u, abort_flag, p, false);
+      if (lane == 0) bulk_wait_all();
+      __syncwarp();
+    } else if constexpr (aux_staged<EPI>()) {
       // Backward epilogue with the saved activations staged by TMA: chunk c
       // of this warp's 32 rows lands in its slot while chunk c-1 is
       // computed; the chunk after the tile's last is the next tile's first.
@@ -1569,7 +1705,15 @@ static int launch_pair(const GemmSpec& s, LaunchCtx& ctx) {
 #ifdef TPFFN_INSTRUMENT
   p.dbg_slot = g_dbg_launch++ & 7;
 #endif
-  if constexpr (!aux_staged<EPI>()) {
+  if constexpr (aux_staged<EPI>()) {
+    if (tma_store_enabled()) {
+      // the backward epilogues' output: dz, or the interleaved [da | dg] rows
+      int sw = 0;
+      if (make_out_map(&to, s.out, false, s.out_rs, s.M, s.NB > 1 ? s.NB : 1, s.out_rs, s.out_bs, &sw) == 0 &&
+          sw == 0)
+        return launch_pair_inst<EPI, AMN, BMN, true>(s, ctx, ta, tb, tx, to, to2, p);
+    }
+  } else {
     if (tma_store_enabled()) {
       // output maps: out (h for the forward epilogues; fp32 for EPI_F32) and
       // out2 (a|g rows, or z); any map that cannot be made keeps the register
