@@ -616,18 +616,19 @@ __host__ __device__ constexpr bool aux_staged() {
 // instruction from the threads.  The buffers take one operand stage.
 constexpr int OUT_BUF = 8192;  // per epilogue warp
 
-// With TMA stores the backward epilogues give each warp two 4 KB slots: the
-// next chunk's saved activations land in one while the other, once read,
-// takes the current chunk's results for the store.  They take two operand
-// stages (five remain).
+// With TMA stores the backward epilogues give each warp two slots: the next
+// chunk's saved activations land in one while the other, once read, takes
+// the current chunk's results for the store.  A slot holds a 32 x 32 block of
+// a and one of g (4 KB, SwiGLU) or one of z (2 KB, GELU); the SwiGLU slots take
+// two operand stages (five remain), the GELU slots one.
 template <int EPI, bool TMA>
 struct PairLayout {
   static constexpr bool AUX = aux_staged<EPI>();
-  static constexpr int STAGES = AUX ? (TMA ? 5 : 6) : (TMA ? 6 : 7);
+  static constexpr int STAGES = AUX ? ((TMA && EPI == EPI_SWIGLU_BWD) ? 5 : 6) : (TMA ? 6 : 7);
   static constexpr int A_BYTES = BM * BK * 2;               // this CTA's 128 rows of A
   static constexpr int B_BYTES = (PAIR_BN / 2) * BK * 2;    // this CTA's half of B
   static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;     // 32 KB
-  static constexpr int AUX_SLOT = 4096;                     // one slot
+  static constexpr int AUX_SLOT = EPI == EPI_SWIGLU_BWD ? 4096 : 2048;  // one slot
   static constexpr int SLOTS = AUX ? (TMA ? 2 : 1) : 0;     // slots per epilogue warp
   static constexpr int AUX_OFF = STAGES * STAGE_BYTES;
   static constexpr int AUX_BYTES = AUX ? epi_warps<EPI>() * SLOTS * AUX_SLOT : (TMA ? 4 * OUT_BUF : 0);
