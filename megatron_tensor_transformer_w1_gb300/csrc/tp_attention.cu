@@ -323,32 +323,20 @@ __global__ void __launch_bounds__(NT, 1) attn_fwd_kernel(const __grid_constant__
       int q_last[2] = {-1, -1}, k_last[2] = {-1, -1}, v_last[2] = {-1, -1};
       uint32_t kv = 0, it = 0;
       bool ok = true;
-      // Q of item number `n` of this CTA into its buffer n & 1, once the
-      // item two back has finished with that buffer
-      auto load_q = [&](int item, uint32_t n) -> bool {
+      for (int item = blockIdx.x; item < p.items && ok; item += gridDim.x, ++it) {
         int qb, b, h;
         decode_item(p, item, p.H, p.causal != 0, qb, b, h);
-        const int qbuf = n & 1;
-        const uint32_t qph = (n >> 1) & 1u;
+        const int nkb = p.causal ? qb + 1 : p.n_qb;
+        const int qbuf = it & 1;
+        const uint32_t qph = (it >> 1) & 1u;
         AT_T0(t16);
-        if (!W(&q_empty[qbuf], qph ^ 1u)) return false;
+        if (!W(&q_empty[qbuf], qph ^ 1u)) break;
         AT_ADD(16, t16);
         mbar_arrive_expect_tx(&q_full[qbuf], TILE);
         const int qc = p.g.qcol(h);
         tma_load_3d(smem + F_Q + qbuf * TILE, &tq, &q_full[qbuf], qc, qb * 128, b);
         tma_load_3d(smem + F_Q + qbuf * TILE + TILE / 2, &tq, &q_full[qbuf], qc + 64, qb * 128, b);
         q_last[qbuf] = static_cast<int>(qph);
-        return true;
-      };
-      // Each item's Q goes out right after the previous item's first K/V
-      // block, a whole item ahead of the S product that reads it (the MMA
-      // thread issues an item's first S during the previous item's last
-      // block); only the first item's Q is loaded on its own.
-      if (blockIdx.x < static_cast<unsigned>(p.items) && !load_q(blockIdx.x, 0)) ok = false;
-      for (int item = blockIdx.x; item < p.items && ok; item += gridDim.x, ++it) {
-        int qb, b, h;
-        decode_item(p, item, p.H, p.causal != 0, qb, b, h);
-        const int nkb = p.causal ? qb + 1 : p.n_qb;
         const int hk = h / p.G, kc = p.g.kcol(hk), vc = p.g.vcol(hk);
         for (int j = 0; j < nkb; ++j, ++kv) {
           const int st = kv & 1;
@@ -369,11 +357,6 @@ __global__ void __launch_bounds__(NT, 1) attn_fwd_kernel(const __grid_constant__
           tma_load_3d(vd, &tq, &v_full[st], vc, j * 128, b);
           tma_load_3d(vd + TILE / 2, &tq, &v_full[st], vc + 64, j * 128, b);
           v_last[st] = static_cast<int>(ph);
-          if (j == 0 && item + static_cast<int>(gridDim.x) < p.items &&
-              !load_q(item + static_cast<int>(gridDim.x), it + 1)) {
-            ok = false;
-            break;
-          }
         }
       }
       // every issued copy lands before the CTA may exit

@@ -1706,15 +1706,18 @@ static int launch_pair(const GemmSpec& s, LaunchCtx& ctx) {
 #ifdef TPFFN_INSTRUMENT
   p.dbg_slot = g_dbg_launch++ & 7;
 #endif
-  if constexpr (aux_staged<EPI>()) {
+  if constexpr (EPI == EPI_SWIGLU_BWD) {
     if (tma_store_enabled()) {
-      // the backward epilogues' output: dz, or the interleaved [da | dg] rows
+      // the SwiGLU backward epilogue's output, the interleaved [da | dg] rows
+      // (the GELU backward epilogue measured slower with TMA stores --
+      // dgrad_h_gelu 0.431-0.435 -> 0.442-0.460 ms on the Megatron-8.3B
+      // shapes -- and keeps its register stores)
       int sw = 0;
       if (make_out_map(&to, s.out, false, s.out_rs, s.M, s.NB > 1 ? s.NB : 1, s.out_rs, s.out_bs, &sw) == 0 &&
           sw == 0)
         return launch_pair_inst<EPI, AMN, BMN, true>(s, ctx, ta, tb, tx, to, to2, p);
     }
-  } else {
+  } else if constexpr (!aux_staged<EPI>()) {
     if (tma_store_enabled()) {
       // output maps: out (h for the forward epilogues; fp32 for EPI_F32) and
       // out2 (a|g rows, or z); any map that cannot be made keeps the register
