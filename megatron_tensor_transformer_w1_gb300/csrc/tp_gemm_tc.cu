@@ -12,7 +12,11 @@
 //                     tcgen05.ld of the fp32 accumulator (warp w reads TMEM
 //                     lanes 32*(w%4)..; with 8, two warps per lane quarter
 //                     split the columns), fused activation or derivative,
-//                     vectorised global stores;
+//                     then the results: staged in shared memory and written
+//                     with TMA stores (the two-SM pair kernel's epilogues,
+//                     except the GELU backward one), or 16-byte stores from
+//                     the threads (the one-SM kernel, the GELU backward
+//                     epilogue, and TPFFN_TMA_STORE=0);
 //   * the accumulator is double-buffered in tensor memory (2 x BN columns),
 //     so the epilogue of one tile overlaps the MMA K-loop of the next;
 //   * every wait on an mbarrier is bounded: after the time limit the waiting
