@@ -613,6 +613,19 @@ __host__ __device__ constexpr bool aux_staged() {
   return EPI == EPI_SWIGLU_BWD || EPI == EPI_GELU_BWD;
 }
 
+// Pair-kernel store modes: TM 0 stores from registers, TM 1 stages boxes for
+// TMA stores, TM 2 does so with eight epilogue warps (two per TMEM lane
+// quarter, each taking half of a tile's columns) for the forward epilogues of
+// GEMMs whose K loop is too short to hide a four-warp epilogue.
+template <int EPI, int TM>
+__host__ __device__ constexpr int pair_epi_warps() {
+  return TM == 2 ? 8 : epi_warps<EPI>();
+}
+template <int EPI, int TM>
+__host__ __device__ constexpr int pair_threads() {
+  return 64 + 32 * pair_epi_warps<EPI, TM>();
+}
+
 // Epilogues that write their tile through shared memory with TMA stores:
 // each epilogue warp stages its 32 rows x 32 columns per output in an 8 KB
 // buffer (64-byte swizzled bf16 boxes, 128-byte swizzled fp32 boxes) and one
@@ -625,17 +638,18 @@ constexpr int OUT_BUF = 8192;  // per epilogue warp
 // the current chunk's results for the store.  A slot holds a 32 x 32 block of
 // a and one of g (4 KB, SwiGLU) or one of z (2 KB, GELU); the SwiGLU slots take
 // two operand stages (five remain), the GELU slots one.
-template <int EPI, bool TMA>
+template <int EPI, int TM>
 struct PairLayout {
   static constexpr bool AUX = aux_staged<EPI>();
-  static constexpr int STAGES = AUX ? ((TMA && EPI == EPI_SWIGLU_BWD) ? 5 : 6) : (TMA ? 6 : 7);
+  static constexpr bool TMA = TM != 0;
+  static constexpr int STAGES = AUX ? ((TMA && EPI == EPI_SWIGLU_BWD) ? 5 : 6) : (TM == 2 ? 5 : (TMA ? 6 : 7));
   static constexpr int A_BYTES = BM * BK * 2;               // this CTA's 128 rows of A
   static constexpr int B_BYTES = (PAIR_BN / 2) * BK * 2;    // this CTA's half of B
   static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;     // 32 KB
   static constexpr int AUX_SLOT = EPI == EPI_SWIGLU_BWD ? 4096 : 2048;  // one slot
   static constexpr int SLOTS = AUX ? (TMA ? 2 : 1) : 0;     // slots per epilogue warp
   static constexpr int AUX_OFF = STAGES * STAGE_BYTES;
-  static constexpr int AUX_BYTES = AUX ? epi_warps<EPI>() * SLOTS * AUX_SLOT : (TMA ? 4 * OUT_BUF : 0);
+  static constexpr int AUX_BYTES = AUX ? epi_warps<EPI>() * SLOTS * AUX_SLOT : (TMA ? pair_epi_warps<EPI, TM>() * OUT_BUF : 0);
   static constexpr int BAR_OFF = AUX_OFF + AUX_BYTES;
   static constexpr int BAR_AREA = 512;  // barriers, then the TMEM address and the abort flag at 496, 500
   static constexpr int SMEM = BAR_OFF + BAR_AREA + 1024;
@@ -707,15 +721,15 @@ __device__ __forceinline__ uint4 pack8_bf16(const float* v) {
 // quarter).  The warp's 32 rows start at row0; lane = its row within them.
 // Rows past M and columns past n_store lie outside the output maps and are
 // not written.  `k` counts this warp's staged chunks (buffer rotation).
-template <int EPI>
+template <int EPI, int NSPLIT>
 __device__ __forceinline__ void epilogue_tile_tma(const Params& p, const CUtensorMap* tmO, const CUtensorMap* tmO2,
                                                   int b, int row0, int lane, int n0, int nb, uint32_t taddr,
-                                                  uint8_t* sbuf, uint32_t& k) {
+                                                  uint8_t* sbuf, uint32_t& k, int part) {
   const uint32_t sb = smem_u32(sbuf);
   if constexpr (EPI == EPI_SWIGLU_FWD) {
     // chunk c: 32 hidden units -> h (2 KB box), a and g (2 KB boxes); one 6 KB buffer
 #pragma unroll 1
-    for (int c = 0; c < 4; ++c) {
+    for (int c = part * (4 / NSPLIT); c < (part + 1) * (4 / NSPLIT); ++c) {
       uint32_t ra[32], rg[32];
       __syncwarp();
       tmem_ld32(taddr + c * 32, ra);
@@ -767,7 +781,7 @@ __device__ __forceinline__ void epilogue_tile_tma(const Params& p, const CUtenso
     // EPI_OUT / EPI_F32 / EPI_GELU_FWD: chunk c = 32 columns; two 4 KB buffers
     constexpr int NBUF = 2;
 #pragma unroll 1
-    for (int c = 0; c < PAIR_BN / 32; ++c) {
+    for (int c = part * (PAIR_BN / 32 / NSPLIT); c < (part + 1) * (PAIR_BN / 32 / NSPLIT); ++c) {
       const int nc = n0 + c * 32;
       if (nc >= p.n_store) break;  // columns past n_store: nothing to store (n_store is a multiple of 8)
       uint32_t r[32];
@@ -836,12 +850,14 @@ __device__ __forceinline__ void epilogue_tile_tma(const Params& p, const CUtenso
   }
 }
 
-template <int EPI, bool AMN, bool BMN, bool TMA = false>
-__global__ void __launch_bounds__(threads_for<EPI>(), 1)
+template <int EPI, bool AMN, bool BMN, int TM = 0>
+__global__ void __launch_bounds__(pair_threads<EPI, TM>(), 1)
     tc_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                         const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmO,
                         const __grid_constant__ CUtensorMap tmO2, const Params p) {
-  using L = PairLayout<EPI, TMA>;
+  using L = PairLayout<EPI, TM>;
+  constexpr bool TMA = TM != 0;
+  constexpr int EW = pair_epi_warps<EPI, TM>();
   constexpr int BN = PAIR_BN;
   constexpr int STAGES = L::STAGES;
   extern __shared__ uint8_t smem_raw[];
@@ -869,7 +885,7 @@ __global__ void __launch_bounds__(threads_for<EPI>(), 1)
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&tfull[i], 1);
-      mbar_init(&tempty[i], 2 * epi_warps<EPI>());  // leader: the epilogue warps of both CTAs
+      mbar_init(&tempty[i], 2 * EW);  // leader: the epilogue warps of both CTAs
     }
     mbar_init(drain, 1);
     if constexpr (aux_staged<EPI>())
@@ -1317,8 +1333,8 @@ __global__ void __launch_bounds__(threads_for<EPI>(), 1)
         const uint32_t taddr = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) +
                                static_cast<uint32_t>(buf * BN);
         if constexpr (TMA) {
-          epilogue_tile_tma<EPI>(p, &tmO, &tmO2, b, row0, lane, nb * BN, nb, taddr,
-                                 smem + L::AUX_OFF + (warp - 2) * OUT_BUF, staged);
+          epilogue_tile_tma<EPI, EW / 4>(p, &tmO, &tmO2, b, row0, lane, nb * BN, nb, taddr,
+                                         smem + L::AUX_OFF + (warp - 2) * OUT_BUF, staged, (warp - 2) >> 2);
         } else {
           const int row = row0 + lane;
           epilogue_tile<BN, EPI>(p, b, row, row < p.M, nb * BN, nb, taddr, (warp - 2) >> 2);
@@ -1594,6 +1610,9 @@ static int make_out_map(CUtensorMap* m, const void* ptr, bool fp32, int64_t cols
   return r == CUDA_SUCCESS ? 0 : TP_ERR_CUDA;
 }
 
+// K loops of at most this many 64-wide blocks count as short (store mode 2).
+constexpr int kShortKBlocks = 24;
+
 // TPFFN_TMA_STORE=0 in the environment makes the pair GEMMs' epilogues store
 // from registers, as the backward epilogues do (for comparisons).
 static bool tma_store_enabled() {
@@ -1603,11 +1622,11 @@ static bool tma_store_enabled() {
 
 // Launch of one pair-kernel instance (its own attribute set-up and cluster
 // occupancy query per device).
-template <int EPI, bool AMN, bool BMN, bool TMA>
+template <int EPI, bool AMN, bool BMN, int TM>
 static int launch_pair_inst(const GemmSpec& s, LaunchCtx& ctx, const CUtensorMap& ta, const CUtensorMap& tb,
                             const CUtensorMap& tx, const CUtensorMap& to, const CUtensorMap& to2, const Params& p) {
-  using L = PairLayout<EPI, TMA>;
-  auto kern = tc_gemm_pair_kernel<EPI, AMN, BMN, TMA>;
+  using L = PairLayout<EPI, TM>;
+  auto kern = tc_gemm_pair_kernel<EPI, AMN, BMN, TM>;
   static std::atomic<uint32_t> attr_done{0};
   static std::atomic<int> max_clusters[32];
   int dev = 0;
@@ -1627,7 +1646,7 @@ static int launch_pair_inst(const GemmSpec& s, LaunchCtx& ctx, const CUtensorMap
   attr[0].val.clusterDim.z = 1;
   attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[1].val.programmaticStreamSerializationAllowed = 1;
-  cfg.blockDim = dim3(threads_for<EPI>(), 1, 1);
+  cfg.blockDim = dim3(pair_threads<EPI, TM>(), 1, 1);
   cfg.dynamicSmemBytes = L::SMEM;
   cfg.stream = ctx.stream;
   cfg.attrs = attr;
@@ -1719,7 +1738,7 @@ static int launch_pair(const GemmSpec& s, LaunchCtx& ctx) {
       int sw = 0;
       if (make_out_map(&to, s.out, false, s.out_rs, s.M, s.NB > 1 ? s.NB : 1, s.out_rs, s.out_bs, &sw) == 0 &&
           sw == 0)
-        return launch_pair_inst<EPI, AMN, BMN, true>(s, ctx, ta, tb, tx, to, to2, p);
+        return launch_pair_inst<EPI, AMN, BMN, 1>(s, ctx, ta, tb, tx, to, to2, p);
     }
   } else if constexpr (!aux_staged<EPI>()) {
     if (tma_store_enabled()) {
@@ -1737,11 +1756,17 @@ static int launch_pair(const GemmSpec& s, LaunchCtx& ctx) {
       }
       if (ok) {
         p.o_swap = sw1;
-        return launch_pair_inst<EPI, AMN, BMN, true>(s, ctx, ta, tb, tx, to, to2, p);
+        // forward epilogues of short K loops (GPT-2-sized widths): eight
+        // epilogue warps, so that the epilogue keeps up with the products
+        if constexpr (EPI == EPI_GELU_FWD || EPI == EPI_SWIGLU_FWD) {
+          if (static_cast<int64_t>(p.G) * p.k_blocks <= kShortKBlocks)
+            return launch_pair_inst<EPI, AMN, BMN, 2>(s, ctx, ta, tb, tx, to, to2, p);
+        }
+        return launch_pair_inst<EPI, AMN, BMN, 1>(s, ctx, ta, tb, tx, to, to2, p);
       }
     }
   }
-  return launch_pair_inst<EPI, AMN, BMN, false>(s, ctx, ta, tb, tx, to, to2, p);
+  return launch_pair_inst<EPI, AMN, BMN, 0>(s, ctx, ta, tb, tx, to, to2, p);
 }
 
 }  // namespace tc
