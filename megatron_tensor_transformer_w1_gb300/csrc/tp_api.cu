@@ -89,8 +89,8 @@ int64_t colsum_chunk(int64_t rows) {
 }
 
 struct WsLayout {
-  size_t h = 0, part = 0, D = 0, cs = 0, ks = 0, total = 0;
-  bool has_part = false, has_ks = false;
+  size_t h = 0, part = 0, D = 0, cs = 0, ks = 0, wk = 0, total = 0;
+  bool has_part = false, has_ks = false, has_wk = false;
 };
 
 // Decode-sized SwiGLU forwards (at most 32 tokens: one 32-row A tile) may
@@ -119,6 +119,39 @@ int choose_ksplit(const tp_ffn_plan* p, int64_t n, int num_sms) {
   return best;
 }
 
+// Weight-gradient GEMMs (K = the token axis) with fewer 256 x 256 output
+// tile pairs than the GPU has SM pairs leave most SMs idle for their whole K
+// loop -- GPT-2-small-shaped shards have 3 x 3 tiles x 4 shards for 76 SM
+// pairs.  Splitting K into parts gives each SM pair a part of a tile; the
+// pair kernel writes each part in fp32 and the shard-sum kernel adds them in
+// part order (deterministic).  The split is taken where it shortens the
+// busiest SM pair's K loop (waves of units x K blocks per unit) by more than
+// a tenth, each part keeping at least 16 K blocks of 64 tokens.
+constexpr int kMaxWgradKsplit = 4;
+int wgrad_ksplit(const tp_ffn_plan* p, int64_t n, int64_t M, int64_t N, int num_sms) {
+  static const bool off = [] {
+    const char* v = getenv("TPFFN_WGRAD_KSPLIT");
+    return v && v[0] == '0';
+  }();
+  if (off || p->dtype != TP_BF16 || p->act == TP_ACT_NONE || !tc_pair_path(M) || num_sms < 2) return 1;
+  const int64_t pairs = num_sms / 2;
+  const int64_t tiles = ((M + 255) / 256) * ((N + 255) / 256) * p->T_p;
+  const int64_t k_blocks = (n + 63) / 64;
+  auto busiest = [&](int64_t k) { return ((tiles * k + pairs - 1) / pairs) * ((k_blocks + k - 1) / k); };
+  int best = 1;
+  for (int k = 2; k <= kMaxWgradKsplit; ++k)
+    if (k_blocks >= 16 * k && 10 * busiest(k) < 9 * busiest(best)) best = k;
+  return best;
+}
+// fp32 bytes of the K parts of the two weight-gradient GEMMs (0: no split)
+size_t wgrad_parts_bytes(const tp_ffn_plan* p, int64_t n, int num_sms) {
+  const size_t T = static_cast<size_t>(p->T_p), d = static_cast<size_t>(p->d), sp = static_cast<size_t>(p->s_pad);
+  const size_t W = static_cast<size_t>(hidden_width(p));
+  const int ka = wgrad_ksplit(p, n, p->d, p->s_pad, num_sms), kb = wgrad_ksplit(p, n, W, p->d, num_sms);
+  const size_t a = ka > 1 ? ka * T * d * sp : 0, b = kb > 1 ? kb * T * W * d : 0;
+  return 4 * (a > b ? a : b);
+}
+
 WsLayout ws_layout(const tp_ffn_plan* p, int64_t n, int flags) {
   WsLayout L;
   size_t off = kAlign;  // error word + header
@@ -138,6 +171,14 @@ WsLayout ws_layout(const tp_ffn_plan* p, int64_t n, int flags) {
     L.has_ks = true;
     L.ks = off;
     off += align_up(static_cast<size_t>(kMaxKsplit) * p->T_p * n * hidden_width(p) * 4);
+  }
+  if (p->act != TP_ACT_NONE) {
+    const size_t wk = wgrad_parts_bytes(p, n, num_sms_current());
+    if (wk) {
+      L.has_wk = true;
+      L.wk = off;
+      off += align_up(wk);
+    }
   }
   L.cs = off;
   const int64_t cs1 = colsum_scratch_floats(p->T_p, n, p->s_pad, colsum_chunk(n));
@@ -599,6 +640,27 @@ static int validate_bwd(const tp_ffn_plan* p, int64_t n, const void* x, const vo
   return TP_OK;
 }
 
+// A weight-gradient GEMM g (bf16 out, dense [NB][M][N] planes): as it stands,
+// or split along K into fp32 parts in the workspace and summed in part order.
+static int run_wgrad(const tp_ffn_plan* p, const GemmSpec& g, int64_t n, const WsLayout& L, char* ws,
+                     LaunchCtx& ctx, const char* sum_name) {
+  const int ks = L.has_wk ? wgrad_ksplit(p, n, g.M, g.N, ctx.num_sms) : 1;
+  const int64_t plane = g.NB * g.M * g.N;
+  if (ks == 1 || g.out_rs != g.N || g.out_bs != g.M * g.N || g.n_store != g.N ||
+      static_cast<size_t>(ks) * plane * 4 > wgrad_parts_bytes(p, n, ctx.num_sms))
+    return run_gemm(p, g, ctx);
+  float* parts = reinterpret_cast<float*>(ws + L.wk);
+  GemmSpec k = g;
+  k.epi = EPI_F32;
+  k.ksplit = ks;
+  k.out = parts;
+  k.out_bs = g.M * g.N;
+  k.out_rs = g.N;
+  int rc = run_gemm(p, k, ctx);
+  if (!rc) rc = launch_shard_sum(parts, ks, g.NB * g.M, g.N, nullptr, g.out, g.out_bf16, ctx, sum_name, plane);
+  return rc;
+}
+
 // Backward on an initialised launch context; `sc` as in fwd_impl, for dx.
 static int bwd_impl(const tp_ffn_plan* p, int64_t n, const void* x, const void* w13p, const void* w2p,
                     const void* saved, const void* dy, void* dx, float* dx_partials, void* dw13p, void* dw2p,
@@ -741,7 +803,7 @@ static int bwd_impl(const tp_ffn_plan* p, int64_t n, const void* x, const void* 
     g.out_rs = sp;
     g.n_store = sp;
     g.out_bf16 = out_bf16;
-    rc = run_gemm(p, g, ctx);
+    rc = run_wgrad(p, g, n, L, ws, ctx, "wgrad_w2_ksum");
     if (rc) return rc;
   }
   {
@@ -759,7 +821,7 @@ static int bwd_impl(const tp_ffn_plan* p, int64_t n, const void* x, const void* 
     g.out_rs = d;
     g.n_store = d;
     g.out_bf16 = out_bf16;
-    rc = run_gemm(p, g, ctx);
+    rc = run_wgrad(p, g, n, L, ws, ctx, p->act == TP_ACT_SWIGLU ? "wgrad_w13_ksum" : "wgrad_w1_ksum");
     if (rc) return rc;
   }
   // ---- 6. bias gradients

@@ -83,7 +83,7 @@ struct Params {
   unsigned long long timeout_ns;
   int debug_skip;
   int dbg_slot;  // launch slot of the optional wait counters (instrumented builds only)
-  int ksplit;    // one-SM kernel: K split into this many parts (1: none)
+  int ksplit;    // K split into this many parts (1: none; fp32 parts only)
   int raster;    // pair kernel tile order (RASTER_*)
   int o_swap;    // pair kernel TMA stores: output maps are {cols, batch, rows} (batch stride < row stride)
 };
@@ -850,6 +850,19 @@ __device__ __forceinline__ void epilogue_tile_tma(const Params& p, const CUtenso
   }
 }
 
+// Work unit of the pair kernel: tile `unit mod tiles` over K part
+// `unit / tiles` of the (shard-major) K blocks, [kb0, kb0 + nkb).  Without a
+// K split, one unit per tile over all K blocks.
+__device__ __forceinline__ int pair_unit(const Params& p, int unit, int num_tiles, int& tile, int& kb0, int& nkb) {
+  const int kh = p.ksplit > 1 ? unit / num_tiles : 0;
+  tile = unit - kh * num_tiles;
+  const int kall = p.G * p.k_blocks;
+  const int kbs = (kall + p.ksplit - 1) / p.ksplit;
+  kb0 = kh * kbs;
+  nkb = min(kall - kb0, kbs);
+  return kh;
+}
+
 template <int EPI, bool AMN, bool BMN, int TM = 0>
 __global__ void __launch_bounds__(pair_threads<EPI, TM>(), 1)
     tc_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
@@ -916,7 +929,7 @@ __global__ void __launch_bounds__(pair_threads<EPI, TM>(), 1)
 
   const int tiles_m2 = (p.tiles_m + 1) >> 1;
   const int num_tiles = tiles_m2 * p.tiles_n * p.NB;
-  const int k_iters = p.G * p.k_blocks;
+  const int num_units = num_tiles * p.ksplit;  // K parts of the split (fp32 partial) GEMMs
 
   if (warp == 0) {
     // ------------------------------------------------ TMA producer (both CTAs)
@@ -927,12 +940,14 @@ __global__ void __launch_bounds__(pair_threads<EPI, TM>(), 1)
 #pragma unroll
       for (int s = 0; s < STAGES; ++s) last_issue_phase[s] = -1;
       bool ok = true;
-      for (int tile = cluster_id; tile < num_tiles && ok; tile += num_clusters) {
+      for (int unit = cluster_id; unit < num_units && ok; unit += num_clusters) {
+        int tile, kb0, nkb;
+        pair_unit(p, unit, num_tiles, tile, kb0, nkb);
         int b, mp, nb;
         decode_pair_tile(p, tile, b, mp, nb);
         const int m0 = mp * 256 + static_cast<int>(rank) * 128;   // this CTA's A rows
         const int n0 = nb * BN + static_cast<int>(rank) * (BN / 2);  // this CTA's half of B
-        for (int it = 0; it < k_iters; ++it) {
+        for (int it = kb0; it < kb0 + nkb; ++it) {
           const int g = it / p.k_blocks;
           const int k0 = (it - g * p.k_blocks) * BK;
           {
@@ -944,7 +959,7 @@ __global__ void __launch_bounds__(pair_threads<EPI, TM>(), 1)
               break;
             }
           }
-          const bool skip = p.debug_skip && tile == cluster_id && it == 0;
+          const bool skip = p.debug_skip && unit == cluster_id && it == kb0;
           if (!skip) {
             uint8_t* sA = smem + stage * L::STAGE_BYTES;
             uint8_t* sB = sA + L::A_BYTES;
@@ -1012,7 +1027,9 @@ __global__ void __launch_bounds__(pair_threads<EPI, TM>(), 1)
 #ifdef TPFFN_INSTRUMENT
       const long long t_start = clock64();
 #endif
-      for (int tile = cluster_id; tile < num_tiles && ok; tile += num_clusters, ++local) {
+      for (int unit = cluster_id; unit < num_units && ok; unit += num_clusters, ++local) {
+        int tile, kb0, nkb;
+        pair_unit(p, unit, num_tiles, tile, kb0, nkb);
         const int buf = local & 1;
         const uint32_t use = static_cast<uint32_t>(local >> 1);
         {
@@ -1023,7 +1040,7 @@ __global__ void __launch_bounds__(pair_threads<EPI, TM>(), 1)
         }
         tc_fence_after();
         const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(buf * BN);
-        for (int it = 0; it < k_iters; ++it) {
+        for (int it = kb0; it < kb0 + nkb; ++it) {
           {
             DBG_T0();
             const bool w_ok = wait_bounded(&full[stage], phase, abort_flag, p);
@@ -1042,7 +1059,7 @@ __global__ void __launch_bounds__(pair_threads<EPI, TM>(), 1)
 #pragma unroll
           for (int k = 0; k < BK / 16; ++k)
             umma_bf16_pair(d_tmem, smem_desc<AMN>(a_addr, k), smem_desc<BMN>(b_addr, k), IDESC,
-                           (it > 0 || k > 0) ? 1u : 0u);
+                           (it > kb0 || k > 0) ? 1u : 0u);
           umma_commit_pair(&empty[stage]);  // frees the stage in both CTAs
           if (++stage == STAGES) {
             stage = 0;
@@ -1316,7 +1333,9 @@ __global__ void __launch_bounds__(pair_threads<EPI, TM>(), 1)
       if (pending) wait_bounded(xb, xph, abort_flag, p, false);
     } else {
       uint32_t staged = 0;  // TMA-store epilogue: chunks this warp has staged
-      for (int tile = cluster_id; tile < num_tiles; tile += num_clusters, ++local) {
+      for (int unit = cluster_id; unit < num_units; unit += num_clusters, ++local) {
+        int tile, kb0, nkb;
+        const int kh = pair_unit(p, unit, num_tiles, tile, kb0, nkb);
         const int buf = local & 1;
         const uint32_t use = static_cast<uint32_t>(local >> 1);
         bool w_ok;
@@ -1329,6 +1348,7 @@ __global__ void __launch_bounds__(pair_threads<EPI, TM>(), 1)
         tc_fence_after();
         int b, mp, nb;
         decode_pair_tile(p, tile, b, mp, nb);
+        b += kh * p.NB;  // K part kh: fp32 batch kh * NB + b (EPI_F32 only)
         const int row0 = mp * 256 + static_cast<int>(rank) * 128 + quarter * 32;
         const uint32_t taddr = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) +
                                static_cast<uint32_t>(buf * BN);
@@ -1661,7 +1681,7 @@ static int launch_pair_inst(const GemmSpec& s, LaunchCtx& ctx, const CUtensorMap
       fprintf(stderr, "tpffn: pair kernel: occupancy query rc=%d clusters=%d -> using %d clusters\n", (int)qe, q, mc);
     max_clusters[dev & 31].store(mc);
   }
-  const long long tiles = static_cast<long long>((p.tiles_m + 1) / 2) * p.tiles_n * p.NB;
+  const long long tiles = static_cast<long long>((p.tiles_m + 1) / 2) * p.tiles_n * p.NB * p.ksplit;  // units
   if (tiles <= 0 || p.k_blocks <= 0) return TP_ERR_INVALID;
   const int clusters = static_cast<int>(tiles < mc ? tiles : mc);
   cfg.gridDim = dim3(2 * clusters, 1, 1);
@@ -1687,9 +1707,11 @@ static int launch_pair(const GemmSpec& s, LaunchCtx& ctx) {
     rc = make_aux_map(&tx, s);
     if (rc) return rc;
   }
-  if (s.ksplit != 1) return TP_ERR_INVALID;  // the K split serves decode-sized GEMMs only
+  // a K split writes fp32 parts (EPI_F32) and needs at least one K block per part
+  if (s.ksplit < 1 || (s.ksplit > 1 && (EPI != EPI_F32 || s.G * ((s.K + BK - 1) / BK) < 2 * s.ksplit)))
+    return TP_ERR_INVALID;
   Params p{};
-  p.ksplit = 1;
+  p.ksplit = s.ksplit;
   p.raster = RASTER_GROUPED;
   if (s.NB > 1 && s.G == 1 && raster_by_sharing()) {
     if (s.A.bsel == 0 && s.B.bsel != 0) p.raster = RASTER_M_FAST;
@@ -1747,7 +1769,7 @@ static int launch_pair(const GemmSpec& s, LaunchCtx& ctx) {
       // stores of the plain epilogue
       const bool f32 = EPI == EPI_F32;
       int sw1 = 0, sw2 = 0;
-      const int64_t nb = s.NB > 1 ? s.NB : 1;
+      const int64_t nb = (s.NB > 1 ? s.NB : 1) * s.ksplit;  // the K parts are further batches
       const int64_t cols1 = EPI == EPI_SWIGLU_FWD ? s.out_rs : s.n_store;
       bool ok = make_out_map(&to, s.out, f32, cols1, s.M, nb, s.out_rs, s.out_bs, &sw1) == 0;
       if (ok && s.out2) {
@@ -1793,6 +1815,8 @@ static bool pair_path_enabled() {
   return on;
 }
 
+bool tc_pair_path(int64_t M) { return M >= 256 && pair_path_enabled(); }
+
 int launch_tc_gemm(const GemmSpec& s, LaunchCtx& ctx) {
   using namespace tc;
   const bool amn = s.A.mn_major != 0, bmn = s.B.mn_major != 0;
@@ -1808,6 +1832,7 @@ int launch_tc_gemm(const GemmSpec& s, LaunchCtx& ctx) {
       case EPI_F32:
         if (!amn && !bmn) return launch_pair<EPI_F32, false, false>(s, ctx);
         if (!amn && bmn) return launch_pair<EPI_F32, false, true>(s, ctx);
+        if (amn && bmn) return launch_pair<EPI_F32, true, true>(s, ctx);  // K-split weight gradients
         break;
       case EPI_OUT:
         if (!amn && !bmn) return launch_pair<EPI_OUT, false, false>(s, ctx);

@@ -49,8 +49,8 @@ struct GemmSpec {
   const void* bias = nullptr; int64_t bias_bs = 0, bias_len = 0;
   int64_t n_store = 0;   // columns n < n_store of the output are written
   int out_bf16 = 1;      // plan dtype of out/out2 (EPI_F32 always fp32)
-  // K split (EPI_F32, G = 1, decode-sized M only): part k of the K blocks is
-  // accumulated on its own and written as fp32 batch k * NB + b of `out`
+  // K split (EPI_F32 only): part k of the K blocks is accumulated on its own
+  // and written as fp32 batch k * NB + b of `out` (one-SM kernel: G = 1)
   int ksplit = 1;
 };
 
@@ -83,6 +83,8 @@ constexpr int DEV_ERR_TIMEOUT = 1;
 
 // tensor-core GEMM (tp_gemm_tc.cu). Returns 0 or a TP_ERR_* code.
 int launch_tc_gemm(const GemmSpec& s, LaunchCtx& ctx);
+// True when a tensor-core GEMM of M rows runs on the two-SM pair kernel.
+bool tc_pair_path(int64_t M);
 // SIMT fp32 GEMM (tp_kernels.cu).
 int launch_simt_gemm(const GemmSpec& s, LaunchCtx& ctx);
 

@@ -138,6 +138,39 @@ def test_many_tiles_per_cluster_against_full_oracle():
     _full_compare(MANY_TILES, True)
 
 
+# Weight-gradient GEMMs with few output tiles split their K (token) axis in
+# two fp32 parts, summed in part order: 2100 tokens = 33 K blocks of 64 (17 +
+# 16, the last one ragged); M = 264 leaves the second 256-row tile pair
+# nearly empty; GELU with biases and SwiGLU both split both weight GEMMs.
+WGRAD_SPLIT = [small_case(2100, 256, 1024, 4, "gelu_tanh", bias=True, seed=114),
+               small_case(2500, 264, 600, 3, "swiglu", seed=115)]
+
+
+@pytest.mark.parametrize("fused", [False, True], ids=["standalone", "fused"])
+@pytest.mark.parametrize("w", WGRAD_SPLIT, ids=[w.name for w in WGRAD_SPLIT])
+def test_wgrad_ksplit_against_full_oracle(w, fused):
+    _full_compare(w, fused)
+
+
+@pytest.mark.parametrize("w", WGRAD_SPLIT + [MANY_TILES], ids=[w.name for w in WGRAD_SPLIT + [MANY_TILES]])
+def test_wgrad_ksplit_is_taken(w):
+    """The cases above run their weight-gradient GEMMs as K parts: the launch
+    records name the part sums right after each split GEMM."""
+    from megatron_tensor_transformer_w1_gb300 import tpffn as abi
+    from megatron_tensor_transformer_w1_gb300.ffn import TensorParallelFFN
+    dev = torch.device("cuda", 0)
+    g = {k: (None if v is None else v.to(dev)) for k, v in make_inputs(w).items()}
+    ffn = TensorParallelFFN(w.d, w.d_ff, w.T_p, w.act, "bf16", device=dev)
+    w13p, w2p = ffn.pack(g["W1"], g["W2"], g["W3"])
+    _, saved, _ = ffn.forward(g["x"], w13p, w2p, g["b1"], g["b2"], fused=True)
+    ffn.backward(g["x"], w13p, w2p, saved, g["dy"], fused=True, bias=w.bias, flags=abi.TP_FLAG_TIMING)
+    names = [n for n, _ in abi.tp_ffn_kernel_times(ffn.plan, 1000)]
+    wg1 = "wgrad_w13" if w.act == "swiglu" else "wgrad_w1"
+    assert "wgrad_w2" in names and names[names.index("wgrad_w2") + 1] == "wgrad_w2_ksum", names
+    if w is not MANY_TILES:  # 64 tiles of 2048 x 512 already fill the SM pairs
+        assert names[names.index(wg1) + 1] == wg1 + "_ksum", names
+
+
 def _sweep_cases(n=10, seed=20261202):
     """Seeded random shapes across both kernel paths (token counts of at most
     32, under 256 and above), both activations, biases on or off, ragged
