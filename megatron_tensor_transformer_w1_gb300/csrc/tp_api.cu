@@ -88,6 +88,24 @@ int64_t colsum_chunk(int64_t rows) {
   return c;
 }
 
+ColsumJob colsum_job(const void* in, int in_bf16, int64_t batch, int64_t rows, int64_t cols, int64_t rs, int64_t bs,
+                     void* out, int out_bf16, int64_t out_bs, float* scratch, int64_t n) {
+  ColsumJob q;
+  q.in = in;
+  q.in_bf16 = in_bf16;
+  q.batch = static_cast<int>(batch);
+  q.rows = rows;
+  q.cols = cols;
+  q.rs = rs;
+  q.bs = bs;
+  q.out = out;
+  q.out_bf16 = out_bf16;
+  q.out_bs = out_bs;
+  q.scratch = scratch;
+  q.chunk_rows = colsum_chunk(n);
+  return q;
+}
+
 struct WsLayout {
   size_t h = 0, part = 0, D = 0, cs = 0, ks = 0, wk = 0, total = 0;
   bool has_part = false, has_ks = false, has_wk = false;
@@ -183,7 +201,8 @@ WsLayout ws_layout(const tp_ffn_plan* p, int64_t n, int flags) {
   L.cs = off;
   const int64_t cs1 = colsum_scratch_floats(p->T_p, n, p->s_pad, colsum_chunk(n));
   const int64_t cs2 = colsum_scratch_floats(1, n, p->d, colsum_chunk(n));
-  off += align_up(static_cast<size_t>(cs1 > cs2 ? cs1 : cs2) * 4);
+  // db1 (GELU plans only) and db2 sum in the same launches, side by side
+  off += align_up(static_cast<size_t>(p->act == TP_ACT_GELU_TANH ? cs1 + cs2 : (cs1 > cs2 ? cs1 : cs2)) * 4);
   L.total = off;
   return L;
 }
@@ -710,9 +729,11 @@ static int bwd_impl(const tp_ffn_plan* p, int64_t n, const void* x, const void* 
     w.n_store = s;
     w.out_bf16 = out_bf16;
     rc = run_gemm(p, w, ctx);
-    if (!rc && db2)
-      rc = launch_colsum(dy, out_bf16, 1, n, d, d, n * d, db2, out_bf16, 0, cs_scratch, colsum_chunk(n), ctx,
-                         "colsum_db2");
+    if (!rc && db2) {
+      ColsumJobs J;
+      J.j[J.n++] = colsum_job(dy, out_bf16, 1, n, d, d, n * d, db2, out_bf16, 0, cs_scratch, n);
+      rc = launch_colsums(J, ctx, "colsum_db2");
+    }
     return rc;
   }
 
@@ -824,13 +845,13 @@ static int bwd_impl(const tp_ffn_plan* p, int64_t n, const void* x, const void* 
     rc = run_wgrad(p, g, n, L, ws, ctx, p->act == TP_ACT_SWIGLU ? "wgrad_w13_ksum" : "wgrad_w1_ksum");
     if (rc) return rc;
   }
-  // ---- 6. bias gradients
-  if (db1)
-    rc = launch_colsum(D, out_bf16, T, n, s, W, n * W, db1, out_bf16, s, cs_scratch, colsum_chunk(n), ctx,
-                       "colsum_db1");
-  if (!rc && db2)
-    rc = launch_colsum(dy, out_bf16, 1, n, d, d, n * d, db2, out_bf16, 0, cs_scratch, colsum_chunk(n), ctx,
-                       "colsum_db2");
+  // ---- 6. bias gradients (both column sums in one pair of launches)
+  ColsumJobs J;
+  if (db1) J.j[J.n++] = colsum_job(D, out_bf16, T, n, s, W, n * W, db1, out_bf16, s, cs_scratch, n);
+  if (db2)
+    J.j[J.n++] = colsum_job(dy, out_bf16, 1, n, d, d, n * d, db2, out_bf16, 0,
+                            cs_scratch + (db1 ? colsum_scratch_floats(T, n, sp, colsum_chunk(n)) : 0), n);
+  if (J.n) rc = launch_colsums(J, ctx, db1 && db2 ? "colsum_db" : db1 ? "colsum_db1" : "colsum_db2");
   return rc;
 }
 

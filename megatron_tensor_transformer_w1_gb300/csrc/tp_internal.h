@@ -111,10 +111,23 @@ int launch_scatter_rows(const void* src, int64_t n, int64_t cols, int esz, const
 int launch_shard_sum_scatter(const float* partials, int T_p, int64_t rows, int64_t cols, const void* bias,
                              const RowSlices& out, int out_bf16, LaunchCtx& ctx, const char* name);
 // Column sums of a [batch][rows][cols] view (row stride rs, batch stride bs)
-// into out[b*out_bs + col] for col < cols, deterministic two-pass order.
-int launch_colsum(const void* in, int in_bf16, int64_t batch, int64_t rows, int64_t cols,
-                  int64_t rs, int64_t bs, void* out, int out_bf16, int64_t out_bs,
-                  float* scratch, int64_t chunk_rows, LaunchCtx& ctx, const char* name);
+// into out[b*out_bs + col] for col < cols, deterministic two-pass order; the
+// chunk sums go to `scratch` (colsum_scratch_floats floats).  Up to two such
+// jobs share one pair of launches.
+struct ColsumJob {
+  const void* in = nullptr;
+  void* out = nullptr;
+  float* scratch = nullptr;
+  long long rows = 0, cols = 0, rs = 0, bs = 0, out_bs = 0, chunk_rows = 64;
+  int in_bf16 = 1, out_bf16 = 1, batch = 0;
+  long long chunks = 0;       // set by launch_colsums
+  int blocks1 = 0, blocks2 = 0;  // set by launch_colsums
+};
+struct ColsumJobs {
+  ColsumJob j[2];
+  int n = 0;
+};
+int launch_colsums(ColsumJobs jobs, LaunchCtx& ctx, const char* name);
 int64_t colsum_scratch_floats(int64_t batch, int64_t rows, int64_t cols, int64_t chunk_rows);
 
 // Attention core of the head-sharded attention sublayer (tp_attention.cu).

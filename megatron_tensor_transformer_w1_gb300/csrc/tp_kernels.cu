@@ -11,6 +11,8 @@
 //   simt_gemm      : fp32 GEMM with the same epilogues as the tensor-core
 //                    kernel, for fp32 plans (TF32 would not meet fp32
 //                    accuracy, so these use plain FMA)
+#include <climits>
+
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
@@ -243,31 +245,47 @@ __global__ void __launch_bounds__(256) shard_sum_scatter_vec8_kernel(const float
 }
 
 // ------------------------------------------------------------------ colsum
+// Column sums over the rows of up to two [batch][rows][cols] inputs (the
+// bias gradients db1 and db2 of one backward call) in two launches, each
+// block taking its job and coordinates from its linear index.
 // Pass 1: a block covers 256 columns of one chunk of rows: 32 column groups
 // of 8 (16-byte loads of bf16 rows where the layout allows) times 8 row
 // lanes, lane l taking rows l, l+8, ...; the lanes' partial sums are then
-// added in lane order, so the result is fixed for a given chunking.
-__global__ void __launch_bounds__(256) colsum_pass1_kernel(const void* in, int in_bf16, long long rows,
-                                                           long long cols, long long rs, long long bs,
-                                                           float* scratch, long long chunk_rows, long long chunks) {
+// added in lane order.  Pass 2: a block covers 32 columns: 8 lanes, lane l
+// adding chunks l, l+8, ... in order, then the lane sums in lane order.  The
+// result is fixed for a given chunking.
+__device__ __forceinline__ int colsum_pick(const ColsumJobs& J, int& local, bool pass2) {
+  const int b0 = pass2 ? J.j[0].blocks2 : J.j[0].blocks1;
+  if (J.n > 1 && local >= b0) {
+    local -= b0;
+    return 1;
+  }
+  return 0;
+}
+
+__global__ void __launch_bounds__(256) colsum_pass1_kernel(const ColsumJobs J) {
   __shared__ float part[8][256 + 4];
-  // a programmatic dependent of the kernel that wrote `in`
+  // a programmatic dependent of the kernel that wrote the inputs
   asm volatile("griddepcontrol.wait;" ::: "memory");
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  int local = static_cast<int>(blockIdx.x);
+  const ColsumJob& q = J.j[colsum_pick(J, local, false)];
+  const int cbs = static_cast<int>((q.cols + 255) / 256);
+  const long long cb = local % cbs;
+  const long long chunk = (local / cbs) % q.chunks;
+  const long long b = (local / cbs) / q.chunks;
   const int cg = threadIdx.x & 31, lane = threadIdx.x >> 5;
-  const long long c0 = blockIdx.x * 256LL + cg * 8;
-  const long long chunk = blockIdx.y;
-  const long long b = blockIdx.z;
-  const long long r0 = chunk * chunk_rows;
-  const long long r1 = min(rows, r0 + chunk_rows);
-  const bool vec = in_bf16 && rs % 8 == 0 && bs % 8 == 0 && (reinterpret_cast<uintptr_t>(in) & 15) == 0 &&
-                   c0 + 8 <= cols;
+  const long long c0 = cb * 256 + cg * 8;
+  const long long r0 = chunk * q.chunk_rows;
+  const long long r1 = min(q.rows, r0 + q.chunk_rows);
+  const bool vec = q.in_bf16 && q.rs % 8 == 0 && q.bs % 8 == 0 && (reinterpret_cast<uintptr_t>(q.in) & 15) == 0 &&
+                   c0 + 8 <= q.cols;
   float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
   for (long long r = r0 + lane; r < r1; r += 8) {
-    const long long base = b * bs + r * rs + c0;
+    const long long base = b * q.bs + r * q.rs + c0;
     if (vec) {
-      const uint4 q = *reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(in) + base);
-      const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&q);
+      const uint4 v = *reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(q.in) + base);
+      const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&v);
 #pragma unroll
       for (int k = 0; k < 4; ++k) {
         const float2 f = __bfloat1622float2(h[k]);
@@ -277,29 +295,40 @@ __global__ void __launch_bounds__(256) colsum_pass1_kernel(const void* in, int i
     } else {
 #pragma unroll
       for (int j = 0; j < 8; ++j)
-        if (c0 + j < cols) acc[j] += to_f(in, base + j, in_bf16);
+        if (c0 + j < q.cols) acc[j] += to_f(q.in, base + j, q.in_bf16);
     }
   }
 #pragma unroll
   for (int j = 0; j < 8; ++j) part[lane][cg * 8 + j] = acc[j];
   __syncthreads();
-  const long long col = blockIdx.x * 256LL + threadIdx.x;
-  if (col >= cols) return;
+  const long long col = cb * 256 + threadIdx.x;
+  if (col >= q.cols) return;
   float sum = 0.f;
 #pragma unroll
   for (int l = 0; l < 8; ++l) sum += part[l][threadIdx.x];
-  scratch[(b * chunks + chunk) * cols + col] = sum;
+  q.scratch[(b * q.chunks + chunk) * q.cols + col] = sum;
 }
-__global__ void colsum_pass2_kernel(const float* scratch, long long cols, long long chunks, void* out, int out_bf16,
-                                    long long out_bs) {
+
+__global__ void __launch_bounds__(256) colsum_pass2_kernel(const ColsumJobs J) {
+  __shared__ float part[8][32 + 1];
   asm volatile("griddepcontrol.wait;" ::: "memory");  // pass 1's chunk sums are visible
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-  const long long col = blockIdx.x * (long long)blockDim.x + threadIdx.x;
-  const long long b = blockIdx.y;
-  if (col >= cols) return;
+  int local = static_cast<int>(blockIdx.x);
+  const ColsumJob& q = J.j[colsum_pick(J, local, true)];
+  const int cbs = static_cast<int>((q.cols + 31) / 32);
+  const long long b = local / cbs;
+  const long long col = (local % cbs) * 32LL + (threadIdx.x & 31);
+  const int lane = threadIdx.x >> 5;
   float acc = 0.f;
-  for (long long c = 0; c < chunks; ++c) acc += scratch[(b * chunks + c) * cols + col];
-  from_f(out, b * out_bs + col, acc, out_bf16);
+  if (col < q.cols)
+    for (long long c = lane; c < q.chunks; c += 8) acc += q.scratch[(b * q.chunks + c) * q.cols + col];
+  part[lane][threadIdx.x & 31] = acc;
+  __syncthreads();
+  if (threadIdx.x >= 32 || col >= q.cols) return;
+  float sum = 0.f;
+#pragma unroll
+  for (int l = 0; l < 8; ++l) sum += part[l][threadIdx.x];
+  from_f(q.out, b * q.out_bs + col, sum, q.out_bf16);
 }
 
 // ---------------------------------------------------------------- SIMT GEMM
@@ -652,20 +681,30 @@ int64_t colsum_scratch_floats(int64_t batch, int64_t rows, int64_t cols, int64_t
   return batch * (chunks > 0 ? chunks : 1) * cols;
 }
 
-int launch_colsum(const void* in, int in_bf16, int64_t batch, int64_t rows, int64_t cols, int64_t rs, int64_t bs,
-                  void* out, int out_bf16, int64_t out_bs, float* scratch, int64_t chunk_rows, LaunchCtx& ctx,
-                  const char* name) {
-  if (batch <= 0 || cols <= 0) return 0;
-  const int64_t chunks = rows > 0 ? (rows + chunk_rows - 1) / chunk_rows : 0;
+int launch_colsums(ColsumJobs J, LaunchCtx& ctx, const char* name) {
+  long long g1 = 0, g2 = 0;
+  int kept = 0;
+  for (int i = 0; i < J.n; ++i) {
+    ColsumJob& q = J.j[i];
+    if (q.batch <= 0 || q.cols <= 0) continue;
+    q.chunks = q.rows > 0 ? (q.rows + q.chunk_rows - 1) / q.chunk_rows : 0;
+    const long long b1 = (q.cols + 255) / 256 * q.chunks * q.batch, b2 = (q.cols + 31) / 32 * q.batch;
+    if (b1 > INT_MAX || b2 > INT_MAX) return TP_ERR_UNSUPPORTED;
+    q.blocks1 = static_cast<int>(b1);
+    q.blocks2 = static_cast<int>(b2);
+    g1 += b1;
+    g2 += b2;
+    J.j[kept++] = q;
+  }
+  J.n = kept;
+  if (kept == 0) return 0;
+  if (g1 > INT_MAX || g2 > INT_MAX) return TP_ERR_UNSUPPORTED;
   if (ctx.before) ctx.before(ctx.user, name, ctx.stream);
-  if (chunks > 0) {
-    dim3 g1(static_cast<unsigned>((cols + 255) / 256), static_cast<unsigned>(chunks), static_cast<unsigned>(batch));
-    launch_pdl(colsum_pass1_kernel, g1, 256, ctx.stream, in, in_bf16, rows, cols, rs, bs, scratch, chunk_rows,
-               chunks);
+  if (g1 > 0) {  // no rows: pass 2 writes zeros
+    launch_pdl(colsum_pass1_kernel, dim3(static_cast<unsigned>(g1)), 256, ctx.stream, J);
     ctx.launches++;
   }
-  dim3 g2(static_cast<unsigned>((cols + 255) / 256), static_cast<unsigned>(batch));
-  launch_pdl(colsum_pass2_kernel, g2, 256, ctx.stream, scratch, cols, chunks, out, out_bf16, out_bs);
+  launch_pdl(colsum_pass2_kernel, dim3(static_cast<unsigned>(g2)), 256, ctx.stream, J);
   ctx.launches++;
   if (ctx.after) ctx.after(ctx.user, ctx.stream);
   return cudaPeekAtLastError() == cudaSuccess ? 0 : TP_ERR_CUDA;
