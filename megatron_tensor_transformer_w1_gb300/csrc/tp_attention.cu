@@ -32,6 +32,10 @@
 //    query head of its GQA group): S^T and dP^T, P^T and dS^T to shared
 //    memory, dV += P^T dO and dK += dS^T Q in TMEM -- the whole group's sum
 //    stays in fp32 and is rounded once.
+// Outputs (o, dQ, dK, dV) leave through shared memory: each softmax warp
+// stages its 32 rows, then either one TMA store writes them (the forward) or
+// the warp stores whole row segments (dq, dk/dv) -- a row per lane stored
+// directly touches 32 rows per store instruction.
 // No atomics anywhere: the results are bit-identical run to run.
 //
 // Every mbarrier wait is bounded (device error word + CTA abort flag, then
@@ -240,16 +244,51 @@ __device__ __forceinline__ int item_of(uint32_t n) {
   return static_cast<int>(n * G + ((n & 1u) ? G - 1u - c : c));
 }
 
-__device__ __forceinline__ void store_row_bf16(__nv_bfloat16* dst, const uint32_t (&r)[32], float mul) {
+// Packs 32 fp32 values (times mul) into 16 bf16 pairs.
+__device__ __forceinline__ void pack_row_bf16(uint32_t* dst, const uint32_t (&r)[32], float mul) {
 #pragma unroll
-  for (int q = 0; q < 4; ++q) {
+  for (int i = 0; i < 16; ++i)
+    dst[i] = pack_bf16x2(__uint_as_float(r[2 * i]) * mul, __uint_as_float(r[2 * i + 1]) * mul);
+}
+
+// A warp's 32 output rows (row r held by lane r as 16 NC bf16 pairs, NC
+// 32-column chunks) go to global memory through the warp's own staging
+// buffer of 32 x 64 NC bytes: each lane writes its row (stage_row_chunk, one
+// 32-column chunk at a time), then the warp reads the rows back so that every
+// store instruction covers whole 64 NC-byte row segments of 32 / (4 NC) rows
+// (store_staged_rows), instead of 16 bytes of each of 32 rows (a row per
+// lane, stored directly, costs one L1 wavefront per row and instruction).
+// Row r goes to base + r * rs if r < valid_rows.  The staging rows are
+// swizzled (16-byte chunk k of row r at k ^ (r & 7), or k ^ ((r >> 1) & 3)
+// for 64-byte rows) so that both passes are free of bank conflicts.
+template <int NC>
+__device__ __forceinline__ int stage_swz(int k, int r) {
+  return NC == 2 ? (k ^ (r & 7)) : (k ^ ((r >> 1) & 3));
+}
+template <int NC>
+__device__ __forceinline__ void stage_row_chunk(uint32_t buf, int c, const uint32_t (&pk)[16]) {
+  const int lane = threadIdx.x & 31;
+#pragma unroll
+  for (int k = 0; k < 4; ++k)
+    st_shared_v4(buf + static_cast<uint32_t>(lane * 64 * NC + 16 * stage_swz<NC>(4 * c + k, lane)), pk[4 * k],
+                 pk[4 * k + 1], pk[4 * k + 2], pk[4 * k + 3]);
+}
+template <int NC>
+__device__ __forceinline__ void store_staged_rows(uint32_t buf, __nv_bfloat16* base, long long rs, int valid_rows) {
+  constexpr int CH = 4 * NC;  // 16-byte chunks per row
+  constexpr int RPI = 32 / CH;  // rows per store instruction
+  const int lane = threadIdx.x & 31;
+  __syncwarp();
+#pragma unroll
+  for (int i = 0; i < CH; ++i) {
+    const int r = i * RPI + lane / CH, k = lane % CH;
     uint4 v;
-    v.x = pack_bf16x2(__uint_as_float(r[q * 8 + 0]) * mul, __uint_as_float(r[q * 8 + 1]) * mul);
-    v.y = pack_bf16x2(__uint_as_float(r[q * 8 + 2]) * mul, __uint_as_float(r[q * 8 + 3]) * mul);
-    v.z = pack_bf16x2(__uint_as_float(r[q * 8 + 4]) * mul, __uint_as_float(r[q * 8 + 5]) * mul);
-    v.w = pack_bf16x2(__uint_as_float(r[q * 8 + 6]) * mul, __uint_as_float(r[q * 8 + 7]) * mul);
-    *reinterpret_cast<uint4*>(dst + q * 8) = v;
+    asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "r"(buf + static_cast<uint32_t>(r * 64 * NC + 16 * stage_swz<NC>(k, r))));
+    if (r < valid_rows) *reinterpret_cast<uint4*>(base + r * rs + k * 8) = v;
   }
+  __syncwarp();  // the buffer is rewritten only after every lane has read it
 }
 
 // ================================================================ forward
@@ -258,7 +297,8 @@ constexpr int F_K = F_Q + 2 * TILE;   // 2 stages
 constexpr int F_V = F_K + 2 * TILE;   // 2 stages
 constexpr int F_X = F_V + 2 * TILE;   // row max / sum exchange [2 halves][128 rows] fp32
 constexpr int F_BAR = F_X + 1024;
-constexpr int F_SMEM = F_BAR + 512 + 1024;
+constexpr int F_O = F_BAR + 1024;     // output staging, 4 KB per softmax warp (1024-byte aligned)
+constexpr int F_SMEM = F_O + 8 * 4096 + 1024;
 
 // P never leaves the chip: the softmax threads write it in bf16 over the S
 // block it came from (two probabilities per 32-bit cell), and the PV product
@@ -273,7 +313,8 @@ constexpr int F_SMEM = F_BAR + 512 + 1024;
 // first 32 of its own 64 S columns).  The halves meet once per work item,
 // when O = (O_0 2^{m_0 - m} + O_1 2^{m_1 - m}) / l is written out, instead of
 // exchanging their maxima for every block.
-__global__ void __launch_bounds__(NT, 1) attn_fwd_kernel(const __grid_constant__ CUtensorMap tq, const Params p) {
+__global__ void __launch_bounds__(NT, 1) attn_fwd_kernel(const __grid_constant__ CUtensorMap tq,
+                                                         const __grid_constant__ CUtensorMap to, const Params p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = align1024(smem_raw);
   uint64_t* bar = reinterpret_cast<uint64_t*>(smem + F_BAR);
@@ -613,22 +654,35 @@ __global__ void __launch_bounds__(NT, 1) attn_fwd_kernel(const __grid_constant__
           if (!W.warp(&pv_done[pglast & 1u], (pglast >> 1) & 1u)) { ok = false; break; }
           tc_fence_after();
           const bool row_ok = pqpos < p.S;
-          __nv_bfloat16* orow = p.o + (static_cast<long long>(pb) * p.S + pqpos) * p.o_rs + ph * HD + half * 64;
+          // this warp's 32 rows x 64 columns of o, staged in the 128-byte
+          // swizzle of the output tensor map and written by one TMA store
+          // (rows past the sequence are outside the map)
+          uint8_t* obuf = smem + F_O + (warp - 2) * 4096;
+          if (lane == 0) bulk_wait_read<0>();  // the previous item's store has read the buffer
+          __syncwarp();
 #pragma unroll 1
           for (int c = 0; c < 2; ++c) {
-            uint32_t o0[32], o1[32];
+            uint32_t o0[32], o1[32], pk[16];
             tmem_ld32(tl + 256 + half * 64 + c * 32, o0);
             tmem_ld32(tl + 384 + half * 64 + c * 32, o1);
             tmem_wait_ld();
 #pragma unroll
             for (int i = 0; i < 32; ++i)
               o0[i] = __float_as_uint(fmaf(__uint_as_float(o0[i]), pf0, __uint_as_float(o1[i]) * pf1));
-            if (row_ok) store_row_bf16(orow + c * 32, o0, pinv);
+            pack_row_bf16(pk, o0, pinv);
+            stage_row_chunk<2>(smem_u32(obuf), c, pk);
+          }
+          // O has been read: the next item's PV products may start
+          tc_fence_before();
+          fence_proxy_async_smem();
+          warp_arrive(o_empty);
+          const int r0 = pqpos - lane;  // this warp's first row
+          if (lane == 0) {
+            if (r0 < p.S) tma_store_3d(&to, obuf, ph * HD + half * 64, r0, pb);
+            bulk_commit();
           }
           // rows past the sequence get lse = +inf: the backward reads them as p = 0
           if (half == 0) p.lse[(static_cast<long long>(pb) * p.H + ph) * p.s_pad + pqpos] = row_ok ? plse : INFINITY;
-          tc_fence_before();
-          warp_arrive(o_empty);
 #ifdef TPFFN_INSTRUMENT
           if (rec) AT_ADD(14, t14);
 #endif
@@ -655,6 +709,8 @@ __global__ void __launch_bounds__(NT, 1) attn_fwd_kernel(const __grid_constant__
 #ifdef TPFFN_INSTRUMENT
     if (rec) AT_ADD(15, t_sm);
 #endif
+    if (lane == 0) bulk_wait_all();  // the output stores are done before the CTA exits
+    __syncwarp();
   }
 
   tc_fence_before();
@@ -912,7 +968,6 @@ __global__ void __launch_bounds__(NT, 1) attn_dq_kernel(const __grid_constant__ 
       decode_item(p, item, p.H, p.causal != 0, qb, b, h);
       const int nkb = nkb_of(qb);
       const int qpos = qb * 128 + row;
-      const bool row_ok = qpos < p.S;
       const long long vrow = (static_cast<long long>(b) * p.H + h) * p.s_pad + qpos;
       // rows past the sequence read lse = +inf (written by the forward): p = 0
       const float lse_r = p.lse[vrow];
@@ -972,17 +1027,22 @@ __global__ void __launch_bounds__(NT, 1) attn_dq_kernel(const __grid_constant__ 
       if (item_of(it + 1) < p.items && !copy_qdo(item_of(it + 1), it + 1)) break;
       if (!W.warp(dq_full, it & 1u)) break;
       tc_fence_after();
-      __nv_bfloat16* out =
-          p.dqkv + (static_cast<long long>(b) * p.S + qpos) * p.dqkv_rs + p.g.qcol(h) + half * 64;
+      // staged in this warp's own quarter of the dS tile, which the item's
+      // last dQ product has read (dq_full) and which this warp rewrites next
+      const uint32_t obuf = smem_u32(smem + Q_DS) + static_cast<uint32_t>(half * 16384 + quarter * 4096);
 #pragma unroll 1
       for (int c = 0; c < 2; ++c) {
-        uint32_t o[32];
+        uint32_t o[32], pk[16];
         tmem_ld32(tl + DQ_ACC + half * 64 + c * 32, o);
         tmem_wait_ld();
-        if (row_ok) store_row_bf16(out + c * 32, o, 1.f);
+        pack_row_bf16(pk, o, 1.f);
+        stage_row_chunk<2>(obuf, c, pk);
       }
       tc_fence_before();
       warp_arrive(dq_empty);
+      const int r0 = qpos - lane;
+      store_staged_rows<2>(obuf, p.dqkv + (static_cast<long long>(b) * p.S + r0) * p.dqkv_rs + p.g.qcol(h) + half * 64,
+                           p.dqkv_rs, p.S - r0);
     }
   }
 
@@ -1011,7 +1071,8 @@ constexpr int V_Q = V_V + TILE;           // VST stages of [128 q][128]
 constexpr int V_DO = V_Q + VST * TILE;    // VST stages
 constexpr int V_VEC = V_DO + VST * TILE;  // VST stages x (128 lse + 128 D) floats
 constexpr int V_BAR = V_VEC + VST * 1024;
-constexpr int V_SMEM = V_BAR + 256 + 1024;
+constexpr int V_O = V_BAR + 256;          // output staging, 2 KB per softmax warp
+constexpr int V_SMEM = V_O + 8 * 2048 + 1024;
 
 // The softmax warps keep P^T and dS^T in tensor memory: each thread writes
 // its bf16 pairs (two per 32-bit cell, lower K in the low half) over the
@@ -1205,7 +1266,6 @@ __global__ void __launch_bounds__(NT, 1) attn_dkdv_kernel(const __grid_constant_
       const int i0 = q0_of(kb), nq = p.n_qb - i0;
       const int n_it = p.G * nq;
       const int kpos = kb * 128 + row;
-      const bool row_ok = kpos < p.S;
       bool ok = true;
       for (int t = 0; t < n_it; ++t) {
         const int i = i0 + t % nq;
@@ -1268,24 +1328,26 @@ __global__ void __launch_bounds__(NT, 1) attn_dkdv_kernel(const __grid_constant_
       if (!ok) break;
       if (!W.warp(dkv_full, it & 1u)) break;
       tc_fence_after();
-      __nv_bfloat16* out = p.dqkv + (static_cast<long long>(b) * p.S + kpos) * p.dqkv_rs + half * 64;
-      const int vcol = p.g.vcol(hk), kcol = p.g.kcol(hk);
-#pragma unroll 1
-      for (int c = 0; c < 2; ++c) {
+      // dV (columns 256..383) and dK (384..511) of this warp's rows, packed
+      uint32_t pk[4][16];
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
         uint32_t o[32];
-        tmem_ld32(tl + 256 + half * 64 + c * 32, o);
+        tmem_ld32(tl + 256 + (c >> 1) * 128 + half * 64 + (c & 1) * 32, o);
         tmem_wait_ld();
-        if (row_ok) store_row_bf16(out + vcol + c * 32, o, 1.f);
-      }
-#pragma unroll 1
-      for (int c = 0; c < 2; ++c) {
-        uint32_t o[32];
-        tmem_ld32(tl + 384 + half * 64 + c * 32, o);
-        tmem_wait_ld();
-        if (row_ok) store_row_bf16(out + kcol + c * 32, o, 1.f);
+        pack_row_bf16(pk[c], o, 1.f);
       }
       tc_fence_before();
       warp_arrive(dkv_empty);
+      const int r0 = kpos - lane;
+      __nv_bfloat16* out = p.dqkv + (static_cast<long long>(b) * p.S + r0) * p.dqkv_rs + half * 64;
+      const int vcol = p.g.vcol(hk), kcol = p.g.kcol(hk);
+      const uint32_t sbuf = smem_u32(smem + V_O) + static_cast<uint32_t>((warp - 2) * 2048);
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        stage_row_chunk<1>(sbuf, 0, pk[c]);
+        store_staged_rows<1>(sbuf, out + ((c >> 1) ? kcol : vcol) + (c & 1) * 32, p.dqkv_rs, p.S - r0);
+      }
       qc += n_it;
       sc += n_it;
     }
@@ -1321,7 +1383,7 @@ __global__ void pack_qkv_kernel(const __nv_bfloat16* Wq, const __nv_bfloat16* Wk
 }
 
 // barrier areas (mbarriers + TMEM slot + abort flag) fit their reserved bytes
-static_assert(F_SMEM - F_BAR - 1024 >= 33 * 8 + 8, "forward barrier area");
+static_assert(F_O - F_BAR >= 33 * 8 + 8 && F_O % 1024 == 0, "forward barrier area, staging alignment");
 static_assert(Q_SMEM - Q_BAR - 1024 >= 21 * 8 + 8, "dq barrier area");
 static_assert(V_SMEM - V_BAR - 1024 >= (8 + 2 * VST) * 8 + 8, "dk/dv barrier area");
 static_assert(F_SMEM <= 232448 && Q_SMEM <= 232448 && V_SMEM <= 232448, "shared memory per CTA");
@@ -1419,14 +1481,15 @@ int launch_attn_fwd(const AttnSpec& a, LaunchCtx& ctx) {
   int rc = check_spec(a);
   if (rc) return rc;
   if (!a.qkv || !a.o || !a.lse) return TP_ERR_INVALID;
-  CUtensorMap tq;
+  CUtensorMap tq, to;
   if ((rc = map_rows(&tq, a.qkv, a.qkv_rs, a.S, a.B, 128))) return rc;
+  if ((rc = map_rows(&to, a.o, a.o_rs, a.S, a.B, 32))) return rc;  // 32-row output boxes
   Params p = make_params(a, ctx);
   p.items = p.n_qb * a.B * a.H;
   static std::atomic<uint32_t> done{0};
   if ((rc = set_smem_once(attn_fwd_kernel, F_SMEM, done))) return rc;
   if (ctx.before) ctx.before(ctx.user, "attn_fwd", ctx.stream);
-  attn_fwd_kernel<<<grid_for(p.items, ctx.num_sms), NT, F_SMEM, ctx.stream>>>(tq, p);
+  attn_fwd_kernel<<<grid_for(p.items, ctx.num_sms), NT, F_SMEM, ctx.stream>>>(tq, to, p);
   if (ctx.after) ctx.after(ctx.user, ctx.stream);
   ctx.launches++;
   return cudaPeekAtLastError() == cudaSuccess ? TP_OK : TP_ERR_CUDA;
