@@ -86,6 +86,8 @@ struct Params {
   int ksplit;    // K split into this many parts (1: none; fp32 parts only)
   int raster;    // pair kernel tile order (RASTER_*)
   int o_swap;    // pair kernel TMA stores: output maps are {cols, batch, rows} (batch stride < row stride)
+  int keep_op;   // pair kernel: operand every batch shares (1: A, 2: B, 0: none); the other one
+                 // streams through L2 with evict_first priority
 };
 
 // Pair-kernel tile orders.  Grouped raster order (the default) lets the
@@ -552,6 +554,33 @@ __device__ __forceinline__ void tma_load_3d_pair(void* dst, const CUtensorMap* t
       "l"(reinterpret_cast<uint64_t>(tm)), "r"(c0), "r"(c1), "r"(c2), "r"(leader_bar)
       : "memory");
 }
+// The same copies with an L2 cache policy (createpolicy) attached.
+__device__ __forceinline__ void tma_load_4d_pair_hint(void* dst, const CUtensorMap* tm, uint32_t leader_bar, int c0,
+                                                      int c1, int c2, int c3, uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.tensor.4d.cta_group::2.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint "
+      "[%0], [%1, {%2, %3, %4, %5}], [%6], %7;" ::"r"(smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(tm)), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(leader_bar), "l"(policy)
+      : "memory");
+}
+__device__ __forceinline__ void tma_load_3d_pair_hint(void* dst, const CUtensorMap* tm, uint32_t leader_bar, int c0,
+                                                      int c1, int c2, uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.cta_group::2.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint "
+      "[%0], [%1, {%2, %3, %4}], [%5], %6;" ::"r"(smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(tm)), "r"(c0), "r"(c1), "r"(c2), "r"(leader_bar), "l"(policy)
+      : "memory");
+}
+__device__ __forceinline__ uint64_t l2_policy_evict_normal() {
+  uint64_t pol;
+  asm volatile("createpolicy.fractional.L2::evict_normal.b64 %0, 1.0;" : "=l"(pol));
+  return pol;
+}
+__device__ __forceinline__ uint64_t l2_policy_evict_first() {
+  uint64_t pol;
+  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
+  return pol;
+}
 __device__ __forceinline__ void tmem_alloc_pair(uint32_t* slot, uint32_t ncols) {
   asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(slot)),
                "r"(ncols)
@@ -940,6 +969,7 @@ __global__ void __launch_bounds__(pair_threads<EPI, TM>(), 1)
 #pragma unroll
       for (int s = 0; s < STAGES; ++s) last_issue_phase[s] = -1;
       bool ok = true;
+      const uint64_t pol_keep = l2_policy_evict_normal(), pol_stream = l2_policy_evict_first();
       for (int unit = cluster_id; unit < num_units && ok; unit += num_clusters) {
         int tile, kb0, nkb;
         pair_unit(p, unit, num_tiles, tile, kb0, nkb);
@@ -972,10 +1002,20 @@ __global__ void __launch_bounds__(pair_threads<EPI, TM>(), 1)
             if (leader) mbar_arrive_expect_tx(&full[stage], 2 * L::STAGE_BYTES);
             const int ab = b * p.a_bsel + g * p.a_gsel;
             const int bb = b * p.b_bsel + g * p.b_gsel;
-            if (!AMN) {
-              tma_load_3d_pair(sA, &tmA, leader_full, k0, p.a_swap ? ab : m0, p.a_swap ? m0 : ab);
+            if (p.keep_op) {
+              // the per-batch operand streams through L2 with evict_first
+              // priority, so that the operand all batches share stays there;
+              // MN-major operands here always use the 4-D map (set on the host)
+              const uint64_t pa = p.keep_op == 1 ? pol_keep : pol_stream;
+              const uint64_t pb = p.keep_op == 1 ? pol_stream : pol_keep;
+              if (!AMN) tma_load_3d_pair_hint(sA, &tmA, leader_full, k0, p.a_swap ? ab : m0, p.a_swap ? m0 : ab, pa);
+              else tma_load_4d_pair_hint(sA, &tmA, leader_full, 0, k0, m0 / 64, ab, pa);
+              if (!BMN) tma_load_3d_pair_hint(sB, &tmB, leader_full, k0, p.b_swap ? bb : n0, p.b_swap ? n0 : bb, pb);
+              else tma_load_4d_pair_hint(sB, &tmB, leader_full, 0, k0, n0 / 64, bb, pb);
             } else {
-              if (p.a_swap == 2) {
+              if (!AMN) {
+                tma_load_3d_pair(sA, &tmA, leader_full, k0, p.a_swap ? ab : m0, p.a_swap ? m0 : ab);
+              } else if (p.a_swap == 2) {
                 tma_load_4d_pair(sA, &tmA, leader_full, 0, k0, m0 / 64, ab);
               } else {
 #pragma unroll
@@ -983,11 +1023,9 @@ __global__ void __launch_bounds__(pair_threads<EPI, TM>(), 1)
                   tma_load_3d_pair(sA + i * 8192, &tmA, leader_full, m0 + 64 * i, p.a_swap ? ab : k0,
                                    p.a_swap ? k0 : ab);
               }
-            }
-            if (!BMN) {
-              tma_load_3d_pair(sB, &tmB, leader_full, k0, p.b_swap ? bb : n0, p.b_swap ? n0 : bb);
-            } else {
-              if (p.b_swap == 2) {
+              if (!BMN) {
+                tma_load_3d_pair(sB, &tmB, leader_full, k0, p.b_swap ? bb : n0, p.b_swap ? n0 : bb);
+              } else if (p.b_swap == 2) {
                 tma_load_4d_pair(sB, &tmB, leader_full, 0, k0, n0 / 64, bb);
               } else {
 #pragma unroll
@@ -1581,6 +1619,11 @@ static int make_aux_map(CUtensorMap* m, const GemmSpec& s) {
 
 // TPFFN_RASTER=1 in the environment selects the shared-operand-fastest
 // orders for the per-shard GEMMs (for comparisons).
+static bool l2_hint_enabled() {
+  static const bool on = !getenv_flag_off("TPFFN_L2HINT");
+  return on;
+}
+
 static bool raster_by_sharing() {
   static const bool on = [] {
     const char* v = getenv("TPFFN_RASTER");
@@ -1713,6 +1756,15 @@ static int launch_pair(const GemmSpec& s, LaunchCtx& ctx) {
   Params p{};
   p.ksplit = s.ksplit;
   p.raster = RASTER_GROUPED;
+  // Weight-gradient GEMMs (both operands MN-major, K = tokens): the
+  // per-shard operand streams through L2 with evict_first priority, which
+  // keeps the one all shards share (x or dy, 67 MB for Llama-3-8B shapes)
+  // there across waves.  TPFFN_L2HINT=0 turns this off (for comparisons).
+  p.keep_op = 0;
+  if (AMN && BMN && s.NB > 1 && s.G == 1 && l2_hint_enabled()) {
+    if (s.A.bsel == 0 && s.B.bsel != 0) p.keep_op = 1;
+    if (s.B.bsel == 0 && s.A.bsel != 0) p.keep_op = 2;
+  }
   if (s.NB > 1 && s.G == 1 && raster_by_sharing()) {
     if (s.A.bsel == 0 && s.B.bsel != 0) p.raster = RASTER_M_FAST;
     if (s.B.bsel == 0 && s.A.bsel != 0) p.raster = RASTER_N_FAST;
@@ -1731,6 +1783,8 @@ static int launch_pair(const GemmSpec& s, LaunchCtx& ctx) {
   p.b_gsel = s.B.gsel;
   p.a_swap = sa;
   p.b_swap = sb;
+  // the cache-hinted copies use the 4-D maps of MN-major operands
+  if (p.keep_op && ((AMN && p.a_swap != 2) || (BMN && p.b_swap != 2))) p.keep_op = 0;
   p.out = s.out;
   p.out_bs = s.out_bs;
   p.out_rs = s.out_rs;
