@@ -373,6 +373,7 @@ __global__ void __launch_bounds__(threads_for<EPI>(), 1)
 #pragma unroll
       for (int s = 0; s < STAGES; ++s) last_issue_phase[s] = -1;
       bool ok = true;
+      const uint64_t pol_stream = l2_policy_evict_first();
       for (int unit = blockIdx.x; unit < num_tiles && ok; unit += gridDim.x) {
         int tile, kb0, k_iters;
         unit_split(p, unit, tile, kb0, k_iters);
@@ -405,7 +406,10 @@ __global__ void __launch_bounds__(threads_for<EPI>(), 1)
                   tma_load_3d(sA + i * 8192, &tmA, &full[stage], m0 + 64 * i, p.a_swap ? ab : k0,
                               p.a_swap ? k0 : ab);
             }
-            if (!BMN) {
+            if (!BMN && p.keep_op == 1) {
+              // weights read once (decode): evicted from L2 first
+              tma_load_3d_hint(sB, &tmB, &full[stage], k0, p.b_swap ? bb : n0, p.b_swap ? n0 : bb, pol_stream);
+            } else if (!BMN) {
               tma_load_3d(sB, &tmB, &full[stage], k0, p.b_swap ? bb : n0, p.b_swap ? n0 : bb);
             } else {
               if (p.b_swap == 2)
@@ -570,16 +574,6 @@ __device__ __forceinline__ void tma_load_3d_pair_hint(void* dst, const CUtensorM
       "[%0], [%1, {%2, %3, %4}], [%5], %6;" ::"r"(smem_u32(dst)),
       "l"(reinterpret_cast<uint64_t>(tm)), "r"(c0), "r"(c1), "r"(c2), "r"(leader_bar), "l"(policy)
       : "memory");
-}
-__device__ __forceinline__ uint64_t l2_policy_evict_normal() {
-  uint64_t pol;
-  asm volatile("createpolicy.fractional.L2::evict_normal.b64 %0, 1.0;" : "=l"(pol));
-  return pol;
-}
-__device__ __forceinline__ uint64_t l2_policy_evict_first() {
-  uint64_t pol;
-  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
-  return pol;
 }
 __device__ __forceinline__ void tmem_alloc_pair(uint32_t* slot, uint32_t ncols) {
   asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(slot)),
@@ -1516,6 +1510,11 @@ static int make_map(CUtensorMap* m, const Operand& op, int rows_box, int* swap) 
   return r == CUDA_SUCCESS ? 0 : TP_ERR_CUDA;
 }
 
+static bool l2_hint_enabled() {
+  static const bool on = !getenv_flag_off("TPFFN_L2HINT");
+  return on;
+}
+
 template <int BN, int STAGES, int EPI, bool AMN, bool BMN, int AR = BM>
 static int launch_inst(const GemmSpec& s, LaunchCtx& ctx) {
   using L = Layout<BN, STAGES, AR>;
@@ -1572,6 +1571,10 @@ static int launch_inst(const GemmSpec& s, LaunchCtx& ctx) {
   p.ksplit = s.ksplit;
   if (s.ksplit < 1 || (s.ksplit > 1 && (EPI != EPI_F32 || s.G != 1 || p.k_blocks < 2 * s.ksplit)))
     return TP_ERR_INVALID;
+  // Decode-sized GEMMs (32-row A tiles) stream their weights once: those
+  // copies go through L2 with evict_first priority, so that the small fp32
+  // parts and partials the next kernel reads stay there.
+  p.keep_op = (AR < BM && !BMN && l2_hint_enabled()) ? 1 : 0;
   const long long tiles = static_cast<long long>(p.tiles_m) * p.tiles_n * p.NB * s.ksplit;  // work units
   if (tiles <= 0 || p.k_blocks <= 0) return TP_ERR_INVALID;
   int grid = static_cast<int>(tiles < ctx.num_sms ? tiles : ctx.num_sms);
@@ -1619,11 +1622,6 @@ static int make_aux_map(CUtensorMap* m, const GemmSpec& s) {
 
 // TPFFN_RASTER=1 in the environment selects the shared-operand-fastest
 // orders for the per-shard GEMMs (for comparisons).
-static bool l2_hint_enabled() {
-  static const bool on = !getenv_flag_off("TPFFN_L2HINT");
-  return on;
-}
-
 static bool raster_by_sharing() {
   static const bool on = [] {
     const char* v = getenv("TPFFN_RASTER");
