@@ -354,8 +354,8 @@ def run_ours(args, ctx):
                 out_free[b].record(cs)
         st.wait_stream(cs)
 
-    k_e2e = max(3, args.steps // 2)
-    e2e_run(2)
+    k_e2e = max(20, args.steps // 2)  # at least ~0.1 s, so that one host hiccup does not dominate
+    e2e_run(3)
     torch.cuda.synchronize(dev)
     dist_barrier(ctx)
     e2, e3 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
