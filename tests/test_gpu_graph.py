@@ -6,8 +6,9 @@ graph.  Every call enqueues only stream work -- a memset of the workspace
 header and kernel launches, with programmatic dependent launches between
 them -- so the replay must give exactly the eager call's bits, also when
 replayed twice in a row, for the training shapes (both sum modes) and for a
-decode-sized SwiGLU forward whose up GEMM is split in two K parts (its
-per-tile part counters are zeroed by the captured memset).
+decode-sized SwiGLU forward whose up GEMM is split in two K parts, and for
+a backward whose weight-gradient GEMMs run in K parts with their ordered
+part sums and the merged bias column sums.
 """
 import pytest
 import torch
@@ -18,7 +19,8 @@ pytestmark = pytest.mark.gpu
 
 CASES = [small_case(333, 264, 600, 3, "swiglu", seed=801),
          small_case(300, 256, 768, 4, "gelu_tanh", bias=True, seed=802),
-         small_case(17, 2048, 3072, 3, "swiglu", seed=803, fwd_only=True)]
+         small_case(17, 2048, 3072, 3, "swiglu", seed=803, fwd_only=True),
+         small_case(2100, 256, 1024, 4, "gelu_tanh", bias=True, seed=804)]  # weight gradients in K parts
 
 
 def _bits(t):
