@@ -166,7 +166,10 @@ TPFFN_API size_t tp_ffn_saved_bytes(const tp_ffn_plan* plan, int64_t n_tokens);
  * needs for n_tokens tokens (one buffer of this size serves both).  It holds
  * the device error word (first 4 bytes), the hidden activations when nothing
  * is saved, the fp32 shard partials of the standalone sum, the backward's
- * hidden gradients and the bias-gradient reduction scratch. */
+ * hidden gradients, the fp32 K parts of split GEMMs (decode-sized SwiGLU up
+ * GEMMs; weight-gradient GEMMs of problems with few output tiles, decided
+ * from the current device's SM count) and the bias-gradient reduction
+ * scratch.  Query it on the device that will run the calls. */
 TPFFN_API size_t tp_ffn_workspace_bytes(const tp_ffn_plan* plan, int64_t n_tokens, int flags);
 
 /* ---------------------------------------------------------------- packing */
