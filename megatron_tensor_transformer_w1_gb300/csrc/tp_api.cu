@@ -146,6 +146,14 @@ int choose_ksplit(const tp_ffn_plan* p, int64_t n, int num_sms) {
 // busiest SM pair's K loop (waves of units x K blocks per unit) by more than
 // a tenth, each part keeping at least 16 K blocks of 64 tokens.
 constexpr int kMaxWgradKsplit = 4;
+// TPFFN_MERGE_SHARDS=0: the W_O backward GEMMs run per shard (for comparisons)
+bool merge_shards_enabled() {
+  static const bool on = [] {
+    const char* v = getenv("TPFFN_MERGE_SHARDS");
+    return !(v && v[0] == '0');
+  }();
+  return on;
+}
 int wgrad_ksplit(const tp_ffn_plan* p, int64_t n, int64_t M, int64_t N, int num_sms) {
   static const bool off = [] {
     const char* v = getenv("TPFFN_WGRAD_KSPLIT");
@@ -659,6 +667,42 @@ static int validate_bwd(const tp_ffn_plan* p, int64_t n, const void* x, const vo
   return TP_OK;
 }
 
+// The backward GEMMs of the row-sharded projection without activation (W_O)
+// have N = s per shard; with s = 384 (the 8.3B block's three heads) each
+// shard's second 256-column tile is half empty.  Run as one GEMM over all
+// shards' columns (N = T_p s) where the tensor-core pair kernel takes it:
+// dc = dy W_O reads shard n / s's B columns (dgrad, `b_side`), dW_O writes
+// shard n / s's packed block (wgrad).  Otherwise, or when the kernel
+// declines, the per-shard GEMM g runs.  Measured on GB300: dW_O merged is
+// faster for s = 384 and 512 (8.3B 932 -> 1451, Llama-3-8B 1258 -> 1357
+// TFLOP/s); dc merged only where it removes half-empty tiles (s = 384: 1196
+// -> 1235; s = 512: 1606 -> 1457, so s a multiple of 256 stays per shard).
+static int run_merged_or_sharded(const tp_ffn_plan* p, const GemmSpec& g, LaunchCtx& ctx, bool b_side) {
+  const int64_t T = p->T_p, s = p->s;
+  if (p->dtype == TP_BF16 && T > 1 && s % 128 == 0 && (!b_side || s % 256 != 0) && p->d_ff == T * s &&
+      merge_shards_enabled()) {
+    GemmSpec m = g;
+    m.N = T * s;
+    m.NB = 1;
+    m.n_store = T * s;
+    if (b_side) {  // dgrad: B = the packed W_O shards, output columns already global
+      m.B.bsel = 0;
+      m.b_cs = s;
+      m.out_bs = 0;
+    } else {  // wgrad: B = all heads' columns of c, output to the packed shards
+      m.B = g.B;
+      m.B.inner = T * s;
+      m.B.batch = 1;
+      m.B.batch_stride = g.B.row_stride * g.B.rows;
+      m.B.bsel = 0;
+      m.out_cs = s;
+    }
+    const int rc = run_gemm(p, m, ctx);
+    if (rc != TP_ERR_UNSUPPORTED) return rc;
+  }
+  return run_gemm(p, g, ctx);
+}
+
 // A weight-gradient GEMM g (bf16 out, dense [NB][M][N] planes): as it stands,
 // or split along K into fp32 parts in the workspace and summed in part order.
 static int run_wgrad(const tp_ffn_plan* p, const GemmSpec& g, int64_t n, const WsLayout& L, char* ws,
@@ -710,7 +754,7 @@ static int bwd_impl(const tp_ffn_plan* p, int64_t n, const void* x, const void* 
     g.out_rs = p->d_ff;
     g.n_store = s;
     g.out_bf16 = out_bf16;
-    rc = run_gemm(p, g, ctx);
+    rc = run_merged_or_sharded(p, g, ctx, true);
     if (!rc && sc) rc = launch_scatter_rows(dx, n, p->d_ff, out_bf16 ? 2 : 4, *sc, ctx, "scatter_dx");
     if (rc) return rc;
     // dW_O^(t) = dy^T c^(t)
@@ -728,7 +772,7 @@ static int bwd_impl(const tp_ffn_plan* p, int64_t n, const void* x, const void* 
     w.out_rs = sp;
     w.n_store = s;
     w.out_bf16 = out_bf16;
-    rc = run_gemm(p, w, ctx);
+    rc = run_merged_or_sharded(p, w, ctx, false);
     if (!rc && db2) {
       ColsumJobs J;
       J.j[J.n++] = colsum_job(dy, out_bf16, 1, n, d, d, n * d, db2, out_bf16, 0, cs_scratch, n);

@@ -86,6 +86,7 @@ struct Params {
   int ksplit;    // K split into this many parts (1: none; fp32 parts only)
   int raster;    // pair kernel tile order (RASTER_*)
   int o_swap;    // pair kernel TMA stores: output maps are {cols, batch, rows} (batch stride < row stride)
+  int out_cs, b_cs;  // pair kernel: shards merged along N (see GemmSpec), 0: off
   int keep_op;   // pair kernel: operand every batch shares (1: A, 2: B, 0: none); the other one
                  // streams through L2 with evict_first priority
 };
@@ -859,6 +860,9 @@ __device__ __forceinline__ void epilogue_tile_tma(const Params& p, const CUtenso
         if (row0 >= p.M) {
           // every row of this warp lies past M: nothing to store (an empty
           // group keeps the buffer accounting)
+        } else if (p.out_cs) {  // shards merged along N: column nc of shard nc / out_cs
+          const int sb = nc / p.out_cs;
+          tma_store_3d(tmO, src, nc - sb * p.out_cs, row0, sb);
         } else if (!p.o_swap) {
           tma_store_3d(tmO, src, nc, row0, b);
           if (EPI == EPI_GELU_FWD && p.out2) tma_store_3d(tmO2, src + 2048, nc, row0, b);
@@ -1019,6 +1023,9 @@ __global__ void __launch_bounds__(pair_threads<EPI, TM>(), 1)
               }
               if (!BMN) {
                 tma_load_3d_pair(sB, &tmB, leader_full, k0, p.b_swap ? bb : n0, p.b_swap ? n0 : bb);
+              } else if (p.b_cs) {  // shards merged along N: B columns of shard n0 / b_cs
+                const int sbb = n0 / p.b_cs;
+                tma_load_4d_pair(sB, &tmB, leader_full, 0, k0, (n0 - sbb * p.b_cs) / 64, sbb);
               } else if (p.b_swap == 2) {
                 tma_load_4d_pair(sB, &tmB, leader_full, 0, k0, n0 / 64, bb);
               } else {
@@ -1751,8 +1758,17 @@ static int launch_pair(const GemmSpec& s, LaunchCtx& ctx) {
   // a K split writes fp32 parts (EPI_F32) and needs at least one K block per part
   if (s.ksplit < 1 || (s.ksplit > 1 && (EPI != EPI_F32 || s.G * ((s.K + BK - 1) / BK) < 2 * s.ksplit)))
     return TP_ERR_INVALID;
+  if (s.out_cs || s.b_cs) {
+    // shards merged along N: plain output epilogues, one batch, TMA stores
+    const bool ok = EPI == EPI_OUT && s.NB == 1 && s.G == 1 && s.ksplit == 1 && !s.bias && tma_store_enabled() &&
+                    (s.out_cs == 0 || (s.out_cs % 128 == 0 && s.N % s.out_cs == 0 && s.n_store == s.N)) &&
+                    (s.b_cs == 0 || (BMN && s.b_cs % 128 == 0));
+    if (!ok) return TP_ERR_UNSUPPORTED;
+  }
   Params p{};
   p.ksplit = s.ksplit;
+  p.out_cs = static_cast<int>(s.out_cs);
+  p.b_cs = static_cast<int>(s.b_cs);
   p.raster = RASTER_GROUPED;
   // Weight-gradient GEMMs (both operands MN-major, K = tokens): the
   // per-shard operand streams through L2 with evict_first priority, which
@@ -1783,6 +1799,7 @@ static int launch_pair(const GemmSpec& s, LaunchCtx& ctx) {
   p.b_swap = sb;
   // the cache-hinted copies use the 4-D maps of MN-major operands
   if (p.keep_op && ((AMN && p.a_swap != 2) || (BMN && p.b_swap != 2))) p.keep_op = 0;
+  if (p.b_cs && p.b_swap != 2) return TP_ERR_UNSUPPORTED;  // merged shards read B through its 4-D map
   p.out = s.out;
   p.out_bs = s.out_bs;
   p.out_rs = s.out_rs;
@@ -1821,13 +1838,16 @@ static int launch_pair(const GemmSpec& s, LaunchCtx& ctx) {
       // stores of the plain epilogue
       const bool f32 = EPI == EPI_F32;
       int sw1 = 0, sw2 = 0;
-      const int64_t nb = (s.NB > 1 ? s.NB : 1) * s.ksplit;  // the K parts are further batches
-      const int64_t cols1 = EPI == EPI_SWIGLU_FWD ? s.out_rs : s.n_store;
+      // the K parts, or the shards merged along N, are further batches
+      const int64_t nb = s.out_cs ? s.N / s.out_cs : (s.NB > 1 ? s.NB : 1) * s.ksplit;
+      const int64_t cols1 = EPI == EPI_SWIGLU_FWD ? s.out_rs : (s.out_cs ? s.out_cs : s.n_store);
       bool ok = make_out_map(&to, s.out, f32, cols1, s.M, nb, s.out_rs, s.out_bs, &sw1) == 0;
       if (ok && s.out2) {
         const int64_t cols2 = EPI == EPI_SWIGLU_FWD ? s.out2_rs : s.n_store;
         ok = make_out_map(&to2, s.out2, false, cols2, s.M, nb, s.out2_rs, s.out2_bs, &sw2) == 0 && sw2 == sw1;
       }
+      if (ok && s.out_cs && sw1) ok = false;  // merged shards store {cols, rows, shard} boxes
+      if (!ok && s.out_cs) return TP_ERR_UNSUPPORTED;
       if (ok) {
         p.o_swap = sw1;
         // forward epilogues of short K loops (GPT-2-sized widths): eight
@@ -1873,6 +1893,7 @@ int launch_tc_gemm(const GemmSpec& s, LaunchCtx& ctx) {
   using namespace tc;
   const bool amn = s.A.mn_major != 0, bmn = s.B.mn_major != 0;
   if (s.n_store % 8) return TP_ERR_UNSUPPORTED;
+  if ((s.out_cs || s.b_cs) && !(s.M >= 256 && pair_path_enabled())) return TP_ERR_UNSUPPORTED;
   if (s.M >= 256 && pair_path_enabled()) {
     switch (s.epi) {
       case EPI_SWIGLU_FWD:

@@ -52,6 +52,12 @@ struct GemmSpec {
   // K split (EPI_F32 only): part k of the K blocks is accumulated on its own
   // and written as fp32 batch k * NB + b of `out` (one-SM kernel: G = 1)
   int ksplit = 1;
+  // Shards merged along N (pair kernel, NB = 1, TMA-store epilogue only;
+  // TP_ERR_UNSUPPORTED otherwise): out_cs > 0 writes output column n to
+  // batch n / out_cs, column n % out_cs of `out` (out_bs apart); b_cs > 0
+  // reads B's column n from batch n / b_cs, column n % b_cs of B's own batch
+  // layout.  Both sizes are multiples of 128.
+  int64_t out_cs = 0, b_cs = 0;
 };
 
 // Launch context of one API call.
