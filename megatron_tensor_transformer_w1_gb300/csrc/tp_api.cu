@@ -772,6 +772,7 @@ static int bwd_impl(const tp_ffn_plan* p, int64_t n, const void* x, const void* 
     w.out_rs = sp;
     w.n_store = s;
     w.out_bf16 = out_bf16;
+    w.no_dep_wait = 1;  // reads dy and c, writes dW_O: nothing the dc GEMM before it touches
     rc = run_merged_or_sharded(p, w, ctx, false);
     if (!rc && db2) {
       ColsumJobs J;
@@ -860,6 +861,9 @@ static int bwd_impl(const tp_ffn_plan* p, int64_t n, const void* x, const void* 
     g.N = sp;
     g.K = n;
     g.NB = static_cast<int>(T);
+    // reads dy and the saved h, writes dW2 (or its K parts): nothing the dx
+    // GEMM or sum before it touches, so it starts in that kernel's tail
+    g.no_dep_wait = 1;
     g.A = mnmajor(dy, d, n, 1, d, n * d, 0, 0);
     g.B = mnmajor(hsaved, sp, n, T, sp, n * sp, 1, 0);
     g.epi = EPI_OUT;

@@ -87,6 +87,9 @@ struct Params {
   int raster;    // pair kernel tile order (RASTER_*)
   int o_swap;    // pair kernel TMA stores: output maps are {cols, batch, rows} (batch stride < row stride)
   int out_cs, b_cs;  // pair kernel: shards merged along N (see GemmSpec), 0: off
+  int dep_mode;  // programmatic dependent launch: 1 wait for the previous kernel, then let the next
+                 // one launch; 2 no wait at the start (reads nothing the previous kernel writes),
+                 // wait before exit; 0 let the next one launch, then wait (for comparisons)
   int keep_op;   // pair kernel: operand every batch shares (1: A, 2: B, 0: none); the other one
                  // streams through L2 with evict_first priority
 };
@@ -99,6 +102,29 @@ struct Params {
 // less (up 1.23 -> 2.12 GB, dh 1.71 -> 2.44 GB: the shared operand does not
 // survive a wave in L2) and were slower for up and dh (1648 -> 1598,
 // 1448 -> 1338 TFLOP/s), so they are opt-in (TPFFN_RASTER=1) for comparisons.
+// Programmatic dependent launch.  Mode 1 (default): wait until the previous
+// kernel has completed and its writes are visible, then let the next kernel
+// launch -- so that whenever a kernel starts, every kernel before its
+// predecessor has completed.  Mode 2, for a GEMM that neither reads nor
+// writes anything its predecessor touches (a weight gradient after the dx
+// GEMM): no wait at the start, so its CTAs fill the SMs the predecessor's
+// last wave leaves idle; one thread per CTA waits before the CTA exits, so
+// that its completion still implies its predecessor's, and its successor (a
+// waiting kernel) launches only when it completes.  Mode 0: the former order
+// (next kernel first, then wait), for comparisons.
+__device__ __forceinline__ void dep_prologue(int mode) {
+  if (mode == 1) {
+    grid_dep_wait();
+    grid_dep_launch();
+  } else if (mode == 0) {
+    grid_dep_launch();
+    grid_dep_wait();
+  }
+}
+__device__ __forceinline__ void dep_epilogue(int mode) {
+  if (mode == 2 && threadIdx.x == 0) grid_dep_wait();
+}
+
 constexpr int RASTER_GROUPED = 0;  // groups of 8 M blocks, N within a group
 constexpr int RASTER_M_FAST = 1;   // A shared by every batch: all M blocks of one N block in turn
 constexpr int RASTER_N_FAST = 2;   // B shared by every batch: all N blocks of one M block in turn
@@ -359,8 +385,7 @@ __global__ void __launch_bounds__(threads_for<EPI>(), 1)
   // launched as a programmatic dependent of the previous kernel (decode-sized
   // GEMMs): everything above overlapped its tail; no global memory is touched
   // before its results are visible
-  grid_dep_launch();
-  grid_dep_wait();
+  dep_prologue(p.dep_mode);
 
   const int num_tiles = p.tiles_m * p.tiles_n * p.NB * p.ksplit;  // work units
   const int k_iters_all = p.G * p.k_blocks;
@@ -509,6 +534,7 @@ __global__ void __launch_bounds__(threads_for<EPI>(), 1)
     tc_fence_after();
     tmem_dealloc(tmem_base, L::TMEM_COLS);
   }
+  dep_epilogue(p.dep_mode);
 }
 
 // ------------------------------------------------------------ 2-SM pair kernel
@@ -950,9 +976,8 @@ __global__ void __launch_bounds__(pair_threads<EPI, TM>(), 1)
   const uint32_t tmem_base = *tmem_slot;
   // a programmatic dependent of the previous kernel: the set-up above
   // overlapped its tail; no global memory is touched before its results are
-  // visible
-  grid_dep_launch();
-  grid_dep_wait();
+  // visible (dep_mode 2: nothing this GEMM reads or writes is touched by it)
+  dep_prologue(p.dep_mode);
 
   const int tiles_m2 = (p.tiles_m + 1) >> 1;
   const int num_tiles = tiles_m2 * p.tiles_n * p.NB;
@@ -1418,6 +1443,7 @@ __global__ void __launch_bounds__(pair_threads<EPI, TM>(), 1)
     tc_fence_after();
     tmem_dealloc_pair(tmem_base, L::TMEM_COLS);
   }
+  dep_epilogue(p.dep_mode);
 }
 
 // ------------------------------------------------------------ host side
@@ -1517,6 +1543,15 @@ static int make_map(CUtensorMap* m, const Operand& op, int rows_box, int* swap) 
   return r == CUDA_SUCCESS ? 0 : TP_ERR_CUDA;
 }
 
+// TPFFN_PDL_OLD=1: the former dependent-launch order; TPFFN_NO_DEP_OVERLAP=1:
+// GEMMs marked independent of their predecessor wait for it all the same
+static int dep_mode_for(const GemmSpec& s) {
+  static const bool old_order = getenv("TPFFN_PDL_OLD") != nullptr;
+  static const bool no_overlap = getenv("TPFFN_NO_DEP_OVERLAP") != nullptr;
+  if (old_order) return 0;
+  return (s.no_dep_wait && !no_overlap) ? 2 : 1;
+}
+
 static bool l2_hint_enabled() {
   static const bool on = !getenv_flag_off("TPFFN_L2HINT");
   return on;
@@ -1578,6 +1613,7 @@ static int launch_inst(const GemmSpec& s, LaunchCtx& ctx) {
   p.ksplit = s.ksplit;
   if (s.ksplit < 1 || (s.ksplit > 1 && (EPI != EPI_F32 || s.G != 1 || p.k_blocks < 2 * s.ksplit)))
     return TP_ERR_INVALID;
+  p.dep_mode = dep_mode_for(s);
   // Decode-sized GEMMs (32-row A tiles) stream their weights once: those
   // copies go through L2 with evict_first priority, so that the small fp32
   // parts and partials the next kernel reads stay there.
@@ -1767,6 +1803,7 @@ static int launch_pair(const GemmSpec& s, LaunchCtx& ctx) {
   }
   Params p{};
   p.ksplit = s.ksplit;
+  p.dep_mode = dep_mode_for(s);
   p.out_cs = static_cast<int>(s.out_cs);
   p.b_cs = static_cast<int>(s.b_cs);
   p.raster = RASTER_GROUPED;

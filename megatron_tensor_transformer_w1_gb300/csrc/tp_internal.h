@@ -58,6 +58,10 @@ struct GemmSpec {
   // reads B's column n from batch n / b_cs, column n % b_cs of B's own batch
   // layout.  Both sizes are multiples of 128.
   int64_t out_cs = 0, b_cs = 0;
+  // The GEMM neither reads nor writes any buffer the kernel launched before it
+  // on the stream touches: it starts without waiting for that kernel (which
+  // must itself have waited for its own predecessor) and waits before exit.
+  int no_dep_wait = 0;
 };
 
 // Launch context of one API call.
