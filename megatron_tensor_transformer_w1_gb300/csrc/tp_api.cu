@@ -716,6 +716,7 @@ static int run_wgrad(const tp_ffn_plan* p, const GemmSpec& g, int64_t n, const W
   GemmSpec k = g;
   k.epi = EPI_F32;
   k.ksplit = ks;
+  k.no_dep_wait = 0;  // small problems: starting in the previous kernel's tail measured slower
   k.out = parts;
   k.out_bs = g.M * g.N;
   k.out_rs = g.N;
@@ -878,6 +879,9 @@ static int bwd_impl(const tp_ffn_plan* p, int64_t n, const void* x, const void* 
   {
     GemmSpec g;
     g.name = p->act == TP_ACT_SWIGLU ? "wgrad_w13" : "wgrad_w1";
+    // reads D (written before the dx GEMM) and x, writes dW1|dW3: nothing
+    // dW2's GEMM or its part sum writes; starts in their tail
+    g.no_dep_wait = 1;
     g.M = W;
     g.N = d;
     g.K = n;

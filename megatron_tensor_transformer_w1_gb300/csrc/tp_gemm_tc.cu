@@ -102,23 +102,25 @@ struct Params {
 // less (up 1.23 -> 2.12 GB, dh 1.71 -> 2.44 GB: the shared operand does not
 // survive a wave in L2) and were slower for up and dh (1648 -> 1598,
 // 1448 -> 1338 TFLOP/s), so they are opt-in (TPFFN_RASTER=1) for comparisons.
-// Programmatic dependent launch.  Mode 1 (default): wait until the previous
-// kernel has completed and its writes are visible, then let the next kernel
-// launch -- so that whenever a kernel starts, every kernel before its
-// predecessor has completed.  Mode 2, for a GEMM that neither reads nor
-// writes anything its predecessor touches (a weight gradient after the dx
-// GEMM): no wait at the start, so its CTAs fill the SMs the predecessor's
-// last wave leaves idle; one thread per CTA waits before the CTA exits, so
-// that its completion still implies its predecessor's, and its successor (a
-// waiting kernel) launches only when it completes.  Mode 0: the former order
-// (next kernel first, then wait), for comparisons.
+// Programmatic dependent launch.  A dependent grid launches once every CTA
+// of this grid has called launch_dependents (or exited).  Mode 1 (default):
+// wait until the previous kernel has completed and its writes are visible,
+// then let the next kernel launch -- so that whenever a kernel starts, every
+// kernel before its predecessor has completed.  Mode 2, for a GEMM that
+// neither reads nor writes anything written by its predecessor or by
+// another mode-2 GEMM right before it (the weight gradients after the dx
+// GEMM): let the next kernel launch and start without waiting, so that its
+// CTAs fill the SMs the predecessor's last wave leaves idle; one thread per
+// CTA waits before the CTA exits, so that its completion still implies its
+// predecessor's.  Mode 0: the former order (next kernel first, then wait),
+// for comparisons.
 __device__ __forceinline__ void dep_prologue(int mode) {
   if (mode == 1) {
     grid_dep_wait();
     grid_dep_launch();
-  } else if (mode == 0) {
+  } else {
     grid_dep_launch();
-    grid_dep_wait();
+    if (mode == 0) grid_dep_wait();
   }
 }
 __device__ __forceinline__ void dep_epilogue(int mode) {

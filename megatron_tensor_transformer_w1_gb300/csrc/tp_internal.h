@@ -58,9 +58,11 @@ struct GemmSpec {
   // reads B's column n from batch n / b_cs, column n % b_cs of B's own batch
   // layout.  Both sizes are multiples of 128.
   int64_t out_cs = 0, b_cs = 0;
-  // The GEMM neither reads nor writes any buffer the kernel launched before it
-  // on the stream touches: it starts without waiting for that kernel (which
-  // must itself have waited for its own predecessor) and waits before exit.
+  // The GEMM neither reads nor writes any buffer that the kernel launched
+  // before it on the stream writes (nor one that a no_dep_wait GEMM right
+  // before it writes): it lets its successor launch and starts without
+  // waiting (the kernel before it must have waited for its own
+  // predecessor), and waits before exit.
   int no_dep_wait = 0;
 };
 
