@@ -778,6 +778,7 @@ static int bwd_impl(const tp_ffn_plan* p, int64_t n, const void* x, const void* 
     if (!rc && db2) {
       ColsumJobs J;
       J.j[J.n++] = colsum_job(dy, out_bf16, 1, n, d, d, n * d, db2, out_bf16, 0, cs_scratch, n);
+      J.no_dep_wait = 1;  // dy: nothing the dW_O GEMM before it writes
       rc = launch_colsums(J, ctx, "colsum_db2");
     }
     return rc;
@@ -903,6 +904,7 @@ static int bwd_impl(const tp_ffn_plan* p, int64_t n, const void* x, const void* 
   if (db2)
     J.j[J.n++] = colsum_job(dy, out_bf16, 1, n, d, d, n * d, db2, out_bf16, 0,
                             cs_scratch + (db1 ? colsum_scratch_floats(T, n, sp, colsum_chunk(n)) : 0), n);
+  J.no_dep_wait = 1;  // D and dy: nothing the weight-gradient kernels before it write
   if (J.n) rc = launch_colsums(J, ctx, db1 && db2 ? "colsum_db" : db1 ? "colsum_db1" : "colsum_db2");
   return rc;
 }

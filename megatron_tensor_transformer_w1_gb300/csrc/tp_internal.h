@@ -138,6 +138,10 @@ struct ColsumJob {
 struct ColsumJobs {
   ColsumJob j[2];
   int n = 0;
+  // the inputs are written by nothing the kernel before it writes: pass 1
+  // starts without waiting for that kernel and waits before exit (see the
+  // GEMMs' no_dep_wait)
+  int no_dep_wait = 0;
 };
 int launch_colsums(ColsumJobs jobs, LaunchCtx& ctx, const char* name);
 int64_t colsum_scratch_floats(int64_t batch, int64_t rows, int64_t cols, int64_t chunk_rows);

@@ -12,6 +12,7 @@
 //                    kernel, for fp32 plans (TF32 would not meet fp32
 //                    accuracy, so these use plain FMA)
 #include <climits>
+#include <cstdlib>
 
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
@@ -108,8 +109,10 @@ template <int OUT_BF16>
 __global__ void __launch_bounds__(256) shard_sum_vec8_kernel(const float* __restrict__ P, int T, long long plane,
                                                              long long cols, const __nv_bfloat16* bias_bf,
                                                              const float* bias_f, void* out, long long stride) {
-  // a programmatic dependent of the GEMM that wrote the partials
+  // a programmatic dependent of the GEMM that wrote the partials; once they
+  // are visible, the next kernel may launch
   asm volatile("griddepcontrol.wait;" ::: "memory");
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   const long long n8 = plane / 8;
   for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < n8; i += (long long)gridDim.x * blockDim.x) {
     const float4* p0 = reinterpret_cast<const float4*>(P) + 2 * i;
@@ -265,8 +268,9 @@ __device__ __forceinline__ int colsum_pick(const ColsumJobs& J, int& local, bool
 
 __global__ void __launch_bounds__(256) colsum_pass1_kernel(const ColsumJobs J) {
   __shared__ float part[8][256 + 4];
-  // a programmatic dependent of the kernel that wrote the inputs
-  asm volatile("griddepcontrol.wait;" ::: "memory");
+  // a programmatic dependent of the kernel that wrote the inputs (or, with
+  // no_dep_wait, of one that wrote none of them: it waits before exit)
+  if (!J.no_dep_wait) asm volatile("griddepcontrol.wait;" ::: "memory");
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   int local = static_cast<int>(blockIdx.x);
   const ColsumJob& q = J.j[colsum_pick(J, local, false)];
@@ -301,6 +305,7 @@ __global__ void __launch_bounds__(256) colsum_pass1_kernel(const ColsumJobs J) {
 #pragma unroll
   for (int j = 0; j < 8; ++j) part[lane][cg * 8 + j] = acc[j];
   __syncthreads();
+  if (J.no_dep_wait && threadIdx.x == 0) asm volatile("griddepcontrol.wait;" ::: "memory");
   const long long col = cb * 256 + threadIdx.x;
   if (col >= q.cols) return;
   float sum = 0.f;
@@ -682,6 +687,8 @@ int64_t colsum_scratch_floats(int64_t batch, int64_t rows, int64_t cols, int64_t
 }
 
 int launch_colsums(ColsumJobs J, LaunchCtx& ctx, const char* name) {
+  static const bool no_overlap = getenv("TPFFN_NO_DEP_OVERLAP") != nullptr;  // for comparisons
+  if (no_overlap) J.no_dep_wait = 0;
   long long g1 = 0, g2 = 0;
   int kept = 0;
   for (int i = 0; i < J.n; ++i) {
