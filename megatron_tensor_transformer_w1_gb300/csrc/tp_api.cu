@@ -259,7 +259,13 @@ int make_ctx(const tp_ffn_plan* p, void* workspace, int flags, cudaStream_t stre
     ctx.after = timing_after;
     ctx.user = const_cast<tp_ffn_plan*>(p);
   }
-  if (cudaMemsetAsync(workspace, 0, sizeof(int), stream) != cudaSuccess) return TP_ERR_CUDA;
+  static const bool memset_reset = getenv("TPFFN_MEMSET") != nullptr;  // for comparisons
+  if (memset_reset) {
+    if (cudaMemsetAsync(workspace, 0, sizeof(int), stream) != cudaSuccess) return TP_ERR_CUDA;
+  } else {
+    if (launch_reset_error_word(ctx.err, stream)) return TP_ERR_CUDA;
+    ctx.launches++;
+  }
   return TP_OK;
 }
 

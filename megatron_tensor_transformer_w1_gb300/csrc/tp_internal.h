@@ -144,6 +144,8 @@ struct ColsumJobs {
   int no_dep_wait = 0;
 };
 int launch_colsums(ColsumJobs jobs, LaunchCtx& ctx, const char* name);
+// Clears the device error word at the start of a call (one tiny kernel).
+int launch_reset_error_word(int* err, cudaStream_t stream);
 int64_t colsum_scratch_floats(int64_t batch, int64_t rows, int64_t cols, int64_t chunk_rows);
 
 // Attention core of the head-sharded attention sublayer (tp_attention.cu).

@@ -686,6 +686,21 @@ int64_t colsum_scratch_floats(int64_t batch, int64_t rows, int64_t cols, int64_t
   return batch * (chunks > 0 ? chunks : 1) * cols;
 }
 
+// The call's device error word cleared at its start, as a programmatic
+// dependent: the call's first kernel may launch at once (its set-up overlaps
+// the previous kernel on the stream), and the word is written only after
+// every kernel before this one has completed.
+__global__ void reset_error_word_kernel(int* err) {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  if (threadIdx.x == 0) *err = 0;
+}
+
+int launch_reset_error_word(int* err, cudaStream_t stream) {
+  launch_pdl(reset_error_word_kernel, dim3(1), 32, stream, err);
+  return cudaPeekAtLastError() == cudaSuccess ? 0 : TP_ERR_CUDA;
+}
+
 int launch_colsums(ColsumJobs J, LaunchCtx& ctx, const char* name) {
   static const bool no_overlap = getenv("TPFFN_NO_DEP_OVERLAP") != nullptr;  // for comparisons
   if (no_overlap) J.no_dep_wait = 0;

@@ -66,7 +66,7 @@ def _reference(name):
 def test_full_size_sampled(name, fused):
     w, inp, ref = _reference(name)
     out, n_fwd = run_gpu_tensors(w, inp, fused=fused, backward=not w.fwd_only)
-    assert n_fwd >= 1
+    assert n_fwd >= 2  # the error-word reset and the compute kernels
     rows, js, ks, cs = (torch.as_tensor(ref[k]).cuda() for k in ("rows", "js", "ks", "cs"))
     get = lambda t: t.to(torch.float64).cpu().numpy()
     A, W = ref["A"], ref["W"]
