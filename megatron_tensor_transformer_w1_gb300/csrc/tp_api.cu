@@ -1338,6 +1338,9 @@ int tp_attn_bwd(const tp_attn_plan* a, int64_t B, int64_t S, const void* x, cons
     g.M = W;
     g.N = d;
     g.K = n;
+    // reads dqkv (written before the dx GEMM) and x, writes dWqkv: nothing
+    // the dx GEMM or sum before it writes; starts in its tail
+    g.no_dep_wait = 1;
     g.A = mnmajor(ws + L.dqkv, W, n, 1, W, n * W, 0, 0);
     g.B = mnmajor(x, d, n, 1, d, n * d, 0, 0);
     g.epi = EPI_OUT;
