@@ -107,8 +107,8 @@ ColsumJob colsum_job(const void* in, int in_bf16, int64_t batch, int64_t rows, i
 }
 
 struct WsLayout {
-  size_t h = 0, part = 0, D = 0, cs = 0, ks = 0, wk = 0, total = 0;
-  bool has_part = false, has_ks = false, has_wk = false;
+  size_t h = 0, part = 0, D = 0, cs = 0, ks = 0, wk = 0, tail = 0, tail_bytes = 0, total = 0;
+  bool has_part = false, has_ks = false, has_wk = false, has_tail = false;
 };
 
 // Decode-sized SwiGLU forwards (at most 32 tokens: one 32-row A tile) may
@@ -205,6 +205,14 @@ WsLayout ws_layout(const tp_ffn_plan* p, int64_t n, int flags) {
       L.wk = off;
       off += align_up(wk);
     }
+  }
+  if ((flags & TP_SUM_FUSED) && p->dtype == TP_BF16 && tc_pair_path(n)) {
+    // fp32 K parts of a fused-sum GEMM's last-wave tiles: at most one
+    // 256 x 256 block per SM pair
+    L.has_tail = true;
+    L.tail = off;
+    L.tail_bytes = static_cast<size_t>(num_sms_current() / 2) * 256 * 256 * 4;
+    off += align_up(L.tail_bytes);
   }
   L.cs = off;
   const int64_t cs1 = colsum_scratch_floats(p->T_p, n, p->s_pad, colsum_chunk(n));
@@ -611,6 +619,10 @@ static int fwd_impl(const tp_ffn_plan* p, int64_t n, const void* x, const void* 
     g.bias = b2;
     g.bias_bs = 0;
     g.bias_len = d;
+    if (L.has_tail) {
+      g.tail_ws = reinterpret_cast<float*>(ws + L.tail);
+      g.tail_ws_bytes = L.tail_bytes;
+    }
     rc = run_gemm(p, g, ctx);
     if (!rc && sc) rc = launch_scatter_rows(y, n, d, out_bf16 ? 2 : 4, *sc, ctx, "scatter_y");
   } else {
@@ -1243,6 +1255,14 @@ int tp_attn_fwd(const tp_attn_plan* a, int64_t B, int64_t S, const void* x, cons
   g.out_rs = a->W;
   g.n_store = a->W;
   g.out_bf16 = 1;
+  {
+    // the W_O forward's last-wave region is free until that GEMM runs
+    const WsLayout WL = ws_layout(a->wo, n, flags);
+    if (WL.has_tail) {
+      g.tail_ws = reinterpret_cast<float*>(ws + L.wo + WL.tail);
+      g.tail_ws_bytes = WL.tail_bytes;
+    }
+  }
   rc = run_gemm(a->wo, g, ctx);
   if (!rc) {
     AttnSpec sp = attn_spec(a, B, S);

@@ -87,6 +87,7 @@ struct Params {
   int raster;    // pair kernel tile order (RASTER_*)
   int o_swap;    // pair kernel TMA stores: output maps are {cols, batch, rows} (batch stride < row stride)
   int out_cs, b_cs;  // pair kernel: shards merged along N (see GemmSpec), 0: off
+  int tail_tiles, tail_parts;  // pair kernel: the last tail_tiles tiles run as tail_parts K parts (0: off)
   int dep_mode;  // programmatic dependent launch: 1 wait for the previous kernel, then let the next
                  // one launch; 2 no wait at the start (reads nothing the previous kernel writes),
                  // wait before exit; 0 let the next one launch, then wait (for comparisons)
@@ -725,7 +726,7 @@ __device__ __forceinline__ uint4 lds128(uint32_t addr) {
 
 // Pair tile order (RASTER_*), over 256-row M blocks; the batch (shard) is
 // the outermost coordinate in every order.
-__device__ __forceinline__ void decode_pair_tile(const Params& p, int tile, int& b, int& mp, int& nb) {
+__host__ __device__ __forceinline__ void decode_pair_tile(const Params& p, int tile, int& b, int& mp, int& nb) {
   const int tiles_m2 = (p.tiles_m + 1) >> 1;
   const int tpb = tiles_m2 * p.tiles_n;
   b = tile / tpb;
@@ -745,7 +746,7 @@ __device__ __forceinline__ void decode_pair_tile(const Params& p, int tile, int&
   constexpr int GM = 8;
   const int group = r / (GM * p.tiles_n);
   const int first_m = group * GM;
-  const int gm = min(tiles_m2 - first_m, GM);
+  const int gm = tiles_m2 - first_m < GM ? tiles_m2 - first_m : GM;
   const int in_group = r - group * GM * p.tiles_n;
   mp = first_m + in_group % gm;
   nb = in_group / gm;
@@ -905,10 +906,62 @@ __device__ __forceinline__ void epilogue_tile_tma(const Params& p, const CUtenso
   }
 }
 
+// Epilogue of a last-wave K part: the warp's 32 rows (tile row r_local on)
+// of the tile's fp32 sum over its K part, stored as 32 x 32 boxes at (column
+// within the tile, row within the tile, tb) of the {256, 256, parts x tail
+// tiles} fp32 map.  Same staging buffers and bulk-group count as
+// epilogue_tile_tma.
+template <int NSPLIT>
+__device__ __forceinline__ void epilogue_tail_part(const Params& p, const CUtensorMap* tmT, int tb, int r_local,
+                                                   int row0, int lane, int n0, uint32_t taddr, uint8_t* sbuf,
+                                                   uint32_t& k, int part) {
+  constexpr int NBUF = 2;
+  const uint32_t sb = smem_u32(sbuf);
+#pragma unroll 1
+  for (int c = part * (PAIR_BN / 32 / NSPLIT); c < (part + 1) * (PAIR_BN / 32 / NSPLIT); ++c) {
+    if (n0 + c * 32 >= p.n_store) break;  // columns the fix-up never reads
+    uint32_t r[32];
+    __syncwarp();
+    tmem_ld32(taddr + c * 32, r);
+    tmem_wait_ld();
+    const uint32_t buf = sb + (k % NBUF) * 4096;
+    if (lane == 0) bulk_wait_read<NBUF - 1>();  // this buffer's previous boxes have left it
+    __syncwarp();
+#pragma unroll
+    for (int q = 0; q < 8; ++q)
+      sts128(sw128(buf, lane, q), make_uint4(r[q * 4], r[q * 4 + 1], r[q * 4 + 2], r[q * 4 + 3]));
+    fence_proxy_async_smem();
+    __syncwarp();
+    if (lane == 0) {
+      if (row0 < p.M) tma_store_3d(tmT, sbuf + (k % NBUF) * 4096, c * 32, r_local, tb);
+      bulk_commit();
+    }
+    ++k;
+  }
+}
+
 // Work unit of the pair kernel: tile `unit mod tiles` over K part
 // `unit / tiles` of the (shard-major) K blocks, [kb0, kb0 + nkb).  Without a
-// K split, one unit per tile over all K blocks.
+// K split, one unit per tile over all K blocks.  With a last-wave split, the
+// first tiles - tail_tiles units are whole tiles and unit whole + u is part
+// u / tail_tiles of tail tile u mod tail_tiles; it returns -1 - u.
 __device__ __forceinline__ int pair_unit(const Params& p, int unit, int num_tiles, int& tile, int& kb0, int& nkb) {
+  if (p.tail_parts > 1) {
+    const int whole = num_tiles - p.tail_tiles;
+    const int kall = p.G * p.k_blocks;
+    if (unit < whole) {
+      tile = unit;
+      kb0 = 0;
+      nkb = kall;
+      return 0;
+    }
+    // part j: K blocks [j kall / parts, (j + 1) kall / parts), none empty
+    const int u = unit - whole, part = u / p.tail_tiles;
+    tile = whole + (u - part * p.tail_tiles);
+    kb0 = part * kall / p.tail_parts;
+    nkb = (part + 1) * kall / p.tail_parts - kb0;
+    return -1 - u;
+  }
   const int kh = p.ksplit > 1 ? unit / num_tiles : 0;
   tile = unit - kh * num_tiles;
   const int kall = p.G * p.k_blocks;
@@ -983,7 +1036,9 @@ __global__ void __launch_bounds__(pair_threads<EPI, TM>(), 1)
 
   const int tiles_m2 = (p.tiles_m + 1) >> 1;
   const int num_tiles = tiles_m2 * p.tiles_n * p.NB;
-  const int num_units = num_tiles * p.ksplit;  // K parts of the split (fp32 partial) GEMMs
+  // K parts of the split (fp32 partial) GEMMs, or of the last wave's tiles
+  const int num_units =
+      p.tail_parts > 1 ? num_tiles + p.tail_tiles * (p.tail_parts - 1) : num_tiles * p.ksplit;
 
   if (warp == 0) {
     // ------------------------------------------------ TMA producer (both CTAs)
@@ -1414,13 +1469,17 @@ __global__ void __launch_bounds__(pair_threads<EPI, TM>(), 1)
         tc_fence_after();
         int b, mp, nb;
         decode_pair_tile(p, tile, b, mp, nb);
-        b += kh * p.NB;  // K part kh: fp32 batch kh * NB + b (EPI_F32 only)
+        if (kh > 0) b += kh * p.NB;  // K part kh: fp32 batch kh * NB + b (EPI_F32 only)
         const int row0 = mp * 256 + static_cast<int>(rank) * 128 + quarter * 32;
         const uint32_t taddr = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) +
                                static_cast<uint32_t>(buf * BN);
         if constexpr (TMA) {
-          epilogue_tile_tma<EPI, EW / 4>(p, &tmO, &tmO2, b, row0, lane, nb * BN, nb, taddr,
-                                         smem + L::AUX_OFF + (warp - 2) * OUT_BUF, staged, (warp - 2) >> 2);
+          if (kh < 0)  // a last-wave K part: fp32 boxes into batch -1 - kh of the tail map (tmO2)
+            epilogue_tail_part<EW / 4>(p, &tmO2, -1 - kh, row0 - mp * 256, row0, lane, nb * BN, taddr,
+                                       smem + L::AUX_OFF + (warp - 2) * OUT_BUF, staged, (warp - 2) >> 2);
+          else
+            epilogue_tile_tma<EPI, EW / 4>(p, &tmO, &tmO2, b, row0, lane, nb * BN, nb, taddr,
+                                           smem + L::AUX_OFF + (warp - 2) * OUT_BUF, staged, (warp - 2) >> 2);
         } else {
           const int row = row0 + lane;
           epilogue_tile<BN, EPI>(p, b, row, row < p.M, nb * BN, nb, taddr, (warp - 2) >> 2);
@@ -1726,6 +1785,13 @@ static bool tma_store_enabled() {
   return on;
 }
 
+// TPFFN_TAIL_SPLIT=0 in the environment turns the last-wave split off (for
+// comparisons).
+static bool tail_split_enabled() {
+  static const bool on = !getenv_flag_off("TPFFN_TAIL_SPLIT");
+  return on;
+}
+
 // Launch of one pair-kernel instance (its own attribute set-up and cluster
 // occupancy query per device).
 template <int EPI, bool AMN, bool BMN, int TM>
@@ -1767,15 +1833,49 @@ static int launch_pair_inst(const GemmSpec& s, LaunchCtx& ctx, const CUtensorMap
       fprintf(stderr, "tpffn: pair kernel: occupancy query rc=%d clusters=%d -> using %d clusters\n", (int)qe, q, mc);
     max_clusters[dev & 31].store(mc);
   }
-  const long long tiles = static_cast<long long>((p.tiles_m + 1) / 2) * p.tiles_n * p.NB * p.ksplit;  // units
+  long long tiles = static_cast<long long>((p.tiles_m + 1) / 2) * p.tiles_n * p.NB * p.ksplit;  // units
   if (tiles <= 0 || p.k_blocks <= 0) return TP_ERR_INVALID;
+  // Last-wave split: a last wave at most half full runs its tiles as K parts
+  // (at least 8 K blocks each) spread over the SM pairs the wave leaves idle
+  Params pl = p;
+  CUtensorMap tt;
+  TailTiles tail;
+  if constexpr (EPI == EPI_OUT && TM != 0) {
+    if (s.tail_ws && s.NB == 1 && s.ksplit == 1 && !s.out_cs && !p.o_swap && tail_split_enabled()) {
+      const int rem = static_cast<int>(tiles % mc);
+      const int kall = p.G * p.k_blocks;
+      int parts = rem > 0 ? mc / rem : 0;
+      if (parts > kall / 8) parts = kall / 8;
+      int sw = 0;
+      if (rem > 0 && rem <= kMaxTailTiles && 2 * rem <= mc && parts >= 2 &&
+          static_cast<size_t>(rem) * parts * 65536 * 4 <= s.tail_ws_bytes &&
+          make_out_map(&tt, s.tail_ws, true, 256, 256, static_cast<int64_t>(rem) * parts, 256, 65536, &sw) == 0 &&
+          sw == 0) {
+        pl.tail_tiles = rem;
+        pl.tail_parts = parts;
+        tail.n = rem;
+        tail.parts = parts;
+        for (int i = 0; i < rem; ++i) {
+          int b, mp, nb;
+          decode_pair_tile(pl, static_cast<int>(tiles) - rem + i, b, mp, nb);
+          tail.mp[i] = mp;
+          tail.nb[i] = nb;
+        }
+        tiles += static_cast<long long>(rem) * (parts - 1);
+      }
+    }
+  }
   const int clusters = static_cast<int>(tiles < mc ? tiles : mc);
   cfg.gridDim = dim3(2 * clusters, 1, 1);
   if (ctx.before) ctx.before(ctx.user, s.name, ctx.stream);
-  cudaError_t e = cudaLaunchKernelEx(&cfg, kern, ta, tb, tx, to, to2, p);
+  cudaError_t e = cudaLaunchKernelEx(&cfg, kern, ta, tb, tx, to, pl.tail_parts ? tt : to2, pl);
   if (ctx.after) ctx.after(ctx.user, ctx.stream);
   ctx.launches++;
-  return e == cudaSuccess && cudaPeekAtLastError() == cudaSuccess ? 0 : TP_ERR_CUDA;
+  if (e != cudaSuccess || cudaPeekAtLastError() != cudaSuccess) return TP_ERR_CUDA;
+  if (pl.tail_parts)
+    return launch_tail_fixup(s.tail_ws, tail, s.out, s.out_rs, s.bias, s.bias_len, s.M, s.n_store, ctx,
+                             "tail_fixup");
+  return 0;
 }
 
 template <int EPI, bool AMN, bool BMN>

@@ -617,6 +617,67 @@ int launch_swiglu_combine(const float* parts, int ksplit, int T_p, int64_t rows,
   return cudaPeekAtLastError() == cudaSuccess ? 0 : TP_ERR_CUDA;
 }
 
+// Fix-up of a pair GEMM's last-wave split: tail tile i (the 256 x 256 output
+// block at rows mp[i] * 256, columns nb[i] * 256) was accumulated as
+// t.parts K parts, part k's fp32 block at P + (k * t.n + i) * 65536 (row-
+// major, 256 columns).  The parts are added in the order k = 0, 1, .., the
+// bias added as the GEMM's own epilogue adds it, and the bf16 result written
+// where that epilogue would have; rows >= M and columns >= n_store are not
+// written.  One thread per 8 columns.
+__global__ void __launch_bounds__(256) tail_fixup_kernel(const float* __restrict__ P, TailTiles t,
+                                                         __nv_bfloat16* __restrict__ out, long long out_rs,
+                                                         const __nv_bfloat16* __restrict__ bias, long long bias_len,
+                                                         long long M, long long n_store) {
+  // a programmatic dependent of the GEMM that wrote the parts
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  const long long total = static_cast<long long>(t.n) * 256 * 32;
+  const long long block = 256 * 256;
+  for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < total;
+       i += (long long)gridDim.x * blockDim.x) {
+    const int ti = static_cast<int>(i >> 13);
+    const int r = static_cast<int>((i >> 5) & 255), c = static_cast<int>(i & 31) * 8;
+    const long long row = static_cast<long long>(t.mp[ti]) * 256 + r, col = static_cast<long long>(t.nb[ti]) * 256 + c;
+    if (row >= M || col >= n_store) continue;
+    const float* q = P + ti * block + r * 256 + c;
+    float v[8];
+    {
+      const float4 a = reinterpret_cast<const float4*>(q)[0], b = reinterpret_cast<const float4*>(q)[1];
+      v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w; v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
+    }
+    for (int k = 1; k < t.parts; ++k) {
+      const float* qk = q + static_cast<long long>(k) * t.n * block;
+      const float4 a = reinterpret_cast<const float4*>(qk)[0], b = reinterpret_cast<const float4*>(qk)[1];
+      v[0] += a.x; v[1] += a.y; v[2] += a.z; v[3] += a.w; v[4] += b.x; v[5] += b.y; v[6] += b.z; v[7] += b.w;
+    }
+    if (bias) {
+#pragma unroll
+      for (int j = 0; j < 8; ++j)
+        if (col + j < bias_len) v[j] += __bfloat162float(bias[col + j]);
+    }
+    __nv_bfloat162 h[4] = {__floats2bfloat162_rn(v[0], v[1]), __floats2bfloat162_rn(v[2], v[3]),
+                           __floats2bfloat162_rn(v[4], v[5]), __floats2bfloat162_rn(v[6], v[7])};
+    *reinterpret_cast<uint4*>(out + row * out_rs + col) = *reinterpret_cast<const uint4*>(h);
+  }
+}
+
+int launch_tail_fixup(const float* parts, const TailTiles& t, void* out, int64_t out_rs, const void* bias,
+                      int64_t bias_len, int64_t M, int64_t n_store, LaunchCtx& ctx, const char* name) {
+  if (t.n < 1 || t.n > kMaxTailTiles || t.parts < 2) return TP_ERR_INVALID;
+  if (reinterpret_cast<uintptr_t>(parts) % 16 || reinterpret_cast<uintptr_t>(out) % 16 || out_rs % 8 ||
+      n_store % 8)
+    return TP_ERR_ALIGN;
+  const long long total = static_cast<long long>(t.n) * 256 * 32;
+  if (ctx.before) ctx.before(ctx.user, name, ctx.stream);
+  launch_pdl(tail_fixup_kernel, dim3(grid_for(total, 256, ctx.num_sms)), 256, ctx.stream, parts, t,
+             static_cast<__nv_bfloat16*>(out), static_cast<long long>(out_rs),
+             static_cast<const __nv_bfloat16*>(bias), static_cast<long long>(bias_len), static_cast<long long>(M),
+             static_cast<long long>(n_store));
+  if (ctx.after) ctx.after(ctx.user, ctx.stream);
+  ctx.launches++;
+  return cudaPeekAtLastError() == cudaSuccess ? 0 : TP_ERR_CUDA;
+}
+
 static SliceTable to_table(const RowSlices& r) {
   SliceTable t{};
   for (int i = 0; i < r.n && i < kMaxSlices; ++i) t.p[i] = static_cast<char*>(r.ptr[i]);

@@ -171,6 +171,36 @@ def test_wgrad_ksplit_is_taken(w):
         assert names[names.index(wg1) + 1] == wg1 + "_ksum", names
 
 
+# Fused-sum forwards whose output tiles leave the last wave of SM pairs at
+# most half full run those tiles as K parts (fp32), summed in part order by a
+# fix-up kernel: 6 tiles of 4 parts (GELU with biases, ragged rows), 6 tiles
+# of 3 unequal parts (9, 9 and 10 of 28 K blocks) and 9 tiles of 3 parts
+# (SwiGLU, ragged rows and d).
+TAIL_SPLIT = [small_case(700, 512, 2048, 2, "gelu_tanh", bias=True, seed=116),
+              small_case(700, 512, 1792, 7, "gelu_tanh", bias=True, seed=118),
+              small_case(600, 760, 1536, 4, "swiglu", seed=117)]
+
+
+@pytest.mark.parametrize("w", TAIL_SPLIT, ids=[w.name for w in TAIL_SPLIT])
+def test_tail_split_against_full_oracle(w):
+    _full_compare(w, True)
+
+
+@pytest.mark.parametrize("w", TAIL_SPLIT + [MANY_TILES], ids=[w.name for w in TAIL_SPLIT + [MANY_TILES]])
+def test_tail_split_is_taken(w):
+    """The fused forward's down GEMM of the cases above splits its last wave:
+    the launch records name the fix-up right after it."""
+    from megatron_tensor_transformer_w1_gb300 import tpffn as abi
+    from megatron_tensor_transformer_w1_gb300.ffn import TensorParallelFFN
+    dev = torch.device("cuda", 0)
+    g = {k: (None if v is None else v.to(dev)) for k, v in make_inputs(w).items()}
+    ffn = TensorParallelFFN(w.d, w.d_ff, w.T_p, w.act, "bf16", device=dev)
+    w13p, w2p = ffn.pack(g["W1"], g["W2"], g["W3"])
+    ffn.forward(g["x"], w13p, w2p, g["b1"], g["b2"], fused=True, flags=abi.TP_FLAG_TIMING)
+    names = [n for n, _ in abi.tp_ffn_kernel_times(ffn.plan, 1000)]
+    assert names[names.index("down_fused_sum") + 1:] == ["tail_fixup"], names
+
+
 def _sweep_cases(n=10, seed=20261202):
     """Seeded random shapes across both kernel paths (token counts of at most
     32, under 256 and above), both activations, biases on or off, ragged
