@@ -623,7 +623,8 @@ int launch_swiglu_combine(const float* parts, int ksplit, int T_p, int64_t rows,
 // major, 256 columns).  The parts are added in the order k = 0, 1, .., the
 // bias added as the GEMM's own epilogue adds it, and the bf16 result written
 // where that epilogue would have; rows >= M and columns >= n_store are not
-// written.  One thread per 8 columns.
+// written.  One thread per 4 columns; the parts are read four at a time with
+// independent loads (the sum order stays k = 0, 1, ..).
 __global__ void __launch_bounds__(256) tail_fixup_kernel(const float* __restrict__ P, TailTiles t,
                                                          __nv_bfloat16* __restrict__ out, long long out_rs,
                                                          const __nv_bfloat16* __restrict__ bias, long long bias_len,
@@ -631,33 +632,39 @@ __global__ void __launch_bounds__(256) tail_fixup_kernel(const float* __restrict
   // a programmatic dependent of the GEMM that wrote the parts
   asm volatile("griddepcontrol.wait;" ::: "memory");
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-  const long long total = static_cast<long long>(t.n) * 256 * 32;
-  const long long block = 256 * 256;
+  const long long total = static_cast<long long>(t.n) * 256 * 64;
+  const long long stride = static_cast<long long>(t.n) * (65536 / 4);  // float4s between parts
   for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < total;
        i += (long long)gridDim.x * blockDim.x) {
-    const int ti = static_cast<int>(i >> 13);
-    const int r = static_cast<int>((i >> 5) & 255), c = static_cast<int>(i & 31) * 8;
+    const int ti = static_cast<int>(i >> 14);
+    const int r = static_cast<int>((i >> 6) & 255), c = static_cast<int>(i & 63) * 4;
     const long long row = static_cast<long long>(t.mp[ti]) * 256 + r, col = static_cast<long long>(t.nb[ti]) * 256 + c;
-    if (row >= M || col >= n_store) continue;
-    const float* q = P + ti * block + r * 256 + c;
-    float v[8];
-    {
-      const float4 a = reinterpret_cast<const float4*>(q)[0], b = reinterpret_cast<const float4*>(q)[1];
-      v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w; v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
+    if (row >= M || col >= n_store) continue;  // n_store is a multiple of 8: the 4 columns are all in or all out
+    const float4* q = reinterpret_cast<const float4*>(P) + ti * (65536 / 4) + r * 64 + c / 4;
+    float4 acc = q[0];
+    int k = 1;
+    for (; k + 3 < t.parts; k += 4) {
+      const float4 a = q[k * stride], b = q[(k + 1) * stride], e = q[(k + 2) * stride], f = q[(k + 3) * stride];
+      acc.x = (((acc.x + a.x) + b.x) + e.x) + f.x;
+      acc.y = (((acc.y + a.y) + b.y) + e.y) + f.y;
+      acc.z = (((acc.z + a.z) + b.z) + e.z) + f.z;
+      acc.w = (((acc.w + a.w) + b.w) + e.w) + f.w;
     }
-    for (int k = 1; k < t.parts; ++k) {
-      const float* qk = q + static_cast<long long>(k) * t.n * block;
-      const float4 a = reinterpret_cast<const float4*>(qk)[0], b = reinterpret_cast<const float4*>(qk)[1];
-      v[0] += a.x; v[1] += a.y; v[2] += a.z; v[3] += a.w; v[4] += b.x; v[5] += b.y; v[6] += b.z; v[7] += b.w;
+    for (; k < t.parts; ++k) {
+      const float4 a = q[k * stride];
+      acc.x += a.x;
+      acc.y += a.y;
+      acc.z += a.z;
+      acc.w += a.w;
     }
+    float v[4] = {acc.x, acc.y, acc.z, acc.w};
     if (bias) {
 #pragma unroll
-      for (int j = 0; j < 8; ++j)
+      for (int j = 0; j < 4; ++j)
         if (col + j < bias_len) v[j] += __bfloat162float(bias[col + j]);
     }
-    __nv_bfloat162 h[4] = {__floats2bfloat162_rn(v[0], v[1]), __floats2bfloat162_rn(v[2], v[3]),
-                           __floats2bfloat162_rn(v[4], v[5]), __floats2bfloat162_rn(v[6], v[7])};
-    *reinterpret_cast<uint4*>(out + row * out_rs + col) = *reinterpret_cast<const uint4*>(h);
+    __nv_bfloat162 h[2] = {__floats2bfloat162_rn(v[0], v[1]), __floats2bfloat162_rn(v[2], v[3])};
+    *reinterpret_cast<uint2*>(out + row * out_rs + col) = *reinterpret_cast<const uint2*>(h);
   }
 }
 
@@ -667,7 +674,7 @@ int launch_tail_fixup(const float* parts, const TailTiles& t, void* out, int64_t
   if (reinterpret_cast<uintptr_t>(parts) % 16 || reinterpret_cast<uintptr_t>(out) % 16 || out_rs % 8 ||
       n_store % 8)
     return TP_ERR_ALIGN;
-  const long long total = static_cast<long long>(t.n) * 256 * 32;
+  const long long total = static_cast<long long>(t.n) * 256 * 64;
   if (ctx.before) ctx.before(ctx.user, name, ctx.stream);
   launch_pdl(tail_fixup_kernel, dim3(grid_for(total, 256, ctx.num_sms)), 256, ctx.stream, parts, t,
              static_cast<__nv_bfloat16*>(out), static_cast<long long>(out_rs),
