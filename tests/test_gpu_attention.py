@@ -183,6 +183,7 @@ SUB_CASES = [  # B, S, d, H, Hkv, T_p, causal, fused
     (1, 200, 384, 8, 8, 4, False, False),
     (3, 70, 128, 4, 4, 4, True, True),
     (1, 130, 256, 16, 2, 2, True, False),  # GQA groups of 8
+    (2, 256, 1024, 8, 8, 4, True, True),  # Q/K/V projection (24 tiles) and W_O forward (8) split into K parts
 ]
 
 

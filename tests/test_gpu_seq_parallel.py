@@ -14,6 +14,7 @@ pytestmark = pytest.mark.gpu
 
 CASES = [small_case(336, 264, 600, 3, "swiglu", seed=701),
          small_case(512, 192, 768, 4, "gelu_tanh", bias=True, seed=702),
+         small_case(512, 256, 2048, 4, "gelu_tanh", bias=True, seed=704),  # fused: last wave in 4 K parts
          Workload("attn_out_sp_300x256_h6x64_tp3", 300, 256, 384, 3, "none", "bf16", seed_index=703,
                   n_heads=6, n_kv_heads=6, head_dim=64)]
 
