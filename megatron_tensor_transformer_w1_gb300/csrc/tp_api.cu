@@ -206,9 +206,9 @@ WsLayout ws_layout(const tp_ffn_plan* p, int64_t n, int flags) {
       off += align_up(wk);
     }
   }
-  if ((flags & TP_SUM_FUSED) && p->dtype == TP_BF16 && tc_pair_path(n)) {
-    // fp32 K parts of a fused-sum GEMM's last-wave tiles: at most one
-    // 256 x 256 block per SM pair
+  if (((flags & TP_SUM_FUSED) || p->act == TP_ACT_GELU_TANH) && p->dtype == TP_BF16 && tc_pair_path(n)) {
+    // fp32 K parts of the last-wave tiles of a fused-sum GEMM or of the GELU
+    // up GEMM: at most one 256 x 256 block per SM pair
     L.has_tail = true;
     L.tail = off;
     L.tail_bytes = static_cast<size_t>(num_sms_current() / 2) * 256 * 256 * 4;
@@ -572,6 +572,10 @@ static int fwd_impl(const tp_ffn_plan* p, int64_t n, const void* x, const void* 
     g.bias_len = p->s;
     g.n_store = sp;
     g.out_bf16 = out_bf16;
+    if (L.has_tail && p->act == TP_ACT_GELU_TANH) {
+      g.tail_ws = reinterpret_cast<float*>(ws + L.tail);
+      g.tail_ws_bytes = L.tail_bytes;
+    }
     const int ks = L.has_ks ? choose_ksplit(p, n, ctx.num_sms) : 1;
     if (ks > 1) {
       // fp32 parts of a and g, then the SwiGLU combine

@@ -1474,8 +1474,8 @@ __global__ void __launch_bounds__(pair_threads<EPI, TM>(), 1)
         const uint32_t taddr = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) +
                                static_cast<uint32_t>(buf * BN);
         if constexpr (TMA) {
-          if (kh < 0)  // a last-wave K part: fp32 boxes into batch -1 - kh of the tail map (tmO2)
-            epilogue_tail_part<EW / 4>(p, &tmO2, -1 - kh, row0 - mp * 256, row0, lane, nb * BN, taddr,
+          if (kh < 0)  // a last-wave K part: fp32 boxes into batch -1 - kh of the tail map (in tmX)
+            epilogue_tail_part<EW / 4>(p, &tmX, -1 - kh, row0 - mp * 256, row0, lane, nb * BN, taddr,
                                        smem + L::AUX_OFF + (warp - 2) * OUT_BUF, staged, (warp - 2) >> 2);
           else
             epilogue_tile_tma<EPI, EW / 4>(p, &tmO, &tmO2, b, row0, lane, nb * BN, nb, taddr,
@@ -1840,8 +1840,9 @@ static int launch_pair_inst(const GemmSpec& s, LaunchCtx& ctx, const CUtensorMap
   Params pl = p;
   CUtensorMap tt;
   TailTiles tail;
-  if constexpr (EPI == EPI_OUT && TM != 0) {
-    if (s.tail_ws && s.NB == 1 && s.ksplit == 1 && !s.out_cs && !p.o_swap && tail_split_enabled()) {
+  if constexpr ((EPI == EPI_OUT || EPI == EPI_GELU_FWD) && TM != 0) {
+    if (s.tail_ws && (EPI == EPI_GELU_FWD || s.NB == 1) && s.ksplit == 1 && !s.out_cs && !p.o_swap &&
+        tail_split_enabled()) {
       const int rem = static_cast<int>(tiles % mc);
       const int kall = p.G * p.k_blocks;
       int parts = rem > 0 ? mc / rem : 0;
@@ -1858,6 +1859,7 @@ static int launch_pair_inst(const GemmSpec& s, LaunchCtx& ctx, const CUtensorMap
         for (int i = 0; i < rem; ++i) {
           int b, mp, nb;
           decode_pair_tile(pl, static_cast<int>(tiles) - rem + i, b, mp, nb);
+          tail.b[i] = b;
           tail.mp[i] = mp;
           tail.nb[i] = nb;
         }
@@ -1868,13 +1870,27 @@ static int launch_pair_inst(const GemmSpec& s, LaunchCtx& ctx, const CUtensorMap
   const int clusters = static_cast<int>(tiles < mc ? tiles : mc);
   cfg.gridDim = dim3(2 * clusters, 1, 1);
   if (ctx.before) ctx.before(ctx.user, s.name, ctx.stream);
-  cudaError_t e = cudaLaunchKernelEx(&cfg, kern, ta, tb, tx, to, pl.tail_parts ? tt : to2, pl);
+  // the tail map travels in the aux-map slot, which these epilogues do not use
+  cudaError_t e = cudaLaunchKernelEx(&cfg, kern, ta, tb, pl.tail_parts ? tt : tx, to, to2, pl);
   if (ctx.after) ctx.after(ctx.user, ctx.stream);
   ctx.launches++;
   if (e != cudaSuccess || cudaPeekAtLastError() != cudaSuccess) return TP_ERR_CUDA;
-  if (pl.tail_parts)
-    return launch_tail_fixup(s.tail_ws, tail, s.out, s.out_rs, s.bias, s.bias_len, s.M, s.n_store, ctx,
-                             "tail_fixup");
+  if (pl.tail_parts) {
+    TailOut o;
+    o.out = s.out;
+    o.out_bs = s.out_bs;
+    o.out_rs = s.out_rs;
+    o.out2 = EPI == EPI_GELU_FWD ? s.out2 : nullptr;
+    o.out2_bs = s.out2_bs;
+    o.out2_rs = s.out2_rs;
+    o.bias = s.bias;
+    o.bias_bs = s.bias_bs;
+    o.bias_len = s.bias_len;
+    o.M = s.M;
+    o.n_store = s.n_store;
+    o.gelu = EPI == EPI_GELU_FWD;
+    return launch_tail_fixup(s.tail_ws, tail, o, ctx, "tail_fixup");
+  }
   return 0;
 }
 

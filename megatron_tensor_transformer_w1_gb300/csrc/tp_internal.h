@@ -64,11 +64,12 @@ struct GemmSpec {
   // waiting (the kernel before it must have waited for its own
   // predecessor), and waits before exit.
   int no_dep_wait = 0;
-  // Last-wave split (pair kernel, EPI_OUT, NB = G-fused sums with TMA
-  // stores): when the output tiles leave the last wave of SM pairs at most
-  // half full, those tiles run as K parts that fill the idle pairs; their
-  // fp32 sums go to tail_ws (tail_ws_bytes) and a fix-up kernel adds them in
-  // part order (+ bias) into `out`.  nullptr: no split.
+  // Last-wave split (pair kernel with TMA stores; EPI_OUT with one batch, or
+  // EPI_GELU_FWD): when the output tiles leave the last wave of SM pairs at
+  // most half full, those tiles run as K parts that fill the idle pairs;
+  // their fp32 sums go to tail_ws (tail_ws_bytes) and a fix-up kernel adds
+  // them in part order, adds the bias (and applies GELU) and writes what the
+  // epilogue would have.  nullptr: no split.
   float* tail_ws = nullptr;
   size_t tail_ws_bytes = 0;
 };
@@ -115,15 +116,26 @@ int launch_pack_columns(const void* W1, const void* W3, void* out, int T_p, int6
 int launch_pack_rows(const void* W2, void* out, int T_p, int64_t s, int64_t s_pad, int64_t d,
                      int esz, int unpack, cudaStream_t st);
 // shard_stride: elements between consecutive shards' partials (0: rows*cols).
-// Tiles of a last-wave split (256 x 256 output blocks at rows mp * 256 and
-// columns nb * 256), each summed from `parts` fp32 K parts.
+// Tiles of a last-wave split (256 x 256 output blocks of batch b at rows
+// mp * 256 and columns nb * 256), each summed from `parts` fp32 K parts.
 constexpr int kMaxTailTiles = 64;
 struct TailTiles {
   int n = 0, parts = 0;
-  int mp[kMaxTailTiles], nb[kMaxTailTiles];
+  int b[kMaxTailTiles], mp[kMaxTailTiles], nb[kMaxTailTiles];
 };
-int launch_tail_fixup(const float* parts, const TailTiles& t, void* out, int64_t out_rs, const void* bias,
-                      int64_t bias_len, int64_t M, int64_t n_store, LaunchCtx& ctx, const char* name);
+// What the fix-up writes: the GEMM epilogue's output (bf16, + bias), or for
+// the GELU forward h = gelu(z) and, when out2 is given, z (both bf16).
+struct TailOut {
+  void* out = nullptr;
+  int64_t out_bs = 0, out_rs = 0;
+  void* out2 = nullptr;
+  int64_t out2_bs = 0, out2_rs = 0;
+  const void* bias = nullptr;
+  int64_t bias_bs = 0, bias_len = 0;
+  int64_t M = 0, n_store = 0;
+  int gelu = 0;
+};
+int launch_tail_fixup(const float* parts, const TailTiles& t, const TailOut& o, LaunchCtx& ctx, const char* name);
 // SwiGLU of the ksplit fp32 parts of a K-split up GEMM (see tp_kernels.cu).
 int launch_swiglu_combine(const float* parts, int ksplit, int T_p, int64_t rows, int64_t s_pad, void* h,
                           void* saved, LaunchCtx& ctx, const char* name);

@@ -618,28 +618,27 @@ int launch_swiglu_combine(const float* parts, int ksplit, int T_p, int64_t rows,
 }
 
 // Fix-up of a pair GEMM's last-wave split: tail tile i (the 256 x 256 output
-// block at rows mp[i] * 256, columns nb[i] * 256) was accumulated as
-// t.parts K parts, part k's fp32 block at P + (k * t.n + i) * 65536 (row-
-// major, 256 columns).  The parts are added in the order k = 0, 1, .., the
-// bias added as the GEMM's own epilogue adds it, and the bf16 result written
-// where that epilogue would have; rows >= M and columns >= n_store are not
+// block of batch b[i] at rows mp[i] * 256, columns nb[i] * 256) was
+// accumulated as t.parts K parts, part k's fp32 block at
+// P + (k * t.n + i) * 65536 (row-major, 256 columns).  The parts are added in
+// the order k = 0, 1, .., then the bias, and the result written as the GEMM's
+// own epilogue would have: v in bf16 (GEMM output), or h = gelu(v) and, with
+// out2, z = v (GELU forward).  Rows >= M and columns >= n_store are not
 // written.  One thread per 4 columns; the parts are read four at a time with
 // independent loads (the sum order stays k = 0, 1, ..).
-__global__ void __launch_bounds__(256) tail_fixup_kernel(const float* __restrict__ P, TailTiles t,
-                                                         __nv_bfloat16* __restrict__ out, long long out_rs,
-                                                         const __nv_bfloat16* __restrict__ bias, long long bias_len,
-                                                         long long M, long long n_store) {
+__global__ void __launch_bounds__(256) tail_fixup_kernel(const float* __restrict__ P, TailTiles t, TailOut o) {
   // a programmatic dependent of the GEMM that wrote the parts
   asm volatile("griddepcontrol.wait;" ::: "memory");
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   const long long total = static_cast<long long>(t.n) * 256 * 64;
   const long long stride = static_cast<long long>(t.n) * (65536 / 4);  // float4s between parts
+  const __nv_bfloat16* bias = static_cast<const __nv_bfloat16*>(o.bias);
   for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < total;
        i += (long long)gridDim.x * blockDim.x) {
     const int ti = static_cast<int>(i >> 14);
     const int r = static_cast<int>((i >> 6) & 255), c = static_cast<int>(i & 63) * 4;
     const long long row = static_cast<long long>(t.mp[ti]) * 256 + r, col = static_cast<long long>(t.nb[ti]) * 256 + c;
-    if (row >= M || col >= n_store) continue;  // n_store is a multiple of 8: the 4 columns are all in or all out
+    if (row >= o.M || col >= o.n_store) continue;  // n_store is a multiple of 8: the 4 columns are all in or all out
     const float4* q = reinterpret_cast<const float4*>(P) + ti * (65536 / 4) + r * 64 + c / 4;
     float4 acc = q[0];
     int k = 1;
@@ -658,28 +657,37 @@ __global__ void __launch_bounds__(256) tail_fixup_kernel(const float* __restrict
       acc.w += a.w;
     }
     float v[4] = {acc.x, acc.y, acc.z, acc.w};
+    const long long bt = t.b[ti];
     if (bias) {
+      const __nv_bfloat16* bp = bias + bt * o.bias_bs;
 #pragma unroll
       for (int j = 0; j < 4; ++j)
-        if (col + j < bias_len) v[j] += __bfloat162float(bias[col + j]);
+        if (col + j < o.bias_len) v[j] += __bfloat162float(bp[col + j]);
+    }
+    if (o.gelu) {
+      if (o.out2) {
+        __nv_bfloat162 z[2] = {__floats2bfloat162_rn(v[0], v[1]), __floats2bfloat162_rn(v[2], v[3])};
+        *reinterpret_cast<uint2*>(static_cast<__nv_bfloat16*>(o.out2) + bt * o.out2_bs + row * o.out2_rs + col) =
+            *reinterpret_cast<const uint2*>(z);
+      }
+#pragma unroll
+      for (int j = 0; j < 4; ++j) v[j] = gelu_tanh_f(v[j]);
     }
     __nv_bfloat162 h[2] = {__floats2bfloat162_rn(v[0], v[1]), __floats2bfloat162_rn(v[2], v[3])};
-    *reinterpret_cast<uint2*>(out + row * out_rs + col) = *reinterpret_cast<const uint2*>(h);
+    *reinterpret_cast<uint2*>(static_cast<__nv_bfloat16*>(o.out) + bt * o.out_bs + row * o.out_rs + col) =
+        *reinterpret_cast<const uint2*>(h);
   }
 }
 
-int launch_tail_fixup(const float* parts, const TailTiles& t, void* out, int64_t out_rs, const void* bias,
-                      int64_t bias_len, int64_t M, int64_t n_store, LaunchCtx& ctx, const char* name) {
+int launch_tail_fixup(const float* parts, const TailTiles& t, const TailOut& o, LaunchCtx& ctx, const char* name) {
   if (t.n < 1 || t.n > kMaxTailTiles || t.parts < 2) return TP_ERR_INVALID;
-  if (reinterpret_cast<uintptr_t>(parts) % 16 || reinterpret_cast<uintptr_t>(out) % 16 || out_rs % 8 ||
-      n_store % 8)
+  const auto a16 = [](const void* q) { return reinterpret_cast<uintptr_t>(q) % 16 == 0; };
+  if (!a16(parts) || !a16(o.out) || (o.out2 && !a16(o.out2)) || o.out_rs % 8 || o.out_bs % 8 || o.out2_rs % 8 ||
+      o.out2_bs % 8 || o.n_store % 8)
     return TP_ERR_ALIGN;
   const long long total = static_cast<long long>(t.n) * 256 * 64;
   if (ctx.before) ctx.before(ctx.user, name, ctx.stream);
-  launch_pdl(tail_fixup_kernel, dim3(grid_for(total, 256, ctx.num_sms)), 256, ctx.stream, parts, t,
-             static_cast<__nv_bfloat16*>(out), static_cast<long long>(out_rs),
-             static_cast<const __nv_bfloat16*>(bias), static_cast<long long>(bias_len), static_cast<long long>(M),
-             static_cast<long long>(n_store));
+  launch_pdl(tail_fixup_kernel, dim3(grid_for(total, 256, ctx.num_sms)), 256, ctx.stream, parts, t, o);
   if (ctx.after) ctx.after(ctx.user, ctx.stream);
   ctx.launches++;
   return cudaPeekAtLastError() == cudaSuccess ? 0 : TP_ERR_CUDA;
