@@ -168,8 +168,8 @@ TPFFN_API size_t tp_ffn_saved_bytes(const tp_ffn_plan* plan, int64_t n_tokens);
  * is saved, the fp32 shard partials of the standalone sum, the backward's
  * hidden gradients, the fp32 K parts of split GEMMs (decode-sized SwiGLU up
  * GEMMs; weight-gradient GEMMs of problems with few output tiles; the last
- * wave of a fused-sum or GELU forward GEMM, one 256 x 256 fp32 block per SM
- * pair --
+ * wave of a forward GEMM (up, or fused-sum down), one 256 x 256 fp32 block
+ * per SM pair --
  * sized from the current device's SM count) and the bias-gradient reduction
  * scratch.  Query it on the device that will run the calls. */
 TPFFN_API size_t tp_ffn_workspace_bytes(const tp_ffn_plan* plan, int64_t n_tokens, int flags);

@@ -206,9 +206,9 @@ WsLayout ws_layout(const tp_ffn_plan* p, int64_t n, int flags) {
       off += align_up(wk);
     }
   }
-  if (((flags & TP_SUM_FUSED) || p->act == TP_ACT_GELU_TANH) && p->dtype == TP_BF16 && tc_pair_path(n)) {
-    // fp32 K parts of the last-wave tiles of a fused-sum GEMM or of the GELU
-    // up GEMM: at most one 256 x 256 block per SM pair
+  if (((flags & TP_SUM_FUSED) || p->act != TP_ACT_NONE) && p->dtype == TP_BF16 && tc_pair_path(n)) {
+    // fp32 K parts of the last-wave tiles of a fused-sum GEMM or of the up
+    // GEMM: at most one 256 x 256 block per SM pair
     L.has_tail = true;
     L.tail = off;
     L.tail_bytes = static_cast<size_t>(num_sms_current() / 2) * 256 * 256 * 4;
@@ -572,7 +572,7 @@ static int fwd_impl(const tp_ffn_plan* p, int64_t n, const void* x, const void* 
     g.bias_len = p->s;
     g.n_store = sp;
     g.out_bf16 = out_bf16;
-    if (L.has_tail && p->act == TP_ACT_GELU_TANH) {
+    if (L.has_tail) {
       g.tail_ws = reinterpret_cast<float*>(ws + L.tail);
       g.tail_ws_bytes = L.tail_bytes;
     }

@@ -910,22 +910,26 @@ __device__ __forceinline__ void epilogue_tile_tma(const Params& p, const CUtenso
 // of the tile's fp32 sum over its K part, stored as 32 x 32 boxes at (column
 // within the tile, row within the tile, tb) of the {256, 256, parts x tail
 // tiles} fp32 map.  Same staging buffers and bulk-group count as
-// epilogue_tile_tma.
-template <int NSPLIT>
+// epilogue_tile_tma; after the SwiGLU epilogue, whose one 6 KB buffer spans
+// both 4 KB buffers used here, each box waits for every earlier store to
+// have read its source.
+template <int EPI, int NSPLIT>
 __device__ __forceinline__ void epilogue_tail_part(const Params& p, const CUtensorMap* tmT, int tb, int r_local,
-                                                   int row0, int lane, int n0, uint32_t taddr, uint8_t* sbuf,
-                                                   uint32_t& k, int part) {
+                                                   int row0, int lane, uint32_t taddr, uint8_t* sbuf, uint32_t& k,
+                                                   int part) {
   constexpr int NBUF = 2;
+  constexpr int IN_FLIGHT = EPI == EPI_SWIGLU_FWD ? 0 : NBUF - 1;
   const uint32_t sb = smem_u32(sbuf);
 #pragma unroll 1
   for (int c = part * (PAIR_BN / 32 / NSPLIT); c < (part + 1) * (PAIR_BN / 32 / NSPLIT); ++c) {
-    if (n0 + c * 32 >= p.n_store) break;  // columns the fix-up never reads
+    // every chunk is stored (the map holds whole tiles); the fix-up skips
+    // the columns past the output's
     uint32_t r[32];
     __syncwarp();
     tmem_ld32(taddr + c * 32, r);
     tmem_wait_ld();
     const uint32_t buf = sb + (k % NBUF) * 4096;
-    if (lane == 0) bulk_wait_read<NBUF - 1>();  // this buffer's previous boxes have left it
+    if (lane == 0) bulk_wait_read<IN_FLIGHT>();  // this buffer's previous boxes have left it
     __syncwarp();
 #pragma unroll
     for (int q = 0; q < 8; ++q)
@@ -1475,8 +1479,8 @@ __global__ void __launch_bounds__(pair_threads<EPI, TM>(), 1)
                                static_cast<uint32_t>(buf * BN);
         if constexpr (TMA) {
           if (kh < 0)  // a last-wave K part: fp32 boxes into batch -1 - kh of the tail map (in tmX)
-            epilogue_tail_part<EW / 4>(p, &tmX, -1 - kh, row0 - mp * 256, row0, lane, nb * BN, taddr,
-                                       smem + L::AUX_OFF + (warp - 2) * OUT_BUF, staged, (warp - 2) >> 2);
+            epilogue_tail_part<EPI, EW / 4>(p, &tmX, -1 - kh, row0 - mp * 256, row0, lane, taddr,
+                                            smem + L::AUX_OFF + (warp - 2) * OUT_BUF, staged, (warp - 2) >> 2);
           else
             epilogue_tile_tma<EPI, EW / 4>(p, &tmO, &tmO2, b, row0, lane, nb * BN, nb, taddr,
                                            smem + L::AUX_OFF + (warp - 2) * OUT_BUF, staged, (warp - 2) >> 2);
@@ -1840,8 +1844,8 @@ static int launch_pair_inst(const GemmSpec& s, LaunchCtx& ctx, const CUtensorMap
   Params pl = p;
   CUtensorMap tt;
   TailTiles tail;
-  if constexpr ((EPI == EPI_OUT || EPI == EPI_GELU_FWD) && TM != 0) {
-    if (s.tail_ws && (EPI == EPI_GELU_FWD || s.NB == 1) && s.ksplit == 1 && !s.out_cs && !p.o_swap &&
+  if constexpr ((EPI == EPI_OUT || EPI == EPI_GELU_FWD || EPI == EPI_SWIGLU_FWD) && TM != 0) {
+    if (s.tail_ws && (EPI != EPI_OUT || s.NB == 1) && s.ksplit == 1 && !s.out_cs && !p.o_swap &&
         tail_split_enabled()) {
       const int rem = static_cast<int>(tiles % mc);
       const int kall = p.G * p.k_blocks;
@@ -1880,7 +1884,7 @@ static int launch_pair_inst(const GemmSpec& s, LaunchCtx& ctx, const CUtensorMap
     o.out = s.out;
     o.out_bs = s.out_bs;
     o.out_rs = s.out_rs;
-    o.out2 = EPI == EPI_GELU_FWD ? s.out2 : nullptr;
+    o.out2 = EPI == EPI_OUT ? nullptr : s.out2;
     o.out2_bs = s.out2_bs;
     o.out2_rs = s.out2_rs;
     o.bias = s.bias;
@@ -1888,7 +1892,7 @@ static int launch_pair_inst(const GemmSpec& s, LaunchCtx& ctx, const CUtensorMap
     o.bias_len = s.bias_len;
     o.M = s.M;
     o.n_store = s.n_store;
-    o.gelu = EPI == EPI_GELU_FWD;
+    o.act = EPI == EPI_GELU_FWD ? 1 : (EPI == EPI_SWIGLU_FWD ? 2 : 0);
     return launch_tail_fixup(s.tail_ws, tail, o, ctx, "tail_fixup");
   }
   return 0;

@@ -123,8 +123,10 @@ struct TailTiles {
   int n = 0, parts = 0;
   int b[kMaxTailTiles], mp[kMaxTailTiles], nb[kMaxTailTiles];
 };
-// What the fix-up writes: the GEMM epilogue's output (bf16, + bias), or for
-// the GELU forward h = gelu(z) and, when out2 is given, z (both bf16).
+// What the fix-up writes: the GEMM epilogue's output (bf16, + bias); for the
+// GELU forward h = gelu(z) and, when out2 is given, z; for the SwiGLU forward
+// (tiles of 128 a-columns then 128 g-columns) h = silu(a) g at the tile's 128
+// hidden units and, when out2 is given, a and g (all bf16).
 struct TailOut {
   void* out = nullptr;
   int64_t out_bs = 0, out_rs = 0;
@@ -133,7 +135,7 @@ struct TailOut {
   const void* bias = nullptr;
   int64_t bias_bs = 0, bias_len = 0;
   int64_t M = 0, n_store = 0;
-  int gelu = 0;
+  int act = 0;  // 0 none, 1 GELU, 2 SwiGLU
 };
 int launch_tail_fixup(const float* parts, const TailTiles& t, const TailOut& o, LaunchCtx& ctx, const char* name);
 // SwiGLU of the ksplit fp32 parts of a K-split up GEMM (see tp_kernels.cu).

@@ -623,15 +623,67 @@ int launch_swiglu_combine(const float* parts, int ksplit, int T_p, int64_t rows,
 // P + (k * t.n + i) * 65536 (row-major, 256 columns).  The parts are added in
 // the order k = 0, 1, .., then the bias, and the result written as the GEMM's
 // own epilogue would have: v in bf16 (GEMM output), or h = gelu(v) and, with
-// out2, z = v (GELU forward).  Rows >= M and columns >= n_store are not
-// written.  One thread per 4 columns; the parts are read four at a time with
-// independent loads (the sum order stays k = 0, 1, ..).
+// out2, z = v (GELU forward), or, for the SwiGLU forward, h = silu(a) g and,
+// with out2, a and g.  Rows >= M and columns >= n_store (hidden units for
+// SwiGLU) are not written.  One thread per 4 columns (4 hidden units, SwiGLU);
+// the parts are read four at a time with independent loads (the sum order
+// stays k = 0, 1, ..).
+__device__ __forceinline__ float4 tail_part_sum(const float4* q, long long stride, int parts) {
+  float4 acc = q[0];
+  int k = 1;
+  for (; k + 3 < parts; k += 4) {
+    const float4 a = q[k * stride], b = q[(k + 1) * stride], e = q[(k + 2) * stride], f = q[(k + 3) * stride];
+    acc.x = (((acc.x + a.x) + b.x) + e.x) + f.x;
+    acc.y = (((acc.y + a.y) + b.y) + e.y) + f.y;
+    acc.z = (((acc.z + a.z) + b.z) + e.z) + f.z;
+    acc.w = (((acc.w + a.w) + b.w) + e.w) + f.w;
+  }
+  for (; k < parts; ++k) {
+    const float4 a = q[k * stride];
+    acc.x += a.x;
+    acc.y += a.y;
+    acc.z += a.z;
+    acc.w += a.w;
+  }
+  return acc;
+}
+__device__ __forceinline__ void store_bf16x4(__nv_bfloat16* dst, const float* v) {
+  __nv_bfloat162 h[2] = {__floats2bfloat162_rn(v[0], v[1]), __floats2bfloat162_rn(v[2], v[3])};
+  *reinterpret_cast<uint2*>(dst) = *reinterpret_cast<const uint2*>(h);
+}
 __global__ void __launch_bounds__(256) tail_fixup_kernel(const float* __restrict__ P, TailTiles t, TailOut o) {
   // a programmatic dependent of the GEMM that wrote the parts
   asm volatile("griddepcontrol.wait;" ::: "memory");
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-  const long long total = static_cast<long long>(t.n) * 256 * 64;
   const long long stride = static_cast<long long>(t.n) * (65536 / 4);  // float4s between parts
+  if (o.act == 2) {
+    // SwiGLU: a at the tile's columns [0, 128), g at [128, 256)
+    const long long total = static_cast<long long>(t.n) * 256 * 32;
+    for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < total;
+         i += (long long)gridDim.x * blockDim.x) {
+      const int ti = static_cast<int>(i >> 13);
+      const int r = static_cast<int>((i >> 5) & 255), u = static_cast<int>(i & 31) * 4;
+      const long long row = static_cast<long long>(t.mp[ti]) * 256 + r;
+      const long long hcol = static_cast<long long>(t.nb[ti]) * 128 + u;
+      if (row >= o.M || hcol >= o.n_store) continue;
+      const float4* q = reinterpret_cast<const float4*>(P) + ti * (65536 / 4) + r * 64 + u / 4;
+      const float4 a4 = tail_part_sum(q, stride, t.parts), g4 = tail_part_sum(q + 32, stride, t.parts);
+      const float a[4] = {a4.x, a4.y, a4.z, a4.w}, g[4] = {g4.x, g4.y, g4.z, g4.w};
+      float h[4];
+#pragma unroll
+      for (int j = 0; j < 4; ++j) h[j] = a[j] * sigmoid_f(a[j]) * g[j];
+      const long long bt = t.b[ti];
+      store_bf16x4(static_cast<__nv_bfloat16*>(o.out) + bt * o.out_bs + row * o.out_rs + hcol, h);
+      if (o.out2) {
+        __nv_bfloat16* sv = static_cast<__nv_bfloat16*>(o.out2) + bt * o.out2_bs + row * o.out2_rs +
+                            static_cast<long long>(t.nb[ti]) * 256 + u;
+        store_bf16x4(sv, a);
+        store_bf16x4(sv + 128, g);
+      }
+    }
+    return;
+  }
+  const long long total = static_cast<long long>(t.n) * 256 * 64;
   const __nv_bfloat16* bias = static_cast<const __nv_bfloat16*>(o.bias);
   for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < total;
        i += (long long)gridDim.x * blockDim.x) {
@@ -639,23 +691,8 @@ __global__ void __launch_bounds__(256) tail_fixup_kernel(const float* __restrict
     const int r = static_cast<int>((i >> 6) & 255), c = static_cast<int>(i & 63) * 4;
     const long long row = static_cast<long long>(t.mp[ti]) * 256 + r, col = static_cast<long long>(t.nb[ti]) * 256 + c;
     if (row >= o.M || col >= o.n_store) continue;  // n_store is a multiple of 8: the 4 columns are all in or all out
-    const float4* q = reinterpret_cast<const float4*>(P) + ti * (65536 / 4) + r * 64 + c / 4;
-    float4 acc = q[0];
-    int k = 1;
-    for (; k + 3 < t.parts; k += 4) {
-      const float4 a = q[k * stride], b = q[(k + 1) * stride], e = q[(k + 2) * stride], f = q[(k + 3) * stride];
-      acc.x = (((acc.x + a.x) + b.x) + e.x) + f.x;
-      acc.y = (((acc.y + a.y) + b.y) + e.y) + f.y;
-      acc.z = (((acc.z + a.z) + b.z) + e.z) + f.z;
-      acc.w = (((acc.w + a.w) + b.w) + e.w) + f.w;
-    }
-    for (; k < t.parts; ++k) {
-      const float4 a = q[k * stride];
-      acc.x += a.x;
-      acc.y += a.y;
-      acc.z += a.z;
-      acc.w += a.w;
-    }
+    const float4 acc = tail_part_sum(reinterpret_cast<const float4*>(P) + ti * (65536 / 4) + r * 64 + c / 4, stride,
+                                     t.parts);
     float v[4] = {acc.x, acc.y, acc.z, acc.w};
     const long long bt = t.b[ti];
     if (bias) {
@@ -664,18 +701,12 @@ __global__ void __launch_bounds__(256) tail_fixup_kernel(const float* __restrict
       for (int j = 0; j < 4; ++j)
         if (col + j < o.bias_len) v[j] += __bfloat162float(bp[col + j]);
     }
-    if (o.gelu) {
-      if (o.out2) {
-        __nv_bfloat162 z[2] = {__floats2bfloat162_rn(v[0], v[1]), __floats2bfloat162_rn(v[2], v[3])};
-        *reinterpret_cast<uint2*>(static_cast<__nv_bfloat16*>(o.out2) + bt * o.out2_bs + row * o.out2_rs + col) =
-            *reinterpret_cast<const uint2*>(z);
-      }
+    if (o.act == 1) {
+      if (o.out2) store_bf16x4(static_cast<__nv_bfloat16*>(o.out2) + bt * o.out2_bs + row * o.out2_rs + col, v);
 #pragma unroll
       for (int j = 0; j < 4; ++j) v[j] = gelu_tanh_f(v[j]);
     }
-    __nv_bfloat162 h[2] = {__floats2bfloat162_rn(v[0], v[1]), __floats2bfloat162_rn(v[2], v[3])};
-    *reinterpret_cast<uint2*>(static_cast<__nv_bfloat16*>(o.out) + bt * o.out_bs + row * o.out_rs + col) =
-        *reinterpret_cast<const uint2*>(h);
+    store_bf16x4(static_cast<__nv_bfloat16*>(o.out) + bt * o.out_bs + row * o.out_rs + col, v);
   }
 }
 
@@ -685,7 +716,7 @@ int launch_tail_fixup(const float* parts, const TailTiles& t, const TailOut& o, 
   if (!a16(parts) || !a16(o.out) || (o.out2 && !a16(o.out2)) || o.out_rs % 8 || o.out_bs % 8 || o.out2_rs % 8 ||
       o.out2_bs % 8 || o.n_store % 8)
     return TP_ERR_ALIGN;
-  const long long total = static_cast<long long>(t.n) * 256 * 64;
+  const long long total = static_cast<long long>(t.n) * 256 * (o.act == 2 ? 32 : 64);
   if (ctx.before) ctx.before(ctx.user, name, ctx.stream);
   launch_pdl(tail_fixup_kernel, dim3(grid_for(total, 256, ctx.num_sms)), 256, ctx.stream, parts, t, o);
   if (ctx.after) ctx.after(ctx.user, ctx.stream);

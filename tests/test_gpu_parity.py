@@ -179,15 +179,18 @@ def test_wgrad_ksplit_is_taken(w):
 TAIL_SPLIT = [small_case(700, 512, 2048, 2, "gelu_tanh", bias=True, seed=116),
               small_case(700, 512, 1792, 7, "gelu_tanh", bias=True, seed=118),
               small_case(600, 760, 1536, 4, "swiglu", seed=117)]
-# The GELU up GEMM takes the same split (the fix-up adds b1, applies GELU and
-# writes h and the saved z): 18 tiles of 2 parts here, and the down GEMM's 12
-# tiles 3 parts.
-TAIL_SPLIT_UP = small_case(600, 1024, 1536, 3, "gelu_tanh", bias=True, seed=121)
+# The up GEMMs take the same split (the fix-up adds b1 and applies GELU, or
+# forms silu(a) g, and writes h and the saved activations): 18 GELU tiles and
+# 36 SwiGLU tiles (ragged rows, d and hidden units) of 2 parts here, and the
+# down GEMMs' 12 tiles 3 parts.
+TAIL_SPLIT_UP = [small_case(600, 1024, 1536, 3, "gelu_tanh", bias=True, seed=121),
+                 small_case(530, 1000, 1500, 3, "swiglu", seed=122)]
 
 
 @pytest.mark.parametrize("fused", [False, True], ids=["standalone", "fused"])
-def test_tail_split_gelu_up_against_full_oracle(fused):
-    _full_compare(TAIL_SPLIT_UP, fused)
+@pytest.mark.parametrize("w", TAIL_SPLIT_UP, ids=[w.name for w in TAIL_SPLIT_UP])
+def test_tail_split_up_against_full_oracle(w, fused):
+    _full_compare(w, fused)
 
 
 @pytest.mark.parametrize("w", TAIL_SPLIT, ids=[w.name for w in TAIL_SPLIT])
@@ -195,19 +198,20 @@ def test_tail_split_against_full_oracle(w):
     _full_compare(w, True)
 
 
-def test_tail_split_gelu_up_is_taken():
-    """Both GEMMs of the case above split their last wave: the fix-up follows
-    each in the launch records."""
+@pytest.mark.parametrize("w", TAIL_SPLIT_UP, ids=[w.name for w in TAIL_SPLIT_UP])
+def test_tail_split_up_is_taken(w):
+    """Both GEMMs of the cases above split their last wave: the fix-up
+    follows each in the launch records."""
     from megatron_tensor_transformer_w1_gb300 import tpffn as abi
     from megatron_tensor_transformer_w1_gb300.ffn import TensorParallelFFN
-    w = TAIL_SPLIT_UP
     dev = torch.device("cuda", 0)
     g = {k: (None if v is None else v.to(dev)) for k, v in make_inputs(w).items()}
     ffn = TensorParallelFFN(w.d, w.d_ff, w.T_p, w.act, "bf16", device=dev)
     w13p, w2p = ffn.pack(g["W1"], g["W2"], g["W3"])
     ffn.forward(g["x"], w13p, w2p, g["b1"], g["b2"], fused=True, flags=abi.TP_FLAG_TIMING)
     names = [n for n, _ in abi.tp_ffn_kernel_times(ffn.plan, 1000)]
-    assert names == ["up_gelu", "tail_fixup", "down_fused_sum", "tail_fixup"], names
+    up = "up_gelu" if w.act == "gelu_tanh" else "up_swiglu"
+    assert names == [up, "tail_fixup", "down_fused_sum", "tail_fixup"], names
 
 
 @pytest.mark.parametrize("w", TAIL_SPLIT + [MANY_TILES], ids=[w.name for w in TAIL_SPLIT + [MANY_TILES]])
