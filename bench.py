@@ -729,16 +729,17 @@ def profile_attention(args):
 
 def profile_ffn(args):
     """A plain loop of FFN steps for profiler captures: the Llama-3-8B shapes
-    (--tokens overrides the token count), pack + forward + backward with the
-    --sum mode, or with --profile-decode the decode-shaped forward alone; no
-    timing, no extras, nothing else launched."""
+    (--profile-workload picks another workload's, with its biases; --tokens
+    overrides the token count), pack + forward + backward with the --sum mode,
+    or with --profile-decode the decode-shaped forward alone; no timing, no
+    extras, nothing else launched."""
     import torch
     from synth import WORKLOADS
     from megatron_tensor_transformer_w1_gb300 import tpffn as abi
     from megatron_tensor_transformer_w1_gb300.ffn import TensorParallelFFN
     dev = torch.device("cuda", 0)
     torch.cuda.set_device(dev)
-    w = WORKLOADS[DECODE if args.profile_decode else MAIN]
+    w = WORKLOADS[DECODE if args.profile_decode else (args.profile_workload or MAIN)]
     if args.tokens and not args.profile_decode:
         w = w.replace(N=args.tokens)
     inp = _device_inputs(w, dev, 20260000 + w.seed_index)
@@ -756,13 +757,16 @@ def profile_ffn(args):
         saved = torch.empty(abi.tp_ffn_saved_bytes(plan, n), dtype=torch.uint8, device=dev)
         dx = torch.empty_like(y)
         dw13p, dw2p = torch.empty_like(w13p), torch.empty_like(w2p)
+        b1, b2 = (inp["b1"], inp["b2"]) if w.bias else (None, None)
+        db1 = torch.empty(w.d_ff, dtype=torch.bfloat16, device=dev) if w.bias and w.act == "gelu_tanh" else None
+        db2 = torch.empty(w.d, dtype=torch.bfloat16, device=dev) if w.bias else None
         for _ in range(args.warmup + args.steps):
             abi.check(abi.tp_ffn_shard_columns(plan, inp["W1"], inp["W3"], w13p, st), "shard_columns")
             abi.check(abi.tp_ffn_shard_rows(plan, inp["W2"], w2p, st), "shard_rows")
-            abi.check(abi.tp_ffn_fwd(plan, n, inp["x"], w13p, w2p, None, None, y, None, saved, ws, ws.numel(), flags,
+            abi.check(abi.tp_ffn_fwd(plan, n, inp["x"], w13p, w2p, b1, b2, y, None, saved, ws, ws.numel(), flags,
                                      st), "fwd")
-            abi.check(abi.tp_ffn_bwd(plan, n, inp["x"], w13p, w2p, saved, inp["dy"], dx, None, dw13p, dw2p, None,
-                                     None, ws, ws.numel(), flags, st), "bwd")
+            abi.check(abi.tp_ffn_bwd(plan, n, inp["x"], w13p, w2p, saved, inp["dy"], dx, None, dw13p, dw2p, db1,
+                                     db2, ws, ws.numel(), flags, st), "bwd")
     torch.cuda.synchronize(dev)
     return {"profile": w.name, "tokens": n, "sum": args.sum, "steps": args.steps, "warmup": args.warmup}
 
@@ -922,6 +926,8 @@ def main():
     ap.add_argument("--attn-batch", type=int, default=0, help="override the attention workload's sequence count")
     ap.add_argument("--profile-ffn", action="store_true",
                     help="only run --warmup + --steps plain FFN steps (profiler captures)")
+    ap.add_argument("--profile-workload", default="", metavar="WORKLOAD",
+                    help="with --profile-ffn: this workload's shapes instead of the Llama-3-8B ones")
     ap.add_argument("--profile-decode", action="store_true",
                     help="with --profile-ffn: the decode-shaped forward instead of the training step")
     args = ap.parse_args()
